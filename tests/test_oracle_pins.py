@@ -1,0 +1,562 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: numbers the
+pages print (tests/golden/lse_dflash2_facts.json), closed forms, textbook
+special cases computed by library routines, invariants, and brute force.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import philox
+from oracle.dflash2 import matmul_rows
+import workloads as wk
+from workloads.gen import weight_shapes
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "lse_dflash2_facts.json")))
+
+
+# ----------------------------------------------------------------------------- geometry
+
+def test_geometry_matches_published_parameter_count():
+    """The layer structure the oracle runs sums to the page's exact parameter count,
+    BF16 byte count and Q8 tensor count (LSE docs, compatible-drafter and Q8
+    paragraphs).  A missing norm, delta projection or bias would break the sums."""
+    g = wk.FULL
+    shp = weight_shapes(g)
+    shared = {"embed", "lm_head"}                     # shared with the target, not in the drafter file
+    own = {k: v for k, v in shp.items() if k not in shared}
+    n_params = sum(int(np.prod(s)) for s in own.values())
+    assert n_params == GOLD["bf16_params"]
+    assert len(own) == 81
+    header = GOLD["bf16_file_bytes"] - 2 * n_params
+    assert 0 < header < 16384                          # safetensors JSON header of 81 tensors
+    mats = [k for k, s in own.items() if len(s) == 2 and k.split(".")[-1] in wk.MATRIX_NAMES]
+    assert len(mats) == 49
+    vecs = [k for k in own if k not in mats]
+    n_tensors_q8 = 3 * len(mats) + len(vecs)
+    assert n_tensors_q8 == GOLD["q8_tensors"]
+    q8_bytes = sum(int(np.prod(own[k])) * 68 // 64 for k in mats) + 2 * sum(int(np.prod(own[k])) for k in vecs)
+    assert 0 < GOLD["q8_file_bytes"] - q8_bytes < 32768
+    assert (g.hidden, g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.ffn) == \
+        (GOLD["hidden"], GOLD["layers"], GOLD["q_heads"], GOLD["kv_heads"], GOLD["head_dim"], GOLD["ffn"])
+    assert (g.block, g.top_k, g.rank, g.window, g.conv_taps, g.conv_group) == \
+        (GOLD["block"], GOLD["top_k"], GOLD["rank"], GOLD["window"], GOLD["conv_taps"], GOLD["conv_group"])
+
+
+# ----------------------------------------------------------------------------- numbers
+
+def test_round_to_bf16_is_nearest_even():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.normal(0, 1, 4000), rng.normal(0, 1e-3, 1000), rng.normal(0, 300, 1000)])
+    r = oracle.round_to_bf16(x)
+    for xi, ri in zip(x[:600], r[:600]):
+        # brute force: the two bf16 neighbours bracketing xi
+        m, e = math.frexp(abs(xi))
+        step = 2.0 ** (e - 8)
+        lo = math.floor(abs(xi) / step) * step
+        hi = lo + step
+        d_lo, d_hi = abs(abs(xi) - lo), abs(hi - abs(xi))
+        if d_lo < d_hi:
+            want = lo
+        elif d_hi < d_lo:
+            want = hi
+        else:
+            want = lo if (round(lo / step) % 2 == 0) else hi
+        assert abs(ri) == want and (ri == 0 or np.sign(ri) == np.sign(xi))
+    # exactly representable in bf16 -> unchanged; matches a float32 -> bf16 bit rounding
+    b = wk.bf16_bits_from_f32(x.astype(np.float32))
+    y = oracle.bf16_to_f64(b)
+    assert np.array_equal(oracle.round_to_bf16(y), y)
+
+
+def test_q8_dequant_worked_example():
+    """w = scale * q + bias per group of 64 (LSE docs, Q8 paragraph: affine Q8, group 64)."""
+    codes = np.arange(-128, 128, dtype=np.int8).reshape(2, 128)
+    scale = wk.bf16_bits_from_f32(np.array([[2.0 ** -7, 0.5], [1.0, 0.0]], np.float32))
+    bias = wk.bf16_bits_from_f32(np.array([[1.0, -2.0], [0.25, 3.0]], np.float32))
+    w = oracle.matrix_f64({"kind": "q8", "codes": codes, "scale": scale, "bias": bias})
+    q = codes.astype(np.float64)
+    assert np.array_equal(w[0, :64], 1.0 + q[0, :64] / 128.0)
+    assert np.array_equal(w[0, 64:], -2.0 + 0.5 * q[0, 64:])
+    assert np.array_equal(w[1, :64], 0.25 + q[1, :64])
+    assert np.array_equal(w[1, 64:], np.full(64, 3.0))
+
+
+def test_rmsnorm_matches_library():
+    rng = np.random.default_rng(2)
+    x = rng.normal(0, 3, (8, 512))
+    wb = wk.bf16_bits_from_f32(rng.normal(1, 0.02, 512).astype(np.float32))
+    w = oracle.bf16_to_f64(wb)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (512,), torch.from_numpy(w), eps=1e-6).numpy()
+    assert np.allclose(oracle.rmsnorm(x, wb, 1e-6), ref, rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+def test_rope_position_zero_identity_and_norm():
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 1, (5, 8, 128))
+    assert np.allclose(oracle.rope_neox(x, [0] * 5, 1e7), x, atol=0, rtol=0)
+    y = oracle.rope_neox(x, [1, 17, 2055, 33000, 10 ** 6], 1e7)
+    # each (j, j+64) pair is rotated: the pair norms are preserved
+    n0 = x[..., :64] ** 2 + x[..., 64:] ** 2
+    n1 = y[..., :64] ** 2 + y[..., 64:] ** 2
+    assert np.allclose(n0, n1, rtol=1e-12)
+
+
+def test_rope_relative_position_property():
+    """<rope(q, m), rope(k, n)> depends only on m - n (the defining property of rotary
+    embeddings); a wrong sign, pairing or frequency breaks it."""
+    rng = np.random.default_rng(4)
+    q = rng.normal(0, 1, (1, 1, 128))
+    k = rng.normal(0, 1, (1, 1, 128))
+    dots = []
+    for m in (5, 1000, 40000):
+        qa = oracle.rope_neox(q, [m], 1e7)
+        ka = oracle.rope_neox(k, [m - 3], 1e7)
+        dots.append(float(np.sum(qa * ka)))
+    assert np.allclose(dots, dots[0], rtol=1e-9)
+    # and it is not trivially constant across different offsets
+    qa = oracle.rope_neox(q, [7], 1e7)
+    ka = oracle.rope_neox(k, [0], 1e7)
+    assert abs(float(np.sum(qa * ka)) - dots[0]) > 1e-6
+
+
+def test_rope_frequencies_theta_1e7():
+    f = oracle.rope_inv_freq(128, 1e7)
+    assert f[0] == 1.0
+    assert np.isclose(f[1], 1e7 ** (-2 / 128), rtol=1e-15)
+    assert np.isclose(f[-1] / f[-2], 1e7 ** (-2 / 128), rtol=1e-13)
+    # NEOX pairing: rotating pair j only moves components j and j+64 (one-hot probe)
+    x = np.zeros((1, 1, 128))
+    x[0, 0, 5] = 1.0
+    y = oracle.rope_neox(x, [1000], 1e7)[0, 0]
+    nz = set(np.nonzero(np.abs(y) > 1e-15)[0])
+    assert nz <= {5, 69}
+    ang = 1000 * f[5]
+    assert np.isclose(y[5], math.cos(ang)) and np.isclose(y[69], math.sin(ang))
+
+
+# ----------------------------------------------------------------------------- conv
+
+def _conv_inputs(B=8, H=64, G=4, seed=5):
+    rng = np.random.default_rng(seed)
+    return rng.normal(0, 1, (B, H)), rng.normal(0, 1, (2, H)), rng.normal(0, 1, (B, 2, G))
+
+
+def test_conv_identity_init():
+    """Bases (1, 0) with a zero dynamic part is the identity (Speculators PR quoted in the
+    vLLM PR thread: identity-initialized, block-local convolutions)."""
+    x, _, _ = _conv_inputs()
+    base = np.stack([np.ones(64), np.zeros(64)])
+    assert np.array_equal(oracle.dyn_conv(x, base, np.zeros((8, 2, 4)), 16), x)
+
+
+def test_conv_pure_shift_and_block_boundary():
+    x, _, _ = _conv_inputs()
+    base = np.stack([np.zeros(64), np.ones(64)])
+    y = oracle.dyn_conv(x, base, np.zeros((8, 2, 4)), 16)
+    assert np.array_equal(y[0], np.zeros(64))          # the anchor sees nothing before the block
+    assert np.array_equal(y[1:], x[:-1])
+
+
+def test_conv_group_locality_and_linearity():
+    x, base, d = _conv_inputs()
+    y = oracle.dyn_conv(x, base, d, 16)
+    d2 = d.copy()
+    d2[3, 1, 2] += 1.0                                 # position 3, tap 1, group 2 (channels 32..47)
+    y2 = oracle.dyn_conv(x, base, d2, 16)
+    diff = np.abs(y2 - y) > 0
+    assert set(np.nonzero(diff.any(axis=1))[0]) == {3}
+    assert set(np.nonzero(diff[3])[0]) == set(range(32, 48))
+    assert np.allclose(y2[3, 32:48] - y[3, 32:48], x[2, 32:48])
+    z = oracle.dyn_conv(2.0 * x - x[::-1], base, d, 16)
+    assert np.allclose(z, 2.0 * y - oracle.dyn_conv(x[::-1], base, d, 16))
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _sdpa(q, k, v, mask=None):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    return torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=mask).numpy()
+
+
+def test_attention_dense_case_matches_library():
+    """With every context key inside the window the block attention is plain
+    noncausal GQA softmax attention (torch SDPA in float64)."""
+    rng = np.random.default_rng(6)
+    B, nq, nkv, hd, L = 8, 8, 2, 128, 300
+    q = rng.normal(0, 1, (B, nq, hd))
+    kb, vb = rng.normal(0, 1, (B, nkv, hd)), rng.normal(0, 1, (B, nkv, hd))
+    kc, vc = rng.normal(0, 1, (L, nkv, hd)), rng.normal(0, 1, (L, nkv, hd))
+    out = oracle.block_attention(q, kb, vb, kc, vc, L, 2048).reshape(B, nq, hd)
+    K = np.concatenate([kc, kb])
+    V = np.concatenate([vc, vb])
+    rep = nq // nkv
+    Kh = np.repeat(K.transpose(1, 0, 2), rep, axis=0)   # [nq][L+B][hd]
+    Vh = np.repeat(V.transpose(1, 0, 2), rep, axis=0)
+    ref = _sdpa(q.transpose(1, 0, 2), Kh, Vh).transpose(1, 0, 2)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_window_matches_masked_library_and_ignores_masked_keys():
+    rng = np.random.default_rng(7)
+    B, nq, nkv, hd, W = 8, 4, 1, 128, 64
+    L = 200
+    q = rng.normal(0, 1, (B, nq, hd))
+    kb, vb = rng.normal(0, 1, (B, nkv, hd)), rng.normal(0, 1, (B, nkv, hd))
+    kc, vc = rng.normal(0, 1, (L, nkv, hd)), rng.normal(0, 1, (L, nkv, hd))
+    out = oracle.block_attention(q, kb, vb, kc, vc, L, W)
+    # boolean mask: query i (position L+i) sees context key k iff L+i-k < W, and all block keys
+    mask = np.zeros((B, L + B), bool)
+    for i in range(B):
+        for k in range(L):
+            mask[i, k] = (L + i - k) < W
+        mask[i, L:] = True
+    K = np.concatenate([kc, kb])[:, 0]
+    V = np.concatenate([vc, vb])[:, 0]
+    ref = _sdpa(q.transpose(1, 0, 2), np.repeat(K[None], nq, 0), np.repeat(V[None], nq, 0),
+                torch.from_numpy(mask)).transpose(1, 0, 2).reshape(B, nq * hd)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[: L - W + 1] = np.nan                          # every key outside all windows
+    vc2[: L - W + 1] = np.nan
+    assert np.array_equal(oracle.block_attention(q, kb, vb, kc2, vc2, L, W), out)
+
+
+def test_live_key_counts_match_page():
+    """LSE docs, attention test paragraph: live counts 17 and 2055 for 8 queries.
+    Reading: keys visible to query 0 = visible context + the 8 block keys; 2055 =
+    2047 + 8 once the context fills the 2048 window (a block-uniform window would
+    give 2056)."""
+    def live(L, i):
+        lo, hi = oracle.visible_context_range(L, i, 2048)
+        return hi - lo + 8
+    assert live(9, 0) == GOLD["attention_live_counts"][0]
+    assert live(4096, 0) == GOLD["attention_live_counts"][1]
+    assert [live(4096, i) for i in range(8)] == [2055 - i for i in range(8)]
+
+
+# ----------------------------------------------------------------------------- top-k
+
+def test_topk_matches_stable_sort_and_edge_policy():
+    rng = np.random.default_rng(8)
+    row = rng.integers(-50, 50, 4097).astype(np.float32)   # many ties
+    ids, vals = oracle.topk(row, 16)
+    ref = np.argsort(-row.astype(np.float64), kind="stable")[:16]
+    assert np.array_equal(ids, ref)
+    # edge rows in the manner of the page's 4097-wide edge test (LSE docs, top-k paragraph)
+    r = rng.normal(0, 1, 4097).astype(np.float32)
+    r[[10, 600, 4000]] = np.nan
+    r[[5, 3000]] = np.inf
+    r[[7]] = -np.inf
+    ids, _ = oracle.topk(r, 16)
+    assert list(ids[:3]) == [10, 600, 4000]              # NaNs first, by index
+    assert list(ids[3:5]) == [5, 3000]                   # +inf next
+    allneg = np.full(4097, -np.inf, np.float32)
+    ids, vals = oracle.topk(allneg, 16)
+    assert list(ids) == list(range(16)) and np.all(np.isneginf(vals))
+    tie = np.zeros(4097, np.float32)
+    tie[[512, 513, 1024, 1536, 4096]] = 1.0                # ties across 512-chunk boundaries
+    ids, _ = oracle.topk(tie, 16)
+    assert list(ids[:5]) == [512, 513, 1024, 1536, 4096] and list(ids[5:]) == list(range(11))
+
+
+# ----------------------------------------------------------------------------- selector
+
+def _gamma(n):
+    u = 2.0 ** -24
+    return n * u / (1 - n * u)
+
+
+def test_selector_scores_library_and_page_rounding_bound():
+    """Scores equal an einsum of the rank-256 triple product; a float32 evaluation in
+    another order stays inside the page's mixed rounding bound
+    gamma_(rank+2) * sum|pred*gate*succ| + 2u/(1-u) * |ref| (LSE docs, selector test)."""
+    rng = np.random.default_rng(9)
+    P, C, r = 16, 16, 256
+    A = rng.normal(0, 0.02, (P, r))
+    Bc = rng.normal(0, 0.02, (C, r))
+    gate = rng.normal(0, 1.4, r)
+    un = rng.normal(0, 1.4, C)
+    s = oracle.selector_scores(A, gate, Bc, un)
+    ref = np.einsum("pr,r,cr->pc", A, gate, Bc) + un[None, :]
+    assert np.allclose(s, ref, rtol=1e-13, atol=1e-15)
+    u = 2.0 ** -24
+    A32, g32, B32, un32 = (a.astype(np.float32) for a in (A, gate, Bc, un))
+    for p in range(P):
+        for c in range(C):
+            acc = np.float32(0)
+            for k in reversed(range(r)):
+                acc = np.float32(acc + np.float32(np.float32(A32[p, k] * g32[k]) * B32[c, k]))
+            s32 = np.float32(acc + un32[c])
+            exact = float(np.sum(A32[p].astype(np.float64) * g32 * B32[c])) + float(un32[c])
+            bound = _gamma(r + 2) * float(np.sum(np.abs(A32[p].astype(np.float64) * g32 * B32[c]))) \
+                + 2 * u / (1 - u) * abs(exact)
+            assert abs(float(s32) - exact) <= bound
+    assert P * C * 7 == GOLD["selector_scores_checked"]
+
+
+def _sel_inputs(seed, V=64, K=4, r=8, P=7, with_q8=False):
+    rng = np.random.default_rng(seed)
+    A = wk.bf16_bits_from_f32(rng.normal(0, 0.5, (V, r)).astype(np.float32))
+    Bm = wk.bf16_bits_from_f32(rng.normal(0, 0.5, (V, r)).astype(np.float32))
+    cand = np.stack([rng.choice(V, K, replace=False) for _ in range(P)]).astype(np.int32)
+    cl = -np.sort(-rng.normal(0, 1, (P, K)), axis=1)
+    gate = rng.normal(0, 1, (P, r))
+    return {"kind": "bf16", "w": A}, {"kind": "bf16", "w": Bm}, cand, cl, gate
+
+
+def test_greedy_walk_is_predecessor_conditioned_argmax():
+    """Greedy path = argmax of the edge score from the chosen predecessor, starting at
+    the anchor (vLLM PR description); checked by brute force over the candidates."""
+    class G:
+        block = 8
+    for seed in range(5):
+        A, Bm, cand, cl, gate = _sel_inputs(seed)
+        anchor = 3
+        res = oracle.walk(G, A, Bm, anchor, cand, cl, gate, 0.0, 0, 0)
+        Af, Bf = oracle.bf16_to_f64(A["w"]), oracle.bf16_to_f64(Bm["w"])
+        prev = anchor
+        for i in range(7):
+            sc = [float(np.sum(Af[prev] * gate[i] * Bf[c])) + cl[i, j] for j, c in enumerate(cand[i])]
+            j = int(np.argmax(sc))
+            assert res["path"][i] == cand[i, j]
+            prev = cand[i, j]
+        assert np.allclose(res["q_rows"].sum(axis=1), 1.0)
+
+
+def test_sampled_walk_low_temperature_equals_greedy_and_distribution():
+    class G:
+        block = 8
+    A, Bm, cand, cl, gate = _sel_inputs(11)
+    g0 = oracle.walk(G, A, Bm, 3, cand, cl, gate, 0.0, 0, 0)
+    gt = oracle.walk(G, A, Bm, 3, cand, cl, gate, 1e-4, 7, 0)
+    assert np.array_equal(g0["path"], gt["path"])
+    # first-position draws over many Philox offsets follow softmax(s / T)
+    T = 1.0
+    n = 4000
+    counts = np.zeros(4)
+    for off in range(n):
+        res = oracle.walk(G, A, Bm, 3, cand[:1], cl[:1], gate[:1], T, 123, off)
+        counts[list(cand[0]).index(res["path"][0])] += 1
+    q = res["q_rows"][0]
+    chi2 = float(np.sum((counts - n * q) ** 2 / (n * q)))
+    assert chi2 < 16.3                                  # 3 dof, p = 0.001
+
+
+# ----------------------------------------------------------------------------- verify
+
+def _breakpoint_integral(fn, points):
+    """Integrate a piecewise-constant function of u on [0,1) exactly, given a superset
+    of its breakpoints: evaluate at interval midpoints, weight by interval length."""
+    pts = sorted(set([0.0, 1.0] + [p for p in points if 0.0 < p < 1.0]))
+    out = []
+    for a, b in zip(pts[:-1], pts[1:]):
+        out.append((b - a, fn(0.5 * (a + b))))
+    return out
+
+
+def test_verify_single_position_is_lossless_exactly():
+    """Probability-ratio rejection with residual sampling emits exactly the target
+    distribution (LSE docs: the target verifies with probability-ratio rejection and
+    residual sampling).  Brute force over a 5-token vocabulary, the draft token drawn
+    from q, both uniforms integrated exactly."""
+    V, K = 5, 2
+    rng = np.random.default_rng(12)
+    for trial in range(6):
+        z = rng.normal(0, 1.5, (8, V))
+        T = [1.0, 0.7, 2.0][trial % 3]
+        p0 = np.exp(z[0] / T - (z[0] / T).max())
+        p0 /= p0.sum()
+        cand = np.zeros((7, K), np.int32)
+        cand[0] = rng.choice(V, K, replace=False)
+        for i in range(1, 7):
+            cand[i] = rng.choice(V, K, replace=False)
+        qv = rng.dirichlet(np.ones(K))
+        q_rows = np.tile(qv, (7, 1))
+        emitted = np.zeros(V)
+        for jd in range(K):
+            d = cand[0, jd]
+            path = np.full(7, d, np.int32)
+            path[1:] = cand[1:, 0]
+            q_full = np.zeros(V)
+            q_full[cand[0]] = qv
+            resid = np.maximum(0, p0 - q_full)
+            cuts = [p0[d] / qv[jd]] + list(np.cumsum(resid) / max(resid.sum(), 1e-300)) + list(np.cumsum(p0))
+            for wa, ua in _breakpoint_integral(lambda u: u, cuts):
+                for wr, ur in _breakpoint_integral(lambda u: u, cuts):
+                    def uni(slot, purpose, ua=ua, ur=ur):
+                        if slot == 0 and purpose == philox.PURPOSE_ACCEPT:
+                            return ua
+                        if slot == 0 and purpose == philox.PURPOSE_RESAMPLE:
+                            return ur
+                        return 0.999999                   # later positions: reject (first token only matters)
+                    res = oracle.verify(z, path, cand, q_rows, T, 0, 0, uniform_fn=uni)
+                    emitted[res["emitted"][0]] += qv[jd] * wa * wr
+        assert np.allclose(emitted, p0, atol=1e-12), (emitted, p0)
+
+
+def test_verify_two_positions_conditional_lossless():
+    """Conditioned on the first draft being accepted, the second emitted token follows
+    the target's second row exactly (the second draft drawn from its q row, both of
+    that position's uniforms integrated exactly)."""
+    V, K = 5, 2
+    rng = np.random.default_rng(13)
+    z = rng.normal(0, 1.0, (8, V))
+    T = 1.0
+    P = np.exp(z - z.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    cand = np.stack([rng.choice(V, K, replace=False) for _ in range(7)]).astype(np.int32)
+    q_rows = rng.dirichlet(np.ones(K), size=7)
+    second = np.zeros(V)
+    for j0 in range(K):
+        for j1 in range(K):
+            path = cand[:, 0].copy()
+            path[0], path[1] = cand[0, j0], cand[1, j1]
+            pq = q_rows[0, j0] * q_rows[1, j1]
+            qf = np.zeros(V)
+            qf[cand[1]] = q_rows[1]
+            resid = np.maximum(0, P[1] - qf)
+            cuts = [P[1][path[1]] / q_rows[1, j1]] + list(np.cumsum(resid) / resid.sum())
+            for wa, ua in _breakpoint_integral(lambda u: u, cuts):
+                for wr, ur in _breakpoint_integral(lambda u: u, cuts):
+                    def uni(slot, purpose, ua=ua, ur=ur):
+                        if slot == 0:
+                            return 0.0 if purpose == philox.PURPOSE_ACCEPT else 0.5   # accept position 1
+                        if slot == 1:
+                            return ua if purpose == philox.PURPOSE_ACCEPT else ur
+                        return 0.999999
+                    res = oracle.verify(z, path, cand, q_rows, T, 0, 0, uniform_fn=uni)
+                    assert res["n_accepted"] >= 1
+                    second[res["emitted"][1]] += pq * wa * wr
+    # first draft accepted with u = 0 always: the second token's law given the first is P[1]
+    marg = second / second.sum()
+    assert np.allclose(marg, P[1], atol=1e-12)
+
+
+def test_verify_greedy_is_argmax_chain():
+    rng = np.random.default_rng(14)
+    V = 50
+    for trial in range(20):
+        z = rng.normal(0, 1, (8, V)).astype(np.float32)
+        t = np.argmax(z, axis=1)
+        n_match = trial % 8
+        path = np.array([t[j] if j < n_match else (t[j] + 1) % V for j in range(7)], np.int32)
+        cand = np.stack([np.array([path[j]] + [x for x in range(16) if x != path[j]][:15]) for j in range(7)]).astype(np.int32)
+        res = oracle.verify(z, path, cand, np.zeros((7, 16)), 0.0, 0, 0)
+        assert res["n_accepted"] == min(n_match, 7)
+        assert res["n_emitted"] == res["n_accepted"] + 1
+        assert list(res["emitted"][: res["n_emitted"]]) == list(t[: res["n_emitted"]])
+
+
+def test_verify_nonfinite_rows():
+    z = np.zeros((8, 10))
+    z[3, 4] = np.nan
+    res = oracle.verify(z, np.zeros(7, np.int32), np.zeros((7, 16), np.int32), np.zeros((7, 16)), 1.0, 0, 0)
+    assert res["status"] == oracle.STATUS_NONFINITE and res["n_emitted"] == 0
+    z = np.zeros((8, 10))
+    z[0] = -np.inf
+    res = oracle.verify(z, np.zeros(7, np.int32), np.zeros((7, 16), np.int32), np.zeros((7, 16)), 0.0, 0, 0)
+    assert res["status"] == oracle.STATUS_NONFINITE
+
+
+# ----------------------------------------------------------------------------- drafter layer
+
+def _torch_layer_reference(g, W, x, c, kctx, vctx, L, pos_blk):
+    """A Qwen3 decoder layer from torch library ops (F.rms_norm, F.linear, SDPA, F.silu),
+    used for the special case of identity convolutions (bases (1,0), zero delta)."""
+    F = torch.nn.functional
+    T = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    w = lambda n: T(oracle.matrix_f64(W[n]))
+    v = lambda n: T(oracle.bf16_to_f64(W[n]))
+    H, hd, nq, nkv = g.hidden, g.head_dim, g.n_q_heads, g.n_kv_heads
+    x = T(x)
+    a = F.rms_norm(x, (H,), v("l0.input_norm"), eps=g.rms_eps)
+    q = F.rms_norm(F.linear(a, w("l0.q")).view(8, nq, hd), (hd,), v("l0.q_norm"), eps=g.rms_eps)
+    k = F.rms_norm(F.linear(a, w("l0.k")).view(8, nkv, hd), (hd,), v("l0.k_norm"), eps=g.rms_eps)
+    vv = F.linear(a, w("l0.v")).view(8, nkv, hd)
+    inv = T(oracle.rope_inv_freq(hd, g.rope_theta))
+    ang = T(pos_blk)[:, None] * inv[None]
+    rot = lambda t: torch.view_as_real(torch.view_as_complex(
+        torch.stack([t[..., :hd // 2], t[..., hd // 2:]], -1).contiguous()) *
+        torch.polar(torch.ones_like(ang), ang)[:, None, :])
+    def rope(t):
+        r = rot(t)
+        return torch.cat([r[..., 0], r[..., 1]], -1)
+    q, k = rope(q), rope(k)
+    K = torch.cat([T(kctx), k])
+    V = torch.cat([T(vctx), vv])
+    rep = nq // nkv
+    o = F.scaled_dot_product_attention(q.transpose(0, 1), K.transpose(0, 1).repeat_interleave(rep, 0),
+                                       V.transpose(0, 1).repeat_interleave(rep, 0))
+    x = x + F.linear(o.transpose(0, 1).reshape(8, nq * hd), w("l0.o"))
+    m = F.rms_norm(x, (H,), v("l0.post_norm"), eps=g.rms_eps)
+    x = x + F.linear(F.silu(F.linear(m, w("l0.gate"))) * F.linear(m, w("l0.up")), w("l0.down"))
+    return x.numpy()
+
+
+def test_draft_layer_reduces_to_qwen3_layer_with_identity_conv():
+    import dataclasses
+    g = dataclasses.replace(wk.TOY, hidden=256, ffn=512, vocab=1024, n_q_heads=4, n_kv_heads=2)
+    W = wk.make_weights(g, "bf16", 21)
+    for n in ("l0.attn_base", "l0.mlp_base"):
+        W[n] = wk.bf16_bits_from_f32(np.stack([np.ones(g.hidden), np.zeros(g.hidden)] * 2).astype(np.float32))
+    for n in ("l0.attn_delta", "l0.mlp_delta"):
+        W[n] = {"kind": "bf16", "w": np.zeros_like(W[n]["w"])}
+    rng = np.random.default_rng(22)
+    ctx_len, n_new = 40, 8
+    cap = 64
+    kc = [wk.bf16_bits_from_f32(rng.normal(0, 1, (cap, 2, 128)).astype(np.float32))]
+    vc = [wk.bf16_bits_from_f32(rng.normal(0, 1, (cap, 2, 128)).astype(np.float32))]
+    taps = rng.normal(0, 1, (n_new, 5 * g.hidden)).astype(np.float32)
+    tr = oracle.draft_block(g, W, 17, ctx_len, n_new, taps, kc, vc)
+    L = ctx_len + n_new
+    x0 = oracle.bf16_to_f64(W["embed"][[17] + [g.mask_id] * 7])
+    ref = _torch_layer_reference(g, W, x0, tr["c"], oracle.bf16_to_f64(kc[0][:L]), oracle.bf16_to_f64(vc[0][:L]),
+                                 L, np.arange(L, L + 8))
+    assert np.allclose(tr["x0"], ref, rtol=1e-10, atol=1e-10)
+    # the appended context rows are the taps projection through W_k / W_v of that layer
+    c = tr["c"]
+    kref = oracle.rope_neox(oracle.rmsnorm((c @ oracle.matrix_f64(W["l0.k"]).T).reshape(8, 2, 128),
+                                           W["l0.k_norm"], g.rms_eps), np.arange(ctx_len, L), g.rope_theta)
+    assert np.allclose(oracle.bf16_to_f64(kc[0][ctx_len:L]), kref, rtol=2 ** -8, atol=1e-30)
+
+
+def test_draft_block_window_isolation():
+    """Cache rows that no block query can see do not affect the draft (window), and the
+    taps only enter through the appended context rows."""
+    import dataclasses
+    g = dataclasses.replace(wk.TOY, window=32, vocab=512)
+    W = wk.make_weights(g, "bf16", 31)
+    rng = np.random.default_rng(32)
+    cap, ctx_len = 128, 90
+    kc = [wk.bf16_bits_from_f32(rng.normal(0, 1, (cap, 1, 128)).astype(np.float32))]
+    vc = [wk.bf16_bits_from_f32(rng.normal(0, 1, (cap, 1, 128)).astype(np.float32))]
+    taps = rng.normal(0, 1, (8, 5 * g.hidden)).astype(np.float32)
+    a = oracle.draft_block(g, W, 5, ctx_len, 8, taps, [kc[0].copy()], [vc[0].copy()])
+    L = ctx_len + 8
+    k2, v2 = kc[0].copy(), vc[0].copy()
+    k2[: L - 32 + 1] = 0x7FC0                            # NaN in every row outside the window
+    v2[: L - 32 + 1] = 0x7FC0
+    b = oracle.draft_block(g, W, 5, ctx_len, 8, taps, [k2], [v2])
+    assert np.array_equal(a["logits"], b["logits"])
+    k3, v3 = kc[0].copy(), vc[0].copy()
+    k3[L - 32 + 1] ^= 0x0101                             # the oldest visible row does matter
+    c3 = oracle.draft_block(g, W, 5, ctx_len, 8, taps, [k3], [v3.copy()])
+    assert not np.array_equal(a["logits"], c3["logits"])
+
+
+def test_philox_structure():
+    """Known structural facts of the definition: the key schedule and that ten rounds
+    of a bijection on the counter give distinct outputs for distinct counters."""
+    outs = {philox.philox4x32_10((i, 0, 0, 0), (1, 2)) for i in range(2000)}
+    assert len(outs) == 2000
+    u = [philox.uniform(42, 0, s, p) for s in range(8) for p in range(3)]
+    assert all(0.0 <= x < 1.0 for x in u) and len(set(u)) == 24
