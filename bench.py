@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of one DFlash2 draft + select + verify step on GB300.
+
+`python bench.py --gpus N --steps K --warmup W` prints one JSON line.
+
+A step = dflash2_draft_block + dflash2_select + dflash2_verify over one batch of
+seeded synthetic inputs of the drafter's full geometry (default workload:
+5 layers, width 5120, 32/8 heads, FFN 17408, vocab 248320, BF16 weights,
+1 request, context 1024, greedy).  The timed region is one CUDA-graph launch of
+exactly K steps, bracketed by a barrier and device synchronisation; inputs are
+resident in HBM and far larger than L2 (6.1 GB of weights stream every step).
+
+`value` is steps/s summed over ranks (independent replicas, weak scaling).
+`e2e` is the same metric through the C ABI with host buffers: every step copies
+its inputs from pinned host memory and reads its result back.  `roofline`
+covers the LM-head + top-16 kernel, timed with CUDA events captured inside the
+graph on the launching stream.  `cpu_baseline` times the oracle on the host.
+
+`--impl reference` times the CPU oracle (the only reference this method has
+here) on the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "DFlash2 draft+verify steps/s at 1 and 16 req; achieved HBM GB/s vs peak"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", type=int, default=2)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=100)
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:  # noqa: BLE001
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "fallback": True}
+
+
+def step_bytes(wl, n_req):
+    """Algorithmic bytes of one step: every weight streamed once (codebooks: only the
+    gathered rows), visible K/V read, new K/V written, taps and target rows read."""
+    g = wl.geom
+    H, F, V = g.hidden, g.ffn, g.vocab
+    mats = (g.q_dim * H + 2 * g.kv_dim * H + H * g.q_dim + 3 * F * H + 2 * g.delta_dim * H)
+    per_weight = 2.0 if wl.weight_format == "bf16" else 68.0 / 64.0
+    w = (mats * g.n_layers + H * g.n_taps * H + g.rank * H) * per_weight
+    w += V * H * 2                                           # LM head (BF16 in both formats)
+    w += (1 + 6 * 16 + 7 * 16) * g.rank * per_weight * n_req  # codebook rows gathered
+    kv_key = 2 * g.kv_dim * 2 * g.n_layers                   # K and V, BF16, all layers
+    kv = sum(min(c, g.window - 1) for c in wl.ctx[:n_req]) * kv_key + 8 * n_req * kv_key
+    taps = n_req * 8 * g.n_taps * H * 4
+    target = n_req * 8 * V * 4
+    return w + kv + taps + target
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.dev = dev_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = [l.split(", ") for l in open(self.path).read().strip().splitlines() if l.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(wl, W, inp, kc_host, vc_host, target_np):
+    """The oracle, as it stands, on one full step of request 0 (bounded: one step)."""
+    import oracle
+    g = wl.geom
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    kl = [kc_host[l, 0].copy() for l in range(g.n_layers)]
+    vl = [vc_host[l, 0].copy() for l in range(g.n_layers)]
+    res = oracle.step(g, W, int(inp["anchors"][0]), int(inp["ctx_len"][0]), int(inp["n_new"][0]),
+                      inp["taps"][0][: int(inp["n_new"][0])], kl, vl, wl.temps[0], wl.philox_seed, 0,
+                      lambda lg: target_np[0].astype(np.float64))
+    dt = time.perf_counter() - t0
+    return {"value": 1.0 / dt, "unit": "steps/s", "cores": cores, "kind": "oracle",
+            "sample": f"1 full step of request 0 of {wl.name} (FP64 NumPy, {dt:.1f} s)"}, res
+
+
+def setup(wl, device_index):
+    """Weights, caches, inputs and target rows of a workload on the device."""
+    import torch
+    import block_drafter_pos_gb300 as bd
+    import workloads as wk
+
+    g = wl.geom
+    t0 = time.time()
+    W = wk.make_weights(g, wl.weight_format, wl.seed)
+    inp = wk.make_request_inputs(wl)
+    R, cap = wl.n_req, wl.kv_capacity
+    kc = np.zeros((g.n_layers, R, cap, g.n_kv_heads, g.head_dim), np.uint16)
+    vc = np.zeros_like(kc)
+    for l in range(g.n_layers):
+        for r in range(R):
+            K, V = inp["kv"][l][r]
+            lo = int(inp["kv_lo"][r])
+            kc[l, r, lo:lo + len(K)] = K
+            vc[l, r, lo:lo + len(V)] = V
+    drafter = bd.Drafter(g, wl.weight_format, W, R, cap)
+    dev = torch.device("cuda", device_index)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    S = {
+        "anchors": T(inp["anchors"]), "ctx_len": T(inp["ctx_len"]), "n_new": T(inp["n_new"]),
+        "taps": T(inp["taps"]), "kc": T(kc.view(np.int16)), "vc": T(vc.view(np.int16)),
+        "cand_ids": torch.zeros((R, 7, 16), dtype=torch.int32, device=dev),
+        "cand_logits": torch.zeros((R, 7, 16), dtype=torch.float32, device=dev),
+        "gate": torch.zeros((R, 7, g.rank), dtype=torch.float32, device=dev),
+        "logits": torch.zeros((R, 7, g.vocab), dtype=torch.float32, device=dev),
+        "temps": T(np.array(wl.temps, np.float32)),
+        "seeds": T(np.full(R, wl.philox_seed, np.uint64).view(np.int64)),
+        "offsets": T(np.array(wl.philox_offsets or [0] * R, np.uint64).view(np.int64)),
+        "path": torch.zeros((R, 7), dtype=torch.int32, device=dev),
+        "q_rows": torch.zeros((R, 7, 16), dtype=torch.float32, device=dev),
+        "status": torch.zeros((R,), dtype=torch.int32, device=dev),
+        "n_acc": torch.zeros((R,), dtype=torch.int32, device=dev),
+        "emitted": torch.zeros((R, 8), dtype=torch.int32, device=dev),
+        "n_emit": torch.zeros((R,), dtype=torch.int32, device=dev),
+    }
+    # untimed pass: drafter logits -> synthetic target rows = drafter logits + N(0, sigma)
+    bd.dflash2_draft_block(drafter.handle, R, S["anchors"], S["ctx_len"], S["n_new"], S["taps"], S["kc"], S["vc"],
+                           S["cand_ids"], S["cand_logits"], S["gate"], S["logits"])
+    torch.cuda.synchronize()
+    lg = S["logits"]
+    target = torch.empty((R, 8, g.vocab), dtype=torch.float32, device=dev)
+    for r in range(R):
+        noise = torch.from_numpy(wk.make_target_noise(wl, 0, r)).to(dev)
+        target[r, :7] = lg[r] + noise[:7]
+        target[r, 7] = lg[r, 6] + noise[7]
+    S["target"] = target
+    setup_s = time.time() - t0
+    return drafter, S, W, inp, kc, vc, setup_s
+
+
+def run_step(bd, h, R, S, ev=None):
+    bd.dflash2_draft_block(h, R, S["anchors"], S["ctx_len"], S["n_new"], S["taps"], S["kc"], S["vc"], S["cand_ids"],
+                           S["cand_logits"], S["gate"], None)
+    bd.dflash2_select(h, R, S["anchors"], S["cand_ids"], S["cand_logits"], S["gate"], S["temps"], S["seeds"],
+                      S["offsets"], S["path"], S["q_rows"], None, S["status"])
+    bd.dflash2_verify(h, R, S["target"], S["path"], S["cand_ids"], S["q_rows"], S["temps"], S["seeds"], S["offsets"],
+                      S["n_acc"], S["emitted"], S["n_emit"], S["status"])
+
+
+def main_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import block_drafter_pos_gb300 as bd
+    import workloads as wk
+
+    torch.cuda.set_device(local_rank)
+    bd.build()
+    wl = wk.workload(args.config)
+    R = wl.n_req
+    drafter, S, W, inp, kc_host, vc_host, setup_s = setup(wl, local_rank)
+    h = drafter.handle
+    K, Wm = args.steps, args.warmup
+    stream = torch.cuda.current_stream()
+    # warm-up (eager), then count launches of one step
+    for _ in range(Wm):
+        run_step(bd, h, R, S)
+    torch.cuda.synchronize()
+    n0 = bd.dflash2_launch_count(h)
+    run_step(bd, h, R, S)
+    launches_per_step = bd.dflash2_launch_count(h) - n0
+    torch.cuda.synchronize()
+    # one CUDA graph of exactly K steps, with the LM-head kernel bracketed by events
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    graph = torch.cuda.CUDAGraph()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(graph, stream=cap_stream):
+            for i in range(K):
+                bd.dflash2_set_lmhead_events(h, ev[i][0], ev[i][1])
+                run_step(bd, h, R, S)
+    bd.dflash2_set_lmhead_events(h, None, None)
+    stream.wait_stream(cap_stream)
+    graph.replay()  # warm replay (graph upload)
+    torch.cuda.synchronize()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.15)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    graph.replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    lm_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    steps_per_s = world * K / (ms / 1e3)
+    # sanity of the timed outputs
+    st = S["status"].cpu().numpy()
+    ne = S["n_emit"].cpu().numpy()
+    assert np.all(st == 0) and np.all(ne >= 1), (st, ne)
+
+    # end to end through the C ABI with host buffers
+    E = args.e2e_steps
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = {k: pin(S[k]) for k in ("anchors", "ctx_len", "n_new", "taps", "temps", "seeds", "offsets", "target")}
+    host_out = {k: torch.empty_like(S[k], device="cpu").pin_memory() for k in ("emitted", "n_emit", "n_acc")}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k, v in host_in.items():
+            S[k].copy_(v, non_blocking=True)
+        run_step(bd, h, R, S)
+        for k, v in host_out.items():
+            v.copy_(S[k], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(E):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * E / (e2e_ms / 1e3)
+
+    pk = peaks()
+    lm_bytes = bd.dflash2_lmhead_bytes(h, R)
+    lm_avg_s = statistics.mean(lm_ms) / 1e3
+    achieved = lm_bytes / lm_avg_s / 1e9
+    sb = step_bytes(wl, R)
+    step_s = ms / 1e3 / K
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.weight_format == "bf16" else "q8g64xf16",
+        "data": "synthetic (seeded, drafter geometry; random weights, no checkpoint)",
+        "config": {"workload": wl.name, "requests_per_gpu": R, "context": wl.ctx[:R], "weights": wl.weight_format,
+                   "temperature": wl.temps[:R], "l2": "inputs larger than L2 (weights stream every step)",
+                   "parallelism": f"{world} independent replica(s)", "timing": "one CUDA graph of K steps"},
+        "drafted_tokens_per_s": steps_per_s * 7 * R,
+        "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
+        "roofline": {"kernel": "lmhead_topk_kernel (LM head GEMV + fused top-16)", "bound": "hbm",
+                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": None, "launch_ms": statistics.mean(lm_ms), "share_of_step": statistics.mean(lm_ms) / (ms / K),
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"},
+        "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches_per_step * K),
+        "clocks": clk,
+        "setup_s": setup_s,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cb, _ = cpu_baseline(wl, W, inp, kc_host, vc_host, S["target"].cpu().numpy())
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main_reference(args, rank, world):
+    """The oracle, as it stands, on host cores: each step one full oracle step of request 0."""
+    if rank != 0:
+        return
+    import workloads as wk
+    import oracle
+
+    wl = wk.workload(args.config)
+    g = wl.geom
+    W = wk.make_weights(g, wl.weight_format, wl.seed)
+    inp = wk.make_request_inputs(wl)
+    cap = wl.kv_capacity
+    kc = np.zeros((g.n_layers, 1, cap, g.n_kv_heads, g.head_dim), np.uint16)
+    vc = np.zeros_like(kc)
+    for l in range(g.n_layers):
+        K, V = inp["kv"][l][0]
+        lo = int(inp["kv_lo"][0])
+        kc[l, 0, lo:lo + len(K)] = K
+        vc[l, 0, lo:lo + len(V)] = V
+    noise = wk.make_target_noise(wl, 0, 0).astype(np.float64)
+
+    def tfn(lg):
+        z = np.concatenate([lg, lg[6:7]], 0)
+        return z + noise
+
+    def one():
+        kl = [kc[l, 0].copy() for l in range(g.n_layers)]
+        vl = [vc[l, 0].copy() for l in range(g.n_layers)]
+        oracle.step(g, W, int(inp["anchors"][0]), int(inp["ctx_len"][0]), 8, inp["taps"][0], kl, vl, wl.temps[0],
+                    wl.philox_seed, 0, tfn)
+
+    steps = max(1, min(args.steps, 3))
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    v = steps / dt
+    cores = len(os.sched_getaffinity(0))
+    sample = f"{steps} full oracle step(s) of request 0 of {wl.name} after {warm} warm-up (FP64 NumPy)"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "requests_per_gpu": wl.n_req, "context": wl.ctx, "weights": wl.weight_format},
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        main_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+    main_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

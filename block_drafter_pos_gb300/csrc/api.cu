@@ -1,0 +1,644 @@
+// Host side of the C ABI: argument validation, scratch layout, and the launch
+// sequence of one draft block (a1-a9), the selector (a10) and the verify (a11).
+// No allocation after dflash2_create; no host synchronisation in the step calls.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "../../include/dflash2.h"
+#include "glue.h"
+#include "internal.h"
+
+using namespace df2;
+
+struct dflash2_handle {
+  dflash2_config cfg;
+  dflash2_weights w;
+  int max_req, kv_cap, num_sms, fmt;
+  int H, G, F, V, nq, nkv, qd, kvd, nch, KT;
+  int n_attn_chunks, n_verify_chunks, lm_ctas;
+  int s_fc, s_delta, s_qkv, s_o, s_gu, s_down, s_sel;
+  // scratch
+  char* arena;
+  size_t arena_bytes;
+  float *x, *ss_x, *ss_c, *delta_a, *delta_m, *q, *kb, *vb, *attn_part, *part, *part_sel;
+  void *act_a, *act_qkv, *act_taps, *act_o, *act_h;
+  float *xs_a, *xs_qkv, *xs_taps, *xs_o, *xs_h;
+  uint16_t* act_fin;
+  unsigned long long* topk_keys;
+  VerifyStat* vstats;
+  double* inv_freq;
+  int64_t launches;
+  cudaEvent_t ev_lm0, ev_lm1;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Smallest split count S (K/S a multiple of 128) with tiles * S >= target, else the largest.
+int choose_splits(int M, int K, int target) {
+  const int tiles = M / 16;
+  const int chunks = K / 128;
+  int best = 1;
+  for (int s = 1; s <= chunks; ++s) {
+    if (chunks % s) continue;
+    best = s;
+    if (tiles * s >= target) break;
+  }
+  return best;
+}
+
+#define DF2_CHECK(expr)                                  \
+  do {                                                   \
+    cudaError_t e_ = (expr);                             \
+    if (e_ != cudaSuccess) return DFLASH2_E_CUDA;        \
+  } while (0)
+
+GemvSeg seg(const dflash2_matrix& m, const void* x, const float* xsum, int ldx, int n_tiles, int M, int K, int splits,
+            float* out) {
+  GemvSeg s;
+  s.w = m.w;
+  s.scale = static_cast<const uint16_t*>(m.scale);
+  s.bias = static_cast<const uint16_t*>(m.bias);
+  s.x = x;
+  s.xsum = xsum;
+  s.out = out;
+  s.M = M;
+  s.K = K;
+  s.ldx = ldx;
+  s.n_tiles = n_tiles;
+  s.splits = splits;
+  s.unit_begin = 0;
+  return s;
+}
+
+dflash2_status run_gemv(dflash2_handle* h, std::initializer_list<GemvSeg> segs, cudaStream_t st) {
+  GemvArgs a;
+  memset(&a, 0, sizeof(a));
+  int u = 0, max_tiles = 0;
+  for (const GemvSeg& s : segs) {
+    a.seg[a.nseg] = s;
+    a.seg[a.nseg].unit_begin = u;
+    u += (s.M / 16) * s.splits;
+    max_tiles = std::max(max_tiles, s.n_tiles);
+    ++a.nseg;
+  }
+  a.total_units = u;
+  DF2_CHECK(launch_gemv(a, h->fmt, max_tiles, h->num_sms, st));
+  h->launches += 1;
+  return DFLASH2_OK;
+}
+
+bool valid_matrix(const dflash2_matrix& m, int fmt) {
+  if (!m.w || !aligned16(m.w)) return false;
+  if (fmt == DFLASH2_WEIGHTS_Q8G64 && (!m.scale || !m.bias)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash2_status_string(dflash2_status s) {
+  switch (s) {
+    case DFLASH2_OK: return "ok";
+    case DFLASH2_E_INVAL: return "invalid argument";
+    case DFLASH2_E_NONFINITE: return "nonfinite logit or selector score";
+    case DFLASH2_E_CUDA: return "CUDA error";
+    case DFLASH2_E_UNSUPPORTED: return "unsupported geometry";
+    default: return "unknown status";
+  }
+}
+
+dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* w, int32_t max_requests,
+                              int32_t kv_capacity, dflash2_handle** out) {
+  if (!cfg || !w || !out || max_requests < 1 || kv_capacity < 1) return DFLASH2_E_INVAL;
+  *out = nullptr;
+  const dflash2_config& c = *cfg;
+  if (c.hidden <= 0 || c.n_layers <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.ffn <= 0 || c.vocab <= 0 ||
+      c.n_taps <= 0 || c.window <= 1 || c.rms_eps < 0.f || c.rope_theta <= 0.0)
+    return DFLASH2_E_INVAL;
+  if (c.mask_token_id < 0 || c.mask_token_id >= c.vocab) return DFLASH2_E_INVAL;
+  if (c.weight_format != DFLASH2_WEIGHTS_BF16 && c.weight_format != DFLASH2_WEIGHTS_Q8G64) return DFLASH2_E_INVAL;
+  if (c.head_dim != 128 || c.block != 8 || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
+      c.conv_group != 16 || c.n_layers > DFLASH2_MAX_LAYERS || c.n_q_heads != 4 * c.n_kv_heads ||
+      c.hidden % 128 || c.ffn % 128 || c.vocab % 16 || max_requests > 4)
+    return DFLASH2_E_UNSUPPORTED;
+  const int fmt = c.weight_format;
+  if (!w->embed || !w->lm_head || !w->hidden_norm || !w->final_norm || !aligned16(w->lm_head)) return DFLASH2_E_INVAL;
+  if (!valid_matrix(w->fc, fmt) || !valid_matrix(w->sel_proj, fmt) || !valid_matrix(w->cb_a, fmt) ||
+      !valid_matrix(w->cb_b, fmt))
+    return DFLASH2_E_INVAL;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash2_layer_weights& L = w->layers[l];
+    if (!L.input_norm || !L.post_norm || !L.q_norm || !L.k_norm || !L.attn_base || !L.mlp_base) return DFLASH2_E_INVAL;
+    const dflash2_matrix* ms[] = {&L.q, &L.k, &L.v, &L.o, &L.gate, &L.up, &L.down, &L.attn_delta, &L.mlp_delta};
+    for (const dflash2_matrix* m : ms)
+      if (!valid_matrix(*m, fmt)) return DFLASH2_E_INVAL;
+  }
+  dflash2_handle* h = new (std::nothrow) dflash2_handle;
+  if (!h) return DFLASH2_E_CUDA;
+  memset(h, 0, sizeof(*h));
+  h->cfg = c;
+  h->w = *w;
+  h->max_req = max_requests;
+  h->kv_cap = kv_capacity;
+  h->fmt = fmt;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete h;
+    return DFLASH2_E_CUDA;
+  }
+  h->H = c.hidden;
+  h->G = c.hidden / 16;
+  h->F = c.ffn;
+  h->V = c.vocab;
+  h->nq = c.n_q_heads;
+  h->nkv = c.n_kv_heads;
+  h->qd = c.n_q_heads * 128;
+  h->kvd = c.n_kv_heads * 128;
+  h->nch = c.hidden / 128;
+  h->KT = c.n_taps * c.hidden;
+  h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
+  h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
+  h->lm_ctas = h->num_sms;  // one 16-warp CTA per SM (the kernel needs 128 registers a thread)
+  const int target = h->num_sms * 16;  // resident warps of the GEMV grid (one 16-warp CTA per SM)
+  h->s_fc = choose_splits(h->H, h->KT, target);
+  h->s_delta = choose_splits(4 * h->G, h->H, target);
+  h->s_qkv = choose_splits(h->qd + 2 * h->kvd, h->H, target);
+  h->s_o = choose_splits(h->H, h->qd, target);
+  h->s_gu = choose_splits(2 * h->F, h->H, target);
+  h->s_down = choose_splits(h->H, h->F, target);
+  h->s_sel = choose_splits(c.rank, h->H, target);
+  const size_t N = 8 * static_cast<size_t>(max_requests);
+  const size_t esz = 2;  // bf16 / fp16 activations
+  size_t part_elems = 0;
+  part_elems = std::max(part_elems, h->s_fc * N * h->H);
+  part_elems = std::max(part_elems, h->s_delta * N * 4 * h->G);
+  part_elems = std::max(part_elems, h->s_qkv * (N * h->qd + 2 * (2 * N) * h->kvd));
+  part_elems = std::max(part_elems, h->s_o * N * h->H);
+  part_elems = std::max(part_elems, h->s_gu * N * 2 * h->F);
+  part_elems = std::max(part_elems, h->s_down * N * h->H);
+  struct Buf {
+    void** p;
+    size_t bytes;
+  };
+  const Buf bufs[] = {
+      {reinterpret_cast<void**>(&h->x), N * h->H * 4},
+      {reinterpret_cast<void**>(&h->ss_x), N * h->nch * 4},
+      {reinterpret_cast<void**>(&h->ss_c), N * h->nch * 4},
+      {reinterpret_cast<void**>(&h->delta_a), N * 4 * h->G * 4},
+      {reinterpret_cast<void**>(&h->delta_m), N * 4 * h->G * 4},
+      {reinterpret_cast<void**>(&h->q), N * h->qd * 4},
+      {reinterpret_cast<void**>(&h->kb), N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->vb), N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->attn_part),
+       static_cast<size_t>(max_requests) * h->nkv * h->n_attn_chunks * 32 * 130 * 4},
+      {reinterpret_cast<void**>(&h->part), part_elems * 4},
+      {reinterpret_cast<void**>(&h->part_sel), h->s_sel * N * c.rank * 4},
+      {reinterpret_cast<void**>(&h->act_a), N * h->H * esz},
+      {reinterpret_cast<void**>(&h->act_qkv), 2 * N * h->H * esz},
+      {reinterpret_cast<void**>(&h->act_taps), N * h->KT * esz},
+      {reinterpret_cast<void**>(&h->act_o), N * h->qd * esz},
+      {reinterpret_cast<void**>(&h->act_h), N * h->F * esz},
+      {reinterpret_cast<void**>(&h->xs_a), N * h->H / 64 * 4},
+      {reinterpret_cast<void**>(&h->xs_qkv), 2 * N * h->H / 64 * 4},
+      {reinterpret_cast<void**>(&h->xs_taps), N * h->KT / 64 * 4},
+      {reinterpret_cast<void**>(&h->xs_o), N * h->qd / 64 * 4},
+      {reinterpret_cast<void**>(&h->xs_h), N * h->F / 64 * 4},
+      {reinterpret_cast<void**>(&h->act_fin), N * h->H * 2},
+      {reinterpret_cast<void**>(&h->topk_keys), N * h->lm_ctas * 16 * 8},
+      {reinterpret_cast<void**>(&h->vstats), static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
+      {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
+  };
+  size_t total = 0;
+  for (const Buf& b : bufs) total += (b.bytes + 255) & ~static_cast<size_t>(255);
+  if (cudaMalloc(&h->arena, total) != cudaSuccess) {
+    delete h;
+    return DFLASH2_E_CUDA;
+  }
+  h->arena_bytes = total;
+  size_t off = 0;
+  for (const Buf& b : bufs) {
+    *b.p = h->arena + off;
+    off += (b.bytes + 255) & ~static_cast<size_t>(255);
+  }
+  if (cudaMemset(h->arena, 0, total) != cudaSuccess) {
+    cudaFree(h->arena);
+    delete h;
+    return DFLASH2_E_CUDA;
+  }
+  double invf[64];
+  for (int j = 0; j < 64; ++j) invf[j] = pow(c.rope_theta, -2.0 * j / 128.0);
+  if (cudaMemcpy(h->inv_freq, invf, sizeof(invf), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(h->arena);
+    delete h;
+    return DFLASH2_E_CUDA;
+  }
+  *out = h;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_destroy(dflash2_handle* h) {
+  if (!h) return DFLASH2_E_INVAL;
+  cudaFree(h->arena);
+  delete h;
+  return DFLASH2_OK;
+}
+
+int64_t dflash2_launch_count(const dflash2_handle* h) { return h ? h->launches : -1; }
+
+dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* stop) {
+  if (!h || ((start == nullptr) != (stop == nullptr))) return DFLASH2_E_INVAL;
+  h->ev_lm0 = static_cast<cudaEvent_t>(start);
+  h->ev_lm1 = static_cast<cudaEvent_t>(stop);
+  return DFLASH2_OK;
+}
+
+int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
+  if (!h || n_req < 1) return -1;
+  const int64_t N = 8 * static_cast<int64_t>(n_req);
+  return static_cast<int64_t>(h->V) * h->H * 2          // LM-head weights, read once
+         + N * h->H * 2                                   // bf16 activations
+         + N * h->lm_ctas * 16 * 8;                       // per-CTA top-16 keys written
+}
+
+dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
+                                   const int32_t* ctx_len, const int32_t* n_new, const float* taps, void* k_cache,
+                                   void* v_cache, int32_t* cand_ids, float* cand_logits, float* gate,
+                                   float* logits_out, void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
+  if (!anchor_ids || !ctx_len || !n_new || !taps || !k_cache || !v_cache || !cand_ids || !cand_logits || !gate)
+    return DFLASH2_E_INVAL;
+  if (!aligned16(taps) || !aligned16(k_cache) || !aligned16(v_cache)) return DFLASH2_E_INVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dflash2_config& c = h->cfg;
+  const int fmt = h->fmt;
+  const int R = n_req;
+  const int N = 8 * R;
+  const int H = h->H, G = h->G;
+  const size_t layer_stride = static_cast<size_t>(h->max_req) * h->kv_cap * h->kvd;  // elements
+  // ---- a1/a2: block embedding, first norm input, taps packing
+  {
+    StartArgs a;
+    a.anchor_ids = anchor_ids;
+    a.n_new = n_new;
+    a.embed = static_cast<const uint16_t*>(h->w.embed);
+    a.norm_w = static_cast<const uint16_t*>(h->w.layers[0].input_norm);
+    a.taps = taps;
+    a.x = h->x;
+    a.act_a = h->act_a;
+    a.xsum_a = h->xs_a;
+    a.ss_x = h->ss_x;
+    a.act_taps = h->act_taps;
+    a.xsum_taps = h->xs_taps;
+    a.H = H;
+    a.n_taps = c.n_taps;
+    a.mask_id = c.mask_token_id;
+    a.nch = h->nch;
+    a.fmt = fmt;
+    a.V = h->V;
+    DF2_CHECK(launch_start(a, R, st));
+    h->launches++;
+  }
+  // ---- a1: taps projection fc [H][5H]
+  {
+    dflash2_status s = run_gemv(h, {seg(h->w.fc, h->act_taps, h->xs_taps, h->KT, R, H, h->KT, h->s_fc, h->part)}, st);
+    if (s) return s;
+    FcFinishArgs a;
+    a.part = h->part;
+    a.norm_w = static_cast<const uint16_t*>(h->w.hidden_norm);
+    a.act = h->act_qkv;
+    a.xsum = h->xs_qkv;
+    a.ss = h->ss_c;
+    a.H = H;
+    a.n_rows = N;
+    a.splits = h->s_fc;
+    a.act_row0 = N;
+    a.nch = h->nch;
+    a.fmt = fmt;
+    DF2_CHECK(launch_fc_finish(a, R, st));
+    h->launches++;
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash2_layer_weights& L = h->w.layers[l];
+    uint16_t* kc = static_cast<uint16_t*>(k_cache) + l * layer_stride;
+    uint16_t* vc = static_cast<uint16_t*>(v_cache) + l * layer_stride;
+    // ---- a3: delta projection of the normed input, conv-in
+    dflash2_status s = run_gemv(h, {seg(L.attn_delta, h->act_a, h->xs_a, H, R, 4 * G, H, h->s_delta, h->part)}, st);
+    if (s) return s;
+    {
+      ConvInArgs a;
+      a.part = h->part;
+      a.ss = h->ss_x;
+      a.x = h->x;
+      a.norm_w = static_cast<const uint16_t*>(L.input_norm);
+      a.base = static_cast<const uint16_t*>(L.attn_base);
+      a.delta = h->delta_a;
+      a.act = h->act_qkv;
+      a.xsum = h->xs_qkv;
+      a.H = H;
+      a.n_rows = N;
+      a.splits = h->s_delta;
+      a.nch = h->nch;
+      a.fmt = fmt;
+      a.eps = c.rms_eps;
+      DF2_CHECK(launch_conv_in(a, R, st));
+      h->launches++;
+    }
+    // ---- a4: q (block rows), k and v (block + new context rows)
+    float* pq = h->part;
+    float* pk = pq + static_cast<size_t>(h->s_qkv) * N * h->qd;
+    float* pv = pk + static_cast<size_t>(h->s_qkv) * 2 * N * h->kvd;
+    s = run_gemv(h,
+                 {seg(L.q, h->act_qkv, h->xs_qkv, H, R, h->qd, H, h->s_qkv, pq),
+                  seg(L.k, h->act_qkv, h->xs_qkv, H, 2 * R, h->kvd, H, h->s_qkv, pk),
+                  seg(L.v, h->act_qkv, h->xs_qkv, H, 2 * R, h->kvd, H, h->s_qkv, pv)},
+                 st);
+    if (s) return s;
+    {
+      QkvFinishArgs a;
+      a.part_q = pq;
+      a.part_k = pk;
+      a.part_v = pv;
+      a.ss_c = h->ss_c;
+      a.q_norm = static_cast<const uint16_t*>(L.q_norm);
+      a.k_norm = static_cast<const uint16_t*>(L.k_norm);
+      a.inv_freq = h->inv_freq;
+      a.ctx_len = ctx_len;
+      a.n_new = n_new;
+      a.q = h->q;
+      a.kb = h->kb;
+      a.vb = h->vb;
+      a.k_cache = kc;
+      a.v_cache = vc;
+      a.n_q_heads = h->nq;
+      a.n_kv_heads = h->nkv;
+      a.n_rows = N;
+      a.splits = h->s_qkv;
+      a.kv_capacity = h->kv_cap;
+      a.H = H;
+      a.nch = h->nch;
+      a.eps = c.rms_eps;
+      DF2_CHECK(launch_qkv_finish(a, R, st));
+      h->launches++;
+    }
+    // ---- a5: block attention over the window
+    {
+      AttnArgs a;
+      a.q = h->q;
+      a.kb = h->kb;
+      a.vb = h->vb;
+      a.k_cache = kc;
+      a.v_cache = vc;
+      a.ctx_len = ctx_len;
+      a.n_new = n_new;
+      a.part = h->attn_part;
+      a.act_o = h->act_o;
+      a.xsum_o = h->xs_o;
+      a.n_q_heads = h->nq;
+      a.n_kv_heads = h->nkv;
+      a.kv_capacity = h->kv_cap;
+      a.window = c.window;
+      a.n_chunks = h->n_attn_chunks;
+      a.fmt = fmt;
+      DF2_CHECK(launch_attention(a, R, st));
+      h->launches += 2;
+    }
+    // ---- a6: output projection, conv-out, residual; post-attention norm input
+    s = run_gemv(h, {seg(L.o, h->act_o, h->xs_o, h->qd, R, H, h->qd, h->s_o, h->part)}, st);
+    if (s) return s;
+    {
+      ConvOutArgs a;
+      a.part = h->part;
+      a.delta = h->delta_a;
+      a.base = static_cast<const uint16_t*>(L.attn_base);
+      a.norm_w = static_cast<const uint16_t*>(L.post_norm);
+      a.x = h->x;
+      a.act = h->act_a;
+      a.xsum = h->xs_a;
+      a.ss = h->ss_x;
+      a.act_bf16 = nullptr;
+      a.H = H;
+      a.n_rows = N;
+      a.splits = h->s_o;
+      a.nch = h->nch;
+      a.fmt = fmt;
+      DF2_CHECK(launch_conv_out(a, R, st));
+      h->launches++;
+    }
+    // ---- a7: MLP sublayer
+    s = run_gemv(h, {seg(L.mlp_delta, h->act_a, h->xs_a, H, R, 4 * G, H, h->s_delta, h->part)}, st);
+    if (s) return s;
+    {
+      ConvInArgs a;
+      a.part = h->part;
+      a.ss = h->ss_x;
+      a.x = h->x;
+      a.norm_w = static_cast<const uint16_t*>(L.post_norm);
+      a.base = static_cast<const uint16_t*>(L.mlp_base);
+      a.delta = h->delta_m;
+      a.act = h->act_qkv;
+      a.xsum = h->xs_qkv;
+      a.H = H;
+      a.n_rows = N;
+      a.splits = h->s_delta;
+      a.nch = h->nch;
+      a.fmt = fmt;
+      a.eps = c.rms_eps;
+      DF2_CHECK(launch_conv_in(a, R, st));
+      h->launches++;
+    }
+    float* pg = h->part;
+    float* pu = pg + static_cast<size_t>(h->s_gu) * N * h->F;
+    s = run_gemv(h,
+                 {seg(L.gate, h->act_qkv, h->xs_qkv, H, R, h->F, H, h->s_gu, pg),
+                  seg(L.up, h->act_qkv, h->xs_qkv, H, R, h->F, H, h->s_gu, pu)},
+                 st);
+    if (s) return s;
+    {
+      SwigluArgs a;
+      a.part_g = pg;
+      a.part_u = pu;
+      a.act = h->act_h;
+      a.xsum = h->xs_h;
+      a.F = h->F;
+      a.n_rows = N;
+      a.splits = h->s_gu;
+      a.fmt = fmt;
+      DF2_CHECK(launch_swiglu(a, R, st));
+      h->launches++;
+    }
+    s = run_gemv(h, {seg(L.down, h->act_h, h->xs_h, h->F, R, H, h->F, h->s_down, h->part)}, st);
+    if (s) return s;
+    {
+      const bool last = l == c.n_layers - 1;
+      ConvOutArgs a;
+      a.part = h->part;
+      a.delta = h->delta_m;
+      a.base = static_cast<const uint16_t*>(L.mlp_base);
+      a.norm_w = static_cast<const uint16_t*>(last ? h->w.final_norm : h->w.layers[l + 1].input_norm);
+      a.x = h->x;
+      a.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
+      a.xsum = h->xs_a;
+      a.ss = h->ss_x;
+      a.act_bf16 = (last && fmt != 0) ? h->act_fin : nullptr;
+      a.H = H;
+      a.n_rows = N;
+      a.splits = h->s_down;
+      a.nch = h->nch;
+      a.fmt = fmt;
+      DF2_CHECK(launch_conv_out(a, R, st));
+      h->launches++;
+    }
+  }
+  // ---- a8: LM head + top-16
+  {
+    LmHeadArgs a;
+    a.w = static_cast<const uint16_t*>(h->w.lm_head);
+    a.x = h->act_fin;
+    a.ss = h->ss_x;
+    a.logits_out = logits_out;
+    a.part_keys = h->topk_keys;
+    a.V = h->V;
+    a.H = H;
+    a.n_rows = N;
+    a.nch = h->nch;
+    a.n_cta = h->lm_ctas;
+    a.eps = c.rms_eps;
+    // external records: inside a stream capture they become event-record nodes the host can time
+    if (h->ev_lm0) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm0, st, cudaEventRecordExternal));
+    DF2_CHECK(launch_lmhead(a, st));
+    if (h->ev_lm1) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm1, st, cudaEventRecordExternal));
+    h->launches++;
+  }
+  // ---- a9: selector projection (its input is the same final hidden, in the matrix's format)
+  {
+    const void* xin = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
+    dflash2_status s = run_gemv(h, {seg(h->w.sel_proj, xin, h->xs_a, H, R, c.rank, H, h->s_sel, h->part_sel)}, st);
+    if (s) return s;
+    TopkMergeArgs a;
+    a.part_keys = h->topk_keys;
+    a.part_sel = h->part_sel;
+    a.ss = h->ss_x;
+    a.cand_ids = cand_ids;
+    a.cand_logits = cand_logits;
+    a.gate = gate;
+    a.n_rows = N;
+    a.n_cta = h->lm_ctas;
+    a.rank = c.rank;
+    a.sel_splits = h->s_sel;
+    a.nch = h->nch;
+    a.H = H;
+    a.eps = c.rms_eps;
+    DF2_CHECK(launch_topk_merge(a, st));
+    h->launches++;
+  }
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
+                                 float* cand_logits, float* logits_out, void* stream) {
+  if (!h || n_rows < 8 || n_rows % 8 || n_rows > 8 * h->max_req) return DFLASH2_E_INVAL;
+  if (!hidden || !cand_ids || !cand_logits || !aligned16(hidden)) return DFLASH2_E_INVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LmHeadArgs a;
+  a.w = static_cast<const uint16_t*>(h->w.lm_head);
+  a.x = static_cast<const uint16_t*>(hidden);
+  a.ss = nullptr;
+  a.logits_out = logits_out;
+  a.part_keys = h->topk_keys;
+  a.V = h->V;
+  a.H = h->H;
+  a.n_rows = n_rows;
+  a.nch = h->nch;
+  a.n_cta = h->lm_ctas;
+  a.eps = h->cfg.rms_eps;
+  DF2_CHECK(launch_lmhead(a, st));
+  TopkMergeArgs m;
+  m.part_keys = h->topk_keys;
+  m.part_sel = nullptr;
+  m.ss = nullptr;
+  m.cand_ids = cand_ids;
+  m.cand_logits = cand_logits;
+  m.gate = nullptr;
+  m.n_rows = n_rows;
+  m.n_cta = h->lm_ctas;
+  m.rank = h->cfg.rank;
+  m.sel_splits = 0;
+  m.nch = h->nch;
+  m.H = h->H;
+  m.eps = h->cfg.rms_eps;
+  DF2_CHECK(launch_topk_merge(m, st));
+  h->launches += 2;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids, const int32_t* cand_ids,
+                              const float* cand_logits, const float* gate, const float* temperature,
+                              const uint64_t* seed, const uint64_t* philox_offset, int32_t* path, float* q_rows,
+                              float* scores_out, int32_t* status, void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
+  if (!anchor_ids || !cand_ids || !cand_logits || !gate || !temperature || !seed || !philox_offset || !path ||
+      !q_rows || !status)
+    return DFLASH2_E_INVAL;
+  SelectArgs a;
+  a.anchor_ids = anchor_ids;
+  a.cand_ids = cand_ids;
+  a.cand_logits = cand_logits;
+  a.gate = gate;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.offset = philox_offset;
+  a.cb_a = h->w.cb_a.w;
+  a.cb_a_scale = static_cast<const uint16_t*>(h->w.cb_a.scale);
+  a.cb_a_bias = static_cast<const uint16_t*>(h->w.cb_a.bias);
+  a.cb_b = h->w.cb_b.w;
+  a.cb_b_scale = static_cast<const uint16_t*>(h->w.cb_b.scale);
+  a.cb_b_bias = static_cast<const uint16_t*>(h->w.cb_b.bias);
+  a.path = path;
+  a.q_rows = q_rows;
+  a.scores_out = scores_out;
+  a.status = status;
+  a.rank = h->cfg.rank;
+  a.fmt = h->fmt;
+  a.V = h->V;
+  DF2_CHECK(launch_select(a, n_req, static_cast<cudaStream_t>(stream)));
+  h->launches++;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* target_logits, const int32_t* path,
+                              const int32_t* cand_ids, const float* q_rows, const float* temperature,
+                              const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
+                              int32_t* emitted, int32_t* n_emitted, int32_t* status, void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
+  if (!target_logits || !path || !cand_ids || !q_rows || !temperature || !seed || !philox_offset || !n_accepted ||
+      !emitted || !n_emitted || !status)
+    return DFLASH2_E_INVAL;
+  VerifyArgs a;
+  a.logits = target_logits;
+  a.path = path;
+  a.cand_ids = cand_ids;
+  a.q_rows = q_rows;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.offset = philox_offset;
+  a.stats = h->vstats;
+  a.n_accepted = n_accepted;
+  a.emitted = emitted;
+  a.n_emitted = n_emitted;
+  a.status = status;
+  a.V = h->V;
+  a.n_chunks = h->n_verify_chunks;
+  DF2_CHECK(launch_verify(a, n_req, static_cast<cudaStream_t>(stream)));
+  h->launches += 2;
+  return DFLASH2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// Argument blocks of the element-wise stages (glue.cu) and the attention,
+// LM-head, selector and verify kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace df2 {
+
+struct StartArgs {
+  const int32_t* anchor_ids;
+  const int32_t* n_new;
+  const uint16_t* embed;   // bf16 [V][H]
+  const uint16_t* norm_w;  // input_norm of layer 0
+  const float* taps;       // [R][8][n_taps*H]
+  float* x;                // residual stream [N][H]
+  void* act_a;             // GEMV input of layer 0's delta projection [N][H]
+  float* xsum_a;
+  float* ss_x;             // [N][nch]
+  void* act_taps;          // [N][n_taps*H]
+  float* xsum_taps;
+  int H, n_taps, mask_id, nch, fmt, V;
+};
+
+struct FcFinishArgs {
+  const float* part;       // [splits][n_rows][H]
+  const uint16_t* norm_w;  // hidden_norm
+  void* act;               // act_qkv (context rows start at act_row0)
+  float* xsum;
+  float* ss;               // [N][nch]  sums of squares of the projected taps
+  int H, n_rows, splits, act_row0, nch, fmt;
+};
+
+struct ConvInArgs {
+  const float* part;       // delta partials [splits][n_rows][4G]
+  const float* ss;         // [N][nch] of x
+  const float* x;          // residual stream
+  const uint16_t* norm_w;
+  const uint16_t* base;    // [4][H]
+  float* delta;            // out: [N][4G] (scaled by 1/rms)
+  void* act;               // out: conv-in'd activations [N][H]
+  float* xsum;
+  int H, n_rows, splits, nch, fmt;
+  float eps;
+};
+
+struct ConvOutArgs {
+  const float* part;       // sublayer output partials [splits][n_rows][H]
+  const float* delta;      // [N][4G]
+  const uint16_t* base;    // [4][H]
+  const uint16_t* norm_w;  // norm of the next sublayer (x * w is emitted)
+  float* x;                // residual stream, updated in place
+  void* act;
+  float* xsum;
+  float* ss;               // [N][nch] of the updated x
+  uint16_t* act_bf16;      // optional second copy of x * w in bf16 (LM-head input), or null
+  int H, n_rows, splits, nch, fmt;
+};
+
+struct SwigluArgs {
+  const float* part_g;
+  const float* part_u;     // [splits][n_rows][F]
+  void* act;               // [N][F]
+  float* xsum;
+  int F, n_rows, splits, fmt;
+};
+
+struct QkvFinishArgs {
+  const float* part_q;     // [splits][n_rows][nq*128]
+  const float* part_k;     // [splits][2*n_rows][nkv*128]: block rows, then context rows
+  const float* part_v;
+  const float* ss_c;       // [N][nch] of the projected taps
+  const uint16_t* q_norm;
+  const uint16_t* k_norm;
+  const double* inv_freq;  // [64]
+  const int32_t* ctx_len;
+  const int32_t* n_new;
+  float* q;                // [N][nq][128]
+  float* kb;               // [N][nkv][128]
+  float* vb;
+  uint16_t* k_cache;       // this layer's slice: [max_req][cap][nkv][128]
+  uint16_t* v_cache;
+  int n_q_heads, n_kv_heads, n_rows, splits, kv_capacity, H, nch;
+  float eps;
+};
+
+cudaError_t launch_start(const StartArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  const float* q;          // [N][nq][128]
+  const float* kb;         // [N][nkv][128]
+  const float* vb;
+  const uint16_t* k_cache; // this layer's slice [max_req][cap][nkv][128]
+  const uint16_t* v_cache;
+  const int32_t* ctx_len;
+  const int32_t* n_new;
+  float* part;             // [R][nkv][n_chunks][32][130]
+  void* act_o;             // [N][nq*128]
+  float* xsum_o;
+  int n_q_heads, n_kv_heads, kv_capacity, window, n_chunks, fmt;
+};
+constexpr int kAttnChunk = 128;
+cudaError_t launch_attention(const AttnArgs& a, int n_req, cudaStream_t st);
+
+// ---------------------------------------------------------------- LM head + top-k
+struct LmHeadArgs {
+  const uint16_t* w;       // bf16 [V][H]
+  const uint16_t* x;       // bf16 [N][H]: x * final_norm_w
+  const float* ss;         // [N][nch] sums of squares of x
+  float* logits_out;       // [R][7][V] or null
+  unsigned long long* part_keys;  // [N][n_cta][16]
+  int V, H, n_rows, nch, n_cta;
+  float eps;
+};
+cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t st);
+
+struct TopkMergeArgs {
+  const unsigned long long* part_keys;  // [N][n_cta][16]
+  const float* part_sel;   // selector projection partials [splits][N][rank]
+  const float* ss;
+  int32_t* cand_ids;       // [R][7][16]
+  float* cand_logits;
+  float* gate;             // [R][7][rank]
+  int n_rows, n_cta, rank, sel_splits, nch, H;
+  float eps;
+};
+cudaError_t launch_topk_merge(const TopkMergeArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------- selector
+struct SelectArgs {
+  const int32_t* anchor_ids;
+  const int32_t* cand_ids;     // [R][7][16]
+  const float* cand_logits;
+  const float* gate;           // [R][7][rank]
+  const float* temperature;
+  const uint64_t* seed;
+  const uint64_t* offset;
+  const void* cb_a;            // bf16 [V][rank] or int8 codes
+  const uint16_t* cb_a_scale;
+  const uint16_t* cb_a_bias;
+  const void* cb_b;
+  const uint16_t* cb_b_scale;
+  const uint16_t* cb_b_bias;
+  int32_t* path;
+  float* q_rows;
+  float* scores_out;           // [R][7][16][16] or null
+  int32_t* status;
+  int rank, fmt, V;
+};
+cudaError_t launch_select(const SelectArgs& a, int n_req, cudaStream_t st);
+
+// ---------------------------------------------------------------- verify
+constexpr int kVerifyChunk = 4096;
+struct VerifyStat {
+  float m;       // chunk max (of z)
+  float s;       // sum exp((z - m) / T) over the chunk (T > 0)
+  int32_t arg;   // argmax (smallest index among equal maxima)
+  int32_t flags; // bit 0: NaN seen, bit 1: +inf seen
+};
+struct VerifyArgs {
+  const float* logits;         // [R][8][V]
+  const int32_t* path;         // [R][7]
+  const int32_t* cand_ids;     // [R][7][16]
+  const float* q_rows;         // [R][7][16]
+  const float* temperature;
+  const uint64_t* seed;
+  const uint64_t* offset;
+  VerifyStat* stats;           // [R][8][n_chunks]
+  int32_t* n_accepted;
+  int32_t* emitted;            // [R][8]
+  int32_t* n_emitted;
+  int32_t* status;
+  int V, n_chunks;
+};
+cudaError_t launch_verify(const VerifyArgs& a, int n_req, cudaStream_t st);
+
+}  // namespace df2

@@ -1,0 +1,340 @@
+// Verification of the 7 proposals (step a11): exact match against the target
+// argmax for greedy requests; probability-ratio rejection with residual sampling
+// for T > 0 ("LSE docs/DFLASH2.md", first paragraph: the target verifies all
+// seven proposals with probability-ratio rejection and residual sampling, greedy
+// requests stay deterministic).
+//
+// Pass 1 (grid R x 8 rows x vocab chunks): per chunk max, argmax (smallest index on
+// ties), sum of exp((z - m) / T), NaN / +inf flags.  Pass 2 (one CTA per request):
+// folds the chunk statistics in a fixed order and runs the sequential accept chain;
+// a residual or bonus draw locates its vocabulary chunk from per-chunk masses and
+// scans that one chunk with a block-wide prefix sum.
+#include <math.h>
+
+#include "common.cuh"
+#include "glue.h"
+#include "philox.cuh"
+
+namespace df2 {
+
+namespace {
+
+constexpr int kB = 8, kP = 7, kK = 16;
+
+__global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
+  __shared__ float sm_m[8], sm_s[8];
+  __shared__ int sm_a[8], sm_f[8];
+  const int rj = blockIdx.x;  // r * 8 + j
+  const int r = rj >> 3;
+  const int chunk = blockIdx.y;
+  const float T = a.temperature[r];
+  const float* z = a.logits + static_cast<size_t>(rj) * a.V;
+  const int v0 = chunk * kVerifyChunk;
+  const int v1 = min(a.V, v0 + kVerifyChunk);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  float m = -INFINITY;
+  int arg = 0x7FFFFFFF;
+  int flags = 0;
+  for (int v = v0 + threadIdx.x; v < v1; v += 256) {
+    const float x = z[v];
+    if (isnan(x)) {
+      flags |= 1;
+      continue;
+    }
+    if (x == INFINITY) flags |= 2;
+    if (x > m || (x == m && v < arg)) {
+      m = x;
+      arg = v;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
+    if (om > m || (om == m && oa < arg)) {
+      m = om;
+      arg = oa;
+    }
+    flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+  }
+  if (lane == 0) {
+    sm_m[wid] = m;
+    sm_a[wid] = arg;
+    sm_f[wid] = flags;
+  }
+  __syncthreads();
+  float M = sm_m[0];
+  int A = sm_a[0], F = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (sm_m[w] > M || (sm_m[w] == M && sm_a[w] < A)) {
+      M = sm_m[w];
+      A = sm_a[w];
+    }
+    F |= sm_f[w];
+  }
+  float s = 0.f;
+  if (T > 0.f && M > -INFINITY && M < INFINITY) {
+    const float inv_t = 1.f / T;
+    for (int v = v0 + threadIdx.x; v < v1; v += 256) {
+      const float x = z[v];
+      if (!isnan(x)) s += expf((x - M) * inv_t);
+    }
+    s = warp_sum(s);
+    __syncthreads();
+    if (lane == 0) sm_s[wid] = s;
+    __syncthreads();
+    s = 0.f;
+    for (int w = 0; w < 8; ++w) s += sm_s[w];
+  }
+  if (threadIdx.x == 0) {
+    VerifyStat st;
+    st.m = M;
+    st.s = s;
+    st.arg = A;
+    st.flags = F;
+    a.stats[static_cast<size_t>(rj) * a.n_chunks + chunk] = st;
+  }
+}
+
+// Inverse-CDF draw over the vocabulary of row j from weights w(x) = p(x) - min(p(x),
+// q(x)) (residual, use_q) or p(x) (bonus / zero residual).  Runs on the whole CTA.
+__device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* st, float M, float tot, float T,
+                        const int* cid, const float* qv, bool use_q, float u, float* csum, float* red) {
+  // chunk masses (fixed order): p-mass of chunk c = s_c * exp((m_c - M)/T) / tot,
+  // minus the candidates' min(p, q) in that chunk when drawing from the residual.
+  const int nc = a.n_chunks;
+  const float inv_t = 1.f / T;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    float mass = (st[c].m > -INFINITY) ? st[c].s * expf((st[c].m - M) * inv_t) / tot : 0.f;
+    if (use_q) {
+      for (int k = 0; k < kK; ++k) {
+        if (cid[k] / kVerifyChunk == c) {
+          const float p = expf((z[cid[k]] - M) * inv_t) / tot;
+          mass -= fminf(p, qv[k]);
+        }
+      }
+      mass = fmaxf(mass, 0.f);
+    }
+    csum[c] = mass;
+  }
+  __syncthreads();
+  __shared__ int sh_chunk;
+  __shared__ float sh_before, sh_total;
+  if (threadIdx.x == 0) {
+    float total = 0.f;
+    for (int c = 0; c < nc; ++c) total += csum[c];
+    bool fallback = use_q && !(total > 1e-30f);
+    if (fallback) {
+      total = 0.f;
+      for (int c = 0; c < nc; ++c) {
+        csum[c] = (st[c].m > -INFINITY) ? st[c].s * expf((st[c].m - M) * inv_t) / tot : 0.f;
+        total += csum[c];
+      }
+    }
+    const float target = u * total;
+    float acc = 0.f;
+    int pick = -1, lastpos = 0;
+    for (int c = 0; c < nc; ++c) {
+      if (csum[c] > 0.f) lastpos = c;
+      if (pick < 0 && acc + csum[c] > target) pick = c;
+      if (pick < 0) acc += csum[c];
+    }
+    sh_before = target - acc;  // remaining mass to cover inside the chunk
+    if (pick < 0) {
+      pick = lastpos;               // rounding left u * total past the end:
+      sh_before = INFINITY;         // take the last positive entry of the last chunk
+    }
+    sh_chunk = pick;
+    sh_total = fallback ? -1.f : 1.f;
+  }
+  __syncthreads();
+  const int c = sh_chunk;
+  const bool q_on = use_q && sh_total > 0.f;
+  const float need = sh_before;
+  const int v0 = c * kVerifyChunk;
+  const int v1 = min(a.V, v0 + kVerifyChunk);
+  // block-wide scan in id order: each thread owns a contiguous run of 16 ids
+  const int per = kVerifyChunk / 256;
+  const int b0 = v0 + threadIdx.x * per;
+  float wv[kVerifyChunk / 256];
+  float run = 0.f;
+  for (int t = 0; t < per; ++t) {
+    const int v = b0 + t;
+    float w = 0.f;
+    if (v < v1) {
+      const float x = z[v];
+      w = isnan(x) ? 0.f : expf((x - M) * inv_t) / tot;
+      if (q_on) {
+        for (int k = 0; k < kK; ++k)
+          if (cid[k] == v) w = fmaxf(0.f, w - qv[k]);
+      }
+    }
+    wv[t] = w;
+    run += w;
+  }
+  // exclusive prefix of the per-thread runs
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  float incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) red[wid] = incl;
+  __syncthreads();
+  float wbase = 0.f;
+  for (int w = 0; w < wid; ++w) wbase += red[w];
+  float acc = wbase + incl - run;
+  __shared__ int sh_pick, sh_last;
+  if (threadIdx.x == 0) {
+    sh_pick = 0x7FFFFFFF;
+    sh_last = -1;
+  }
+  __syncthreads();
+  int found = 0x7FFFFFFF, lastpos = -1;
+  for (int t = 0; t < per; ++t) {
+    if (wv[t] > 0.f) lastpos = b0 + t;
+    acc += wv[t];
+    if (found == 0x7FFFFFFF && acc > need && wv[t] > 0.f) found = b0 + t;
+  }
+  if (found != 0x7FFFFFFF) atomicMin(&sh_pick, found);
+  if (lastpos >= 0) atomicMax(&sh_last, lastpos);
+  __syncthreads();
+  int x = sh_pick != 0x7FFFFFFF ? sh_pick : sh_last;
+  if (x < 0) x = st[c].arg;
+  __syncthreads();
+  return x;
+}
+
+__global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
+  extern __shared__ float csum[];  // [n_chunks]
+  __shared__ float red[8];
+  __shared__ float rowM[kB], rowS[kB];
+  __shared__ int rowA[kB], rowBad;
+  __shared__ int cid[kK];
+  __shared__ float qv[kK];
+  __shared__ int sh_decision;
+  const int r = blockIdx.x;
+  int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
+  if (a.status[r] != 0) {
+    if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
+    if (threadIdx.x == 0) {
+      a.n_accepted[r] = 0;
+      a.n_emitted[r] = 0;
+    }
+    return;
+  }
+  const float T = a.temperature[r];
+  const VerifyStat* st = a.stats + static_cast<size_t>(r) * kB * a.n_chunks;
+  if (threadIdx.x < kB) {
+    const int j = threadIdx.x;
+    const VerifyStat* sj = st + static_cast<size_t>(j) * a.n_chunks;
+    float M = -INFINITY;
+    int A = 0x7FFFFFFF, F = 0;
+    for (int c = 0; c < a.n_chunks; ++c) {
+      F |= sj[c].flags;
+      if (sj[c].m > M || (sj[c].m == M && sj[c].arg < A)) {
+        M = sj[c].m;
+        A = sj[c].arg;
+      }
+    }
+    float S = 0.f;
+    if (T > 0.f && M > -INFINITY && M < INFINITY)
+      for (int c = 0; c < a.n_chunks; ++c)
+        if (sj[c].m > -INFINITY) S += sj[c].s * expf((sj[c].m - M) / T);
+    rowM[j] = M;
+    rowS[j] = S;
+    rowA[j] = A;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bad = 0;
+    for (int j = 0; j < kB; ++j) {
+      const VerifyStat* sj = st + static_cast<size_t>(j) * a.n_chunks;
+      for (int c = 0; c < a.n_chunks; ++c) bad |= sj[c].flags;
+      if (!(rowM[j] > -INFINITY) || !(rowM[j] < INFINITY)) bad = 1;
+    }
+    rowBad = bad;
+  }
+  __syncthreads();
+  if (rowBad) {
+    if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
+    if (threadIdx.x == 0) {
+      a.n_accepted[r] = 0;
+      a.n_emitted[r] = 0;
+      a.status[r] = 2;
+    }
+    return;
+  }
+  const int32_t* path = a.path + static_cast<size_t>(r) * kP;
+  if (!(T > 0.f)) {
+    if (threadIdx.x == 0) {
+      int n = 0;
+      while (n < kP && path[n] == rowA[n]) {
+        emitted[n] = path[n];
+        ++n;
+      }
+      emitted[n] = rowA[n];
+      for (int j = n + 1; j < kB; ++j) emitted[j] = -1;
+      a.n_accepted[r] = n;
+      a.n_emitted[r] = n + 1;
+    }
+    return;
+  }
+  const uint64_t seed = a.seed[r], off = a.offset[r];
+  const float* zr = a.logits + static_cast<size_t>(r) * kB * a.V;
+  for (int j = 0; j < kP; ++j) {
+    const float* z = zr + static_cast<size_t>(j) * a.V;
+    if (threadIdx.x < kK) {
+      cid[threadIdx.x] = min(max(a.cand_ids[(static_cast<size_t>(r) * kP + j) * kK + threadIdx.x], 0), a.V - 1);
+      qv[threadIdx.x] = a.q_rows[(static_cast<size_t>(r) * kP + j) * kK + threadIdx.x];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int d = min(max(path[j], 0), a.V - 1);
+      float qd = 0.f;
+      for (int k = 0; k < kK; ++k)
+        if (cid[k] == d) qd = qv[k];
+      const float pd = expf((z[d] - rowM[j]) / T) / rowS[j];
+      const float u = philox_uniform(seed, off, static_cast<uint32_t>(j), kPurposeAccept);
+      sh_decision = (qd > 0.f) ? (u * qd < pd) : 1;
+    }
+    __syncthreads();
+    if (sh_decision) {
+      if (threadIdx.x == 0) emitted[j] = path[j];
+      __syncthreads();
+      continue;
+    }
+    const float u = philox_uniform(seed, off, static_cast<uint32_t>(j), kPurposeResample);
+    const int x = draw_row(a, z, st + static_cast<size_t>(j) * a.n_chunks, rowM[j], rowS[j], T, cid, qv, true, u,
+                           csum, red);
+    if (threadIdx.x == 0) {
+      emitted[j] = x;
+      for (int t = j + 1; t < kB; ++t) emitted[t] = -1;
+      a.n_accepted[r] = j;
+      a.n_emitted[r] = j + 1;
+    }
+    return;
+  }
+  const float u = philox_uniform(seed, off, static_cast<uint32_t>(kP), kPurposeResample);
+  const float* z = zr + static_cast<size_t>(kP) * a.V;
+  const int x = draw_row(a, z, st + static_cast<size_t>(kP) * a.n_chunks, rowM[kP], rowS[kP], T, cid, qv, false, u,
+                         csum, red);
+  if (threadIdx.x == 0) {
+    emitted[kP] = x;
+    a.n_accepted[r] = kP;
+    a.n_emitted[r] = kP + 1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs& a, int n_req, cudaStream_t st) {
+  verify_stats_kernel<<<dim3(n_req * kB, a.n_chunks), 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  verify_chain_kernel<<<n_req, 256, a.n_chunks * sizeof(float), st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace df2

@@ -1,0 +1,211 @@
+/*
+ * dflash2.h - C ABI of one DFlash2 draft + select + verify step on an sm_103a GPU.
+ *
+ * The step is the one described by the DFlash2 pages:
+ *   - "LSE docs/DFLASH2.md": drafter geometry (5 layers, width 5120, 32 query /
+ *     8 KV heads, head dim 128, FFN 17408, RoPE theta 1e7), the 8-position block
+ *     (anchor + 7 mask tokens, noncausal, 2048-key sliding window over context
+ *     K/V), 2-tap dynamic convolution over groups of 16 channels, top-16
+ *     candidates with rank-256 selector codebooks, probability-ratio rejection
+ *     with residual sampling, the top-k ordering policy and the affine Q8/g64
+ *     weight format;
+ *   - "[Spec Decode] DFlash2: local convolution + candidate selector - #52816"
+ *     (vLLM PR description): the convolution formula, the selector edge score,
+ *     the walk from the verified anchor and the q returned for the verify.
+ *
+ * Conventions (all entry points):
+ *   - Every tensor argument is a DEVICE pointer owned by the caller, unless the
+ *     argument says "host".  The handle owns only its scratch.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL =
+ *     the legacy default stream).  They do not synchronise, and allocate nothing
+ *     after dflash2_create.
+ *   - Errors the host can see (bad sizes, NULL pointers, misalignment) return
+ *     DFLASH2_E_INVAL before anything is launched.  A launch failure returns
+ *     DFLASH2_E_CUDA.  Errors found on the device (a NaN or +inf logit or
+ *     selector score) go to the per-request `status` words; such a request gets
+ *     n_accepted = n_emitted = 0.
+ *   - One handle serves one stream at a time (its scratch is shared by calls).
+ *   - Integers are int32 unless stated; BF16 is stored as 16-bit patterns.
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t dflash2_status;
+enum {
+  DFLASH2_OK = 0,
+  DFLASH2_E_INVAL = 1,        /* bad argument: size, NULL pointer, alignment            */
+  DFLASH2_E_NONFINITE = 2,    /* device status word: NaN/+inf logit or selector score   */
+  DFLASH2_E_CUDA = 3,         /* CUDA launch or runtime error                           */
+  DFLASH2_E_UNSUPPORTED = 4   /* geometry or request count with no instantiated kernel  */
+};
+
+enum { DFLASH2_WEIGHTS_BF16 = 0, DFLASH2_WEIGHTS_Q8G64 = 1 };
+
+#define DFLASH2_MAX_LAYERS 8
+
+/* Drafter geometry ("LSE docs/DFLASH2.md", compatible-drafter paragraph). */
+typedef struct dflash2_config {
+  int32_t hidden;         /* H: 5120                                              */
+  int32_t n_layers;       /* 5 (<= DFLASH2_MAX_LAYERS)                            */
+  int32_t n_q_heads;      /* 32                                                   */
+  int32_t n_kv_heads;     /* 8                                                    */
+  int32_t head_dim;       /* 128 (the only value with kernels)                    */
+  int32_t ffn;            /* F: 17408                                             */
+  int32_t vocab;          /* V: 248320                                            */
+  int32_t n_taps;         /* target feature taps: 5                               */
+  int32_t block;          /* positions per draft block: 8 (anchor + 7 masks)      */
+  int32_t top_k;          /* candidates per position: 16                          */
+  int32_t rank;           /* selector codebook rank: 256                          */
+  int32_t window;         /* sliding window over context keys: 2048               */
+  int32_t conv_taps;      /* dynamic convolution taps: 2                          */
+  int32_t conv_group;     /* channels per dynamic coefficient: 16                 */
+  int32_t mask_token_id;  /* id of the mask token (embedding row)                 */
+  int32_t weight_format;  /* DFLASH2_WEIGHTS_BF16 or DFLASH2_WEIGHTS_Q8G64        */
+  double rope_theta;      /* 1e7                                                  */
+  float rms_eps;          /* RMSNorm epsilon: 1e-6                                */
+} dflash2_config;
+
+/* One weight matrix W [out][in], row-major.
+ * BF16 format: w = bf16[out][in]; scale = bias = NULL.
+ * Q8G64 format ("LSE docs/DFLASH2.md", Q8 paragraph): w = int8 codes [out][in],
+ * scale and bias = bf16 [out][in/64]; the weight is scale * code + bias. */
+typedef struct dflash2_matrix {
+  const void* w;
+  const void* scale;
+  const void* bias;
+} dflash2_matrix;
+
+/* Per-layer weights.  Norm weights and convolution bases are BF16 in both formats.
+ *   input_norm, post_norm [H]; q_norm, k_norm [head_dim]
+ *   q [nq*hd][H], k [nkv*hd][H], v [nkv*hd][H], o [H][nq*hd]
+ *   gate, up [F][H], down [H][F]
+ *   attn_delta, mlp_delta [2*conv_taps*H/conv_group][H]: row (io*taps + t)*G + g,
+ *     io 0 = the convolution before the sublayer, 1 = after it, G = H/conv_group
+ *   attn_base, mlp_base [2*conv_taps][H]: row io*taps + t */
+typedef struct dflash2_layer_weights {
+  const void* input_norm;
+  const void* post_norm;
+  const void* q_norm;
+  const void* k_norm;
+  const void* attn_base;
+  const void* mlp_base;
+  dflash2_matrix q, k, v, o, gate, up, down, attn_delta, mlp_delta;
+} dflash2_layer_weights;
+
+/* All weights.  embed and lm_head [V][H] are BF16 (shared with the target);
+ * fc [H][n_taps*H]; hidden_norm, final_norm [H]; sel_proj [rank][H];
+ * cb_a, cb_b [V][rank] (selector codebooks, predecessor and successor). */
+typedef struct dflash2_weights {
+  const void* embed;
+  const void* lm_head;
+  const void* hidden_norm;
+  const void* final_norm;
+  dflash2_matrix fc, sel_proj, cb_a, cb_b;
+  dflash2_layer_weights layers[DFLASH2_MAX_LAYERS];
+} dflash2_weights;
+
+typedef struct dflash2_handle dflash2_handle;
+
+/* Creates a handle: validates the geometry, copies the weight pointers (the
+ * weights stay caller-owned and must outlive the handle) and allocates the
+ * scratch for up to `max_requests` requests.  `kv_capacity` is the number of
+ * positions per request in the caller's K/V caches.  Must be called with the
+ * target device current.  Returns DFLASH2_E_UNSUPPORTED for a geometry the
+ * kernels do not cover (head_dim != 128, block != 8, top_k != 16, ...). */
+dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* w, int32_t max_requests,
+                              int32_t kv_capacity, dflash2_handle** out);
+
+dflash2_status dflash2_destroy(dflash2_handle* h);
+
+/* Draft block: steps a1-a9 of the method for n_req requests.
+ *   anchor_ids [R]       verified anchor token of each request
+ *   ctx_len [R]          keys already in the cache before this call
+ *   n_new [R]            new context rows to append (0..block)
+ *   taps [R][block][n_taps*H] float32: target feature taps of the new rows
+ *                        (rows >= n_new[r] are ignored)
+ *   k_cache, v_cache     bf16 [n_layers][max_requests][kv_capacity][nkv][hd]; rows
+ *                        ctx_len..ctx_len+n_new-1 of each request are written (the
+ *                        new context rows' K after k_norm and RoPE, and V), then
+ *                        rows max(0, L-window+1)..L-1 are read, L = ctx_len+n_new
+ *   cand_ids [R][block-1][top_k]     top-16 vocabulary ids of positions 1..7, in
+ *                        order: NaN first (by id), then value descending, ties to
+ *                        the smaller id ("LSE docs/DFLASH2.md", top-k paragraph)
+ *   cand_logits [R][block-1][top_k] float32 drafter logits of those ids
+ *   gate [R][block-1][rank] float32  selector projection of the final hidden state
+ *   logits_out [R][block-1][V] float32 or NULL: full drafter logits (debugging,
+ *                        test harness)
+ * Requires ctx_len + n_new + 0 <= kv_capacity. */
+dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
+                                   const int32_t* ctx_len, const int32_t* n_new, const float* taps,
+                                   void* k_cache, void* v_cache, int32_t* cand_ids, float* cand_logits,
+                                   float* gate, float* logits_out, void* stream);
+
+/* Selector walk (step a10; vLLM PR #52816 description, candidate selector):
+ * score(p -> c) = <A[p] * gate_i, B[c]> + cand_logit_i[c]; the walk starts at the
+ * anchor.  temperature[r] == 0: greedy, argmax with ties to the smaller id, q row
+ * one-hot.  temperature[r] > 0: q_i = softmax(score / T) over the 16 candidates, the
+ * choice is the first j with cumsum_j > u * sum, u from Philox4x32-10 with key =
+ * seed[r], counter = (philox_offset[r] lo32, hi32, slot = i-1, purpose 0).
+ *   path [R][block-1] chosen ids; q_rows [R][block-1][top_k] float32
+ *   scores_out [R][block-1][top_k][top_k] float32 or NULL: the score lattice
+ *   status [R] written: DFLASH2_OK or DFLASH2_E_NONFINITE (nonfinite logit/score)
+ *   temperature [R] float32 (negative -> status DFLASH2_E_INVAL); seed, philox_offset [R] uint64 */
+dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
+                              const int32_t* cand_ids, const float* cand_logits, const float* gate,
+                              const float* temperature, const uint64_t* seed, const uint64_t* philox_offset,
+                              int32_t* path, float* q_rows, float* scores_out, int32_t* status, void* stream);
+
+/* Verification (step a11; "LSE docs/DFLASH2.md", first paragraph).
+ *   target_logits [R][block][V] float32: row j is the target's distribution for
+ *   block position j+1 (row block-1 = the bonus position).
+ *   Greedy (T == 0): accept while path[j] == argmax row j (ties -> smaller id);
+ *   emit the argmax at the first mismatch, or of the last row if all accepted.
+ *   T > 0: p_j = softmax(row j / T); accept if u < p_j(d)/q_j(d) (purpose 1, slot
+ *   j); on rejection draw from max(0, p_j - q_j) normalised by inverse CDF in id
+ *   order (purpose 2, slot j; from p_j if that mass <= 1e-30); if all accepted draw
+ *   the bonus from the last row (purpose 2, slot block-1).
+ *   n_accepted [R]; emitted [R][block] (-1 padded); n_emitted [R] = n_accepted+1.
+ *   status [R] in/out: a request whose status is nonzero on entry is skipped
+ *   (n_accepted = n_emitted = 0); a NaN or +inf in a row, or a row whose maximum
+ *   is -inf, sets DFLASH2_E_NONFINITE. */
+dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* target_logits, const int32_t* path,
+                              const int32_t* cand_ids, const float* q_rows, const float* temperature,
+                              const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
+                              int32_t* emitted, int32_t* n_emitted, int32_t* status, void* stream);
+
+/* LM head + top-16 alone (step a8 on given final hidden states): logits of block
+ * positions 1..7 = W_lm . hidden (hidden already normalised, BF16), top-16 with the
+ * ordering of dflash2_draft_block.  Row n of `hidden` is request n/8, block position
+ * n%8 (position 0 is not projected).  n_rows: multiple of 8, <= 8*max_requests.
+ *   hidden [n_rows][H] bf16; cand_ids, cand_logits [n_rows/8][block-1][top_k];
+ *   logits_out [n_rows/8][block-1][V] float32 or NULL. */
+dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
+                                 float* cand_logits, float* logits_out, void* stream);
+
+/* Number of kernel launches the handle has issued since it was created (all
+ * entry points).  Host-side counter; no device work. */
+int64_t dflash2_launch_count(const dflash2_handle* h);
+
+/* Profiling hook: when both events are non-NULL (cudaEvent_t passed as void*),
+ * dflash2_draft_block records `start` right before and `stop` right after its
+ * LM-head + top-16 kernel on the call's stream.  NULL, NULL turns it off. */
+dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* stop);
+
+/* Algorithmic bytes the LM-head + top-16 kernel of one draft_block call streams
+ * (LM-head weights + activations + candidate outputs), for roofline reports. */
+int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req);
+
+/* Human-readable text of a status code (static string). */
+const char* dflash2_status_string(dflash2_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

@@ -8,6 +8,7 @@ binding) and the CPU oracle take their inputs from here.
 from .configs import Geometry, Workload, TOY, FULL, WORKLOADS, workload  # noqa: F401
 from .gen import (  # noqa: F401
     bf16_bits_from_f32, f32_from_bf16_bits, quantize_q8g64, make_weights,
-    make_request_inputs, make_target_noise, tap_rows, WEIGHT_NAMES_GLOBAL,
+    make_request_inputs, make_target_noise, tap_rows, kv_rows, make_selector_inputs,
+    make_verify_inputs, WEIGHT_NAMES_GLOBAL,
     WEIGHT_NAMES_LAYER, MATRIX_NAMES,
 )

@@ -245,3 +245,42 @@ def make_target_noise(wl: Workload, step: int, req: int) -> np.ndarray:
     """N(0, sigma_req^2) noise [block][V] added to drafter logits to form target logits."""
     g = wl.geom
     return normal_f32((g.block, g.vocab), wl.sigma[req], 0.0, wl.seed, f"noise/{step}/{req}")
+
+
+def make_selector_inputs(V: int, R: int, seed: int, integer: bool = False, K: int = 16, P: int = 7, rank: int = 256):
+    """Synthetic selector inputs shaped like a draft block's output: distinct candidate
+    ids per position, candidate logits in descending order, a gate vector per position.
+    integer=True draws small integers (exact in every precision, with many ties)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x5E1])))
+    anchors = rng.integers(0, V, size=R).astype(np.int32)
+    cand = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(P)]) for _ in range(R)]).astype(np.int32)
+    if integer:
+        cl = -np.sort(-rng.integers(-3, 4, size=(R, P, K)), axis=2).astype(np.float32)
+        gate = rng.integers(-2, 3, size=(R, P, rank)).astype(np.float32)
+    else:
+        cl = -np.sort(-rng.normal(0, 1.4, size=(R, P, K)), axis=2).astype(np.float32)
+        gate = rng.normal(0, 1.4, size=(R, P, rank)).astype(np.float32)
+    return {"anchors": anchors, "cand_ids": cand, "cand_logits": cl, "gate": gate}
+
+
+def make_verify_inputs(V: int, R: int, seed: int, temps, integer: bool = False, accept_depth=None, K: int = 16):
+    """Synthetic verify inputs: target rows [R][8][V], a path through distinct candidate
+    ids [R][7][16] with q rows [R][7][16].  Target rows are N(0, 1.5) (integers in
+    [-4, 4] when integer=True) with the path token raised by `boost` on the first
+    accept_depth[r] rows, so acceptance depths vary."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x7E2])))
+    P = 7
+    if integer:
+        z = rng.integers(-4, 5, size=(R, 8, V)).astype(np.float32)
+    else:
+        z = rng.normal(0, 1.5, size=(R, 8, V)).astype(np.float32)
+    cand = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(P)]) for _ in range(R)]).astype(np.int32)
+    q = rng.dirichlet(np.ones(K) * 0.5, size=(R, P)).astype(np.float32)
+    pick = rng.integers(0, K, size=(R, P))
+    path = np.take_along_axis(cand, pick[..., None], axis=2)[..., 0].astype(np.int32)
+    depth = accept_depth if accept_depth is not None else rng.integers(0, 8, size=R)
+    for r in range(R):
+        for j in range(min(int(depth[r]), P)):
+            z[r, j, path[r, j]] += 6.0 if not integer else 8.0
+    return {"target": z, "path": path, "cand_ids": cand, "q_rows": q,
+            "temps": np.asarray(temps, np.float32)}
