@@ -213,6 +213,10 @@ def main_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     # one CUDA graph of exactly K steps, with the LM-head kernel bracketed by events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:  # torch creates the CUDA events on first record; the graph re-records them
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream()
     cap_stream.wait_stream(stream)

@@ -1,12 +1,18 @@
 // Host side of the C ABI: argument validation, scratch layout, and the launch
 // sequence of one draft block (a1-a9), the selector (a10) and the verify (a11).
 // No allocation after dflash2_create; no host synchronisation in the step calls.
+//
+// Per layer the draft block launches: delta projection, conv-in, QKV projection,
+// q/k norm + RoPE + cache append, block attention (+ combine), output projection
+// (epilogue: conv-out + residual + post-norm input), delta projection, conv-in,
+// gate/up projection (epilogue: SwiGLU), down projection (epilogue: conv-out +
+// residual + next norm input).  Every kernel is launched with programmatic
+// dependent launch so its prologue overlaps the previous kernel's tail.
 #include <math.h>
 #include <string.h>
 
 #include <algorithm>
 #include <new>
-#include <vector>
 
 #include "../../include/dflash2.h"
 #include "glue.h"
@@ -18,16 +24,20 @@ struct dflash2_handle {
   dflash2_config cfg;
   dflash2_weights w;
   int max_req, kv_cap, num_sms, fmt;
-  int H, G, F, V, nq, nkv, qd, kvd, nch, KT;
+  bool pdl;
+  int H, G, F, V, nq, nkv, qd, kvd, KT;
+  int nch128, nch16;  // chunks of the two kinds of sums-of-squares partials
   int n_attn_chunks, n_verify_chunks, lm_ctas;
-  int s_fc, s_delta, s_qkv, s_o, s_gu, s_down, s_sel;
   // scratch
   char* arena;
   size_t arena_bytes;
-  float *x, *ss_x, *ss_c, *delta_a, *delta_m, *q, *kb, *vb, *attn_part, *part, *part_sel;
+  float *x, *ss128, *ss16, *ss_c, *dproj, *delta_a, *delta_m, *fc_out, *q_out, *k_out, *v_out, *sel_out;
+  float *q, *kb, *vb, *attn_part, *part;
+  int* counters;
   void *act_a, *act_qkv, *act_taps, *act_o, *act_h;
-  float *xs_a, *xs_qkv, *xs_taps, *xs_o, *xs_h;
   uint16_t* act_fin;
+  // element offsets of the low-order activation planes (x = hi + lo)
+  size_t lo_a, lo_qkv, lo_taps, lo_o, lo_h, lo_fin;
   unsigned long long* topk_keys;
   VerifyStat* vstats;
   double* inv_freq;
@@ -39,56 +49,46 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Smallest split count S (K/S a multiple of 128) with tiles * S >= target, else the largest.
-int choose_splits(int M, int K, int target) {
-  const int tiles = M / 16;
-  const int chunks = K / 128;
-  int best = 1;
-  for (int s = 1; s <= chunks; ++s) {
-    if (chunks % s) continue;
-    best = s;
-    if (tiles * s >= target) break;
-  }
-  return best;
-}
-
-#define DF2_CHECK(expr)                                  \
-  do {                                                   \
-    cudaError_t e_ = (expr);                             \
-    if (e_ != cudaSuccess) return DFLASH2_E_CUDA;        \
+#define DF2_CHECK(expr)                           \
+  do {                                            \
+    cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return DFLASH2_E_CUDA; \
   } while (0)
 
-GemvSeg seg(const dflash2_matrix& m, const void* x, const float* xsum, int ldx, int n_tiles, int M, int K, int splits,
-            float* out) {
+GemvSeg seg_base(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, int n_tiles, int rows, int K) {
   GemvSeg s;
+  memset(&s, 0, sizeof(s));
   s.w = m.w;
   s.scale = static_cast<const uint16_t*>(m.scale);
   s.bias = static_cast<const uint16_t*>(m.bias);
   s.x = x;
-  s.xsum = xsum;
-  s.out = out;
-  s.M = M;
-  s.K = K;
+  s.xlo_off = xlo;
   s.ldx = ldx;
+  s.K = K;
   s.n_tiles = n_tiles;
-  s.splits = splits;
-  s.unit_begin = 0;
+  s.tiles = rows / 16;
+  s.epi = kEpiStore;
+  return s;
+}
+
+GemvSeg seg_store(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, int n_tiles, int M, int K, float* out) {
+  GemvSeg s = seg_base(m, x, xlo, ldx, n_tiles, M, K);
+  s.out = out;
+  s.ldo = M;
   return s;
 }
 
 dflash2_status run_gemv(dflash2_handle* h, std::initializer_list<GemvSeg> segs, cudaStream_t st) {
   GemvArgs a;
   memset(&a, 0, sizeof(a));
-  int u = 0, max_tiles = 0;
+  int max_tiles = 0;
   for (const GemvSeg& s : segs) {
-    a.seg[a.nseg] = s;
-    a.seg[a.nseg].unit_begin = u;
-    u += (s.M / 16) * s.splits;
+    a.seg[a.nseg++] = s;
     max_tiles = std::max(max_tiles, s.n_tiles);
-    ++a.nseg;
   }
-  a.total_units = u;
-  DF2_CHECK(launch_gemv(a, h->fmt, max_tiles, h->num_sms, st));
+  a.part = h->part;
+  a.counters = h->counters;
+  DF2_CHECK(launch_gemv(a, h->fmt, max_tiles, h->num_sms, h->pdl, st));
   h->launches += 1;
   return DFLASH2_OK;
 }
@@ -97,6 +97,36 @@ bool valid_matrix(const dflash2_matrix& m, int fmt) {
   if (!m.w || !aligned16(m.w)) return false;
   if (fmt == DFLASH2_WEIGHTS_Q8G64 && (!m.scale || !m.bias)) return false;
   return true;
+}
+
+// Scratch of the largest GEMV launch of a step (partial slots, tile counters).
+void gemv_scratch(const dflash2_handle* h, int R, size_t* part_floats, int* counters) {
+  const int N = 8 * R;
+  const dflash2_matrix dummy = {nullptr, nullptr, nullptr};
+  GemvSeg list[][3] = {
+      {seg_base(dummy, nullptr, 0, h->KT, R, h->H, h->KT)},
+      {seg_base(dummy, nullptr, 0, h->H, R, 4 * h->G, h->H)},
+      {seg_base(dummy, nullptr, 0, h->H, R, h->qd, h->H), seg_base(dummy, nullptr, 0, h->H, 2 * R, h->kvd, h->H),
+       seg_base(dummy, nullptr, 0, h->H, 2 * R, h->kvd, h->H)},
+      {seg_base(dummy, nullptr, 0, h->qd, R, h->H, h->qd)},
+      {seg_base(dummy, nullptr, 0, h->H, R, 2 * h->F, h->H)},
+      {seg_base(dummy, nullptr, 0, h->F, R, h->H, h->F)},
+      {seg_base(dummy, nullptr, 0, h->H, R, h->cfg.rank, h->H)},
+  };
+  const int nsegs[] = {1, 1, 3, 1, 1, 1, 1};
+  (void)N;
+  *part_floats = 0;
+  *counters = 0;
+  for (int i = 0; i < 7; ++i) {
+    GemvArgs a;
+    memset(&a, 0, sizeof(a));
+    for (int j = 0; j < nsegs[i]; ++j) a.seg[a.nseg++] = list[i][j];
+    size_t pf = 0;
+    int nc = 0;
+    gemv_plan(a, h->fmt, h->num_sms, &pf, &nc);
+    *part_floats = std::max(*part_floats, pf);
+    *counters = std::max(*counters, nc);
+  }
 }
 
 }  // namespace
@@ -126,7 +156,8 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   if (c.weight_format != DFLASH2_WEIGHTS_BF16 && c.weight_format != DFLASH2_WEIGHTS_Q8G64) return DFLASH2_E_INVAL;
   if (c.head_dim != 128 || c.block != 8 || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
       c.conv_group != 16 || c.n_layers > DFLASH2_MAX_LAYERS || c.n_q_heads != 4 * c.n_kv_heads ||
-      c.hidden % 128 || c.ffn % 128 || c.vocab % 16 || max_requests > 4)
+      c.hidden % 128 || c.ffn % 128 || c.vocab % 16 || max_requests > 4 ||
+      (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1 > 64)
     return DFLASH2_E_UNSUPPORTED;
   const int fmt = c.weight_format;
   if (!w->embed || !w->lm_head || !w->hidden_norm || !w->final_norm || !aligned16(w->lm_head)) return DFLASH2_E_INVAL;
@@ -148,6 +179,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->max_req = max_requests;
   h->kv_cap = kv_capacity;
   h->fmt = fmt;
+  h->pdl = true;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -162,60 +194,58 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->nkv = c.n_kv_heads;
   h->qd = c.n_q_heads * 128;
   h->kvd = c.n_kv_heads * 128;
-  h->nch = c.hidden / 128;
   h->KT = c.n_taps * c.hidden;
+  h->nch128 = c.hidden / 128;
+  h->nch16 = c.hidden / 16;
   h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
   h->lm_ctas = h->num_sms;  // one 16-warp CTA per SM (the kernel needs 128 registers a thread)
-  const int target = h->num_sms * 16;  // resident warps of the GEMV grid (one 16-warp CTA per SM)
-  h->s_fc = choose_splits(h->H, h->KT, target);
-  h->s_delta = choose_splits(4 * h->G, h->H, target);
-  h->s_qkv = choose_splits(h->qd + 2 * h->kvd, h->H, target);
-  h->s_o = choose_splits(h->H, h->qd, target);
-  h->s_gu = choose_splits(2 * h->F, h->H, target);
-  h->s_down = choose_splits(h->H, h->F, target);
-  h->s_sel = choose_splits(c.rank, h->H, target);
   const size_t N = 8 * static_cast<size_t>(max_requests);
   const size_t esz = 2;  // bf16 / fp16 activations
-  size_t part_elems = 0;
-  part_elems = std::max(part_elems, h->s_fc * N * h->H);
-  part_elems = std::max(part_elems, h->s_delta * N * 4 * h->G);
-  part_elems = std::max(part_elems, h->s_qkv * (N * h->qd + 2 * (2 * N) * h->kvd));
-  part_elems = std::max(part_elems, h->s_o * N * h->H);
-  part_elems = std::max(part_elems, h->s_gu * N * 2 * h->F);
-  part_elems = std::max(part_elems, h->s_down * N * h->H);
+  size_t part_floats = 0;
+  int n_counters = 0;
+  gemv_scratch(h, max_requests, &part_floats, &n_counters);
   struct Buf {
     void** p;
     size_t bytes;
   };
   const Buf bufs[] = {
       {reinterpret_cast<void**>(&h->x), N * h->H * 4},
-      {reinterpret_cast<void**>(&h->ss_x), N * h->nch * 4},
-      {reinterpret_cast<void**>(&h->ss_c), N * h->nch * 4},
+      {reinterpret_cast<void**>(&h->ss128), N * h->nch128 * 4},
+      {reinterpret_cast<void**>(&h->ss16), N * h->nch16 * 4},
+      {reinterpret_cast<void**>(&h->ss_c), N * h->nch128 * 4},
+      {reinterpret_cast<void**>(&h->dproj), N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_a), N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_m), N * 4 * h->G * 4},
+      {reinterpret_cast<void**>(&h->fc_out), N * h->H * 4},
+      {reinterpret_cast<void**>(&h->q_out), N * h->qd * 4},
+      {reinterpret_cast<void**>(&h->k_out), 2 * N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->v_out), 2 * N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->sel_out), N * c.rank * 4},
       {reinterpret_cast<void**>(&h->q), N * h->qd * 4},
       {reinterpret_cast<void**>(&h->kb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->vb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->attn_part),
        static_cast<size_t>(max_requests) * h->nkv * h->n_attn_chunks * 32 * 130 * 4},
-      {reinterpret_cast<void**>(&h->part), part_elems * 4},
-      {reinterpret_cast<void**>(&h->part_sel), h->s_sel * N * c.rank * 4},
-      {reinterpret_cast<void**>(&h->act_a), N * h->H * esz},
-      {reinterpret_cast<void**>(&h->act_qkv), 2 * N * h->H * esz},
-      {reinterpret_cast<void**>(&h->act_taps), N * h->KT * esz},
-      {reinterpret_cast<void**>(&h->act_o), N * h->qd * esz},
-      {reinterpret_cast<void**>(&h->act_h), N * h->F * esz},
-      {reinterpret_cast<void**>(&h->xs_a), N * h->H / 64 * 4},
-      {reinterpret_cast<void**>(&h->xs_qkv), 2 * N * h->H / 64 * 4},
-      {reinterpret_cast<void**>(&h->xs_taps), N * h->KT / 64 * 4},
-      {reinterpret_cast<void**>(&h->xs_o), N * h->qd / 64 * 4},
-      {reinterpret_cast<void**>(&h->xs_h), N * h->F / 64 * 4},
-      {reinterpret_cast<void**>(&h->act_fin), N * h->H * 2},
+      {reinterpret_cast<void**>(&h->part), part_floats * 4},
+      {reinterpret_cast<void**>(&h->counters), static_cast<size_t>(n_counters) * 4},
+      {reinterpret_cast<void**>(&h->act_a), 2 * N * h->H * esz},  // hi and lo planes
+      {reinterpret_cast<void**>(&h->act_qkv), 2 * 2 * N * h->H * esz},
+      {reinterpret_cast<void**>(&h->act_taps), 2 * N * h->KT * esz},
+      {reinterpret_cast<void**>(&h->act_o), 2 * N * h->qd * esz},
+      {reinterpret_cast<void**>(&h->act_h), 2 * N * h->F * esz},
+      {reinterpret_cast<void**>(&h->act_fin), 2 * N * h->H * 2},
       {reinterpret_cast<void**>(&h->topk_keys), N * h->lm_ctas * 16 * 8},
-      {reinterpret_cast<void**>(&h->vstats), static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
+      {reinterpret_cast<void**>(&h->vstats),
+       static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
       {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
   };
+  h->lo_a = N * h->H;
+  h->lo_qkv = 2 * N * h->H;
+  h->lo_taps = N * h->KT;
+  h->lo_o = N * h->qd;
+  h->lo_h = N * h->F;
+  h->lo_fin = N * h->H;
   size_t total = 0;
   for (const Buf& b : bufs) total += (b.bytes + 255) & ~static_cast<size_t>(255);
   if (cudaMalloc(&h->arena, total) != cudaSuccess) {
@@ -228,14 +258,10 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
     *b.p = h->arena + off;
     off += (b.bytes + 255) & ~static_cast<size_t>(255);
   }
-  if (cudaMemset(h->arena, 0, total) != cudaSuccess) {
-    cudaFree(h->arena);
-    delete h;
-    return DFLASH2_E_CUDA;
-  }
   double invf[64];
   for (int j = 0; j < 64; ++j) invf[j] = pow(c.rope_theta, -2.0 * j / 128.0);
-  if (cudaMemcpy(h->inv_freq, invf, sizeof(invf), cudaMemcpyHostToDevice) != cudaSuccess) {
+  if (cudaMemset(h->arena, 0, total) != cudaSuccess ||
+      cudaMemcpy(h->inv_freq, invf, sizeof(invf), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaFree(h->arena);
     delete h;
     return DFLASH2_E_CUDA;
@@ -263,9 +289,9 @@ dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* s
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
   if (!h || n_req < 1) return -1;
   const int64_t N = 8 * static_cast<int64_t>(n_req);
-  return static_cast<int64_t>(h->V) * h->H * 2          // LM-head weights, read once
-         + N * h->H * 2                                   // bf16 activations
-         + N * h->lm_ctas * 16 * 8;                       // per-CTA top-16 keys written
+  return static_cast<int64_t>(h->V) * h->H * 2  // LM-head weights, read once
+         + 2 * N * h->H * 2                      // bf16 hidden state, hi and lo planes
+         + N * h->lm_ctas * 16 * 8;              // per-CTA top-16 keys written
 }
 
 dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
@@ -279,11 +305,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dflash2_config& c = h->cfg;
   const int fmt = h->fmt;
+  const bool pdl = h->pdl;
   const int R = n_req;
   const int N = 8 * R;
   const int H = h->H, G = h->G;
   const size_t layer_stride = static_cast<size_t>(h->max_req) * h->kv_cap * h->kvd;  // elements
-  // ---- a1/a2: block embedding, first norm input, taps packing
+  // ---- a2: block embedding, first norm input, taps packing
   {
     StartArgs a;
     a.anchor_ids = anchor_ids;
@@ -293,79 +320,75 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.taps = taps;
     a.x = h->x;
     a.act_a = h->act_a;
-    a.xsum_a = h->xs_a;
-    a.ss_x = h->ss_x;
+    a.act_a_lo = h->lo_a;
+    a.ss_x = h->ss128;
     a.act_taps = h->act_taps;
-    a.xsum_taps = h->xs_taps;
+    a.act_taps_lo = h->lo_taps;
     a.H = H;
     a.n_taps = c.n_taps;
     a.mask_id = c.mask_token_id;
-    a.nch = h->nch;
+    a.nch = h->nch128;
     a.fmt = fmt;
     a.V = h->V;
-    DF2_CHECK(launch_start(a, R, st));
+    DF2_CHECK(launch_start(a, R, pdl, st));
     h->launches++;
   }
-  // ---- a1: taps projection fc [H][5H]
+  // ---- a1: taps projection fc [H][n_taps H], then hidden_norm input of the context rows
   {
-    dflash2_status s = run_gemv(h, {seg(h->w.fc, h->act_taps, h->xs_taps, h->KT, R, H, h->KT, h->s_fc, h->part)}, st);
+    dflash2_status s = run_gemv(h, {seg_store(h->w.fc, h->act_taps, h->lo_taps, h->KT, R, H, h->KT, h->fc_out)}, st);
     if (s) return s;
     FcFinishArgs a;
-    a.part = h->part;
+    a.y = h->fc_out;
     a.norm_w = static_cast<const uint16_t*>(h->w.hidden_norm);
     a.act = h->act_qkv;
-    a.xsum = h->xs_qkv;
+    a.act_lo = h->lo_qkv;
     a.ss = h->ss_c;
     a.H = H;
-    a.n_rows = N;
-    a.splits = h->s_fc;
     a.act_row0 = N;
-    a.nch = h->nch;
+    a.nch = h->nch128;
     a.fmt = fmt;
-    DF2_CHECK(launch_fc_finish(a, R, st));
+    DF2_CHECK(launch_fc_finish(a, R, pdl, st));
     h->launches++;
   }
+  const float* ss_in = h->ss128;  // sums of squares of the current x and their chunk count
+  int nch_in = h->nch128;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& L = h->w.layers[l];
     uint16_t* kc = static_cast<uint16_t*>(k_cache) + l * layer_stride;
     uint16_t* vc = static_cast<uint16_t*>(v_cache) + l * layer_stride;
     // ---- a3: delta projection of the normed input, conv-in
-    dflash2_status s = run_gemv(h, {seg(L.attn_delta, h->act_a, h->xs_a, H, R, 4 * G, H, h->s_delta, h->part)}, st);
+    dflash2_status s =
+        run_gemv(h, {seg_store(L.attn_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
-      a.part = h->part;
-      a.ss = h->ss_x;
+      a.dproj = h->dproj;
+      a.ss = ss_in;
       a.x = h->x;
       a.norm_w = static_cast<const uint16_t*>(L.input_norm);
       a.base = static_cast<const uint16_t*>(L.attn_base);
       a.delta = h->delta_a;
       a.act = h->act_qkv;
-      a.xsum = h->xs_qkv;
+      a.act_lo = h->lo_qkv;
       a.H = H;
-      a.n_rows = N;
-      a.splits = h->s_delta;
-      a.nch = h->nch;
+      a.nch = nch_in;
       a.fmt = fmt;
       a.eps = c.rms_eps;
-      DF2_CHECK(launch_conv_in(a, R, st));
+      DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
     // ---- a4: q (block rows), k and v (block + new context rows)
-    float* pq = h->part;
-    float* pk = pq + static_cast<size_t>(h->s_qkv) * N * h->qd;
-    float* pv = pk + static_cast<size_t>(h->s_qkv) * 2 * N * h->kvd;
     s = run_gemv(h,
-                 {seg(L.q, h->act_qkv, h->xs_qkv, H, R, h->qd, H, h->s_qkv, pq),
-                  seg(L.k, h->act_qkv, h->xs_qkv, H, 2 * R, h->kvd, H, h->s_qkv, pk),
-                  seg(L.v, h->act_qkv, h->xs_qkv, H, 2 * R, h->kvd, H, h->s_qkv, pv)},
+                 {seg_store(L.q, h->act_qkv, h->lo_qkv, H, R, h->qd, H, h->q_out),
+                  seg_store(L.k, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->k_out),
+                  seg_store(L.v, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->v_out)},
                  st);
     if (s) return s;
     {
       QkvFinishArgs a;
-      a.part_q = pq;
-      a.part_k = pk;
-      a.part_v = pv;
+      a.q_out = h->q_out;
+      a.k_out = h->k_out;
+      a.v_out = h->v_out;
       a.ss_c = h->ss_c;
       a.q_norm = static_cast<const uint16_t*>(L.q_norm);
       a.k_norm = static_cast<const uint16_t*>(L.k_norm);
@@ -380,12 +403,11 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.n_q_heads = h->nq;
       a.n_kv_heads = h->nkv;
       a.n_rows = N;
-      a.splits = h->s_qkv;
       a.kv_capacity = h->kv_cap;
       a.H = H;
-      a.nch = h->nch;
+      a.nch = h->nch128;
       a.eps = c.rms_eps;
-      DF2_CHECK(launch_qkv_finish(a, R, st));
+      DF2_CHECK(launch_qkv_finish(a, R, pdl, st));
       h->launches++;
     }
     // ---- a5: block attention over the window
@@ -400,101 +422,86 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.n_new = n_new;
       a.part = h->attn_part;
       a.act_o = h->act_o;
-      a.xsum_o = h->xs_o;
+      a.act_o_lo = h->lo_o;
       a.n_q_heads = h->nq;
       a.n_kv_heads = h->nkv;
       a.kv_capacity = h->kv_cap;
       a.window = c.window;
       a.n_chunks = h->n_attn_chunks;
       a.fmt = fmt;
-      DF2_CHECK(launch_attention(a, R, st));
+      DF2_CHECK(launch_attention(a, R, pdl, st));
       h->launches += 2;
     }
-    // ---- a6: output projection, conv-out, residual; post-attention norm input
-    s = run_gemv(h, {seg(L.o, h->act_o, h->xs_o, h->qd, R, H, h->qd, h->s_o, h->part)}, st);
-    if (s) return s;
+    // ---- a6: output projection; epilogue: conv-out, residual, post-attention norm input
     {
-      ConvOutArgs a;
-      a.part = h->part;
-      a.delta = h->delta_a;
-      a.base = static_cast<const uint16_t*>(L.attn_base);
-      a.norm_w = static_cast<const uint16_t*>(L.post_norm);
-      a.x = h->x;
-      a.act = h->act_a;
-      a.xsum = h->xs_a;
-      a.ss = h->ss_x;
-      a.act_bf16 = nullptr;
-      a.H = H;
-      a.n_rows = N;
-      a.splits = h->s_o;
-      a.nch = h->nch;
-      a.fmt = fmt;
-      DF2_CHECK(launch_conv_out(a, R, st));
-      h->launches++;
+      GemvSeg sg = seg_base(L.o, h->act_o, h->lo_o, h->qd, R, H, h->qd);
+      sg.epi = kEpiConvOut;
+      sg.act = h->act_a;
+      sg.act_lo = h->lo_a;
+      sg.ld_act = H;
+      sg.act_fmt = fmt;
+      sg.xres = h->x;
+      sg.delta = h->delta_a;
+      sg.base = static_cast<const uint16_t*>(L.attn_base);
+      sg.norm_w = static_cast<const uint16_t*>(L.post_norm);
+      sg.ss = h->ss16;
+      sg.G = G;
+      s = run_gemv(h, {sg}, st);
+      if (s) return s;
     }
+    ss_in = h->ss16;
+    nch_in = h->nch16;
     // ---- a7: MLP sublayer
-    s = run_gemv(h, {seg(L.mlp_delta, h->act_a, h->xs_a, H, R, 4 * G, H, h->s_delta, h->part)}, st);
+    s = run_gemv(h, {seg_store(L.mlp_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
-      a.part = h->part;
-      a.ss = h->ss_x;
+      a.dproj = h->dproj;
+      a.ss = ss_in;
       a.x = h->x;
       a.norm_w = static_cast<const uint16_t*>(L.post_norm);
       a.base = static_cast<const uint16_t*>(L.mlp_base);
       a.delta = h->delta_m;
       a.act = h->act_qkv;
-      a.xsum = h->xs_qkv;
+      a.act_lo = h->lo_qkv;
       a.H = H;
-      a.n_rows = N;
-      a.splits = h->s_delta;
-      a.nch = h->nch;
+      a.nch = nch_in;
       a.fmt = fmt;
       a.eps = c.rms_eps;
-      DF2_CHECK(launch_conv_in(a, R, st));
+      DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
-    float* pg = h->part;
-    float* pu = pg + static_cast<size_t>(h->s_gu) * N * h->F;
-    s = run_gemv(h,
-                 {seg(L.gate, h->act_qkv, h->xs_qkv, H, R, h->F, H, h->s_gu, pg),
-                  seg(L.up, h->act_qkv, h->xs_qkv, H, R, h->F, H, h->s_gu, pu)},
-                 st);
-    if (s) return s;
     {
-      SwigluArgs a;
-      a.part_g = pg;
-      a.part_u = pu;
-      a.act = h->act_h;
-      a.xsum = h->xs_h;
-      a.F = h->F;
-      a.n_rows = N;
-      a.splits = h->s_gu;
-      a.fmt = fmt;
-      DF2_CHECK(launch_swiglu(a, R, st));
-      h->launches++;
+      GemvSeg sg = seg_base(L.gate, h->act_qkv, h->lo_qkv, H, R, 2 * h->F, H);  // tile = 8 gate + 8 up rows
+      sg.w2 = L.up.w;
+      sg.scale2 = static_cast<const uint16_t*>(L.up.scale);
+      sg.bias2 = static_cast<const uint16_t*>(L.up.bias);
+      sg.epi = kEpiSwiglu;
+      sg.act = h->act_h;
+      sg.act_lo = h->lo_h;
+      sg.ld_act = h->F;
+      sg.act_fmt = fmt;
+      s = run_gemv(h, {sg}, st);
+      if (s) return s;
     }
-    s = run_gemv(h, {seg(L.down, h->act_h, h->xs_h, h->F, R, H, h->F, h->s_down, h->part)}, st);
-    if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
-      ConvOutArgs a;
-      a.part = h->part;
-      a.delta = h->delta_m;
-      a.base = static_cast<const uint16_t*>(L.mlp_base);
-      a.norm_w = static_cast<const uint16_t*>(last ? h->w.final_norm : h->w.layers[l + 1].input_norm);
-      a.x = h->x;
-      a.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
-      a.xsum = h->xs_a;
-      a.ss = h->ss_x;
-      a.act_bf16 = (last && fmt != 0) ? h->act_fin : nullptr;
-      a.H = H;
-      a.n_rows = N;
-      a.splits = h->s_down;
-      a.nch = h->nch;
-      a.fmt = fmt;
-      DF2_CHECK(launch_conv_out(a, R, st));
-      h->launches++;
+      GemvSeg sg = seg_base(L.down, h->act_h, h->lo_h, h->F, R, H, h->F);
+      sg.epi = kEpiConvOut;
+      sg.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
+      sg.act_lo = (last && fmt == 0) ? h->lo_fin : h->lo_a;
+      sg.ld_act = H;
+      sg.act_fmt = fmt;
+      sg.act2 = (last && fmt != 0) ? h->act_fin : nullptr;  // LM-head input is bf16 in both formats
+      sg.act2_lo = h->lo_fin;
+      sg.xres = h->x;
+      sg.delta = h->delta_m;
+      sg.base = static_cast<const uint16_t*>(L.mlp_base);
+      sg.norm_w = static_cast<const uint16_t*>(last ? h->w.final_norm : h->w.layers[l + 1].input_norm);
+      sg.ss = h->ss16;
+      sg.G = G;
+      s = run_gemv(h, {sg}, st);
+      if (s) return s;
     }
   }
   // ---- a8: LM head + top-16
@@ -502,41 +509,42 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     LmHeadArgs a;
     a.w = static_cast<const uint16_t*>(h->w.lm_head);
     a.x = h->act_fin;
-    a.ss = h->ss_x;
+    a.x_lo = h->lo_fin;
+    a.ss = h->ss16;
     a.logits_out = logits_out;
     a.part_keys = h->topk_keys;
     a.V = h->V;
     a.H = H;
     a.n_rows = N;
-    a.nch = h->nch;
+    a.nch = h->nch16;
     a.n_cta = h->lm_ctas;
     a.eps = c.rms_eps;
     // external records: inside a stream capture they become event-record nodes the host can time
     if (h->ev_lm0) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm0, st, cudaEventRecordExternal));
-    DF2_CHECK(launch_lmhead(a, st));
+    DF2_CHECK(launch_lmhead(a, pdl, st));
     if (h->ev_lm1) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm1, st, cudaEventRecordExternal));
     h->launches++;
   }
-  // ---- a9: selector projection (its input is the same final hidden, in the matrix's format)
+  // ---- a9: selector projection (same final hidden, in the matrix's format), merge top-16
   {
     const void* xin = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
-    dflash2_status s = run_gemv(h, {seg(h->w.sel_proj, xin, h->xs_a, H, R, c.rank, H, h->s_sel, h->part_sel)}, st);
+    const size_t xlo = fmt == 0 ? h->lo_fin : h->lo_a;
+    dflash2_status s = run_gemv(h, {seg_store(h->w.sel_proj, xin, xlo, H, R, c.rank, H, h->sel_out)}, st);
     if (s) return s;
     TopkMergeArgs a;
     a.part_keys = h->topk_keys;
-    a.part_sel = h->part_sel;
-    a.ss = h->ss_x;
+    a.sel = h->sel_out;
+    a.ss = h->ss16;
     a.cand_ids = cand_ids;
     a.cand_logits = cand_logits;
     a.gate = gate;
     a.n_rows = N;
     a.n_cta = h->lm_ctas;
     a.rank = c.rank;
-    a.sel_splits = h->s_sel;
-    a.nch = h->nch;
+    a.nch = h->nch16;
     a.H = H;
     a.eps = c.rms_eps;
-    DF2_CHECK(launch_topk_merge(a, st));
+    DF2_CHECK(launch_topk_merge(a, pdl, st));
     h->launches++;
   }
   return DFLASH2_OK;
@@ -550,19 +558,20 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   LmHeadArgs a;
   a.w = static_cast<const uint16_t*>(h->w.lm_head);
   a.x = static_cast<const uint16_t*>(hidden);
+  a.x_lo = 0;
   a.ss = nullptr;
   a.logits_out = logits_out;
   a.part_keys = h->topk_keys;
   a.V = h->V;
   a.H = h->H;
   a.n_rows = n_rows;
-  a.nch = h->nch;
+  a.nch = h->nch16;
   a.n_cta = h->lm_ctas;
   a.eps = h->cfg.rms_eps;
-  DF2_CHECK(launch_lmhead(a, st));
+  DF2_CHECK(launch_lmhead(a, h->pdl, st));
   TopkMergeArgs m;
   m.part_keys = h->topk_keys;
-  m.part_sel = nullptr;
+  m.sel = nullptr;
   m.ss = nullptr;
   m.cand_ids = cand_ids;
   m.cand_logits = cand_logits;
@@ -570,11 +579,10 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   m.n_rows = n_rows;
   m.n_cta = h->lm_ctas;
   m.rank = h->cfg.rank;
-  m.sel_splits = 0;
-  m.nch = h->nch;
+  m.nch = h->nch16;
   m.H = h->H;
   m.eps = h->cfg.rms_eps;
-  DF2_CHECK(launch_topk_merge(m, st));
+  DF2_CHECK(launch_topk_merge(m, h->pdl, st));
   h->launches += 2;
   return DFLASH2_OK;
 }
@@ -608,7 +616,7 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   a.rank = h->cfg.rank;
   a.fmt = h->fmt;
   a.V = h->V;
-  DF2_CHECK(launch_select(a, n_req, static_cast<cudaStream_t>(stream)));
+  DF2_CHECK(launch_select(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches++;
   return DFLASH2_OK;
 }
@@ -636,7 +644,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   a.status = status;
   a.V = h->V;
   a.n_chunks = h->n_verify_chunks;
-  DF2_CHECK(launch_verify(a, n_req, static_cast<cudaStream_t>(stream)));
+  DF2_CHECK(launch_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches += 2;
   return DFLASH2_OK;
 }

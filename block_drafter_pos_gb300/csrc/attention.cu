@@ -6,253 +6,307 @@
 // L + i - k < window.  GQA: the 4 query heads of one KV head share its keys.
 //
 // Split over keys (flash-decoding style): one CTA per (request, KV head, chunk of
-// 128 context keys), plus one CTA for the 8 block keys; all 32 queries of the KV
+// 64 context keys), plus one CTA for the 8 block keys; all 32 queries of a KV
 // head group (4 heads x 8 positions) are handled together so every key is read
-// once.  Keys outside the window are never read.  A combine kernel merges the
-// chunk partials (max, sum, unnormalised output) in a fixed order.
+// once.  Keys outside the window are never read.  Context chunks run on the
+// tensor cores (mma.sync m16n8k16, bf16 K/V as stored, queries and probabilities
+// split into bf16 hi + lo for fp32-level accuracy); the block chunk uses FFMA on
+// the fp32 block keys.  A combine kernel merges the chunk partials (max, sum,
+// unnormalised output) in a fixed order.
 #include <math.h>
 
 #include "common.cuh"
 #include "glue.h"
+#include "internal.h"
 
 namespace df2 {
 
 namespace {
 
 constexpr int kHd = 128;
-constexpr int kQ = 32;        // queries per KV head group (4 heads x 8 positions)
+constexpr int kQ = 32;          // queries per KV head group (4 heads x 8 positions)
 constexpr int kKeys = kAttnChunk;
-constexpr int kPad = kHd + 1;
 constexpr int kPartStride = kHd + 2;
+constexpr int kLd = kHd + 8;    // bf16 row pitch (272 B): conflict-free fragment loads
+constexpr int kPLd = kKeys + 8;
 
-struct AttnSmem {
-  float q[kQ][kHd];
-  float kv[kKeys][kPad];
-  float p[kQ][kKeys];
+struct CtxSmem {
+  __nv_bfloat16 qh[kQ][kLd], ql[kQ][kLd];  // scaled queries, hi and lo parts
+  __nv_bfloat16 k[kKeys][kLd];
+  __nv_bfloat16 v[kKeys][kLd];
+  float s[kQ][kKeys + 4];                  // scores (log2 units), then probabilities
+  __nv_bfloat16 ph[kQ][kPLd], pl[kQ][kPLd];
 };
 
-__global__ void __launch_bounds__(256) attn_chunk_kernel(const AttnArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
-  const int nkv = a.n_kv_heads;
-  const int r = blockIdx.x / nkv, kvh = blockIdx.x % nkv;
-  const int chunk = blockIdx.y;
-  const int tid = threadIdx.x;
-  const int nn = min(max(a.n_new[r], 0), 8);
-  const int L = min(max(a.ctx_len[r], 0), a.kv_capacity - nn) + nn;  // same clamping as the cache append
-  const int lo0 = max(0, L - (a.window - 1));
-  const int n_ctx = L - lo0;
-  const int n_ctx_chunks = (n_ctx + kKeys - 1) / kKeys;
-  const bool block_chunk = chunk == a.n_chunks - 1;
-  float* out = a.part + ((static_cast<size_t>(r) * nkv + kvh) * a.n_chunks + chunk) * kQ * kPartStride;
-  int k_begin = 0, nk = 0;
-  if (block_chunk) {
-    nk = 8;
-  } else if (chunk < n_ctx_chunks) {
-    k_begin = lo0 + chunk * kKeys;
-    nk = min(kKeys, L - k_begin);
-  }
-  if (nk == 0) {
-    if (tid < kQ) {
-      out[tid * kPartStride + 0] = -INFINITY;
-      out[tid * kPartStride + 1] = 0.f;
-    }
-    return;
-  }
-  const int rep = a.n_q_heads / nkv;  // 4
+struct BlkSmem {
+  float q[kQ][kHd];
+  float kv[8][kHd + 1];
+  float p[kQ][8];
+};
+
+DF2_DEV uint32_t ld32(const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* smem_row) {
+  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(smem_row));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// ------------------------------------------------------------------ context chunk (tensor cores)
+DF2_DEV void ctx_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, int k_begin, int nk, int L,
+                       float* out) {
+  CtxSmem& sm = *reinterpret_cast<CtxSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int nkv = a.n_kv_heads, rep = a.n_q_heads / nkv;
   const float qscale = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;  // log2(e)/sqrt(hd)
-  // queries: qi = hr * 8 + i  ->  head kvh*rep + hr, block row r*8 + i
+  // queries -> bf16 hi/lo (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i)
   for (int e = tid; e < kQ * kHd; e += 256) {
     const int qi = e / kHd, d = e % kHd;
     const int hr = qi >> 3, i = qi & 7;
-    sm.q[qi][d] = a.q[((static_cast<size_t>(r) * 8 + i) * a.n_q_heads + kvh * rep + hr) * kHd + d] * qscale;
+    const float v = a.q[((static_cast<size_t>(r) * 8 + i) * a.n_q_heads + kvh * rep + hr) * kHd + d] * qscale;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    sm.qh[qi][d] = h;
+    sm.ql[qi][d] = __float2bfloat16_rn(v - __bfloat162float(h));
   }
-  // keys
-  if (block_chunk) {
-    for (int e = tid; e < 8 * kHd; e += 256) {
-      const int k = e / kHd, d = e % kHd;
-      sm.kv[k][d] = a.kb[((static_cast<size_t>(r) * 8 + k) * nkv + kvh) * kHd + d];
+  // keys and values of the chunk (rows >= nk are zero)
+  const uint16_t* kc = a.k_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
+  const uint16_t* vc = a.v_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
+  for (int e = tid; e < kKeys * (kHd / 8); e += 256) {
+    const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
+    uint4 kv4 = make_uint4(0, 0, 0, 0), vv4 = make_uint4(0, 0, 0, 0);
+    if (k < nk) {
+      kv4 = ld_stream(kc + static_cast<size_t>(k) * nkv * kHd + d8);
+      vv4 = ld_stream(vc + static_cast<size_t>(k) * nkv * kHd + d8);
     }
-  } else {
-    const uint16_t* kc = a.k_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
-    for (int e = tid; e < nk * (kHd / 8); e += 256) {
-      const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-      const uint4 v = ld_stream(kc + static_cast<size_t>(k) * nkv * kHd + d8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        sm.kv[k][d8 + 2 * j] = __uint_as_float(w[j] << 16);
-        sm.kv[k][d8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-    }
+    *reinterpret_cast<uint4*>(&sm.k[k][d8]) = kv4;
+    *reinterpret_cast<uint4*>(&sm.v[k][d8]) = vv4;
   }
   __syncthreads();
-  // scores: thread -> 4 queries (warp id) x 4 keys (lane + 32 j)
+  // S = Q K^T: 2 query tiles x 8 key tiles; warp w takes key tile w for both query tiles
   {
-    const int qg = tid >> 5, kg = tid & 31;
-    float s[4][4] = {};
-    for (int d = 0; d < kHd; ++d) {
-      float qv[4], kv[4];
+    const int nt = wid;
+    float c[2][4] = {};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[i] = sm.q[qg * 4 + i][d];
+    for (int ks = 0; ks < kHd / 16; ++ks) {
+      const uint32_t b0 = ld32(&sm.k[nt * 8 + g][ks * 16 + 2 * q]);
+      const uint32_t b1 = ld32(&sm.k[nt * 8 + g][ks * 16 + 8 + 2 * q]);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) kv[j] = sm.kv[kg + 32 * j][d];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qv[i], kv[j], s[i][j]);
+      for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = mt * 16 + g;
+        mma_bf16(c[mt], ld32(&sm.qh[r0][ks * 16 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 2 * q]),
+                 ld32(&sm.qh[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+        mma_bf16(c[mt], ld32(&sm.ql[r0][ks * 16 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 2 * q]),
+                 ld32(&sm.ql[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+      }
     }
+    const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int qi = qg * 4 + i;
-      const int pos_i = qi & 7;
+    for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int k = kg + 32 * j;
-        bool ok = k < nk;
-        if (!block_chunk) ok = ok && (k_begin + k >= L + pos_i - (a.window - 1));
-        sm.p[qi][k] = ok ? s[i][j] : -INFINITY;
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int qi = mt * 16 + g + 8 * h2;
+        const int pos_i = qi & 7;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = nt * 8 + 2 * q + e;
+          const bool ok = k < nk && k >= lim + pos_i;
+          sm.s[qi][k] = ok ? c[mt][2 * h2 + e] : -INFINITY;
+        }
       }
     }
   }
   __syncthreads();
-  // softmax statistics per query: warp w handles queries 4w..4w+3
-  {
-    const int w = tid >> 5, lane = tid & 31;
-    for (int i = 0; i < 4; ++i) {
-      const int qi = w * 4 + i;
-      float v[4];
-      float m = -INFINITY;
+  // softmax statistics per query: warp w handles queries 4w..4w+3, lane keys lane, lane+32
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[j] = sm.p[qi][lane + 32 * j];
-        m = fmaxf(m, v[j]);
-      }
-      m = warp_max(m);
-      float l = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float p = (m == -INFINITY) ? 0.f : exp2f(v[j] - m);
-        sm.p[qi][lane + 32 * j] = p;
-        l += p;
-      }
-      l = warp_sum(l);
-      if (lane == 0) {
-        out[qi * kPartStride + 0] = m;
-        out[qi * kPartStride + 1] = l;
-      }
+  for (int i = 0; i < 4; ++i) {
+    const int qi = wid * 4 + i;
+    const float v0 = sm.s[qi][lane], v1 = sm.s[qi][lane + 32];
+    const float m = warp_max(fmaxf(v0, v1));
+    const float p0 = (m == -INFINITY) ? 0.f : exp2f(v0 - m);
+    const float p1 = (m == -INFINITY) ? 0.f : exp2f(v1 - m);
+    const float l = warp_sum(p0 + p1);
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+    sm.ph[qi][lane] = h0;
+    sm.ph[qi][lane + 32] = h1;
+    sm.pl[qi][lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
+    sm.pl[qi][lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
+    if (lane == 0) {
+      out[qi * kPartStride + 0] = m;
+      out[qi * kPartStride + 1] = l;
     }
   }
   __syncthreads();
-  // values
-  if (block_chunk) {
-    for (int e = tid; e < 8 * kHd; e += 256) {
-      const int k = e / kHd, d = e % kHd;
-      sm.kv[k][d] = a.vb[((static_cast<size_t>(r) * 8 + k) * nkv + kvh) * kHd + d];
-    }
-  } else {
-    const uint16_t* vc = a.v_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
-    for (int e = tid; e < nk * (kHd / 8); e += 256) {
-      const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-      const uint4 v = ld_stream(vc + static_cast<size_t>(k) * nkv * kHd + d8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // O = P V: 2 query tiles x 16 dim tiles; warp w takes dim tiles 2w, 2w+1
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        sm.kv[k][d8 + 2 * j] = __uint_as_float(w[j] << 16);
-        sm.kv[k][d8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  for (int dn = 0; dn < 2; ++dn) {
+    const int nt = wid * 2 + dn;
+    float c[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kKeys / 16; ++ks) {
+      uint32_t b0, b1;
+      ldmatrix_x2_trans(b0, b1, &sm.v[ks * 16 + (lane & 15)][nt * 8]);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = mt * 16 + g;
+        mma_bf16(c[mt], ld32(&sm.ph[r0][ks * 16 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 2 * q]),
+                 ld32(&sm.ph[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+        mma_bf16(c[mt], ld32(&sm.pl[r0][ks * 16 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 2 * q]),
+                 ld32(&sm.pl[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
       }
     }
-  }
-  __syncthreads();
-  // out[q][d] = sum_k p[q][k] v[k][d]: thread -> 4 queries (warp id) x 4 dims (lane + 32 j)
-  {
-    const int qg = tid >> 5, dg = tid & 31;
-    float o[4][4] = {};
-    for (int k = 0; k < nk; ++k) {
-      float pv[4], vv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) pv[i] = sm.p[qg * 4 + i][k];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) vv[j] = sm.kv[k][dg + 32 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) o[i][j] = fmaf(pv[i], vv[j], o[i][j]);
+    for (int mt = 0; mt < 2; ++mt) {
+      const int q0 = mt * 16 + g, d0 = nt * 8 + 2 * q;
+      out[q0 * kPartStride + 2 + d0] = c[mt][0];
+      out[q0 * kPartStride + 2 + d0 + 1] = c[mt][1];
+      out[(q0 + 8) * kPartStride + 2 + d0] = c[mt][2];
+      out[(q0 + 8) * kPartStride + 2 + d0 + 1] = c[mt][3];
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) out[(qg * 4 + i) * kPartStride + 2 + dg + 32 * j] = o[i][j];
   }
 }
 
-// grid (R, nq), 128 threads: merge chunk partials of one query head for the 8 positions.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
-  __shared__ float sm[4 * 8];
-  const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+// ------------------------------------------------------------------ block chunk (8 fp32 keys, FFMA)
+DF2_DEV void blk_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, float* out) {
+  BlkSmem& sm = *reinterpret_cast<BlkSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nkv = a.n_kv_heads, rep = a.n_q_heads / nkv;
+  const float qscale = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;
+  for (int e = tid; e < kQ * kHd; e += 256) {
+    const int qi = e / kHd, d = e % kHd;
+    sm.q[qi][d] = a.q[((static_cast<size_t>(r) * 8 + (qi & 7)) * a.n_q_heads + kvh * rep + (qi >> 3)) * kHd + d] * qscale;
+  }
+  for (int e = tid; e < 8 * kHd; e += 256) {
+    const int k = e / kHd, d = e % kHd;
+    sm.kv[k][d] = a.kb[((static_cast<size_t>(r) * 8 + k) * nkv + kvh) * kHd + d];
+  }
+  __syncthreads();
+  {  // 32 queries x 8 keys = 256 dot products, one per thread
+    const int qi = tid >> 3, k = tid & 7;
+    float s = 0.f;
+    for (int d = 0; d < kHd; ++d) s = fmaf(sm.q[qi][d], sm.kv[k][d], s);
+    sm.p[qi][k] = s;
+  }
+  __syncthreads();
+  if (tid < kQ) {
+    float m = -INFINITY;
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, sm.p[tid][k]);
+    float l = 0.f;
+    for (int k = 0; k < 8; ++k) {
+      const float p = exp2f(sm.p[tid][k] - m);
+      sm.p[tid][k] = p;
+      l += p;
+    }
+    out[tid * kPartStride + 0] = m;
+    out[tid * kPartStride + 1] = l;
+  }
+  for (int e = tid; e < 8 * kHd; e += 256) {
+    const int k = e / kHd, d = e % kHd;
+    sm.kv[k][d] = a.vb[((static_cast<size_t>(r) * 8 + k) * nkv + kvh) * kHd + d];
+  }
+  __syncthreads();
+  for (int e = tid; e < kQ * kHd; e += 256) {
+    const int qi = e / kHd, d = e % kHd;
+    float o = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o = fmaf(sm.p[qi][k], sm.kv[k][d], o);
+    out[qi * kPartStride + 2 + d] = o;
+  }
+  (void)lane;
+  (void)wid;
+}
+
+__global__ void __launch_bounds__(256) attn_chunk_kernel(const AttnArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  pdl_begin();
+  const int nkv = a.n_kv_heads;
+  const int r = blockIdx.x / nkv, kvh = blockIdx.x % nkv;
+  const int chunk = blockIdx.y;
+  const int nn = min(max(a.n_new[r], 0), 8);
+  const int L = min(max(a.ctx_len[r], 0), a.kv_capacity - nn) + nn;  // same clamping as the cache append
+  const int lo0 = max(0, L - (a.window - 1));
+  const int n_ctx_chunks = (L - lo0 + kKeys - 1) / kKeys;
+  float* out = a.part + ((static_cast<size_t>(r) * nkv + kvh) * a.n_chunks + chunk) * kQ * kPartStride;
+  if (chunk == a.n_chunks - 1) {
+    blk_chunk(a, smem_raw, r, kvh, out);
+  } else if (chunk < n_ctx_chunks) {
+    const int k_begin = lo0 + chunk * kKeys;
+    ctx_chunk(a, smem_raw, r, kvh, k_begin, min(kKeys, L - k_begin), L, out);
+  } else if (threadIdx.x < kQ) {  // no keys in this chunk
+    out[threadIdx.x * kPartStride + 0] = -INFINITY;
+    out[threadIdx.x * kPartStride + 1] = 0.f;
+  }
+}
+
+// One warp per (request, query head, block position): merges the chunk partials in
+// chunk order; lane holds dims lane + 32 j.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  pdl_begin();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x;
+  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // head * 8 + position
+  if (item >= a.n_q_heads * 8) return;
+  const int h = item >> 3, i = item & 7;
   const int nkv = a.n_kv_heads;
   const int rep = a.n_q_heads / nkv;
   const int kvh = h / rep, hr = h % rep;
+  const int qi = hr * 8 + i;
   const float* base = a.part + (static_cast<size_t>(r) * nkv + kvh) * a.n_chunks * kQ * kPartStride;
-  float ov[8];
-  for (int i = 0; i < 8; ++i) {
-    const int qi = hr * 8 + i;
-    float M = -INFINITY;
-    for (int c = 0; c < a.n_chunks; ++c) {
+  // chunk statistics: lane c holds chunks c and c + 32 (n_chunks <= 64)
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int c = lane + 32 * u;
+    if (c < a.n_chunks) {
       const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride;
-      if (pc[1] > 0.f) M = fmaxf(M, pc[0]);
+      l[u] = pc[1];
+      if (l[u] > 0.f) m[u] = pc[0];
     }
-    float acc = 0.f, den = 0.f;
-    for (int c = 0; c < a.n_chunks; ++c) {
-      const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride;
-      if (pc[1] > 0.f) {
-        const float f = exp2f(pc[0] - M);
-        den += f * pc[1];
-        acc += f * pc[2 + d];
-      }
-    }
-    ov[i] = acc / den;
+  }
+  const float M = warp_max(fmaxf(m[0], m[1]));
+  float f[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) f[u] = (l[u] > 0.f) ? exp2f(m[u] - M) : 0.f;
+  const float den = warp_sum(f[0] * l[0] + f[1] * l[1]);
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < a.n_chunks; ++c) {
+    const float fc = __shfl_sync(0xffffffffu, f[c >> 5], c & 31);
+    if (fc == 0.f) continue;  // uniform across the warp
+    const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride + 2;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] += fc * pc[lane + 32 * j];
   }
   const int ld = a.n_q_heads * kHd;
-  const int c = h * kHd + d;
-  if (a.fmt == 0) {
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.act_o);
-    for (int i = 0; i < 8; ++i) o[(static_cast<size_t>(r) * 8 + i) * ld + c] = __float2bfloat16_rn(ov[i]);
-  } else {
-    __half* o = reinterpret_cast<__half*>(a.act_o);
-    const int lane = d & 31, wid = d >> 5;
-    float rs[8];
-    for (int i = 0; i < 8; ++i) {
-      const __half hv = __float2half_rn(ov[i]);
-      o[(static_cast<size_t>(r) * 8 + i) * ld + c] = hv;
-      rs[i] = warp_sum(__half2float(hv));
-    }
-    if (lane == 0)
-      for (int i = 0; i < 8; ++i) sm[wid * 8 + i] = rs[i];
-    __syncthreads();
-    if (d < 16) {
-      const int gq = d / 8, i = d % 8;
-      const int KG = ld / 64;
-      a.xsum_o[(static_cast<size_t>(r) * 8 + i) * KG + h * 2 + gq] = sm[(2 * gq) * 8 + i] + sm[(2 * gq + 1) * 8 + i];
+  for (int j = 0; j < 4; ++j) {
+    const size_t idx = (static_cast<size_t>(r) * 8 + i) * ld + h * kHd + lane + 32 * j;
+    const float v = o[j] / den;
+    if (a.fmt == 0) {
+      __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      p[idx] = hi;
+      if (a.act_o_lo) p[a.act_o_lo + idx] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    } else {
+      __half* p = reinterpret_cast<__half*>(a.act_o);
+      const __half hi = __float2half_rn(v);
+      p[idx] = hi;
+      if (a.act_o_lo) p[a.act_o_lo + idx] = __float2half_rn(v - __half2float(hi));
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnArgs& a, int n_req, cudaStream_t st) {
-  static bool attr_set = false;
-  const size_t smem = sizeof(AttnSmem);
+cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  static bool attr_set = false;  // set once, outside any later stream capture
+  const size_t smem = sizeof(CtxSmem) > sizeof(BlkSmem) ? sizeof(CtxSmem) : sizeof(BlkSmem);
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  attn_chunk_kernel<<<dim3(n_req * a.n_kv_heads, a.n_chunks), 256, smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_ex(attn_chunk_kernel, dim3(n_req * a.n_kv_heads, a.n_chunks), dim3(256), smem, st, pdl, a);
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(n_req, a.n_q_heads), 128, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_ex(attn_combine_kernel, dim3(n_req, (a.n_q_heads * 8 + 7) / 8), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace df2

@@ -55,6 +55,20 @@ DF2_DEV uint32_t codes_to_half2(uint32_t w_biased, uint32_t sel) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream has
+// completed (its writes visible), and let the next kernel start being scheduled.
+// Both are no-ops for a kernel launched without the attribute.
+DF2_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DF2_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DF2_DEV void pdl_begin() {
+  pdl_wait();
+  pdl_trigger();
+}
+
+// 1/rms of one row from nch per-chunk sums of squares, computed by a whole warp
+// (fixed lane order and shuffle tree: bit-reproducible).  All lanes get the value.
+DF2_DEV float warp_inv_rms(const float* ss, int row, int nch, int H, float eps);
+
 DF2_DEV float bf16_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 DF2_DEV float warp_sum(float v) {
@@ -67,6 +81,13 @@ DF2_DEV float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+DF2_DEV float warp_inv_rms(const float* ss, int row, int nch, int H, float eps) {
+  float s = 0.f;
+  for (int j = threadIdx.x & 31; j < nch; j += 32) s += ss[static_cast<size_t>(row) * nch + j];
+  s = warp_sum(s);
+  return rsqrtf(s / static_cast<float>(H) + eps);
 }
 
 // Block-wide sum; `red` holds >= 32 floats of shared memory.  All threads get the sum.

@@ -1,4 +1,4 @@
-// Argument blocks of the element-wise stages (glue.cu) and the attention,
+// Argument blocks of the element-wise stages (glue.cu) and of the attention,
 // LM-head, selector and verify kernels.
 #pragma once
 
@@ -7,6 +7,9 @@
 
 namespace df2 {
 
+// Activation buffers hold a high plane and, at element offset *_lo, a low-order
+// plane (value = hi + lo); bf16 for BF16 weights (fmt 0), fp16 for Q8 (fmt 1).
+
 struct StartArgs {
   const int32_t* anchor_ids;
   const int32_t* n_new;
@@ -14,61 +17,40 @@ struct StartArgs {
   const uint16_t* norm_w;  // input_norm of layer 0
   const float* taps;       // [R][8][n_taps*H]
   float* x;                // residual stream [N][H]
-  void* act_a;             // GEMV input of layer 0's delta projection [N][H]
-  float* xsum_a;
-  float* ss_x;             // [N][nch]
+  void* act_a;             // x * w: input of layer 0's delta projection [N][H]
+  size_t act_a_lo;
+  float* ss_x;             // [N][H/128]
   void* act_taps;          // [N][n_taps*H]
-  float* xsum_taps;
+  size_t act_taps_lo;
   int H, n_taps, mask_id, nch, fmt, V;
 };
 
 struct FcFinishArgs {
-  const float* part;       // [splits][n_rows][H]
+  const float* y;          // taps projection [N][H]
   const uint16_t* norm_w;  // hidden_norm
-  void* act;               // act_qkv (context rows start at act_row0)
-  float* xsum;
-  float* ss;               // [N][nch]  sums of squares of the projected taps
-  int H, n_rows, splits, act_row0, nch, fmt;
+  void* act;               // QKV input; context rows start at act_row0
+  size_t act_lo;
+  float* ss;               // [N][H/128] sums of squares of y
+  int H, act_row0, nch, fmt;
 };
 
 struct ConvInArgs {
-  const float* part;       // delta partials [splits][n_rows][4G]
-  const float* ss;         // [N][nch] of x
+  const float* dproj;      // delta projection of x * w, [N][4G] (not yet scaled by 1/rms)
+  const float* ss;         // [N][nch] sums of squares of x
   const float* x;          // residual stream
   const uint16_t* norm_w;
   const uint16_t* base;    // [4][H]
-  float* delta;            // out: [N][4G] (scaled by 1/rms)
-  void* act;               // out: conv-in'd activations [N][H]
-  float* xsum;
-  int H, n_rows, splits, nch, fmt;
+  float* delta;            // out: [N][4G] scaled by 1/rms
+  void* act;               // out: conv-in'd sublayer input [N][H]
+  size_t act_lo;
+  int H, nch, fmt;
   float eps;
 };
 
-struct ConvOutArgs {
-  const float* part;       // sublayer output partials [splits][n_rows][H]
-  const float* delta;      // [N][4G]
-  const uint16_t* base;    // [4][H]
-  const uint16_t* norm_w;  // norm of the next sublayer (x * w is emitted)
-  float* x;                // residual stream, updated in place
-  void* act;
-  float* xsum;
-  float* ss;               // [N][nch] of the updated x
-  uint16_t* act_bf16;      // optional second copy of x * w in bf16 (LM-head input), or null
-  int H, n_rows, splits, nch, fmt;
-};
-
-struct SwigluArgs {
-  const float* part_g;
-  const float* part_u;     // [splits][n_rows][F]
-  void* act;               // [N][F]
-  float* xsum;
-  int F, n_rows, splits, fmt;
-};
-
 struct QkvFinishArgs {
-  const float* part_q;     // [splits][n_rows][nq*128]
-  const float* part_k;     // [splits][2*n_rows][nkv*128]: block rows, then context rows
-  const float* part_v;
+  const float* q_out;      // [N][nq*128]
+  const float* k_out;      // [2N][nkv*128]: block rows, then context rows
+  const float* v_out;
   const float* ss_c;       // [N][nch] of the projected taps
   const uint16_t* q_norm;
   const uint16_t* k_norm;
@@ -80,16 +62,14 @@ struct QkvFinishArgs {
   float* vb;
   uint16_t* k_cache;       // this layer's slice: [max_req][cap][nkv][128]
   uint16_t* v_cache;
-  int n_q_heads, n_kv_heads, n_rows, splits, kv_capacity, H, nch;
+  int n_q_heads, n_kv_heads, n_rows, kv_capacity, H, nch;
   float eps;
 };
 
-cudaError_t launch_start(const StartArgs& a, int n_req, cudaStream_t st);
-cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, cudaStream_t st);
-cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, cudaStream_t st);
-cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, cudaStream_t st);
-cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, cudaStream_t st);
-cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st);
+cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, bool pdl, cudaStream_t st);
+cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st);
+cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
@@ -102,35 +82,36 @@ struct AttnArgs {
   const int32_t* n_new;
   float* part;             // [R][nkv][n_chunks][32][130]
   void* act_o;             // [N][nq*128]
-  float* xsum_o;
+  size_t act_o_lo;
   int n_q_heads, n_kv_heads, kv_capacity, window, n_chunks, fmt;
 };
-constexpr int kAttnChunk = 128;
-cudaError_t launch_attention(const AttnArgs& a, int n_req, cudaStream_t st);
+constexpr int kAttnChunk = 64;
+cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- LM head + top-k
 struct LmHeadArgs {
   const uint16_t* w;       // bf16 [V][H]
   const uint16_t* x;       // bf16 [N][H]: x * final_norm_w
-  const float* ss;         // [N][nch] sums of squares of x
+  size_t x_lo;             // element offset of the low-order plane of x (0: none)
+  const float* ss;         // [N][nch] sums of squares of x, or null (x already normalised)
   float* logits_out;       // [R][7][V] or null
   unsigned long long* part_keys;  // [N][n_cta][16]
   int V, H, n_rows, nch, n_cta;
   float eps;
 };
-cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t st);
+cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st);
 
 struct TopkMergeArgs {
   const unsigned long long* part_keys;  // [N][n_cta][16]
-  const float* part_sel;   // selector projection partials [splits][N][rank]
+  const float* sel;        // selector projection [N][rank], or null
   const float* ss;
   int32_t* cand_ids;       // [R][7][16]
   float* cand_logits;
   float* gate;             // [R][7][rank]
-  int n_rows, n_cta, rank, sel_splits, nch, H;
+  int n_rows, n_cta, rank, nch, H;
   float eps;
 };
-cudaError_t launch_topk_merge(const TopkMergeArgs& a, cudaStream_t st);
+cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- selector
 struct SelectArgs {
@@ -153,7 +134,7 @@ struct SelectArgs {
   int32_t* status;
   int rank, fmt, V;
 };
-cudaError_t launch_select(const SelectArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- verify
 constexpr int kVerifyChunk = 4096;
@@ -178,6 +159,6 @@ struct VerifyArgs {
   int32_t* status;
   int V, n_chunks;
 };
-cudaError_t launch_verify(const VerifyArgs& a, int n_req, cudaStream_t st);
+cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 }  // namespace df2

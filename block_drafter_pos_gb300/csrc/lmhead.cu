@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "glue.h"
+#include "internal.h"
 
 namespace df2 {
 
@@ -41,16 +42,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) lmhead_topk_kernel(const LmHea
   const int t0 = static_cast<int>((static_cast<long long>(tiles_total) * blockIdx.x) / gridDim.x);
   const int t1 = static_cast<int>((static_cast<long long>(tiles_total) * (blockIdx.x + 1)) / gridDim.x);
   for (int e = threadIdx.x; e < NT * 8 * kTopK; e += blockDim.x) run[e] = 0ull;
-  if (threadIdx.x < n_rows) {
-    float rs = 1.f;  // no statistics: the hidden state is already normalised
-    if (a.ss != nullptr) {
-      float s = 0.f;
-      for (int j = 0; j < a.nch; ++j) s += a.ss[threadIdx.x * a.nch + j];
-      rs = rsqrtf(s / static_cast<float>(a.H) + a.eps);
-    }
-    rscale[threadIdx.x] = rs;
-  }
-  __syncthreads();
+  pdl_trigger();
+  bool waited = false;
   for (int tb = t0; tb < t1; tb += kWarps) {
     const int tile = tb + wid;
     // ---- GEMV: one 16-row tile per warp
@@ -67,6 +60,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) lmhead_topk_kernel(const LmHea
       for (int j = 0; j < 4; ++j) {
         ra[j] = ld_stream(w0 + 32 * j);
         rb[j] = ld_stream(w1 + 32 * j);
+      }
+      if (!waited) {  // weights first; the hidden state comes from the previous kernel
+        pdl_wait();
+        waited = true;
       }
       for (int k = 0; k < a.H; k += 128) {
         uint4 ca[4], cb[4];
@@ -91,6 +88,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) lmhead_topk_kernel(const LmHea
               const uint4 x = ld_cached(xt + 32 * j);
               mma_bf16(acc[t], ca[j].x, cb[j].x, ca[j].y, cb[j].y, x.x, x.y);
               mma_bf16(acc[t], ca[j].z, cb[j].z, ca[j].w, cb[j].w, x.z, x.w);
+              if (a.x_lo) {  // low-order part of the hidden state: x = hi + lo
+                const uint4 y = ld_cached(xt + a.x_lo + 32 * j);
+                mma_bf16(acc[t], ca[j].x, cb[j].x, ca[j].y, cb[j].y, y.x, y.y);
+                mma_bf16(acc[t], ca[j].z, cb[j].z, ca[j].w, cb[j].w, y.z, y.w);
+              }
             }
           }
         }
@@ -100,12 +102,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1) lmhead_topk_kernel(const LmHea
       for (int t = 0; t < NT; ++t) {
         if (t >= nt) break;
         const int n0 = t * 8 + 2 * q;
-        logit[(n0)*kSub + lr] = acc[t][0] * rscale[n0];
-        logit[(n0 + 1) * kSub + lr] = acc[t][1] * rscale[n0 + 1];
-        logit[(n0)*kSub + lr + 8] = acc[t][2] * rscale[n0];
-        logit[(n0 + 1) * kSub + lr + 8] = acc[t][3] * rscale[n0 + 1];
+        logit[(n0)*kSub + lr] = acc[t][0];
+        logit[(n0 + 1) * kSub + lr] = acc[t][1];
+        logit[(n0)*kSub + lr + 8] = acc[t][2];
+        logit[(n0 + 1) * kSub + lr + 8] = acc[t][3];
       }
     }
+    if (!waited) {  // warps without a tile in this sub-block
+      pdl_wait();
+      waited = true;
+    }
+    if (tb == t0) {  // final-norm scale of each row (1 when the input is already normalised)
+      for (int n = wid; n < n_rows; n += kWarps) {
+        const float rs = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
+        if (lane == 0) rscale[n] = rs;
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < n_rows * kSub; e += blockDim.x) logit[e] *= rscale[e / kSub];
     __syncthreads();
     const int v0 = tb * 16;
     const int nv = min(kSub, (t1 - tb) * 16);
@@ -168,14 +182,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) lmhead_topk_kernel(const LmHea
 __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) {
   __shared__ unsigned long long wbest[8];
   __shared__ float rs;
+  pdl_begin();
   const int n = blockIdx.x;
   const int pos = n & 7, rq = n >> 3;
   if (pos == 0) return;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (threadIdx.x == 0 && a.ss != nullptr) {
-    float s = 0.f;
-    for (int j = 0; j < a.nch; ++j) s += a.ss[n * a.nch + j];
-    rs = rsqrtf(s / static_cast<float>(a.H) + a.eps);
+  if (wid == 0) {
+    const float v = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
+    if (lane == 0) rs = v;
   }
   const int total = a.n_cta * kTopK;
   const unsigned long long* src = a.part_keys + static_cast<size_t>(n) * total;
@@ -202,41 +216,36 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
     }
   }
   __syncthreads();
-  if (a.part_sel == nullptr) return;
-  const size_t plane = static_cast<size_t>(a.n_rows) * a.rank;
-  for (int j = threadIdx.x; j < a.rank; j += blockDim.x) {
-    float s = 0.f;
-    for (int sp = 0; sp < a.sel_splits; ++sp) s += a.part_sel[sp * plane + static_cast<size_t>(n) * a.rank + j];
-    a.gate[(static_cast<size_t>(rq) * 7 + pos - 1) * a.rank + j] = s * rs;
-  }
+  if (a.sel == nullptr) return;
+  for (int j = threadIdx.x; j < a.rank; j += blockDim.x)
+    a.gate[(static_cast<size_t>(rq) * 7 + pos - 1) * a.rank + j] = a.sel[static_cast<size_t>(n) * a.rank + j] * rs;
 }
 
 template <int NT>
-cudaError_t launch_nt(const LmHeadArgs& a, cudaStream_t st) {
+cudaError_t launch_nt(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(NT) * 8 * kSub * sizeof(float) + static_cast<size_t>(NT) * 8 * kTopK * 8;
   static bool attr_set = false;  // set once, outside any later stream capture
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  lmhead_topk_kernel<NT><<<a.n_cta, kWarps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_ex(lmhead_topk_kernel<NT>, dim3(a.n_cta), dim3(kWarps * 32), smem, st, pdl, a);
 }
 
 }  // namespace
 
-cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t st) {
+cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
   const int nt = a.n_rows / 8;
-  if (nt <= 1) return launch_nt<1>(a, st);
-  if (nt <= 2) return launch_nt<2>(a, st);
-  if (nt <= 4) return launch_nt<4>(a, st);
+  if (nt <= 1) return launch_nt<1>(a, pdl, st);
+  if (nt <= 2) return launch_nt<2>(a, pdl, st);
+  if (nt <= 4) return launch_nt<4>(a, pdl, st);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_topk_merge(const TopkMergeArgs& a, cudaStream_t st) {
-  topk_merge_kernel<<<a.n_rows, 256, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st) {
+  return launch_ex(topk_merge_kernel, dim3(a.n_rows), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace df2

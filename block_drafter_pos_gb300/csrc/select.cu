@@ -13,6 +13,7 @@
 
 #include "common.cuh"
 #include "glue.h"
+#include "internal.h"
 #include "philox.cuh"
 
 namespace df2 {
@@ -21,75 +22,115 @@ namespace {
 
 constexpr int kP = 7, kK = 16, kRank = 256;
 
-// Loads one codebook row (bf16 or Q8/g64) as fp32 into dst[kRank].
-__device__ void load_cb_row(float* dst, const void* cb, const uint16_t* sc, const uint16_t* bi, int fmt, int id,
-                            int lane) {
-  for (int r = lane; r < kRank; r += 32) {
-    float v;
-    if (fmt == 0) {
-      v = bf16_to_f32(reinterpret_cast<const uint16_t*>(cb)[static_cast<size_t>(id) * kRank + r]);
-    } else {
-      const int8_t c = reinterpret_cast<const int8_t*>(cb)[static_cast<size_t>(id) * kRank + r];
-      const int gi = static_cast<size_t>(id) * (kRank / 64) + r / 64;
-      v = bf16_to_f32(sc[gi]) * static_cast<float>(c) + bf16_to_f32(bi[gi]);
-    }
-    dst[r] = v;
-  }
+constexpr int kRowsA = 1 + (kP - 1) * kK;  // anchor + candidates of positions 1..6
+constexpr int kRowsB = kP * kK;            // candidates of positions 1..7
+constexpr int kRows = kRowsA + kRowsB;
+
+// Codebook rows staged in shared memory in their stored format: bf16 (256 x 2 B) or
+// Q8 codes (256 B) plus 4 groups of (scale, bias).
+struct SelSmem {
+  uint16_t bf[kRows][kRank];   // BF16 rows (unused for Q8)
+  int8_t q8[kRows][kRank];     // Q8 codes (unused for BF16)
+  uint16_t sb[kRows][8];       // Q8: scale[4], bias[4]
+  float gate[kP][kRank];
+  float lat[kP][kK][kK];       // scores [position][pred][cand]
+  int cids[kP][kK];
+  float cl[kP][kK];
+  int bad;
+};
+
+// Row `row` of the staged codebook rows, element r, as fp32.
+DF2_DEV float cb_val(const SelSmem& sm, int fmt, int row, int r) {
+  if (fmt == 0) return bf16_to_f32(sm.bf[row][r]);
+  const int g = r >> 6;
+  return bf16_to_f32(sm.sb[row][g]) * static_cast<float>(sm.q8[row][r]) + bf16_to_f32(sm.sb[row][4 + g]);
 }
 
 __global__ void __launch_bounds__(256) select_kernel(const SelectArgs a) {
-  __shared__ float apred[kK][kRank];   // predecessor rows of A (16 KB)
-  __shared__ float bg[kK][kRank];      // gate_i * B[c] rows (16 KB)
-  __shared__ float lat[kP][kK][kK];    // scores [position][pred][cand]
-  __shared__ int cids[kP][kK];
-  __shared__ float cl[kP][kK];
-  __shared__ int bad;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  pdl_begin();
   const int r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) bad = 0;
+  if (tid == 0) sm.bad = 0;
   for (int e = tid; e < kP * kK; e += 256) {
-    cids[e / kK][e % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + e], 0), a.V - 1);
+    sm.cids[e / kK][e % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + e], 0), a.V - 1);
     const float v = a.cand_logits[static_cast<size_t>(r) * kP * kK + e];
-    cl[e / kK][e % kK] = v;
-    if (!isfinite(v)) atomicOr(&bad, 1);
+    sm.cl[e / kK][e % kK] = v;
+    if (!isfinite(v)) atomicOr(&sm.bad, 1);
   }
+  for (int e = tid; e < kP * kRank; e += 256) sm.gate[e / kRank][e % kRank] = a.gate[static_cast<size_t>(r) * kP * kRank + e];
   __syncthreads();
   const int anchor = min(max(a.anchor_ids[r], 0), a.V - 1);
-  for (int i = 0; i < kP; ++i) {
-    // predecessor rows: the anchor for position 1, else the 16 candidates of position i-1
-    for (int p = wid; p < kK; p += 8) {
-      const int id = (i == 0) ? anchor : cids[i - 1][p];
-      if (i == 0 && p > 0) continue;
-      load_cb_row(apred[p], a.cb_a, a.cb_a_scale, a.cb_a_bias, a.fmt, id, lane);
+  // stage every needed codebook row at once (one round trip): row k < kRowsA is the
+  // predecessor row A[id], k >= kRowsA the successor row B[id]
+  const int chunks = a.fmt == 0 ? kRank * 2 / 16 : kRank / 16;  // 16-byte pieces per row
+  for (int e = tid; e < kRows * chunks; e += 256) {
+    const int k = e / chunks, c = e % chunks;
+    int id;
+    const void* cb;
+    if (k < kRowsA) {
+      id = k == 0 ? anchor : sm.cids[(k - 1) / kK][(k - 1) % kK];
+      cb = a.cb_a;
+    } else {
+      id = sm.cids[(k - kRowsA) / kK][(k - kRowsA) % kK];
+      cb = a.cb_b;
     }
-    const float* gi = a.gate + (static_cast<size_t>(r) * kP + i) * kRank;
-    for (int c = wid; c < kK; c += 8) {
-      load_cb_row(bg[c], a.cb_b, a.cb_b_scale, a.cb_b_bias, a.fmt, cids[i][c], lane);
-      __syncwarp();
-      for (int k = lane; k < kRank; k += 32) bg[c][k] *= gi[k];
-    }
-    __syncthreads();
-    const int npred = (i == 0) ? 1 : kK;
-    for (int pc = wid; pc < npred * kK; pc += 8) {
-      const int p = pc / kK, c = pc % kK;
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < kRank / 32; ++k) s = fmaf(apred[p][lane + 32 * k], bg[c][lane + 32 * k], s);
-      s = warp_sum(s) + cl[i][c];
-      if (lane == 0) {
-        if (!isfinite(s)) atomicOr(&bad, 1);
-        if (i == 0) {
-          for (int pp = 0; pp < kK; ++pp) lat[0][pp][c] = s;
-        } else {
-          lat[i][p][c] = s;
-        }
+    if (a.fmt == 0) {
+      *reinterpret_cast<uint4*>(&sm.bf[k][c * 8]) =
+          ld_cached(reinterpret_cast<const uint16_t*>(cb) + static_cast<size_t>(id) * kRank + c * 8);
+    } else {
+      *reinterpret_cast<uint4*>(&sm.q8[k][c * 16]) =
+          ld_cached(reinterpret_cast<const int8_t*>(cb) + static_cast<size_t>(id) * kRank + c * 16);
+      if (c < 4) {
+        const uint16_t* sc = k < kRowsA ? a.cb_a_scale : a.cb_b_scale;
+        const uint16_t* bi = k < kRowsA ? a.cb_a_bias : a.cb_b_bias;
+        sm.sb[k][c] = sc[static_cast<size_t>(id) * 4 + c];
+        sm.sb[k][4 + c] = bi[static_cast<size_t>(id) * 4 + c];
       }
     }
-    __syncthreads();
   }
+  __syncthreads();
+  // lattice: one warp per (position, pred, cand); lanes split the rank (fixed tree)
+  const int n_pairs = kK + (kP - 1) * kK * kK;
+  for (int pc = wid; pc < n_pairs; pc += 8) {
+    int i, p, c;
+    if (pc < kK) {
+      i = 0;
+      p = 0;
+      c = pc;
+    } else {
+      const int e = pc - kK;
+      i = 1 + e / (kK * kK);
+      p = (e / kK) % kK;
+      c = e % kK;
+    }
+    const int ra = i == 0 ? 0 : 1 + (i - 1) * kK + p;
+    const int rb = kRowsA + i * kK + c;
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRank / 32; ++k) {
+      const int rr = lane + 32 * k;
+      s = fmaf(cb_val(sm, a.fmt, ra, rr), sm.gate[i][rr] * cb_val(sm, a.fmt, rb, rr), s);
+    }
+    s = warp_sum(s) + sm.cl[i][c];
+    if (lane == 0) {
+      if (!isfinite(s)) atomicOr(&sm.bad, 1);
+      if (i == 0) {
+        for (int pp = 0; pp < kK; ++pp) sm.lat[0][pp][c] = s;
+      } else {
+        sm.lat[i][p][c] = s;
+      }
+    }
+  }
+  __syncthreads();
   if (a.scores_out) {
-    for (int e = tid; e < kP * kK * kK; e += 256) a.scores_out[static_cast<size_t>(r) * kP * kK * kK + e] = (&lat[0][0][0])[e];
+    for (int e = tid; e < kP * kK * kK; e += 256)
+      a.scores_out[static_cast<size_t>(r) * kP * kK * kK + e] = (&sm.lat[0][0][0])[e];
   }
+  const int bad = sm.bad;
+  auto& lat = sm.lat;
+  auto& cids = sm.cids;
   if (tid != 0) return;
   const float T = a.temperature[r];
   int32_t* path = a.path + static_cast<size_t>(r) * kP;
@@ -141,9 +182,15 @@ __global__ void __launch_bounds__(256) select_kernel(const SelectArgs a) {
 
 }  // namespace
 
-cudaError_t launch_select(const SelectArgs& a, int n_req, cudaStream_t st) {
-  select_kernel<<<n_req, 256, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  static bool attr_set = false;  // set once, outside any later stream capture
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(SelSmem)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(select_kernel, dim3(n_req), dim3(256), sizeof(SelSmem), st, pdl, a);
 }
 
 }  // namespace df2

@@ -13,6 +13,7 @@
 
 #include "common.cuh"
 #include "glue.h"
+#include "internal.h"
 #include "philox.cuh"
 
 namespace df2 {
@@ -24,6 +25,7 @@ constexpr int kB = 8, kP = 7, kK = 16;
 __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   __shared__ float sm_m[8], sm_s[8];
   __shared__ int sm_a[8], sm_f[8];
+  pdl_begin();
   const int rj = blockIdx.x;  // r * 8 + j
   const int r = rj >> 3;
   const int chunk = blockIdx.y;
@@ -210,10 +212,11 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
   extern __shared__ float csum[];  // [n_chunks]
   __shared__ float red[8];
   __shared__ float rowM[kB], rowS[kB];
-  __shared__ int rowA[kB], rowBad;
+  __shared__ int rowA[kB], rowF[kB], rowBad;
   __shared__ int cid[kK];
   __shared__ float qv[kK];
   __shared__ int sh_decision;
+  pdl_begin();
   const int r = blockIdx.x;
   int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
   if (a.status[r] != 0) {
@@ -226,34 +229,45 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
   }
   const float T = a.temperature[r];
   const VerifyStat* st = a.stats + static_cast<size_t>(r) * kB * a.n_chunks;
-  if (threadIdx.x < kB) {
-    const int j = threadIdx.x;
+  {
+    // warp j folds the chunk statistics of row j (lane-strided, fixed shuffle tree)
+    const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const VerifyStat* sj = st + static_cast<size_t>(j) * a.n_chunks;
     float M = -INFINITY;
     int A = 0x7FFFFFFF, F = 0;
-    for (int c = 0; c < a.n_chunks; ++c) {
+    for (int c = lane; c < a.n_chunks; c += 32) {
       F |= sj[c].flags;
       if (sj[c].m > M || (sj[c].m == M && sj[c].arg < A)) {
         M = sj[c].m;
         A = sj[c].arg;
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, M, o);
+      const int oa = __shfl_xor_sync(0xffffffffu, A, o);
+      if (om > M || (om == M && oa < A)) {
+        M = om;
+        A = oa;
+      }
+      F |= __shfl_xor_sync(0xffffffffu, F, o);
+    }
     float S = 0.f;
     if (T > 0.f && M > -INFINITY && M < INFINITY)
-      for (int c = 0; c < a.n_chunks; ++c)
+      for (int c = lane; c < a.n_chunks; c += 32)
         if (sj[c].m > -INFINITY) S += sj[c].s * expf((sj[c].m - M) / T);
-    rowM[j] = M;
-    rowS[j] = S;
-    rowA[j] = A;
+    S = warp_sum(S);
+    if (lane == 0) {
+      rowM[j] = M;
+      rowS[j] = S;
+      rowA[j] = A;
+      rowF[j] = F != 0 || !(M > -INFINITY) || !(M < INFINITY);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int bad = 0;
-    for (int j = 0; j < kB; ++j) {
-      const VerifyStat* sj = st + static_cast<size_t>(j) * a.n_chunks;
-      for (int c = 0; c < a.n_chunks; ++c) bad |= sj[c].flags;
-      if (!(rowM[j] > -INFINITY) || !(rowM[j] < INFINITY)) bad = 1;
-    }
+    for (int j = 0; j < kB; ++j) bad |= rowF[j];
     rowBad = bad;
   }
   __syncthreads();
@@ -329,12 +343,10 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
 
 }  // namespace
 
-cudaError_t launch_verify(const VerifyArgs& a, int n_req, cudaStream_t st) {
-  verify_stats_kernel<<<dim3(n_req * kB, a.n_chunks), 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  cudaError_t e = launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), 0, st, pdl, a);
   if (e != cudaSuccess) return e;
-  verify_chain_kernel<<<n_req, 256, a.n_chunks * sizeof(float), st>>>(a);
-  return cudaGetLastError();
+  return launch_ex(verify_chain_kernel, dim3(n_req), dim3(256), a.n_chunks * sizeof(float), st, pdl, a);
 }
 
 }  // namespace df2

@@ -101,6 +101,26 @@ def test_draft_block_multi_request_ragged():
         assert rel_l2(logits[r], tr["logits"]) < 2e-2, r
 
 
+def test_draft_block_gqa_two_layers_full_window():
+    """2 layers, 8 query / 2 KV heads (GQA group mapping), the 2048-key window at its
+    full size (one request past it), 2 requests."""
+    g = dataclasses.replace(wk.TOY, hidden=1024, n_layers=2, n_q_heads=8, n_kv_heads=2, ffn=2048, vocab=16384)
+    wl = wk.Workload("mid_r2", g, "bf16", 2, [300, 2600], [0.0, 0.0], [0.5] * 2, seed=12)
+    W = wk.make_weights(g, "bf16", wl.seed)
+    inp = wk.make_request_inputs(wl)
+    kc, vc = new_caches(wl, inp)
+    step = GpuStep(wl, W)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    step.draft(t(inp["anchors"]), t(inp["ctx_len"]), t(inp["n_new"]), t(inp["taps"]), i16(kc), i16(vc))
+    torch.cuda.synchronize()
+    logits = step.logits.cpu().numpy()
+    gate = step.gate.cpu().numpy()
+    for r in range(2):
+        tr = oracle_draft(wl, W, inp, kc, vc, r)
+        assert rel_l2(logits[r], tr["logits"]) < 1e-3, r
+        assert rel_l2(gate[r], tr["gate"]) < 1e-3, r
+
+
 def _select_case(V, R, seed, integer, temps):
     si = wk.make_selector_inputs(V, R, seed, integer=integer)
     g = dataclasses.replace(wk.TOY, vocab=V)

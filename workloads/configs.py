@@ -129,5 +129,13 @@ WORKLOADS = {
 }
 
 
+# Profiling-only workload (not one of the benchmark configurations): one layer of the
+# full width with a small vocabulary, so a profiler capture holds about 1 GB.
+WORKLOADS[6] = Workload("profile_one_full_layer", Geometry("full_width_1layer", hidden=5120, n_layers=1, n_q_heads=32,
+                                                            n_kv_heads=8, head_dim=128, ffn=17408, vocab=16384),
+                        "bf16", 1, [1024], [0.0], [1.0], seed=6,
+                        description="profiling: one full-width layer, vocab 16384, 1 request, ctx 1024")
+
+
 def workload(i: int) -> Workload:
     return WORKLOADS[i]
