@@ -3,15 +3,17 @@
 // No allocation after dflash2_create; no host synchronisation in the step calls.
 //
 // Per layer the draft block launches: delta projection, conv-in, QKV projection,
-// q/k norm + RoPE + cache append, block attention (+ combine), output projection
-// (epilogue: conv-out + residual + post-norm input), delta projection, conv-in,
-// gate/up projection (epilogue: SwiGLU), down projection (epilogue: conv-out +
-// residual + next norm input).  Every kernel is launched with programmatic
+// q/k norm + RoPE + cache append, block attention (+ combine), output projection,
+// conv-out + residual, delta projection, conv-in, gate/up projection, SwiGLU,
+// down projection, conv-out + residual.  Each projection writes one fp32 plane per
+// K split; the kernel after it adds the planes in split order (deterministic, no
+// atomics, no inter-CTA signalling).  Every kernel is launched with programmatic
 // dependent launch so its prologue overlaps the previous kernel's tail.
 #include <math.h>
 #include <string.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <new>
 
 #include "../../include/dflash2.h"
@@ -26,14 +28,15 @@ struct dflash2_handle {
   int max_req, kv_cap, num_sms, fmt;
   bool pdl;
   int H, G, F, V, nq, nkv, qd, kvd, KT;
-  int nch128, nch16;  // chunks of the two kinds of sums-of-squares partials
+  int nch128;  // 128-channel chunks of the sums-of-squares partials
   int n_attn_chunks, n_verify_chunks, lm_ctas;
+  // K splits of each projection (fixed at create from the grid size)
+  int s_fc, s_delta, s_qkv, s_o, s_gu, s_down, s_sel;
   // scratch
   char* arena;
   size_t arena_bytes;
-  float *x, *ss128, *ss16, *ss_c, *dproj, *delta_a, *delta_m, *fc_out, *q_out, *k_out, *v_out, *sel_out;
-  float *q, *kb, *vb, *attn_part, *part;
-  int* counters;
+  float *x, *ss128, *ss_c, *dproj, *delta_a, *delta_m, *fc_out, *q_out, *k_out, *v_out, *sel_out;
+  float *q, *kb, *vb, *attn_part, *ypart, *gpart, *upart;
   void *act_a, *act_qkv, *act_taps, *act_o, *act_h;
   uint16_t* act_fin;
   // element offsets of the low-order activation planes (x = hi + lo)
@@ -55,7 +58,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
     if (e_ != cudaSuccess) return DFLASH2_E_CUDA; \
   } while (0)
 
-GemvSeg seg_base(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, int n_tiles, int rows, int K) {
+// One projection segment: out[s] = W[:, split s] X[:, split s]^T for the
+// 8 * n_tiles activation rows starting at x.
+GemvSeg seg(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, int n_tiles, int M, int K, int splits,
+            float* out) {
   GemvSeg s;
   memset(&s, 0, sizeof(s));
   s.w = m.w;
@@ -64,17 +70,11 @@ GemvSeg seg_base(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, in
   s.x = x;
   s.xlo_off = xlo;
   s.ldx = ldx;
+  s.M = M;
   s.K = K;
   s.n_tiles = n_tiles;
-  s.tiles = rows / 16;
-  s.epi = kEpiStore;
-  return s;
-}
-
-GemvSeg seg_store(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, int n_tiles, int M, int K, float* out) {
-  GemvSeg s = seg_base(m, x, xlo, ldx, n_tiles, M, K);
+  s.splits = splits;
   s.out = out;
-  s.ldo = M;
   return s;
 }
 
@@ -86,8 +86,6 @@ dflash2_status run_gemv(dflash2_handle* h, std::initializer_list<GemvSeg> segs, 
     a.seg[a.nseg++] = s;
     max_tiles = std::max(max_tiles, s.n_tiles);
   }
-  a.part = h->part;
-  a.counters = h->counters;
   DF2_CHECK(launch_gemv(a, h->fmt, max_tiles, h->num_sms, h->pdl, st));
   h->launches += 1;
   return DFLASH2_OK;
@@ -97,36 +95,6 @@ bool valid_matrix(const dflash2_matrix& m, int fmt) {
   if (!m.w || !aligned16(m.w)) return false;
   if (fmt == DFLASH2_WEIGHTS_Q8G64 && (!m.scale || !m.bias)) return false;
   return true;
-}
-
-// Scratch of the largest GEMV launch of a step (partial slots, tile counters).
-void gemv_scratch(const dflash2_handle* h, int R, size_t* part_floats, int* counters) {
-  const int N = 8 * R;
-  const dflash2_matrix dummy = {nullptr, nullptr, nullptr};
-  GemvSeg list[][3] = {
-      {seg_base(dummy, nullptr, 0, h->KT, R, h->H, h->KT)},
-      {seg_base(dummy, nullptr, 0, h->H, R, 4 * h->G, h->H)},
-      {seg_base(dummy, nullptr, 0, h->H, R, h->qd, h->H), seg_base(dummy, nullptr, 0, h->H, 2 * R, h->kvd, h->H),
-       seg_base(dummy, nullptr, 0, h->H, 2 * R, h->kvd, h->H)},
-      {seg_base(dummy, nullptr, 0, h->qd, R, h->H, h->qd)},
-      {seg_base(dummy, nullptr, 0, h->H, R, 2 * h->F, h->H)},
-      {seg_base(dummy, nullptr, 0, h->F, R, h->H, h->F)},
-      {seg_base(dummy, nullptr, 0, h->H, R, h->cfg.rank, h->H)},
-  };
-  const int nsegs[] = {1, 1, 3, 1, 1, 1, 1};
-  (void)N;
-  *part_floats = 0;
-  *counters = 0;
-  for (int i = 0; i < 7; ++i) {
-    GemvArgs a;
-    memset(&a, 0, sizeof(a));
-    for (int j = 0; j < nsegs[i]; ++j) a.seg[a.nseg++] = list[i][j];
-    size_t pf = 0;
-    int nc = 0;
-    gemv_plan(a, h->fmt, h->num_sms, &pf, &nc);
-    *part_floats = std::max(*part_floats, pf);
-    *counters = std::max(*counters, nc);
-  }
 }
 
 }  // namespace
@@ -196,15 +164,19 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->kvd = c.n_kv_heads * 128;
   h->KT = c.n_taps * c.hidden;
   h->nch128 = c.hidden / 128;
-  h->nch16 = c.hidden / 16;
   h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
   h->lm_ctas = h->num_sms;  // one 16-warp CTA per SM (the kernel needs 128 registers a thread)
+  // K splits by total 16-row tiles of each launch (independent of the request count)
+  h->s_fc = gemv_choose_splits(h->H / 16, h->KT, h->num_sms);
+  h->s_delta = gemv_choose_splits(4 * h->G / 16, h->H, h->num_sms);
+  h->s_qkv = gemv_choose_splits((h->qd + 2 * h->kvd) / 16, h->H, h->num_sms);
+  h->s_o = gemv_choose_splits(h->H / 16, h->qd, h->num_sms);
+  h->s_gu = gemv_choose_splits(2 * h->F / 16, h->H, h->num_sms);
+  h->s_down = gemv_choose_splits(h->H / 16, h->F, h->num_sms);
+  h->s_sel = gemv_choose_splits(c.rank / 16, h->H, h->num_sms);
   const size_t N = 8 * static_cast<size_t>(max_requests);
   const size_t esz = 2;  // bf16 / fp16 activations
-  size_t part_floats = 0;
-  int n_counters = 0;
-  gemv_scratch(h, max_requests, &part_floats, &n_counters);
   struct Buf {
     void** p;
     size_t bytes;
@@ -212,23 +184,23 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   const Buf bufs[] = {
       {reinterpret_cast<void**>(&h->x), N * h->H * 4},
       {reinterpret_cast<void**>(&h->ss128), N * h->nch128 * 4},
-      {reinterpret_cast<void**>(&h->ss16), N * h->nch16 * 4},
       {reinterpret_cast<void**>(&h->ss_c), N * h->nch128 * 4},
-      {reinterpret_cast<void**>(&h->dproj), N * 4 * h->G * 4},
+      {reinterpret_cast<void**>(&h->dproj), h->s_delta * N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_a), N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_m), N * 4 * h->G * 4},
-      {reinterpret_cast<void**>(&h->fc_out), N * h->H * 4},
-      {reinterpret_cast<void**>(&h->q_out), N * h->qd * 4},
-      {reinterpret_cast<void**>(&h->k_out), 2 * N * h->kvd * 4},
-      {reinterpret_cast<void**>(&h->v_out), 2 * N * h->kvd * 4},
-      {reinterpret_cast<void**>(&h->sel_out), N * c.rank * 4},
+      {reinterpret_cast<void**>(&h->fc_out), h->s_fc * N * h->H * 4},
+      {reinterpret_cast<void**>(&h->q_out), h->s_qkv * N * h->qd * 4},
+      {reinterpret_cast<void**>(&h->k_out), h->s_qkv * 2 * N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->v_out), h->s_qkv * 2 * N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->sel_out), h->s_sel * N * c.rank * 4},
       {reinterpret_cast<void**>(&h->q), N * h->qd * 4},
       {reinterpret_cast<void**>(&h->kb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->vb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->attn_part),
        static_cast<size_t>(max_requests) * h->nkv * h->n_attn_chunks * 32 * 130 * 4},
-      {reinterpret_cast<void**>(&h->part), part_floats * 4},
-      {reinterpret_cast<void**>(&h->counters), static_cast<size_t>(n_counters) * 4},
+      {reinterpret_cast<void**>(&h->ypart), std::max(h->s_o, h->s_down) * N * h->H * 4},
+      {reinterpret_cast<void**>(&h->gpart), h->s_gu * N * h->F * 4},
+      {reinterpret_cast<void**>(&h->upart), h->s_gu * N * h->F * 4},
       {reinterpret_cast<void**>(&h->act_a), 2 * N * h->H * esz},  // hi and lo planes
       {reinterpret_cast<void**>(&h->act_qkv), 2 * 2 * N * h->H * esz},
       {reinterpret_cast<void**>(&h->act_taps), 2 * N * h->KT * esz},
@@ -335,7 +307,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   }
   // ---- a1: taps projection fc [H][n_taps H], then hidden_norm input of the context rows
   {
-    dflash2_status s = run_gemv(h, {seg_store(h->w.fc, h->act_taps, h->lo_taps, h->KT, R, H, h->KT, h->fc_out)}, st);
+    dflash2_status s =
+        run_gemv(h, {seg(h->w.fc, h->act_taps, h->lo_taps, h->KT, R, H, h->KT, h->s_fc, h->fc_out)}, st);
     if (s) return s;
     FcFinishArgs a;
     a.y = h->fc_out;
@@ -347,23 +320,23 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.act_row0 = N;
     a.nch = h->nch128;
     a.fmt = fmt;
+    a.splits = h->s_fc;
+    a.n_rows = N;
     DF2_CHECK(launch_fc_finish(a, R, pdl, st));
     h->launches++;
   }
-  const float* ss_in = h->ss128;  // sums of squares of the current x and their chunk count
-  int nch_in = h->nch128;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& L = h->w.layers[l];
     uint16_t* kc = static_cast<uint16_t*>(k_cache) + l * layer_stride;
     uint16_t* vc = static_cast<uint16_t*>(v_cache) + l * layer_stride;
     // ---- a3: delta projection of the normed input, conv-in
     dflash2_status s =
-        run_gemv(h, {seg_store(L.attn_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->dproj)}, st);
+        run_gemv(h, {seg(L.attn_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->s_delta, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
       a.dproj = h->dproj;
-      a.ss = ss_in;
+      a.ss = h->ss128;
       a.x = h->x;
       a.norm_w = static_cast<const uint16_t*>(L.input_norm);
       a.base = static_cast<const uint16_t*>(L.attn_base);
@@ -371,17 +344,19 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act = h->act_qkv;
       a.act_lo = h->lo_qkv;
       a.H = H;
-      a.nch = nch_in;
+      a.nch = h->nch128;
       a.fmt = fmt;
+      a.splits = h->s_delta;
+      a.n_rows = N;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
     // ---- a4: q (block rows), k and v (block + new context rows)
     s = run_gemv(h,
-                 {seg_store(L.q, h->act_qkv, h->lo_qkv, H, R, h->qd, H, h->q_out),
-                  seg_store(L.k, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->k_out),
-                  seg_store(L.v, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->v_out)},
+                 {seg(L.q, h->act_qkv, h->lo_qkv, H, R, h->qd, H, h->s_qkv, h->q_out),
+                  seg(L.k, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->s_qkv, h->k_out),
+                  seg(L.v, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->s_qkv, h->v_out)},
                  st);
     if (s) return s;
     {
@@ -406,11 +381,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.kv_capacity = h->kv_cap;
       a.H = H;
       a.nch = h->nch128;
+      a.splits = h->s_qkv;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_qkv_finish(a, R, pdl, st));
       h->launches++;
     }
-    // ---- a5: block attention over the window
+  // ---- a5: block attention over the window
     {
       AttnArgs a;
       a.q = h->q;
@@ -432,32 +408,36 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       DF2_CHECK(launch_attention(a, R, pdl, st));
       h->launches += 2;
     }
-    // ---- a6: output projection; epilogue: conv-out, residual, post-attention norm input
+    // ---- a6: output projection, conv-out + residual, post-attention norm input
+    s = run_gemv(h, {seg(L.o, h->act_o, h->lo_o, h->qd, R, H, h->qd, h->s_o, h->ypart)}, st);
+    if (s) return s;
     {
-      GemvSeg sg = seg_base(L.o, h->act_o, h->lo_o, h->qd, R, H, h->qd);
-      sg.epi = kEpiConvOut;
-      sg.act = h->act_a;
-      sg.act_lo = h->lo_a;
-      sg.ld_act = H;
-      sg.act_fmt = fmt;
-      sg.xres = h->x;
-      sg.delta = h->delta_a;
-      sg.base = static_cast<const uint16_t*>(L.attn_base);
-      sg.norm_w = static_cast<const uint16_t*>(L.post_norm);
-      sg.ss = h->ss16;
-      sg.G = G;
-      s = run_gemv(h, {sg}, st);
-      if (s) return s;
+      ConvOutArgs a;
+      a.part = h->ypart;
+      a.delta = h->delta_a;
+      a.base = static_cast<const uint16_t*>(L.attn_base);
+      a.norm_w = static_cast<const uint16_t*>(L.post_norm);
+      a.x = h->x;
+      a.act = h->act_a;
+      a.act_lo = h->lo_a;
+      a.act2 = nullptr;
+      a.act2_lo = 0;
+      a.ss = h->ss128;
+      a.H = H;
+      a.nch = h->nch128;
+      a.fmt = fmt;
+      a.splits = h->s_o;
+      a.n_rows = N;
+      DF2_CHECK(launch_conv_out(a, R, pdl, st));
+      h->launches++;
     }
-    ss_in = h->ss16;
-    nch_in = h->nch16;
     // ---- a7: MLP sublayer
-    s = run_gemv(h, {seg_store(L.mlp_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->dproj)}, st);
+    s = run_gemv(h, {seg(L.mlp_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->s_delta, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
       a.dproj = h->dproj;
-      a.ss = ss_in;
+      a.ss = h->ss128;
       a.x = h->x;
       a.norm_w = static_cast<const uint16_t*>(L.post_norm);
       a.base = static_cast<const uint16_t*>(L.mlp_base);
@@ -465,43 +445,55 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act = h->act_qkv;
       a.act_lo = h->lo_qkv;
       a.H = H;
-      a.nch = nch_in;
+      a.nch = h->nch128;
       a.fmt = fmt;
+      a.splits = h->s_delta;
+      a.n_rows = N;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
+    s = run_gemv(h,
+                 {seg(L.gate, h->act_qkv, h->lo_qkv, H, R, h->F, H, h->s_gu, h->gpart),
+                  seg(L.up, h->act_qkv, h->lo_qkv, H, R, h->F, H, h->s_gu, h->upart)},
+                 st);
+    if (s) return s;
     {
-      GemvSeg sg = seg_base(L.gate, h->act_qkv, h->lo_qkv, H, R, 2 * h->F, H);  // tile = 8 gate + 8 up rows
-      sg.w2 = L.up.w;
-      sg.scale2 = static_cast<const uint16_t*>(L.up.scale);
-      sg.bias2 = static_cast<const uint16_t*>(L.up.bias);
-      sg.epi = kEpiSwiglu;
-      sg.act = h->act_h;
-      sg.act_lo = h->lo_h;
-      sg.ld_act = h->F;
-      sg.act_fmt = fmt;
-      s = run_gemv(h, {sg}, st);
-      if (s) return s;
+      SwigluArgs a;
+      a.part_g = h->gpart;
+      a.part_u = h->upart;
+      a.act = h->act_h;
+      a.act_lo = h->lo_h;
+      a.F = h->F;
+      a.fmt = fmt;
+      a.splits = h->s_gu;
+      a.n_rows = N;
+      DF2_CHECK(launch_swiglu(a, R, pdl, st));
+      h->launches++;
     }
+    s = run_gemv(h, {seg(L.down, h->act_h, h->lo_h, h->F, R, H, h->F, h->s_down, h->ypart)}, st);
+    if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
-      GemvSeg sg = seg_base(L.down, h->act_h, h->lo_h, h->F, R, H, h->F);
-      sg.epi = kEpiConvOut;
-      sg.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
-      sg.act_lo = (last && fmt == 0) ? h->lo_fin : h->lo_a;
-      sg.ld_act = H;
-      sg.act_fmt = fmt;
-      sg.act2 = (last && fmt != 0) ? h->act_fin : nullptr;  // LM-head input is bf16 in both formats
-      sg.act2_lo = h->lo_fin;
-      sg.xres = h->x;
-      sg.delta = h->delta_m;
-      sg.base = static_cast<const uint16_t*>(L.mlp_base);
-      sg.norm_w = static_cast<const uint16_t*>(last ? h->w.final_norm : h->w.layers[l + 1].input_norm);
-      sg.ss = h->ss16;
-      sg.G = G;
-      s = run_gemv(h, {sg}, st);
-      if (s) return s;
+      ConvOutArgs a;
+      a.part = h->ypart;
+      a.delta = h->delta_m;
+      a.base = static_cast<const uint16_t*>(L.mlp_base);
+      a.norm_w = static_cast<const uint16_t*>(last ? h->w.final_norm : h->w.layers[l + 1].input_norm);
+      a.x = h->x;
+      // LM-head input is bf16 in both formats; the next layer's input is in the matrices' format
+      a.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
+      a.act_lo = (last && fmt == 0) ? h->lo_fin : h->lo_a;
+      a.act2 = (last && fmt != 0) ? h->act_fin : nullptr;
+      a.act2_lo = h->lo_fin;
+      a.ss = h->ss128;
+      a.H = H;
+      a.nch = h->nch128;
+      a.fmt = fmt;
+      a.splits = h->s_down;
+      a.n_rows = N;
+      DF2_CHECK(launch_conv_out(a, R, pdl, st));
+      h->launches++;
     }
   }
   // ---- a8: LM head + top-16
@@ -510,13 +502,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.w = static_cast<const uint16_t*>(h->w.lm_head);
     a.x = h->act_fin;
     a.x_lo = h->lo_fin;
-    a.ss = h->ss16;
+    a.ss = h->ss128;
     a.logits_out = logits_out;
     a.part_keys = h->topk_keys;
     a.V = h->V;
     a.H = H;
     a.n_rows = N;
-    a.nch = h->nch16;
+    a.nch = h->nch128;
     a.n_cta = h->lm_ctas;
     a.eps = c.rms_eps;
     // external records: inside a stream capture they become event-record nodes the host can time
@@ -529,19 +521,21 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   {
     const void* xin = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
     const size_t xlo = fmt == 0 ? h->lo_fin : h->lo_a;
-    dflash2_status s = run_gemv(h, {seg_store(h->w.sel_proj, xin, xlo, H, R, c.rank, H, h->sel_out)}, st);
+    dflash2_status s =
+        run_gemv(h, {seg(h->w.sel_proj, xin, xlo, H, R, c.rank, H, h->s_sel, h->sel_out)}, st);
     if (s) return s;
     TopkMergeArgs a;
     a.part_keys = h->topk_keys;
     a.sel = h->sel_out;
-    a.ss = h->ss16;
+    a.ss = h->ss128;
     a.cand_ids = cand_ids;
     a.cand_logits = cand_logits;
     a.gate = gate;
     a.n_rows = N;
     a.n_cta = h->lm_ctas;
     a.rank = c.rank;
-    a.nch = h->nch16;
+    a.nch = h->nch128;
+    a.sel_splits = h->s_sel;
     a.H = H;
     a.eps = c.rms_eps;
     DF2_CHECK(launch_topk_merge(a, pdl, st));
@@ -565,7 +559,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   a.V = h->V;
   a.H = h->H;
   a.n_rows = n_rows;
-  a.nch = h->nch16;
+  a.nch = h->nch128;
   a.n_cta = h->lm_ctas;
   a.eps = h->cfg.rms_eps;
   DF2_CHECK(launch_lmhead(a, h->pdl, st));
@@ -579,7 +573,8 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   m.n_rows = n_rows;
   m.n_cta = h->lm_ctas;
   m.rank = h->cfg.rank;
-  m.nch = h->nch16;
+  m.nch = h->nch128;
+  m.sel_splits = 0;
   m.H = h->H;
   m.eps = h->cfg.rms_eps;
   DF2_CHECK(launch_topk_merge(m, h->pdl, st));

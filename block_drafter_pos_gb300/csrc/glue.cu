@@ -1,8 +1,9 @@
 // Element-wise stages between the weight-streaming projections: block embedding
 // and taps packing (start), the taps-projection norm input (fc_finish), the
-// dynamic convolution before a sublayer (conv_in), and q/k norm + RoPE + context
-// cache append after the QKV projection (qkv_finish).  The convolution after a
-// sublayer, the residual add and SwiGLU run in the GEMV epilogues (gemv.cu).
+// dynamic convolution before a sublayer (conv_in) and after it with the residual
+// add (conv_out), SwiGLU, and q/k norm + RoPE + context cache append after the QKV
+// projection (qkv_finish).  Each consumer adds the producer GEMV's split planes in
+// split order.
 //
 // RMSNorm is deferred: producers write x * w and per-chunk sums of squares, and
 // the consumer applies 1/rms (the scale commutes with the projections).  Row
@@ -93,9 +94,12 @@ __global__ void __launch_bounds__(kCh) fc_finish_kernel(const FcFinishArgs a) {
   const int row0 = r * kB;
   const float w = bf16_to_f32(a.norm_w[c]);
   float yv[kB];
+  const size_t plane = static_cast<size_t>(a.n_rows) * a.H;
 #pragma unroll
   for (int j = 0; j < kB; ++j) {
-    yv[j] = a.y[static_cast<size_t>(row0 + j) * a.H + c];
+    float y = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) y += a.y[sp * plane + static_cast<size_t>(row0 + j) * a.H + c];
+    yv[j] = y;
     put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(a.act_row0 + row0 + j) * a.H + c, yv[j] * w);
   }
   emit_ss(yv, row0, a.ss, a.nch, sm);
@@ -122,7 +126,11 @@ __global__ void __launch_bounds__(kCh) conv_in_kernel(const ConvInArgs a) {
   for (int e = threadIdx.x; e < kB * 32; e += kCh) {
     const int i = e >> 5, io = (e >> 4) & 1, t = (e >> 3) & 1, gl = e & 7;
     const int gidx = (io * 2 + t) * G + blockIdx.y * (kCh / 16) + gl;
-    const float d = a.dproj[static_cast<size_t>(row0 + i) * (4 * G) + gidx] * rr[i];
+    const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
+    float dsum = 0.f;
+#pragma unroll 4
+    for (int sp = 0; sp < a.splits; ++sp) dsum += a.dproj[sp * plane + static_cast<size_t>(row0 + i) * (4 * G) + gidx];
+    const float d = dsum * rr[i];
     if (io == 0) dsh[i][t][gl] = d;
     a.delta[static_cast<size_t>(row0 + i) * (4 * G) + gidx] = d;
   }
@@ -138,6 +146,64 @@ __global__ void __launch_bounds__(kCh) conv_in_kernel(const ConvInArgs a) {
     put_act(a.act, a.act_lo, a.fmt, idx, (b0 + dsh[i][0][gl]) * ai + (b1 + dsh[i][1][gl]) * prev);
     prev = ai;
   }
+}
+
+// ------------------------------------------------------------------ conv after a sublayer + residual
+// y = sum of split planes; x_i += (b2 + d2_i) y_i + (b3 + d3_i) y_{i-1} (the
+// convolution wrapping the sublayer's output); act = x * w_next; ss of x.
+__global__ void __launch_bounds__(kCh) conv_out_kernel(const ConvOutArgs a) {
+  __shared__ float sm[4 * kB];
+  pdl_begin();
+  const int r = blockIdx.x;
+  const int c = blockIdx.y * kCh + threadIdx.x;
+  const int row0 = r * kB;
+  const int G = a.H / 16;
+  const int g = c >> 4;
+  const size_t plane = static_cast<size_t>(a.n_rows) * a.H;
+  const float b2 = bf16_to_f32(a.base[2 * a.H + c]), b3 = bf16_to_f32(a.base[3 * a.H + c]);
+  const float w = bf16_to_f32(a.norm_w[c]);
+  float y[kB];
+#pragma unroll
+  for (int i = 0; i < kB; ++i) y[i] = 0.f;
+  for (int sp = 0; sp < a.splits; ++sp) {  // split planes in order; the 8 rows' loads are independent
+#pragma unroll
+    for (int i = 0; i < kB; ++i) y[i] += a.part[sp * plane + static_cast<size_t>(row0 + i) * a.H + c];
+  }
+  float xv[kB];
+#pragma unroll
+  for (int i = 0; i < kB; ++i) {
+    const float* d = a.delta + static_cast<size_t>(row0 + i) * (4 * G);
+    const float yprev = i > 0 ? y[i - 1] : 0.f;
+    const size_t idx = static_cast<size_t>(row0 + i) * a.H + c;
+    xv[i] = a.x[idx] + (b2 + d[2 * G + g]) * y[i] + (b3 + d[3 * G + g]) * yprev;
+    a.x[idx] = xv[i];
+    put_act(a.act, a.act_lo, a.fmt, idx, xv[i] * w);
+    if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, idx, xv[i] * w);
+  }
+  emit_ss(xv, row0, a.ss, a.nch, sm);
+}
+
+// ------------------------------------------------------------------ SwiGLU
+// h = silu(gate) * up from the split planes of the two projections.
+__global__ void __launch_bounds__(kCh) swiglu_kernel(const SwigluArgs a) {
+  pdl_begin();
+  const int r = blockIdx.x;
+  const int c = blockIdx.y * kCh + threadIdx.x;
+  const int row0 = r * kB;
+  const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
+  float gs[kB], us[kB];
+#pragma unroll
+  for (int i = 0; i < kB; ++i) gs[i] = us[i] = 0.f;
+  for (int sp = 0; sp < a.splits; ++sp) {
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      gs[i] += a.part_g[sp * plane + static_cast<size_t>(row0 + i) * a.F + c];
+      us[i] += a.part_u[sp * plane + static_cast<size_t>(row0 + i) * a.F + c];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kB; ++i)
+    put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(row0 + i) * a.F + c, gs[i] / (1.f + __expf(-gs[i])) * us[i]);
 }
 
 // ------------------------------------------------------------------ q/k norm, RoPE, cache append
@@ -173,15 +239,19 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
   if (ctx_row && jj >= nn) return;
   const int row0 = r * kB;
   const float* src;
+  size_t plane;
   if (kind == 0) {
     src = a.q_out + (static_cast<size_t>(row0 + jj) * nq + hh) * 128;
+    plane = static_cast<size_t>(a.n_rows) * nq * 128;
   } else {
     const size_t prow = ctx_row ? static_cast<size_t>(a.n_rows) + row0 + jj : static_cast<size_t>(row0 + jj);
     src = (kind == 1 ? a.k_out : a.v_out) + (prow * nkv + hh) * 128;
+    plane = static_cast<size_t>(2 * a.n_rows) * nkv * 128;
   }
-  float v[4];
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int sp = 0; sp < a.splits; ++sp)  // split planes in order
 #pragma unroll
-  for (int c = 0; c < 4; ++c) v[c] = src[lane + 32 * c];
+    for (int c = 0; c < 4; ++c) v[c] += src[sp * plane + lane + 32 * c];
   if (ctx_row) {
     const float rc = warp_inv_rms(a.ss_c, row0 + jj, a.nch, a.H, a.eps);
 #pragma unroll
@@ -230,6 +300,12 @@ cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, bool pdl, cudaStr
 }
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st) {
   return launch_ex(conv_in_kernel, dim3(n_req, a.H / kCh), dim3(kCh), 0, st, pdl, a);
+}
+cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  return launch_ex(conv_out_kernel, dim3(n_req, a.H / kCh), dim3(kCh), 0, st, pdl, a);
+}
+cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  return launch_ex(swiglu_kernel, dim3(n_req, a.F / kCh), dim3(kCh), 0, st, pdl, a);
 }
 cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st) {
   const int n_items = kB * a.n_q_heads + 4 * kB * a.n_kv_heads;

@@ -26,16 +26,16 @@ struct StartArgs {
 };
 
 struct FcFinishArgs {
-  const float* y;          // taps projection [N][H]
+  const float* y;          // taps projection partials [splits][N][H]
   const uint16_t* norm_w;  // hidden_norm
   void* act;               // QKV input; context rows start at act_row0
   size_t act_lo;
   float* ss;               // [N][H/128] sums of squares of y
-  int H, act_row0, nch, fmt;
+  int H, act_row0, nch, fmt, splits, n_rows;
 };
 
 struct ConvInArgs {
-  const float* dproj;      // delta projection of x * w, [N][4G] (not yet scaled by 1/rms)
+  const float* dproj;      // delta projection partials of x * w, [splits][N][4G] (not yet scaled by 1/rms)
   const float* ss;         // [N][nch] sums of squares of x
   const float* x;          // residual stream
   const uint16_t* norm_w;
@@ -43,13 +43,37 @@ struct ConvInArgs {
   float* delta;            // out: [N][4G] scaled by 1/rms
   void* act;               // out: conv-in'd sublayer input [N][H]
   size_t act_lo;
-  int H, nch, fmt;
+  int H, nch, fmt, splits, n_rows;
   float eps;
 };
 
+// Dynamic convolution after a sublayer, residual add, next norm's input.
+struct ConvOutArgs {
+  const float* part;       // sublayer output partials [splits][N][H]
+  const float* delta;      // [N][4G] (io 1 = conv after the sublayer)
+  const uint16_t* base;    // [4][H]
+  const uint16_t* norm_w;  // norm weight of the next sublayer
+  float* x;                // residual stream [N][H], updated in place
+  void* act;               // x * w_next in the next projection's format, plus low plane at act + act_lo
+  size_t act_lo;
+  uint16_t* act2;          // optional bf16 copy (LM-head input), or null
+  size_t act2_lo;
+  float* ss;               // [N][H/128] sums of squares of the updated x
+  int H, nch, fmt, splits, n_rows;
+};
+
+// SwiGLU of the gate and up projections: act = silu(gate) * up.
+struct SwigluArgs {
+  const float* part_g;     // gate partials [splits][N][F]
+  const float* part_u;     // up partials [splits][N][F]
+  void* act;               // [N][F] plus low plane at act + act_lo
+  size_t act_lo;
+  int F, fmt, splits, n_rows;
+};
+
 struct QkvFinishArgs {
-  const float* q_out;      // [N][nq*128]
-  const float* k_out;      // [2N][nkv*128]: block rows, then context rows
+  const float* q_out;      // partials [splits][N][nq*128]
+  const float* k_out;      // partials [splits][2N][nkv*128]: block rows, then context rows
   const float* v_out;
   const float* ss_c;       // [N][nch] of the projected taps
   const uint16_t* q_norm;
@@ -62,7 +86,7 @@ struct QkvFinishArgs {
   float* vb;
   uint16_t* k_cache;       // this layer's slice: [max_req][cap][nkv][128]
   uint16_t* v_cache;
-  int n_q_heads, n_kv_heads, n_rows, kv_capacity, H, nch;
+  int n_q_heads, n_kv_heads, n_rows, kv_capacity, H, nch, splits;
   float eps;
 };
 
@@ -70,6 +94,8 @@ cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t s
 cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, bool pdl, cudaStream_t st);
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st);
 cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st);
+cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st);
+cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
@@ -103,12 +129,12 @@ cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st);
 
 struct TopkMergeArgs {
   const unsigned long long* part_keys;  // [N][n_cta][16]
-  const float* sel;        // selector projection [N][rank], or null
+  const float* sel;        // selector projection partials [sel_splits][N][rank], or null
   const float* ss;
   int32_t* cand_ids;       // [R][7][16]
   float* cand_logits;
   float* gate;             // [R][7][rank]
-  int n_rows, n_cta, rank, nch, H;
+  int n_rows, n_cta, rank, nch, H, sel_splits;
   float eps;
 };
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st);

@@ -217,8 +217,12 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   }
   __syncthreads();
   if (a.sel == nullptr) return;
-  for (int j = threadIdx.x; j < a.rank; j += blockDim.x)
-    a.gate[(static_cast<size_t>(rq) * 7 + pos - 1) * a.rank + j] = a.sel[static_cast<size_t>(n) * a.rank + j] * rs;
+  const size_t plane = static_cast<size_t>(a.n_rows) * a.rank;
+  for (int j = threadIdx.x; j < a.rank; j += blockDim.x) {
+    float v = 0.f;
+    for (int sp = 0; sp < a.sel_splits; ++sp) v += a.sel[sp * plane + static_cast<size_t>(n) * a.rank + j];
+    a.gate[(static_cast<size_t>(rq) * 7 + pos - 1) * a.rank + j] = v * rs;
+  }
 }
 
 template <int NT>
