@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.dflash2_verify.argtypes = [vp, i32] + [vp] * 12
         L.dflash2_head_topk.argtypes = [vp, i32] + [vp] * 5
         L.dflash2_head_topk.restype = i32
+        L.dflash2_head_topk_noalloc.argtypes = [vp, i32, i32, i32] + [vp] * 5
+        L.dflash2_head_topk_noalloc.restype = i32
         L.dflash2_launch_count.argtypes = [vp]
         L.dflash2_launch_count.restype = i64
         L.dflash2_set_lmhead_events.argtypes = [vp, vp, vp]
@@ -143,6 +145,15 @@ def dflash2_verify(h, n_req, target_logits, path, cand_ids, q_rows, temperature,
 def dflash2_head_topk(h, n_rows, hidden, cand_ids, cand_logits, logits_out=None, stream=None):
     _check(lib().dflash2_head_topk(h, n_rows, _p(hidden), _p(cand_ids), _p(cand_logits), _p(logits_out),
                                    _stream(stream)), "dflash2_head_topk")
+
+
+def dflash2_head_topk_noalloc(lm_head, vocab, hidden_dim, n_rows, hidden, cand_ids, cand_logits, logits_out=None,
+                              stream=None):
+    """LM head + top-16 that allocates nothing: for callers that cannot call
+    cudaMalloc (its scratch is a fixed device array inside the library)."""
+    _check(lib().dflash2_head_topk_noalloc(_p(lm_head), vocab, hidden_dim, n_rows, _p(hidden), _p(cand_ids),
+                                           _p(cand_logits), _p(logits_out), _stream(stream)),
+           "dflash2_head_topk_noalloc")
 
 
 def dflash2_launch_count(h) -> int:

@@ -1,0 +1,106 @@
+// LM head + top-16 for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all.  Examples: a serving runtime whose
+// allocator owns every byte of HBM, or a plug-in that runs inside another
+// framework's memory pool.  Others cannot afford an allocation on their path: a
+// first-use cudaMalloc can synchronise the device or fail with out-of-memory in
+// the middle of a step.  The handle-based entry points reserve their scratch at
+// dflash2_create time; this one needs no handle.  The per-CTA candidate lists of
+// the LM-head kernel live in one fixed device array of this library.  The array
+// is loaded with the library and held on every GPU that uses it until the
+// process exits.
+#include <mutex>
+
+#include "../../include/dflash2.h"
+#include "glue.h"
+
+using namespace df2;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kKeys = static_cast<size_t>(DFLASH2_NOALLOC_MAX_ROWS) * DFLASH2_NOALLOC_MAX_CTAS * 16;
+
+// [rows][CTAs][16] candidate keys (value bits + vocabulary id), 640 KiB.
+static __device__ __align__(256) unsigned long long g_noalloc_keys[kKeys];
+
+struct DeviceSlot {
+  unsigned long long* keys;  // device address of g_noalloc_keys on this device
+  int n_cta;
+};
+
+std::mutex g_mu;
+DeviceSlot g_slots[kMaxDevices];
+bool g_ready[kMaxDevices];
+
+// Looks up the array's device address and the SM count once per device, with
+// that device current.  The name g_noalloc_keys is only a host-side stand-in in
+// host code; the kernels must get this address instead.
+cudaError_t device_slot(DeviceSlot* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ready[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_keys);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_slots[dev].keys = static_cast<unsigned long long*>(p);
+    g_slots[dev].n_cta = sms < DFLASH2_NOALLOC_MAX_CTAS ? sms : DFLASH2_NOALLOC_MAX_CTAS;
+    g_ready[dev] = true;
+  }
+  *out = g_slots[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t vocab, int32_t hidden_dim,
+                                                    int32_t n_rows, const void* hidden, int32_t* cand_ids,
+                                                    float* cand_logits, float* logits_out, void* stream) {
+  if (!lm_head || !hidden || !cand_ids || !cand_logits) return DFLASH2_E_INVAL;
+  if ((reinterpret_cast<uintptr_t>(lm_head) & 15u) || (reinterpret_cast<uintptr_t>(hidden) & 15u))
+    return DFLASH2_E_INVAL;
+  if (vocab < 16 || hidden_dim < 128 || n_rows < 8 || n_rows % 8) return DFLASH2_E_INVAL;
+  // sizes the fixed scratch or the kernel's instantiations do not cover
+  if (n_rows > DFLASH2_NOALLOC_MAX_ROWS || vocab % 16 || hidden_dim % 128) return DFLASH2_E_UNSUPPORTED;
+  DeviceSlot slot;
+  if (device_slot(&slot) != cudaSuccess) return DFLASH2_E_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Every (row, CTA) list the merge reads is rewritten by the LM-head launch
+  // first, so nothing left in the array by an earlier call is ever read.
+  LmHeadArgs a;
+  a.w = static_cast<const uint16_t*>(lm_head);
+  a.x = static_cast<const uint16_t*>(hidden);
+  a.x_lo = 0;
+  a.ss = nullptr;
+  a.logits_out = logits_out;
+  a.part_keys = slot.keys;
+  a.V = vocab;
+  a.H = hidden_dim;
+  a.n_rows = n_rows;
+  a.nch = hidden_dim / 128;
+  a.n_cta = slot.n_cta;
+  a.eps = 0.f;
+  if (launch_lmhead(a, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
+  TopkMergeArgs m;
+  m.part_keys = slot.keys;
+  m.sel = nullptr;
+  m.ss = nullptr;
+  m.cand_ids = cand_ids;
+  m.cand_logits = cand_logits;
+  m.gate = nullptr;
+  m.n_rows = n_rows;
+  m.n_cta = slot.n_cta;
+  m.rank = 0;
+  m.nch = hidden_dim / 128;
+  m.H = hidden_dim;
+  m.sel_splits = 0;
+  m.eps = 0.f;
+  if (launch_topk_merge(m, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
+  return DFLASH2_OK;
+}

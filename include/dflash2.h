@@ -201,6 +201,39 @@ dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* s
  * (LM-head weights + activations + candidate outputs), for roofline reports. */
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req);
 
+/* ---- LM head + top-16 without any device allocation ----
+ * The paper has no counterpart of this call: it exists for users of this
+ * library that cannot allocate device memory.  Some run inside a runtime whose
+ * allocator owns all of HBM, or as a plug-in of another framework's memory pool.
+ * Others must not risk a cudaMalloc on their path, because one can synchronise
+ * the device or fail for lack of memory in the middle of a step.  It computes
+ * what dflash2_head_topk computes (logits of block positions 1..7 of each
+ * request and their top-16, with hidden already normalised), but needs no
+ * handle.  Its scratch (the per-CTA candidate lists, 640 KiB) is one fixed
+ * device array inside this library, held on every GPU that uses it until the
+ * process exits.
+ *   lm_head  [vocab][hidden_dim] bf16, 16-byte aligned, caller-owned.
+ *   hidden   [n_rows][hidden_dim] bf16, 16-byte aligned; row n is block position
+ *            n%8 of request n/8 (position 0 is not projected).
+ *   cand_ids, cand_logits  [n_rows/8][7][16]; logits_out [n_rows/8][7][vocab] or NULL.
+ * Returns DFLASH2_E_INVAL for null or misaligned pointers, n_rows not a positive
+ * multiple of 8, vocab < 16 or hidden_dim < 128, and DFLASH2_E_UNSUPPORTED for
+ * n_rows > DFLASH2_NOALLOC_MAX_ROWS, vocab not a multiple of 16 or hidden_dim not
+ * a multiple of 128; nothing is launched then.  Uses
+ * min(SM count, DFLASH2_NOALLOC_MAX_CTAS) CTAs.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  It calls no
+ * cudaMalloc or cudaFree and no allocating library routine.  All calls share the
+ * one array: calls whose kernels overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller.  Every entry a call
+ * reads is written earlier in the same call, so nothing needs clearing between
+ * calls. */
+#define DFLASH2_NOALLOC_MAX_ROWS 32
+#define DFLASH2_NOALLOC_MAX_CTAS 160
+dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t vocab, int32_t hidden_dim, int32_t n_rows,
+                                         const void* hidden, int32_t* cand_ids, float* cand_logits,
+                                         float* logits_out, void* stream);
+
 /* Human-readable text of a status code (static string). */
 const char* dflash2_status_string(dflash2_status s);
 
