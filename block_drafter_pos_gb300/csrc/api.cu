@@ -28,14 +28,14 @@ struct dflash2_handle {
   int max_req, kv_cap, num_sms, fmt;
   bool pdl;
   int H, G, F, V, nq, nkv, qd, kvd, KT;
-  int nch128;  // 128-channel chunks of the sums-of-squares partials
+  int nch_ss;  // 32-channel chunks of the sums-of-squares partials
   int n_attn_chunks, n_verify_chunks, lm_ctas;
   // K splits of each projection (fixed at create from the grid size)
   int s_fc, s_delta, s_qkv, s_o, s_gu, s_down, s_sel;
   // scratch
   char* arena;
   size_t arena_bytes;
-  float *x, *ss128, *ss_c, *dproj, *delta_a, *delta_m, *fc_out, *q_out, *k_out, *v_out, *sel_out;
+  float *x, *ss, *ss_c, *dproj, *delta_a, *delta_m, *fc_out, *q_out, *k_out, *v_out, *sel_out;
   float *q, *kb, *vb, *attn_part, *ypart, *gpart, *upart;
   void *act_a, *act_qkv, *act_taps, *act_o, *act_h;
   uint16_t* act_fin;
@@ -163,7 +163,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->qd = c.n_q_heads * 128;
   h->kvd = c.n_kv_heads * 128;
   h->KT = c.n_taps * c.hidden;
-  h->nch128 = c.hidden / 128;
+  h->nch_ss = c.hidden / 32;
   h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
   h->lm_ctas = h->num_sms;  // one 16-warp CTA per SM (the kernel needs 128 registers a thread)
@@ -183,8 +183,8 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   };
   const Buf bufs[] = {
       {reinterpret_cast<void**>(&h->x), N * h->H * 4},
-      {reinterpret_cast<void**>(&h->ss128), N * h->nch128 * 4},
-      {reinterpret_cast<void**>(&h->ss_c), N * h->nch128 * 4},
+      {reinterpret_cast<void**>(&h->ss), N * h->nch_ss * 4},
+      {reinterpret_cast<void**>(&h->ss_c), N * h->nch_ss * 4},
       {reinterpret_cast<void**>(&h->dproj), h->s_delta * N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_a), N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_m), N * 4 * h->G * 4},
@@ -293,13 +293,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.x = h->x;
     a.act_a = h->act_a;
     a.act_a_lo = h->lo_a;
-    a.ss_x = h->ss128;
+    a.ss_x = h->ss;
     a.act_taps = h->act_taps;
     a.act_taps_lo = h->lo_taps;
     a.H = H;
     a.n_taps = c.n_taps;
     a.mask_id = c.mask_token_id;
-    a.nch = h->nch128;
+    a.nch = h->nch_ss;
     a.fmt = fmt;
     a.V = h->V;
     DF2_CHECK(launch_start(a, R, pdl, st));
@@ -318,7 +318,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.ss = h->ss_c;
     a.H = H;
     a.act_row0 = N;
-    a.nch = h->nch128;
+    a.nch = h->nch_ss;
     a.fmt = fmt;
     a.splits = h->s_fc;
     a.n_rows = N;
@@ -336,7 +336,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     {
       ConvInArgs a;
       a.dproj = h->dproj;
-      a.ss = h->ss128;
+      a.ss = h->ss;
       a.x = h->x;
       a.norm_w = static_cast<const uint16_t*>(L.input_norm);
       a.base = static_cast<const uint16_t*>(L.attn_base);
@@ -344,7 +344,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act = h->act_qkv;
       a.act_lo = h->lo_qkv;
       a.H = H;
-      a.nch = h->nch128;
+      a.nch = h->nch_ss;
       a.fmt = fmt;
       a.splits = h->s_delta;
       a.n_rows = N;
@@ -380,7 +380,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.n_rows = N;
       a.kv_capacity = h->kv_cap;
       a.H = H;
-      a.nch = h->nch128;
+      a.nch = h->nch_ss;
       a.splits = h->s_qkv;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_qkv_finish(a, R, pdl, st));
@@ -422,9 +422,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act_lo = h->lo_a;
       a.act2 = nullptr;
       a.act2_lo = 0;
-      a.ss = h->ss128;
+      a.ss = h->ss;
       a.H = H;
-      a.nch = h->nch128;
+      a.nch = h->nch_ss;
       a.fmt = fmt;
       a.splits = h->s_o;
       a.n_rows = N;
@@ -437,7 +437,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     {
       ConvInArgs a;
       a.dproj = h->dproj;
-      a.ss = h->ss128;
+      a.ss = h->ss;
       a.x = h->x;
       a.norm_w = static_cast<const uint16_t*>(L.post_norm);
       a.base = static_cast<const uint16_t*>(L.mlp_base);
@@ -445,7 +445,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act = h->act_qkv;
       a.act_lo = h->lo_qkv;
       a.H = H;
-      a.nch = h->nch128;
+      a.nch = h->nch_ss;
       a.fmt = fmt;
       a.splits = h->s_delta;
       a.n_rows = N;
@@ -486,9 +486,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act_lo = (last && fmt == 0) ? h->lo_fin : h->lo_a;
       a.act2 = (last && fmt != 0) ? h->act_fin : nullptr;
       a.act2_lo = h->lo_fin;
-      a.ss = h->ss128;
+      a.ss = h->ss;
       a.H = H;
-      a.nch = h->nch128;
+      a.nch = h->nch_ss;
       a.fmt = fmt;
       a.splits = h->s_down;
       a.n_rows = N;
@@ -502,13 +502,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.w = static_cast<const uint16_t*>(h->w.lm_head);
     a.x = h->act_fin;
     a.x_lo = h->lo_fin;
-    a.ss = h->ss128;
+    a.ss = h->ss;
     a.logits_out = logits_out;
     a.part_keys = h->topk_keys;
     a.V = h->V;
     a.H = H;
     a.n_rows = N;
-    a.nch = h->nch128;
+    a.nch = h->nch_ss;
     a.n_cta = h->lm_ctas;
     a.eps = c.rms_eps;
     // external records: inside a stream capture they become event-record nodes the host can time
@@ -527,14 +527,14 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     TopkMergeArgs a;
     a.part_keys = h->topk_keys;
     a.sel = h->sel_out;
-    a.ss = h->ss128;
+    a.ss = h->ss;
     a.cand_ids = cand_ids;
     a.cand_logits = cand_logits;
     a.gate = gate;
     a.n_rows = N;
     a.n_cta = h->lm_ctas;
     a.rank = c.rank;
-    a.nch = h->nch128;
+    a.nch = h->nch_ss;
     a.sel_splits = h->s_sel;
     a.H = H;
     a.eps = c.rms_eps;
@@ -559,7 +559,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   a.V = h->V;
   a.H = h->H;
   a.n_rows = n_rows;
-  a.nch = h->nch128;
+  a.nch = h->nch_ss;
   a.n_cta = h->lm_ctas;
   a.eps = h->cfg.rms_eps;
   DF2_CHECK(launch_lmhead(a, h->pdl, st));
@@ -573,7 +573,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   m.n_rows = n_rows;
   m.n_cta = h->lm_ctas;
   m.rank = h->cfg.rank;
-  m.nch = h->nch128;
+  m.nch = h->nch_ss;
   m.sel_splits = 0;
   m.H = h->H;
   m.eps = h->cfg.rms_eps;

@@ -18,7 +18,8 @@ namespace df2 {
 namespace {
 
 constexpr int kB = 8;       // block positions
-constexpr int kCh = 128;    // channels per CTA (one thread per channel, all 8 rows)
+constexpr int kCw = 32;     // channels per CTA of the channel kernels: warp i = block row i, lane = channel
+constexpr int kThreads = kB * kCw;
 
 DF2_DEV void put_act(void* act, size_t lo, int fmt, size_t idx, float v) {
   if (fmt == 0) {
@@ -34,176 +35,132 @@ DF2_DEV void put_act(void* act, size_t lo, int fmt, size_t idx, float v) {
   }
 }
 
-// Per-row sum of squares of this CTA's 128 channels -> ss[row][blockIdx.y].
-__device__ void emit_ss(const float (&v)[kB], int row0, float* ss, int nch, float* sm) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  float r[kB];
+// Sum of the split planes p[s * plane], s = 0..S-1, added in split order.  The
+// loads of 8 planes are issued together so the latency is paid once per 8.
+DF2_DEV float plane_sum(const float* p, size_t plane, int S) {
+  float y = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float t[8];
 #pragma unroll
-  for (int i = 0; i < kB; ++i) r[i] = warp_sum(v[i] * v[i]);
-  __syncthreads();
-  if (lane == 0) {
+    for (int j = 0; j < 8; ++j) t[j] = (s0 + j < S) ? p[static_cast<size_t>(s0 + j) * plane] : 0.f;
 #pragma unroll
-    for (int i = 0; i < kB; ++i) sm[wid * kB + i] = r[i];
+    for (int j = 0; j < 8; ++j) y += t[j];
   }
-  __syncthreads();
-  if (threadIdx.x < kB) {
-    const int i = threadIdx.x;
-    ss[static_cast<size_t>(row0 + i) * nch + blockIdx.y] = ((sm[i] + sm[kB + i]) + sm[2 * kB + i]) + sm[3 * kB + i];
-  }
+  return y;
+}
+
+// Per-row sum of squares of this CTA's 32 channels -> ss[row][blockIdx.y] (one warp = one row).
+DF2_DEV void emit_ss(float v, int row, float* ss, int nch) {
+  const float s = warp_sum(v * v);
+  if ((threadIdx.x & 31) == 0) ss[static_cast<size_t>(row) * nch + blockIdx.y] = s;
 }
 
 // ------------------------------------------------------------------ start of the step
-__global__ void __launch_bounds__(kCh) start_kernel(const StartArgs a) {
-  __shared__ float sm[4 * kB];
+// blockIdx.y < H/32: block embedding, first norm input and its sums of squares;
+// above: taps of the new context rows packed into the fc projection's input.
+__global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
   pdl_begin();
   const int r = blockIdx.x;
-  const int c = blockIdx.y * kCh + threadIdx.x;
-  const int row0 = r * kB;
-  if (blockIdx.y * kCh < a.H) {
+  const int i = threadIdx.x >> 5;
+  const int row = r * kB + i;
+  const int ny = a.H / kCw;
+  if (static_cast<int>(blockIdx.y) < ny) {
+    const int c = blockIdx.y * kCw + (threadIdx.x & 31);
     const int anchor = min(max(a.anchor_ids[r], 0), a.V - 1);  // ids are clamped into the table
-    const float w = bf16_to_f32(a.norm_w[c]);
-    float xv[kB];
-#pragma unroll
-    for (int i = 0; i < kB; ++i) {
-      const int id = (i == 0) ? anchor : a.mask_id;
-      xv[i] = bf16_to_f32(a.embed[static_cast<size_t>(id) * a.H + c]);
-      const size_t idx = static_cast<size_t>(row0 + i) * a.H + c;
-      a.x[idx] = xv[i];
-      put_act(a.act_a, a.act_a_lo, a.fmt, idx, xv[i] * w);
-    }
-    emit_ss(xv, row0, a.ss_x, a.nch, sm);
-  }
-  // taps of the new context rows (rows >= n_new are zero)
-  const int nn = min(max(a.n_new[r], 0), kB);
-  const int KT = a.n_taps * a.H;
-#pragma unroll
-  for (int j = 0; j < kB; ++j) {
-    const size_t idx = static_cast<size_t>(row0 + j) * KT + c;
-    put_act(a.act_taps, a.act_taps_lo, a.fmt, idx, (j < nn) ? a.taps[idx] : 0.f);
+    const int id = (i == 0) ? anchor : a.mask_id;
+    const float xv = bf16_to_f32(a.embed[static_cast<size_t>(id) * a.H + c]);
+    const size_t idx = static_cast<size_t>(row) * a.H + c;
+    a.x[idx] = xv;
+    put_act(a.act_a, a.act_a_lo, a.fmt, idx, xv * bf16_to_f32(a.norm_w[c]));
+    emit_ss(xv, row, a.ss_x, a.nch);
+  } else {
+    const int c = (blockIdx.y - ny) * kCw + (threadIdx.x & 31);
+    const int nn = min(max(a.n_new[r], 0), kB);  // rows >= n_new are zero
+    const size_t idx = static_cast<size_t>(row) * (a.n_taps * a.H) + c;
+    put_act(a.act_taps, a.act_taps_lo, a.fmt, idx, (i < nn) ? a.taps[idx] : 0.f);
   }
 }
 
 // ------------------------------------------------------------------ taps projection finish
 // c = y * w_hidden_norm into the context rows of the QKV input (1/rms of y is
 // applied after the K/V projection); ss of y.
-__global__ void __launch_bounds__(kCh) fc_finish_kernel(const FcFinishArgs a) {
-  __shared__ float sm[4 * kB];
+__global__ void __launch_bounds__(kThreads) fc_finish_kernel(const FcFinishArgs a) {
   pdl_begin();
-  const int r = blockIdx.x;
-  const int c = blockIdx.y * kCh + threadIdx.x;
-  const int row0 = r * kB;
-  const float w = bf16_to_f32(a.norm_w[c]);
-  float yv[kB];
-  const size_t plane = static_cast<size_t>(a.n_rows) * a.H;
-#pragma unroll
-  for (int j = 0; j < kB; ++j) {
-    float y = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) y += a.y[sp * plane + static_cast<size_t>(row0 + j) * a.H + c];
-    yv[j] = y;
-    put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(a.act_row0 + row0 + j) * a.H + c, yv[j] * w);
-  }
-  emit_ss(yv, row0, a.ss, a.nch, sm);
+  const int row = blockIdx.x * kB + (threadIdx.x >> 5);
+  const int c = blockIdx.y * kCw + (threadIdx.x & 31);
+  const float y = plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, a.splits);
+  put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(a.act_row0 + row) * a.H + c, y * bf16_to_f32(a.norm_w[c]));
+  emit_ss(y, row, a.ss, a.nch);
 }
 
 // ------------------------------------------------------------------ conv before a sublayer
 // r_i = 1/rms(x_i); delta = r_i * (W_delta (x_i * w)) for all four (io, tap) rows;
 // a_i = r_i x_i w;  a'_i = (b0 + d0_i) a_i + (b1 + d1_i) a_{i-1}.
-__global__ void __launch_bounds__(kCh) conv_in_kernel(const ConvInArgs a) {
-  __shared__ float dsh[kB][2][kCh / 16];  // [row][tap][local group] of the conv before the sublayer
-  __shared__ float rr[kB];
+__global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
+  __shared__ float ash[kB][kCw];
   pdl_begin();
-  const int r = blockIdx.x;
-  const int c = blockIdx.y * kCh + threadIdx.x;
-  const int row0 = r * kB;
+  const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kB + i;
+  const int c = blockIdx.y * kCw + lane;
   const int G = a.H / 16;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int i = wid; i < kB; i += kCh / 32) {
-    const float v = warp_inv_rms(a.ss, row0 + i, a.nch, a.H, a.eps);
-    if (lane == 0) rr[i] = v;
+  const float rr = warp_inv_rms(a.ss, row, a.nch, a.H, a.eps);
+  // lanes 0..7: the (io, tap, local group) delta values of this row and the CTA's 2 groups
+  float dv = 0.f;
+  if (lane < 8) {
+    const int io = lane >> 2, t = (lane >> 1) & 1, gl = lane & 1;
+    const int gidx = (io * 2 + t) * G + blockIdx.y * 2 + gl;
+    dv = plane_sum(a.dproj + static_cast<size_t>(row) * (4 * G) + gidx, static_cast<size_t>(a.n_rows) * (4 * G),
+                   a.splits) * rr;
+    a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
   }
+  const int gl = lane >> 4;
+  const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 2 + gl);
+  const size_t idx = static_cast<size_t>(row) * a.H + c;
+  const float ai = a.x[idx] * rr * bf16_to_f32(a.norm_w[c]);
+  ash[i][lane] = ai;
   __syncthreads();
-  // 8 rows x 4 (io, tap) x 8 local groups = 256 delta values, 2 per thread
-  for (int e = threadIdx.x; e < kB * 32; e += kCh) {
-    const int i = e >> 5, io = (e >> 4) & 1, t = (e >> 3) & 1, gl = e & 7;
-    const int gidx = (io * 2 + t) * G + blockIdx.y * (kCh / 16) + gl;
-    const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
-    float dsum = 0.f;
-#pragma unroll 4
-    for (int sp = 0; sp < a.splits; ++sp) dsum += a.dproj[sp * plane + static_cast<size_t>(row0 + i) * (4 * G) + gidx];
-    const float d = dsum * rr[i];
-    if (io == 0) dsh[i][t][gl] = d;
-    a.delta[static_cast<size_t>(row0 + i) * (4 * G) + gidx] = d;
-  }
-  __syncthreads();
-  const int gl = threadIdx.x >> 4;
-  const float w = bf16_to_f32(a.norm_w[c]);
+  const float prev = i > 0 ? ash[i - 1][lane] : 0.f;
   const float b0 = bf16_to_f32(a.base[c]), b1 = bf16_to_f32(a.base[a.H + c]);
-  float prev = 0.f;
-#pragma unroll
-  for (int i = 0; i < kB; ++i) {
-    const size_t idx = static_cast<size_t>(row0 + i) * a.H + c;
-    const float ai = a.x[idx] * rr[i] * w;
-    put_act(a.act, a.act_lo, a.fmt, idx, (b0 + dsh[i][0][gl]) * ai + (b1 + dsh[i][1][gl]) * prev);
-    prev = ai;
-  }
+  put_act(a.act, a.act_lo, a.fmt, idx, (b0 + d0) * ai + (b1 + d1) * prev);
 }
 
 // ------------------------------------------------------------------ conv after a sublayer + residual
 // y = sum of split planes; x_i += (b2 + d2_i) y_i + (b3 + d3_i) y_{i-1} (the
 // convolution wrapping the sublayer's output); act = x * w_next; ss of x.
-__global__ void __launch_bounds__(kCh) conv_out_kernel(const ConvOutArgs a) {
-  __shared__ float sm[4 * kB];
+__global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a) {
+  __shared__ float ysh[kB][kCw];
   pdl_begin();
-  const int r = blockIdx.x;
-  const int c = blockIdx.y * kCh + threadIdx.x;
-  const int row0 = r * kB;
+  const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kB + i;
+  const int c = blockIdx.y * kCw + lane;
   const int G = a.H / 16;
   const int g = c >> 4;
-  const size_t plane = static_cast<size_t>(a.n_rows) * a.H;
+  const size_t idx = static_cast<size_t>(row) * a.H + c;
+  const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, a.splits);
+  ysh[i][lane] = y;
+  __syncthreads();
+  const float yprev = i > 0 ? ysh[i - 1][lane] : 0.f;
+  const float* d = a.delta + static_cast<size_t>(row) * (4 * G);
   const float b2 = bf16_to_f32(a.base[2 * a.H + c]), b3 = bf16_to_f32(a.base[3 * a.H + c]);
+  const float xv = a.x[idx] + (b2 + d[2 * G + g]) * y + (b3 + d[3 * G + g]) * yprev;
+  a.x[idx] = xv;
   const float w = bf16_to_f32(a.norm_w[c]);
-  float y[kB];
-#pragma unroll
-  for (int i = 0; i < kB; ++i) y[i] = 0.f;
-  for (int sp = 0; sp < a.splits; ++sp) {  // split planes in order; the 8 rows' loads are independent
-#pragma unroll
-    for (int i = 0; i < kB; ++i) y[i] += a.part[sp * plane + static_cast<size_t>(row0 + i) * a.H + c];
-  }
-  float xv[kB];
-#pragma unroll
-  for (int i = 0; i < kB; ++i) {
-    const float* d = a.delta + static_cast<size_t>(row0 + i) * (4 * G);
-    const float yprev = i > 0 ? y[i - 1] : 0.f;
-    const size_t idx = static_cast<size_t>(row0 + i) * a.H + c;
-    xv[i] = a.x[idx] + (b2 + d[2 * G + g]) * y[i] + (b3 + d[3 * G + g]) * yprev;
-    a.x[idx] = xv[i];
-    put_act(a.act, a.act_lo, a.fmt, idx, xv[i] * w);
-    if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, idx, xv[i] * w);
-  }
-  emit_ss(xv, row0, a.ss, a.nch, sm);
+  put_act(a.act, a.act_lo, a.fmt, idx, xv * w);
+  if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, idx, xv * w);
+  emit_ss(xv, row, a.ss, a.nch);
 }
 
 // ------------------------------------------------------------------ SwiGLU
 // h = silu(gate) * up from the split planes of the two projections.
-__global__ void __launch_bounds__(kCh) swiglu_kernel(const SwigluArgs a) {
+__global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
   pdl_begin();
-  const int r = blockIdx.x;
-  const int c = blockIdx.y * kCh + threadIdx.x;
-  const int row0 = r * kB;
+  const int row = blockIdx.x * kB + (threadIdx.x >> 5);
+  const int c = blockIdx.y * kCw + (threadIdx.x & 31);
+  const size_t idx = static_cast<size_t>(row) * a.F + c;
   const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
-  float gs[kB], us[kB];
-#pragma unroll
-  for (int i = 0; i < kB; ++i) gs[i] = us[i] = 0.f;
-  for (int sp = 0; sp < a.splits; ++sp) {
-#pragma unroll
-    for (int i = 0; i < kB; ++i) {
-      gs[i] += a.part_g[sp * plane + static_cast<size_t>(row0 + i) * a.F + c];
-      us[i] += a.part_u[sp * plane + static_cast<size_t>(row0 + i) * a.F + c];
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kB; ++i)
-    put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(row0 + i) * a.F + c, gs[i] / (1.f + __expf(-gs[i])) * us[i]);
+  const float gs = plane_sum(a.part_g + idx, plane, a.splits);
+  const float us = plane_sum(a.part_u + idx, plane, a.splits);
+  put_act(a.act, a.act_lo, a.fmt, idx, gs / (1.f + __expf(-gs)) * us);
 }
 
 // ------------------------------------------------------------------ q/k norm, RoPE, cache append
@@ -249,9 +206,16 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
     plane = static_cast<size_t>(2 * a.n_rows) * nkv * 128;
   }
   float v[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int sp = 0; sp < a.splits; ++sp)  // split planes in order
+  for (int sp = 0; sp < a.splits; sp += 2) {  // split planes in order, two planes' loads at a time
+    float t[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] += src[sp * plane + lane + 32 * c];
+    for (int c = 0; c < 4; ++c) {
+      t[c] = src[sp * plane + lane + 32 * c];
+      t[4 + c] = (sp + 1 < a.splits) ? src[(sp + 1) * plane + lane + 32 * c] : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = (v[c] + t[c]) + t[4 + c];
+  }
   if (ctx_row) {
     const float rc = warp_inv_rms(a.ss_c, row0 + jj, a.nch, a.H, a.eps);
 #pragma unroll
@@ -293,19 +257,19 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
 }  // namespace
 
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(start_kernel, dim3(n_req, (a.n_taps * a.H) / kCh), dim3(kCh), 0, st, pdl, a);
+  return launch_ex(start_kernel, dim3(n_req, (a.H + a.n_taps * a.H) / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(fc_finish_kernel, dim3(n_req, a.H / kCh), dim3(kCh), 0, st, pdl, a);
+  return launch_ex(fc_finish_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(conv_in_kernel, dim3(n_req, a.H / kCh), dim3(kCh), 0, st, pdl, a);
+  return launch_ex(conv_in_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(conv_out_kernel, dim3(n_req, a.H / kCh), dim3(kCh), 0, st, pdl, a);
+  return launch_ex(conv_out_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(swiglu_kernel, dim3(n_req, a.F / kCh), dim3(kCh), 0, st, pdl, a);
+  return launch_ex(swiglu_kernel, dim3(n_req, a.F / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st) {
   const int n_items = kB * a.n_q_heads + 4 * kB * a.n_kv_heads;

@@ -19,7 +19,7 @@ struct StartArgs {
   float* x;                // residual stream [N][H]
   void* act_a;             // x * w: input of layer 0's delta projection [N][H]
   size_t act_a_lo;
-  float* ss_x;             // [N][H/128]
+  float* ss_x;             // [N][H/32]
   void* act_taps;          // [N][n_taps*H]
   size_t act_taps_lo;
   int H, n_taps, mask_id, nch, fmt, V;
@@ -30,7 +30,7 @@ struct FcFinishArgs {
   const uint16_t* norm_w;  // hidden_norm
   void* act;               // QKV input; context rows start at act_row0
   size_t act_lo;
-  float* ss;               // [N][H/128] sums of squares of y
+  float* ss;               // [N][H/32] sums of squares of y
   int H, act_row0, nch, fmt, splits, n_rows;
 };
 
@@ -58,7 +58,7 @@ struct ConvOutArgs {
   size_t act_lo;
   uint16_t* act2;          // optional bf16 copy (LM-head input), or null
   size_t act2_lo;
-  float* ss;               // [N][H/128] sums of squares of the updated x
+  float* ss;               // [N][H/32] sums of squares of the updated x
   int H, nch, fmt, splits, n_rows;
 };
 
