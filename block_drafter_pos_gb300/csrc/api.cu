@@ -32,6 +32,12 @@ struct dflash2_handle {
   int n_attn_chunks, n_verify_chunks, lm_ctas;
   // K splits of each projection (fixed at create from the grid size)
   int s_fc, s_delta, s_qkv, s_o, s_gu, s_down, s_sel;
+  // tensor maps of the projection matrices (bulk-copy descriptors, encoded at create)
+  CUtensorMap map_fc, map_sel;
+  CUtensorMap map_layer[DFLASH2_MAX_LAYERS][9];  // q k v o gate up down attn_delta mlp_delta
+  // activation-buffer maps (hi rows then lo rows), encoded once the scratch exists
+  CUtensorMap xm_taps, xm_a, xm_qkv, xm_o, xm_h, xm_fin;
+  int* gemv_err;  // device word set by a GEMV whose pipeline wait gave up
   // scratch
   char* arena;
   size_t arena_bytes;
@@ -60,16 +66,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // One projection segment: out[s] = W[:, split s] X[:, split s]^T for the
 // 8 * n_tiles activation rows starting at x.
-GemvSeg seg(const dflash2_matrix& m, const void* x, size_t xlo, int ldx, int n_tiles, int M, int K, int splits,
-            float* out) {
+enum { kQ, kK, kV, kO, kGate, kUp, kDown, kAttnDelta, kMlpDelta };
+
+// x_rows: rows of one plane of the activation buffer behind xmap (its lo plane starts there).
+GemvSeg seg(const CUtensorMap& wmap, const dflash2_matrix& m, const CUtensorMap& xmap, int x_rows, int n_tiles, int M,
+            int K, int splits, float* out) {
   GemvSeg s;
   memset(&s, 0, sizeof(s));
-  s.w = m.w;
+  s.wmap = wmap;
+  s.xmap = xmap;
+  s.x_lo_row = x_rows;
   s.scale = static_cast<const uint16_t*>(m.scale);
   s.bias = static_cast<const uint16_t*>(m.bias);
-  s.x = x;
-  s.xlo_off = xlo;
-  s.ldx = ldx;
   s.M = M;
   s.K = K;
   s.n_tiles = n_tiles;
@@ -86,6 +94,7 @@ dflash2_status run_gemv(dflash2_handle* h, std::initializer_list<GemvSeg> segs, 
     a.seg[a.nseg++] = s;
     max_tiles = std::max(max_tiles, s.n_tiles);
   }
+  a.err = h->gemv_err;
   DF2_CHECK(launch_gemv(a, h->fmt, max_tiles, h->num_sms, h->pdl, st));
   h->launches += 1;
   return DFLASH2_OK;
@@ -93,7 +102,8 @@ dflash2_status run_gemv(dflash2_handle* h, std::initializer_list<GemvSeg> segs, 
 
 bool valid_matrix(const dflash2_matrix& m, int fmt) {
   if (!m.w || !aligned16(m.w)) return false;
-  if (fmt == DFLASH2_WEIGHTS_Q8G64 && (!m.scale || !m.bias)) return false;
+  // Q8 scale/bias rows are read 8 groups (16 bytes) at a time
+  if (fmt == DFLASH2_WEIGHTS_Q8G64 && (!m.scale || !m.bias || !aligned16(m.scale) || !aligned16(m.bias))) return false;
   return true;
 }
 
@@ -124,7 +134,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   if (c.weight_format != DFLASH2_WEIGHTS_BF16 && c.weight_format != DFLASH2_WEIGHTS_Q8G64) return DFLASH2_E_INVAL;
   if (c.head_dim != 128 || c.block != 8 || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
       c.conv_group != 16 || c.n_layers > DFLASH2_MAX_LAYERS || c.n_q_heads != 4 * c.n_kv_heads ||
-      c.hidden % 128 || c.ffn % 128 || c.vocab % 16 || max_requests > 4 ||
+      c.hidden % 256 || c.ffn % 128 || c.vocab % 16 || max_requests > 4 ||
       (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1 > 64)
     return DFLASH2_E_UNSUPPORTED;
   const int fmt = c.weight_format;
@@ -168,13 +178,34 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
   h->lm_ctas = h->num_sms;  // one 16-warp CTA per SM (the kernel needs 128 registers a thread)
   // K splits by total 16-row tiles of each launch (independent of the request count)
-  h->s_fc = gemv_choose_splits(h->H / 16, h->KT, h->num_sms);
-  h->s_delta = gemv_choose_splits(4 * h->G / 16, h->H, h->num_sms);
-  h->s_qkv = gemv_choose_splits((h->qd + 2 * h->kvd) / 16, h->H, h->num_sms);
-  h->s_o = gemv_choose_splits(h->H / 16, h->qd, h->num_sms);
-  h->s_gu = gemv_choose_splits(2 * h->F / 16, h->H, h->num_sms);
-  h->s_down = gemv_choose_splits(h->H / 16, h->F, h->num_sms);
-  h->s_sel = gemv_choose_splits(c.rank / 16, h->H, h->num_sms);
+  {
+    // K splits by 64-row weight blocks and the size of one output plane at max_requests
+    const double N8 = 8.0 * max_requests, fb = 4.0;
+    h->s_fc = gemv_choose_splits(h->H / 64, h->KT, N8 * h->H * fb, h->num_sms, fmt);
+    h->s_delta = gemv_choose_splits(4 * h->G / 64, h->H, N8 * 4 * h->G * fb, h->num_sms, fmt);
+    h->s_qkv = gemv_choose_splits((h->qd + 2 * h->kvd) / 64, h->H, N8 * (h->qd + 4 * h->kvd) * fb, h->num_sms, fmt);
+    h->s_o = gemv_choose_splits(h->H / 64, h->qd, N8 * h->H * fb, h->num_sms, fmt);
+    h->s_gu = gemv_choose_splits(2 * h->F / 64, h->H, N8 * 2 * h->F * fb, h->num_sms, fmt);
+    h->s_down = gemv_choose_splits(h->H / 64, h->F, N8 * h->H * fb, h->num_sms, fmt);
+    h->s_sel = gemv_choose_splits(c.rank / 64, h->H, N8 * c.rank * fb, h->num_sms, fmt);
+  }
+  bool maps_ok = h->s_fc && h->s_delta && h->s_qkv && h->s_o && h->s_gu && h->s_down && h->s_sel;
+  maps_ok = maps_ok && gemv_encode_wmap(&h->map_fc, w->fc.w, h->H, h->KT, fmt) &&
+            gemv_encode_wmap(&h->map_sel, w->sel_proj.w, c.rank, h->H, fmt);
+  for (int l = 0; l < c.n_layers && maps_ok; ++l) {
+    const dflash2_layer_weights& L = w->layers[l];
+    const struct {
+      const dflash2_matrix* m;
+      int M, K;
+    } mats[9] = {{&L.q, h->qd, h->H},        {&L.k, h->kvd, h->H},     {&L.v, h->kvd, h->H},
+                 {&L.o, h->H, h->qd},        {&L.gate, h->F, h->H},    {&L.up, h->F, h->H},
+                 {&L.down, h->H, h->F},      {&L.attn_delta, 4 * h->G, h->H}, {&L.mlp_delta, 4 * h->G, h->H}};
+    for (int i = 0; i < 9 && maps_ok; ++i) maps_ok = gemv_encode_wmap(&h->map_layer[l][i], mats[i].m->w, mats[i].M, mats[i].K, fmt);
+  }
+  if (!maps_ok) {
+    delete h;
+    return DFLASH2_E_UNSUPPORTED;
+  }
   const size_t N = 8 * static_cast<size_t>(max_requests);
   const size_t esz = 2;  // bf16 / fp16 activations
   struct Buf {
@@ -211,6 +242,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->vstats),
        static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
       {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
+      {reinterpret_cast<void**>(&h->gemv_err), 4},
   };
   h->lo_a = N * h->H;
   h->lo_qkv = 2 * N * h->H;
@@ -237,6 +269,18 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
     cudaFree(h->arena);
     delete h;
     return DFLASH2_E_CUDA;
+  }
+  // activation maps: one per GEMV input buffer (rows of one plane; the lo plane follows)
+  const bool xok = gemv_encode_xmap(&h->xm_taps, h->act_taps, static_cast<int>(N), h->KT, fmt) &&
+                   gemv_encode_xmap(&h->xm_a, h->act_a, static_cast<int>(N), h->H, fmt) &&
+                   gemv_encode_xmap(&h->xm_qkv, h->act_qkv, static_cast<int>(2 * N), h->H, fmt) &&
+                   gemv_encode_xmap(&h->xm_o, h->act_o, static_cast<int>(N), h->qd, fmt) &&
+                   gemv_encode_xmap(&h->xm_h, h->act_h, static_cast<int>(N), h->F, fmt) &&
+                   (fmt != 0 || gemv_encode_xmap(&h->xm_fin, h->act_fin, static_cast<int>(N), h->H, 0));
+  if (!xok) {
+    cudaFree(h->arena);
+    delete h;
+    return DFLASH2_E_UNSUPPORTED;
   }
   *out = h;
   return DFLASH2_OK;
@@ -282,6 +326,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   const int N = 8 * R;
   const int H = h->H, G = h->G;
   const size_t layer_stride = static_cast<size_t>(h->max_req) * h->kv_cap * h->kvd;  // elements
+  const int N8 = 8 * h->max_req;  // rows of one plane of each activation buffer
   // ---- a2: block embedding, first norm input, taps packing
   {
     StartArgs a;
@@ -308,7 +353,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // ---- a1: taps projection fc [H][n_taps H], then hidden_norm input of the context rows
   {
     dflash2_status s =
-        run_gemv(h, {seg(h->w.fc, h->act_taps, h->lo_taps, h->KT, R, H, h->KT, h->s_fc, h->fc_out)}, st);
+        run_gemv(h, {seg(h->map_fc, h->w.fc, h->xm_taps, N8, R, H, h->KT, h->s_fc, h->fc_out)}, st);
     if (s) return s;
     FcFinishArgs a;
     a.y = h->fc_out;
@@ -331,7 +376,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     uint16_t* vc = static_cast<uint16_t*>(v_cache) + l * layer_stride;
     // ---- a3: delta projection of the normed input, conv-in
     dflash2_status s =
-        run_gemv(h, {seg(L.attn_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->s_delta, h->dproj)}, st);
+        run_gemv(h, {seg(h->map_layer[l][kAttnDelta], L.attn_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
@@ -354,9 +399,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     }
     // ---- a4: q (block rows), k and v (block + new context rows)
     s = run_gemv(h,
-                 {seg(L.q, h->act_qkv, h->lo_qkv, H, R, h->qd, H, h->s_qkv, h->q_out),
-                  seg(L.k, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->s_qkv, h->k_out),
-                  seg(L.v, h->act_qkv, h->lo_qkv, H, 2 * R, h->kvd, H, h->s_qkv, h->v_out)},
+                 {seg(h->map_layer[l][kQ], L.q, h->xm_qkv, 2 * N8, R, h->qd, H, h->s_qkv, h->q_out),
+                  seg(h->map_layer[l][kK], L.k, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->s_qkv, h->k_out),
+                  seg(h->map_layer[l][kV], L.v, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->s_qkv, h->v_out)},
                  st);
     if (s) return s;
     {
@@ -409,7 +454,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       h->launches += 2;
     }
     // ---- a6: output projection, conv-out + residual, post-attention norm input
-    s = run_gemv(h, {seg(L.o, h->act_o, h->lo_o, h->qd, R, H, h->qd, h->s_o, h->ypart)}, st);
+    s = run_gemv(h, {seg(h->map_layer[l][kO], L.o, h->xm_o, N8, R, H, h->qd, h->s_o, h->ypart)}, st);
     if (s) return s;
     {
       ConvOutArgs a;
@@ -432,7 +477,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       h->launches++;
     }
     // ---- a7: MLP sublayer
-    s = run_gemv(h, {seg(L.mlp_delta, h->act_a, h->lo_a, H, R, 4 * G, H, h->s_delta, h->dproj)}, st);
+    s = run_gemv(h, {seg(h->map_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
@@ -454,8 +499,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       h->launches++;
     }
     s = run_gemv(h,
-                 {seg(L.gate, h->act_qkv, h->lo_qkv, H, R, h->F, H, h->s_gu, h->gpart),
-                  seg(L.up, h->act_qkv, h->lo_qkv, H, R, h->F, H, h->s_gu, h->upart)},
+                 {seg(h->map_layer[l][kGate], L.gate, h->xm_qkv, 2 * N8, R, h->F, H, h->s_gu, h->gpart),
+                  seg(h->map_layer[l][kUp], L.up, h->xm_qkv, 2 * N8, R, h->F, H, h->s_gu, h->upart)},
                  st);
     if (s) return s;
     {
@@ -471,7 +516,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       DF2_CHECK(launch_swiglu(a, R, pdl, st));
       h->launches++;
     }
-    s = run_gemv(h, {seg(L.down, h->act_h, h->lo_h, h->F, R, H, h->F, h->s_down, h->ypart)}, st);
+    s = run_gemv(h, {seg(h->map_layer[l][kDown], L.down, h->xm_h, N8, R, H, h->F, h->s_down, h->ypart)}, st);
     if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
@@ -519,10 +564,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   }
   // ---- a9: selector projection (same final hidden, in the matrix's format), merge top-16
   {
-    const void* xin = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
-    const size_t xlo = fmt == 0 ? h->lo_fin : h->lo_a;
-    dflash2_status s =
-        run_gemv(h, {seg(h->w.sel_proj, xin, xlo, H, R, c.rank, H, h->s_sel, h->sel_out)}, st);
+    const CUtensorMap& xin = fmt == 0 ? h->xm_fin : h->xm_a;  // same final hidden, in the matrix's format
+    dflash2_status s = run_gemv(h, {seg(h->map_sel, h->w.sel_proj, xin, N8, R, c.rank, H, h->s_sel, h->sel_out)}, st);
     if (s) return s;
     TopkMergeArgs a;
     a.part_keys = h->topk_keys;

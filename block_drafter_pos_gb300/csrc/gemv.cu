@@ -3,28 +3,41 @@
 //
 // Design (sm_103a):
 //  * The weights are read exactly once per step, so the kernel is bound by HBM
-//    bandwidth.  A work unit is a 16-row weight tile times one K split; every warp
-//    of a persistent grid (one 16-warp CTA per SM) walks its units grid-stride, the
-//    warps of one CTA on consecutive tiles of the same split.  One lane streams 16
-//    contiguous bytes of a weight row per load (ld.global.nc.L1::no_allocate.v4)
-//    straight into mma.sync m16n8k16 as the A operand.  The order of the K sum
-//    inside one MMA is free, so the physical K positions a lane holds fill the
-//    MMA's logical K slots and the activation (B) fragment is loaded with the same
-//    permutation.
-//  * Weight loads run one batch (4 x 32 K) ahead of the MMAs; independent
-//    accumulator chains keep the MMA dependency latency off the critical path.
-//  * Each split's partial goes to its own output plane with plain stores (no
-//    fences or atomics on the streaming path); the consumer kernel adds the planes
-//    in split order, so every result is bit-reproducible.  The split count comes
-//    from a cost model over the grid (gemv_choose_splits).
-//  * Activations may carry a low-order plane (x = hi + lo) for ~16-bit accuracy.
-//  * Programmatic dependent launch: the first weight loads are issued before
-//    griddepcontrol.wait, so the weight stream starts while the previous kernel
-//    drains.
+//    bandwidth; what it needs is enough bytes in flight to cover HBM latency and
+//    no other long-latency load on the consumers' path.
+//  * A work unit is a 64-row weight block times one K split.  Each CTA (two per
+//    SM) walks its units grid-stride with one producer warp and four consumer
+//    warps.  The producer fills a ring of shared-memory stages with bulk tensor
+//    copies (cp.async.bulk.tensor) completing on the stage's "full" mbarrier: 64
+//    weight rows x 128 K (64-byte rows, 64-byte swizzle), plus the matching
+//    activation slice, both planes, in 8-row boxes.  The consumers release a stage
+//    through its "empty" mbarrier.  The weight copies of the first stages are
+//    issued before griddepcontrol.wait (weights never depend on the previous
+//    kernel); the activation copies after it.
+//  * Each consumer warp owns 16 of the 64 rows: mma.sync m16n8k16 with the weights
+//    as the A operand.  The order of the K sum inside one MMA is free: a lane
+//    reads 8 consecutive K of rows g and g + 8 and of activation row g (16-byte
+//    shared-memory loads, bank-conflict-free under the swizzle), so A and B agree
+//    on which K each MMA slot holds.
+//  * Each split's partial goes to its own output plane with plain stores; the
+//    consumer kernel adds the planes in split order, so every result is
+//    bit-reproducible.  The split count comes from a cost model over the grid
+//    (gemv_choose_splits).
+//  * Activations carry a low-order plane (x = hi + lo) for ~16-bit accuracy, with
+//    independent accumulator chains for the two planes.
 //  * Q8/group64 ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias per
-//    group of 64): codes are exact in fp16; each group is one fp16 MMA chain from
-//    zero, folded as scale * (sum q x) + bias * (sum x), with sum x taken by one
-//    more MMA chain against a row of ones.
+//    group of 64 along K, bf16 scale and bias): the int8 codes become exact fp16
+//    values by a byte permute against the 1024 exponent, and the affine map is
+//    applied in fp16 (w = q * s + b, one fused multiply-add per pair).  A group's
+//    scale and bias are loaded one stage ahead.  The fp16 activation slice uses
+//    128-byte rows (64 K, 128-byte swizzle) so a lane's 16 consecutive K are two
+//    conflict-free loads.
+//  * Every mbarrier wait is bounded; a wait that gives up sets the error word, and
+//    the producer lets its outstanding copies land (again bounded) before exiting.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,8 +45,80 @@ namespace df2 {
 
 namespace {
 
-constexpr int kWarpsPerCta = 16;
-constexpr int kKStep = 128;  // K elements per batch (4 x 32)
+constexpr int kConsumers = 4;        // consumer warps per CTA (16 weight rows each)
+constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kCtasPerSm = 2;
+constexpr int kBlockRows = 64;       // weight rows per unit
+constexpr int kRingBudget = 100 * 1024;
+constexpr long long kSpinLimit = 1ll << 22;
+
+// Shared-memory geometry of one stage for a format and a number of 8-row activation tiles.
+template <int FMT, int NT>
+struct StageGeo {
+  static constexpr int kWBytes = FMT == 0 ? 16384 : 8192;  // 64 rows x 128 K
+  static constexpr int kXPlane = 2048 * NT;                 // 8*NT rows x 128 K x 2 B
+  static constexpr int kBytes = kWBytes + 2 * kXPlane;
+  static constexpr int kDepthRaw = kRingBudget / kBytes;
+  static constexpr int kDepth = kDepthRaw < 2 ? 2 : (kDepthRaw > 6 ? 6 : kDepthRaw);
+  static constexpr int kSmem = kDepth * kBytes + 1024;  // + slack for 1 KB alignment
+};
+
+DF2_DEV uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+DF2_DEV void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+DF2_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase of the given parity; false if it did not complete.
+DF2_DEV bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+DF2_DEV uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+DF2_DEV uint64_t evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+DF2_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+DF2_DEV uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
+DF2_DEV void mbar_init_count(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+DF2_DEV void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 
 DF2_DEV int find_seg(const GemvArgs& a, int u) {
   int s = 0;
@@ -43,13 +128,44 @@ DF2_DEV int find_seg(const GemvArgs& a, int u) {
   return s;
 }
 
+// Walks one CTA's (unit, stage) sequence: units blockIdx.x, + gridDim.x, ...
+struct Cursor {
+  int u, st, seg, row0, k0, split, nst;
+  bool valid;
+  DF2_DEV void load(const GemvArgs& a) {
+    valid = u < a.total_units;
+    if (!valid) return;
+    seg = find_seg(a, u);
+    const GemvSeg& sg = a.seg[seg];
+    const int local = u - sg.unit_begin;
+    const int blocks = sg.M / kBlockRows;
+    split = local / blocks;
+    row0 = (local % blocks) * kBlockRows;
+    const int kchunk = sg.K / sg.splits;
+    k0 = split * kchunk;
+    nst = kchunk / kGemvStageK;
+    st = 0;
+  }
+  DF2_DEV void start(const GemvArgs& a) {
+    u = blockIdx.x;
+    load(a);
+  }
+  DF2_DEV void next(const GemvArgs& a) {
+    if (++st == nst) {
+      u += gridDim.x;
+      load(a);
+    }
+  }
+  DF2_DEV int kabs() const { return k0 + st * kGemvStageK; }
+};
+
 template <int NT>
-DF2_DEV void store_tile(const GemvSeg& sg, int split, int row0, int nt, const float (&acc)[NT][4], int lane) {
+DF2_DEV void store_tile(const GemvSeg& sg, int split, int row0, const float (&acc)[NT][4], int lane) {
   const int g = lane >> 2, q = lane & 3;
   float* out = sg.out + static_cast<size_t>(split) * (sg.n_tiles * 8) * sg.M;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    if (t < nt) {
+    if (t < sg.n_tiles) {
       const int n0 = t * 8 + 2 * q;
       out[static_cast<size_t>(n0) * sg.M + row0 + g] = acc[t][0];
       out[static_cast<size_t>(n0 + 1) * sg.M + row0 + g] = acc[t][1];
@@ -59,236 +175,313 @@ DF2_DEV void store_tile(const GemvSeg& sg, int split, int row0, int nt, const fl
   }
 }
 
-// ------------------------------------------------------------------ BF16 weights
+// BF16 stage: weights 4 boxes [32 K][64 rows] (4 KB each); activations per tile
+// and plane 4 boxes [32 K][8 rows] (512 B each).  wa: this lane's row g in box 0;
+// xa: this lane's row g in tile 0, box 0, hi plane.
 template <int NT>
-__global__ void __launch_bounds__(kWarpsPerCta * 32) gemv_bf16_kernel(const __grid_constant__ GemvArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int warp = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int nwarps = gridDim.x * kWarpsPerCta;
-  const int g = lane >> 2, q = lane & 3;
-#ifndef DF2_GEMV_NO_PDL
-  pdl_trigger();
-  bool waited = false;
-#endif
-  for (int u = warp; u < a.total_units; u += nwarps) {
-    const GemvSeg& sg = a.seg[find_seg(a, u)];
-    const int local = u - sg.unit_begin;
-    const int tiles = sg.M >> 4;
-    const int tile = local % tiles, split = local / tiles;
-    const int kchunk = sg.K / sg.splits;
-    const int k0 = split * kchunk;
-    const int row0 = tile * 16;
-    const int nt = sg.n_tiles;
-    const __nv_bfloat16* w0 =
-        reinterpret_cast<const __nv_bfloat16*>(sg.w) + static_cast<size_t>(row0 + g) * sg.K + k0 + 8 * q;
-    const __nv_bfloat16* w1 = w0 + static_cast<size_t>(8) * sg.K;
-    const __nv_bfloat16* xb =
-        reinterpret_cast<const __nv_bfloat16*>(sg.x) + static_cast<size_t>(g) * sg.ldx + k0 + 8 * q;
-    const size_t xlo = sg.xlo_off;
-    // independent chains: (hi, lo plane) x (first, second 16 K of a 32 step)
-    float acc[NT][4], acc2[NT][4], acc3[NT][4], acc4[NT][4];
+DF2_DEV void stage_bf16(int n_tiles, uint32_t wa, uint32_t xa, float (&c0)[NT][4], float (&c1)[NT][4],
+                        float (&c2)[NT][4], float (&c3)[NT][4]) {
+  constexpr int kXPlane = 2048 * NT;
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
+  for (int b = 0; b < 4; ++b) {
+    const uint4 a0 = lds128(wa + b * 4096);        // row g
+    const uint4 a1 = lds128(wa + b * 4096 + 512);  // row g + 8
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[t][e] = acc2[t][e] = acc3[t][e] = acc4[t][e] = 0.f;
-    uint4 ra[4], rb[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      ra[j] = ld_stream(w0 + 32 * j);
-      rb[j] = ld_stream(w1 + 32 * j);
-    }
-#ifndef DF2_GEMV_NO_PDL
-    if (!waited) {  // weights are independent of earlier kernels; activations are not
-      pdl_wait();
-      waited = true;
-    }
-#endif
-    for (int k = 0; k < kchunk; k += kKStep) {
-      uint4 ca[4], cb[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ca[j] = ra[j];
-        cb[j] = rb[j];
-      }
-      if (k + kKStep < kchunk) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ra[j] = ld_stream(w0 + k + kKStep + 32 * j);
-          rb[j] = ld_stream(w1 + k + kKStep + 32 * j);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (t < nt) {
-          const __nv_bfloat16* xt = xb + static_cast<size_t>(t * 8) * sg.ldx + k;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 x = ld_cached(xt + 32 * j);
-            mma_bf16(acc[t], ca[j].x, cb[j].x, ca[j].y, cb[j].y, x.x, x.y);
-            mma_bf16(acc2[t], ca[j].z, cb[j].z, ca[j].w, cb[j].w, x.z, x.w);
-            if (xlo) {
-              const uint4 y = ld_cached(xt + xlo + 32 * j);
-              mma_bf16(acc3[t], ca[j].x, cb[j].x, ca[j].y, cb[j].y, y.x, y.y);
-              mma_bf16(acc4[t], ca[j].z, cb[j].z, ca[j].w, cb[j].w, y.z, y.w);
-            }
-          }
-        }
+    for (int t = 0; t < NT; ++t) {
+      if (t < n_tiles) {
+        const uint32_t xb = xa + (t * 4 + b) * 512;
+        const uint4 x = lds128(xb), y = lds128(xb + kXPlane);
+        mma_bf16(c0[t], a0.x, a1.x, a0.y, a1.y, x.x, x.y);
+        mma_bf16(c1[t], a0.z, a1.z, a0.w, a1.w, x.z, x.w);
+        mma_bf16(c2[t], a0.x, a1.x, a0.y, a1.y, y.x, y.y);
+        mma_bf16(c3[t], a0.z, a1.z, a0.w, a1.w, y.z, y.w);
       }
     }
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[t][e] = (acc[t][e] + acc2[t][e]) + (acc3[t][e] + acc4[t][e]);
-    store_tile<NT>(sg, split, row0, nt, acc, lane);
   }
-#ifndef DF2_GEMV_NO_PDL
-  if (!waited) pdl_wait();  // every CTA orders itself after the previous kernel
-#endif
 }
 
-// ------------------------------------------------------------------ Q8/group64 weights
-template <int NT>
-__global__ void __launch_bounds__(kWarpsPerCta * 32) gemv_q8_kernel(const __grid_constant__ GemvArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int warp = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int nwarps = gridDim.x * kWarpsPerCta;
-  const int g = lane >> 2, q = lane & 3;
-  const uint32_t one2 = 0x3C003C00u;  // half2(1, 1)
-#ifndef DF2_GEMV_NO_PDL
-  pdl_trigger();
-  bool waited = false;
-#endif
-  for (int u = warp; u < a.total_units; u += nwarps) {
-    const GemvSeg& sg = a.seg[find_seg(a, u)];
-    const int local = u - sg.unit_begin;
-    const int tiles = sg.M >> 4;
-    const int tile = local % tiles, split = local / tiles;
-    const int kchunk = sg.K / sg.splits;
-    const int k0 = split * kchunk;
-    const int row0 = tile * 16;
-    const int nt = sg.n_tiles;
-    const int KG = sg.K >> 6;
-    const int8_t* c0p = reinterpret_cast<const int8_t*>(sg.w) + static_cast<size_t>(row0 + g) * sg.K + k0 + 16 * q;
-    const int8_t* c1p = c0p + static_cast<size_t>(8) * sg.K;
-    const uint16_t* s0p = sg.scale + static_cast<size_t>(row0 + g) * KG + (k0 >> 6);
-    const uint16_t* b0p = sg.bias + static_cast<size_t>(row0 + g) * KG + (k0 >> 6);
-    const size_t rs8 = static_cast<size_t>(8) * KG;
-    const __half* xb = reinterpret_cast<const __half*>(sg.x) + static_cast<size_t>(g) * sg.ldx + k0 + 16 * q;
-    const size_t xlo = sg.xlo_off;
-    float acc[NT][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-    const int ngroups = kchunk >> 6;
-    uint4 rc0[2], rc1[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      rc0[j] = ld_stream(c0p + 64 * j);
-      rc1[j] = ld_stream(c1p + 64 * j);
-    }
-#ifndef DF2_GEMV_NO_PDL
-    if (!waited) {
-      pdl_wait();
-      waited = true;
-    }
-#endif
-    for (int gi = 0; gi < ngroups; gi += 2) {
-      uint4 cc0[2], cc1[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        cc0[j] = rc0[j];
-        cc1[j] = rc1[j];
-      }
-      if (gi + 2 < ngroups) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          rc0[j] = ld_stream(c0p + 64 * (gi + 2 + j));
-          rc1[j] = ld_stream(c1p + 64 * (gi + 2 + j));
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int grp = gi + j;
-        const float s0 = bf16_to_f32(__ldg(s0p + grp)), s1 = bf16_to_f32(__ldg(s0p + rs8 + grp));
-        const float b0 = bf16_to_f32(__ldg(b0p + grp)), b1 = bf16_to_f32(__ldg(b0p + rs8 + grp));
-        const uint32_t u0[4] = {cc0[j].x ^ 0x80808080u, cc0[j].y ^ 0x80808080u, cc0[j].z ^ 0x80808080u,
-                                cc0[j].w ^ 0x80808080u};
-        const uint32_t u1[4] = {cc1[j].x ^ 0x80808080u, cc1[j].y ^ 0x80808080u, cc1[j].z ^ 0x80808080u,
-                                cc1[j].w ^ 0x80808080u};
-        uint32_t A[4][4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          A[m][0] = codes_to_half2(u0[m], 0x4140);
-          A[m][1] = codes_to_half2(u1[m], 0x4140);
-          A[m][2] = codes_to_half2(u0[m], 0x4342);
-          A[m][3] = codes_to_half2(u1[m], 0x4342);
-        }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (t < nt) {
-            const __half* xt = xb + static_cast<size_t>(t * 8) * sg.ldx + 64 * grp;
-            const uint4 xa = ld_cached(xt);
-            const uint4 xc = ld_cached(xt + 8);
-            // independent chains: codes x hi, ones x hi (column sums), codes x lo, ones x lo
-            float cg[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
-            float cgl[4] = {0.f, 0.f, 0.f, 0.f}, csl[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_f16(cg, A[0][0], A[0][1], A[0][2], A[0][3], xa.x, xa.y);
-            mma_f16(cs, one2, one2, one2, one2, xa.x, xa.y);
-            mma_f16(cg, A[1][0], A[1][1], A[1][2], A[1][3], xa.z, xa.w);
-            mma_f16(cs, one2, one2, one2, one2, xa.z, xa.w);
-            mma_f16(cg, A[2][0], A[2][1], A[2][2], A[2][3], xc.x, xc.y);
-            mma_f16(cs, one2, one2, one2, one2, xc.x, xc.y);
-            mma_f16(cg, A[3][0], A[3][1], A[3][2], A[3][3], xc.z, xc.w);
-            mma_f16(cs, one2, one2, one2, one2, xc.z, xc.w);
-            if (xlo) {
-              const uint4 ya = ld_cached(xt + xlo);
-              const uint4 yc = ld_cached(xt + xlo + 8);
-              mma_f16(cgl, A[0][0], A[0][1], A[0][2], A[0][3], ya.x, ya.y);
-              mma_f16(csl, one2, one2, one2, one2, ya.x, ya.y);
-              mma_f16(cgl, A[1][0], A[1][1], A[1][2], A[1][3], ya.z, ya.w);
-              mma_f16(csl, one2, one2, one2, one2, ya.z, ya.w);
-              mma_f16(cgl, A[2][0], A[2][1], A[2][2], A[2][3], yc.x, yc.y);
-              mma_f16(csl, one2, one2, one2, one2, yc.x, yc.y);
-              mma_f16(cgl, A[3][0], A[3][1], A[3][2], A[3][3], yc.z, yc.w);
-              mma_f16(csl, one2, one2, one2, one2, yc.z, yc.w);
-            }
-            acc[t][0] += s0 * (cg[0] + cgl[0]) + b0 * (cs[0] + csl[0]);
-            acc[t][1] += s0 * (cg[1] + cgl[1]) + b0 * (cs[1] + csl[1]);
-            acc[t][2] += s1 * (cg[2] + cgl[2]) + b1 * (cs[2] + csl[2]);
-            acc[t][3] += s1 * (cg[3] + cgl[3]) + b1 * (cs[3] + csl[3]);
-          }
-        }
-      }
-    }
-    store_tile<NT>(sg, split, row0, nt, acc, lane);
-  }
-#ifndef DF2_GEMV_NO_PDL
-  if (!waited) pdl_wait();
-#endif
+DF2_DEV __half2 bf16_bits_half2(uint32_t w, int hi) {
+  return __float2half2_rn(bf16_to_f32(static_cast<uint16_t>(hi ? (w >> 16) : (w & 0xFFFFu))));
 }
 
+DF2_DEV uint32_t dequant2(uint32_t codes_biased, uint32_t sel, __half2 s, __half2 b) {
+  const uint32_t qh = codes_to_half2(codes_biased, sel);
+  __half2 w = __hfma2(*reinterpret_cast<const __half2*>(&qh), s, b);
+  return *reinterpret_cast<uint32_t*>(&w);
+}
+
+// Scale and bias of one Q8 stage (2 groups) for rows g and g + 8: bf16 pairs.
+struct Q8Affine {
+  uint32_t s0, s1, b0, b1;
+};
+
+DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs) {
+  const int KG = sg.K >> 6;
+  const size_t i0 = static_cast<size_t>(row) * KG + (kabs >> 6);
+  const size_t i1 = i0 + static_cast<size_t>(8) * KG;
+  Q8Affine r;
+  r.s0 = __ldg(reinterpret_cast<const uint32_t*>(sg.scale + i0));
+  r.s1 = __ldg(reinterpret_cast<const uint32_t*>(sg.scale + i1));
+  r.b0 = __ldg(reinterpret_cast<const uint32_t*>(sg.bias + i0));
+  r.b1 = __ldg(reinterpret_cast<const uint32_t*>(sg.bias + i1));
+  return r;
+}
+
+// Q8 stage: codes 2 boxes [64 K][64 rows] (4 KB each, one group each); fp16
+// activations per tile and plane 2 boxes [64 K][8 rows] (1 KB each, 128-byte
+// swizzle).  wa: this lane's row g in box 0; xrow: row g of tile 0, box 0, hi.
 template <int NT>
-cudaError_t launch_nt(const GemvArgs& a, int fmt, int num_sms, bool pdl, cudaStream_t st) {
-  int ctas = num_sms;  // one 16-warp CTA per SM (the kernels use up to 128 registers a thread)
-  const int need = (a.total_units + kWarpsPerCta - 1) / kWarpsPerCta;
-  if (ctas > need) ctas = need;
+DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, const Q8Affine& af,
+                      float (&c0)[NT][4], float (&c1)[NT][4], float (&c2)[NT][4], float (&c3)[NT][4]) {
+  constexpr int kXPlane = 2048 * NT;
+  const uint32_t pa = static_cast<uint32_t>(((2 * q) ^ g) << 4), pc = static_cast<uint32_t>(((2 * q + 1) ^ g) << 4);
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi) {
+    const uint4 r0 = lds128(wa + gi * 4096);        // 16 codes of row g
+    const uint4 r1 = lds128(wa + gi * 4096 + 512);  // row g + 8
+    const __half2 sg0 = bf16_bits_half2(af.s0, gi), sg1 = bf16_bits_half2(af.s1, gi);
+    const __half2 bg0 = bf16_bits_half2(af.b0, gi), bg1 = bf16_bits_half2(af.b1, gi);
+    const uint32_t u0[4] = {r0.x ^ 0x80808080u, r0.y ^ 0x80808080u, r0.z ^ 0x80808080u, r0.w ^ 0x80808080u};
+    const uint32_t u1[4] = {r1.x ^ 0x80808080u, r1.y ^ 0x80808080u, r1.z ^ 0x80808080u, r1.w ^ 0x80808080u};
+    uint32_t A[4][4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      A[m][0] = dequant2(u0[m], 0x4140, sg0, bg0);
+      A[m][1] = dequant2(u1[m], 0x4140, sg1, bg1);
+      A[m][2] = dequant2(u0[m], 0x4342, sg0, bg0);
+      A[m][3] = dequant2(u1[m], 0x4342, sg1, bg1);
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < n_tiles) {
+        const uint32_t xb = xrow + (t * 2 + gi) * 1024;
+        const uint4 xa = lds128(xb + pa), xc = lds128(xb + pc);  // K 16q..16q+7, 16q+8..16q+15
+        const uint4 ya = lds128(xb + kXPlane + pa), yc = lds128(xb + kXPlane + pc);
+        mma_f16(c0[t], A[0][0], A[0][1], A[0][2], A[0][3], xa.x, xa.y);
+        mma_f16(c1[t], A[1][0], A[1][1], A[1][2], A[1][3], xa.z, xa.w);
+        mma_f16(c0[t], A[2][0], A[2][1], A[2][2], A[2][3], xc.x, xc.y);
+        mma_f16(c1[t], A[3][0], A[3][1], A[3][2], A[3][3], xc.z, xc.w);
+        mma_f16(c2[t], A[0][0], A[0][1], A[0][2], A[0][3], ya.x, ya.y);
+        mma_f16(c3[t], A[1][0], A[1][1], A[1][2], A[1][3], ya.z, ya.w);
+        mma_f16(c2[t], A[2][0], A[2][1], A[2][2], A[2][3], yc.x, yc.y);
+        mma_f16(c3[t], A[3][0], A[3][1], A[3][2], A[3][3], yc.z, yc.w);
+      }
+    }
+  }
+}
+
+template <int NT, int FMT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid_constant__ GemvArgs a) {
+  using Geo = StageGeo<FMT, NT>;
+  constexpr int D = Geo::kDepth;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[D], empty_bar[D];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t full0 = smem_u32(&full_bar[0]), empty0 = smem_u32(&empty_bar[0]);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < D; ++s) {
+      mbar_init_count(full0 + 8 * s, 1);
+      mbar_init_count(empty0 + 8 * s, kConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  if (wid == kConsumers) {
+    // ---------------------------------------------------------------- producer warp
+    const uint64_t policy = evict_first_policy();  // weights: streamed once
+    const uint64_t xpolicy = evict_last_policy();  // activations: read by every CTA
+    constexpr int kWBoxes = FMT == 0 ? 4 : 2;       // weight boxes per stage
+    constexpr int kXBoxes = FMT == 0 ? 4 : 2;       // activation boxes per tile and plane
+    constexpr int kXBoxK = kGemvStageK / kXBoxes;   // K per activation box
+    constexpr int kXBoxBytes = 8 * kXBoxK * 2;
+    auto issue_w = [&](const Cursor& c, int slot) {
+      if (lane < kWBoxes)
+        tma_load_2d(ring + slot * Geo::kBytes + lane * 4096, &a.seg[c.seg].wmap, c.kabs() + lane * (kGemvStageK / kWBoxes),
+                    c.row0, full0 + 8 * slot, policy);
+    };
+    auto issue_x = [&](const Cursor& c, int slot) {
+      const GemvSeg& sg = a.seg[c.seg];
+      const int n = sg.n_tiles * kXBoxes * 2;  // boxes of this stage: tile x box x plane
+      for (int i = lane; i < n; i += 32) {
+        const int plane = i / (sg.n_tiles * kXBoxes);
+        const int rem = i % (sg.n_tiles * kXBoxes);
+        const int t = rem / kXBoxes, b = rem % kXBoxes;
+        const uint32_t dst = ring + slot * Geo::kBytes + Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + b) * kXBoxBytes;
+        tma_load_2d(dst, &sg.xmap, c.kabs() + b * kXBoxK, plane * sg.x_lo_row + t * 8, full0 + 8 * slot, xpolicy);
+      }
+    };
+    auto arm = [&](const Cursor& c, int slot) {
+      const int xbytes = 2 * a.seg[c.seg].n_tiles * kXBoxes * kXBoxBytes;
+      if (lane == 0) mbar_expect_tx(full0 + 8 * slot, Geo::kWBytes + xbytes);
+      __syncwarp();
+    };
+    Cursor cw;
+    cw.start(a);
+    int np = 0;
+    while (np < D && cw.valid) {  // weights of the first stages: before the wait on the previous kernel
+      arm(cw, np);
+      issue_w(cw, np);
+      cw.next(a);
+      ++np;
+    }
+    pdl_wait();
+    Cursor cx;
+    cx.start(a);
+    int it = 0;
+    bool ok = true;
+    while (cx.valid) {
+      const int slot = it % D;
+      if (it >= np) {
+        const uint32_t parity = static_cast<uint32_t>(((it / D) + 1) & 1);
+        if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * slot, parity))) {
+          ok = false;
+          break;
+        }
+        arm(cx, slot);
+        issue_w(cx, slot);
+      }
+      issue_x(cx, slot);
+      cx.next(a);
+      ++it;
+    }
+    if (!ok && lane == 0 && a.err != nullptr) atomicExch(a.err, 1);
+    // the copies of the last stages land before this CTA's shared memory is released (bounded);
+    // a failed wait happens only after every earlier stage was fully issued
+    const int issued = it;
+    for (int j = issued > D ? issued - D : 0; j < issued; ++j)
+      mbar_wait(full0 + 8 * (j % D), static_cast<uint32_t>((j / D) & 1));
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumer warps
+  pdl_wait();
+  const int g = lane >> 2, q = lane & 3;
+  const uint32_t swz = static_cast<uint32_t>((q ^ ((g >> 1) & 3)) << 4);
+  const uint32_t wrow = static_cast<uint32_t>((wid * 16 + g) * 64) + swz;  // row g of this warp in a weight box
+  const uint32_t xrow = FMT == 0 ? static_cast<uint32_t>(g * 64) + swz : static_cast<uint32_t>(g * 128);
+  float c0[NT][4], c1[NT][4], c2[NT][4], c3[NT][4];
+  Cursor c;
+  c.start(a);
+  Q8Affine af = {0u, 0u, 0u, 0u};
+  if (FMT == 1 && c.valid) af = load_affine(a.seg[c.seg], c.row0 + wid * 16 + g, c.kabs());
+  int it = 0;
+  while (c.valid) {
+    if (c.st == 0) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c0[t][e] = c1[t][e] = c2[t][e] = c3[t][e] = 0.f;
+    }
+    const int slot = it % D;
+    const GemvSeg& sg = a.seg[c.seg];
+    // scale and bias of the next stage, loaded while this one computes
+    Cursor cn = c;
+    cn.next(a);
+    Q8Affine afn = af;
+    if (FMT == 1 && cn.valid) afn = load_affine(a.seg[cn.seg], cn.row0 + wid * 16 + g, cn.kabs());
+    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, static_cast<uint32_t>((it / D) & 1)))) {
+      if (lane == 0 && a.err != nullptr) atomicExch(a.err, 1);
+      break;
+    }
+    const uint32_t base = ring + slot * Geo::kBytes;
+    if (FMT == 0)
+      stage_bf16<NT>(sg.n_tiles, base + wrow, base + Geo::kWBytes + xrow, c0, c1, c2, c3);
+    else
+      stage_q8<NT>(sg.n_tiles, base + wrow, base + Geo::kWBytes + xrow, g, q, af, c0, c1, c2, c3);
+    __syncwarp();  // every lane's reads of this stage are done before it is released
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    if (c.st + 1 == c.nst) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c0[t][e] = (c0[t][e] + c1[t][e]) + (c2[t][e] + c3[t][e]);
+      store_tile<NT>(sg, c.split, c.row0 + wid * 16, c0, lane);
+    }
+    c = cn;
+    af = afn;
+    ++it;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* p, int inner, int rows, int box_inner,
+               int box_rows, CUtensorMapSwizzle swz, CUtensorMapL2promotion promo) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr || p == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * esz};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(p), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT, int FMT>
+cudaError_t launch_nt(const GemvArgs& a, int num_sms, bool pdl, cudaStream_t st) {
+  constexpr int smem = StageGeo<FMT, NT>::kSmem;
+  static bool attr_set = false;  // set once, outside any later stream capture
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int ctas = num_sms * kCtasPerSm;
+  if (ctas > a.total_units) ctas = a.total_units;
   if (ctas < 1) ctas = 1;
-  if (fmt == 0) return launch_ex(gemv_bf16_kernel<NT>, dim3(ctas), dim3(kWarpsPerCta * 32), 0, st, pdl, a);
-  return launch_ex(gemv_q8_kernel<NT>, dim3(ctas), dim3(kWarpsPerCta * 32), 0, st, pdl, a);
+  return launch_ex(gemv_kernel<NT, FMT>, dim3(ctas), dim3(kThreads), smem, st, pdl, a);
 }
 
 }  // namespace
 
-int gemv_choose_splits(int tiles, int K, int num_sms) {
-  const long long W = static_cast<long long>(num_sms) * kWarpsPerCta;
-  const int chunks = K / kKStep;
-  int best_s = 1;
-  double best = -1.0;
-  for (int s = 1; s <= chunks; ++s) {
-    if (chunks % s) continue;
-    const long long rounds = (static_cast<long long>(tiles) * s + W - 1) / W;
-    // a warp's batches (+1 pipeline start per unit) and the consumer's per-plane reads
-    const double cost = static_cast<double>(rounds) * (chunks / s + 1) + 0.25 * s;
-    if (best < 0.0 || cost < best) {
+bool gemv_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt) {
+  if (M % kBlockRows || K % kGemvStageK) return false;
+  if (fmt == 0)
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, 32, kBlockRows, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, 64, kBlockRows, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
+bool gemv_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt) {
+  if (rows % 8 || K % kGemvStageK) return false;
+  if (fmt == 0)
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, 2 * rows, 32, 8, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, 2 * rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+}
+
+int gemv_choose_splits(int blocks, int K, double plane_bytes, int num_sms, int fmt) {
+  if (blocks < 1 || K % kGemvStageK) return 0;
+  const long long C = static_cast<long long>(num_sms) * kCtasPerSm;
+  const int kst = K / kGemvStageK;
+  // one stage of every CTA at ~6.5 TB/s, in seconds; the consumer reads planes at ~5 TB/s from L2
+  const double stage_s = static_cast<double>(C) * (fmt == 0 ? 16384.0 : 8192.0) / 6.5e12;
+  const double plane_cost = plane_bytes / 5.0e12 / stage_s;
+  int best_s = 0;
+  double best = 0.0;
+  for (int s = 1; s <= kst; ++s) {
+    if (kst % s) continue;
+    const long long rounds = (static_cast<long long>(blocks) * s + C - 1) / C;
+    const double cost = static_cast<double>(rounds) * (kst / s + 0.25) + plane_cost * s;
+    if (best_s == 0 || cost < best) {
       best = cost;
       best_s = s;
     }
@@ -300,15 +493,24 @@ cudaError_t launch_gemv(GemvArgs& a, int fmt, int max_tiles, int num_sms, bool p
   int units = 0;
   for (int i = 0; i < a.nseg; ++i) {
     GemvSeg& sg = a.seg[i];
-    if (sg.splits < 1 || sg.M % 16 || sg.K % sg.splits || (sg.K / sg.splits) % kKStep) return cudaErrorInvalidValue;
+    if (sg.splits < 1 || sg.M % kBlockRows || sg.K % sg.splits || (sg.K / sg.splits) % kGemvStageK ||
+        sg.n_tiles < 1 || sg.n_tiles > max_tiles)
+      return cudaErrorInvalidValue;
     sg.unit_begin = units;
-    units += (sg.M / 16) * sg.splits;
+    units += (sg.M / kBlockRows) * sg.splits;
   }
   a.total_units = units;
-  if (max_tiles <= 1) return launch_nt<1>(a, fmt, num_sms, pdl, st);
-  if (max_tiles <= 2) return launch_nt<2>(a, fmt, num_sms, pdl, st);
-  if (max_tiles <= 4) return launch_nt<4>(a, fmt, num_sms, pdl, st);
-  if (max_tiles <= 8) return launch_nt<8>(a, fmt, num_sms, pdl, st);
+  if (fmt == 0) {
+    if (max_tiles <= 1) return launch_nt<1, 0>(a, num_sms, pdl, st);
+    if (max_tiles <= 2) return launch_nt<2, 0>(a, num_sms, pdl, st);
+    if (max_tiles <= 4) return launch_nt<4, 0>(a, num_sms, pdl, st);
+    if (max_tiles <= 8) return launch_nt<8, 0>(a, num_sms, pdl, st);
+  } else {
+    if (max_tiles <= 1) return launch_nt<1, 1>(a, num_sms, pdl, st);
+    if (max_tiles <= 2) return launch_nt<2, 1>(a, num_sms, pdl, st);
+    if (max_tiles <= 4) return launch_nt<4, 1>(a, num_sms, pdl, st);
+    if (max_tiles <= 8) return launch_nt<8, 1>(a, num_sms, pdl, st);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -117,7 +117,13 @@ typedef struct dflash2_handle dflash2_handle;
  * scratch for up to `max_requests` requests.  `kv_capacity` is the number of
  * positions per request in the caller's K/V caches.  Must be called with the
  * target device current.  Returns DFLASH2_E_UNSUPPORTED for a geometry the
- * kernels do not cover (head_dim != 128, block != 8, top_k != 16, ...). */
+ * kernels do not cover: head_dim != 128, block != 8, top_k != 16, rank != 256,
+ * conv taps != 2 or group != 16, n_q_heads != 4 * n_kv_heads, hidden or ffn not
+ * a multiple of 512, vocab not a multiple of 16, more than 8 layers or 4
+ * requests, or a window over 64 attention chunks of 64 keys.  Every weight
+ * matrix, Q8 scale and Q8 bias must start on a 16-byte boundary
+ * (DFLASH2_E_INVAL otherwise).  Encodes one bulk-copy descriptor per projection
+ * matrix, so the weights must not move while the handle lives. */
 dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* w, int32_t max_requests,
                               int32_t kv_capacity, dflash2_handle** out);
 
