@@ -36,15 +36,15 @@ DF2_DEV void put_act(void* act, size_t lo, int fmt, size_t idx, float v) {
 }
 
 // Sum of the split planes p[s * plane], s = 0..S-1, added in split order.  The
-// loads of 8 planes are issued together so the latency is paid once per 8.
+// loads of up to 32 planes are issued together so the latency is paid once per 32.
 DF2_DEV float plane_sum(const float* p, size_t plane, int S) {
   float y = 0.f;
-  for (int s0 = 0; s0 < S; s0 += 8) {
-    float t[8];
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    float t[32];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) t[j] = (s0 + j < S) ? p[static_cast<size_t>(s0 + j) * plane] : 0.f;
+    for (int j = 0; j < 32; ++j) t[j] = (s0 + j < S) ? p[static_cast<size_t>(s0 + j) * plane] : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) y += t[j];
+    for (int j = 0; j < 32; ++j) y += t[j];
   }
   return y;
 }
@@ -104,14 +104,28 @@ __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
   const int c = blockIdx.y * kCw + lane;
   const int G = a.H / 16;
   const float rr = warp_inv_rms(a.ss, row, a.nch, a.H, a.eps);
-  // lanes 0..7: the (io, tap, local group) delta values of this row and the CTA's 2 groups
-  float dv = 0.f;
-  if (lane < 8) {
-    const int io = lane >> 2, t = (lane >> 1) & 1, gl = lane & 1;
+  // the (io, tap, local group) delta values of this row and the CTA's 2 groups: value
+  // e = lane & 7, its split planes pg, pg + 4, ... summed by lane e + 8 pg, then the
+  // four partial sums combined in a fixed tree (lanes 0..7 end with the total)
+  float dv;
+  {
+    const int e = lane & 7, pg = lane >> 3;
+    const int io = e >> 2, t = (e >> 1) & 1, gl = e & 1;
     const int gidx = (io * 2 + t) * G + blockIdx.y * 2 + gl;
-    dv = plane_sum(a.dproj + static_cast<size_t>(row) * (4 * G) + gidx, static_cast<size_t>(a.n_rows) * (4 * G),
-                   a.splits) * rr;
-    a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
+    const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
+    const float* p = a.dproj + static_cast<size_t>(row) * (4 * G) + gidx;
+    float part = 0.f;
+    for (int s0 = pg; s0 < a.splits; s0 += 32) {
+      float tt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tt[j] = (s0 + 4 * j < a.splits) ? p[static_cast<size_t>(s0 + 4 * j) * plane] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part += tt[j];
+    }
+    part += __shfl_xor_sync(0xffffffffu, part, 8);
+    part += __shfl_xor_sync(0xffffffffu, part, 16);
+    dv = part * rr;
+    if (lane < 8) a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
   }
   const int gl = lane >> 4;
   const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 2 + gl);

@@ -6,7 +6,8 @@
 // softmax(score / T) at T > 0, and returns q over the 16 candidates.
 //
 // One CTA per request.  The full 7 x 16 x 16 lattice is scored first (position 1
-// from the anchor), then one thread walks it.  Any nonfinite candidate logit or
+// from the anchor), one thread per (position, predecessor, candidate) pair over
+// padded shared-memory rows, then one warp walks it (lane j = candidate j).  Any nonfinite candidate logit or
 // score marks the request DFLASH2_E_NONFINITE ("LSE docs/DFLASH2.md": the
 // selector rejects nonfinite scores).
 #include <math.h>
@@ -28,9 +29,12 @@ constexpr int kRows = kRowsA + kRowsB;
 
 // Codebook rows staged in shared memory in their stored format: bf16 (256 x 2 B) or
 // Q8 codes (256 B) plus 4 groups of (scale, bias).
+constexpr int kPadBf = kRank + 8;   // bf16 row stride: consecutive rows start 16 B apart mod 128 B
+constexpr int kPadQ8 = kRank + 16;  // int8 row stride, same idea
+
 struct SelSmem {
-  uint16_t bf[kRows][kRank];   // BF16 rows (unused for Q8)
-  int8_t q8[kRows][kRank];     // Q8 codes (unused for BF16)
+  uint16_t bf[kRows][kPadBf];  // BF16 rows (unused for Q8)
+  int8_t q8[kRows][kPadQ8];    // Q8 codes (unused for BF16)
   uint16_t sb[kRows][8];       // Q8: scale[4], bias[4]
   float gate[kP][kRank];
   float lat[kP][kK][kK];       // scores [position][pred][cand]
@@ -39,33 +43,74 @@ struct SelSmem {
   int bad;
 };
 
-// Row `row` of the staged codebook rows, element r, as fp32.
-DF2_DEV float cb_val(const SelSmem& sm, int fmt, int row, int r) {
-  if (fmt == 0) return bf16_to_f32(sm.bf[row][r]);
-  const int g = r >> 6;
-  return bf16_to_f32(sm.sb[row][g]) * static_cast<float>(sm.q8[row][r]) + bf16_to_f32(sm.sb[row][4 + g]);
+constexpr int kThreads = 512;
+
+DF2_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+DF2_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Edge score of predecessor row ra and candidate row rb at position i (without the unary term).
+DF2_DEV float edge_dot(const SelSmem& sm, int fmt, int i, int ra, int rb) {
+  const float* g = sm.gate[i];
+  float s = 0.f;
+  if (fmt == 0) {
+    const uint4* A = reinterpret_cast<const uint4*>(sm.bf[ra]);
+    const uint4* B = reinterpret_cast<const uint4*>(sm.bf[rb]);
+#pragma unroll 4
+    for (int k = 0; k < kRank / 8; ++k) {
+      const uint4 av = A[k], bv = B[k];
+      const float4 g0 = *reinterpret_cast<const float4*>(g + 8 * k);
+      const float4 g1 = *reinterpret_cast<const float4*>(g + 8 * k + 4);
+      s = fmaf(bf_lo(av.x), g0.x * bf_lo(bv.x), s);
+      s = fmaf(bf_hi(av.x), g0.y * bf_hi(bv.x), s);
+      s = fmaf(bf_lo(av.y), g0.z * bf_lo(bv.y), s);
+      s = fmaf(bf_hi(av.y), g0.w * bf_hi(bv.y), s);
+      s = fmaf(bf_lo(av.z), g1.x * bf_lo(bv.z), s);
+      s = fmaf(bf_hi(av.z), g1.y * bf_hi(bv.z), s);
+      s = fmaf(bf_lo(av.w), g1.z * bf_lo(bv.w), s);
+      s = fmaf(bf_hi(av.w), g1.w * bf_hi(bv.w), s);
+    }
+  } else {
+#pragma unroll
+    for (int grp = 0; grp < kRank / 64; ++grp) {
+      const float sa = bf16_to_f32(sm.sb[ra][grp]), ba = bf16_to_f32(sm.sb[ra][4 + grp]);
+      const float sb = bf16_to_f32(sm.sb[rb][grp]), bb = bf16_to_f32(sm.sb[rb][4 + grp]);
+      const int8_t* A = sm.q8[ra] + 64 * grp;
+      const int8_t* B = sm.q8[rb] + 64 * grp;
+      const float* gg = g + 64 * grp;
+#pragma unroll 4
+      for (int k = 0; k < 64; k += 4) {
+        const char4 av = *reinterpret_cast<const char4*>(A + k), bv = *reinterpret_cast<const char4*>(B + k);
+        const float4 g4 = *reinterpret_cast<const float4*>(gg + k);
+        s = fmaf(fmaf(sa, static_cast<float>(av.x), ba), g4.x * fmaf(sb, static_cast<float>(bv.x), bb), s);
+        s = fmaf(fmaf(sa, static_cast<float>(av.y), ba), g4.y * fmaf(sb, static_cast<float>(bv.y), bb), s);
+        s = fmaf(fmaf(sa, static_cast<float>(av.z), ba), g4.z * fmaf(sb, static_cast<float>(bv.z), bb), s);
+        s = fmaf(fmaf(sa, static_cast<float>(av.w), ba), g4.w * fmaf(sb, static_cast<float>(bv.w), bb), s);
+      }
+    }
+  }
+  return s;
 }
 
-__global__ void __launch_bounds__(256) select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   pdl_begin();
   const int r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (tid == 0) sm.bad = 0;
-  for (int e = tid; e < kP * kK; e += 256) {
+  for (int e = tid; e < kP * kK; e += kThreads) {
     sm.cids[e / kK][e % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + e], 0), a.V - 1);
     const float v = a.cand_logits[static_cast<size_t>(r) * kP * kK + e];
     sm.cl[e / kK][e % kK] = v;
     if (!isfinite(v)) atomicOr(&sm.bad, 1);
   }
-  for (int e = tid; e < kP * kRank; e += 256) sm.gate[e / kRank][e % kRank] = a.gate[static_cast<size_t>(r) * kP * kRank + e];
+  for (int e = tid; e < kP * kRank; e += kThreads) sm.gate[e / kRank][e % kRank] = a.gate[static_cast<size_t>(r) * kP * kRank + e];
   __syncthreads();
   const int anchor = min(max(a.anchor_ids[r], 0), a.V - 1);
   // stage every needed codebook row at once (one round trip): row k < kRowsA is the
   // predecessor row A[id], k >= kRowsA the successor row B[id]
   const int chunks = a.fmt == 0 ? kRank * 2 / 16 : kRank / 16;  // 16-byte pieces per row
-  for (int e = tid; e < kRows * chunks; e += 256) {
+  for (int e = tid; e < kRows * chunks; e += kThreads) {
     const int k = e / chunks, c = e % chunks;
     int id;
     const void* cb;
@@ -91,9 +136,9 @@ __global__ void __launch_bounds__(256) select_kernel(const SelectArgs a) {
     }
   }
   __syncthreads();
-  // lattice: one warp per (position, pred, cand); lanes split the rank (fixed tree)
+  // lattice: one thread per (position, pred, cand)
   const int n_pairs = kK + (kP - 1) * kK * kK;
-  for (int pc = wid; pc < n_pairs; pc += 8) {
+  for (int pc = tid; pc < n_pairs; pc += kThreads) {
     int i, p, c;
     if (pc < kK) {
       i = 0;
@@ -107,77 +152,78 @@ __global__ void __launch_bounds__(256) select_kernel(const SelectArgs a) {
     }
     const int ra = i == 0 ? 0 : 1 + (i - 1) * kK + p;
     const int rb = kRowsA + i * kK + c;
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < kRank / 32; ++k) {
-      const int rr = lane + 32 * k;
-      s = fmaf(cb_val(sm, a.fmt, ra, rr), sm.gate[i][rr] * cb_val(sm, a.fmt, rb, rr), s);
-    }
-    s = warp_sum(s) + sm.cl[i][c];
-    if (lane == 0) {
-      if (!isfinite(s)) atomicOr(&sm.bad, 1);
-      if (i == 0) {
-        for (int pp = 0; pp < kK; ++pp) sm.lat[0][pp][c] = s;
-      } else {
-        sm.lat[i][p][c] = s;
-      }
+    const float s = edge_dot(sm, a.fmt, i, ra, rb) + sm.cl[i][c];
+    if (!isfinite(s)) atomicOr(&sm.bad, 1);
+    if (i == 0) {
+      for (int pp = 0; pp < kK; ++pp) sm.lat[0][pp][c] = s;
+    } else {
+      sm.lat[i][p][c] = s;
     }
   }
   __syncthreads();
   if (a.scores_out) {
-    for (int e = tid; e < kP * kK * kK; e += 256)
+    for (int e = tid; e < kP * kK * kK; e += kThreads)
       a.scores_out[static_cast<size_t>(r) * kP * kK * kK + e] = (&sm.lat[0][0][0])[e];
   }
   const int bad = sm.bad;
   auto& lat = sm.lat;
   auto& cids = sm.cids;
-  if (tid != 0) return;
+  if (wid != 0) return;
+  // ---- the walk: one warp, lane j < 16 holds candidate j
   const float T = a.temperature[r];
   int32_t* path = a.path + static_cast<size_t>(r) * kP;
   float* qrow = a.q_rows + static_cast<size_t>(r) * kP * kK;
   if (!(T >= 0.f) || bad) {
-    for (int i = 0; i < kP; ++i) {
-      path[i] = -1;
-      for (int j = 0; j < kK; ++j) qrow[i * kK + j] = 0.f;
-    }
-    a.status[r] = (T >= 0.f) ? 2 : 1;
+    if (lane < kP) path[lane] = -1;
+    for (int e = lane; e < kP * kK; e += 32) qrow[e] = 0.f;
+    if (lane == 0) a.status[r] = (T >= 0.f) ? 2 : 1;
     return;
   }
   const uint64_t seed = a.seed[r], off = a.offset[r];
+  const bool live = lane < kK;
   int prev = 0;
   for (int i = 0; i < kP; ++i) {
-    const float* s = lat[i][prev];
-    int pick = 0;
+    const float sj = live ? lat[i][prev][lane] : -INFINITY;
+    const int cid = live ? cids[i][lane] : 0x7FFFFFFF;
+    int pick;
+    float q;
     if (T == 0.f) {
-      for (int j = 1; j < kK; ++j)
-        if (s[j] > s[pick] || (s[j] == s[pick] && cids[i][j] < cids[i][pick])) pick = j;
-      for (int j = 0; j < kK; ++j) qrow[i * kK + j] = (j == pick) ? 1.f : 0.f;
+      // argmax, equal scores -> smaller candidate id
+      float bv = sj;
+      int bi = lane, bc = cid;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o), oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (ov > bv || (ov == bv && oc < bc)) {
+          bv = ov;
+          bi = oi;
+          bc = oc;
+        }
+      }
+      pick = bi;
+      q = (lane == pick) ? 1.f : 0.f;
     } else {
-      float m = s[0];
-      for (int j = 1; j < kK; ++j) m = fmaxf(m, s[j]);
-      float e[kK];
-      float tot = 0.f;
-      for (int j = 0; j < kK; ++j) {
-        e[j] = expf((s[j] - m) / T);
-        tot += e[j];
+      const float m = warp_max(sj);
+      const float e = live ? expf((sj - m) / T) : 0.f;
+      const float tot = warp_sum(e);
+      float cum = e;  // inclusive prefix sum over lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, cum, o);
+        if (lane >= o) cum += t;
       }
       const float u = philox_uniform(seed, off, static_cast<uint32_t>(i), kPurposeWalk);
-      const float target = u * tot;
-      float cum = 0.f;
-      pick = -1;
-      int last_pos = 0;
-      for (int j = 0; j < kK; ++j) {
-        cum += e[j];
-        if (e[j] > 0.f) last_pos = j;
-        if (pick < 0 && cum > target) pick = j;
-      }
-      if (pick < 0) pick = last_pos;
-      for (int j = 0; j < kK; ++j) qrow[i * kK + j] = e[j] / tot;
+      const unsigned over = __ballot_sync(0xffffffffu, live && cum > u * tot);
+      const unsigned pos = __ballot_sync(0xffffffffu, live && e > 0.f);
+      pick = over ? __ffs(over) - 1 : (pos ? 31 - __clz(pos) : 0);
+      q = e / tot;
     }
-    path[i] = cids[i][pick];
+    if (live) qrow[i * kK + lane] = q;
+    if (lane == 0) path[i] = cids[i][pick];
     prev = pick;
   }
-  a.status[r] = 0;
+  if (lane == 0) a.status[r] = 0;
 }
 
 }  // namespace
@@ -190,7 +236,7 @@ cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(select_kernel, dim3(n_req), dim3(256), sizeof(SelSmem), st, pdl, a);
+  return launch_ex(select_kernel, dim3(n_req), dim3(kThreads), sizeof(SelSmem), st, pdl, a);
 }
 
 }  // namespace df2
