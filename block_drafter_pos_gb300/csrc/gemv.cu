@@ -9,16 +9,19 @@
 //    SM) walks its units grid-stride with one producer warp and four consumer
 //    warps.  The producer fills a ring of shared-memory stages with bulk tensor
 //    copies (cp.async.bulk.tensor) completing on the stage's "full" mbarrier: 64
-//    weight rows x 128 K (64-byte rows, 64-byte swizzle), plus the matching
-//    activation slice, both planes, in 8-row boxes.  The consumers release a stage
+//    weight rows x 128 K, plus the matching activation slice, both planes, in
+//    8-row boxes.  Copies move 64 K per row: 128-byte rows (128-byte swizzle) for
+//    bf16 weights and for activations, 64-byte rows (64-byte swizzle) for int8
+//    codes.  The copy engine's cost grows with the number of rows it fetches, so
+//    rows are kept as long as the swizzle allows.  The consumers release a stage
 //    through its "empty" mbarrier.  The weight copies of the first stages are
 //    issued before griddepcontrol.wait (weights never depend on the previous
 //    kernel); the activation copies after it.
 //  * Each consumer warp owns 16 of the 64 rows: mma.sync m16n8k16 with the weights
 //    as the A operand.  The order of the K sum inside one MMA is free: a lane
-//    reads 8 consecutive K of rows g and g + 8 and of activation row g (16-byte
-//    shared-memory loads, bank-conflict-free under the swizzle), so A and B agree
-//    on which K each MMA slot holds.
+//    reads the same consecutive K of weight rows g and g + 8 and of activation row
+//    g (16-byte shared-memory loads, bank-conflict-free under the swizzle), so A
+//    and B agree on which K each MMA slot holds.
 //  * Each split's partial goes to its own output plane with plain stores; the
 //    consumer kernel adds the planes in split order, so every result is
 //    bit-reproducible.  The split count comes from a cost model over the grid
@@ -45,21 +48,26 @@ namespace df2 {
 
 namespace {
 
-constexpr int kConsumers = 4;        // consumer warps per CTA (16 weight rows each)
+constexpr int kBlockRows = 64;                // weight rows per unit
+constexpr int kStageK = kGemvStageK;          // K per stage
+constexpr int kConsumers = kBlockRows / 16;   // consumer warps per CTA (16 weight rows each)
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;
-constexpr int kBlockRows = 64;       // weight rows per unit
-constexpr int kRingBudget = 100 * 1024;
+constexpr int kRingBudget = (kCtasPerSm == 1 ? 208 : 200 / kCtasPerSm) * 1024;
+constexpr int kMaxDepth = 24;
+// One weight copy: 64 K x kBlockRows rows (128-byte rows for bf16, 64-byte rows for int8 codes).
+template <int FMT>
+constexpr int wbox_bytes() { return 64 * (FMT == 0 ? 2 : 1) * kBlockRows; }
 constexpr long long kSpinLimit = 1ll << 22;
 
 // Shared-memory geometry of one stage for a format and a number of 8-row activation tiles.
 template <int FMT, int NT>
 struct StageGeo {
-  static constexpr int kWBytes = FMT == 0 ? 16384 : 8192;  // 64 rows x 128 K
-  static constexpr int kXPlane = 2048 * NT;                 // 8*NT rows x 128 K x 2 B
+  static constexpr int kWBytes = kBlockRows * kStageK * (FMT == 0 ? 2 : 1);
+  static constexpr int kXPlane = 8 * NT * kStageK * 2;  // 8*NT rows x kStageK x 2 B
   static constexpr int kBytes = kWBytes + 2 * kXPlane;
   static constexpr int kDepthRaw = kRingBudget / kBytes;
-  static constexpr int kDepth = kDepthRaw < 2 ? 2 : (kDepthRaw > 6 ? 6 : kDepthRaw);
+  static constexpr int kDepth = kDepthRaw < 2 ? 2 : (kDepthRaw > kMaxDepth ? kMaxDepth : kDepthRaw);
   static constexpr int kSmem = kDepth * kBytes + 1024;  // + slack for 1 KB alignment
 };
 
@@ -143,7 +151,7 @@ struct Cursor {
     row0 = (local % blocks) * kBlockRows;
     const int kchunk = sg.K / sg.splits;
     k0 = split * kchunk;
-    nst = kchunk / kGemvStageK;
+    nst = kchunk / kStageK;
     st = 0;
   }
   DF2_DEV void start(const GemvArgs& a) {
@@ -156,7 +164,7 @@ struct Cursor {
       load(a);
     }
   }
-  DF2_DEV int kabs() const { return k0 + st * kGemvStageK; }
+  DF2_DEV int kabs() const { return k0 + st * kStageK; }
 };
 
 template <int NT>
@@ -175,34 +183,42 @@ DF2_DEV void store_tile(const GemvSeg& sg, int split, int row0, const float (&ac
   }
 }
 
-// BF16 stage: weights 4 boxes [32 K][64 rows] (4 KB each); activations per tile
-// and plane 4 boxes [32 K][8 rows] (512 B each).  wa: this lane's row g in box 0;
-// xa: this lane's row g in tile 0, box 0, hi plane.
+// BF16 stage: weights kStageK/64 boxes [64 K][kBlockRows rows] (128-byte rows,
+// 128-byte swizzle); activations per tile and plane kStageK/64 boxes [64 K][8 rows]
+// (1 KB each, same swizzle).  A lane reads the two 16-byte pieces 2q and 2q + 1
+// (K 16q .. 16q + 15 of the box) of weight rows g, g + 8 and activation row g.
+// wa / xrow: row g of box 0 (weights of this warp / tile 0, hi plane).
 template <int NT>
-DF2_DEV void stage_bf16(int n_tiles, uint32_t wa, uint32_t xa, float (&c0)[NT][4], float (&c1)[NT][4],
-                        float (&c2)[NT][4], float (&c3)[NT][4]) {
-  constexpr int kXPlane = 2048 * NT;
+DF2_DEV void stage_bf16(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, float (&c0)[NT][4],
+                        float (&c1)[NT][4], float (&c2)[NT][4], float (&c3)[NT][4]) {
+  constexpr int kXPlane = 8 * NT * kStageK * 2;
+  constexpr int kB = kStageK / 64;
+  const uint32_t pa = static_cast<uint32_t>(((2 * q) ^ g) << 4), pc = static_cast<uint32_t>(((2 * q + 1) ^ g) << 4);
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint4 a0 = lds128(wa + b * 4096);        // row g
-    const uint4 a1 = lds128(wa + b * 4096 + 512);  // row g + 8
+  for (int b = 0; b < kB; ++b) {
+    const uint32_t wb = wa + b * wbox_bytes<0>();
+    const uint4 a0 = lds128(wb + pa), a0b = lds128(wb + pc);                // row g
+    const uint4 a1 = lds128(wb + 1024 + pa), a1b = lds128(wb + 1024 + pc);  // row g + 8
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       if (t < n_tiles) {
-        const uint32_t xb = xa + (t * 4 + b) * 512;
-        const uint4 x = lds128(xb), y = lds128(xb + kXPlane);
-        mma_bf16(c0[t], a0.x, a1.x, a0.y, a1.y, x.x, x.y);
-        mma_bf16(c1[t], a0.z, a1.z, a0.w, a1.w, x.z, x.w);
-        mma_bf16(c2[t], a0.x, a1.x, a0.y, a1.y, y.x, y.y);
-        mma_bf16(c3[t], a0.z, a1.z, a0.w, a1.w, y.z, y.w);
+        const uint32_t xb = xrow + (t * kB + b) * 1024;
+        const uint4 x0 = lds128(xb + pa), x1 = lds128(xb + pc);
+        const uint4 y0 = lds128(xb + kXPlane + pa), y1 = lds128(xb + kXPlane + pc);
+        mma_bf16(c0[t], a0.x, a1.x, a0.y, a1.y, x0.x, x0.y);
+        mma_bf16(c1[t], a0.z, a1.z, a0.w, a1.w, x0.z, x0.w);
+        mma_bf16(c0[t], a0b.x, a1b.x, a0b.y, a1b.y, x1.x, x1.y);
+        mma_bf16(c1[t], a0b.z, a1b.z, a0b.w, a1b.w, x1.z, x1.w);
+        mma_bf16(c2[t], a0.x, a1.x, a0.y, a1.y, y0.x, y0.y);
+        mma_bf16(c3[t], a0.z, a1.z, a0.w, a1.w, y0.z, y0.w);
+        mma_bf16(c2[t], a0b.x, a1b.x, a0b.y, a1b.y, y1.x, y1.y);
+        mma_bf16(c3[t], a0b.z, a1b.z, a0b.w, a1b.w, y1.z, y1.w);
       }
     }
   }
 }
 
-DF2_DEV __half2 bf16_bits_half2(uint32_t w, int hi) {
-  return __float2half2_rn(bf16_to_f32(static_cast<uint16_t>(hi ? (w >> 16) : (w & 0xFFFFu))));
-}
+DF2_DEV __half2 bf16_bits_half2(uint16_t b) { return __float2half2_rn(bf16_to_f32(b)); }
 
 DF2_DEV uint32_t dequant2(uint32_t codes_biased, uint32_t sel, __half2 s, __half2 b) {
   const uint32_t qh = codes_to_half2(codes_biased, sel);
@@ -210,9 +226,10 @@ DF2_DEV uint32_t dequant2(uint32_t codes_biased, uint32_t sel, __half2 s, __half
   return *reinterpret_cast<uint32_t*>(&w);
 }
 
-// Scale and bias of one Q8 stage (2 groups) for rows g and g + 8: bf16 pairs.
+// Scale and bias (bf16 bits) of one Q8 stage's kStageK / 64 groups for rows g and g + 8.
+constexpr int kAffGroups = kStageK / 64;
 struct Q8Affine {
-  uint32_t s0, s1, b0, b1;
+  uint16_t s0[kAffGroups], s1[kAffGroups], b0[kAffGroups], b1[kAffGroups];
 };
 
 DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs) {
@@ -220,27 +237,31 @@ DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs) {
   const size_t i0 = static_cast<size_t>(row) * KG + (kabs >> 6);
   const size_t i1 = i0 + static_cast<size_t>(8) * KG;
   Q8Affine r;
-  r.s0 = __ldg(reinterpret_cast<const uint32_t*>(sg.scale + i0));
-  r.s1 = __ldg(reinterpret_cast<const uint32_t*>(sg.scale + i1));
-  r.b0 = __ldg(reinterpret_cast<const uint32_t*>(sg.bias + i0));
-  r.b1 = __ldg(reinterpret_cast<const uint32_t*>(sg.bias + i1));
+#pragma unroll
+  for (int j = 0; j < kAffGroups; ++j) {
+    r.s0[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i0 + j);
+    r.s1[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i1 + j);
+    r.b0[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i0 + j);
+    r.b1[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i1 + j);
+  }
   return r;
 }
 
-// Q8 stage: codes 2 boxes [64 K][64 rows] (4 KB each, one group each); fp16
-// activations per tile and plane 2 boxes [64 K][8 rows] (1 KB each, 128-byte
-// swizzle).  wa: this lane's row g in box 0; xrow: row g of tile 0, box 0, hi.
+// Q8 stage: codes kStageK/64 boxes [64 K][kBlockRows rows] (one group each);
+// fp16 activations per tile and plane kStageK/64 boxes [64 K][8 rows] (1 KB each,
+// 128-byte swizzle).  wa: this lane's row g in box 0; xrow: row g of tile 0, box 0, hi.
 template <int NT>
 DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, const Q8Affine& af,
                       float (&c0)[NT][4], float (&c1)[NT][4], float (&c2)[NT][4], float (&c3)[NT][4]) {
-  constexpr int kXPlane = 2048 * NT;
+  constexpr int kXPlane = 8 * NT * kStageK * 2;
+  constexpr int kG = kStageK / 64;
   const uint32_t pa = static_cast<uint32_t>(((2 * q) ^ g) << 4), pc = static_cast<uint32_t>(((2 * q + 1) ^ g) << 4);
 #pragma unroll
-  for (int gi = 0; gi < 2; ++gi) {
-    const uint4 r0 = lds128(wa + gi * 4096);        // 16 codes of row g
-    const uint4 r1 = lds128(wa + gi * 4096 + 512);  // row g + 8
-    const __half2 sg0 = bf16_bits_half2(af.s0, gi), sg1 = bf16_bits_half2(af.s1, gi);
-    const __half2 bg0 = bf16_bits_half2(af.b0, gi), bg1 = bf16_bits_half2(af.b1, gi);
+  for (int gi = 0; gi < kG; ++gi) {
+    const uint4 r0 = lds128(wa + gi * wbox_bytes<1>());        // 16 codes of row g
+    const uint4 r1 = lds128(wa + gi * wbox_bytes<1>() + 512);  // row g + 8
+    const __half2 sg0 = bf16_bits_half2(af.s0[gi]), sg1 = bf16_bits_half2(af.s1[gi]);
+    const __half2 bg0 = bf16_bits_half2(af.b0[gi]), bg1 = bf16_bits_half2(af.b1[gi]);
     const uint32_t u0[4] = {r0.x ^ 0x80808080u, r0.y ^ 0x80808080u, r0.z ^ 0x80808080u, r0.w ^ 0x80808080u};
     const uint32_t u1[4] = {r1.x ^ 0x80808080u, r1.y ^ 0x80808080u, r1.z ^ 0x80808080u, r1.w ^ 0x80808080u};
     uint32_t A[4][4];
@@ -254,7 +275,7 @@ DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, con
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       if (t < n_tiles) {
-        const uint32_t xb = xrow + (t * 2 + gi) * 1024;
+        const uint32_t xb = xrow + (t * kG + gi) * 1024;
         const uint4 xa = lds128(xb + pa), xc = lds128(xb + pc);  // K 16q..16q+7, 16q+8..16q+15
         const uint4 ya = lds128(xb + kXPlane + pa), yc = lds128(xb + kXPlane + pc);
         mma_f16(c0[t], A[0][0], A[0][1], A[0][2], A[0][3], xa.x, xa.y);
@@ -294,13 +315,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     // ---------------------------------------------------------------- producer warp
     const uint64_t policy = evict_first_policy();  // weights: streamed once
     const uint64_t xpolicy = evict_last_policy();  // activations: read by every CTA
-    constexpr int kWBoxes = FMT == 0 ? 4 : 2;       // weight boxes per stage
-    constexpr int kXBoxes = FMT == 0 ? 4 : 2;       // activation boxes per tile and plane
-    constexpr int kXBoxK = kGemvStageK / kXBoxes;   // K per activation box
+    constexpr int kWBoxes = kStageK / 64;  // weight boxes per stage (64 K each)
+    constexpr int kXBoxes = kStageK / 64;  // activation boxes per tile and plane (64 K x 8 rows)
+    constexpr int kXBoxK = 64;
     constexpr int kXBoxBytes = 8 * kXBoxK * 2;
     auto issue_w = [&](const Cursor& c, int slot) {
       if (lane < kWBoxes)
-        tma_load_2d(ring + slot * Geo::kBytes + lane * 4096, &a.seg[c.seg].wmap, c.kabs() + lane * (kGemvStageK / kWBoxes),
+        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs() + lane * 64,
                     c.row0, full0 + 8 * slot, policy);
     };
     auto issue_x = [&](const Cursor& c, int slot) {
@@ -361,12 +382,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   pdl_wait();
   const int g = lane >> 2, q = lane & 3;
   const uint32_t swz = static_cast<uint32_t>((q ^ ((g >> 1) & 3)) << 4);
-  const uint32_t wrow = static_cast<uint32_t>((wid * 16 + g) * 64) + swz;  // row g of this warp in a weight box
-  const uint32_t xrow = FMT == 0 ? static_cast<uint32_t>(g * 64) + swz : static_cast<uint32_t>(g * 128);
+  // row g of this warp in a weight box (bf16: 128-byte rows, pieces chosen in stage_bf16;
+  // int8: 64-byte rows, piece q under the 64-byte swizzle), and row g of an activation box
+  const uint32_t wrow = FMT == 0 ? static_cast<uint32_t>((wid * 16 + g) * 128)
+                                 : static_cast<uint32_t>((wid * 16 + g) * 64) + swz;
+  const uint32_t xrow = static_cast<uint32_t>(g * 128);
   float c0[NT][4], c1[NT][4], c2[NT][4], c3[NT][4];
   Cursor c;
   c.start(a);
-  Q8Affine af = {0u, 0u, 0u, 0u};
+  Q8Affine af = {};
   if (FMT == 1 && c.valid) af = load_affine(a.seg[c.seg], c.row0 + wid * 16 + g, c.kabs());
   int it = 0;
   while (c.valid) {
@@ -389,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     }
     const uint32_t base = ring + slot * Geo::kBytes;
     if (FMT == 0)
-      stage_bf16<NT>(sg.n_tiles, base + wrow, base + Geo::kWBytes + xrow, c0, c1, c2, c3);
+      stage_bf16<NT>(sg.n_tiles, base + wrow, base + Geo::kWBytes + xrow, g, q, c0, c1, c2, c3);
     else
       stage_q8<NT>(sg.n_tiles, base + wrow, base + Geo::kWBytes + xrow, g, q, af, c0, c1, c2, c3);
     __syncwarp();  // every lane's reads of this stage are done before it is released
@@ -451,29 +475,29 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, bool pdl, cudaStream_t st)
 }  // namespace
 
 bool gemv_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt) {
-  if (M % kBlockRows || K % kGemvStageK) return false;
+  if (M % kBlockRows || K % kStageK) return false;
   if (fmt == 0)
-    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, 32, kBlockRows, CU_TENSOR_MAP_SWIZZLE_64B,
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, 64, kBlockRows, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, 64, kBlockRows, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 bool gemv_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt) {
-  if (rows % 8 || K % kGemvStageK) return false;
+  if (rows % 8 || K % kStageK) return false;
   if (fmt == 0)
-    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, 2 * rows, 32, 8, CU_TENSOR_MAP_SWIZZLE_64B,
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, 2 * rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K, 2 * rows, 64, 8, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 int gemv_choose_splits(int blocks, int K, double plane_bytes, int num_sms, int fmt) {
-  if (blocks < 1 || K % kGemvStageK) return 0;
+  if (blocks < 1 || K % kStageK) return 0;
   const long long C = static_cast<long long>(num_sms) * kCtasPerSm;
-  const int kst = K / kGemvStageK;
+  const int kst = K / kStageK;
   // one stage of every CTA at ~6.5 TB/s, in seconds; the consumer reads planes at ~5 TB/s from L2
-  const double stage_s = static_cast<double>(C) * (fmt == 0 ? 16384.0 : 8192.0) / 6.5e12;
+  const double stage_s = static_cast<double>(C) * kBlockRows * kStageK * (fmt == 0 ? 2.0 : 1.0) / 6.5e12;
   const double plane_cost = plane_bytes / 5.0e12 / stage_s;
   int best_s = 0;
   double best = 0.0;
@@ -493,7 +517,7 @@ cudaError_t launch_gemv(GemvArgs& a, int fmt, int max_tiles, int num_sms, bool p
   int units = 0;
   for (int i = 0; i < a.nseg; ++i) {
     GemvSeg& sg = a.seg[i];
-    if (sg.splits < 1 || sg.M % kBlockRows || sg.K % sg.splits || (sg.K / sg.splits) % kGemvStageK ||
+    if (sg.splits < 1 || sg.M % kBlockRows || sg.K % sg.splits || (sg.K / sg.splits) % kStageK ||
         sg.n_tiles < 1 || sg.n_tiles > max_tiles)
       return cudaErrorInvalidValue;
     sg.unit_begin = units;
