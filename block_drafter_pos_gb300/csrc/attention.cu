@@ -52,34 +52,67 @@ DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* smem_row)
 }
 
 // ------------------------------------------------------------------ context chunk (tensor cores)
+// Every thread's K/V loads of the chunk, issued together: 4 rows x 16 bytes of K and of V.
+struct KvRegs {
+  uint4 k[4], v[4];
+};
+
+DF2_DEV KvRegs load_kv(const AttnArgs& a, int r, int kvh, int k_begin, int nk) {
+  const int tid = threadIdx.x, nkv = a.n_kv_heads;
+  const uint16_t* kc = a.k_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
+  const uint16_t* vc = a.v_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
+  KvRegs x;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + 256 * j;
+    const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
+    x.k[j] = x.v[j] = make_uint4(0, 0, 0, 0);
+    if (k < nk) {
+      x.k[j] = ld_stream(kc + static_cast<size_t>(k) * nkv * kHd + d8);
+      x.v[j] = ld_stream(vc + static_cast<size_t>(k) * nkv * kHd + d8);
+    }
+  }
+  return x;
+}
+
+// early: the chunk's K/V were loaded before the wait on the previous kernel (no
+// newly appended row in the chunk); otherwise they are loaded after it.
 DF2_DEV void ctx_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, int k_begin, int nk, int L,
-                       float* out) {
+                       bool early, float* out) {
   CtxSmem& sm = *reinterpret_cast<CtxSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const int nkv = a.n_kv_heads, rep = a.n_q_heads / nkv;
+  const int rep = a.n_q_heads / a.n_kv_heads;
   const float qscale = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;  // log2(e)/sqrt(hd)
-  // queries -> bf16 hi/lo (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i)
-  for (int e = tid; e < kQ * kHd; e += 256) {
+  KvRegs kv;
+  if (early) kv = load_kv(a, r, kvh, k_begin, nk);
+  pdl_wait();
+  pdl_trigger();
+  if (!early) kv = load_kv(a, r, kvh, k_begin, nk);
+  // queries -> bf16 hi/lo (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i); loads first
+  float qv[kQ * kHd / 256];
+#pragma unroll
+  for (int j = 0; j < kQ * kHd / 256; ++j) {
+    const int e = tid + 256 * j;
     const int qi = e / kHd, d = e % kHd;
     const int hr = qi >> 3, i = qi & 7;
-    const float v = a.q[((static_cast<size_t>(r) * 8 + i) * a.n_q_heads + kvh * rep + hr) * kHd + d] * qscale;
+    qv[j] = a.q[((static_cast<size_t>(r) * 8 + i) * a.n_q_heads + kvh * rep + hr) * kHd + d];
+  }
+#pragma unroll
+  for (int j = 0; j < kQ * kHd / 256; ++j) {
+    const int e = tid + 256 * j;
+    const int qi = e / kHd, d = e % kHd;
+    const float v = qv[j] * qscale;
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
     sm.qh[qi][d] = h;
     sm.ql[qi][d] = __float2bfloat16_rn(v - __bfloat162float(h));
   }
-  // keys and values of the chunk (rows >= nk are zero)
-  const uint16_t* kc = a.k_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
-  const uint16_t* vc = a.v_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
-  for (int e = tid; e < kKeys * (kHd / 8); e += 256) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + 256 * j;
     const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-    uint4 kv4 = make_uint4(0, 0, 0, 0), vv4 = make_uint4(0, 0, 0, 0);
-    if (k < nk) {
-      kv4 = ld_stream(kc + static_cast<size_t>(k) * nkv * kHd + d8);
-      vv4 = ld_stream(vc + static_cast<size_t>(k) * nkv * kHd + d8);
-    }
-    *reinterpret_cast<uint4*>(&sm.k[k][d8]) = kv4;
-    *reinterpret_cast<uint4*>(&sm.v[k][d8]) = vv4;
+    *reinterpret_cast<uint4*>(&sm.k[k][d8]) = kv.k[j];
+    *reinterpret_cast<uint4*>(&sm.v[k][d8]) = kv.v[j];
   }
   __syncthreads();
   // S = Q K^T: 2 query tiles x 8 key tiles; warp w takes key tile w for both query tiles
@@ -217,7 +250,6 @@ DF2_DEV void blk_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kv
 
 __global__ void __launch_bounds__(256) attn_chunk_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  pdl_begin();
   const int nkv = a.n_kv_heads;
   const int r = blockIdx.x / nkv, kvh = blockIdx.x % nkv;
   const int chunk = blockIdx.y;
@@ -227,13 +259,19 @@ __global__ void __launch_bounds__(256) attn_chunk_kernel(const AttnArgs a) {
   const int n_ctx_chunks = (L - lo0 + kKeys - 1) / kKeys;
   float* out = a.part + ((static_cast<size_t>(r) * nkv + kvh) * a.n_chunks + chunk) * kQ * kPartStride;
   if (chunk == a.n_chunks - 1) {
+    pdl_begin();
     blk_chunk(a, smem_raw, r, kvh, out);
   } else if (chunk < n_ctx_chunks) {
     const int k_begin = lo0 + chunk * kKeys;
-    ctx_chunk(a, smem_raw, r, kvh, k_begin, min(kKeys, L - k_begin), L, out);
-  } else if (threadIdx.x < kQ) {  // no keys in this chunk
-    out[threadIdx.x * kPartStride + 0] = -INFINITY;
-    out[threadIdx.x * kPartStride + 1] = 0.f;
+    const int nk = min(kKeys, L - k_begin);
+    // rows L - nn .. L - 1 are appended by the previous kernel; older rows are not written this step
+    ctx_chunk(a, smem_raw, r, kvh, k_begin, nk, L, k_begin + nk <= L - nn, out);
+  } else {
+    pdl_begin();
+    if (threadIdx.x < kQ) {  // no keys in this chunk
+      out[threadIdx.x * kPartStride + 0] = -INFINITY;
+      out[threadIdx.x * kPartStride + 1] = 0.f;
+    }
   }
 }
 
@@ -268,12 +306,21 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   for (int u = 0; u < 2; ++u) f[u] = (l[u] > 0.f) ? exp2f(m[u] - M) : 0.f;
   const float den = warp_sum(f[0] * l[0] + f[1] * l[1]);
   float o[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = 0; c < a.n_chunks; ++c) {
-    const float fc = __shfl_sync(0xffffffffu, f[c >> 5], c & 31);
-    if (fc == 0.f) continue;  // uniform across the warp
-    const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride + 2;
+  for (int c0 = 0; c0 < a.n_chunks; c0 += 8) {  // 8 chunks' loads in flight, added in chunk order
+    float fc[8], t[8][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] += fc * pc[lane + 32 * j];
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u;
+      fc[u] = c < a.n_chunks ? __shfl_sync(0xffffffffu, f[(c >> 5) & 1], c & 31) : 0.f;
+      const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride + 2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[u][j] = fc[u] != 0.f ? pc[lane + 32 * j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (fc[u] != 0.f) o[j] += fc[u] * t[u][j];
   }
   const int ld = a.n_q_heads * kHd;
   for (int j = 0; j < 4; ++j) {

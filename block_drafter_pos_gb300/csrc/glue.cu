@@ -36,17 +36,22 @@ DF2_DEV void put_act(void* act, size_t lo, int fmt, size_t idx, float v) {
 }
 
 // Sum of the split planes p[s * plane], s = 0..S-1, added in split order.  The
-// loads of up to 32 planes are issued together so the latency is paid once per 32.
-DF2_DEV float plane_sum(const float* p, size_t plane, int S) {
+// loads of up to B planes are issued together so their latency is paid once.
+template <int B>
+DF2_DEV float plane_sum_b(const float* p, size_t plane, int S) {
   float y = 0.f;
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    float t[32];
+  for (int s0 = 0; s0 < S; s0 += B) {
+    float t[B];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) t[j] = (s0 + j < S) ? p[static_cast<size_t>(s0 + j) * plane] : 0.f;
+    for (int j = 0; j < B; ++j) t[j] = (s0 + j < S) ? p[static_cast<size_t>(s0 + j) * plane] : 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) y += t[j];
+    for (int j = 0; j < B; ++j) y += t[j];
   }
   return y;
+}
+
+DF2_DEV float plane_sum(const float* p, size_t plane, int S) {
+  return S <= 8 ? plane_sum_b<8>(p, plane, S) : plane_sum_b<32>(p, plane, S);
 }
 
 // Per-row sum of squares of this CTA's 32 channels -> ss[row][blockIdx.y] (one warp = one row).
@@ -220,15 +225,16 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
     plane = static_cast<size_t>(2 * a.n_rows) * nkv * 128;
   }
   float v[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int sp = 0; sp < a.splits; sp += 2) {  // split planes in order, two planes' loads at a time
-    float t[8];
+  for (int s0 = 0; s0 < a.splits; s0 += 8) {  // split planes in order, 8 planes' loads in flight
+    float t[8][4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      t[c] = src[sp * plane + lane + 32 * c];
-      t[4 + c] = (sp + 1 < a.splits) ? src[(sp + 1) * plane + lane + 32 * c] : 0.f;
-    }
+    for (int u = 0; u < 8; ++u)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) v[c] = (v[c] + t[c]) + t[4 + c];
+      for (int c = 0; c < 4; ++c) t[u][c] = (s0 + u < a.splits) ? src[(s0 + u) * plane + lane + 32 * c] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] += t[u][c];
   }
   if (ctx_row) {
     const float rc = warp_inv_rms(a.ss_c, row0 + jj, a.nch, a.H, a.eps);
@@ -245,11 +251,17 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
     // NEOX: out[j] = x[j] cos - x[j+64] sin; out[j+64] = x[j+64] cos + x[j] sin
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      double sn, cs;
-      sincos(static_cast<double>(pos) * a.inv_freq[lane + 32 * c], &sn, &cs);
+      // angle in FP64 (position x FP64 inverse frequency), reduced by 2 pi in FP64
+      // (Cody-Waite, with 2 pi split into a double and its remainder); only the
+      // reduced angle in [-pi, pi] goes through single-precision sin/cos
+      const double ang = static_cast<double>(pos) * a.inv_freq[lane + 32 * c];
+      const double turns = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
+      const double red = fma(-turns, 6.283185307179586, ang) - turns * 2.4492935982947064e-16;
+      float sn, cs;
+      sincosf(static_cast<float>(red), &sn, &cs);
       const float x1 = v[c], x2 = v[c + 2];
-      v[c] = static_cast<float>(x1 * cs - x2 * sn);
-      v[c + 2] = static_cast<float>(x2 * cs + x1 * sn);
+      v[c] = x1 * cs - x2 * sn;
+      v[c + 2] = x2 * cs + x1 * sn;
     }
   }
   if (!ctx_row) {
