@@ -37,6 +37,7 @@ struct dflash2_handle {
   CUtensorMap map_layer[DFLASH2_MAX_LAYERS][9];  // q k v o gate up down attn_delta mlp_delta
   // activation-buffer maps (hi rows then lo rows), encoded once the scratch exists
   CUtensorMap xm_taps, xm_a, xm_qkv, xm_o, xm_h, xm_fin;
+  CUtensorMap map_lm, xm_lm;  // LM head weights; final hidden (bf16 in both formats) for the LM head
   int* gemv_err;  // device word set by a GEMV whose pipeline wait gave up
   // scratch
   char* arena;
@@ -176,7 +177,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->nch_ss = c.hidden / 32;
   h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
-  h->lm_ctas = h->num_sms;  // one 16-warp CTA per SM (the kernel needs 128 registers a thread)
+  h->lm_ctas = lmhead_ctas(h->num_sms);
   // K splits by total 16-row tiles of each launch (independent of the request count)
   {
     // K splits by 64-row weight blocks and the size of one output plane at max_requests
@@ -276,7 +277,9 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
                    gemv_encode_xmap(&h->xm_qkv, h->act_qkv, static_cast<int>(2 * N), h->H, fmt) &&
                    gemv_encode_xmap(&h->xm_o, h->act_o, static_cast<int>(N), h->qd, fmt) &&
                    gemv_encode_xmap(&h->xm_h, h->act_h, static_cast<int>(N), h->F, fmt) &&
-                   (fmt != 0 || gemv_encode_xmap(&h->xm_fin, h->act_fin, static_cast<int>(N), h->H, 0));
+                   (fmt != 0 || gemv_encode_xmap(&h->xm_fin, h->act_fin, static_cast<int>(N), h->H, 0)) &&
+                   lm_encode_map(&h->map_lm, w->lm_head, h->H, h->V, 64) &&
+                   lm_encode_map(&h->xm_lm, h->act_fin, h->H, static_cast<int>(2 * N), 8);
   if (!xok) {
     cudaFree(h->arena);
     delete h;
@@ -544,9 +547,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // ---- a8: LM head + top-16
   {
     LmHeadArgs a;
-    a.w = static_cast<const uint16_t*>(h->w.lm_head);
-    a.x = h->act_fin;
-    a.x_lo = h->lo_fin;
+    a.wmap = h->map_lm;
+    a.xmap = h->xm_lm;
+    a.x_lo_row = N8;
     a.ss = h->ss;
     a.logits_out = logits_out;
     a.part_keys = h->topk_keys;
@@ -556,6 +559,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.nch = h->nch_ss;
     a.n_cta = h->lm_ctas;
     a.eps = c.rms_eps;
+    a.err = h->gemv_err;
     // external records: inside a stream capture they become event-record nodes the host can time
     if (h->ev_lm0) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm0, st, cudaEventRecordExternal));
     DF2_CHECK(launch_lmhead(a, pdl, st));
@@ -593,9 +597,9 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   if (!hidden || !cand_ids || !cand_logits || !aligned16(hidden)) return DFLASH2_E_INVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LmHeadArgs a;
-  a.w = static_cast<const uint16_t*>(h->w.lm_head);
-  a.x = static_cast<const uint16_t*>(hidden);
-  a.x_lo = 0;
+  a.wmap = h->map_lm;
+  if (!lm_encode_map(&a.xmap, hidden, h->H, n_rows, 8)) return DFLASH2_E_CUDA;
+  a.x_lo_row = -1;
   a.ss = nullptr;
   a.logits_out = logits_out;
   a.part_keys = h->topk_keys;
@@ -605,6 +609,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   a.nch = h->nch_ss;
   a.n_cta = h->lm_ctas;
   a.eps = h->cfg.rms_eps;
+  a.err = h->gemv_err;
   DF2_CHECK(launch_lmhead(a, h->pdl, st));
   TopkMergeArgs m;
   m.part_keys = h->topk_keys;

@@ -2,6 +2,7 @@
 // LM-head, selector and verify kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -116,15 +117,21 @@ cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_
 
 // ---------------------------------------------------------------- LM head + top-k
 struct LmHeadArgs {
-  const uint16_t* w;       // bf16 [V][H]
-  const uint16_t* x;       // bf16 [N][H]: x * final_norm_w
-  size_t x_lo;             // element offset of the low-order plane of x (0: none)
+  CUtensorMap wmap;        // LM head bf16 [V][H] (lm_encode_map, 64-row boxes)
+  CUtensorMap xmap;        // hidden bf16 [rows][H], hi plane rows then lo plane rows (8-row boxes)
+  int x_lo_row;            // first row of the low-order plane in xmap, or -1 (none)
   const float* ss;         // [N][nch] sums of squares of x, or null (x already normalised)
   float* logits_out;       // [R][7][V] or null
   unsigned long long* part_keys;  // [N][n_cta][16]
   int V, H, n_rows, nch, n_cta;
   float eps;
+  int* err;                // set nonzero if a pipeline wait gave up, or null
 };
+// Bulk-copy map of a bf16 matrix [rows][inner] in boxes of box_rows x 64 elements
+// (128-byte rows, 128-byte swizzle); rows past the end read as zero.
+bool lm_encode_map(CUtensorMap* map, const void* p, int inner, int rows, int box_rows);
+// CTAs of the LM-head launch (the per-CTA candidate lists the merge reads).
+int lmhead_ctas(int num_sms);
 cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st);
 
 struct TopkMergeArgs {

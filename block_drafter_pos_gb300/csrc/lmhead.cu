@@ -1,14 +1,16 @@
 // Shared LM head fused with the vocabulary top-16 (step a8), plus the merge that
 // also finishes the selector projection (step a9).
 //
-// The LM head [V][H] is the largest single weight stream of the step.  A
-// persistent grid walks it once: each CTA owns a contiguous range of vocabulary
-// rows and processes it in sub-blocks of 256 rows (one 16-row tile per warp,
-// mma.sync m16n8k16 with the weights as the A operand, as in gemv.cu).  The
-// sub-block's logits go to shared memory, are scaled by the row's 1/rms (final
-// RMSNorm, applied after the projection), optionally written out, and folded into
-// a running top-16 per block row.  Only the 16 best (value, index) keys per CTA
-// and row leave the kernel; the merge kernel picks the global top-16.
+// The LM head [V][H] is the largest single weight stream of the step.  It runs
+// on the same pipeline as the projections (pipeline.cuh): each CTA (two per SM)
+// owns a contiguous range of 64-row vocabulary blocks; a producer warp streams
+// the block's weights and the hidden state through a ring of shared-memory
+// stages with bulk tensor copies, and four consumer warps run the MMAs (16 rows
+// each).  When a block is done its 64 x N logits go to shared memory, are scaled
+// by the row's 1/rms (final RMSNorm, applied after the projection), optionally
+// written out, and folded into a running top-16 per block row.  Only the 16 best
+// (value, index) keys per CTA and row leave the kernel; the merge kernel picks
+// the global top-16.
 //
 // Ordering ("LSE docs/DFLASH2.md", top-k paragraph): NaN first (by index), then
 // descending value with +/-inf in their usual places, equal values -> smaller
@@ -18,162 +20,182 @@
 #include "common.cuh"
 #include "glue.h"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace df2 {
 
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kSub = kWarps * 16;  // vocabulary rows per sub-block
-constexpr int kMaxRows = 32;       // block rows (8 per request) handled by this kernel
+using namespace pipe;
+
 constexpr int kTopK = 16;
 
-template <int NT>
-__global__ void __launch_bounds__(kWarps * 32, 1) lmhead_topk_kernel(const LmHeadArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* logit = reinterpret_cast<float*>(smem_raw);                                   // [NT*8][kSub]
-  unsigned long long* run = reinterpret_cast<unsigned long long*>(logit + NT * 8 * kSub);  // [NT*8][16]
-  __shared__ float rscale[kMaxRows];
+DF2_DEV void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory"); }
+
+template <int NT, bool LO>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __grid_constant__ LmHeadArgs a) {
+  using Geo = StageGeo<0, NT>;
+  constexpr int D = Geo::kDepth;
+  constexpr int kXBoxes = kStageK / 64;  // activation boxes per tile and plane
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[D], empty_bar[D];
+  __shared__ float logit[NT * 8][kBlockRows + 1];
+  __shared__ unsigned long long run[NT * 8][kTopK];
+  __shared__ float rscale[NT * 8];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int g = lane >> 2, q = lane & 3;
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t full0 = smem_u32(&full_bar[0]), empty0 = smem_u32(&empty_bar[0]);
   const int n_rows = a.n_rows;
-  const int nt = n_rows >> 3;  // n-tiles actually present (<= NT)
-  const int tiles_total = a.V / 16;
-  const int t0 = static_cast<int>((static_cast<long long>(tiles_total) * blockIdx.x) / gridDim.x);
-  const int t1 = static_cast<int>((static_cast<long long>(tiles_total) * (blockIdx.x + 1)) / gridDim.x);
-  for (int e = threadIdx.x; e < NT * 8 * kTopK; e += blockDim.x) run[e] = 0ull;
+  const int nt = n_rows >> 3;
+  for (int e = threadIdx.x; e < NT * 8 * kTopK; e += blockDim.x) (&run[0][0])[e] = 0ull;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < D; ++s) {
+      mbar_init_count(full0 + 8 * s, 1);
+      mbar_init_count(empty0 + 8 * s, kConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   pdl_trigger();
-  bool waited = false;
-  for (int tb = t0; tb < t1; tb += kWarps) {
-    const int tile = tb + wid;
-    // ---- GEMV: one 16-row tile per warp
-    if (tile < t1) {
-      const int row0 = tile * 16;
-      const __nv_bfloat16* w0 = reinterpret_cast<const __nv_bfloat16*>(a.w) + static_cast<size_t>(row0 + g) * a.H + 8 * q;
-      const __nv_bfloat16* w1 = w0 + static_cast<size_t>(8) * a.H;
-      const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(a.x) + static_cast<size_t>(g) * a.H + 8 * q;
-      float acc[NT][4];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-      uint4 ra[4], rb[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ra[j] = ld_stream(w0 + 32 * j);
-        rb[j] = ld_stream(w1 + 32 * j);
+  const int blocks = (a.V + kBlockRows - 1) / kBlockRows;
+  const int b0 = static_cast<int>((static_cast<long long>(blocks) * blockIdx.x) / gridDim.x);
+  const int b1 = static_cast<int>((static_cast<long long>(blocks) * (blockIdx.x + 1)) / gridDim.x);
+  const int nst = a.H / kStageK;
+  const int total = (b1 - b0) * nst;  // stages of this CTA: block b0 + it / nst, K (it % nst) * kStageK
+
+  if (wid == kConsumers) {
+    // ---------------------------------------------------------------- producer warp
+    const uint64_t policy = evict_first_policy(), xpolicy = evict_last_policy();
+    const int xbytes = nt * kXBoxes * 1024 * (LO ? 2 : 1);
+    auto arm_w = [&](int it) {
+      const int slot = it % D;
+      if (lane == 0) mbar_expect_tx(full0 + 8 * slot, Geo::kWBytes + xbytes);
+      __syncwarp();
+      if (lane < kStageK / 64)
+        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<0>(), &a.wmap, (it % nst) * kStageK + lane * 64,
+                    (b0 + it / nst) * kBlockRows, full0 + 8 * slot, policy);
+    };
+    auto issue_x = [&](int it) {
+      const int slot = it % D;
+      const int n = nt * kXBoxes * (LO ? 2 : 1);
+      for (int i = lane; i < n; i += 32) {
+        const int plane = i / (nt * kXBoxes), rem = i % (nt * kXBoxes);
+        const int t = rem / kXBoxes, b = rem % kXBoxes;
+        tma_load_2d(ring + slot * Geo::kBytes + Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + b) * 1024,
+                    &a.xmap, (it % nst) * kStageK + b * 64, plane * a.x_lo_row + t * 8, full0 + 8 * slot, xpolicy);
       }
-      if (!waited) {  // weights first; the hidden state comes from the previous kernel
-        pdl_wait();
-        waited = true;
+    };
+    const int np = total < D ? total : D;
+    for (int it = 0; it < np; ++it) arm_w(it);  // weights first: they do not depend on the previous kernel
+    pdl_wait();
+    bool ok = true;
+    int it = 0;
+    for (; it < total; ++it) {
+      if (it >= np) {
+        if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * (it % D), static_cast<uint32_t>(((it / D) + 1) & 1)))) {
+          ok = false;
+          break;
+        }
+        arm_w(it);
       }
-      for (int k = 0; k < a.H; k += 128) {
-        uint4 ca[4], cb[4];
+      issue_x(it);
+    }
+    if (!ok && lane == 0 && a.err != nullptr) atomicExch(a.err, 1);
+    for (int j = it > D ? it - D : 0; j < it; ++j) mbar_wait(full0 + 8 * (j % D), static_cast<uint32_t>((j / D) & 1));
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumer warps
+  pdl_wait();
+  for (int n = wid; n < n_rows; n += kConsumers) {  // final-norm scale of each row (1: already normalised)
+    const float rs = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
+    if (lane == 0) rscale[n] = rs;
+  }
+  const int g = lane >> 2, q = lane & 3;
+  const uint32_t wrow = static_cast<uint32_t>((wid * 16 + g) * 128);
+  const uint32_t xrow = static_cast<uint32_t>(g * 128);
+  float c0[NT][4], c1[NT][4], c2[NT][4], c3[NT][4];
+  for (int it = 0; it < total; ++it) {
+    const int st = it % nst;
+    if (st == 0) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ca[j] = ra[j];
-          cb[j] = rb[j];
-        }
-        if (k + 128 < a.H) {
+      for (int t = 0; t < NT; ++t)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            ra[j] = ld_stream(w0 + k + 128 + 32 * j);
-            rb[j] = ld_stream(w1 + k + 128 + 32 * j);
-          }
-        }
+        for (int e = 0; e < 4; ++e) c0[t][e] = c1[t][e] = c2[t][e] = c3[t][e] = 0.f;
+    }
+    const int slot = it % D;
+    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, static_cast<uint32_t>((it / D) & 1)))) {
+      if (lane == 0 && a.err != nullptr) atomicExch(a.err, 1);
+      break;
+    }
+    const uint32_t base = ring + slot * Geo::kBytes;
+    stage_bf16<NT, LO>(nt, base + wrow, base + Geo::kWBytes + xrow, g, q, c0, c1, c2, c3);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    if (st + 1 < nst) continue;
+    // ---- block done: logits to shared memory, then scale, write out and fold into the top-16
+    const int lr = wid * 16 + g;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (t < nt) {
-            const __nv_bfloat16* xt = xb + static_cast<size_t>(t * 8) * a.H + k;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 x = ld_cached(xt + 32 * j);
-              mma_bf16(acc[t], ca[j].x, cb[j].x, ca[j].y, cb[j].y, x.x, x.y);
-              mma_bf16(acc[t], ca[j].z, cb[j].z, ca[j].w, cb[j].w, x.z, x.w);
-              if (a.x_lo) {  // low-order part of the hidden state: x = hi + lo
-                const uint4 y = ld_cached(xt + a.x_lo + 32 * j);
-                mma_bf16(acc[t], ca[j].x, cb[j].x, ca[j].y, cb[j].y, y.x, y.y);
-                mma_bf16(acc[t], ca[j].z, cb[j].z, ca[j].w, cb[j].w, y.z, y.w);
-              }
-            }
-          }
-        }
-      }
-      const int lr = wid * 16 + g;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (t >= nt) break;
+    for (int t = 0; t < NT; ++t) {
+      if (t < nt) {
         const int n0 = t * 8 + 2 * q;
-        logit[(n0)*kSub + lr] = acc[t][0];
-        logit[(n0 + 1) * kSub + lr] = acc[t][1];
-        logit[(n0)*kSub + lr + 8] = acc[t][2];
-        logit[(n0 + 1) * kSub + lr + 8] = acc[t][3];
+        logit[n0][lr] = (c0[t][0] + c1[t][0]) + (c2[t][0] + c3[t][0]);
+        logit[n0 + 1][lr] = (c0[t][1] + c1[t][1]) + (c2[t][1] + c3[t][1]);
+        logit[n0][lr + 8] = (c0[t][2] + c1[t][2]) + (c2[t][2] + c3[t][2]);
+        logit[n0 + 1][lr + 8] = (c0[t][3] + c1[t][3]) + (c2[t][3] + c3[t][3]);
       }
     }
-    if (!waited) {  // warps without a tile in this sub-block
-      pdl_wait();
-      waited = true;
-    }
-    if (tb == t0) {  // final-norm scale of each row (1 when the input is already normalised)
-      for (int n = wid; n < n_rows; n += kWarps) {
-        const float rs = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
-        if (lane == 0) rscale[n] = rs;
-      }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n_rows * kSub; e += blockDim.x) logit[e] *= rscale[e / kSub];
-    __syncthreads();
-    const int v0 = tb * 16;
-    const int nv = min(kSub, (t1 - tb) * 16);
-    // ---- optional full logits (positions 1..7 only)
-    if (a.logits_out) {
-      for (int e = threadIdx.x; e < n_rows * kSub; e += blockDim.x) {
-        const int n = e / kSub, j = e % kSub;
-        const int pos = n & 7;
-        if (pos != 0 && j < nv) {
-          const int rq = n >> 3;
-          a.logits_out[(static_cast<size_t>(rq) * 7 + pos - 1) * a.V + v0 + j] = logit[n * kSub + j];
-        }
-      }
-    }
-    // ---- running top-16 per row: warp w handles rows w, w + 16, ...
-    for (int n = wid; n < n_rows; n += kWarps) {
-      if ((n & 7) == 0) continue;  // the anchor position is not sampled
-      unsigned long long* rn = run + n * kTopK;
+    consumer_sync();
+    const int v0 = (b0 + it / nst) * kBlockRows;
+    for (int n = wid; n < n_rows; n += kConsumers) {
+      const int pos = n & 7;
+      if (pos == 0) continue;  // the anchor position is not sampled
+      const float rs = rscale[n];
+      unsigned long long* rn = run[n];
       const unsigned long long thr = rn[kTopK - 1];
-      unsigned long long mine[kSub / 32];
+      unsigned long long mine[2];
       bool any = false;
 #pragma unroll
-      for (int j = 0; j < kSub / 32; ++j) {
+      for (int j = 0; j < 2; ++j) {
         const int idx = lane + 32 * j;
-        const unsigned long long key = idx < nv ? topk_key(logit[n * kSub + idx], static_cast<uint32_t>(v0 + idx)) : 0ull;
+        const int v = v0 + idx;
+        const float val = logit[n][idx] * rs;
+        if (a.logits_out != nullptr && v < a.V)
+          a.logits_out[(static_cast<size_t>(n >> 3) * 7 + pos - 1) * a.V + v] = val;
+        const unsigned long long key = v < a.V ? topk_key(val, static_cast<uint32_t>(v)) : 0ull;
         mine[j] = key > thr ? key : 0ull;
         any |= mine[j] != 0ull;
       }
       if (!__any_sync(0xffffffffu, any)) continue;
+      // insert the passing candidates one by one into the sorted list held by lanes
+      // 0..15 (descending): rank by ballot, shift the tail down one lane
       unsigned long long held = lane < kTopK ? rn[lane] : 0ull;
-      unsigned long long result = 0ull;
-      for (int round = 0; round < kTopK; ++round) {
-        unsigned long long best = held;
+      unsigned long long cut = thr;
 #pragma unroll
-        for (int j = 0; j < kSub / 32; ++j) best = mine[j] > best ? mine[j] : best;
-        const unsigned long long win = warp_max_u64(best);
-        if (lane == round) result = win;
-        if (win != 0ull) {
-          if (held == win) held = 0ull;
-#pragma unroll
-          for (int j = 0; j < kSub / 32; ++j)
-            if (mine[j] == win) mine[j] = 0ull;
+      for (int j = 0; j < 2; ++j) {
+        unsigned m = __ballot_sync(0xffffffffu, mine[j] != 0ull);
+        while (m != 0u) {
+          const int src = __ffs(m) - 1;
+          m &= m - 1u;
+          const unsigned long long cand = __shfl_sync(0xffffffffu, mine[j], src);
+          if (cand <= cut) continue;  // uniform: every lane holds the same cut
+          const int p = __popc(__ballot_sync(0xffffffffu, lane < kTopK && held > cand));
+          const unsigned long long up = __shfl_up_sync(0xffffffffu, held, 1);
+          if (lane < kTopK && lane > p) held = up;
+          if (lane == p) held = cand;
+          cut = __shfl_sync(0xffffffffu, held, kTopK - 1);
         }
       }
-      __syncwarp();
-      if (lane < kTopK) rn[lane] = result;
+      if (lane < kTopK) rn[lane] = held;
       __syncwarp();
     }
-    __syncthreads();
+    consumer_sync();  // the logit tile is free for the next block
   }
   // ---- per-CTA top-16 out
-  for (int e = threadIdx.x; e < n_rows * kTopK; e += blockDim.x) {
+  for (int e = threadIdx.x; e < n_rows * kTopK; e += kConsumers * 32) {
     const int n = e / kTopK, j = e % kTopK;
-    a.part_keys[(static_cast<size_t>(n) * a.n_cta + blockIdx.x) * kTopK + j] = run[n * kTopK + j];
+    a.part_keys[(static_cast<size_t>(n) * a.n_cta + blockIdx.x) * kTopK + j] = run[n][j];
   }
 }
 
@@ -191,17 +213,23 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
     const float v = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
     if (lane == 0) rs = v;
   }
-  const int total = a.n_cta * kTopK;
+  const int total = a.n_cta * kTopK;  // <= 256 * kPer (checked at launch)
   const unsigned long long* src = a.part_keys + static_cast<size_t>(n) * total;
+  constexpr int kPer = 32;
+  unsigned long long keys[kPer];  // every CTA's list, loaded once
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = threadIdx.x + 256 * j;
+    keys[j] = e < total ? src[e] : 0ull;
+  }
   // keys are unique (distinct indices) and picked in decreasing order, so the keys
   // still available in a round are exactly those below the previous winner.
   unsigned long long last = ~0ull;
   for (int round = 0; round < kTopK; ++round) {
     unsigned long long best = 0ull;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-      const unsigned long long k = src[e];
-      if (k < last && k > best) best = k;
-    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (keys[j] < last && keys[j] > best) best = keys[j];
     best = warp_max_u64(best);
     if (lane == 0) wbest[wid] = best;
     __syncthreads();
@@ -232,30 +260,34 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   }
 }
 
-template <int NT>
+template <int NT, bool LO>
 cudaError_t launch_nt(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(NT) * 8 * kSub * sizeof(float) + static_cast<size_t>(NT) * 8 * kTopK * 8;
+  constexpr int smem = StageGeo<0, NT>::kSmem;
   static bool attr_set = false;  // set once, outside any later stream capture
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<NT, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(lmhead_topk_kernel<NT>, dim3(a.n_cta), dim3(kWarps * 32), smem, st, pdl, a);
+  return launch_ex(lmhead_kernel<NT, LO>, dim3(a.n_cta), dim3(kThreads), smem, st, pdl, a);
 }
 
 }  // namespace
 
+int lmhead_ctas(int num_sms) { return num_sms * kCtasPerSm; }
+
 cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
   const int nt = a.n_rows / 8;
-  if (nt <= 1) return launch_nt<1>(a, pdl, st);
-  if (nt <= 2) return launch_nt<2>(a, pdl, st);
-  if (nt <= 4) return launch_nt<4>(a, pdl, st);
+  if (a.n_rows < 8 || a.n_rows % 8 || a.H % kStageK || a.n_cta < 1) return cudaErrorInvalidValue;
+  const bool lo = a.x_lo_row >= 0;
+  if (nt <= 1) return lo ? launch_nt<1, true>(a, pdl, st) : launch_nt<1, false>(a, pdl, st);
+  if (nt <= 2) return lo ? launch_nt<2, true>(a, pdl, st) : launch_nt<2, false>(a, pdl, st);
+  if (nt <= 4) return lo ? launch_nt<4, true>(a, pdl, st) : launch_nt<4, false>(a, pdl, st);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st) {
+  if (a.n_cta < 1 || a.n_cta * kTopK > 256 * 32) return cudaErrorInvalidValue;
   return launch_ex(topk_merge_kernel, dim3(a.n_rows), dim3(256), 0, st, pdl, a);
 }
 

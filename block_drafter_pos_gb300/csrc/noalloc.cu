@@ -50,7 +50,8 @@ cudaError_t device_slot(DeviceSlot* out) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     g_slots[dev].keys = static_cast<unsigned long long*>(p);
-    g_slots[dev].n_cta = sms < DFLASH2_NOALLOC_MAX_CTAS ? sms : DFLASH2_NOALLOC_MAX_CTAS;
+    const int ctas = lmhead_ctas(sms);
+    g_slots[dev].n_cta = ctas < DFLASH2_NOALLOC_MAX_CTAS ? ctas : DFLASH2_NOALLOC_MAX_CTAS;
     g_ready[dev] = true;
   }
   *out = g_slots[dev];
@@ -74,18 +75,20 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   // Every (row, CTA) list the merge reads is rewritten by the LM-head launch
   // first, so nothing left in the array by an earlier call is ever read.
   LmHeadArgs a;
-  a.w = static_cast<const uint16_t*>(lm_head);
-  a.x = static_cast<const uint16_t*>(hidden);
-  a.x_lo = 0;
+  // bulk-copy descriptors live in the kernel's parameters: encoding them allocates nothing
+  if (!lm_encode_map(&a.wmap, lm_head, hidden_dim, vocab, 64) || !lm_encode_map(&a.xmap, hidden, hidden_dim, n_rows, 8))
+    return DFLASH2_E_CUDA;
+  a.x_lo_row = -1;
   a.ss = nullptr;
   a.logits_out = logits_out;
   a.part_keys = slot.keys;
   a.V = vocab;
   a.H = hidden_dim;
   a.n_rows = n_rows;
-  a.nch = hidden_dim / 128;
+  a.nch = hidden_dim / 32;
   a.n_cta = slot.n_cta;
   a.eps = 0.f;
+  a.err = nullptr;
   if (launch_lmhead(a, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
   TopkMergeArgs m;
   m.part_keys = slot.keys;
