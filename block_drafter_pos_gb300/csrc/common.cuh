@@ -84,8 +84,15 @@ DF2_DEV float warp_max(float v) {
 }
 
 DF2_DEV float warp_inv_rms(const float* ss, int row, int nch, int H, float eps) {
+  const float* p = ss + static_cast<size_t>(row) * nch + (threadIdx.x & 31);
   float s = 0.f;
-  for (int j = threadIdx.x & 31; j < nch; j += 32) s += ss[static_cast<size_t>(row) * nch + j];
+  for (int j0 = 0; j0 < nch; j0 += 256) {  // up to 8 loads per lane in flight, added in order
+    float t[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) t[u] = (j0 + 32 * u + static_cast<int>(threadIdx.x & 31) < nch) ? p[j0 + 32 * u] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += t[u];
+  }
   s = warp_sum(s);
   return rsqrtf(s / static_cast<float>(H) + eps);
 }

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __gr
 // grid (n_rows), 256 threads: global top-16 of one block row from the per-CTA lists,
 // and the selector gate of that row (sum of split partials, times 1/rms).
 __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) {
-  __shared__ unsigned long long wbest[8];
+  __shared__ unsigned long long wtop[8][kTopK];
   __shared__ float rs;
   pdl_begin();
   const int n = blockIdx.x;
@@ -224,23 +224,36 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   }
   // keys are unique (distinct indices) and picked in decreasing order, so the keys
   // still available in a round are exactly those below the previous winner.
-  unsigned long long last = ~0ull;
+  // Level 1: each warp's top-16 of its own keys (no block barrier).
+  unsigned long long last = ~0ull, mine16 = 0ull;
   for (int round = 0; round < kTopK; ++round) {
     unsigned long long best = 0ull;
 #pragma unroll
     for (int j = 0; j < kPer; ++j)
       if (keys[j] < last && keys[j] > best) best = keys[j];
-    best = warp_max_u64(best);
-    if (lane == 0) wbest[wid] = best;
-    __syncthreads();
-    unsigned long long win = 0ull;
-    for (int w = 0; w < 8; ++w) win = wbest[w] > win ? wbest[w] : win;
-    __syncthreads();
-    last = win;
-    if (threadIdx.x == 0) {
-      const size_t o = (static_cast<size_t>(rq) * 7 + pos - 1) * kTopK + round;
-      a.cand_ids[o] = static_cast<int32_t>(key_index(win));
-      a.cand_logits[o] = key_value(win);
+    last = warp_max_u64(best);
+    if (lane == round) mine16 = last;
+  }
+  if (lane < kTopK) wtop[wid][lane] = mine16;
+  __syncthreads();
+  // Level 2: warp 0 merges the 8 lists (4 keys per lane).
+  if (wid == 0) {
+    unsigned long long k4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k4[j] = (&wtop[0][0])[lane + 32 * j];
+    last = ~0ull;
+    for (int round = 0; round < kTopK; ++round) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (k4[j] < last && k4[j] > best) best = k4[j];
+      const unsigned long long win = warp_max_u64(best);
+      last = win;
+      if (lane == 0) {
+        const size_t o = (static_cast<size_t>(rq) * 7 + pos - 1) * kTopK + round;
+        a.cand_ids[o] = static_cast<int32_t>(key_index(win));
+        a.cand_logits[o] = key_value(win);
+      }
     }
   }
   __syncthreads();

@@ -110,29 +110,48 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   // stage every needed codebook row at once (one round trip): row k < kRowsA is the
   // predecessor row A[id], k >= kRowsA the successor row B[id]
   const int chunks = a.fmt == 0 ? kRank * 2 / 16 : kRank / 16;  // 16-byte pieces per row
-  for (int e = tid; e < kRows * chunks; e += kThreads) {
-    const int k = e / chunks, c = e % chunks;
-    int id;
-    const void* cb;
-    if (k < kRowsA) {
-      id = k == 0 ? anchor : sm.cids[(k - 1) / kK][(k - 1) % kK];
-      cb = a.cb_a;
-    } else {
-      id = sm.cids[(k - kRowsA) / kK][(k - kRowsA) % kK];
-      cb = a.cb_b;
-    }
-    if (a.fmt == 0) {
-      *reinterpret_cast<uint4*>(&sm.bf[k][c * 8]) =
-          ld_cached(reinterpret_cast<const uint16_t*>(cb) + static_cast<size_t>(id) * kRank + c * 8);
-    } else {
-      *reinterpret_cast<uint4*>(&sm.q8[k][c * 16]) =
-          ld_cached(reinterpret_cast<const int8_t*>(cb) + static_cast<size_t>(id) * kRank + c * 16);
-      if (c < 4) {
-        const uint16_t* sc = k < kRowsA ? a.cb_a_scale : a.cb_b_scale;
-        const uint16_t* bi = k < kRowsA ? a.cb_a_bias : a.cb_b_bias;
-        sm.sb[k][c] = sc[static_cast<size_t>(id) * 4 + c];
-        sm.sb[k][4 + c] = bi[static_cast<size_t>(id) * 4 + c];
+  // every thread's pieces are loaded first (all in flight together), then stored
+  constexpr int kPer = (kRows * kRank * 2 / 16 + kThreads - 1) / kThreads;
+  uint4 piece[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = tid + kThreads * j;
+    piece[j] = make_uint4(0, 0, 0, 0);
+    if (e < kRows * chunks) {
+      const int k = e / chunks, c = e % chunks;
+      int id;
+      const void* cb;
+      if (k < kRowsA) {
+        id = k == 0 ? anchor : sm.cids[(k - 1) / kK][(k - 1) % kK];
+        cb = a.cb_a;
+      } else {
+        id = sm.cids[(k - kRowsA) / kK][(k - kRowsA) % kK];
+        cb = a.cb_b;
       }
+      piece[j] = a.fmt == 0 ? ld_cached(reinterpret_cast<const uint16_t*>(cb) + static_cast<size_t>(id) * kRank + c * 8)
+                            : ld_cached(reinterpret_cast<const int8_t*>(cb) + static_cast<size_t>(id) * kRank + c * 16);
+    }
+  }
+  if (a.fmt != 0) {  // Q8: 4 groups of (scale, bias) per row
+    for (int e = tid; e < kRows * 4; e += kThreads) {
+      const int k = e >> 2, c = e & 3;
+      const int id = k < kRowsA ? (k == 0 ? anchor : sm.cids[(k - 1) / kK][(k - 1) % kK])
+                                : sm.cids[(k - kRowsA) / kK][(k - kRowsA) % kK];
+      const uint16_t* sc = k < kRowsA ? a.cb_a_scale : a.cb_b_scale;
+      const uint16_t* bi = k < kRowsA ? a.cb_a_bias : a.cb_b_bias;
+      sm.sb[k][c] = sc[static_cast<size_t>(id) * 4 + c];
+      sm.sb[k][4 + c] = bi[static_cast<size_t>(id) * 4 + c];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = tid + kThreads * j;
+    if (e < kRows * chunks) {
+      const int k = e / chunks, c = e % chunks;
+      if (a.fmt == 0)
+        *reinterpret_cast<uint4*>(&sm.bf[k][c * 8]) = piece[j];
+      else
+        *reinterpret_cast<uint4*>(&sm.q8[k][c * 16]) = piece[j];
     }
   }
   __syncthreads();
