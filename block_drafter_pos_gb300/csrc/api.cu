@@ -353,10 +353,36 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     DF2_CHECK(launch_start(a, R, pdl, st));
     h->launches++;
   }
-  // ---- a1: taps projection fc [H][n_taps H], then hidden_norm input of the context rows
+  // conv before the attention sublayer of layer l (delta projection already in dproj)
+  auto conv_in_attn = [&](int l) {
+    const dflash2_layer_weights& L = h->w.layers[l];
+    ConvInArgs a;
+    a.dproj = h->dproj;
+    a.ss = h->ss;
+    a.x = h->x;
+    a.norm_w = static_cast<const uint16_t*>(L.input_norm);
+    a.base = static_cast<const uint16_t*>(L.attn_base);
+    a.delta = h->delta_a;
+    a.act = h->act_qkv;
+    a.act_lo = h->lo_qkv;
+    a.H = H;
+    a.nch = h->nch_ss;
+    a.fmt = fmt;
+    a.splits = h->s_delta;
+    a.n_rows = N;
+    a.eps = c.rms_eps;
+    return a;
+  };
+  // ---- a1 and layer 0's a3: the taps projection fc [H][n_taps H] and the first
+  // delta projection read only what the start kernel wrote, so they share a launch;
+  // so do the hidden_norm input of the context rows and the first conv-in.
   {
     dflash2_status s =
-        run_gemv(h, {seg(h->map_fc, h->w.fc, h->xm_taps, N8, R, H, h->KT, h->s_fc, h->fc_out)}, st);
+        run_gemv(h,
+                 {seg(h->map_fc, h->w.fc, h->xm_taps, N8, R, H, h->KT, h->s_fc, h->fc_out),
+                  seg(h->map_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta,
+                      h->dproj)},
+                 st);
     if (s) return s;
     FcFinishArgs a;
     a.y = h->fc_out;
@@ -370,34 +396,20 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.fmt = fmt;
     a.splits = h->s_fc;
     a.n_rows = N;
-    DF2_CHECK(launch_fc_finish(a, R, pdl, st));
+    DF2_CHECK(launch_fc_finish_conv_in(a, conv_in_attn(0), R, pdl, st));
     h->launches++;
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& L = h->w.layers[l];
     uint16_t* kc = static_cast<uint16_t*>(k_cache) + l * layer_stride;
     uint16_t* vc = static_cast<uint16_t*>(v_cache) + l * layer_stride;
-    // ---- a3: delta projection of the normed input, conv-in
-    dflash2_status s =
-        run_gemv(h, {seg(h->map_layer[l][kAttnDelta], L.attn_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta, h->dproj)}, st);
-    if (s) return s;
-    {
-      ConvInArgs a;
-      a.dproj = h->dproj;
-      a.ss = h->ss;
-      a.x = h->x;
-      a.norm_w = static_cast<const uint16_t*>(L.input_norm);
-      a.base = static_cast<const uint16_t*>(L.attn_base);
-      a.delta = h->delta_a;
-      a.act = h->act_qkv;
-      a.act_lo = h->lo_qkv;
-      a.H = H;
-      a.nch = h->nch_ss;
-      a.fmt = fmt;
-      a.splits = h->s_delta;
-      a.n_rows = N;
-      a.eps = c.rms_eps;
-      DF2_CHECK(launch_conv_in(a, R, pdl, st));
+    dflash2_status s = DFLASH2_OK;
+    if (l > 0) {
+      // ---- a3: delta projection of the normed input, conv-in
+      s = run_gemv(h, {seg(h->map_layer[l][kAttnDelta], L.attn_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta, h->dproj)},
+                   st);
+      if (s) return s;
+      DF2_CHECK(launch_conv_in(conv_in_attn(l), R, pdl, st));
       h->launches++;
     }
     // ---- a4: q (block rows), k and v (block + new context rows)

@@ -89,8 +89,7 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
 // ------------------------------------------------------------------ taps projection finish
 // c = y * w_hidden_norm into the context rows of the QKV input (1/rms of y is
 // applied after the K/V projection); ss of y.
-__global__ void __launch_bounds__(kThreads) fc_finish_kernel(const FcFinishArgs a) {
-  pdl_begin();
+DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
   const float y = plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, a.splits);
@@ -101,9 +100,8 @@ __global__ void __launch_bounds__(kThreads) fc_finish_kernel(const FcFinishArgs 
 // ------------------------------------------------------------------ conv before a sublayer
 // r_i = 1/rms(x_i); delta = r_i * (W_delta (x_i * w)) for all four (io, tap) rows;
 // a_i = r_i x_i w;  a'_i = (b0 + d0_i) a_i + (b1 + d1_i) a_{i-1}.
-__global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
+DF2_DEV void conv_in_body(const ConvInArgs& a) {
   __shared__ float ash[kB][kCw];
-  pdl_begin();
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
   const int c = blockIdx.y * kCw + lane;
@@ -141,6 +139,22 @@ __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
   const float prev = i > 0 ? ash[i - 1][lane] : 0.f;
   const float b0 = bf16_to_f32(a.base[c]), b1 = bf16_to_f32(a.base[a.H + c]);
   put_act(a.act, a.act_lo, a.fmt, idx, (b0 + d0) * ai + (b1 + d1) * prev);
+}
+
+__global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
+  pdl_begin();
+  conv_in_body(a);
+}
+
+// First layer: the taps-projection finish and the conv before the attention
+// sublayer read different inputs and write different outputs, so they share one
+// launch (blockIdx.z selects the role).
+__global__ void __launch_bounds__(kThreads) fc_finish_conv_in_kernel(const FcFinishArgs f, const ConvInArgs c) {
+  pdl_begin();
+  if (blockIdx.z == 0)
+    fc_finish_body(f);
+  else
+    conv_in_body(c);
 }
 
 // ------------------------------------------------------------------ conv after a sublayer + residual
@@ -285,8 +299,9 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st) {
   return launch_ex(start_kernel, dim3(n_req, (a.H + a.n_taps * a.H) / kCw), dim3(kThreads), 0, st, pdl, a);
 }
-cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(fc_finish_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
+cudaError_t launch_fc_finish_conv_in(const FcFinishArgs& f, const ConvInArgs& c, int n_req, bool pdl, cudaStream_t st) {
+  if (f.H != c.H) return cudaErrorInvalidValue;
+  return launch_ex(fc_finish_conv_in_kernel, dim3(n_req, f.H / kCw, 2), dim3(kThreads), 0, st, pdl, f, c);
 }
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st) {
   return launch_ex(conv_in_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);

@@ -92,8 +92,8 @@ struct QkvFinishArgs {
 };
 
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st);
-cudaError_t launch_fc_finish(const FcFinishArgs& a, int n_req, bool pdl, cudaStream_t st);
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st);
+cudaError_t launch_fc_finish_conv_in(const FcFinishArgs& f, const ConvInArgs& c, int n_req, bool pdl, cudaStream_t st);
 cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st);
 cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st);
 cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, bool pdl, cudaStream_t st);

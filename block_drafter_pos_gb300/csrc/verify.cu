@@ -22,10 +22,12 @@ namespace {
 
 constexpr int kB = 8, kP = 7, kK = 16;
 
+// The target logits and temperatures are caller inputs, so the chunk statistics are
+// computed before the wait on the previous kernel; only the store waits.
 __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   __shared__ float sm_m[8], sm_s[8];
   __shared__ int sm_a[8], sm_f[8];
-  pdl_begin();
+  pdl_trigger();
   const int rj = blockIdx.x;  // r * 8 + j
   const int r = rj >> 3;
   const int chunk = blockIdx.y;
@@ -34,11 +36,21 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   const int v0 = chunk * kVerifyChunk;
   const int v1 = min(a.V, v0 + kVerifyChunk);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int kPer = kVerifyChunk / 256;
+  float xs[kPer];  // this thread's logits of the chunk, loaded once (all in flight)
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + 256 * j;
+    xs[j] = v < v1 ? z[v] : -INFINITY;
+  }
   float m = -INFINITY;
   int arg = 0x7FFFFFFF;
   int flags = 0;
-  for (int v = v0 + threadIdx.x; v < v1; v += 256) {
-    const float x = z[v];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + 256 * j;
+    const float x = xs[j];
+    if (v >= v1) continue;
     if (isnan(x)) {
       flags |= 1;
       continue;
@@ -77,9 +89,10 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   float s = 0.f;
   if (T > 0.f && M > -INFINITY && M < INFINITY) {
     const float inv_t = 1.f / T;
-    for (int v = v0 + threadIdx.x; v < v1; v += 256) {
-      const float x = z[v];
-      if (!isnan(x)) s += expf((x - M) * inv_t);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = v0 + threadIdx.x + 256 * j;
+      if (v < v1 && !isnan(xs[j])) s += expf((xs[j] - M) * inv_t);
     }
     s = warp_sum(s);
     __syncthreads();
@@ -88,6 +101,7 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
     s = 0.f;
     for (int w = 0; w < 8; ++w) s += sm_s[w];
   }
+  pdl_wait();  // the statistics buffer is read by the previous step's chain kernel
   if (threadIdx.x == 0) {
     VerifyStat st;
     st.m = M;
