@@ -30,8 +30,8 @@ struct dflash2_handle {
   int H, G, F, V, nq, nkv, qd, kvd, KT;
   int nch_ss;  // 32-channel chunks of the sums-of-squares partials
   int n_attn_chunks, n_verify_chunks, lm_ctas;
-  // K splits of each projection (fixed at create from the grid size)
-  int s_fc, s_delta, s_qkv, s_o, s_gu, s_down, s_sel;
+  // where each projection's partial planes are (the launches' shapes are fixed at create)
+  GemvPlanes pl_fc, pl_d0, pl_d, pl_q, pl_k, pl_v, pl_o, pl_g, pl_u, pl_down, pl_sel;
   // tensor maps of the projection matrices (bulk-copy descriptors, encoded at create)
   CUtensorMap map_fc, map_sel;
   CUtensorMap map_layer[DFLASH2_MAX_LAYERS][9];  // q k v o gate up down attn_delta mlp_delta
@@ -71,7 +71,7 @@ enum { kQ, kK, kV, kO, kGate, kUp, kDown, kAttnDelta, kMlpDelta };
 
 // x_rows: rows of one plane of the activation buffer behind xmap (its lo plane starts there).
 GemvSeg seg(const CUtensorMap& wmap, const dflash2_matrix& m, const CUtensorMap& xmap, int x_rows, int n_tiles, int M,
-            int K, int splits, float* out) {
+            int K, float* out) {
   GemvSeg s;
   memset(&s, 0, sizeof(s));
   s.wmap = wmap;
@@ -82,7 +82,6 @@ GemvSeg seg(const CUtensorMap& wmap, const dflash2_matrix& m, const CUtensorMap&
   s.M = M;
   s.K = K;
   s.n_tiles = n_tiles;
-  s.splits = splits;
   s.out = out;
   return s;
 }
@@ -178,20 +177,38 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
   h->lm_ctas = lmhead_ctas(h->num_sms);
-  // K splits by total 16-row tiles of each launch (independent of the request count)
+  // plane maps of every projection launch (shapes only; the same plan as launch_gemv's)
+  int maxp_fc = 0, maxp_d = 0, maxp_q = 0, maxp_k = 0, maxp_v = 0, maxp_y = 0, maxp_g = 0, maxp_u = 0, maxp_sel = 0;
   {
-    // K splits by 64-row weight blocks and the size of one output plane at max_requests
-    const double N8 = 8.0 * max_requests, fb = 4.0;
-    h->s_fc = gemv_choose_splits(h->H / 64, h->KT, N8 * h->H * fb, h->num_sms, fmt);
-    h->s_delta = gemv_choose_splits(4 * h->G / 64, h->H, N8 * 4 * h->G * fb, h->num_sms, fmt);
-    h->s_qkv = gemv_choose_splits((h->qd + 2 * h->kvd) / 64, h->H, N8 * (h->qd + 4 * h->kvd) * fb, h->num_sms, fmt);
-    h->s_o = gemv_choose_splits(h->H / 64, h->qd, N8 * h->H * fb, h->num_sms, fmt);
-    h->s_gu = gemv_choose_splits(2 * h->F / 64, h->H, N8 * 2 * h->F * fb, h->num_sms, fmt);
-    h->s_down = gemv_choose_splits(h->H / 64, h->F, N8 * h->H * fb, h->num_sms, fmt);
-    h->s_sel = gemv_choose_splits(c.rank / 64, h->H, N8 * c.rank * fb, h->num_sms, fmt);
+    auto shape = [](int M, int K) {
+      GemvSeg g;
+      memset(&g, 0, sizeof(g));
+      g.M = M;
+      g.K = K;
+      g.n_tiles = 1;
+      return g;
+    };
+    auto plan = [&](std::initializer_list<GemvSeg> segs, std::initializer_list<GemvPlanes*> pls,
+                    std::initializer_list<int*> maxes) {
+      GemvArgs a;
+      memset(&a, 0, sizeof(a));
+      for (const GemvSeg& g : segs) a.seg[a.nseg++] = g;
+      const int C = gemv_plan(a, h->num_sms);
+      int i = 0;
+      for (GemvPlanes* p : pls) *p = gemv_planes(a, i++, C);
+      i = 0;
+      for (int* mx : maxes) *mx = std::max(*mx, gemv_max_planes(a, i++, C));
+    };
+    plan({shape(h->H, h->KT), shape(4 * h->G, h->H)}, {&h->pl_fc, &h->pl_d0}, {&maxp_fc, &maxp_d});
+    plan({shape(4 * h->G, h->H)}, {&h->pl_d}, {&maxp_d});
+    plan({shape(h->qd, h->H), shape(h->kvd, h->H), shape(h->kvd, h->H)}, {&h->pl_q, &h->pl_k, &h->pl_v},
+         {&maxp_q, &maxp_k, &maxp_v});
+    plan({shape(h->H, h->qd)}, {&h->pl_o}, {&maxp_y});
+    plan({shape(h->F, h->H), shape(h->F, h->H)}, {&h->pl_g, &h->pl_u}, {&maxp_g, &maxp_u});
+    plan({shape(h->H, h->F)}, {&h->pl_down}, {&maxp_y});
+    plan({shape(c.rank, h->H)}, {&h->pl_sel}, {&maxp_sel});
   }
-  bool maps_ok = h->s_fc && h->s_delta && h->s_qkv && h->s_o && h->s_gu && h->s_down && h->s_sel;
-  maps_ok = maps_ok && gemv_encode_wmap(&h->map_fc, w->fc.w, h->H, h->KT, fmt) &&
+  bool maps_ok = gemv_encode_wmap(&h->map_fc, w->fc.w, h->H, h->KT, fmt) &&
             gemv_encode_wmap(&h->map_sel, w->sel_proj.w, c.rank, h->H, fmt);
   for (int l = 0; l < c.n_layers && maps_ok; ++l) {
     const dflash2_layer_weights& L = w->layers[l];
@@ -217,22 +234,22 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->x), N * h->H * 4},
       {reinterpret_cast<void**>(&h->ss), N * h->nch_ss * 4},
       {reinterpret_cast<void**>(&h->ss_c), N * h->nch_ss * 4},
-      {reinterpret_cast<void**>(&h->dproj), h->s_delta * N * 4 * h->G * 4},
+      {reinterpret_cast<void**>(&h->dproj), maxp_d * N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_a), N * 4 * h->G * 4},
       {reinterpret_cast<void**>(&h->delta_m), N * 4 * h->G * 4},
-      {reinterpret_cast<void**>(&h->fc_out), h->s_fc * N * h->H * 4},
-      {reinterpret_cast<void**>(&h->q_out), h->s_qkv * N * h->qd * 4},
-      {reinterpret_cast<void**>(&h->k_out), h->s_qkv * 2 * N * h->kvd * 4},
-      {reinterpret_cast<void**>(&h->v_out), h->s_qkv * 2 * N * h->kvd * 4},
-      {reinterpret_cast<void**>(&h->sel_out), h->s_sel * N * c.rank * 4},
+      {reinterpret_cast<void**>(&h->fc_out), maxp_fc * N * h->H * 4},
+      {reinterpret_cast<void**>(&h->q_out), maxp_q * N * h->qd * 4},
+      {reinterpret_cast<void**>(&h->k_out), maxp_k * 2 * N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->v_out), maxp_v * 2 * N * h->kvd * 4},
+      {reinterpret_cast<void**>(&h->sel_out), maxp_sel * N * c.rank * 4},
       {reinterpret_cast<void**>(&h->q), N * h->qd * 4},
       {reinterpret_cast<void**>(&h->kb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->vb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->attn_part),
        static_cast<size_t>(max_requests) * h->nkv * h->n_attn_chunks * 32 * 130 * 4},
-      {reinterpret_cast<void**>(&h->ypart), std::max(h->s_o, h->s_down) * N * h->H * 4},
-      {reinterpret_cast<void**>(&h->gpart), h->s_gu * N * h->F * 4},
-      {reinterpret_cast<void**>(&h->upart), h->s_gu * N * h->F * 4},
+      {reinterpret_cast<void**>(&h->ypart), maxp_y * N * h->H * 4},
+      {reinterpret_cast<void**>(&h->gpart), maxp_g * N * h->F * 4},
+      {reinterpret_cast<void**>(&h->upart), maxp_u * N * h->F * 4},
       {reinterpret_cast<void**>(&h->act_a), 2 * N * h->H * esz},  // hi and lo planes
       {reinterpret_cast<void**>(&h->act_qkv), 2 * 2 * N * h->H * esz},
       {reinterpret_cast<void**>(&h->act_taps), 2 * N * h->KT * esz},
@@ -368,7 +385,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.H = H;
     a.nch = h->nch_ss;
     a.fmt = fmt;
-    a.splits = h->s_delta;
+    a.pl = l == 0 ? h->pl_d0 : h->pl_d;
     a.n_rows = N;
     a.eps = c.rms_eps;
     return a;
@@ -379,8 +396,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   {
     dflash2_status s =
         run_gemv(h,
-                 {seg(h->map_fc, h->w.fc, h->xm_taps, N8, R, H, h->KT, h->s_fc, h->fc_out),
-                  seg(h->map_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta,
+                 {seg(h->map_fc, h->w.fc, h->xm_taps, N8, R, H, h->KT, h->fc_out),
+                  seg(h->map_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, N8, R, 4 * G, H,
                       h->dproj)},
                  st);
     if (s) return s;
@@ -394,7 +411,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.act_row0 = N;
     a.nch = h->nch_ss;
     a.fmt = fmt;
-    a.splits = h->s_fc;
+    a.pl = h->pl_fc;
     a.n_rows = N;
     DF2_CHECK(launch_fc_finish_conv_in(a, conv_in_attn(0), R, pdl, st));
     h->launches++;
@@ -406,7 +423,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     dflash2_status s = DFLASH2_OK;
     if (l > 0) {
       // ---- a3: delta projection of the normed input, conv-in
-      s = run_gemv(h, {seg(h->map_layer[l][kAttnDelta], L.attn_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta, h->dproj)},
+      s = run_gemv(h, {seg(h->map_layer[l][kAttnDelta], L.attn_delta, h->xm_a, N8, R, 4 * G, H, h->dproj)},
                    st);
       if (s) return s;
       DF2_CHECK(launch_conv_in(conv_in_attn(l), R, pdl, st));
@@ -414,9 +431,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     }
     // ---- a4: q (block rows), k and v (block + new context rows)
     s = run_gemv(h,
-                 {seg(h->map_layer[l][kQ], L.q, h->xm_qkv, 2 * N8, R, h->qd, H, h->s_qkv, h->q_out),
-                  seg(h->map_layer[l][kK], L.k, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->s_qkv, h->k_out),
-                  seg(h->map_layer[l][kV], L.v, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->s_qkv, h->v_out)},
+                 {seg(h->map_layer[l][kQ], L.q, h->xm_qkv, 2 * N8, R, h->qd, H, h->q_out),
+                  seg(h->map_layer[l][kK], L.k, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->k_out),
+                  seg(h->map_layer[l][kV], L.v, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->v_out)},
                  st);
     if (s) return s;
     {
@@ -441,7 +458,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.kv_capacity = h->kv_cap;
       a.H = H;
       a.nch = h->nch_ss;
-      a.splits = h->s_qkv;
+      a.pq = h->pl_q;
+      a.pk = h->pl_k;
+      a.pv = h->pl_v;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_qkv_finish(a, R, pdl, st));
       h->launches++;
@@ -469,7 +488,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       h->launches += 2;
     }
     // ---- a6: output projection, conv-out + residual, post-attention norm input
-    s = run_gemv(h, {seg(h->map_layer[l][kO], L.o, h->xm_o, N8, R, H, h->qd, h->s_o, h->ypart)}, st);
+    s = run_gemv(h, {seg(h->map_layer[l][kO], L.o, h->xm_o, N8, R, H, h->qd, h->ypart)}, st);
     if (s) return s;
     {
       ConvOutArgs a;
@@ -486,13 +505,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
-      a.splits = h->s_o;
+      a.pl = h->pl_o;
       a.n_rows = N;
       DF2_CHECK(launch_conv_out(a, R, pdl, st));
       h->launches++;
     }
     // ---- a7: MLP sublayer
-    s = run_gemv(h, {seg(h->map_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, N8, R, 4 * G, H, h->s_delta, h->dproj)}, st);
+    s = run_gemv(h, {seg(h->map_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, N8, R, 4 * G, H, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
@@ -507,15 +526,15 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
-      a.splits = h->s_delta;
+      a.pl = h->pl_d;
       a.n_rows = N;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
     s = run_gemv(h,
-                 {seg(h->map_layer[l][kGate], L.gate, h->xm_qkv, 2 * N8, R, h->F, H, h->s_gu, h->gpart),
-                  seg(h->map_layer[l][kUp], L.up, h->xm_qkv, 2 * N8, R, h->F, H, h->s_gu, h->upart)},
+                 {seg(h->map_layer[l][kGate], L.gate, h->xm_qkv, 2 * N8, R, h->F, H, h->gpart),
+                  seg(h->map_layer[l][kUp], L.up, h->xm_qkv, 2 * N8, R, h->F, H, h->upart)},
                  st);
     if (s) return s;
     {
@@ -526,12 +545,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act_lo = h->lo_h;
       a.F = h->F;
       a.fmt = fmt;
-      a.splits = h->s_gu;
+      a.pg = h->pl_g;
+      a.pu = h->pl_u;
       a.n_rows = N;
       DF2_CHECK(launch_swiglu(a, R, pdl, st));
       h->launches++;
     }
-    s = run_gemv(h, {seg(h->map_layer[l][kDown], L.down, h->xm_h, N8, R, H, h->F, h->s_down, h->ypart)}, st);
+    s = run_gemv(h, {seg(h->map_layer[l][kDown], L.down, h->xm_h, N8, R, H, h->F, h->ypart)}, st);
     if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
@@ -550,7 +570,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
-      a.splits = h->s_down;
+      a.pl = h->pl_down;
       a.n_rows = N;
       DF2_CHECK(launch_conv_out(a, R, pdl, st));
       h->launches++;
@@ -581,7 +601,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // ---- a9: selector projection (same final hidden, in the matrix's format), merge top-16
   {
     const CUtensorMap& xin = fmt == 0 ? h->xm_fin : h->xm_a;  // same final hidden, in the matrix's format
-    dflash2_status s = run_gemv(h, {seg(h->map_sel, h->w.sel_proj, xin, N8, R, c.rank, H, h->s_sel, h->sel_out)}, st);
+    dflash2_status s = run_gemv(h, {seg(h->map_sel, h->w.sel_proj, xin, N8, R, c.rank, H, h->sel_out)}, st);
     if (s) return s;
     TopkMergeArgs a;
     a.part_keys = h->topk_keys;
@@ -594,7 +614,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.n_cta = h->lm_ctas;
     a.rank = c.rank;
     a.nch = h->nch_ss;
-    a.sel_splits = h->s_sel;
+    a.psel = h->pl_sel;
     a.H = H;
     a.eps = c.rms_eps;
     DF2_CHECK(launch_topk_merge(a, pdl, st));
@@ -623,7 +643,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   a.eps = h->cfg.rms_eps;
   a.err = h->gemv_err;
   DF2_CHECK(launch_lmhead(a, h->pdl, st));
-  TopkMergeArgs m;
+  TopkMergeArgs m = {};
   m.part_keys = h->topk_keys;
   m.sel = nullptr;
   m.ss = nullptr;
@@ -634,7 +654,6 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   m.n_cta = h->lm_ctas;
   m.rank = h->cfg.rank;
   m.nch = h->nch_ss;
-  m.sel_splits = 0;
   m.H = h->H;
   m.eps = h->cfg.rms_eps;
   DF2_CHECK(launch_topk_merge(m, h->pdl, st));

@@ -5,9 +5,11 @@
 //  * The weights are read exactly once per step, so the kernel is bound by HBM
 //    bandwidth; what it needs is enough bytes in flight to cover HBM latency and
 //    no other long-latency load on the consumers' path.
-//  * A work unit is a 64-row weight block times one K split.  Each CTA (two per
-//    SM) walks its units grid-stride with one producer warp and four consumer
-//    warps.  The producer fills a ring of shared-memory stages with bulk tensor
+//  * A launch's work is the sequence of stages (64-row weight block x 128 K) of
+//    its segments; CTA c of C (two per SM) takes the contiguous share
+//    [c T / C, (c + 1) T / C) of the T stages (stream-K), so every CTA streams
+//    the same bytes whatever the matrix shapes.  Each CTA has one producer warp
+//    and four consumer warps.  The producer fills a ring of shared-memory stages with bulk tensor
 //    copies (cp.async.bulk.tensor) completing on the stage's "full" mbarrier: 64
 //    weight rows x 128 K, plus the matching activation slice, both planes, in
 //    8-row boxes.  Copies move 64 K per row: 128-byte rows (128-byte swizzle) for
@@ -22,10 +24,11 @@
 //    reads the same consecutive K of weight rows g and g + 8 and of activation row
 //    g (16-byte shared-memory loads, bank-conflict-free under the swizzle), so A
 //    and B agree on which K each MMA slot holds.
-//  * Each split's partial goes to its own output plane with plain stores; the
-//    consumer kernel adds the planes in split order, so every result is
-//    bit-reproducible.  The split count comes from a cost model over the grid
-//    (gemv_choose_splits).
+//  * A block whose stages are shared by several CTAs gets one partial plane per
+//    CTA, written with plain stores at plane (CTA - first CTA of the block); the
+//    consumer kernel adds the block's planes in order (gemv_plane_count gives
+//    their number in closed form), so every result is bit-reproducible, with no
+//    atomics and no inter-CTA signalling.
 //  * Activations carry a low-order plane (x = hi + lo) for ~16-bit accuracy, with
 //    independent accumulator chains for the two planes.
 //  * Q8/group64 ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias per
@@ -39,6 +42,7 @@
 //    the producer lets its outstanding copies land (again bounded) before exiting.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -52,49 +56,68 @@ namespace {
 
 using namespace pipe;
 
-DF2_DEV int find_seg(const GemvArgs& a, int u) {
+DF2_DEV int find_seg(const GemvArgs& a, long long t) {
   int s = 0;
 #pragma unroll
   for (int i = 1; i < kMaxSeg; ++i)
-    if (i < a.nseg && u >= a.seg[i].unit_begin) s = i;
+    if (i < a.nseg && t >= a.seg[i].stage_begin) s = i;
   return s;
 }
 
-// Walks one CTA's (unit, stage) sequence: units blockIdx.x, + gridDim.x, ...
+// Walks this CTA's stage range [t0, t1): for stage t the segment, 64-row block and
+// K offset, and whether it opens or closes a piece (the CTA's share of a block).
 struct Cursor {
-  int u, st, seg, row0, k0, split, nst;
+  long long t, t1;
+  int seg, row0, kabs, kst, kstage;
   bool valid;
   DF2_DEV void load(const GemvArgs& a) {
-    valid = u < a.total_units;
+    valid = t < t1;
     if (!valid) return;
-    seg = find_seg(a, u);
+    seg = find_seg(a, t);
     const GemvSeg& sg = a.seg[seg];
-    const int local = u - sg.unit_begin;
-    const int blocks = sg.M / kBlockRows;
-    split = local / blocks;
-    row0 = (local % blocks) * kBlockRows;
-    const int kchunk = sg.K / sg.splits;
-    k0 = split * kchunk;
-    nst = kchunk / kStageK;
-    st = 0;
+    kst = sg.K / kStageK;
+    const long long local = t - sg.stage_begin;
+    row0 = static_cast<int>(local / kst) * kBlockRows;
+    kstage = static_cast<int>(local % kst);
+    kabs = kstage * kStageK;
   }
   DF2_DEV void start(const GemvArgs& a) {
-    u = blockIdx.x;
+    const long long T = a.total_stages, C = gridDim.x;
+    t = (static_cast<long long>(blockIdx.x) * T) / C;
+    t1 = (static_cast<long long>(blockIdx.x + 1) * T) / C;
     load(a);
   }
-  DF2_DEV void next(const GemvArgs& a) {
-    if (++st == nst) {
-      u += gridDim.x;
-      load(a);
+  DF2_DEV void next(const GemvArgs& a) {  // incremental: no division inside a segment
+    if (++t >= t1) {
+      valid = false;
+      return;
+    }
+    if (++kstage < kst) {
+      kabs += kStageK;
+      return;
+    }
+    kstage = 0;
+    kabs = 0;
+    row0 += kBlockRows;
+    if (row0 >= a.seg[seg].M) {
+      ++seg;
+      row0 = 0;
+      kst = a.seg[seg].K / kStageK;
     }
   }
-  DF2_DEV int kabs() const { return k0 + st * kStageK; }
+  DF2_DEV bool opens(long long t_first) const { return kstage == 0 || t == t_first; }
+  DF2_DEV bool closes() const { return kstage == kst - 1 || t == t1 - 1; }
+  // plane of this CTA's piece of the current block
+  DF2_DEV int plane(const GemvArgs& a) const {
+    const long long b0 = t - kstage;  // the block's first stage
+    return static_cast<int>(blockIdx.x) - gemv_cta_of_stage(b0, gridDim.x, a.total_stages);
+  }
 };
 
 template <int NT>
-DF2_DEV void store_tile(const GemvSeg& sg, int split, int row0, const float (&acc)[NT][4], int lane) {
+DF2_DEV void store_tile(const GemvSeg& sg, int plane, int row0, const float (&acc)[NT][4], int lane) {
   const int g = lane >> 2, q = lane & 3;
-  float* out = sg.out + static_cast<size_t>(split) * (sg.n_tiles * 8) * sg.M;
+  float* out = sg.out + static_cast<size_t>(plane) * (sg.n_tiles * 8) * sg.M;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     if (t < sg.n_tiles) {
@@ -210,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     constexpr int kXBoxBytes = 8 * kXBoxK * 2;
     auto issue_w = [&](const Cursor& c, int slot) {
       if (lane < kWBoxes)
-        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs() + lane * 64,
+        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs + lane * 64,
                     c.row0, full0 + 8 * slot, policy);
     };
     auto issue_x = [&](const Cursor& c, int slot) {
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
         const int rem = i % (sg.n_tiles * kXBoxes);
         const int t = rem / kXBoxes, b = rem % kXBoxes;
         const uint32_t dst = ring + slot * Geo::kBytes + Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + b) * kXBoxBytes;
-        tma_load_2d(dst, &sg.xmap, c.kabs() + b * kXBoxK, plane * sg.x_lo_row + t * 8, full0 + 8 * slot, xpolicy);
+        tma_load_2d(dst, &sg.xmap, c.kabs + b * kXBoxK, plane * sg.x_lo_row + t * 8, full0 + 8 * slot, xpolicy);
       }
     };
     auto arm = [&](const Cursor& c, int slot) {
@@ -279,11 +302,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   float c0[NT][4], c1[NT][4], c2[NT][4], c3[NT][4];
   Cursor c;
   c.start(a);
+  const long long t_first = c.t;
   Q8Affine af = {};
-  if (FMT == 1 && c.valid) af = load_affine(a.seg[c.seg], c.row0 + wid * 16 + g, c.kabs());
+  if (FMT == 1 && c.valid) af = load_affine(a.seg[c.seg], c.row0 + wid * 16 + g, c.kabs);
   int it = 0;
   while (c.valid) {
-    if (c.st == 0) {
+    if (c.opens(t_first)) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -295,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     Cursor cn = c;
     cn.next(a);
     Q8Affine afn = af;
-    if (FMT == 1 && cn.valid) afn = load_affine(a.seg[cn.seg], cn.row0 + wid * 16 + g, cn.kabs());
+    if (FMT == 1 && cn.valid) afn = load_affine(a.seg[cn.seg], cn.row0 + wid * 16 + g, cn.kabs);
     if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, static_cast<uint32_t>((it / D) & 1)))) {
       if (lane == 0 && a.err != nullptr) atomicExch(a.err, 1);
       break;
@@ -307,12 +331,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
       stage_q8<NT>(sg.n_tiles, base + wrow, base + Geo::kWBytes + xrow, g, q, af, c0, c1, c2, c3);
     __syncwarp();  // every lane's reads of this stage are done before it is released
     if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-    if (c.st + 1 == c.nst) {
+    if (c.closes()) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) c0[t][e] = (c0[t][e] + c1[t][e]) + (c2[t][e] + c3[t][e]);
-      store_tile<NT>(sg, c.split, c.row0 + wid * 16, c0, lane);
+      store_tile<NT>(sg, c.plane(a), c.row0 + wid * 16, c0, lane);
     }
     c = cn;
     af = afn;
@@ -347,7 +371,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* p,
 }
 
 template <int NT, int FMT>
-cudaError_t launch_nt(const GemvArgs& a, int num_sms, bool pdl, cudaStream_t st) {
+cudaError_t launch_nt(const GemvArgs& a, int ctas, bool pdl, cudaStream_t st) {
   constexpr int smem = StageGeo<FMT, NT>::kSmem;
   static bool attr_set = false;  // set once, outside any later stream capture
   if (!attr_set) {
@@ -355,9 +379,6 @@ cudaError_t launch_nt(const GemvArgs& a, int num_sms, bool pdl, cudaStream_t st)
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  int ctas = num_sms * kCtasPerSm;
-  if (ctas > a.total_units) ctas = a.total_units;
-  if (ctas < 1) ctas = 1;
   return launch_ex(gemv_kernel<NT, FMT>, dim3(ctas), dim3(kThreads), smem, st, pdl, a);
 }
 
@@ -387,48 +408,51 @@ bool lm_encode_map(CUtensorMap* map, const void* p, int inner, int rows, int box
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-int gemv_choose_splits(int blocks, int K, double plane_bytes, int num_sms, int fmt) {
-  if (blocks < 1 || K % kStageK) return 0;
-  const long long C = static_cast<long long>(num_sms) * kCtasPerSm;
-  const int kst = K / kStageK;
-  // one stage of every CTA at ~6.5 TB/s, in seconds; the consumer reads planes at ~5 TB/s from L2
-  const double stage_s = static_cast<double>(C) * kBlockRows * kStageK * (fmt == 0 ? 2.0 : 1.0) / 6.5e12;
-  const double plane_cost = plane_bytes / 5.0e12 / stage_s;
-  int best_s = 0;
-  double best = 0.0;
-  for (int s = 1; s <= kst; ++s) {
-    if (kst % s) continue;
-    const long long rounds = (static_cast<long long>(blocks) * s + C - 1) / C;
-    const double cost = static_cast<double>(rounds) * (kst / s + 0.25) + plane_cost * s;
-    if (best_s == 0 || cost < best) {
-      best = cost;
-      best_s = s;
-    }
+int gemv_plan(GemvArgs& a, int num_sms) {
+  long long T = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    GemvSeg& sg = a.seg[i];
+    sg.stage_begin = T;
+    T += static_cast<long long>(sg.M / kBlockRows) * (sg.K / kStageK);
   }
-  return best_s;
+  a.total_stages = T;
+  const long long C = static_cast<long long>(num_sms) * kCtasPerSm;
+  return static_cast<int>(C < T ? C : (T > 0 ? T : 1));
+}
+
+GemvPlanes gemv_planes(const GemvArgs& a, int i, int C) {
+  GemvPlanes p;
+  p.T = a.total_stages;
+  p.base = a.seg[i].stage_begin;
+  p.C = C;
+  p.kst = a.seg[i].K / kStageK;
+  return p;
+}
+
+int gemv_max_planes(const GemvArgs& a, int i, int C) {
+  const GemvPlanes p = gemv_planes(a, i, C);
+  int mx = 0;
+  for (int m = 0; m < a.seg[i].M; m += kBlockRows) mx = std::max(mx, gemv_plane_count(p, m));
+  return mx;
 }
 
 cudaError_t launch_gemv(GemvArgs& a, int fmt, int max_tiles, int num_sms, bool pdl, cudaStream_t st) {
-  int units = 0;
   for (int i = 0; i < a.nseg; ++i) {
-    GemvSeg& sg = a.seg[i];
-    if (sg.splits < 1 || sg.M % kBlockRows || sg.K % sg.splits || (sg.K / sg.splits) % kStageK ||
-        sg.n_tiles < 1 || sg.n_tiles > max_tiles)
-      return cudaErrorInvalidValue;
-    sg.unit_begin = units;
-    units += (sg.M / kBlockRows) * sg.splits;
+    const GemvSeg& sg = a.seg[i];
+    if (sg.M % kBlockRows || sg.K % kStageK || sg.n_tiles < 1 || sg.n_tiles > max_tiles) return cudaErrorInvalidValue;
   }
-  a.total_units = units;
+  const int C = gemv_plan(a, num_sms);
+  if (a.total_stages < 1) return cudaErrorInvalidValue;
   if (fmt == 0) {
-    if (max_tiles <= 1) return launch_nt<1, 0>(a, num_sms, pdl, st);
-    if (max_tiles <= 2) return launch_nt<2, 0>(a, num_sms, pdl, st);
-    if (max_tiles <= 4) return launch_nt<4, 0>(a, num_sms, pdl, st);
-    if (max_tiles <= 8) return launch_nt<8, 0>(a, num_sms, pdl, st);
+    if (max_tiles <= 1) return launch_nt<1, 0>(a, C, pdl, st);
+    if (max_tiles <= 2) return launch_nt<2, 0>(a, C, pdl, st);
+    if (max_tiles <= 4) return launch_nt<4, 0>(a, C, pdl, st);
+    if (max_tiles <= 8) return launch_nt<8, 0>(a, C, pdl, st);
   } else {
-    if (max_tiles <= 1) return launch_nt<1, 1>(a, num_sms, pdl, st);
-    if (max_tiles <= 2) return launch_nt<2, 1>(a, num_sms, pdl, st);
-    if (max_tiles <= 4) return launch_nt<4, 1>(a, num_sms, pdl, st);
-    if (max_tiles <= 8) return launch_nt<8, 1>(a, num_sms, pdl, st);
+    if (max_tiles <= 1) return launch_nt<1, 1>(a, C, pdl, st);
+    if (max_tiles <= 2) return launch_nt<2, 1>(a, C, pdl, st);
+    if (max_tiles <= 4) return launch_nt<4, 1>(a, C, pdl, st);
+    if (max_tiles <= 8) return launch_nt<8, 1>(a, C, pdl, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
 DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
-  const float y = plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, a.splits);
+  const float y =
+      plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, gemv_plane_count(a.pl, c));
   put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(a.act_row0 + row) * a.H + c, y * bf16_to_f32(a.norm_w[c]));
   emit_ss(y, row, a.ss, a.nch);
 }
@@ -117,11 +118,12 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
     const int gidx = (io * 2 + t) * G + blockIdx.y * 2 + gl;
     const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
     const float* p = a.dproj + static_cast<size_t>(row) * (4 * G) + gidx;
+    const int np = gemv_plane_count(a.pl, gidx);
     float part = 0.f;
-    for (int s0 = pg; s0 < a.splits; s0 += 32) {
+    for (int s0 = pg; s0 < np; s0 += 32) {
       float tt[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) tt[j] = (s0 + 4 * j < a.splits) ? p[static_cast<size_t>(s0 + 4 * j) * plane] : 0.f;
+      for (int j = 0; j < 8; ++j) tt[j] = (s0 + 4 * j < np) ? p[static_cast<size_t>(s0 + 4 * j) * plane] : 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) part += tt[j];
     }
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
   const int G = a.H / 16;
   const int g = c >> 4;
   const size_t idx = static_cast<size_t>(row) * a.H + c;
-  const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, a.splits);
+  const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, gemv_plane_count(a.pl, c));
   ysh[i][lane] = y;
   __syncthreads();
   const float yprev = i > 0 ? ysh[i - 1][lane] : 0.f;
@@ -191,8 +193,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
   const size_t idx = static_cast<size_t>(row) * a.F + c;
   const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
-  const float gs = plane_sum(a.part_g + idx, plane, a.splits);
-  const float us = plane_sum(a.part_u + idx, plane, a.splits);
+  const float gs = plane_sum(a.part_g + idx, plane, gemv_plane_count(a.pg, c));
+  const float us = plane_sum(a.part_u + idx, plane, gemv_plane_count(a.pu, c));
   put_act(a.act, a.act_lo, a.fmt, idx, gs / (1.f + __expf(-gs)) * us);
 }
 
@@ -230,6 +232,7 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
   const int row0 = r * kB;
   const float* src;
   size_t plane;
+  const GemvPlanes& pm = kind == 0 ? a.pq : (kind == 1 ? a.pk : a.pv);
   if (kind == 0) {
     src = a.q_out + (static_cast<size_t>(row0 + jj) * nq + hh) * 128;
     plane = static_cast<size_t>(a.n_rows) * nq * 128;
@@ -238,13 +241,17 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
     src = (kind == 1 ? a.k_out : a.v_out) + (prow * nkv + hh) * 128;
     plane = static_cast<size_t>(2 * a.n_rows) * nkv * 128;
   }
+  // dims lane + 32 c: c = 0, 1 in the head's first 64-row block, c = 2, 3 in its second
+  const int np0 = gemv_plane_count(pm, hh * 128), np1 = gemv_plane_count(pm, hh * 128 + 64);
+  const int npx = np0 > np1 ? np0 : np1;
   float v[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s0 = 0; s0 < a.splits; s0 += 8) {  // split planes in order, 8 planes' loads in flight
+  for (int s0 = 0; s0 < npx; s0 += 8) {  // planes in order, 8 planes' loads in flight
     float t[8][4];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) t[u][c] = (s0 + u < a.splits) ? src[(s0 + u) * plane + lane + 32 * c] : 0.f;
+      for (int c = 0; c < 4; ++c)
+        t[u][c] = (s0 + u < (c < 2 ? np0 : np1)) ? src[(s0 + u) * plane + lane + 32 * c] : 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "internal.h"
+
 namespace df2 {
 
 // Activation buffers hold a high plane and, at element offset *_lo, a low-order
@@ -27,16 +29,17 @@ struct StartArgs {
 };
 
 struct FcFinishArgs {
-  const float* y;          // taps projection partials [splits][N][H]
+  const float* y;          // taps projection partial planes [p][N][H]
   const uint16_t* norm_w;  // hidden_norm
   void* act;               // QKV input; context rows start at act_row0
   size_t act_lo;
   float* ss;               // [N][H/32] sums of squares of y
-  int H, act_row0, nch, fmt, splits, n_rows;
+  int H, act_row0, nch, fmt, n_rows;
+  GemvPlanes pl;           // planes of y
 };
 
 struct ConvInArgs {
-  const float* dproj;      // delta projection partials of x * w, [splits][N][4G] (not yet scaled by 1/rms)
+  const float* dproj;      // delta projection partial planes of x * w, [p][N][4G] (not yet scaled by 1/rms)
   const float* ss;         // [N][nch] sums of squares of x
   const float* x;          // residual stream
   const uint16_t* norm_w;
@@ -44,13 +47,14 @@ struct ConvInArgs {
   float* delta;            // out: [N][4G] scaled by 1/rms
   void* act;               // out: conv-in'd sublayer input [N][H]
   size_t act_lo;
-  int H, nch, fmt, splits, n_rows;
+  int H, nch, fmt, n_rows;
   float eps;
+  GemvPlanes pl;           // planes of dproj
 };
 
 // Dynamic convolution after a sublayer, residual add, next norm's input.
 struct ConvOutArgs {
-  const float* part;       // sublayer output partials [splits][N][H]
+  const float* part;       // sublayer output partial planes [p][N][H]
   const float* delta;      // [N][4G] (io 1 = conv after the sublayer)
   const uint16_t* base;    // [4][H]
   const uint16_t* norm_w;  // norm weight of the next sublayer
@@ -60,21 +64,23 @@ struct ConvOutArgs {
   uint16_t* act2;          // optional bf16 copy (LM-head input), or null
   size_t act2_lo;
   float* ss;               // [N][H/32] sums of squares of the updated x
-  int H, nch, fmt, splits, n_rows;
+  int H, nch, fmt, n_rows;
+  GemvPlanes pl;           // planes of part
 };
 
 // SwiGLU of the gate and up projections: act = silu(gate) * up.
 struct SwigluArgs {
-  const float* part_g;     // gate partials [splits][N][F]
-  const float* part_u;     // up partials [splits][N][F]
+  const float* part_g;     // gate partial planes [p][N][F]
+  const float* part_u;     // up partial planes [p][N][F]
   void* act;               // [N][F] plus low plane at act + act_lo
   size_t act_lo;
-  int F, fmt, splits, n_rows;
+  int F, fmt, n_rows;
+  GemvPlanes pg, pu;       // planes of the two projections
 };
 
 struct QkvFinishArgs {
-  const float* q_out;      // partials [splits][N][nq*128]
-  const float* k_out;      // partials [splits][2N][nkv*128]: block rows, then context rows
+  const float* q_out;      // partial planes [p][N][nq*128]
+  const float* k_out;      // partial planes [p][2N][nkv*128]: block rows, then context rows
   const float* v_out;
   const float* ss_c;       // [N][nch] of the projected taps
   const uint16_t* q_norm;
@@ -87,8 +93,9 @@ struct QkvFinishArgs {
   float* vb;
   uint16_t* k_cache;       // this layer's slice: [max_req][cap][nkv][128]
   uint16_t* v_cache;
-  int n_q_heads, n_kv_heads, n_rows, kv_capacity, H, nch, splits;
+  int n_q_heads, n_kv_heads, n_rows, kv_capacity, H, nch;
   float eps;
+  GemvPlanes pq, pk, pv;   // planes of the three projections
 };
 
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st);
@@ -136,13 +143,14 @@ cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st);
 
 struct TopkMergeArgs {
   const unsigned long long* part_keys;  // [N][n_cta][16]
-  const float* sel;        // selector projection partials [sel_splits][N][rank], or null
+  const float* sel;        // selector projection partial planes [p][N][rank], or null
   const float* ss;
   int32_t* cand_ids;       // [R][7][16]
   float* cand_logits;
   float* gate;             // [R][7][rank]
-  int n_rows, n_cta, rank, nch, H, sel_splits;
+  int n_rows, n_cta, rank, nch, H;
   float eps;
+  GemvPlanes psel;         // planes of sel
 };
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st);
 

@@ -12,27 +12,59 @@ constexpr int kMaxSeg = 4;
 // K elements of one pipeline stage of the weight-streaming GEMV (64 weight rows).
 constexpr int kGemvStageK = 128;
 
-// One weight-streaming GEMV segment: for every K split s,
-//   out[s][n][m] = sum_{k in split s} W[m][k] * X[n][k],  n < 8 * n_tiles, m < M.
-// The consumer adds the split planes in split order.
+#ifdef __CUDACC__
+#define DF2_HD __host__ __device__
+#else
+#define DF2_HD
+#endif
+
+// One weight-streaming GEMV segment (a matrix and its activations) of a launch.
+// A launch's work is the sequence of (64-row weight block, kGemvStageK of K)
+// stages of its segments, in order; CTA c of C takes stages
+// [floor(c T / C), floor((c + 1) T / C)) of the T in total (stream-K: balanced to
+// one stage whatever the shapes).  A block's K sum is split among the CTAs that
+// share its stages; each writes its part to plane (c - first CTA of the block):
+//   out[p][n][m] = sum over CTA p's stages of block m/64 of W[m][k] * X[n][k].
+// The consumer adds planes 0 .. plane_count - 1 in order (GemvPlanes).
 struct GemvSeg {
-  CUtensorMap wmap;       // W [M][K]: bf16 boxes 32 K x 64 rows or int8 boxes 64 K x 64 rows, 64-byte swizzle
+  CUtensorMap wmap;       // W [M][K]: bf16 boxes 64 K x 64 rows (128-byte swizzle) or int8 64 K x 64 rows (64-byte)
   CUtensorMap xmap;       // X planes [2][rows][K] (hi rows, then lo rows): boxes of 8 rows (gemv_encode_xmap)
   const uint16_t* scale;  // Q8: bf16 [M][K/64]
   const uint16_t* bias;
   int x_lo_row;           // first row of the low-order plane in xmap
   int M, K, n_tiles;
-  int splits;             // K splits (K / splits is a multiple of kGemvStageK)
-  float* out;             // [splits][n_tiles * 8][M]
-  int unit_begin;         // first global work unit (64-row block, split) of this segment (set by the launcher)
+  float* out;             // [planes][n_tiles * 8][M]
+  long long stage_begin;  // first stage of this segment in the launch (set by gemv_plan)
 };
 
 struct GemvArgs {
   GemvSeg seg[kMaxSeg];
   int nseg;
-  int total_units;
-  int* err;               // set nonzero if a pipeline wait gave up (never in a correct run), or null
+  long long total_stages;  // T (set by gemv_plan)
+  int* err;                // set nonzero if a pipeline wait gave up (never in a correct run), or null
 };
+
+// Where the partial planes of one segment's output channel m are: planes
+// 0 .. count(m) - 1, with count from the block's first and last stage.
+struct GemvPlanes {
+  long long T, base;  // launch stages; the segment's first stage
+  int C, kst;         // launch CTAs; stages per 64-row block
+};
+
+DF2_HD inline int gemv_cta_of_stage(long long t, int C, long long T) {
+  return static_cast<int>(((t + 1) * static_cast<long long>(C) - 1) / T);
+}
+
+DF2_HD inline int gemv_plane_count(const GemvPlanes& p, int m) {
+  const long long b0 = p.base + static_cast<long long>(m >> 6) * p.kst;
+  return gemv_cta_of_stage(b0 + p.kst - 1, p.C, p.T) - gemv_cta_of_stage(b0, p.C, p.T) + 1;
+}
+
+// Fills stage_begin and total_stages; returns the CTA count of the launch.
+int gemv_plan(GemvArgs& a, int num_sms);
+// Plane map of segment i of a planned launch with C CTAs, and its largest plane count.
+GemvPlanes gemv_planes(const GemvArgs& a, int i, int C);
+int gemv_max_planes(const GemvArgs& a, int i, int C);
 
 // Encodes the tensor map of one weight matrix [M][K] (bf16 when fmt == 0, int8
 // codes when fmt == 1).  Returns false if the driver rejects it.
@@ -45,12 +77,6 @@ bool gemv_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt)
 // fmt: 0 = BF16 weights, 1 = Q8G64 weights.  max_tiles: largest n_tiles over segments.
 // pdl: launch with programmatic stream serialisation.
 cudaError_t launch_gemv(GemvArgs& a, int fmt, int max_tiles, int num_sms, bool pdl, cudaStream_t st);
-
-// K split for a launch over `blocks` 64-row weight blocks of depth K whose one
-// output plane is `plane_bytes`: minimises whole-grid rounds of (block, split)
-// units times their length in pipeline stages, plus the consumer's cost of
-// adding planes.
-int gemv_choose_splits(int blocks, int K, double plane_bytes, int num_sms, int fmt);
 
 // Launch helper: cudaLaunchKernelEx with the programmatic stream serialisation
 // attribute when pdl is set.

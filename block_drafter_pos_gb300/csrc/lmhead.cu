@@ -262,10 +262,11 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   for (int j = threadIdx.x; j < a.rank; j += blockDim.x) {
     const float* p = a.sel + static_cast<size_t>(n) * a.rank + j;
     float v = 0.f;
-    for (int s0 = 0; s0 < a.sel_splits; s0 += 16) {  // split planes in order, 16 loads in flight
+    const int np = gemv_plane_count(a.psel, j);
+    for (int s0 = 0; s0 < np; s0 += 16) {  // planes in order, 16 loads in flight
       float t[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) t[k] = (s0 + k < a.sel_splits) ? p[static_cast<size_t>(s0 + k) * plane] : 0.f;
+      for (int k = 0; k < 16; ++k) t[k] = (s0 + k < np) ? p[static_cast<size_t>(s0 + k) * plane] : 0.f;
 #pragma unroll
       for (int k = 0; k < 16; ++k) v += t[k];
     }

@@ -90,7 +90,7 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   a.eps = 0.f;
   a.err = nullptr;
   if (launch_lmhead(a, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
-  TopkMergeArgs m;
+  TopkMergeArgs m = {};
   m.part_keys = slot.keys;
   m.sel = nullptr;
   m.ss = nullptr;
@@ -102,7 +102,6 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   m.rank = 0;
   m.nch = hidden_dim / 128;
   m.H = hidden_dim;
-  m.sel_splits = 0;
   m.eps = 0.f;
   if (launch_topk_merge(m, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
   return DFLASH2_OK;
