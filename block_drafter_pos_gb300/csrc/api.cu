@@ -39,6 +39,7 @@ struct dflash2_handle {
   CUtensorMap xm_taps, xm_a, xm_qkv, xm_o, xm_h, xm_fin;
   CUtensorMap map_lm, xm_lm;  // LM head weights; final hidden (bf16 in both formats) for the LM head
   int* gemv_err;  // device word set by a GEMV whose pipeline wait gave up
+  unsigned int* verify_cnt;  // [max_req] verify chunk counters (zero between launches)
   // scratch
   char* arena;
   size_t arena_bytes;
@@ -261,6 +262,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
        static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
       {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
       {reinterpret_cast<void**>(&h->gemv_err), 4},
+      {reinterpret_cast<void**>(&h->verify_cnt), static_cast<size_t>(max_requests) * 4},
   };
   h->lo_a = N * h->H;
   h->lo_qkv = 2 * N * h->H;
@@ -712,6 +714,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   a.seed = seed;
   a.offset = philox_offset;
   a.stats = h->vstats;
+  a.counters = h->verify_cnt;
   a.n_accepted = n_accepted;
   a.emitted = emitted;
   a.n_emitted = n_emitted;
@@ -719,7 +722,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   a.V = h->V;
   a.n_chunks = h->n_verify_chunks;
   DF2_CHECK(launch_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
-  h->launches += 2;
+  h->launches += 1;
   return DFLASH2_OK;
 }
 

@@ -63,8 +63,11 @@ DF2_DEV void emit_ss(float v, int row, float* ss, int nch) {
 // ------------------------------------------------------------------ start of the step
 // blockIdx.y < H/32: block embedding, first norm input and its sums of squares;
 // above: taps of the new context rows packed into the fc projection's input.
+// Everything it reads is a caller input and nothing the previous kernel reads is
+// written here, so the wait on the previous kernel comes last: it only keeps
+// that kernel ahead of every later one.
 __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
-  pdl_begin();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int i = threadIdx.x >> 5;
   const int row = r * kB + i;
@@ -84,6 +87,7 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
     const size_t idx = static_cast<size_t>(row) * (a.n_taps * a.H) + c;
     put_act(a.act_taps, a.act_taps_lo, a.fmt, idx, (i < nn) ? a.taps[idx] : 0.f);
   }
+  pdl_wait();
 }
 
 // ------------------------------------------------------------------ taps projection finish

@@ -198,6 +198,7 @@ struct VerifyArgs {
   int32_t* emitted;            // [R][8]
   int32_t* n_emitted;
   int32_t* status;
+  unsigned int* counters;      // [R] finished chunk statistics of the launch; zero before and after it
   int V, n_chunks;
 };
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st);

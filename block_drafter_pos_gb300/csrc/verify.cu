@@ -22,94 +22,14 @@ namespace {
 
 constexpr int kB = 8, kP = 7, kK = 16;
 
-// The target logits and temperatures are caller inputs, so the chunk statistics are
-// computed before the wait on the previous kernel; only the store waits.
-__global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
-  __shared__ float sm_m[8], sm_s[8];
-  __shared__ int sm_a[8], sm_f[8];
-  pdl_trigger();
-  const int rj = blockIdx.x;  // r * 8 + j
-  const int r = rj >> 3;
-  const int chunk = blockIdx.y;
-  const float T = a.temperature[r];
-  const float* z = a.logits + static_cast<size_t>(rj) * a.V;
-  const int v0 = chunk * kVerifyChunk;
-  const int v1 = min(a.V, v0 + kVerifyChunk);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  constexpr int kPer = kVerifyChunk / 256;
-  float xs[kPer];  // this thread's logits of the chunk, loaded once (all in flight)
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int v = v0 + threadIdx.x + 256 * j;
-    xs[j] = v < v1 ? z[v] : -INFINITY;
-  }
-  float m = -INFINITY;
-  int arg = 0x7FFFFFFF;
-  int flags = 0;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int v = v0 + threadIdx.x + 256 * j;
-    const float x = xs[j];
-    if (v >= v1) continue;
-    if (isnan(x)) {
-      flags |= 1;
-      continue;
-    }
-    if (x == INFINITY) flags |= 2;
-    if (x > m || (x == m && v < arg)) {
-      m = x;
-      arg = v;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, m, o);
-    const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
-    if (om > m || (om == m && oa < arg)) {
-      m = om;
-      arg = oa;
-    }
-    flags |= __shfl_xor_sync(0xffffffffu, flags, o);
-  }
-  if (lane == 0) {
-    sm_m[wid] = m;
-    sm_a[wid] = arg;
-    sm_f[wid] = flags;
-  }
-  __syncthreads();
-  float M = sm_m[0];
-  int A = sm_a[0], F = 0;
-  for (int w = 0; w < 8; ++w) {
-    if (sm_m[w] > M || (sm_m[w] == M && sm_a[w] < A)) {
-      M = sm_m[w];
-      A = sm_a[w];
-    }
-    F |= sm_f[w];
-  }
-  float s = 0.f;
-  if (T > 0.f && M > -INFINITY && M < INFINITY) {
-    const float inv_t = 1.f / T;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int v = v0 + threadIdx.x + 256 * j;
-      if (v < v1 && !isnan(xs[j])) s += expf((xs[j] - M) * inv_t);
-    }
-    s = warp_sum(s);
-    __syncthreads();
-    if (lane == 0) sm_s[wid] = s;
-    __syncthreads();
-    s = 0.f;
-    for (int w = 0; w < 8; ++w) s += sm_s[w];
-  }
-  pdl_wait();  // the statistics buffer is read by the previous step's chain kernel
-  if (threadIdx.x == 0) {
-    VerifyStat st;
-    st.m = M;
-    st.s = s;
-    st.arg = A;
-    st.flags = F;
-    a.stats[static_cast<size_t>(rj) * a.n_chunks + chunk] = st;
-  }
+// Chunk statistics written by other CTAs of the launch, read from L2.
+DF2_DEV VerifyStat ldst(const VerifyStat* p) {
+  VerifyStat v;
+  v.m = __ldcg(&p->m);
+  v.s = __ldcg(&p->s);
+  v.arg = __ldcg(&p->arg);
+  v.flags = __ldcg(&p->flags);
+  return v;
 }
 
 // Inverse-CDF draw over the vocabulary of row j from weights w(x) = p(x) - min(p(x),
@@ -121,7 +41,8 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
   const int nc = a.n_chunks;
   const float inv_t = 1.f / T;
   for (int c = threadIdx.x; c < nc; c += blockDim.x) {
-    float mass = (st[c].m > -INFINITY) ? st[c].s * expf((st[c].m - M) * inv_t) / tot : 0.f;
+    const VerifyStat sc = ldst(st + c);
+    float mass = (sc.m > -INFINITY) ? sc.s * expf((sc.m - M) * inv_t) / tot : 0.f;
     if (use_q) {
       for (int k = 0; k < kK; ++k) {
         if (cid[k] / kVerifyChunk == c) {
@@ -143,7 +64,8 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
     if (fallback) {
       total = 0.f;
       for (int c = 0; c < nc; ++c) {
-        csum[c] = (st[c].m > -INFINITY) ? st[c].s * expf((st[c].m - M) * inv_t) / tot : 0.f;
+        const VerifyStat sc = ldst(st + c);
+        csum[c] = (sc.m > -INFINITY) ? sc.s * expf((sc.m - M) * inv_t) / tot : 0.f;
         total += csum[c];
       }
     }
@@ -217,12 +139,14 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
   if (lastpos >= 0) atomicMax(&sh_last, lastpos);
   __syncthreads();
   int x = sh_pick != 0x7FFFFFFF ? sh_pick : sh_last;
-  if (x < 0) x = st[c].arg;
+  if (x < 0) x = ldst(st + c).arg;
   __syncthreads();
   return x;
 }
 
-__global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
+// The accept / emit chain of request r (run by the statistics CTA that completes
+// the request's set).
+__device__ void chain_body(const VerifyArgs& a, int r) {
   extern __shared__ float csum[];  // [n_chunks]
   __shared__ float red[8];
   __shared__ float rowM[kB], rowS[kB];
@@ -230,8 +154,6 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
   __shared__ int cid[kK];
   __shared__ float qv[kK];
   __shared__ int sh_decision;
-  pdl_begin();
-  const int r = blockIdx.x;
   int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
   if (a.status[r] != 0) {
     if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
@@ -250,10 +172,11 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
     float M = -INFINITY;
     int A = 0x7FFFFFFF, F = 0;
     for (int c = lane; c < a.n_chunks; c += 32) {
-      F |= sj[c].flags;
-      if (sj[c].m > M || (sj[c].m == M && sj[c].arg < A)) {
-        M = sj[c].m;
-        A = sj[c].arg;
+      const VerifyStat sc = ldst(sj + c);
+      F |= sc.flags;
+      if (sc.m > M || (sc.m == M && sc.arg < A)) {
+        M = sc.m;
+        A = sc.arg;
       }
     }
 #pragma unroll
@@ -269,7 +192,7 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
     float S = 0.f;
     if (T > 0.f && M > -INFINITY && M < INFINITY)
       for (int c = lane; c < a.n_chunks; c += 32)
-        if (sj[c].m > -INFINITY) S += sj[c].s * expf((sj[c].m - M) / T);
+        if (const VerifyStat sc = ldst(sj + c); sc.m > -INFINITY) S += sc.s * expf((sc.m - M) / T);
     S = warp_sum(S);
     if (lane == 0) {
       rowM[j] = M;
@@ -355,12 +278,113 @@ __global__ void __launch_bounds__(256) verify_chain_kernel(const VerifyArgs a) {
   }
 }
 
+// The target logits and temperatures are caller inputs, so the chunk statistics are
+// computed before the wait on the previous kernel; only the store waits.
+__global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
+  __shared__ float sm_m[8], sm_s[8];
+  __shared__ int sm_a[8], sm_f[8];
+  pdl_trigger();
+  const int rj = blockIdx.x;  // r * 8 + j
+  const int r = rj >> 3;
+  const int chunk = blockIdx.y;
+  const float T = a.temperature[r];
+  const float* z = a.logits + static_cast<size_t>(rj) * a.V;
+  const int v0 = chunk * kVerifyChunk;
+  const int v1 = min(a.V, v0 + kVerifyChunk);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int kPer = kVerifyChunk / 256;
+  float xs[kPer];  // this thread's logits of the chunk, loaded once (all in flight)
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + 256 * j;
+    xs[j] = v < v1 ? z[v] : -INFINITY;
+  }
+  float m = -INFINITY;
+  int arg = 0x7FFFFFFF;
+  int flags = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + threadIdx.x + 256 * j;
+    const float x = xs[j];
+    if (v >= v1) continue;
+    if (isnan(x)) {
+      flags |= 1;
+      continue;
+    }
+    if (x == INFINITY) flags |= 2;
+    if (x > m || (x == m && v < arg)) {
+      m = x;
+      arg = v;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
+    if (om > m || (om == m && oa < arg)) {
+      m = om;
+      arg = oa;
+    }
+    flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+  }
+  if (lane == 0) {
+    sm_m[wid] = m;
+    sm_a[wid] = arg;
+    sm_f[wid] = flags;
+  }
+  __syncthreads();
+  float M = sm_m[0];
+  int A = sm_a[0], F = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (sm_m[w] > M || (sm_m[w] == M && sm_a[w] < A)) {
+      M = sm_m[w];
+      A = sm_a[w];
+    }
+    F |= sm_f[w];
+  }
+  float s = 0.f;
+  if (T > 0.f && M > -INFINITY && M < INFINITY) {
+    const float inv_t = 1.f / T;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = v0 + threadIdx.x + 256 * j;
+      if (v < v1 && !isnan(xs[j])) s += expf((xs[j] - M) * inv_t);
+    }
+    s = warp_sum(s);
+    __syncthreads();
+    if (lane == 0) sm_s[wid] = s;
+    __syncthreads();
+    s = 0.f;
+    for (int w = 0; w < 8; ++w) s += sm_s[w];
+  }
+  pdl_wait();  // the statistics buffer is read by the previous step's chain
+  if (threadIdx.x == 0) {
+    VerifyStat st;
+    st.m = M;
+    st.s = s;
+    st.arg = A;
+    st.flags = F;
+    a.stats[static_cast<size_t>(rj) * a.n_chunks + chunk] = st;
+  }
+  // count this chunk; the CTA that completes request r's 8 x n_chunks runs its chain
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int prev = atomicAdd(a.counters + r, 1u);
+    last = prev == static_cast<unsigned int>(kB * a.n_chunks - 1);
+    if (last) a.counters[r] = 0u;  // every CTA of the set has counted
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  chain_body(a, r);
+}
+
 }  // namespace
 
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  cudaError_t e = launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), 0, st, pdl, a);
-  if (e != cudaSuccess) return e;
-  return launch_ex(verify_chain_kernel, dim3(n_req), dim3(256), a.n_chunks * sizeof(float), st, pdl, a);
+  return launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), a.n_chunks * sizeof(float), st, pdl, a);
 }
 
 }  // namespace df2
