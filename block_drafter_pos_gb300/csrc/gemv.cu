@@ -236,16 +236,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
         tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs + lane * 64,
                     c.row0, full0 + 8 * slot, policy);
     };
+    // this lane's activation box (plane, tile, 64-K box), recomputed when the segment changes
+    int xs_seg = -1, x_row = 0, x_b = 0;
+    uint32_t x_dst = 0;
+    bool x_on = false;
     auto issue_x = [&](const Cursor& c, int slot) {
       const GemvSeg& sg = a.seg[c.seg];
-      const int n = sg.n_tiles * kXBoxes * 2;  // boxes of this stage: tile x box x plane
-      for (int i = lane; i < n; i += 32) {
-        const int plane = i / (sg.n_tiles * kXBoxes);
-        const int rem = i % (sg.n_tiles * kXBoxes);
-        const int t = rem / kXBoxes, b = rem % kXBoxes;
-        const uint32_t dst = ring + slot * Geo::kBytes + Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + b) * kXBoxBytes;
-        tma_load_2d(dst, &sg.xmap, c.kabs + b * kXBoxK, plane * sg.x_lo_row + t * 8, full0 + 8 * slot, xpolicy);
+      if (c.seg != xs_seg) {
+        xs_seg = c.seg;
+        const int per = sg.n_tiles * kXBoxes;  // boxes per plane (<= 16)
+        x_on = lane < 2 * per;
+        const int plane = lane / per, rem = lane % per, t = rem / kXBoxes;
+        x_b = rem % kXBoxes;
+        x_dst = Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + x_b) * kXBoxBytes;
+        x_row = plane * sg.x_lo_row + t * 8;
       }
+      if (x_on)
+        tma_load_2d(ring + slot * Geo::kBytes + x_dst, &sg.xmap, c.kabs + x_b * kXBoxK, x_row, full0 + 8 * slot, xpolicy);
     };
     auto arm = [&](const Cursor& c, int slot) {
       const int xbytes = 2 * a.seg[c.seg].n_tiles * kXBoxes * kXBoxBytes;

@@ -68,23 +68,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __gr
     // ---------------------------------------------------------------- producer warp
     const uint64_t policy = evict_first_policy(), xpolicy = evict_last_policy();
     const int xbytes = nt * kXBoxes * 1024 * (LO ? 2 : 1);
+    // the next stage whose weights get armed (K stage within the block, block)
+    int w_st = 0, w_blk = b0;
     auto arm_w = [&](int it) {
       const int slot = it % D;
       if (lane == 0) mbar_expect_tx(full0 + 8 * slot, Geo::kWBytes + xbytes);
       __syncwarp();
       if (lane < kStageK / 64)
-        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<0>(), &a.wmap, (it % nst) * kStageK + lane * 64,
-                    (b0 + it / nst) * kBlockRows, full0 + 8 * slot, policy);
-    };
-    auto issue_x = [&](int it) {
-      const int slot = it % D;
-      const int n = nt * kXBoxes * (LO ? 2 : 1);
-      for (int i = lane; i < n; i += 32) {
-        const int plane = i / (nt * kXBoxes), rem = i % (nt * kXBoxes);
-        const int t = rem / kXBoxes, b = rem % kXBoxes;
-        tma_load_2d(ring + slot * Geo::kBytes + Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + b) * 1024,
-                    &a.xmap, (it % nst) * kStageK + b * 64, plane * a.x_lo_row + t * 8, full0 + 8 * slot, xpolicy);
+        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<0>(), &a.wmap, w_st * kStageK + lane * 64,
+                    w_blk * kBlockRows, full0 + 8 * slot, policy);
+      if (++w_st == nst) {
+        w_st = 0;
+        ++w_blk;
       }
+    };
+    // this lane's activation box (the same every stage): plane, tile, 64-K box
+    const int n_x = nt * kXBoxes * (LO ? 2 : 1);
+    const int x_plane = lane / (nt * kXBoxes), x_rem = lane % (nt * kXBoxes);
+    const int x_t = x_rem / kXBoxes, x_b = x_rem % kXBoxes;
+    const uint32_t x_dst = Geo::kWBytes + x_plane * Geo::kXPlane + (x_t * kXBoxes + x_b) * 1024;
+    const int x_row = x_plane * a.x_lo_row + x_t * 8;
+    int x_st = 0;
+    auto issue_x = [&](int it) {
+      if (lane < n_x)  // n_x <= 32 (nt <= 4, 2 boxes, 2 planes)
+        tma_load_2d(ring + (it % D) * Geo::kBytes + x_dst, &a.xmap, x_st * kStageK + x_b * 64, x_row,
+                    full0 + 8 * (it % D), xpolicy);
+      if (++x_st == nst) x_st = 0;
     };
     const int np = total < D ? total : D;
     for (int it = 0; it < np; ++it) arm_w(it);  // weights first: they do not depend on the previous kernel
@@ -116,8 +125,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __gr
   const uint32_t wrow = static_cast<uint32_t>((wid * 16 + g) * 128);
   const uint32_t xrow = static_cast<uint32_t>(g * 128);
   float c0[NT][4], c1[NT][4], c2[NT][4], c3[NT][4];
+  int st = -1, blk = b0 - 1;  // K stage within the block, block
   for (int it = 0; it < total; ++it) {
-    const int st = it % nst;
+    if (++st == nst || it == 0) {
+      st = 0;
+      ++blk;
+    }
     if (st == 0) {
 #pragma unroll
       for (int t = 0; t < NT; ++t)
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __gr
       }
     }
     consumer_sync();
-    const int v0 = (b0 + it / nst) * kBlockRows;
+    const int v0 = blk * kBlockRows;
     for (int n = wid; n < n_rows; n += kConsumers) {
       const int pos = n & 7;
       if (pos == 0) continue;  // the anchor position is not sampled
