@@ -38,6 +38,12 @@ import numpy as np  # noqa: E402
 METRIC = "DFlash2 draft+verify steps/s at 1 and 16 req; achieved HBM GB/s vs peak"
 
 
+# DRAM bytes (read + write) of one LM-head launch, from the ncu capture summarised in
+# profiles/lmhead_topk_traffic.md, keyed by (vocabulary, width, requests).  Taken on
+# the current lmhead_kernel; re-capture when the kernel changes.
+LMHEAD_TRAFFIC = {(248320, 5120, 1): 2.54e9 + 2.87e6}
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -304,9 +310,10 @@ def main_ours(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s)", "timing": "one CUDA graph of K steps"},
         "drafted_tokens_per_s": steps_per_s * 7 * R,
         "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
-        "roofline": {"kernel": "lmhead_topk_kernel (LM head GEMV + fused top-16)", "bound": "hbm",
+        "roofline": {"kernel": "lmhead_kernel (LM head GEMV + fused top-16)", "bound": "hbm",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                     "traffic": None, "launch_ms": statistics.mean(lm_ms), "share_of_step": statistics.mean(lm_ms) / (ms / K),
+                     "traffic": LMHEAD_TRAFFIC.get((wl.geom.vocab, wl.geom.hidden, R)),
+                     "launch_ms": statistics.mean(lm_ms), "share_of_step": statistics.mean(lm_ms) / (ms / K),
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"},
         "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches_per_step * K),
