@@ -135,7 +135,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   if (c.weight_format != DFLASH2_WEIGHTS_BF16 && c.weight_format != DFLASH2_WEIGHTS_Q8G64) return DFLASH2_E_INVAL;
   if (c.head_dim != 128 || c.block != 8 || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
       c.conv_group != 16 || c.n_layers > DFLASH2_MAX_LAYERS || c.n_q_heads != 4 * c.n_kv_heads ||
-      c.hidden % 256 || c.ffn % 128 || c.vocab % 16 || max_requests > 4 ||
+      c.hidden % 256 || c.ffn % (c.weight_format == DFLASH2_WEIGHTS_BF16 ? 128 : 256) || c.vocab % 16 || max_requests > 4 ||
       (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1 > 64)
     return DFLASH2_E_UNSUPPORTED;
   const int fmt = c.weight_format;
@@ -194,7 +194,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       GemvArgs a;
       memset(&a, 0, sizeof(a));
       for (const GemvSeg& g : segs) a.seg[a.nseg++] = g;
-      const int C = gemv_plan(a, h->num_sms);
+      const int C = gemv_plan(a, h->num_sms, fmt);
       int i = 0;
       for (GemvPlanes* p : pls) *p = gemv_planes(a, i++, C);
       i = 0;

@@ -75,11 +75,11 @@ struct Cursor {
     if (!valid) return;
     seg = find_seg(a, t);
     const GemvSeg& sg = a.seg[seg];
-    kst = sg.K / kStageK;
+    kst = sg.K / a.stage_k;
     const long long local = t - sg.stage_begin;
     row0 = static_cast<int>(local / kst) * kBlockRows;
     kstage = static_cast<int>(local % kst);
-    kabs = kstage * kStageK;
+    kabs = kstage * a.stage_k;
   }
   DF2_DEV void start(const GemvArgs& a) {
     const long long T = a.total_stages, C = gridDim.x;
@@ -93,7 +93,7 @@ struct Cursor {
       return;
     }
     if (++kstage < kst) {
-      kabs += kStageK;
+      kabs += a.stage_k;
       return;
     }
     kstage = 0;
@@ -102,7 +102,7 @@ struct Cursor {
     if (row0 >= a.seg[seg].M) {
       ++seg;
       row0 = 0;
-      kst = a.seg[seg].K / kStageK;
+      kst = a.seg[seg].K / a.stage_k;
     }
   }
   DF2_DEV bool opens(long long t_first) const { return kstage == 0 || t == t_first; }
@@ -138,8 +138,8 @@ DF2_DEV uint32_t dequant2(uint32_t codes_biased, uint32_t sel, __half2 s, __half
   return *reinterpret_cast<uint32_t*>(&w);
 }
 
-// Scale and bias (bf16 bits) of one Q8 stage's kStageK / 64 groups for rows g and g + 8.
-constexpr int kAffGroups = kStageK / 64;
+// Scale and bias (bf16 bits) of one Q8 stage's groups for rows g and g + 8.
+constexpr int kAffGroups = stage_k<1>() / 64;
 struct Q8Affine {
   uint16_t s0[kAffGroups], s1[kAffGroups], b0[kAffGroups], b1[kAffGroups];
 };
@@ -159,14 +159,14 @@ DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs) {
   return r;
 }
 
-// Q8 stage: codes kStageK/64 boxes [64 K][kBlockRows rows] (one group each);
-// fp16 activations per tile and plane kStageK/64 boxes [64 K][8 rows] (1 KB each,
+// Q8 stage: codes in 4 boxes [64 K][kBlockRows rows] (one group each, 256 K);
+// fp16 activations per tile and plane 4 boxes [64 K][8 rows] (1 KB each,
 // 128-byte swizzle).  wa: this lane's row g in box 0; xrow: row g of tile 0, box 0, hi.
 template <int NT>
 DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, const Q8Affine& af,
                       float (&c0)[NT][4], float (&c1)[NT][4], float (&c2)[NT][4], float (&c3)[NT][4]) {
-  constexpr int kXPlane = 8 * NT * kStageK * 2;
-  constexpr int kG = kStageK / 64;
+  constexpr int kXPlane = 8 * NT * stage_k<1>() * 2;
+  constexpr int kG = stage_k<1>() / 64;
   const uint32_t pa = static_cast<uint32_t>(((2 * q) ^ g) << 4), pc = static_cast<uint32_t>(((2 * q + 1) ^ g) << 4);
 #pragma unroll
   for (int gi = 0; gi < kG; ++gi) {
@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     // ---------------------------------------------------------------- producer warp
     const uint64_t policy = evict_first_policy();  // weights: streamed once
     const uint64_t xpolicy = evict_last_policy();  // activations: read by every CTA
-    constexpr int kWBoxes = kStageK / 64;  // weight boxes per stage (64 K each)
-    constexpr int kXBoxes = kStageK / 64;  // activation boxes per tile and plane (64 K x 8 rows)
+    constexpr int kWBoxes = stage_k<FMT>() / 64;  // weight boxes per stage (64 K each)
+    constexpr int kXBoxes = stage_k<FMT>() / 64;  // activation boxes per tile and plane (64 K x 8 rows)
     constexpr int kXBoxK = 64;
     constexpr int kXBoxBytes = 8 * kXBoxK * 2;
     auto issue_w = [&](const Cursor& c, int slot) {
@@ -236,23 +236,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
         tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs + lane * 64,
                     c.row0, full0 + 8 * slot, policy);
     };
-    // this lane's activation box (plane, tile, 64-K box), recomputed when the segment changes
-    int xs_seg = -1, x_row = 0, x_b = 0;
-    uint32_t x_dst = 0;
-    bool x_on = false;
+    // this lane's activation boxes (plane, tile, 64-K box): box indices lane and lane + 32,
+    // recomputed when the segment changes
+    constexpr int kXPerLane = (2 * NT * kXBoxes + 31) / 32;
+    int xs_seg = -1, x_row[kXPerLane], x_b[kXPerLane];
+    uint32_t x_dst[kXPerLane];
+    bool x_on[kXPerLane];
     auto issue_x = [&](const Cursor& c, int slot) {
       const GemvSeg& sg = a.seg[c.seg];
       if (c.seg != xs_seg) {
         xs_seg = c.seg;
-        const int per = sg.n_tiles * kXBoxes;  // boxes per plane (<= 16)
-        x_on = lane < 2 * per;
-        const int plane = lane / per, rem = lane % per, t = rem / kXBoxes;
-        x_b = rem % kXBoxes;
-        x_dst = Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + x_b) * kXBoxBytes;
-        x_row = plane * sg.x_lo_row + t * 8;
+        const int per = sg.n_tiles * kXBoxes;  // boxes per plane
+#pragma unroll
+        for (int j = 0; j < kXPerLane; ++j) {
+          const int box = lane + 32 * j;
+          x_on[j] = box < 2 * per;
+          const int plane = box / per, rem = box % per, t = rem / kXBoxes;
+          x_b[j] = rem % kXBoxes;
+          x_dst[j] = Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + x_b[j]) * kXBoxBytes;
+          x_row[j] = plane * sg.x_lo_row + t * 8;
+        }
       }
-      if (x_on)
-        tma_load_2d(ring + slot * Geo::kBytes + x_dst, &sg.xmap, c.kabs + x_b * kXBoxK, x_row, full0 + 8 * slot, xpolicy);
+#pragma unroll
+      for (int j = 0; j < kXPerLane; ++j)
+        if (x_on[j])
+          tma_load_2d(ring + slot * Geo::kBytes + x_dst[j], &sg.xmap, c.kabs + x_b[j] * kXBoxK, x_row[j],
+                      full0 + 8 * slot, xpolicy);
     };
     auto arm = [&](const Cursor& c, int slot) {
       const int xbytes = 2 * a.seg[c.seg].n_tiles * kXBoxes * kXBoxBytes;
@@ -415,12 +424,13 @@ bool lm_encode_map(CUtensorMap* map, const void* p, int inner, int rows, int box
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-int gemv_plan(GemvArgs& a, int num_sms) {
+int gemv_plan(GemvArgs& a, int num_sms, int fmt) {
+  a.stage_k = fmt == 0 ? stage_k<0>() : stage_k<1>();
   long long T = 0;
   for (int i = 0; i < a.nseg; ++i) {
     GemvSeg& sg = a.seg[i];
     sg.stage_begin = T;
-    T += static_cast<long long>(sg.M / kBlockRows) * (sg.K / kStageK);
+    T += static_cast<long long>(sg.M / kBlockRows) * (sg.K / a.stage_k);
   }
   a.total_stages = T;
   const long long C = static_cast<long long>(num_sms) * kCtasPerSm;
@@ -432,7 +442,7 @@ GemvPlanes gemv_planes(const GemvArgs& a, int i, int C) {
   p.T = a.total_stages;
   p.base = a.seg[i].stage_begin;
   p.C = C;
-  p.kst = a.seg[i].K / kStageK;
+  p.kst = a.seg[i].K / a.stage_k;
   return p;
 }
 
@@ -444,11 +454,12 @@ int gemv_max_planes(const GemvArgs& a, int i, int C) {
 }
 
 cudaError_t launch_gemv(GemvArgs& a, int fmt, int max_tiles, int num_sms, bool pdl, cudaStream_t st) {
+  const int ks = fmt == 0 ? stage_k<0>() : stage_k<1>();
   for (int i = 0; i < a.nseg; ++i) {
     const GemvSeg& sg = a.seg[i];
-    if (sg.M % kBlockRows || sg.K % kStageK || sg.n_tiles < 1 || sg.n_tiles > max_tiles) return cudaErrorInvalidValue;
+    if (sg.M % kBlockRows || sg.K % ks || sg.n_tiles < 1 || sg.n_tiles > max_tiles) return cudaErrorInvalidValue;
   }
-  const int C = gemv_plan(a, num_sms);
+  const int C = gemv_plan(a, num_sms, fmt);
   if (a.total_stages < 1) return cudaErrorInvalidValue;
   if (fmt == 0) {
     if (max_tiles <= 1) return launch_nt<1, 0>(a, C, pdl, st);

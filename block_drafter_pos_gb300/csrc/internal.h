@@ -41,6 +41,7 @@ struct GemvArgs {
   GemvSeg seg[kMaxSeg];
   int nseg;
   long long total_stages;  // T (set by gemv_plan)
+  int stage_k;             // K per stage: 128 (bf16) or 256 (int8) (set by gemv_plan)
   int* err;                // set nonzero if a pipeline wait gave up (never in a correct run), or null
 };
 
@@ -60,8 +61,9 @@ DF2_HD inline int gemv_plane_count(const GemvPlanes& p, int m) {
   return gemv_cta_of_stage(b0 + p.kst - 1, p.C, p.T) - gemv_cta_of_stage(b0, p.C, p.T) + 1;
 }
 
-// Fills stage_begin and total_stages; returns the CTA count of the launch.
-int gemv_plan(GemvArgs& a, int num_sms);
+// Fills stage_begin, total_stages and stage_k for the weight format; returns the
+// CTA count of the launch.
+int gemv_plan(GemvArgs& a, int num_sms, int fmt);
 // Plane map of segment i of a planned launch with C CTAs, and its largest plane count.
 GemvPlanes gemv_planes(const GemvArgs& a, int i, int C);
 int gemv_max_planes(const GemvArgs& a, int i, int C);

@@ -13,7 +13,11 @@ namespace df2 {
 namespace pipe {
 
 constexpr int kBlockRows = 64;                // weight rows per unit
-constexpr int kStageK = kGemvStageK;          // K per stage
+constexpr int kStageK = kGemvStageK;          // K per stage of bf16 weights (16 KB of 64 rows)
+// K per stage by weight format: int8 stages hold twice the K in the same 16 KB
+// (the pipeline streams at a rate set by stages, not bytes).
+template <int FMT>
+constexpr int stage_k() { return FMT == 0 ? kStageK : 2 * kStageK; }
 constexpr int kConsumers = kBlockRows / 16;   // consumer warps per CTA (16 weight rows each)
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;
@@ -27,8 +31,8 @@ constexpr long long kSpinLimit = 1ll << 22;
 // Shared-memory geometry of one stage for a format and a number of 8-row activation tiles.
 template <int FMT, int NT>
 struct StageGeo {
-  static constexpr int kWBytes = kBlockRows * kStageK * (FMT == 0 ? 2 : 1);
-  static constexpr int kXPlane = 8 * NT * kStageK * 2;  // 8*NT rows x kStageK x 2 B
+  static constexpr int kWBytes = kBlockRows * stage_k<FMT>() * (FMT == 0 ? 2 : 1);
+  static constexpr int kXPlane = 8 * NT * stage_k<FMT>() * 2;  // 8*NT rows x stage K x 2 B
   static constexpr int kBytes = kWBytes + 2 * kXPlane;
   static constexpr int kDepthRaw = kRingBudget / kBytes;
   static constexpr int kDepth = kDepthRaw < 2 ? 2 : (kDepthRaw > kMaxDepth ? kMaxDepth : kDepthRaw);
