@@ -138,66 +138,86 @@ DF2_DEV uint32_t dequant2(uint32_t codes_biased, uint32_t sel, __half2 s, __half
   return *reinterpret_cast<uint32_t*>(&w);
 }
 
-// Scale and bias (bf16 bits) of one Q8 stage's groups for rows g and g + 8.
-constexpr int kAffGroups = stage_k<1>() / 64;
+// Scale and bias (bf16 bits) of the two groups a lane meets in one Q8 stage (one per
+// code box: group 2b + q/2 of the stage), for rows g and g + 8.
+constexpr int kAffGroups = stage_k<1>() / wbox_k<1>();
 struct Q8Affine {
   uint16_t s0[kAffGroups], s1[kAffGroups], b0[kAffGroups], b1[kAffGroups];
 };
 
-DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs) {
+DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs, int q) {
   const int KG = sg.K >> 6;
-  const size_t i0 = static_cast<size_t>(row) * KG + (kabs >> 6);
+  const size_t i0 = static_cast<size_t>(row) * KG + (kabs >> 6) + (q >> 1);
   const size_t i1 = i0 + static_cast<size_t>(8) * KG;
   Q8Affine r;
 #pragma unroll
   for (int j = 0; j < kAffGroups; ++j) {
-    r.s0[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i0 + j);
-    r.s1[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i1 + j);
-    r.b0[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i0 + j);
-    r.b1[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i1 + j);
+    r.s0[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i0 + 2 * j);
+    r.s1[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i1 + 2 * j);
+    r.b0[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i0 + 2 * j);
+    r.b1[j] = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i1 + 2 * j);
   }
   return r;
 }
 
-// Q8 stage: codes in 4 boxes [64 K][kBlockRows rows] (one group each, 256 K);
-// fp16 activations per tile and plane 4 boxes [64 K][8 rows] (1 KB each,
-// 128-byte swizzle).  wa: this lane's row g in box 0; xrow: row g of tile 0, box 0, hi.
+// Q8 stage: codes in two boxes [128 K][kBlockRows rows] (128-byte rows, 128-byte
+// swizzle); fp16 activations per tile and plane in four boxes [64 K][8 rows] (1 KB
+// each, 128-byte swizzle).  In code box b, lane (g, q) takes K 32q .. 32q + 31 (one
+// group of 64: 2b + q/2): pieces 2q and 2q + 1 of rows g and g + 8, and pieces
+// 4(q & 1) .. 4(q & 1) + 3 of activation box 2b + q/2.  Lanes with q >= 2 take
+// the two halves in the opposite order (weight pieces 2q + 1 then 2q, activation
+// piece j ^ 2 in register j), which puts every quarter-warp's 16-byte loads on
+// distinct banks; which K an MMA slot holds then depends on q alone, the same for
+// A and B.  wa: row g of this warp in code box 0; xrow: row g of tile 0, box 0, hi.
 template <int NT>
 DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, const Q8Affine& af,
                       float (&c0)[NT][4], float (&c1)[NT][4], float (&c2)[NT][4], float (&c3)[NT][4]) {
   constexpr int kXPlane = 8 * NT * stage_k<1>() * 2;
-  constexpr int kG = stage_k<1>() / 64;
-  const uint32_t pa = static_cast<uint32_t>(((2 * q) ^ g) << 4), pc = static_cast<uint32_t>(((2 * q + 1) ^ g) << 4);
+  constexpr int kXBoxes = stage_k<1>() / 64;
+  constexpr int kWBoxes = stage_k<1>() / wbox_k<1>();
+  const int sw = q & 2;
+  const uint32_t pf = static_cast<uint32_t>(((2 * q + (sw >> 1)) ^ g) << 4);
+  const uint32_t ps = static_cast<uint32_t>(((2 * q + 1 - (sw >> 1)) ^ g) << 4);
+  uint32_t xo[4];
 #pragma unroll
-  for (int gi = 0; gi < kG; ++gi) {
-    const uint4 r0 = lds128(wa + gi * wbox_bytes<1>());        // 16 codes of row g
-    const uint4 r1 = lds128(wa + gi * wbox_bytes<1>() + 512);  // row g + 8
-    const __half2 sg0 = bf16_bits_half2(af.s0[gi]), sg1 = bf16_bits_half2(af.s1[gi]);
-    const __half2 bg0 = bf16_bits_half2(af.b0[gi]), bg1 = bf16_bits_half2(af.b1[gi]);
-    const uint32_t u0[4] = {r0.x ^ 0x80808080u, r0.y ^ 0x80808080u, r0.z ^ 0x80808080u, r0.w ^ 0x80808080u};
-    const uint32_t u1[4] = {r1.x ^ 0x80808080u, r1.y ^ 0x80808080u, r1.z ^ 0x80808080u, r1.w ^ 0x80808080u};
-    uint32_t A[4][4];
+  for (int j = 0; j < 4; ++j)
+    xo[j] = static_cast<uint32_t>((((4 * (q & 1) + (j ^ sw)) ^ g) << 4) + (q >> 1) * 1024);
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      A[m][0] = dequant2(u0[m], 0x4140, sg0, bg0);
-      A[m][1] = dequant2(u1[m], 0x4140, sg1, bg1);
-      A[m][2] = dequant2(u0[m], 0x4342, sg0, bg0);
-      A[m][3] = dequant2(u1[m], 0x4342, sg1, bg1);
-    }
+  for (int b = 0; b < kWBoxes; ++b) {
+    const uint32_t wb = wa + b * wbox_bytes<1>();
+    const uint4 w0[2] = {lds128(wb + pf), lds128(wb + ps)};                // row g, two halves
+    const uint4 w1[2] = {lds128(wb + 1024 + pf), lds128(wb + 1024 + ps)};  // row g + 8
+    const __half2 sg0 = bf16_bits_half2(af.s0[b]), sg1 = bf16_bits_half2(af.s1[b]);
+    const __half2 bg0 = bf16_bits_half2(af.b0[b]), bg1 = bf16_bits_half2(af.b1[b]);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      if (t < n_tiles) {
-        const uint32_t xb = xrow + (t * kG + gi) * 1024;
-        const uint4 xa = lds128(xb + pa), xc = lds128(xb + pc);  // K 16q..16q+7, 16q+8..16q+15
-        const uint4 ya = lds128(xb + kXPlane + pa), yc = lds128(xb + kXPlane + pc);
-        mma_f16(c0[t], A[0][0], A[0][1], A[0][2], A[0][3], xa.x, xa.y);
-        mma_f16(c1[t], A[1][0], A[1][1], A[1][2], A[1][3], xa.z, xa.w);
-        mma_f16(c0[t], A[2][0], A[2][1], A[2][2], A[2][3], xc.x, xc.y);
-        mma_f16(c1[t], A[3][0], A[3][1], A[3][2], A[3][3], xc.z, xc.w);
-        mma_f16(c2[t], A[0][0], A[0][1], A[0][2], A[0][3], ya.x, ya.y);
-        mma_f16(c3[t], A[1][0], A[1][1], A[1][2], A[1][3], ya.z, ya.w);
-        mma_f16(c2[t], A[2][0], A[2][1], A[2][2], A[2][3], yc.x, yc.y);
-        mma_f16(c3[t], A[3][0], A[3][1], A[3][2], A[3][3], yc.z, yc.w);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t u0[4] = {w0[h].x ^ 0x80808080u, w0[h].y ^ 0x80808080u, w0[h].z ^ 0x80808080u,
+                              w0[h].w ^ 0x80808080u};
+      const uint32_t u1[4] = {w1[h].x ^ 0x80808080u, w1[h].y ^ 0x80808080u, w1[h].z ^ 0x80808080u,
+                              w1[h].w ^ 0x80808080u};
+      uint32_t A[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        A[m][0] = dequant2(u0[m], 0x4140, sg0, bg0);
+        A[m][1] = dequant2(u1[m], 0x4140, sg1, bg1);
+        A[m][2] = dequant2(u0[m], 0x4342, sg0, bg0);
+        A[m][3] = dequant2(u1[m], 0x4342, sg1, bg1);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (t < n_tiles) {
+          const uint32_t xb = xrow + (t * kXBoxes + 2 * b) * 1024;
+          const uint4 xa = lds128(xb + xo[2 * h]), xc = lds128(xb + xo[2 * h + 1]);  // 8 + 8 K of this half
+          const uint4 ya = lds128(xb + kXPlane + xo[2 * h]), yc = lds128(xb + kXPlane + xo[2 * h + 1]);
+          mma_f16(c0[t], A[0][0], A[0][1], A[0][2], A[0][3], xa.x, xa.y);
+          mma_f16(c1[t], A[1][0], A[1][1], A[1][2], A[1][3], xa.z, xa.w);
+          mma_f16(c0[t], A[2][0], A[2][1], A[2][2], A[2][3], xc.x, xc.y);
+          mma_f16(c1[t], A[3][0], A[3][1], A[3][2], A[3][3], xc.z, xc.w);
+          mma_f16(c2[t], A[0][0], A[0][1], A[0][2], A[0][3], ya.x, ya.y);
+          mma_f16(c3[t], A[1][0], A[1][1], A[1][2], A[1][3], ya.z, ya.w);
+          mma_f16(c2[t], A[2][0], A[2][1], A[2][2], A[2][3], yc.x, yc.y);
+          mma_f16(c3[t], A[3][0], A[3][1], A[3][2], A[3][3], yc.z, yc.w);
+        }
       }
     }
   }
@@ -227,13 +247,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     // ---------------------------------------------------------------- producer warp
     const uint64_t policy = evict_first_policy();  // weights: streamed once
     const uint64_t xpolicy = evict_last_policy();  // activations: read by every CTA
-    constexpr int kWBoxes = stage_k<FMT>() / 64;  // weight boxes per stage (64 K each)
+    constexpr int kWBoxes = stage_k<FMT>() / wbox_k<FMT>();  // weight boxes per stage
     constexpr int kXBoxes = stage_k<FMT>() / 64;  // activation boxes per tile and plane (64 K x 8 rows)
     constexpr int kXBoxK = 64;
     constexpr int kXBoxBytes = 8 * kXBoxK * 2;
     auto issue_w = [&](const Cursor& c, int slot) {
       if (lane < kWBoxes)
-        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs + lane * 64,
+        tma_load_2d(ring + slot * Geo::kBytes + lane * wbox_bytes<FMT>(), &a.seg[c.seg].wmap, c.kabs + lane * wbox_k<FMT>(),
                     c.row0, full0 + 8 * slot, policy);
     };
     // this lane's activation boxes (plane, tile, 64-K box): box indices lane and lane + 32,
@@ -309,18 +329,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   // ------------------------------------------------------------------ consumer warps
   pdl_wait();
   const int g = lane >> 2, q = lane & 3;
-  const uint32_t swz = static_cast<uint32_t>((q ^ ((g >> 1) & 3)) << 4);
-  // row g of this warp in a weight box (bf16: 128-byte rows, pieces chosen in stage_bf16;
-  // int8: 64-byte rows, piece q under the 64-byte swizzle), and row g of an activation box
-  const uint32_t wrow = FMT == 0 ? static_cast<uint32_t>((wid * 16 + g) * 128)
-                                 : static_cast<uint32_t>((wid * 16 + g) * 64) + swz;
+  // row g of this warp in a weight box (128-byte rows; the stage functions choose the
+  // pieces), and row g of an activation box
+  const uint32_t wrow = static_cast<uint32_t>((wid * 16 + g) * 128);
   const uint32_t xrow = static_cast<uint32_t>(g * 128);
   float c0[NT][4], c1[NT][4], c2[NT][4], c3[NT][4];
   Cursor c;
   c.start(a);
   const long long t_first = c.t;
   Q8Affine af = {};
-  if (FMT == 1 && c.valid) af = load_affine(a.seg[c.seg], c.row0 + wid * 16 + g, c.kabs);
+  if (FMT == 1 && c.valid) af = load_affine(a.seg[c.seg], c.row0 + wid * 16 + g, c.kabs, q);
   int it = 0;
   while (c.valid) {
     if (c.opens(t_first)) {
@@ -335,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     Cursor cn = c;
     cn.next(a);
     Q8Affine afn = af;
-    if (FMT == 1 && cn.valid) afn = load_affine(a.seg[cn.seg], cn.row0 + wid * 16 + g, cn.kabs);
+    if (FMT == 1 && cn.valid) afn = load_affine(a.seg[cn.seg], cn.row0 + wid * 16 + g, cn.kabs, q);
     if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * slot, static_cast<uint32_t>((it / D) & 1)))) {
       if (lane == 0 && a.err != nullptr) atomicExch(a.err, 1);
       break;
@@ -405,7 +423,7 @@ bool gemv_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt) {
   if (fmt == 0)
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, 64, kBlockRows, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, 64, kBlockRows, CU_TENSOR_MAP_SWIZZLE_64B,
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, wbox_k<1>(), kBlockRows, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 

@@ -23,9 +23,12 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;
 constexpr int kRingBudget = (kCtasPerSm == 1 ? 208 : 200 / kCtasPerSm) * 1024;
 constexpr int kMaxDepth = 24;
-// One weight copy: 64 K x kBlockRows rows (128-byte rows for bf16, 64-byte rows for int8 codes).
+// One weight copy: kBlockRows rows of 128 bytes (64 K of bf16, 128 K of int8 codes),
+// 128-byte swizzle.
 template <int FMT>
-constexpr int wbox_bytes() { return 64 * (FMT == 0 ? 2 : 1) * kBlockRows; }
+constexpr int wbox_k() { return FMT == 0 ? 64 : 128; }
+template <int FMT>
+constexpr int wbox_bytes() { return 128 * kBlockRows; }
 constexpr long long kSpinLimit = 1ll << 22;
 
 // Shared-memory geometry of one stage for a format and a number of 8-row activation tiles.
