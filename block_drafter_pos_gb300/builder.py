@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdflash2.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["api.cu", "gemv.cu", "glue.cu", "attention.cu", "lmhead.cu", "select.cu", "verify.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemv.cu", "wide.cu", "glue.cu", "attention.cu", "lmhead.cu", "select.cu", "verify.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

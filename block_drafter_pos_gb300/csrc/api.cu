@@ -31,7 +31,15 @@ struct dflash2_handle {
   int nch_ss;  // 32-channel chunks of the sums-of-squares partials
   int n_attn_chunks, n_verify_chunks, lm_ctas;
   // where each projection's partial planes are (the launches' shapes are fixed at create)
-  GemvPlanes pl_fc, pl_d0, pl_d, pl_q, pl_k, pl_v, pl_o, pl_g, pl_u, pl_down, pl_sel;
+  // plane maps of every projection launch: the GEMV (up to 4 requests) and the
+  // tensor-core GEMM (more requests; set up when max_requests > 4)
+  struct PlaneSet {
+    GemvPlanes fc, d0, d, q, k, v, o, g, u, down, sel, lm;
+  } pn, pw;
+  bool wide;  // the tensor-core path is set up
+  CUtensorMap wmap_fc, wmap_sel, wmap_lm, wmap_layer[DFLASH2_MAX_LAYERS][9];  // its weight maps
+  float* lm_part;  // [p][N][V] LM-head partial planes of the GEMM path
+  int lm_chunks;   // vocabulary chunks of its top-16
   // tensor maps of the projection matrices (bulk-copy descriptors, encoded at create)
   CUtensorMap map_fc, map_sel;
   CUtensorMap map_layer[DFLASH2_MAX_LAYERS][9];  // q k v o gate up down attn_delta mlp_delta
@@ -70,10 +78,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 8 * n_tiles activation rows starting at x.
 enum { kQ, kK, kV, kO, kGate, kUp, kDown, kAttnDelta, kMlpDelta };
 
-// x_rows: rows of one plane of the activation buffer behind xmap (its lo plane starts there).
-GemvSeg seg(const CUtensorMap& wmap, const dflash2_matrix& m, const CUtensorMap& xmap, int x_rows, int n_tiles, int M,
-            int K, float* out) {
-  GemvSeg s;
+// One projection segment of either path.  x_rows: rows of one plane of the
+// activation buffer behind xmap (its lo plane starts there); x: that buffer, from
+// which the GEMM path encodes its own activation map; wide_map: the weight map of
+// the GEMM path.
+struct SegSpec {
+  GemvSeg g;
+  const CUtensorMap* wide_map;
+  const void* x;
+};
+
+SegSpec seg(const CUtensorMap& wmap, const CUtensorMap& wide_map, const dflash2_matrix& m, const CUtensorMap& xmap,
+            const void* x, int x_rows, int n_tiles, int M, int K, float* out) {
+  SegSpec r;
+  GemvSeg& s = r.g;
   memset(&s, 0, sizeof(s));
   s.wmap = wmap;
   s.xmap = xmap;
@@ -84,19 +102,32 @@ GemvSeg seg(const CUtensorMap& wmap, const dflash2_matrix& m, const CUtensorMap&
   s.K = K;
   s.n_tiles = n_tiles;
   s.out = out;
-  return s;
+  r.wide_map = &wide_map;
+  r.x = x;
+  return r;
 }
 
-dflash2_status run_gemv(dflash2_handle* h, std::initializer_list<GemvSeg> segs, cudaStream_t st) {
+// Launches the segments on the GEMV (wide == false) or on the tensor-core GEMM.
+dflash2_status run_gemv(dflash2_handle* h, bool wide, std::initializer_list<SegSpec> segs, cudaStream_t st,
+                        int fmt = -1) {
+  if (fmt < 0) fmt = h->fmt;
   GemvArgs a;
   memset(&a, 0, sizeof(a));
   int max_tiles = 0;
-  for (const GemvSeg& s : segs) {
-    a.seg[a.nseg++] = s;
-    max_tiles = std::max(max_tiles, s.n_tiles);
+  for (const SegSpec& s : segs) {
+    GemvSeg& g = a.seg[a.nseg++];
+    g = s.g;
+    max_tiles = std::max(max_tiles, g.n_tiles);
+    if (wide) {
+      g.wmap = *s.wide_map;
+      if (!wide_encode_xmap(&g.xmap, s.x, 8 * g.n_tiles, g.K, fmt)) return DFLASH2_E_CUDA;
+    }
   }
   a.err = h->gemv_err;
-  DF2_CHECK(launch_gemv(a, h->fmt, max_tiles, h->num_sms, h->pdl, st));
+  if (wide)
+    DF2_CHECK(launch_wide(a, fmt, h->num_sms, h->pdl, st));
+  else
+    DF2_CHECK(launch_gemv(a, fmt, max_tiles, h->num_sms, h->pdl, st));
   h->launches += 1;
   return DFLASH2_OK;
 }
@@ -135,7 +166,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   if (c.weight_format != DFLASH2_WEIGHTS_BF16 && c.weight_format != DFLASH2_WEIGHTS_Q8G64) return DFLASH2_E_INVAL;
   if (c.head_dim != 128 || c.block != 8 || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
       c.conv_group != 16 || c.n_layers > DFLASH2_MAX_LAYERS || c.n_q_heads != 4 * c.n_kv_heads ||
-      c.hidden % 256 || c.ffn % (c.weight_format == DFLASH2_WEIGHTS_BF16 ? 128 : 256) || c.vocab % 16 || max_requests > 4 ||
+      c.hidden % 256 || c.ffn % (c.weight_format == DFLASH2_WEIGHTS_BF16 ? 128 : 256) || c.vocab % 16 || max_requests > DFLASH2_MAX_REQUESTS ||
       (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1 > 64)
     return DFLASH2_E_UNSUPPORTED;
   const int fmt = c.weight_format;
@@ -178,8 +209,12 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->n_attn_chunks = (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1;
   h->n_verify_chunks = (c.vocab + kVerifyChunk - 1) / kVerifyChunk;
   h->lm_ctas = lmhead_ctas(h->num_sms);
-  // plane maps of every projection launch (shapes only; the same plan as launch_gemv's)
-  int maxp_fc = 0, maxp_d = 0, maxp_q = 0, maxp_k = 0, maxp_v = 0, maxp_y = 0, maxp_g = 0, maxp_u = 0, maxp_sel = 0;
+  // plane maps of every projection launch (shapes only; the same plans as launch_gemv's
+  // and launch_wide's), and the largest plane count of each output buffer over both
+  h->wide = max_requests > 4;
+  h->lm_chunks = (c.vocab + kLogitChunk - 1) / kLogitChunk;
+  int maxp_fc = 0, maxp_d = 0, maxp_q = 0, maxp_k = 0, maxp_v = 0, maxp_y = 0, maxp_g = 0, maxp_u = 0, maxp_sel = 0,
+      maxp_lm = 0;
   {
     auto shape = [](int M, int K) {
       GemvSeg g;
@@ -189,25 +224,33 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       g.n_tiles = 1;
       return g;
     };
-    auto plan = [&](std::initializer_list<GemvSeg> segs, std::initializer_list<GemvPlanes*> pls,
-                    std::initializer_list<int*> maxes) {
-      GemvArgs a;
-      memset(&a, 0, sizeof(a));
-      for (const GemvSeg& g : segs) a.seg[a.nseg++] = g;
-      const int C = gemv_plan(a, h->num_sms, fmt);
-      int i = 0;
-      for (GemvPlanes* p : pls) *p = gemv_planes(a, i++, C);
-      i = 0;
-      for (int* mx : maxes) *mx = std::max(*mx, gemv_max_planes(a, i++, C));
-    };
-    plan({shape(h->H, h->KT), shape(4 * h->G, h->H)}, {&h->pl_fc, &h->pl_d0}, {&maxp_fc, &maxp_d});
-    plan({shape(4 * h->G, h->H)}, {&h->pl_d}, {&maxp_d});
-    plan({shape(h->qd, h->H), shape(h->kvd, h->H), shape(h->kvd, h->H)}, {&h->pl_q, &h->pl_k, &h->pl_v},
-         {&maxp_q, &maxp_k, &maxp_v});
-    plan({shape(h->H, h->qd)}, {&h->pl_o}, {&maxp_y});
-    plan({shape(h->F, h->H), shape(h->F, h->H)}, {&h->pl_g, &h->pl_u}, {&maxp_g, &maxp_u});
-    plan({shape(h->H, h->F)}, {&h->pl_down}, {&maxp_y});
-    plan({shape(c.rank, h->H)}, {&h->pl_sel}, {&maxp_sel});
+    for (int path = 0; path < (h->wide ? 2 : 1); ++path) {
+      dflash2_handle::PlaneSet& P = path == 0 ? h->pn : h->pw;
+      auto plan = [&](std::initializer_list<GemvSeg> segs, std::initializer_list<GemvPlanes*> pls,
+                      std::initializer_list<int*> maxes) {
+        GemvArgs a;
+        memset(&a, 0, sizeof(a));
+        for (const GemvSeg& g : segs) a.seg[a.nseg++] = g;
+        const int C = path == 0 ? gemv_plan(a, h->num_sms, fmt) : wide_plan(a, h->num_sms);
+        int i = 0;
+        for (GemvPlanes* p : pls) *p = path == 0 ? gemv_planes(a, i++, C) : wide_planes(a, i++, C);
+        i = 0;
+        for (int* mx : maxes) {
+          const int n = path == 0 ? gemv_max_planes(a, i, C) : wide_max_planes(a, i, C);
+          *mx = std::max(*mx, n);
+          ++i;
+        }
+      };
+      plan({shape(h->H, h->KT), shape(4 * h->G, h->H)}, {&P.fc, &P.d0}, {&maxp_fc, &maxp_d});
+      plan({shape(4 * h->G, h->H)}, {&P.d}, {&maxp_d});
+      plan({shape(h->qd, h->H), shape(h->kvd, h->H), shape(h->kvd, h->H)}, {&P.q, &P.k, &P.v},
+           {&maxp_q, &maxp_k, &maxp_v});
+      plan({shape(h->H, h->qd)}, {&P.o}, {&maxp_y});
+      plan({shape(h->F, h->H), shape(h->F, h->H)}, {&P.g, &P.u}, {&maxp_g, &maxp_u});
+      plan({shape(h->H, h->F)}, {&P.down}, {&maxp_y});
+      plan({shape(c.rank, h->H)}, {&P.sel}, {&maxp_sel});
+      if (path == 1) plan({shape(h->V, h->H)}, {&P.lm}, {&maxp_lm});
+    }
   }
   bool maps_ok = gemv_encode_wmap(&h->map_fc, w->fc.w, h->H, h->KT, fmt) &&
             gemv_encode_wmap(&h->map_sel, w->sel_proj.w, c.rank, h->H, fmt);
@@ -220,6 +263,21 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
                  {&L.o, h->H, h->qd},        {&L.gate, h->F, h->H},    {&L.up, h->F, h->H},
                  {&L.down, h->H, h->F},      {&L.attn_delta, 4 * h->G, h->H}, {&L.mlp_delta, 4 * h->G, h->H}};
     for (int i = 0; i < 9 && maps_ok; ++i) maps_ok = gemv_encode_wmap(&h->map_layer[l][i], mats[i].m->w, mats[i].M, mats[i].K, fmt);
+  }
+  if (h->wide) {
+    // the tensor-core GEMM: 128-row weight blocks (every output width a multiple of 128)
+    maps_ok = maps_ok && (4 * h->G) % 128 == 0 && h->V % 128 == 0 &&
+              wide_encode_wmap(&h->wmap_fc, w->fc.w, h->H, h->KT, fmt) &&
+              wide_encode_wmap(&h->wmap_sel, w->sel_proj.w, c.rank, h->H, fmt) &&
+              wide_encode_wmap(&h->wmap_lm, w->lm_head, h->V, h->H, 0);
+    for (int l = 0; l < c.n_layers && maps_ok; ++l) {
+      const dflash2_layer_weights& L = w->layers[l];
+      const dflash2_matrix* ms[9] = {&L.q, &L.k, &L.v, &L.o, &L.gate, &L.up, &L.down, &L.attn_delta, &L.mlp_delta};
+      const int MK[9][2] = {{h->qd, h->H}, {h->kvd, h->H}, {h->kvd, h->H}, {h->H, h->qd}, {h->F, h->H},
+                            {h->F, h->H}, {h->H, h->F}, {4 * h->G, h->H}, {4 * h->G, h->H}};
+      for (int i = 0; i < 9 && maps_ok; ++i)
+        maps_ok = wide_encode_wmap(&h->wmap_layer[l][i], ms[i]->w, MK[i][0], MK[i][1], fmt);
+    }
   }
   if (!maps_ok) {
     delete h;
@@ -257,7 +315,8 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->act_o), 2 * N * h->qd * esz},
       {reinterpret_cast<void**>(&h->act_h), 2 * N * h->F * esz},
       {reinterpret_cast<void**>(&h->act_fin), 2 * N * h->H * 2},
-      {reinterpret_cast<void**>(&h->topk_keys), N * h->lm_ctas * 16 * 8},
+      {reinterpret_cast<void**>(&h->topk_keys), N * std::max(h->lm_ctas, h->wide ? h->lm_chunks : 0) * 16 * 8},
+      {reinterpret_cast<void**>(&h->lm_part), static_cast<size_t>(maxp_lm) * N * h->V * 4},
       {reinterpret_cast<void**>(&h->vstats),
        static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
       {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
@@ -349,6 +408,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   const int H = h->H, G = h->G;
   const size_t layer_stride = static_cast<size_t>(h->max_req) * h->kv_cap * h->kvd;  // elements
   const int N8 = 8 * h->max_req;  // rows of one plane of each activation buffer
+  // more than four requests: every projection on the tensor-core GEMM
+  const bool wide = R > 4;
+  const dflash2_handle::PlaneSet& P = wide ? h->pw : h->pn;
   // ---- a2: block embedding, first norm input, taps packing
   {
     StartArgs a;
@@ -387,7 +449,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.H = H;
     a.nch = h->nch_ss;
     a.fmt = fmt;
-    a.pl = l == 0 ? h->pl_d0 : h->pl_d;
+    a.pl = l == 0 ? P.d0 : P.d;
     a.n_rows = N;
     a.eps = c.rms_eps;
     return a;
@@ -397,9 +459,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // so do the hidden_norm input of the context rows and the first conv-in.
   {
     dflash2_status s =
-        run_gemv(h,
-                 {seg(h->map_fc, h->w.fc, h->xm_taps, N8, R, H, h->KT, h->fc_out),
-                  seg(h->map_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, N8, R, 4 * G, H,
+        run_gemv(h, wide,
+                 {seg(h->map_fc, h->wmap_fc, h->w.fc, h->xm_taps, h->act_taps, N8, R, H, h->KT, h->fc_out),
+                  seg(h->map_layer[0][kAttnDelta], h->wmap_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, h->act_a, N8, R, 4 * G, H,
                       h->dproj)},
                  st);
     if (s) return s;
@@ -413,7 +475,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.act_row0 = N;
     a.nch = h->nch_ss;
     a.fmt = fmt;
-    a.pl = h->pl_fc;
+    a.pl = P.fc;
     a.n_rows = N;
     DF2_CHECK(launch_fc_finish_conv_in(a, conv_in_attn(0), R, pdl, st));
     h->launches++;
@@ -425,17 +487,17 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     dflash2_status s = DFLASH2_OK;
     if (l > 0) {
       // ---- a3: delta projection of the normed input, conv-in
-      s = run_gemv(h, {seg(h->map_layer[l][kAttnDelta], L.attn_delta, h->xm_a, N8, R, 4 * G, H, h->dproj)},
+      s = run_gemv(h, wide, {seg(h->map_layer[l][kAttnDelta], h->wmap_layer[l][kAttnDelta], L.attn_delta, h->xm_a, h->act_a, N8, R, 4 * G, H, h->dproj)},
                    st);
       if (s) return s;
       DF2_CHECK(launch_conv_in(conv_in_attn(l), R, pdl, st));
       h->launches++;
     }
     // ---- a4: q (block rows), k and v (block + new context rows)
-    s = run_gemv(h,
-                 {seg(h->map_layer[l][kQ], L.q, h->xm_qkv, 2 * N8, R, h->qd, H, h->q_out),
-                  seg(h->map_layer[l][kK], L.k, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->k_out),
-                  seg(h->map_layer[l][kV], L.v, h->xm_qkv, 2 * N8, 2 * R, h->kvd, H, h->v_out)},
+    s = run_gemv(h, wide,
+                 {seg(h->map_layer[l][kQ], h->wmap_layer[l][kQ], L.q, h->xm_qkv, h->act_qkv, 2 * N8, R, h->qd, H, h->q_out),
+                  seg(h->map_layer[l][kK], h->wmap_layer[l][kK], L.k, h->xm_qkv, h->act_qkv, 2 * N8, 2 * R, h->kvd, H, h->k_out),
+                  seg(h->map_layer[l][kV], h->wmap_layer[l][kV], L.v, h->xm_qkv, h->act_qkv, 2 * N8, 2 * R, h->kvd, H, h->v_out)},
                  st);
     if (s) return s;
     {
@@ -460,9 +522,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.kv_capacity = h->kv_cap;
       a.H = H;
       a.nch = h->nch_ss;
-      a.pq = h->pl_q;
-      a.pk = h->pl_k;
-      a.pv = h->pl_v;
+      a.pq = P.q;
+      a.pk = P.k;
+      a.pv = P.v;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_qkv_finish(a, R, pdl, st));
       h->launches++;
@@ -490,7 +552,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       h->launches += 2;
     }
     // ---- a6: output projection, conv-out + residual, post-attention norm input
-    s = run_gemv(h, {seg(h->map_layer[l][kO], L.o, h->xm_o, N8, R, H, h->qd, h->ypart)}, st);
+    s = run_gemv(h, wide, {seg(h->map_layer[l][kO], h->wmap_layer[l][kO], L.o, h->xm_o, h->act_o, N8, R, H, h->qd, h->ypart)}, st);
     if (s) return s;
     {
       ConvOutArgs a;
@@ -507,13 +569,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
-      a.pl = h->pl_o;
+      a.pl = P.o;
       a.n_rows = N;
       DF2_CHECK(launch_conv_out(a, R, pdl, st));
       h->launches++;
     }
     // ---- a7: MLP sublayer
-    s = run_gemv(h, {seg(h->map_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, N8, R, 4 * G, H, h->dproj)}, st);
+    s = run_gemv(h, wide, {seg(h->map_layer[l][kMlpDelta], h->wmap_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, h->act_a, N8, R, 4 * G, H, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a;
@@ -528,15 +590,15 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
-      a.pl = h->pl_d;
+      a.pl = P.d;
       a.n_rows = N;
       a.eps = c.rms_eps;
       DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
-    s = run_gemv(h,
-                 {seg(h->map_layer[l][kGate], L.gate, h->xm_qkv, 2 * N8, R, h->F, H, h->gpart),
-                  seg(h->map_layer[l][kUp], L.up, h->xm_qkv, 2 * N8, R, h->F, H, h->upart)},
+    s = run_gemv(h, wide,
+                 {seg(h->map_layer[l][kGate], h->wmap_layer[l][kGate], L.gate, h->xm_qkv, h->act_qkv, 2 * N8, R, h->F, H, h->gpart),
+                  seg(h->map_layer[l][kUp], h->wmap_layer[l][kUp], L.up, h->xm_qkv, h->act_qkv, 2 * N8, R, h->F, H, h->upart)},
                  st);
     if (s) return s;
     {
@@ -547,13 +609,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.act_lo = h->lo_h;
       a.F = h->F;
       a.fmt = fmt;
-      a.pg = h->pl_g;
-      a.pu = h->pl_u;
+      a.pg = P.g;
+      a.pu = P.u;
       a.n_rows = N;
       DF2_CHECK(launch_swiglu(a, R, pdl, st));
       h->launches++;
     }
-    s = run_gemv(h, {seg(h->map_layer[l][kDown], L.down, h->xm_h, N8, R, H, h->F, h->ypart)}, st);
+    s = run_gemv(h, wide, {seg(h->map_layer[l][kDown], h->wmap_layer[l][kDown], L.down, h->xm_h, h->act_h, N8, R, H, h->F, h->ypart)}, st);
     if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
@@ -572,14 +634,16 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
-      a.pl = h->pl_down;
+      a.pl = P.down;
       a.n_rows = N;
       DF2_CHECK(launch_conv_out(a, R, pdl, st));
       h->launches++;
     }
   }
   // ---- a8: LM head + top-16
-  {
+  // external records: inside a stream capture they become event-record nodes the host can time
+  if (h->ev_lm0) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm0, st, cudaEventRecordExternal));
+  if (!wide) {
     LmHeadArgs a;
     a.wmap = h->map_lm;
     a.xmap = h->xm_lm;
@@ -594,16 +658,37 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.n_cta = h->lm_ctas;
     a.eps = c.rms_eps;
     a.err = h->gemv_err;
-    // external records: inside a stream capture they become event-record nodes the host can time
-    if (h->ev_lm0) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm0, st, cudaEventRecordExternal));
     DF2_CHECK(launch_lmhead(a, pdl, st));
-    if (h->ev_lm1) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm1, st, cudaEventRecordExternal));
+    h->launches++;
+  } else {
+    // logits of every block row as partial planes (tensor-core GEMM, bf16 hidden state),
+    // then the top-16 of each vocabulary chunk of each sampled row
+    dflash2_status s = run_gemv(
+        h, true, {seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm, h->act_fin,
+                      N8, R, h->V, H, h->lm_part)},
+        st, 0);
+    if (s) return s;
+    LogitsTopkArgs a;
+    a.part = h->lm_part;
+    a.ss = h->ss;
+    a.logits_out = logits_out;
+    a.part_keys = h->topk_keys;
+    a.V = h->V;
+    a.H = H;
+    a.n_rows = N;
+    a.nch = h->nch_ss;
+    a.n_chunks = h->lm_chunks;
+    a.eps = c.rms_eps;
+    a.pl = P.lm;
+    DF2_CHECK(launch_logits_topk(a, R, pdl, st));
     h->launches++;
   }
+  if (h->ev_lm1) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm1, st, cudaEventRecordExternal));
   // ---- a9: selector projection (same final hidden, in the matrix's format), merge top-16
   {
     const CUtensorMap& xin = fmt == 0 ? h->xm_fin : h->xm_a;  // same final hidden, in the matrix's format
-    dflash2_status s = run_gemv(h, {seg(h->map_sel, h->w.sel_proj, xin, N8, R, c.rank, H, h->sel_out)}, st);
+    const void* xin_p = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
+    dflash2_status s = run_gemv(h, wide, {seg(h->map_sel, h->wmap_sel, h->w.sel_proj, xin, xin_p, N8, R, c.rank, H, h->sel_out)}, st);
     if (s) return s;
     TopkMergeArgs a;
     a.part_keys = h->topk_keys;
@@ -613,10 +698,10 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.cand_logits = cand_logits;
     a.gate = gate;
     a.n_rows = N;
-    a.n_cta = h->lm_ctas;
+    a.n_cta = wide ? h->lm_chunks : h->lm_ctas;
     a.rank = c.rank;
     a.nch = h->nch_ss;
-    a.psel = h->pl_sel;
+    a.psel = P.sel;
     a.H = H;
     a.eps = c.rms_eps;
     DF2_CHECK(launch_topk_merge(a, pdl, st));
@@ -630,6 +715,40 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   if (!h || n_rows < 8 || n_rows % 8 || n_rows > 8 * h->max_req) return DFLASH2_E_INVAL;
   if (!hidden || !cand_ids || !cand_logits || !aligned16(hidden)) return DFLASH2_E_INVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n_rows > 32) {  // more rows than the LM-head kernel holds: tensor-core GEMM, chunked top-16
+    if (!h->wide) return DFLASH2_E_UNSUPPORTED;
+    dflash2_status s = run_gemv(h, true,
+                                {seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm,
+                                     hidden, n_rows, n_rows / 8, h->V, h->H, h->lm_part)},
+                                st, 0);
+    if (s) return s;
+    LogitsTopkArgs a;
+    a.part = h->lm_part;
+    a.ss = nullptr;
+    a.logits_out = logits_out;
+    a.part_keys = h->topk_keys;
+    a.V = h->V;
+    a.H = h->H;
+    a.n_rows = n_rows;
+    a.nch = h->nch_ss;
+    a.n_chunks = h->lm_chunks;
+    a.eps = h->cfg.rms_eps;
+    a.pl = h->pw.lm;
+    DF2_CHECK(launch_logits_topk(a, n_rows / 8, h->pdl, st));
+    TopkMergeArgs m = {};
+    m.part_keys = h->topk_keys;
+    m.cand_ids = cand_ids;
+    m.cand_logits = cand_logits;
+    m.n_rows = n_rows;
+    m.n_cta = h->lm_chunks;
+    m.rank = h->cfg.rank;
+    m.nch = h->nch_ss;
+    m.H = h->H;
+    m.eps = h->cfg.rms_eps;
+    DF2_CHECK(launch_topk_merge(m, h->pdl, st));
+    h->launches += 2;
+    return DFLASH2_OK;
+  }
   LmHeadArgs a;
   a.wmap = h->map_lm;
   if (!lm_encode_map(&a.xmap, hidden, h->H, n_rows, 8)) return DFLASH2_E_CUDA;

@@ -418,6 +418,11 @@ cudaError_t launch_nt(const GemvArgs& a, int ctas, bool pdl, cudaStream_t st) {
 
 }  // namespace
 
+bool tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* p, int inner, int rows,
+                   int box_inner, int box_rows, CUtensorMapSwizzle swz) {
+  return encode_2d(map, dt, esz, p, inner, rows, box_inner, box_rows, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 bool gemv_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt) {
   if (M % kBlockRows || K % kStageK) return false;
   if (fmt == 0)
@@ -461,6 +466,7 @@ GemvPlanes gemv_planes(const GemvArgs& a, int i, int C) {
   p.base = a.seg[i].stage_begin;
   p.C = C;
   p.kst = a.seg[i].K / a.stage_k;
+  p.bshift = 6;
   return p;
 }
 

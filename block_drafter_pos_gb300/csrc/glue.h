@@ -141,6 +141,23 @@ bool lm_encode_map(CUtensorMap* map, const void* p, int inner, int rows, int box
 int lmhead_ctas(int num_sms);
 cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st);
 
+// Top-16 of the LM head's logits when they come from the tensor-core GEMM as partial
+// planes: grid (n_chunks, 7 R), one non-anchor row x kLogitChunk vocabulary entries
+// per CTA; writes that chunk's 16 largest keys to part_keys[n][chunk] (the layout of
+// the LM-head kernel's per-CTA lists, so the same merge follows) and, if asked, the
+// logits.
+constexpr int kLogitChunk = 4096;
+struct LogitsTopkArgs {
+  const float* part;       // [p][N][V] partial planes of W_lm h (h not yet scaled by 1/rms)
+  const float* ss;         // [N][nch] sums of squares of the final hidden state
+  float* logits_out;       // [R][7][V] or null
+  unsigned long long* part_keys;  // [N][n_chunks][16]
+  int V, H, n_rows, nch, n_chunks;
+  float eps;
+  GemvPlanes pl;           // planes of part
+};
+cudaError_t launch_logits_topk(const LogitsTopkArgs& a, int n_req, bool pdl, cudaStream_t st);
+
 struct TopkMergeArgs {
   const unsigned long long* part_keys;  // [N][n_cta][16]
   const float* sel;        // selector projection partial planes [p][N][rank], or null

@@ -49,7 +49,8 @@ struct GemvArgs {
 // 0 .. count(m) - 1, with count from the block's first and last stage.
 struct GemvPlanes {
   long long T, base;  // launch stages; the segment's first stage
-  int C, kst;         // launch CTAs; stages per 64-row block
+  int C, kst;         // launch CTAs; stages per weight block
+  int bshift;         // log2 of the rows of one weight block (64 for the GEMV, 128 for the GEMM)
 };
 
 DF2_HD inline int gemv_cta_of_stage(long long t, int C, long long T) {
@@ -57,7 +58,7 @@ DF2_HD inline int gemv_cta_of_stage(long long t, int C, long long T) {
 }
 
 DF2_HD inline int gemv_plane_count(const GemvPlanes& p, int m) {
-  const long long b0 = p.base + static_cast<long long>(m >> 6) * p.kst;
+  const long long b0 = p.base + static_cast<long long>(m >> p.bshift) * p.kst;
   return gemv_cta_of_stage(b0 + p.kst - 1, p.C, p.T) - gemv_cta_of_stage(b0, p.C, p.T) + 1;
 }
 
@@ -75,6 +76,25 @@ bool gemv_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt);
 // Encodes the tensor map of an activation buffer of `rows` rows of width K per
 // plane, hi plane then lo plane (bf16 when fmt == 0, fp16 when fmt == 1).
 bool gemv_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt);
+
+// Two-dimensional bulk-copy descriptor of a row-major [rows][inner] array of esz-byte
+// elements, boxes of box_rows x box_inner; rows past the end read as zero.
+bool tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* p, int inner, int rows,
+                   int box_inner, int box_rows, CUtensorMapSwizzle swz);
+
+// ---------------------------------------------------------------- tensor-core GEMM
+// The same segments, stage order, stream-K split and partial planes as the GEMV,
+// for calls with many activation rows (8 * n_tiles <= 256): weight blocks of 128
+// rows, stages of 64 K, activations one plane (the high plane of the buffers).
+// Fills stage_begin, total_stages and stage_k; returns the CTA count (one per SM).
+int wide_plan(GemvArgs& a, int num_sms);
+GemvPlanes wide_planes(const GemvArgs& a, int i, int C);
+int wide_max_planes(const GemvArgs& a, int i, int C);
+// Weight map: bf16 boxes 64 K x 128 rows (128-byte swizzle) or int8 boxes 64 x 128 (64-byte swizzle).
+bool wide_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt);
+// Activation map of `rows` rows of width K: boxes 64 K x round_up(rows, 16) rows (128-byte swizzle).
+bool wide_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt);
+cudaError_t launch_wide(GemvArgs& a, int fmt, int num_sms, bool pdl, cudaStream_t st);
 
 // fmt: 0 = BF16 weights, 1 = Q8G64 weights.  max_tiles: largest n_tiles over segments.
 // pdl: launch with programmatic stream serialisation.

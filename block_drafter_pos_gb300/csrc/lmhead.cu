@@ -287,6 +287,83 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   }
 }
 
+// grid (n_chunks, 7 R), 256 threads, 16 consecutive vocabulary entries per thread.
+__global__ void __launch_bounds__(256) logits_topk_kernel(const LogitsTopkArgs a) {
+  __shared__ unsigned long long wtop[8][kTopK];
+  __shared__ float rs_sh;
+  pdl_begin();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int rq = blockIdx.y / 7, pos = blockIdx.y % 7 + 1, n = rq * 8 + pos;
+  if (wid == 0) {
+    const float v = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
+    if (lane == 0) rs_sh = v;
+  }
+  __syncthreads();
+  const float rs = rs_sh;
+  const int v0 = blockIdx.x * kLogitChunk + threadIdx.x * 16;
+  unsigned long long keys[16];
+  if (v0 < a.V) {  // V is a multiple of 16: the thread's 16 entries are all in range, in one weight block
+    const size_t plane = static_cast<size_t>(a.n_rows) * a.V;
+    const float* src = a.part + static_cast<size_t>(n) * a.V + v0;
+    const int np = gemv_plane_count(a.pl, v0);
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int p = 0; p < np; ++p) {  // planes in order
+      const float4* q = reinterpret_cast<const float4*>(src + static_cast<size_t>(p) * plane);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 t = __ldcs(q + j);
+        acc[4 * j] += t.x;
+        acc[4 * j + 1] += t.y;
+        acc[4 * j + 2] += t.z;
+        acc[4 * j + 3] += t.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      acc[j] *= rs;
+      keys[j] = topk_key(acc[j], static_cast<uint32_t>(v0 + j));
+    }
+    if (a.logits_out != nullptr) {
+      float4* o = reinterpret_cast<float4*>(a.logits_out + (static_cast<size_t>(rq) * 7 + pos - 1) * a.V + v0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) keys[j] = 0ull;
+  }
+  // keys are unique, so the keys still available in a round are those below the last winner
+  unsigned long long last = ~0ull, mine16 = 0ull;
+  for (int round = 0; round < kTopK; ++round) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (keys[j] < last && keys[j] > best) best = keys[j];
+    last = warp_max_u64(best);
+    if (lane == round) mine16 = last;
+  }
+  if (lane < kTopK) wtop[wid][lane] = mine16;
+  __syncthreads();
+  if (wid == 0) {
+    unsigned long long k4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k4[j] = (&wtop[0][0])[lane + 32 * j];
+    last = ~0ull;
+    unsigned long long out = 0ull;
+    for (int round = 0; round < kTopK; ++round) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (k4[j] < last && k4[j] > best) best = k4[j];
+      last = warp_max_u64(best);
+      if (lane == round) out = last;
+    }
+    if (lane < kTopK) a.part_keys[(static_cast<size_t>(n) * a.n_chunks + blockIdx.x) * kTopK + lane] = out;
+  }
+}
+
 template <int NT, bool LO>
 cudaError_t launch_nt(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
   constexpr int smem = StageGeo<0, NT>::kSmem;
@@ -316,6 +393,11 @@ cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st) {
   if (a.n_cta < 1 || a.n_cta * kTopK > 256 * 32) return cudaErrorInvalidValue;
   return launch_ex(topk_merge_kernel, dim3(a.n_rows), dim3(256), 0, st, pdl, a);
+}
+
+cudaError_t launch_logits_topk(const LogitsTopkArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  if (a.V % 16 || a.n_chunks < 1 || a.n_chunks * kTopK > 8192) return cudaErrorInvalidValue;
+  return launch_ex(logits_topk_kernel, dim3(a.n_chunks, 7 * n_req), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace df2

@@ -48,6 +48,8 @@ enum {
 enum { DFLASH2_WEIGHTS_BF16 = 0, DFLASH2_WEIGHTS_Q8G64 = 1 };
 
 #define DFLASH2_MAX_LAYERS 8
+/* Largest max_requests of dflash2_create (128 block rows per step). */
+#define DFLASH2_MAX_REQUESTS 16
 
 /* Drafter geometry ("LSE docs/DFLASH2.md", compatible-drafter paragraph). */
 typedef struct dflash2_config {
@@ -118,9 +120,13 @@ typedef struct dflash2_handle dflash2_handle;
  * positions per request in the caller's K/V caches.  Must be called with the
  * target device current.  Returns DFLASH2_E_UNSUPPORTED for a geometry the
  * kernels do not cover: head_dim != 128, block != 8, top_k != 16, rank != 256,
- * conv taps != 2 or group != 16, n_q_heads != 4 * n_kv_heads, hidden or ffn not
- * a multiple of 512, vocab not a multiple of 16, more than 8 layers or 4
- * requests, or a window over 64 attention chunks of 64 keys.  Every weight
+ * conv taps != 2 or group != 16, n_q_heads != 4 * n_kv_heads, hidden not a
+ * multiple of 256, ffn not a multiple of 128 (BF16) or 256 (Q8G64), vocab not a
+ * multiple of 16, more than DFLASH2_MAX_LAYERS layers or DFLASH2_MAX_REQUESTS
+ * requests, or a window over 64 attention chunks of 64 keys; and, when
+ * max_requests > 4 (the calls with more than four requests run every projection
+ * on the tensor-core GEMM, in 128-row weight blocks), hidden / 4 or vocab not a
+ * multiple of 128.  Every weight
  * matrix, Q8 scale and Q8 bias must start on a 16-byte boundary
  * (DFLASH2_E_INVAL otherwise).  Encodes one bulk-copy descriptor per projection
  * matrix, so the weights must not move while the handle lives. */
@@ -189,6 +195,9 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
  * positions 1..7 = W_lm . hidden (hidden already normalised, BF16), top-16 with the
  * ordering of dflash2_draft_block.  Row n of `hidden` is request n/8, block position
  * n%8 (position 0 is not projected).  n_rows: multiple of 8, <= 8*max_requests.
+ * Up to 32 rows run on the LM-head kernel; more rows (a handle created with
+ * max_requests > 4, else DFLASH2_E_UNSUPPORTED) on the tensor-core GEMM, with the
+ * logits in handle scratch, then a chunked top-16.
  *   hidden [n_rows][H] bf16; cand_ids, cand_logits [n_rows/8][block-1][top_k];
  *   logits_out [n_rows/8][block-1][V] float32 or NULL. */
 dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
@@ -200,7 +209,8 @@ int64_t dflash2_launch_count(const dflash2_handle* h);
 
 /* Profiling hook: when both events are non-NULL (cudaEvent_t passed as void*),
  * dflash2_draft_block records `start` right before and `stop` right after its
- * LM-head + top-16 kernel on the call's stream.  NULL, NULL turns it off. */
+ * LM-head + top-16 kernel (the GEMM and the chunked top-16 with more than four
+ * requests) on the call's stream.  NULL, NULL turns it off. */
 dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* stop);
 
 /* Algorithmic bytes the LM-head + top-16 kernel of one draft_block call streams
