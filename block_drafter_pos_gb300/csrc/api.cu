@@ -86,6 +86,7 @@ struct SegSpec {
   GemvSeg g;
   const CUtensorMap* wide_map;
   const void* x;
+  bool x_tiled;  // the GEMM path finds x in its operand layout (written so by this library's kernels)
 };
 
 SegSpec seg(const CUtensorMap& wmap, const CUtensorMap& wide_map, const dflash2_matrix& m, const CUtensorMap& xmap,
@@ -104,6 +105,7 @@ SegSpec seg(const CUtensorMap& wmap, const CUtensorMap& wide_map, const dflash2_
   s.out = out;
   r.wide_map = &wide_map;
   r.x = x;
+  r.x_tiled = true;
   return r;
 }
 
@@ -120,7 +122,12 @@ dflash2_status run_gemv(dflash2_handle* h, bool wide, std::initializer_list<SegS
     max_tiles = std::max(max_tiles, g.n_tiles);
     if (wide) {
       g.wmap = *s.wide_map;
-      if (!wide_encode_xmap(&g.xmap, s.x, 8 * g.n_tiles, g.K, fmt)) return DFLASH2_E_CUDA;
+      if (s.x_tiled) {
+        g.xt = s.x;
+        g.xt_rows = (g.x_lo_row + 15) & ~15;  // the rows of one plane, rounded up to 16: the rows of one slice
+      } else if (!wide_encode_xmap(&g.xmap, s.x, 8 * g.n_tiles, g.K, fmt)) {
+        return DFLASH2_E_CUDA;
+      }
     }
   }
   a.err = h->gemv_err;
@@ -227,11 +234,11 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
     for (int path = 0; path < (h->wide ? 2 : 1); ++path) {
       dflash2_handle::PlaneSet& P = path == 0 ? h->pn : h->pw;
       auto plan = [&](std::initializer_list<GemvSeg> segs, std::initializer_list<GemvPlanes*> pls,
-                      std::initializer_list<int*> maxes) {
+                      std::initializer_list<int*> maxes, int f) {
         GemvArgs a;
         memset(&a, 0, sizeof(a));
         for (const GemvSeg& g : segs) a.seg[a.nseg++] = g;
-        const int C = path == 0 ? gemv_plan(a, h->num_sms, fmt) : wide_plan(a, h->num_sms);
+        const int C = path == 0 ? gemv_plan(a, h->num_sms, fmt) : wide_plan(a, h->num_sms, f);
         int i = 0;
         for (GemvPlanes* p : pls) *p = path == 0 ? gemv_planes(a, i++, C) : wide_planes(a, i++, C);
         i = 0;
@@ -241,15 +248,15 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
           ++i;
         }
       };
-      plan({shape(h->H, h->KT), shape(4 * h->G, h->H)}, {&P.fc, &P.d0}, {&maxp_fc, &maxp_d});
-      plan({shape(4 * h->G, h->H)}, {&P.d}, {&maxp_d});
+      plan({shape(h->H, h->KT), shape(4 * h->G, h->H)}, {&P.fc, &P.d0}, {&maxp_fc, &maxp_d}, fmt);
+      plan({shape(4 * h->G, h->H)}, {&P.d}, {&maxp_d}, fmt);
       plan({shape(h->qd, h->H), shape(h->kvd, h->H), shape(h->kvd, h->H)}, {&P.q, &P.k, &P.v},
-           {&maxp_q, &maxp_k, &maxp_v});
-      plan({shape(h->H, h->qd)}, {&P.o}, {&maxp_y});
-      plan({shape(h->F, h->H), shape(h->F, h->H)}, {&P.g, &P.u}, {&maxp_g, &maxp_u});
-      plan({shape(h->H, h->F)}, {&P.down}, {&maxp_y});
-      plan({shape(c.rank, h->H)}, {&P.sel}, {&maxp_sel});
-      if (path == 1) plan({shape(h->V, h->H)}, {&P.lm}, {&maxp_lm});
+           {&maxp_q, &maxp_k, &maxp_v}, fmt);
+      plan({shape(h->H, h->qd)}, {&P.o}, {&maxp_y}, fmt);
+      plan({shape(h->F, h->H), shape(h->F, h->H)}, {&P.g, &P.u}, {&maxp_g, &maxp_u}, fmt);
+      plan({shape(h->H, h->F)}, {&P.down}, {&maxp_y}, fmt);
+      plan({shape(c.rank, h->H)}, {&P.sel}, {&maxp_sel}, fmt);
+      if (path == 1) plan({shape(h->V, h->H)}, {&P.lm}, {&maxp_lm}, 0);
     }
   }
   bool maps_ok = gemv_encode_wmap(&h->map_fc, w->fc.w, h->H, h->KT, fmt) &&
@@ -386,6 +393,11 @@ dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* s
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
   if (!h || n_req < 1) return -1;
   const int64_t N = 8 * static_cast<int64_t>(n_req);
+  if (n_req > 4)                                   // tensor-core GEMM + chunked top-16
+    return static_cast<int64_t>(h->V) * h->H * 2   // LM-head weights, read once
+           + N * h->H * 2                          // bf16 hidden state, one plane
+           + 2 * N * h->V * 4                      // logits written, then read by the top-16
+           + N * h->lm_chunks * 16 * 8;            // per-chunk top-16 keys written
   return static_cast<int64_t>(h->V) * h->H * 2  // LM-head weights, read once
          + 2 * N * h->H * 2                      // bf16 hidden state, hi and lo planes
          + N * h->lm_ctas * 16 * 8;              // per-CTA top-16 keys written
@@ -411,9 +423,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // more than four requests: every projection on the tensor-core GEMM
   const bool wide = R > 4;
   const dflash2_handle::PlaneSet& P = wide ? h->pw : h->pn;
+  // the tensor-core path reads its activations as one plane in the GEMM's operand
+  // layout, slices of 8 max_requests rows rounded up to 16 (16 max_requests for the
+  // QKV input): a slice holds every row the MMA reads (rows rounded up to 16)
+  const int tA = wide ? (N8 + 15) & ~15 : 0, tQ = wide ? 2 * N8 : 0;
   // ---- a2: block embedding, first norm input, taps packing
   {
-    StartArgs a;
+    StartArgs a = {};
     a.anchor_ids = anchor_ids;
     a.n_new = n_new;
     a.embed = static_cast<const uint16_t*>(h->w.embed);
@@ -421,10 +437,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.taps = taps;
     a.x = h->x;
     a.act_a = h->act_a;
-    a.act_a_lo = h->lo_a;
+    a.act_a_lo = wide ? 0 : h->lo_a;
+    a.tiled_a = tA;
     a.ss_x = h->ss;
     a.act_taps = h->act_taps;
-    a.act_taps_lo = h->lo_taps;
+    a.act_taps_lo = wide ? 0 : h->lo_taps;
+    a.tiled_taps = tA;
     a.H = H;
     a.n_taps = c.n_taps;
     a.mask_id = c.mask_token_id;
@@ -437,7 +455,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // conv before the attention sublayer of layer l (delta projection already in dproj)
   auto conv_in_attn = [&](int l) {
     const dflash2_layer_weights& L = h->w.layers[l];
-    ConvInArgs a;
+    ConvInArgs a = {};
     a.dproj = h->dproj;
     a.ss = h->ss;
     a.x = h->x;
@@ -445,7 +463,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.base = static_cast<const uint16_t*>(L.attn_base);
     a.delta = h->delta_a;
     a.act = h->act_qkv;
-    a.act_lo = h->lo_qkv;
+    a.act_lo = wide ? 0 : h->lo_qkv;
+    a.tiled = tQ;
     a.H = H;
     a.nch = h->nch_ss;
     a.fmt = fmt;
@@ -465,11 +484,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
                       h->dproj)},
                  st);
     if (s) return s;
-    FcFinishArgs a;
+    FcFinishArgs a = {};
     a.y = h->fc_out;
     a.norm_w = static_cast<const uint16_t*>(h->w.hidden_norm);
     a.act = h->act_qkv;
-    a.act_lo = h->lo_qkv;
+    a.act_lo = wide ? 0 : h->lo_qkv;
+    a.tiled = tQ;
     a.ss = h->ss_c;
     a.H = H;
     a.act_row0 = N;
@@ -501,7 +521,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
                  st);
     if (s) return s;
     {
-      QkvFinishArgs a;
+      QkvFinishArgs a = {};
       a.q_out = h->q_out;
       a.k_out = h->k_out;
       a.v_out = h->v_out;
@@ -531,7 +551,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     }
   // ---- a5: block attention over the window
     {
-      AttnArgs a;
+      AttnArgs a = {};
       a.q = h->q;
       a.kb = h->kb;
       a.vb = h->vb;
@@ -541,7 +561,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.n_new = n_new;
       a.part = h->attn_part;
       a.act_o = h->act_o;
-      a.act_o_lo = h->lo_o;
+      a.act_o_lo = wide ? 0 : h->lo_o;
+      a.tiled_o = tA;
       a.n_q_heads = h->nq;
       a.n_kv_heads = h->nkv;
       a.kv_capacity = h->kv_cap;
@@ -555,14 +576,15 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     s = run_gemv(h, wide, {seg(h->map_layer[l][kO], h->wmap_layer[l][kO], L.o, h->xm_o, h->act_o, N8, R, H, h->qd, h->ypart)}, st);
     if (s) return s;
     {
-      ConvOutArgs a;
+      ConvOutArgs a = {};
       a.part = h->ypart;
       a.delta = h->delta_a;
       a.base = static_cast<const uint16_t*>(L.attn_base);
       a.norm_w = static_cast<const uint16_t*>(L.post_norm);
       a.x = h->x;
       a.act = h->act_a;
-      a.act_lo = h->lo_a;
+      a.act_lo = wide ? 0 : h->lo_a;
+      a.tiled = tA;
       a.act2 = nullptr;
       a.act2_lo = 0;
       a.ss = h->ss;
@@ -578,7 +600,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     s = run_gemv(h, wide, {seg(h->map_layer[l][kMlpDelta], h->wmap_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, h->act_a, N8, R, 4 * G, H, h->dproj)}, st);
     if (s) return s;
     {
-      ConvInArgs a;
+      ConvInArgs a = {};
       a.dproj = h->dproj;
       a.ss = h->ss;
       a.x = h->x;
@@ -586,7 +608,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.base = static_cast<const uint16_t*>(L.mlp_base);
       a.delta = h->delta_m;
       a.act = h->act_qkv;
-      a.act_lo = h->lo_qkv;
+      a.act_lo = wide ? 0 : h->lo_qkv;
+      a.tiled = tQ;
       a.H = H;
       a.nch = h->nch_ss;
       a.fmt = fmt;
@@ -602,11 +625,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
                  st);
     if (s) return s;
     {
-      SwigluArgs a;
+      SwigluArgs a = {};
       a.part_g = h->gpart;
       a.part_u = h->upart;
       a.act = h->act_h;
-      a.act_lo = h->lo_h;
+      a.act_lo = wide ? 0 : h->lo_h;
+      a.tiled = tA;
       a.F = h->F;
       a.fmt = fmt;
       a.pg = P.g;
@@ -619,7 +643,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
-      ConvOutArgs a;
+      ConvOutArgs a = {};
       a.part = h->ypart;
       a.delta = h->delta_m;
       a.base = static_cast<const uint16_t*>(L.mlp_base);
@@ -627,9 +651,11 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.x = h->x;
       // LM-head input is bf16 in both formats; the next layer's input is in the matrices' format
       a.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
-      a.act_lo = (last && fmt == 0) ? h->lo_fin : h->lo_a;
+      a.act_lo = wide ? 0 : (last && fmt == 0) ? h->lo_fin : h->lo_a;
+      a.tiled = tA;
       a.act2 = (last && fmt != 0) ? h->act_fin : nullptr;
-      a.act2_lo = h->lo_fin;
+      a.act2_lo = wide ? 0 : h->lo_fin;
+      a.tiled2 = tA;
       a.ss = h->ss;
       a.H = H;
       a.nch = h->nch_ss;
@@ -644,7 +670,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // external records: inside a stream capture they become event-record nodes the host can time
   if (h->ev_lm0) DF2_CHECK(cudaEventRecordWithFlags(h->ev_lm0, st, cudaEventRecordExternal));
   if (!wide) {
-    LmHeadArgs a;
+    LmHeadArgs a = {};
     a.wmap = h->map_lm;
     a.xmap = h->xm_lm;
     a.x_lo_row = N8;
@@ -668,7 +694,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
                       N8, R, h->V, H, h->lm_part)},
         st, 0);
     if (s) return s;
-    LogitsTopkArgs a;
+    LogitsTopkArgs a = {};
     a.part = h->lm_part;
     a.ss = h->ss;
     a.logits_out = logits_out;
@@ -690,7 +716,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     const void* xin_p = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
     dflash2_status s = run_gemv(h, wide, {seg(h->map_sel, h->wmap_sel, h->w.sel_proj, xin, xin_p, N8, R, c.rank, H, h->sel_out)}, st);
     if (s) return s;
-    TopkMergeArgs a;
+    TopkMergeArgs a = {};
     a.part_keys = h->topk_keys;
     a.sel = h->sel_out;
     a.ss = h->ss;
@@ -717,12 +743,12 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (n_rows > 32) {  // more rows than the LM-head kernel holds: tensor-core GEMM, chunked top-16
     if (!h->wide) return DFLASH2_E_UNSUPPORTED;
-    dflash2_status s = run_gemv(h, true,
-                                {seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm,
-                                     hidden, n_rows, n_rows / 8, h->V, h->H, h->lm_part)},
-                                st, 0);
+    SegSpec sp = seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm, hidden, n_rows,
+                     n_rows / 8, h->V, h->H, h->lm_part);
+    sp.x_tiled = false;  // the caller's row-major hidden state: bulk tensor copies
+    dflash2_status s = run_gemv(h, true, {sp}, st, 0);
     if (s) return s;
-    LogitsTopkArgs a;
+    LogitsTopkArgs a = {};
     a.part = h->lm_part;
     a.ss = nullptr;
     a.logits_out = logits_out;
@@ -749,7 +775,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
     h->launches += 2;
     return DFLASH2_OK;
   }
-  LmHeadArgs a;
+  LmHeadArgs a = {};
   a.wmap = h->map_lm;
   if (!lm_encode_map(&a.xmap, hidden, h->H, n_rows, 8)) return DFLASH2_E_CUDA;
   a.x_lo_row = -1;
@@ -790,7 +816,7 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   if (!anchor_ids || !cand_ids || !cand_logits || !gate || !temperature || !seed || !philox_offset || !path ||
       !q_rows || !status)
     return DFLASH2_E_INVAL;
-  SelectArgs a;
+  SelectArgs a = {};
   a.anchor_ids = anchor_ids;
   a.cand_ids = cand_ids;
   a.cand_logits = cand_logits;
@@ -824,7 +850,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   if (!target_logits || !path || !cand_ids || !q_rows || !temperature || !seed || !philox_offset || !n_accepted ||
       !emitted || !n_emitted || !status)
     return DFLASH2_E_INVAL;
-  VerifyArgs a;
+  VerifyArgs a = {};
   a.logits = target_logits;
   a.path = path;
   a.cand_ids = cand_ids;

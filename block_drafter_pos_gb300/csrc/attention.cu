@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   }
   const int ld = a.n_q_heads * kHd;
   for (int j = 0; j < 4; ++j) {
-    const size_t idx = (static_cast<size_t>(r) * 8 + i) * ld + h * kHd + lane + 32 * j;
+    const size_t idx = act_offset(r * 8 + i, h * kHd + lane + 32 * j, ld, a.tiled_o);
     const float v = o[j] / den;
     if (a.fmt == 0) {
       __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);

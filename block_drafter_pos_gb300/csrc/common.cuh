@@ -55,6 +55,17 @@ DF2_DEV uint32_t codes_to_half2(uint32_t w_biased, uint32_t sel) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Element offset of activation (row, col) in a buffer of row width K: row-major when
+// T == 0; when T > 0 the tensor-core GEMM's operand layout, slices of 64 columns of
+// T rows each ([K/64][T][64]), the 16-byte pieces of a row placed under the
+// 128-byte swizzle (piece p of row r at p ^ (r mod 8)), so that one 64-column
+// slice of the first rows is one contiguous block, ready for a single bulk copy.
+DF2_DEV size_t act_offset(int row, int col, int K, int T) {
+  if (T == 0) return static_cast<size_t>(row) * K + col;
+  const int w = col & 63;
+  return (static_cast<size_t>(col >> 6) * T + row) * 64 + ((((w >> 3) ^ (row & 7)) << 3) | (w & 7));
+}
+
 // Programmatic dependent launch: wait until the previous kernel in the stream has
 // completed (its writes visible), and let the next kernel start being scheduled.
 // Both are no-ops for a kernel launched without the attribute.

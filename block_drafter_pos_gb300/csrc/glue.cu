@@ -79,13 +79,14 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
     const float xv = bf16_to_f32(a.embed[static_cast<size_t>(id) * a.H + c]);
     const size_t idx = static_cast<size_t>(row) * a.H + c;
     a.x[idx] = xv;
-    put_act(a.act_a, a.act_a_lo, a.fmt, idx, xv * bf16_to_f32(a.norm_w[c]));
+    put_act(a.act_a, a.act_a_lo, a.fmt, act_offset(row, c, a.H, a.tiled_a), xv * bf16_to_f32(a.norm_w[c]));
     emit_ss(xv, row, a.ss_x, a.nch);
   } else {
     const int c = (blockIdx.y - ny) * kCw + (threadIdx.x & 31);
     const int nn = min(max(a.n_new[r], 0), kB);  // rows >= n_new are zero
     const size_t idx = static_cast<size_t>(row) * (a.n_taps * a.H) + c;
-    put_act(a.act_taps, a.act_taps_lo, a.fmt, idx, (i < nn) ? a.taps[idx] : 0.f);
+    put_act(a.act_taps, a.act_taps_lo, a.fmt, act_offset(row, c, a.n_taps * a.H, a.tiled_taps),
+            (i < nn) ? a.taps[idx] : 0.f);
   }
   pdl_wait();
 }
@@ -98,7 +99,7 @@ DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
   const float y =
       plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, gemv_plane_count(a.pl, c));
-  put_act(a.act, a.act_lo, a.fmt, static_cast<size_t>(a.act_row0 + row) * a.H + c, y * bf16_to_f32(a.norm_w[c]));
+  put_act(a.act, a.act_lo, a.fmt, act_offset(a.act_row0 + row, c, a.H, a.tiled), y * bf16_to_f32(a.norm_w[c]));
   emit_ss(y, row, a.ss, a.nch);
 }
 
@@ -144,7 +145,7 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
   __syncthreads();
   const float prev = i > 0 ? ash[i - 1][lane] : 0.f;
   const float b0 = bf16_to_f32(a.base[c]), b1 = bf16_to_f32(a.base[a.H + c]);
-  put_act(a.act, a.act_lo, a.fmt, idx, (b0 + d0) * ai + (b1 + d1) * prev);
+  put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), (b0 + d0) * ai + (b1 + d1) * prev);
 }
 
 __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
@@ -184,8 +185,8 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
   const float xv = a.x[idx] + (b2 + d[2 * G + g]) * y + (b3 + d[3 * G + g]) * yprev;
   a.x[idx] = xv;
   const float w = bf16_to_f32(a.norm_w[c]);
-  put_act(a.act, a.act_lo, a.fmt, idx, xv * w);
-  if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, idx, xv * w);
+  put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), xv * w);
+  if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, act_offset(row, c, a.H, a.tiled2), xv * w);
   emit_ss(xv, row, a.ss, a.nch);
 }
 
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
   const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
   const float gs = plane_sum(a.part_g + idx, plane, gemv_plane_count(a.pg, c));
   const float us = plane_sum(a.part_u + idx, plane, gemv_plane_count(a.pu, c));
-  put_act(a.act, a.act_lo, a.fmt, idx, gs / (1.f + __expf(-gs)) * us);
+  put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.F, a.tiled), gs / (1.f + __expf(-gs)) * us);
 }
 
 // ------------------------------------------------------------------ q/k norm, RoPE, cache append

@@ -26,6 +26,7 @@ struct StartArgs {
   void* act_taps;          // [N][n_taps*H]
   size_t act_taps_lo;
   int H, n_taps, mask_id, nch, fmt, V;
+  int tiled_a, tiled_taps;  // > 0: tensor-core operand layout with that many rows per slice (act_offset)
 };
 
 struct FcFinishArgs {
@@ -36,6 +37,7 @@ struct FcFinishArgs {
   float* ss;               // [N][H/32] sums of squares of y
   int H, act_row0, nch, fmt, n_rows;
   GemvPlanes pl;           // planes of y
+  int tiled;               // > 0: act in the tensor-core operand layout (act_offset)
 };
 
 struct ConvInArgs {
@@ -50,6 +52,7 @@ struct ConvInArgs {
   int H, nch, fmt, n_rows;
   float eps;
   GemvPlanes pl;           // planes of dproj
+  int tiled;               // > 0: act in the tensor-core operand layout (act_offset)
 };
 
 // Dynamic convolution after a sublayer, residual add, next norm's input.
@@ -66,6 +69,7 @@ struct ConvOutArgs {
   float* ss;               // [N][H/32] sums of squares of the updated x
   int H, nch, fmt, n_rows;
   GemvPlanes pl;           // planes of part
+  int tiled, tiled2;       // > 0: act / act2 in the tensor-core operand layout (act_offset)
 };
 
 // SwiGLU of the gate and up projections: act = silu(gate) * up.
@@ -76,6 +80,7 @@ struct SwigluArgs {
   size_t act_lo;
   int F, fmt, n_rows;
   GemvPlanes pg, pu;       // planes of the two projections
+  int tiled;               // > 0: act in the tensor-core operand layout (act_offset)
 };
 
 struct QkvFinishArgs {
@@ -118,6 +123,7 @@ struct AttnArgs {
   void* act_o;             // [N][nq*128]
   size_t act_o_lo;
   int n_q_heads, n_kv_heads, kv_capacity, window, n_chunks, fmt;
+  int tiled_o;             // > 0: act_o in the tensor-core operand layout (act_offset)
 };
 constexpr int kAttnChunk = 64;
 cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st);

@@ -35,6 +35,8 @@ struct GemvSeg {
   int M, K, n_tiles;
   float* out;             // [planes][n_tiles * 8][M]
   long long stage_begin;  // first stage of this segment in the launch (set by gemv_plan)
+  const void* xt;         // tensor-core GEMM: X in its operand layout (slices of xt_rows rows), or null (xmap)
+  int xt_rows;
 };
 
 struct GemvArgs {
@@ -85,12 +87,13 @@ bool tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void
 // ---------------------------------------------------------------- tensor-core GEMM
 // The same segments, stage order, stream-K split and partial planes as the GEMV,
 // for calls with many activation rows (8 * n_tiles <= 256): weight blocks of 128
-// rows, stages of 64 K, activations one plane (the high plane of the buffers).
+// rows, stages of 64 K (bf16) or 128 K (int8), activations one 16-bit plane, read
+// from the operand layout the element-wise kernels write (xt) or through xmap.
 // Fills stage_begin, total_stages and stage_k; returns the CTA count (one per SM).
-int wide_plan(GemvArgs& a, int num_sms);
+int wide_plan(GemvArgs& a, int num_sms, int fmt);
 GemvPlanes wide_planes(const GemvArgs& a, int i, int C);
 int wide_max_planes(const GemvArgs& a, int i, int C);
-// Weight map: bf16 boxes 64 K x 128 rows (128-byte swizzle) or int8 boxes 64 x 128 (64-byte swizzle).
+// Weight map: bf16 boxes 64 K x 128 rows or int8 boxes 128 K x 128 rows (128-byte rows, 128-byte swizzle).
 bool wide_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt);
 // Activation map of `rows` rows of width K: boxes 64 K x round_up(rows, 16) rows (128-byte swizzle).
 bool wide_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt);

@@ -288,15 +288,28 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
 }
 
 // grid (n_chunks, 7 R), 256 threads, 16 consecutive vocabulary entries per thread.
+// The chunk's 16 largest keys are found without ranking all 4096: the 16th largest
+// of a warp's 32 per-thread maxima (a bitonic sort across the warp) is a lower
+// bound T of the chunk's 16th largest key (16 distinct entries reach it), so only
+// the entries >= the largest such T are candidates; one warp ranks those.  If the
+// candidates overflow the buffer (few distinct values, e.g. a chunk past the
+// vocabulary's end), every warp ranks its own entries and warp 0 merges.
 __global__ void __launch_bounds__(256) logits_topk_kernel(const LogitsTopkArgs a) {
+  constexpr int kCap = 1024;
+  __shared__ unsigned long long cand[kCap];
+  __shared__ unsigned long long wthr[8];
   __shared__ unsigned long long wtop[8][kTopK];
+  __shared__ int n_cand;
   __shared__ float rs_sh;
   pdl_begin();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int rq = blockIdx.y / 7, pos = blockIdx.y % 7 + 1, n = rq * 8 + pos;
   if (wid == 0) {
     const float v = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
-    if (lane == 0) rs_sh = v;
+    if (lane == 0) {
+      rs_sh = v;
+      n_cand = 0;
+    }
   }
   __syncthreads();
   const float rs = rs_sh;
@@ -311,13 +324,15 @@ __global__ void __launch_bounds__(256) logits_topk_kernel(const LogitsTopkArgs a
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
     for (int p = 0; p < np; ++p) {  // planes in order
       const float4* q = reinterpret_cast<const float4*>(src + static_cast<size_t>(p) * plane);
+      float4 t[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[j] = __ldcs(q + j);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 t = __ldcs(q + j);
-        acc[4 * j] += t.x;
-        acc[4 * j + 1] += t.y;
-        acc[4 * j + 2] += t.z;
-        acc[4 * j + 3] += t.w;
+        acc[4 * j] += t[j].x;
+        acc[4 * j + 1] += t[j].y;
+        acc[4 * j + 2] += t[j].z;
+        acc[4 * j + 3] += t[j].w;
       }
     }
 #pragma unroll
@@ -334,8 +349,50 @@ __global__ void __launch_bounds__(256) logits_topk_kernel(const LogitsTopkArgs a
 #pragma unroll
     for (int j = 0; j < 16; ++j) keys[j] = 0ull;
   }
+  // the warp's per-thread maxima sorted in decreasing order (bitonic network); lane 15 holds the 16th
+  unsigned long long v = 0ull;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v = keys[j] > v ? keys[j] : v;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  }
+  if (lane == 15) wthr[wid] = v;
+  __syncthreads();
+  unsigned long long T = wthr[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) T = wthr[w] > T ? wthr[w] : T;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (keys[j] >= T) {
+      const int p = atomicAdd(&n_cand, 1);
+      if (p < kCap) cand[p] = keys[j];
+    }
+  __syncthreads();
+  const int nc = n_cand;
+  unsigned long long last = ~0ull;
+  if (nc <= kCap) {
+    if (wid != 0) return;
+    unsigned long long out = 0ull;
+    for (int round = 0; round < kTopK; ++round) {
+      unsigned long long best = 0ull;
+      for (int i = lane; i < nc; i += 32) {
+        const unsigned long long c = cand[i];
+        if (c < last && c > best) best = c;
+      }
+      last = warp_max_u64(best);
+      if (lane == round) out = last;
+    }
+    if (lane < kTopK) a.part_keys[(static_cast<size_t>(n) * a.n_chunks + blockIdx.x) * kTopK + lane] = out;
+    return;
+  }
   // keys are unique, so the keys still available in a round are those below the last winner
-  unsigned long long last = ~0ull, mine16 = 0ull;
+  unsigned long long mine16 = 0ull;
   for (int round = 0; round < kTopK; ++round) {
     unsigned long long best = 0ull;
 #pragma unroll

@@ -8,9 +8,11 @@
 //    launch's segments are split into contiguous runs, one per CTA (one CTA per SM,
 //    stream-K), and a block shared by several CTAs gets one partial plane per CTA
 //    (plane = CTA - first CTA of the block), which the next kernel adds in order.
-//  * One CTA per SM with warp roles: warp 0 issues the bulk tensor copies of a stage
-//    (the weight tile and the activation tile, 128-byte swizzle, completing on the
-//    stage's "full" mbarrier); one thread of warp 1 issues tcgen05.mma (M = 128
+//  * One CTA per SM with warp roles: warp 0 issues the bulk tensor copies of the
+//    weight tiles into a deep ring (they come from HBM and never depend on the
+//    previous kernel), warp 2 those of the activation tiles into a shallow one (they
+//    stay in L2), each completing on its stage's "full" mbarrier (128-byte swizzle);
+//    one thread of warp 1 issues tcgen05.mma (M = 128
 //    weight rows, N = the activation rows rounded up to 16, K = 16 per instruction,
 //    both operands from shared memory through matrix descriptors) into an fp32
 //    accumulator in tensor memory, and tcgen05.commit releases the stage; warps 4..7
@@ -20,9 +22,11 @@
 //    overlaps the products of the next.
 //  * Q8/group64 weights ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias
 //    per group of 64 along K): the copy brings the int8 codes (64-byte swizzle), and
-//    warps 8..11 turn them into fp16 values in the operand layout (one weight row per
-//    thread: byte permute against the 1024 exponent, w = q * s + b in fp16), then
-//    hand the stage to the MMA thread through a second mbarrier after a proxy fence.
+//    warps 8..15 turn them into fp16 values in a ring of operand tiles (one weight
+//    row and half the stage's K per thread: byte permute against the 1024 exponent,
+//    w = q * s + b in fp16), release the code slot as soon as the codes are in
+//    registers, and hand the operand tile to the MMA thread through its mbarrier
+//    after a proxy fence.
 //    One stage is exactly one quantisation group along K.
 //  * The activations are read as one 16-bit plane (bf16 for bf16 weights, fp16 for
 //    Q8), the high plane of the buffers the element-wise kernels write.
@@ -51,23 +55,46 @@ using pipe::smem_u32;
 using pipe::tma_load_2d;
 
 constexpr int kTM = 128;         // weight rows per block: the MMA's M
-constexpr int kTK = 64;          // K per stage: one 128-byte swizzle atom of 16-bit values
+constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of 16-bit values
 constexpr int kMaxN = 256;       // activation rows per product: the MMA's largest N
-constexpr int kTmemCols = 512;   // two accumulators of up to 256 fp32 columns
-constexpr int kRingBytes = 200 * 1024;
 
-// Shared-memory stage: A tile [128 rows][64 K] 16-bit (the weights, or their fp16
-// values for Q8), B tile [up to 256 rows][64 K] 16-bit, and for Q8 the int8 codes
-// [128 rows][64].  Every region starts on a 1 KB boundary (the swizzle atoms).
+// K per stage: one bf16 weight copy of 128-byte rows (64 K), or one int8 copy of
+// 128-byte rows (128 K: two atoms of fp16 operand).
 template <int FMT>
+constexpr int stage_k() { return FMT == 0 ? 64 : 128; }
+// CTAs per SM: bf16 runs two independent pipelines per SM (each with half the
+// tensor memory); int8 one, whose sixteen converter warps fill the register file.
+constexpr int ctas_per_sm(int fmt) { return fmt == 0 ? 2 : 1; }
+
+// Three rings of shared-memory stages, each region on a 1 KB boundary (the swizzle
+// atoms): the weight copies W [128 rows][128 bytes] (bf16: the A operand itself;
+// int8: codes), which come from HBM; for int8 the fp16 operand tiles A (two atoms
+// [128 rows][64 K]) the converter warps write; and the activation tiles B
+// (stage_k / 64 atoms [NMAX rows][64 K]), which come from L2.  The accumulators:
+// kBufs of NMAX fp32 columns in tensor memory (two, so the epilogue of one block
+// overlaps the products of the next, where the columns allow).
+template <int FMT, int NMAX>
 struct WideGeo {
-  static constexpr int kA = kTM * kTK * 2;
-  static constexpr int kB = kMaxN * kTK * 2;
-  static constexpr int kCodes = FMT == 1 ? kTM * kTK : 0;
-  static constexpr int kStage = kA + kB + kCodes;
-  static constexpr int kDepth = kRingBytes / kStage;
-  static constexpr int kSmem = kDepth * kStage + 1024;
-  static constexpr int kWarps = FMT == 1 ? 12 : 8;
+  static constexpr int kKS = stage_k<FMT>();
+  static constexpr int kAtoms = kKS / kAtomK;
+  static constexpr int kW = kTM * 128;
+  static constexpr int kA = FMT == 1 ? kTM * kKS * 2 : 0;
+  static constexpr int kBAtom = NMAX * kAtomK * 2;
+  static constexpr int kB = kAtoms * kBAtom;
+  static constexpr int kCtas = ctas_per_sm(FMT);
+  static constexpr int kTmemCols = 512 / kCtas;
+  static constexpr int kBufs = kTmemCols / NMAX >= 2 ? 2 : 1;
+  static constexpr int kDA = FMT == 1 ? 2 : 0;
+  static constexpr int kDB = FMT == 1 ? 2 : (NMAX == 128 ? 2 : 1);
+  static constexpr int kRing = (FMT == 0 ? 100 : NMAX == 256 ? 224 : 208) * 1024;
+  static constexpr int kDW = (kRing - kDB * kB - kDA * kA) / kW;
+  static constexpr int kOffA = kDW * kW;
+  static constexpr int kOffB = kOffA + kDA * kA;
+  static constexpr int kSmem = kOffB + kDB * kB + 1024;
+  static constexpr int kConvGroups = 2;  // int8: converter warp groups, taking alternate stages
+  static constexpr int kWarps = FMT == 1 ? 8 + 8 * kConvGroups : 8;
+  static_assert(kDW >= 2, "weight ring");
+  static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
 // Shared-memory matrix descriptor of a K-major tile of 128-byte rows under the
@@ -120,6 +147,7 @@ DF2_DEV void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t 
 }
 
 // Position in the launch's stage sequence: CTA c takes [c T / C, (c + 1) T / C).
+template <int KS>
 struct WCursor {
   long long t, t1;
   int seg, row0, kstage, kst, kabs;
@@ -133,11 +161,11 @@ struct WCursor {
     seg = 0;
     while (seg + 1 < a.nseg && t >= a.seg[seg + 1].stage_begin) ++seg;
     const GemvSeg& sg = a.seg[seg];
-    kst = sg.K / kTK;
+    kst = sg.K / KS;
     const long long local = t - sg.stage_begin;
     row0 = static_cast<int>(local / kst) * kTM;
     kstage = static_cast<int>(local % kst);
-    kabs = kstage * kTK;
+    kabs = kstage * KS;
   }
   DF2_DEV void next(const GemvArgs& a) {
     if (++t >= t1) {
@@ -145,7 +173,7 @@ struct WCursor {
       return;
     }
     if (++kstage < kst) {
-      kabs += kTK;
+      kabs += KS;
       return;
     }
     kstage = 0;
@@ -154,7 +182,7 @@ struct WCursor {
     if (row0 >= a.seg[seg].M) {
       ++seg;
       row0 = 0;
-      kst = a.seg[seg].K / kTK;
+      kst = a.seg[seg].K / KS;
     }
   }
   DF2_DEV bool opens(long long t_first) const { return kstage == 0 || t == t_first; }
@@ -166,41 +194,60 @@ struct WCursor {
 
 DF2_DEV int n_mma_of(const GemvSeg& sg) { return (sg.n_tiles * 8 + 15) & ~15; }
 
+// Bulk copy of `bytes` contiguous bytes into shared memory, completing on an mbarrier.
+DF2_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 DF2_DEV uint32_t dequant_pair(uint32_t codes_biased, uint32_t sel, __half2 s, __half2 b) {
   const uint32_t qh = codes_to_half2(codes_biased, sel);
   __half2 w = __hfma2(*reinterpret_cast<const __half2*>(&qh), s, b);
   return *reinterpret_cast<uint32_t*>(&w);
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(WideGeo<FMT>::kWarps * 32, 1) wide_kernel(const __grid_constant__ GemvArgs a) {
-  using Geo = WideGeo<FMT>;
-  constexpr int D = Geo::kDepth;
+template <int FMT, int NMAX>
+__global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, NMAX>::kCtas) wide_kernel(const __grid_constant__ GemvArgs a) {
+  using Geo = WideGeo<FMT, NMAX>;
+  using Cur = WCursor<Geo::kKS>;
+  constexpr int DW = Geo::kDW, DB = Geo::kDB, DA = Geo::kDA > 0 ? Geo::kDA : 1;
+  constexpr int kConv = 8;  // converter warps per group (int8)
+  constexpr int NB = Geo::kBufs;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[D], conv_bar[D], empty_bar[D], dfull_bar[2], dempty_bar[2], done_bar;
+  __shared__ __align__(8) uint64_t wfull_b[DW], wempty_b[DW], bfull_b[DB], bempty_b[DB], afull_b[DA], aempty_b[DA];
+  __shared__ __align__(8) uint64_t dfull_b[2], dempty_b[2], done_b;
   __shared__ uint32_t tmem_base_sh;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t full0 = smem_u32(&full_bar[0]), conv0 = smem_u32(&conv_bar[0]);
-  const uint32_t empty0 = smem_u32(&empty_bar[0]), dfull0 = smem_u32(&dfull_bar[0]);
-  const uint32_t dempty0 = smem_u32(&dempty_bar[0]), done = smem_u32(&done_bar);
+  const uint32_t wfull = smem_u32(&wfull_b[0]), wempty = smem_u32(&wempty_b[0]);
+  const uint32_t bfull = smem_u32(&bfull_b[0]), bempty = smem_u32(&bempty_b[0]);
+  const uint32_t afull = smem_u32(&afull_b[0]), aempty = smem_u32(&aempty_b[0]);
+  const uint32_t dfull = smem_u32(&dfull_b[0]), dempty = smem_u32(&dempty_b[0]), done = smem_u32(&done_b);
   if (threadIdx.x == 0) {
-#pragma unroll
-    for (int s = 0; s < D; ++s) {
-      mbar_init_count(full0 + 8 * s, 1);
-      mbar_init_count(conv0 + 8 * s, 4);
-      mbar_init_count(empty0 + 8 * s, 1);
+    for (int s = 0; s < DW; ++s) {
+      mbar_init_count(wfull + 8 * s, 1);
+      mbar_init_count(wempty + 8 * s, FMT == 0 ? 1 : kConv);  // released by the products / the converters
+    }
+    for (int s = 0; s < DB; ++s) {
+      mbar_init_count(bfull + 8 * s, 1);
+      mbar_init_count(bempty + 8 * s, 1);
+    }
+    for (int s = 0; s < DA; ++s) {
+      mbar_init_count(afull + 8 * s, kConv);
+      mbar_init_count(aempty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init_count(dfull0 + 8 * b, 1);
-      mbar_init_count(dempty0 + 8 * b, 4);
+      mbar_init_count(dfull + 8 * b, 1);
+      mbar_init_count(dempty + 8 * b, 4);
     }
     mbar_init_count(done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (wid == 1) {  // the whole warp allocates the accumulator columns (and frees them at the end)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
-                 "r"(kTmemCols)
+                 "r"(Geo::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -212,84 +259,108 @@ __global__ void __launch_bounds__(WideGeo<FMT>::kWarps * 32, 1) wide_kernel(cons
   bool ok = true;
 
   if (wid == 0) {
-    // ------------------------------------------------------------ copy producer (one lane)
+    // ------------------------------------------------------------ weight copies (one lane)
+    // The weights never depend on the previous kernel: no wait on it here.
     if (lane == 0) {
-      const uint64_t wpol = evict_first_policy();  // weights: streamed once
-      const uint64_t xpol = evict_last_policy();   // activations: read by every CTA
-      auto arm_w = [&](const WCursor& c, int slot) {
-        const GemvSeg& sg = a.seg[c.seg];
-        mbar_expect_tx(full0 + 8 * slot, (FMT == 0 ? Geo::kA : Geo::kCodes) + n_mma_of(sg) * kTK * 2);
-        const uint32_t dst = ring + slot * Geo::kStage + (FMT == 0 ? 0 : Geo::kA + Geo::kB);
-        tma_load_2d(dst, &sg.wmap, c.kabs, c.row0, full0 + 8 * slot, wpol);
-      };
-      WCursor cw;
-      cw.start(a);
-      int np = 0;
-      while (np < D && cw.valid) {  // weights of the first stages: before the wait on the previous kernel
-        arm_w(cw, np);
-        cw.next(a);
-        ++np;
-      }
-      pdl_wait();
-      WCursor cx;
-      cx.start(a);
-      int it = 0;
-      while (cx.valid) {
-        const int slot = it % D;
-        if (it >= np) {
-          if (!mbar_wait(empty0 + 8 * slot, static_cast<uint32_t>(((it / D) + 1) & 1))) {
-            ok = false;
-            break;
-          }
-          arm_w(cx, slot);
+      const uint64_t pol = evict_first_policy();  // streamed once
+      Cur c;
+      c.start(a);
+      int i = 0;
+      while (c.valid) {
+        const int s = i % DW;
+        if (i >= DW && !mbar_wait(wempty + 8 * s, static_cast<uint32_t>(((i / DW) + 1) & 1))) {
+          ok = false;
+          break;
         }
-        tma_load_2d(ring + slot * Geo::kStage + Geo::kA, &a.seg[cx.seg].xmap, cx.kabs, 0, full0 + 8 * slot, xpol);
-        cx.next(a);
-        ++it;
+        mbar_expect_tx(wfull + 8 * s, Geo::kW);
+        tma_load_2d(ring + s * Geo::kW, &a.seg[c.seg].wmap, c.kabs, c.row0, wfull + 8 * s, pol);
+        c.next(a);
+        ++i;
       }
-      // the copies of the last stages land before the shared memory is released (bounded)
-      for (int j = it > D ? it - D : 0; j < it; ++j) mbar_wait(full0 + 8 * (j % D), static_cast<uint32_t>((j / D) & 1));
+      // the last copies land before the shared memory is released (bounded)
+      for (int j = i > DW ? i - DW : 0; j < i; ++j) mbar_wait(wfull + 8 * (j % DW), static_cast<uint32_t>((j / DW) & 1));
+    }
+  } else if (wid == 2) {
+    // ------------------------------------------------------------ activation copies (one lane)
+    if (lane == 0) {
+      pdl_wait();  // the activations are the previous kernel's output
+      const uint64_t pol = evict_last_policy();  // read by every CTA
+      Cur c;
+      c.start(a);
+      int i = 0;
+      while (c.valid) {
+        const int s = i % DB;
+        if (i >= DB && !mbar_wait(bempty + 8 * s, static_cast<uint32_t>(((i / DB) + 1) & 1))) {
+          ok = false;
+          break;
+        }
+        const GemvSeg& sg = a.seg[c.seg];
+        const int nm = n_mma_of(sg);
+        mbar_expect_tx(bfull + 8 * s, Geo::kAtoms * nm * kAtomK * 2);
+        const uint32_t dst = ring + Geo::kOffB + s * Geo::kB;
+#pragma unroll
+        for (int j = 0; j < Geo::kAtoms; ++j) {
+          if (sg.xt != nullptr) {  // one contiguous block per 64-K slice: rows 0 .. nm - 1 of the slice
+            const char* src = static_cast<const char*>(sg.xt) +
+                              (static_cast<size_t>(c.kabs / kAtomK + j) * sg.xt_rows) * (kAtomK * 2);
+            bulk_load(dst + j * Geo::kBAtom, src, static_cast<uint32_t>(nm * kAtomK * 2), bfull + 8 * s, pol);
+          } else {
+            tma_load_2d(dst + j * Geo::kBAtom, &sg.xmap, c.kabs + j * kAtomK, 0, bfull + 8 * s, pol);
+          }
+        }
+        c.next(a);
+        ++i;
+      }
+      for (int j = i > DB ? i - DB : 0; j < i; ++j) mbar_wait(bfull + 8 * (j % DB), static_cast<uint32_t>((j / DB) & 1));
     }
   } else if (wid == 1) {
     // ------------------------------------------------------------ MMA issuer (one lane)
     if (lane == 0) {
-      WCursor c;
+      Cur c;
       c.start(a);
       const long long t_first = c.t;
-      int it = 0, tile = 0;
+      int i = 0, tile = 0;
       uint32_t d_tmem = tmem, idesc = 0;
       while (c.valid) {
-        const int slot = it % D;
-        const uint32_t par = static_cast<uint32_t>((it / D) & 1);
         const bool first = c.opens(t_first);
         if (first) {
-          const int buf = tile & 1;
-          // the epilogue has drained this accumulator (block tile - 2)
-          if (tile >= 2 && !mbar_wait(dempty0 + 8 * buf, static_cast<uint32_t>(((tile >> 1) + 1) & 1))) {
+          const int buf = tile % NB;
+          // the epilogue has drained this accumulator (block tile - NB)
+          if (tile >= NB && !mbar_wait(dempty + 8 * buf, static_cast<uint32_t>(((tile / NB) + 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          d_tmem = tmem + static_cast<uint32_t>(buf * 256);
+          d_tmem = tmem + static_cast<uint32_t>(buf * NMAX);
           idesc = instr_desc(FMT, n_mma_of(a.seg[c.seg]));
         }
-        if (!mbar_wait(full0 + 8 * slot, par) || (FMT == 1 && !mbar_wait(conv0 + 8 * slot, par))) {
+        const int sb = i % DB, sw = i % DW, sa = i % DA;
+        const bool in = mbar_wait(bfull + 8 * sb, static_cast<uint32_t>((i / DB) & 1)) &&
+                        (FMT == 0 ? mbar_wait(wfull + 8 * sw, static_cast<uint32_t>((i / DW) & 1))
+                                  : mbar_wait(afull + 8 * sa, static_cast<uint32_t>((i / DA) & 1)));
+        if (!in) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sa = ring + slot * Geo::kStage;
-        const uint64_t ad = sw128_desc(sa), bd = sw128_desc(sa + Geo::kA);
+        const uint32_t aaddr = FMT == 0 ? ring + sw * Geo::kW : ring + Geo::kOffA + sa * Geo::kA;
+        const uint32_t baddr = ring + Geo::kOffB + sb * Geo::kB;
 #pragma unroll
-        for (int k = 0; k < kTK / 16; ++k)  // 16 K = 32 bytes further along the swizzled rows
-          umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-        umma_commit(empty0 + 8 * slot);  // the stage is free once these products are done
+        for (int j = 0; j < Geo::kAtoms; ++j) {
+          const uint64_t ad = sw128_desc(aaddr + j * kTM * 128), bd = sw128_desc(baddr + j * Geo::kBAtom);
+#pragma unroll
+          for (int k = 0; k < kAtomK / 16; ++k)  // 16 K = 32 bytes further along the swizzled rows
+            umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (first && j == 0 && k == 0) ? 0u : 1u);
+        }
+        // the stages are free once these products are done
+        umma_commit(bempty + 8 * sb);
+        umma_commit(FMT == 0 ? wempty + 8 * sw : aempty + 8 * sa);
         if (c.closes()) {
-          umma_commit(dfull0 + 8 * (tile & 1));
+          umma_commit(dfull + 8 * (tile % NB));
           ++tile;
         }
         c.next(a);
-        ++it;
+        ++i;
       }
       // every product issued has completed before the columns are freed (bounded)
       umma_commit(done);
@@ -299,13 +370,13 @@ __global__ void __launch_bounds__(WideGeo<FMT>::kWarps * 32, 1) wide_kernel(cons
     // ------------------------------------------------------------ epilogue: accumulator -> partial plane
     pdl_wait();  // the planes are written only after the previous kernel has completed
     const int quarter = wid & 3;  // tensor-memory lanes 32 quarter .. 32 quarter + 31
-    WCursor c;
+    Cur c;
     c.start(a);
     int tile = 0;
     while (c.valid) {
       if (c.closes()) {
-        const int buf = tile & 1;
-        if (!mbar_wait(dfull0 + 8 * buf, static_cast<uint32_t>((tile >> 1) & 1))) {
+        const int buf = tile % NB;
+        if (!mbar_wait(dfull + 8 * buf, static_cast<uint32_t>((tile / NB) & 1))) {
           ok = false;
           break;
         }
@@ -314,7 +385,7 @@ __global__ void __launch_bounds__(WideGeo<FMT>::kWarps * 32, 1) wide_kernel(cons
         const int n_rows = sg.n_tiles * 8, nm = n_mma_of(sg);
         const int m = c.row0 + quarter * 32 + lane;
         float* out = sg.out + static_cast<size_t>(c.plane(a)) * n_rows * sg.M + m;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * 256);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * NMAX);
         for (int n0 = 0; n0 < nm; n0 += 16) {
           uint32_t r[16];
           tmem_ld16(taddr + n0, r);
@@ -324,60 +395,75 @@ __global__ void __launch_bounds__(WideGeo<FMT>::kWarps * 32, 1) wide_kernel(cons
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(dempty0 + 8 * buf);
+        if (lane == 0) mbar_arrive(dempty + 8 * buf);
         ++tile;
       }
       c.next(a);
     }
   } else if (FMT == 1 && wid >= 8) {
-    // ------------------------------------------------------------ int8 codes -> fp16 operand tile
-    const int r = (wid - 8) * 32 + lane;  // weight row within the block
-    WCursor c;
+    // ------------------------------------------------------------ int8 codes -> fp16 operand tiles
+    const int cw = wid - 8;
+    const int grp = cw >> 3;                    // this group converts the stages i with i mod 2 == grp
+    const int r = (cw & 3) * 32 + lane;         // weight row within the block
+    const int hk = (cw >> 2) & 1;               // 64-K half of the stage: one quantisation group, one atom
+    Cur c;
     c.start(a);
-    auto affine = [&](const WCursor& cc, uint16_t& s, uint16_t& b) {
+    if (grp == 1) c.next(a);
+    auto affine = [&](const Cur& cc, uint16_t& s, uint16_t& b) {
       const GemvSeg& sg = a.seg[cc.seg];
-      const size_t i = static_cast<size_t>(cc.row0 + r) * (sg.K >> 6) + (cc.kabs >> 6);
-      s = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + i);
-      b = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + i);
+      const size_t idx = static_cast<size_t>(cc.row0 + r) * (sg.K >> 6) + (cc.kabs >> 6) + hk;
+      s = __ldg(reinterpret_cast<const unsigned short*>(sg.scale) + idx);
+      b = __ldg(reinterpret_cast<const unsigned short*>(sg.bias) + idx);
     };
     uint16_t s_cur = 0, b_cur = 0;
     if (c.valid) affine(c, s_cur, b_cur);
-    int it = 0;
+    int i = grp;
     while (c.valid) {
-      const int slot = it % D;
-      WCursor cn = c;
+      const int sw = i % DW, sa = i % DA;
+      Cur cn = c;
       cn.next(a);
+      if (cn.valid) cn.next(a);
       uint16_t s_nx = s_cur, b_nx = b_cur;
       if (cn.valid) affine(cn, s_nx, b_nx);  // the next group's scale and bias, loaded during this stage
-      if (!mbar_wait(full0 + 8 * slot, static_cast<uint32_t>((it / D) & 1))) {
+      if (!mbar_wait(wfull + 8 * sw, static_cast<uint32_t>((i / DW) & 1))) {
         ok = false;
         break;
       }
-      const uint32_t st = ring + slot * Geo::kStage;
-      const uint32_t codes = st + Geo::kA + Geo::kB + r * 64;                    // 64-byte rows, 64-byte swizzle
-      const uint32_t arow = st + (r >> 3) * 1024 + (r & 7) * 128;               // 128-byte rows, 128-byte swizzle
+      // 128-byte code rows under the 128-byte swizzle: piece p (16 codes) of row r at p ^ (r mod 8)
+      const uint32_t crow = ring + sw * Geo::kW + r * 128;
+      uint4 w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = lds128(crow + (((4 * hk + j) ^ (r & 7)) << 4));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wempty + 8 * sw);  // the codes are in registers: the copy slot is free
+      if (i >= DA && !mbar_wait(aempty + 8 * sa, static_cast<uint32_t>(((i / DA) + 1) & 1))) {
+        ok = false;
+        break;
+      }
+      // atom hk of the operand tile: 128-byte rows, 128-byte swizzle
+      const uint32_t arow = ring + Geo::kOffA + sa * Geo::kA + hk * (kTM * 128) + (r >> 3) * 1024 + (r & 7) * 128;
       const __half2 sh = __float2half2_rn(bf16_to_f32(s_cur)), bh = __float2half2_rn(bf16_to_f32(b_cur));
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {  // codes 16 ch .. 16 ch + 15
-        const uint4 w = lds128(codes + ((ch ^ ((r >> 1) & 3)) << 4));
-        const uint32_t u[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-        uint32_t h[8];
+      for (int j = 0; j < 4; ++j) {  // codes 16 j .. 16 j + 15 of the group -> fp16 pieces 2 j, 2 j + 1
+        const uint32_t u[4] = {w[j].x ^ 0x80808080u, w[j].y ^ 0x80808080u, w[j].z ^ 0x80808080u,
+                               w[j].w ^ 0x80808080u};
+        uint32_t hv[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          h[2 * m] = dequant_pair(u[m], 0x4140, sh, bh);
-          h[2 * m + 1] = dequant_pair(u[m], 0x4342, sh, bh);
+          hv[2 * m] = dequant_pair(u[m], 0x4140, sh, bh);
+          hv[2 * m + 1] = dequant_pair(u[m], 0x4342, sh, bh);
         }
-        sts128(arow + (((2 * ch) ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
-        sts128(arow + (((2 * ch + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+        sts128(arow + (((2 * j) ^ (r & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
+        sts128(arow + (((2 * j + 1) ^ (r & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
       }
       // generic-proxy stores become visible to the tensor cores' reads before the hand-over
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(conv0 + 8 * slot);
+      if (lane == 0) mbar_arrive(afull + 8 * sa);
       s_cur = s_nx;
       b_cur = b_nx;
       c = cn;
-      ++it;
+      i += 2;
     }
   }
   if (!ok && a.err != nullptr) atomicExch(a.err, 1);
@@ -386,34 +472,36 @@ __global__ void __launch_bounds__(WideGeo<FMT>::kWarps * 32, 1) wide_kernel(cons
   __syncthreads();
   if (wid == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Geo::kTmemCols) : "memory");
   }
 }
 
-template <int FMT>
+template <int FMT, int NMAX>
 cudaError_t launch_fmt(const GemvArgs& a, int ctas, bool pdl, cudaStream_t st) {
-  constexpr int smem = WideGeo<FMT>::kSmem;
+  constexpr int smem = WideGeo<FMT, NMAX>::kSmem;
   static bool attr_set = false;  // set once, outside any later stream capture
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(wide_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(wide_kernel<FMT, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(wide_kernel<FMT>, dim3(ctas), dim3(WideGeo<FMT>::kWarps * 32), smem, st, pdl, a);
+  return launch_ex(wide_kernel<FMT, NMAX>, dim3(ctas), dim3(WideGeo<FMT, NMAX>::kWarps * 32), smem, st, pdl, a);
 }
+
+int ks_of(int fmt) { return fmt == 0 ? stage_k<0>() : stage_k<1>(); }
 
 }  // namespace
 
-int wide_plan(GemvArgs& a, int num_sms) {
-  a.stage_k = kTK;
+int wide_plan(GemvArgs& a, int num_sms, int fmt) {
+  a.stage_k = ks_of(fmt);
   long long T = 0;
   for (int i = 0; i < a.nseg; ++i) {
     GemvSeg& sg = a.seg[i];
     sg.stage_begin = T;
-    T += static_cast<long long>(sg.M / kTM) * (sg.K / kTK);
+    T += static_cast<long long>(sg.M / kTM) * (sg.K / a.stage_k);
   }
   a.total_stages = T;
-  const long long C = num_sms;
+  const long long C = static_cast<long long>(num_sms) * ctas_per_sm(fmt);
   return static_cast<int>(C < T ? C : (T > 0 ? T : 1));
 }
 
@@ -422,7 +510,7 @@ GemvPlanes wide_planes(const GemvArgs& a, int i, int C) {
   p.T = a.total_stages;
   p.base = a.seg[i].stage_begin;
   p.C = C;
-  p.kst = a.seg[i].K / kTK;
+  p.kst = a.seg[i].K / a.stage_k;
   p.bshift = 7;
   return p;
 }
@@ -438,28 +526,34 @@ int wide_max_planes(const GemvArgs& a, int i, int C) {
 }
 
 bool wide_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt) {
-  if (M % kTM || K % kTK) return false;
+  if (M % kTM || K % ks_of(fmt)) return false;
   if (fmt == 0)
-    return tma_encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, kTK, kTM, CU_TENSOR_MAP_SWIZZLE_128B);
-  return tma_encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, kTK, kTM, CU_TENSOR_MAP_SWIZZLE_64B);
+    return tma_encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B);
+  return tma_encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, 128, kTM, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool wide_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt) {
-  if (rows < 1 || rows > kMaxN || K % kTK) return false;
+  if (rows < 1 || rows > kMaxN || K % kAtomK) return false;
   const int nm = (rows + 15) & ~15;
   return tma_encode_2d(map, fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, K,
-                       rows, kTK, nm, CU_TENSOR_MAP_SWIZZLE_128B);
+                       rows, kAtomK, nm, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 cudaError_t launch_wide(GemvArgs& a, int fmt, int num_sms, bool pdl, cudaStream_t st) {
+  const int ks = ks_of(fmt);
+  int nmax = 0;
   for (int i = 0; i < a.nseg; ++i) {
     const GemvSeg& sg = a.seg[i];
-    if (sg.M % kTM || sg.K % kTK || sg.n_tiles < 1 || sg.n_tiles * 8 > kMaxN) return cudaErrorInvalidValue;
+    if (sg.M % kTM || sg.K % ks || sg.n_tiles < 1 || sg.n_tiles * 8 > kMaxN) return cudaErrorInvalidValue;
     if (fmt == 1 && (sg.scale == nullptr || sg.bias == nullptr)) return cudaErrorInvalidValue;
+    const int nm = (sg.n_tiles * 8 + 15) & ~15;
+    if (sg.xt != nullptr && (sg.xt_rows < nm || (reinterpret_cast<uintptr_t>(sg.xt) & 15u))) return cudaErrorInvalidValue;
+    nmax = nm > nmax ? nm : nmax;
   }
-  const int C = wide_plan(a, num_sms);
+  const int C = wide_plan(a, num_sms, fmt);
   if (a.total_stages < 1) return cudaErrorInvalidValue;
-  return fmt == 0 ? launch_fmt<0>(a, C, pdl, st) : launch_fmt<1>(a, C, pdl, st);
+  if (fmt == 0) return nmax <= 128 ? launch_fmt<0, 128>(a, C, pdl, st) : launch_fmt<0, 256>(a, C, pdl, st);
+  return nmax <= 128 ? launch_fmt<1, 128>(a, C, pdl, st) : launch_fmt<1, 256>(a, C, pdl, st);
 }
 
 }  // namespace df2

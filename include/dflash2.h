@@ -214,7 +214,9 @@ int64_t dflash2_launch_count(const dflash2_handle* h);
 dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* stop);
 
 /* Algorithmic bytes the LM-head + top-16 kernel of one draft_block call streams
- * (LM-head weights + activations + candidate outputs), for roofline reports. */
+ * (LM-head weights + activations + candidate outputs; with more than four
+ * requests also the logits the GEMM writes and the top-16 kernel reads), for
+ * roofline reports. */
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req);
 
 /* ---- LM head + top-16 without any device allocation ----
