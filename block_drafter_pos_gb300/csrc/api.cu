@@ -567,7 +567,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.n_kv_heads = h->nkv;
       a.kv_capacity = h->kv_cap;
       a.window = c.window;
-      a.n_chunks = h->n_attn_chunks;
+      // context chunks per part: one while the parts alone fill the GPU, four with more requests
+      a.cpc = R > 4 ? 4 : 1;
+      a.n_chunks = (h->n_attn_chunks - 1 + a.cpc - 1) / a.cpc + 1;
       a.fmt = fmt;
       DF2_CHECK(launch_attention(a, R, pdl, st));
       h->launches += 2;

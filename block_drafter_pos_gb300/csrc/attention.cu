@@ -36,6 +36,7 @@ struct CtxSmem {
   __nv_bfloat16 v[kKeys][kLd];
   float s[kQ][kKeys + 4];                  // scores (log2 units), then probabilities
   __nv_bfloat16 ph[kQ][kPLd], pl[kQ][kPLd];
+  float alpha[kQ];                         // rescale of the running output, per query
 };
 
 struct BlkSmem {
@@ -75,20 +76,27 @@ DF2_DEV KvRegs load_kv(const AttnArgs& a, int r, int kvh, int k_begin, int nk) {
   return x;
 }
 
-// early: the chunk's K/V were loaded before the wait on the previous kernel (no
-// newly appended row in the chunk); otherwise they are loaded after it.
-DF2_DEV void ctx_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, int k_begin, int nk, int L,
-                       bool early, float* out) {
+// Context chunks c0 .. c1 - 1 of one (request, KV head), 64 keys each, with a
+// running (online) softmax: per query the running maximum m and sum l, and the
+// unnormalised output O, rescaled by 2^(m_old - m_new) whenever the maximum
+// grows.  The next chunk's K/V loads are issued before the current chunk is
+// computed.  The first chunk's K/V are loaded before the wait on the previous
+// kernel when none of its rows is appended by it.  Writes the part's (m, l, O).
+DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, int lo0, int c0, int c1, int L,
+                      int nn, float* out) {
   CtxSmem& sm = *reinterpret_cast<CtxSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int rep = a.n_q_heads / a.n_kv_heads;
   const float qscale = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;  // log2(e)/sqrt(hd)
+  auto kbeg = [&](int c) { return lo0 + c * kKeys; };
+  auto nkeys = [&](int c) { return min(kKeys, L - kbeg(c)); };
   KvRegs kv;
-  if (early) kv = load_kv(a, r, kvh, k_begin, nk);
+  const bool early = kbeg(c0) + nkeys(c0) <= L - nn;  // rows L - nn .. L - 1 are appended by the previous kernel
+  if (early) kv = load_kv(a, r, kvh, kbeg(c0), nkeys(c0));
   pdl_wait();
   pdl_trigger();
-  if (!early) kv = load_kv(a, r, kvh, k_begin, nk);
+  if (!early) kv = load_kv(a, r, kvh, kbeg(c0), nkeys(c0));
   // queries -> bf16 hi/lo (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i); loads first
   float qv[kQ * kHd / 256];
 #pragma unroll
@@ -107,93 +115,126 @@ DF2_DEV void ctx_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kv
     sm.qh[qi][d] = h;
     sm.ql[qi][d] = __float2bfloat16_rn(v - __bfloat162float(h));
   }
+  float m_run[4], l_run[4];  // queries 4 wid .. 4 wid + 3 (the same in every lane of the warp)
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int e = tid + 256 * j;
-    const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-    *reinterpret_cast<uint4*>(&sm.k[k][d8]) = kv.k[j];
-    *reinterpret_cast<uint4*>(&sm.v[k][d8]) = kv.v[j];
+  for (int i = 0; i < 4; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
   }
-  __syncthreads();
-  // S = Q K^T: 2 query tiles x 8 key tiles; warp w takes key tile w for both query tiles
-  {
-    const int nt = wid;
-    float c[2][4] = {};
+  float o[2][2][4] = {};  // dim tiles 2 wid + dn, query tiles mt
+  for (int c = c0; c < c1; ++c) {
+    const int k_begin = kbeg(c), nk = nkeys(c);
 #pragma unroll
-    for (int ks = 0; ks < kHd / 16; ++ks) {
-      const uint32_t b0 = ld32(&sm.k[nt * 8 + g][ks * 16 + 2 * q]);
-      const uint32_t b1 = ld32(&sm.k[nt * 8 + g][ks * 16 + 8 + 2 * q]);
+    for (int j = 0; j < 4; ++j) {
+      const int e = tid + 256 * j;
+      const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
+      *reinterpret_cast<uint4*>(&sm.k[k][d8]) = kv.k[j];
+      *reinterpret_cast<uint4*>(&sm.v[k][d8]) = kv.v[j];
+    }
+    if (c + 1 < c1) kv = load_kv(a, r, kvh, kbeg(c + 1), nkeys(c + 1));  // in flight during this chunk
+    __syncthreads();
+    // S = Q K^T: 2 query tiles x 8 key tiles; warp w takes key tile w for both query tiles
+    {
+      const int nt = wid;
+      float cs[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < kHd / 16; ++ks) {
+        const uint32_t b0 = ld32(&sm.k[nt * 8 + g][ks * 16 + 2 * q]);
+        const uint32_t b1 = ld32(&sm.k[nt * 8 + g][ks * 16 + 8 + 2 * q]);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int r0 = mt * 16 + g;
+          mma_bf16(cs[mt], ld32(&sm.qh[r0][ks * 16 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 2 * q]),
+                   ld32(&sm.qh[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+          mma_bf16(cs[mt], ld32(&sm.ql[r0][ks * 16 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 2 * q]),
+                   ld32(&sm.ql[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+        }
+      }
+      const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        const int r0 = mt * 16 + g;
-        mma_bf16(c[mt], ld32(&sm.qh[r0][ks * 16 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 2 * q]),
-                 ld32(&sm.qh[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
-        mma_bf16(c[mt], ld32(&sm.ql[r0][ks * 16 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 2 * q]),
-                 ld32(&sm.ql[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
-      }
-    }
-    const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int qi = mt * 16 + g + 8 * h2;
+          const int pos_i = qi & 7;
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int qi = mt * 16 + g + 8 * h2;
-        const int pos_i = qi & 7;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int k = nt * 8 + 2 * q + e;
-          const bool ok = k < nk && k >= lim + pos_i;
-          sm.s[qi][k] = ok ? c[mt][2 * h2 + e] : -INFINITY;
+          for (int e = 0; e < 2; ++e) {
+            const int k = nt * 8 + 2 * q + e;
+            const bool ok = k < nk && k >= lim + pos_i;
+            sm.s[qi][k] = ok ? cs[mt][2 * h2 + e] : -INFINITY;
+          }
         }
       }
     }
-  }
-  __syncthreads();
-  // softmax statistics per query: warp w handles queries 4w..4w+3, lane keys lane, lane+32
+    __syncthreads();
+    // running softmax statistics: warp w handles queries 4w..4w+3, lane keys lane, lane+32
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int qi = wid * 4 + i;
-    const float v0 = sm.s[qi][lane], v1 = sm.s[qi][lane + 32];
-    const float m = warp_max(fmaxf(v0, v1));
-    const float p0 = (m == -INFINITY) ? 0.f : exp2f(v0 - m);
-    const float p1 = (m == -INFINITY) ? 0.f : exp2f(v1 - m);
-    const float l = warp_sum(p0 + p1);
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-    sm.ph[qi][lane] = h0;
-    sm.ph[qi][lane + 32] = h1;
-    sm.pl[qi][lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
-    sm.pl[qi][lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
-    if (lane == 0) {
-      out[qi * kPartStride + 0] = m;
-      out[qi * kPartStride + 1] = l;
+    for (int i = 0; i < 4; ++i) {
+      const int qi = wid * 4 + i;
+      const float v0 = sm.s[qi][lane], v1 = sm.s[qi][lane + 32];
+      const float m_new = fmaxf(m_run[i], warp_max(fmaxf(v0, v1)));
+      const bool none = m_new == -INFINITY;  // no visible key yet
+      const float alpha = none ? 1.f : exp2f(m_run[i] - m_new);
+      const float p0 = none ? 0.f : exp2f(v0 - m_new);
+      const float p1 = none ? 0.f : exp2f(v1 - m_new);
+      l_run[i] = l_run[i] * alpha + warp_sum(p0 + p1);
+      m_run[i] = m_new;
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+      sm.ph[qi][lane] = h0;
+      sm.ph[qi][lane + 32] = h1;
+      sm.pl[qi][lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
+      sm.pl[qi][lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
+      if (lane == 0) sm.alpha[qi] = alpha;
     }
-  }
-  __syncthreads();
-  // O = P V: 2 query tiles x 16 dim tiles; warp w takes dim tiles 2w, 2w+1
+    __syncthreads();
+    // O = alpha O + P V: 2 query tiles x 16 dim tiles; warp w takes dim tiles 2w, 2w+1
 #pragma unroll
-  for (int dn = 0; dn < 2; ++dn) {
-    const int nt = wid * 2 + dn;
-    float c[2][4] = {};
+    for (int mt = 0; mt < 2; ++mt) {
+      const float a0 = sm.alpha[mt * 16 + g], a1 = sm.alpha[mt * 16 + g + 8];
 #pragma unroll
-    for (int ks = 0; ks < kKeys / 16; ++ks) {
-      uint32_t b0, b1;
-      ldmatrix_x2_trans(b0, b1, &sm.v[ks * 16 + (lane & 15)][nt * 8]);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int r0 = mt * 16 + g;
-        mma_bf16(c[mt], ld32(&sm.ph[r0][ks * 16 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 2 * q]),
-                 ld32(&sm.ph[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
-        mma_bf16(c[mt], ld32(&sm.pl[r0][ks * 16 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 2 * q]),
-                 ld32(&sm.pl[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+      for (int dn = 0; dn < 2; ++dn) {
+        o[dn][mt][0] *= a0;
+        o[dn][mt][1] *= a0;
+        o[dn][mt][2] *= a1;
+        o[dn][mt][3] *= a1;
       }
     }
 #pragma unroll
+    for (int dn = 0; dn < 2; ++dn) {
+      const int nt = wid * 2 + dn;
+#pragma unroll
+      for (int ks = 0; ks < kKeys / 16; ++ks) {
+        uint32_t b0, b1;
+        ldmatrix_x2_trans(b0, b1, &sm.v[ks * 16 + (lane & 15)][nt * 8]);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int r0 = mt * 16 + g;
+          mma_bf16(o[dn][mt], ld32(&sm.ph[r0][ks * 16 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 2 * q]),
+                   ld32(&sm.ph[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+          mma_bf16(o[dn][mt], ld32(&sm.pl[r0][ks * 16 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 2 * q]),
+                   ld32(&sm.pl[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+        }
+      }
+    }
+    __syncthreads();  // k, v, p and alpha are rewritten by the next chunk
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[(wid * 4 + i) * kPartStride + 0] = m_run[i];
+      out[(wid * 4 + i) * kPartStride + 1] = l_run[i];
+    }
+  }
+#pragma unroll
+  for (int dn = 0; dn < 2; ++dn) {
+    const int nt = wid * 2 + dn;
+#pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
       const int q0 = mt * 16 + g, d0 = nt * 8 + 2 * q;
-      out[q0 * kPartStride + 2 + d0] = c[mt][0];
-      out[q0 * kPartStride + 2 + d0 + 1] = c[mt][1];
-      out[(q0 + 8) * kPartStride + 2 + d0] = c[mt][2];
-      out[(q0 + 8) * kPartStride + 2 + d0 + 1] = c[mt][3];
+      out[q0 * kPartStride + 2 + d0] = o[dn][mt][0];
+      out[q0 * kPartStride + 2 + d0 + 1] = o[dn][mt][1];
+      out[(q0 + 8) * kPartStride + 2 + d0] = o[dn][mt][2];
+      out[(q0 + 8) * kPartStride + 2 + d0 + 1] = o[dn][mt][3];
     }
   }
 }
@@ -248,27 +289,27 @@ DF2_DEV void blk_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kv
   (void)wid;
 }
 
-__global__ void __launch_bounds__(256) attn_chunk_kernel(const AttnArgs a) {
+// grid (R * nkv, n_chunks): part p < n_chunks - 1 takes context chunks
+// p cpc .. p cpc + cpc - 1 (those that exist); the last part the 8 block keys.
+__global__ void __launch_bounds__(256, 3) attn_chunk_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int nkv = a.n_kv_heads;
   const int r = blockIdx.x / nkv, kvh = blockIdx.x % nkv;
-  const int chunk = blockIdx.y;
+  const int part = blockIdx.y;
   const int nn = min(max(a.n_new[r], 0), 8);
   const int L = min(max(a.ctx_len[r], 0), a.kv_capacity - nn) + nn;  // same clamping as the cache append
   const int lo0 = max(0, L - (a.window - 1));
   const int n_ctx_chunks = (L - lo0 + kKeys - 1) / kKeys;
-  float* out = a.part + ((static_cast<size_t>(r) * nkv + kvh) * a.n_chunks + chunk) * kQ * kPartStride;
-  if (chunk == a.n_chunks - 1) {
+  const int c0 = part * a.cpc, c1 = min(c0 + a.cpc, n_ctx_chunks);
+  float* out = a.part + ((static_cast<size_t>(r) * nkv + kvh) * a.n_chunks + part) * kQ * kPartStride;
+  if (part == a.n_chunks - 1) {
     pdl_begin();
     blk_chunk(a, smem_raw, r, kvh, out);
-  } else if (chunk < n_ctx_chunks) {
-    const int k_begin = lo0 + chunk * kKeys;
-    const int nk = min(kKeys, L - k_begin);
-    // rows L - nn .. L - 1 are appended by the previous kernel; older rows are not written this step
-    ctx_chunk(a, smem_raw, r, kvh, k_begin, nk, L, k_begin + nk <= L - nn, out);
+  } else if (c0 < c1) {
+    ctx_part(a, smem_raw, r, kvh, lo0, c0, c1, L, nn, out);
   } else {
     pdl_begin();
-    if (threadIdx.x < kQ) {  // no keys in this chunk
+    if (threadIdx.x < kQ) {  // no keys in this part
       out[threadIdx.x * kPartStride + 0] = -INFINITY;
       out[threadIdx.x * kPartStride + 1] = 0.f;
     }

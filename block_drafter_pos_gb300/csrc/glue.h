@@ -119,10 +119,12 @@ struct AttnArgs {
   const uint16_t* v_cache;
   const int32_t* ctx_len;
   const int32_t* n_new;
-  float* part;             // [R][nkv][n_chunks][32][130]
+  float* part;             // [R][nkv][n_chunks][32][130] per part: (m, l, unnormalised output) of 32 queries
   void* act_o;             // [N][nq*128]
   size_t act_o_lo;
-  int n_q_heads, n_kv_heads, kv_capacity, window, n_chunks, fmt;
+  int n_q_heads, n_kv_heads, kv_capacity, window, fmt;
+  int n_chunks;            // parts: ceil(context chunks / cpc) + 1 (the block keys)
+  int cpc;                 // context chunks of 64 keys per part
   int tiled_o;             // > 0: act_o in the tensor-core operand layout (act_offset)
 };
 constexpr int kAttnChunk = 64;
