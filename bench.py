@@ -310,7 +310,7 @@ def main_ours(args, rank, world, local_rank):
                    "parallelism": f"{world} independent replica(s)", "timing": "one CUDA graph of K steps"},
         "drafted_tokens_per_s": steps_per_s * 7 * R,
         "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
-        "roofline": {"kernel": ("lmhead_kernel (LM head GEMV + fused top-16)" if R <= 4 else
+        "roofline": {"kernel": ("lmhead_kernel (LM head GEMV + fused top-16)" if R < (5 if wl.weight_format == "bf16" else 4) else
                                 "wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel"), "bound": "hbm",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                      "traffic": LMHEAD_TRAFFIC.get((wl.geom.vocab, wl.geom.hidden, R)),

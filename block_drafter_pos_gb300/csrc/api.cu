@@ -32,7 +32,8 @@ struct dflash2_handle {
   int n_attn_chunks, n_verify_chunks, lm_ctas;
   // where each projection's partial planes are (the launches' shapes are fixed at create)
   // plane maps of every projection launch: the GEMV (up to 4 requests) and the
-  // tensor-core GEMM (more requests; set up when max_requests > 4)
+  // tensor-core GEMM (calls with at least wide_min_requests requests; set up when
+  // max_requests reaches that)
   struct PlaneSet {
     GemvPlanes fc, d0, d, q, k, v, o, g, u, down, sel, lm;
   } pn, pw;
@@ -139,6 +140,11 @@ dflash2_status run_gemv(dflash2_handle* h, bool wide, std::initializer_list<SegS
   return DFLASH2_OK;
 }
 
+// Calls with at least this many requests run every projection on the tensor-core
+// GEMM (measured: with int8 weights it overtakes the GEMV at four requests, whose
+// key/value launch needs the GEMV's 8-tile variant; with bf16 at five).
+int wide_min_requests(int fmt) { return fmt == DFLASH2_WEIGHTS_BF16 ? 5 : 4; }
+
 bool valid_matrix(const dflash2_matrix& m, int fmt) {
   if (!m.w || !aligned16(m.w)) return false;
   // Q8 scale/bias rows are read 8 groups (16 bytes) at a time
@@ -218,7 +224,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->lm_ctas = lmhead_ctas(h->num_sms);
   // plane maps of every projection launch (shapes only; the same plans as launch_gemv's
   // and launch_wide's), and the largest plane count of each output buffer over both
-  h->wide = max_requests > 4;
+  h->wide = max_requests >= wide_min_requests(fmt);
   h->lm_chunks = (c.vocab + kLogitChunk - 1) / kLogitChunk;
   int maxp_fc = 0, maxp_d = 0, maxp_q = 0, maxp_k = 0, maxp_v = 0, maxp_y = 0, maxp_g = 0, maxp_u = 0, maxp_sel = 0,
       maxp_lm = 0;
@@ -393,7 +399,7 @@ dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* s
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
   if (!h || n_req < 1) return -1;
   const int64_t N = 8 * static_cast<int64_t>(n_req);
-  if (n_req > 4)                                   // tensor-core GEMM + chunked top-16
+  if (n_req >= wide_min_requests(h->fmt))          // tensor-core GEMM + chunked top-16
     return static_cast<int64_t>(h->V) * h->H * 2   // LM-head weights, read once
            + N * h->H * 2                          // bf16 hidden state, one plane
            + 2 * N * h->V * 4                      // logits written, then read by the top-16
@@ -420,8 +426,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   const int H = h->H, G = h->G;
   const size_t layer_stride = static_cast<size_t>(h->max_req) * h->kv_cap * h->kvd;  // elements
   const int N8 = 8 * h->max_req;  // rows of one plane of each activation buffer
-  // more than four requests: every projection on the tensor-core GEMM
-  const bool wide = R > 4;
+  // many requests: every projection on the tensor-core GEMM
+  const bool wide = R >= wide_min_requests(fmt);
   const dflash2_handle::PlaneSet& P = wide ? h->pw : h->pn;
   // the tensor-core path reads its activations as one plane in the GEMM's operand
   // layout, slices of 8 max_requests rows rounded up to 16 (16 max_requests for the
@@ -568,7 +574,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.kv_capacity = h->kv_cap;
       a.window = c.window;
       // context chunks per part: one while the parts alone fill the GPU, four with more requests
-      a.cpc = R > 4 ? 4 : 1;
+      a.cpc = R >= 4 ? 4 : 1;
       a.n_chunks = (h->n_attn_chunks - 1 + a.cpc - 1) / a.cpc + 1;
       a.fmt = fmt;
       DF2_CHECK(launch_attention(a, R, pdl, st));

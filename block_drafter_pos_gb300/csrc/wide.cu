@@ -1,6 +1,6 @@
 // Projections with many activation rows on the fifth-generation tensor cores
 // (tcgen05): y[n][m] = sum_k W[m][k] x[n][k] for up to 256 activation rows, the
-// shape of a step with more than four requests (8 block rows per request, plus the
+// shape of a step with many requests (8 block rows per request, plus the
 // new context rows for the key and value projections).
 //
 // Design (sm_103a):
@@ -24,9 +24,9 @@
 //    per group of 64 along K): the copy brings the int8 codes (64-byte swizzle), and
 //    warps 8..15 turn them into fp16 values in a ring of operand tiles (one weight
 //    row and half the stage's K per thread: byte permute against the 1024 exponent,
-//    w = q * s + b in fp16), release the code slot as soon as the codes are in
-//    registers, and hand the operand tile to the MMA thread through its mbarrier
-//    after a proxy fence.
+//    w = q * s + b in fp16), release the code slot once the codes have been used,
+//    and hand the operand tile to the MMA thread through its mbarrier after a
+//    proxy fence.
 //    One stage is exactly one quantisation group along K.
 //  * The activations are read as one 16-bit plane (bf16 for bf16 weights, fp16 for
 //    Q8), the high plane of the buffers the element-wise kernels write.
@@ -434,8 +434,6 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
       uint4 w[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) w[j] = lds128(crow + (((4 * hk + j) ^ (r & 7)) << 4));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(wempty + 8 * sw);  // the codes are in registers: the copy slot is free
       if (i >= DA && !mbar_wait(aempty + 8 * sa, static_cast<uint32_t>(((i / DA) + 1) & 1))) {
         ok = false;
         break;
@@ -456,6 +454,12 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
         sts128(arow + (((2 * j) ^ (r & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
         sts128(arow + (((2 * j + 1) ^ (r & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
       }
+      // Every lane has used its codes (the stores above depend on them), so none of
+      // its loads of the code slot is still in flight: the slot is free for the next
+      // copy.  Releasing it before the values are used would let the copy overwrite
+      // a slot a load is still reading.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wempty + 8 * sw);
       // generic-proxy stores become visible to the tensor cores' reads before the hand-over
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();

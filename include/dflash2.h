@@ -124,9 +124,9 @@ typedef struct dflash2_handle dflash2_handle;
  * multiple of 256, ffn not a multiple of 128 (BF16) or 256 (Q8G64), vocab not a
  * multiple of 16, more than DFLASH2_MAX_LAYERS layers or DFLASH2_MAX_REQUESTS
  * requests, or a window over 64 attention chunks of 64 keys; and, when
- * max_requests > 4 (the calls with more than four requests run every projection
- * on the tensor-core GEMM, in 128-row weight blocks), hidden / 4 or vocab not a
- * multiple of 128.  Every weight
+ * max_requests reaches 5 (BF16) or 4 (Q8G64), hidden / 4 or vocab not a multiple
+ * of 128: calls with that many requests run every projection on the tensor-core
+ * GEMM, in 128-row weight blocks.  Every weight
  * matrix, Q8 scale and Q8 bias must start on a 16-byte boundary
  * (DFLASH2_E_INVAL otherwise).  Encodes one bulk-copy descriptor per projection
  * matrix, so the weights must not move while the handle lives. */
@@ -195,9 +195,9 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
  * positions 1..7 = W_lm . hidden (hidden already normalised, BF16), top-16 with the
  * ordering of dflash2_draft_block.  Row n of `hidden` is request n/8, block position
  * n%8 (position 0 is not projected).  n_rows: multiple of 8, <= 8*max_requests.
- * Up to 32 rows run on the LM-head kernel; more rows (a handle created with
- * max_requests > 4, else DFLASH2_E_UNSUPPORTED) on the tensor-core GEMM, with the
- * logits in handle scratch, then a chunked top-16.
+ * Up to 32 rows run on the LM-head kernel; more rows (a handle whose calls reach
+ * the tensor-core GEMM, see dflash2_create, else DFLASH2_E_UNSUPPORTED) on the
+ * tensor-core GEMM, with the logits in handle scratch, then a chunked top-16.
  *   hidden [n_rows][H] bf16; cand_ids, cand_logits [n_rows/8][block-1][top_k];
  *   logits_out [n_rows/8][block-1][V] float32 or NULL. */
 dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
@@ -209,13 +209,13 @@ int64_t dflash2_launch_count(const dflash2_handle* h);
 
 /* Profiling hook: when both events are non-NULL (cudaEvent_t passed as void*),
  * dflash2_draft_block records `start` right before and `stop` right after its
- * LM-head + top-16 kernel (the GEMM and the chunked top-16 with more than four
- * requests) on the call's stream.  NULL, NULL turns it off. */
+ * LM-head + top-16 kernel (the GEMM and the chunked top-16 on the tensor-core
+ * path) on the call's stream.  NULL, NULL turns it off. */
 dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* stop);
 
 /* Algorithmic bytes the LM-head + top-16 kernel of one draft_block call streams
- * (LM-head weights + activations + candidate outputs; with more than four
- * requests also the logits the GEMM writes and the top-16 kernel reads), for
+ * (LM-head weights + activations + candidate outputs; on the tensor-core path
+ * also the logits the GEMM writes and the top-16 kernel reads), for
  * roofline reports. */
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req);
 

@@ -1,6 +1,8 @@
 """GPU parity at the full DFlash2 geometry (5 layers, width 5120, vocab 248320) on
-the benchmark workloads: the drafter outputs of every request against the FP64
-oracle, and the select/verify outputs against properties that hold at any size."""
+the benchmark workloads: the drafter outputs of every request (a spread of four
+of the 16 requests of configuration 5, which runs on the tensor-core path) against
+the FP64 oracle, and the select/verify outputs against properties that hold at any
+size."""
 import numpy as np
 import pytest
 import torch
@@ -20,7 +22,11 @@ def built():
     assert torch.cuda.is_available()
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4])
+# requests checked against the oracle (all of them, or a spread for 16 requests)
+ORACLE_REQS = {5: (0, 5, 10, 15)}
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_full_geometry_step(cfg):
     wl = wk.workload(cfg)
     g = wl.geom
@@ -38,7 +44,7 @@ def test_full_geometry_step(cfg):
     gate = step.gate.cpu().numpy()
     kc_gpu = kct.cpu().numpy().view(np.uint16)
     near = 0
-    for r in range(R):
+    for r in ORACLE_REQS.get(cfg, range(R)):
         tr = oracle_draft(wl, W, inp, kc, vc, r)
         assert rel_l2(logits[r], tr["logits"]) < 2e-2, r
         assert rel_l2(gate[r], tr["gate"]) < 2e-2, r

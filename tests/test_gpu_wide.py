@@ -1,4 +1,4 @@
-"""GPU parity of the tensor-core path against the oracle: a call with more than four
+"""GPU parity of the tensor-core path against the oracle: a call with many
 requests runs every projection and the LM head on the tcgen05 GEMM (128-row weight
 blocks, activations one 16-bit plane) and the top-16 on the chunked kernel.  Toy
 width (512, vocab 8192) with 5 and 16 requests, ragged contexts and appends, both
@@ -130,3 +130,31 @@ def test_head_topk_many_rows_exact_integer_logits():
         want = topk_of(exact[n])
         assert np.array_equal(ids_h[r, i], want)
         assert np.array_equal(vals_h[r, i], exact[n][want])
+
+
+def test_wide_path_many_stages_per_cta():
+    """A mid-size geometry (width 2048, FFN 4096, vocabulary 32768, 2 layers) with 16
+    requests and Q8 weights: every CTA of the tensor-core GEMM runs many stages and
+    crosses weight blocks (the fc projection ~8 stages per CTA, the LM head ~27), so
+    the rings wrap, accumulators are reused and partial planes are added, which the
+    toy width (one stage per CTA) never does.  Four requests against the oracle."""
+    g = dataclasses.replace(wk.TOY, hidden=2048, n_layers=2, n_q_heads=16, n_kv_heads=4, ffn=4096, vocab=32768,
+                            window=256)
+    rng = np.random.default_rng(77)
+    R = 16
+    ctx = [int(x) for x in rng.integers(8, 400, size=R)]
+    wl = wk.Workload("mid_wide_q8_r16", g, "q8", R, ctx, [0.0] * R, [0.5] * R, seed=31)
+    W = wk.make_weights(g, "q8", wl.seed)
+    inp = wk.make_request_inputs(wl)
+    kc, vc, step, kct, vct = _run(wl, W, inp)
+    logits = step.logits.cpu().numpy()
+    gate = step.gate.cpu().numpy()
+    ids = step.cand_ids.cpu().numpy()
+    for r in (0, 5, 10, 15):
+        tr = oracle_draft(wl, W, inp, kc, vc, r)
+        assert rel_l2(logits[r], tr["logits"]) < 2e-2, r
+        assert rel_l2(gate[r], tr["gate"]) < 2e-2, r
+        for i in range(7):
+            assert np.array_equal(ids[r, i], topk_of(logits[r, i]))
+            err = float(np.max(np.abs(logits[r, i] - tr["logits"][i])))
+            certified_topk(ids[r, i], tr["logits"][i], err)
