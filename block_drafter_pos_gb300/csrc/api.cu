@@ -433,6 +433,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   // layout, slices of 8 max_requests rows rounded up to 16 (16 max_requests for the
   // QKV input): a slice holds every row the MMA reads (rows rounded up to 16)
   const int tA = wide ? (N8 + 15) & ~15 : 0, tQ = wide ? 2 * N8 : 0;
+  // the projections' inputs carry a low-order plane only on the GEMV path with bf16
+  // weights (fp16 rounds to 2^-12 relative; the GEMM reads one plane)
+  auto lo_of = [&](size_t lo) { return (wide || fmt != 0) ? static_cast<size_t>(0) : lo; };
   // ---- a2: block embedding, first norm input, taps packing
   {
     StartArgs a = {};
@@ -443,11 +446,11 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.taps = taps;
     a.x = h->x;
     a.act_a = h->act_a;
-    a.act_a_lo = wide ? 0 : h->lo_a;
+    a.act_a_lo = lo_of(h->lo_a);
     a.tiled_a = tA;
     a.ss_x = h->ss;
     a.act_taps = h->act_taps;
-    a.act_taps_lo = wide ? 0 : h->lo_taps;
+    a.act_taps_lo = lo_of(h->lo_taps);
     a.tiled_taps = tA;
     a.H = H;
     a.n_taps = c.n_taps;
@@ -469,7 +472,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.base = static_cast<const uint16_t*>(L.attn_base);
     a.delta = h->delta_a;
     a.act = h->act_qkv;
-    a.act_lo = wide ? 0 : h->lo_qkv;
+    a.act_lo = lo_of(h->lo_qkv);
     a.tiled = tQ;
     a.H = H;
     a.nch = h->nch_ss;
@@ -494,7 +497,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.y = h->fc_out;
     a.norm_w = static_cast<const uint16_t*>(h->w.hidden_norm);
     a.act = h->act_qkv;
-    a.act_lo = wide ? 0 : h->lo_qkv;
+    a.act_lo = lo_of(h->lo_qkv);
     a.tiled = tQ;
     a.ss = h->ss_c;
     a.H = H;
@@ -567,7 +570,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.n_new = n_new;
       a.part = h->attn_part;
       a.act_o = h->act_o;
-      a.act_o_lo = wide ? 0 : h->lo_o;
+      a.act_o_lo = lo_of(h->lo_o);
       a.tiled_o = tA;
       a.n_q_heads = h->nq;
       a.n_kv_heads = h->nkv;
@@ -591,7 +594,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.norm_w = static_cast<const uint16_t*>(L.post_norm);
       a.x = h->x;
       a.act = h->act_a;
-      a.act_lo = wide ? 0 : h->lo_a;
+      a.act_lo = lo_of(h->lo_a);
       a.tiled = tA;
       a.act2 = nullptr;
       a.act2_lo = 0;
@@ -616,7 +619,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.base = static_cast<const uint16_t*>(L.mlp_base);
       a.delta = h->delta_m;
       a.act = h->act_qkv;
-      a.act_lo = wide ? 0 : h->lo_qkv;
+      a.act_lo = lo_of(h->lo_qkv);
       a.tiled = tQ;
       a.H = H;
       a.nch = h->nch_ss;
@@ -637,7 +640,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.part_g = h->gpart;
       a.part_u = h->upart;
       a.act = h->act_h;
-      a.act_lo = wide ? 0 : h->lo_h;
+      a.act_lo = lo_of(h->lo_h);
       a.tiled = tA;
       a.F = h->F;
       a.fmt = fmt;
@@ -659,7 +662,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.x = h->x;
       // LM-head input is bf16 in both formats; the next layer's input is in the matrices' format
       a.act = (last && fmt == 0) ? static_cast<void*>(h->act_fin) : h->act_a;
-      a.act_lo = wide ? 0 : (last && fmt == 0) ? h->lo_fin : h->lo_a;
+      a.act_lo = (last && fmt == 0) ? (wide ? 0 : h->lo_fin) : lo_of(h->lo_a);
       a.tiled = tA;
       a.act2 = (last && fmt != 0) ? h->act_fin : nullptr;
       a.act2_lo = wide ? 0 : h->lo_fin;

@@ -29,8 +29,9 @@
 //    consumer kernel adds the block's planes in order (gemv_plane_count gives
 //    their number in closed form), so every result is bit-reproducible, with no
 //    atomics and no inter-CTA signalling.
-//  * Activations carry a low-order plane (x = hi + lo) for ~16-bit accuracy, with
-//    independent accumulator chains for the two planes.
+//  * bf16 activations carry a low-order plane (x = hi + lo) for ~16-bit accuracy,
+//    with independent accumulator chains for the two planes; fp16 activations (int8
+//    weights) round to 2^-12 relative and are one plane.
 //  * Q8/group64 ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias per
 //    group of 64 along K, bf16 scale and bias): the int8 codes become exact fp16
 //    values by a byte permute against the 1024 exponent, and the affine map is
@@ -172,7 +173,6 @@ DF2_DEV Q8Affine load_affine(const GemvSeg& sg, int row, int kabs, int q) {
 template <int NT>
 DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, const Q8Affine& af,
                       float (&c0)[NT][4], float (&c1)[NT][4], float (&c2)[NT][4], float (&c3)[NT][4]) {
-  constexpr int kXPlane = 8 * NT * stage_k<1>() * 2;
   constexpr int kXBoxes = stage_k<1>() / 64;
   constexpr int kWBoxes = stage_k<1>() / wbox_k<1>();
   const int sw = q & 2;
@@ -208,15 +208,11 @@ DF2_DEV void stage_q8(int n_tiles, uint32_t wa, uint32_t xrow, int g, int q, con
         if (t < n_tiles) {
           const uint32_t xb = xrow + (t * kXBoxes + 2 * b) * 1024;
           const uint4 xa = lds128(xb + xo[2 * h]), xc = lds128(xb + xo[2 * h + 1]);  // 8 + 8 K of this half
-          const uint4 ya = lds128(xb + kXPlane + xo[2 * h]), yc = lds128(xb + kXPlane + xo[2 * h + 1]);
+          // one fp16 plane; four independent accumulator chains
           mma_f16(c0[t], A[0][0], A[0][1], A[0][2], A[0][3], xa.x, xa.y);
           mma_f16(c1[t], A[1][0], A[1][1], A[1][2], A[1][3], xa.z, xa.w);
-          mma_f16(c0[t], A[2][0], A[2][1], A[2][2], A[2][3], xc.x, xc.y);
-          mma_f16(c1[t], A[3][0], A[3][1], A[3][2], A[3][3], xc.z, xc.w);
-          mma_f16(c2[t], A[0][0], A[0][1], A[0][2], A[0][3], ya.x, ya.y);
-          mma_f16(c3[t], A[1][0], A[1][1], A[1][2], A[1][3], ya.z, ya.w);
-          mma_f16(c2[t], A[2][0], A[2][1], A[2][2], A[2][3], yc.x, yc.y);
-          mma_f16(c3[t], A[3][0], A[3][1], A[3][2], A[3][3], yc.z, yc.w);
+          mma_f16(c2[t], A[2][0], A[2][1], A[2][2], A[2][3], xc.x, xc.y);
+          mma_f16(c3[t], A[3][0], A[3][1], A[3][2], A[3][3], xc.z, xc.w);
         }
       }
     }
@@ -258,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
     };
     // this lane's activation boxes (plane, tile, 64-K box): box indices lane and lane + 32,
     // recomputed when the segment changes
-    constexpr int kXPerLane = (2 * NT * kXBoxes + 31) / 32;
+    constexpr int kXPerLane = (Geo::kXPlanes * NT * kXBoxes + 31) / 32;
     int xs_seg = -1, x_row[kXPerLane], x_b[kXPerLane];
     uint32_t x_dst[kXPerLane];
     bool x_on[kXPerLane];
@@ -270,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
 #pragma unroll
         for (int j = 0; j < kXPerLane; ++j) {
           const int box = lane + 32 * j;
-          x_on[j] = box < 2 * per;
+          x_on[j] = box < Geo::kXPlanes * per;
           const int plane = box / per, rem = box % per, t = rem / kXBoxes;
           x_b[j] = rem % kXBoxes;
           x_dst[j] = Geo::kWBytes + plane * Geo::kXPlane + (t * kXBoxes + x_b[j]) * kXBoxBytes;
@@ -284,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
                       full0 + 8 * slot, xpolicy);
     };
     auto arm = [&](const Cursor& c, int slot) {
-      const int xbytes = 2 * a.seg[c.seg].n_tiles * kXBoxes * kXBoxBytes;
+      const int xbytes = Geo::kXPlanes * a.seg[c.seg].n_tiles * kXBoxes * kXBoxBytes;
       if (lane == 0) mbar_expect_tx(full0 + 8 * slot, Geo::kWBytes + xbytes);
       __syncwarp();
     };

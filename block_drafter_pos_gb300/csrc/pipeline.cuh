@@ -36,7 +36,10 @@ template <int FMT, int NT>
 struct StageGeo {
   static constexpr int kWBytes = kBlockRows * stage_k<FMT>() * (FMT == 0 ? 2 : 1);
   static constexpr int kXPlane = 8 * NT * stage_k<FMT>() * 2;  // 8*NT rows x stage K x 2 B
-  static constexpr int kBytes = kWBytes + 2 * kXPlane;
+  // activation planes: bf16 carries a low-order plane (hi + lo); fp16 (int8 weights)
+  // rounds to 2^-12 relative and needs none
+  static constexpr int kXPlanes = FMT == 0 ? 2 : 1;
+  static constexpr int kBytes = kWBytes + kXPlanes * kXPlane;
   static constexpr int kDepthRaw = kRingBudget / kBytes;
   static constexpr int kDepth = kDepthRaw < 2 ? 2 : (kDepthRaw > kMaxDepth ? kMaxDepth : kDepthRaw);
   static constexpr int kSmem = kDepth * kBytes + 1024;  // + slack for 1 KB alignment
