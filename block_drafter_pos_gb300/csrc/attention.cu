@@ -316,21 +316,22 @@ __global__ void __launch_bounds__(256, 3) attn_chunk_kernel(const AttnArgs a) {
   }
 }
 
-// One warp per (request, query head, block position): merges the chunk partials in
-// chunk order; lane holds dims lane + 32 j.
+// One warp per (request, query head, block position, 32 of the 128 dimensions):
+// merges the parts' partials in part order; lane holds dimension 32 quarter + lane.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x;
-  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // head * 8 + position
-  if (item >= a.n_q_heads * 8) return;
-  const int h = item >> 3, i = item & 7;
+  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // (head * 8 + position) * 4 + quarter
+  if (item >= a.n_q_heads * 8 * 4) return;
+  const int quarter = item & 3, h = item >> 5, i = (item >> 2) & 7;
   const int nkv = a.n_kv_heads;
   const int rep = a.n_q_heads / nkv;
   const int kvh = h / rep, hr = h % rep;
   const int qi = hr * 8 + i;
+  const int d = quarter * 32 + lane;
   const float* base = a.part + (static_cast<size_t>(r) * nkv + kvh) * a.n_chunks * kQ * kPartStride;
-  // chunk statistics: lane c holds chunks c and c + 32 (n_chunks <= 64)
+  // part statistics: lane c holds parts c and c + 32 (n_chunks <= 64)
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
@@ -346,38 +347,32 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) f[u] = (l[u] > 0.f) ? exp2f(m[u] - M) : 0.f;
   const float den = warp_sum(f[0] * l[0] + f[1] * l[1]);
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c0 = 0; c0 < a.n_chunks; c0 += 8) {  // 8 chunks' loads in flight, added in chunk order
-    float fc[8], t[8][4];
+  float o = 0.f;
+  for (int c0 = 0; c0 < a.n_chunks; c0 += 16) {  // 16 parts' loads in flight, added in part order
+    float fc[16], t[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 16; ++u) {
       const int c = c0 + u;
       fc[u] = c < a.n_chunks ? __shfl_sync(0xffffffffu, f[(c >> 5) & 1], c & 31) : 0.f;
-      const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride + 2;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) t[u][j] = fc[u] != 0.f ? pc[lane + 32 * j] : 0.f;
+      t[u] = fc[u] != 0.f ? base[(static_cast<size_t>(c) * kQ + qi) * kPartStride + 2 + d] : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (fc[u] != 0.f) o[j] += fc[u] * t[u][j];
+    for (int u = 0; u < 16; ++u)
+      if (fc[u] != 0.f) o += fc[u] * t[u];
   }
   const int ld = a.n_q_heads * kHd;
-  for (int j = 0; j < 4; ++j) {
-    const size_t idx = act_offset(r * 8 + i, h * kHd + lane + 32 * j, ld, a.tiled_o);
-    const float v = o[j] / den;
-    if (a.fmt == 0) {
-      __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      p[idx] = hi;
-      if (a.act_o_lo) p[a.act_o_lo + idx] = __float2bfloat16_rn(v - __bfloat162float(hi));
-    } else {
-      __half* p = reinterpret_cast<__half*>(a.act_o);
-      const __half hi = __float2half_rn(v);
-      p[idx] = hi;
-      if (a.act_o_lo) p[a.act_o_lo + idx] = __float2half_rn(v - __half2float(hi));
-    }
+  const size_t idx = act_offset(r * 8 + i, h * kHd + d, ld, a.tiled_o);
+  const float v = o / den;
+  if (a.fmt == 0) {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    p[idx] = hi;
+    if (a.act_o_lo) p[a.act_o_lo + idx] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  } else {
+    __half* p = reinterpret_cast<__half*>(a.act_o);
+    const __half hi = __float2half_rn(v);
+    p[idx] = hi;
+    if (a.act_o_lo) p[a.act_o_lo + idx] = __float2half_rn(v - __half2float(hi));
   }
 }
 
@@ -394,7 +389,7 @@ cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_
   }
   cudaError_t e = launch_ex(attn_chunk_kernel, dim3(n_req * a.n_kv_heads, a.n_chunks), dim3(256), smem, st, pdl, a);
   if (e != cudaSuccess) return e;
-  return launch_ex(attn_combine_kernel, dim3(n_req, (a.n_q_heads * 8 + 7) / 8), dim3(256), 0, st, pdl, a);
+  return launch_ex(attn_combine_kernel, dim3(n_req, (a.n_q_heads * 8 * 4 + 7) / 8), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace df2
