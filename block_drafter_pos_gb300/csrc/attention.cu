@@ -316,20 +316,24 @@ __global__ void __launch_bounds__(256, 3) attn_chunk_kernel(const AttnArgs a) {
   }
 }
 
-// One warp per (request, query head, block position, 32 of the 128 dimensions):
-// merges the parts' partials in part order; lane holds dimension 32 quarter + lane.
+// One warp per (request, query head, block position, 128 / DW of the dimensions):
+// merges the parts' partials in part order; lane holds dimensions
+// (128 / DW) quarter + lane + 32 j.  DW = 4 spreads a request over more warps when
+// there are few requests.
+template <int DW>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  constexpr int kJ = 4 / DW;  // dimensions per lane
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x;
-  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // (head * 8 + position) * 4 + quarter
-  if (item >= a.n_q_heads * 8 * 4) return;
-  const int quarter = item & 3, h = item >> 5, i = (item >> 2) & 7;
+  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // (head * 8 + position) * DW + quarter
+  if (item >= a.n_q_heads * 8 * DW) return;
+  const int quarter = item % DW, h = item / (8 * DW), i = (item / DW) & 7;
   const int nkv = a.n_kv_heads;
   const int rep = a.n_q_heads / nkv;
   const int kvh = h / rep, hr = h % rep;
   const int qi = hr * 8 + i;
-  const int d = quarter * 32 + lane;
+  const int d0 = quarter * (kHd / DW) + lane;
   const float* base = a.part + (static_cast<size_t>(r) * nkv + kvh) * a.n_chunks * kQ * kPartStride;
   // part statistics: lane c holds parts c and c + 32 (n_chunks <= 64)
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -347,32 +351,42 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) f[u] = (l[u] > 0.f) ? exp2f(m[u] - M) : 0.f;
   const float den = warp_sum(f[0] * l[0] + f[1] * l[1]);
-  float o = 0.f;
-  for (int c0 = 0; c0 < a.n_chunks; c0 += 16) {  // 16 parts' loads in flight, added in part order
-    float fc[16], t[16];
+  float o[kJ];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
+  for (int j = 0; j < kJ; ++j) o[j] = 0.f;
+  constexpr int kB = 32 / kJ;  // parts whose loads are in flight together
+  for (int c0 = 0; c0 < a.n_chunks; c0 += kB) {  // added in part order
+    float fc[kB], t[kB][kJ];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
       const int c = c0 + u;
       fc[u] = c < a.n_chunks ? __shfl_sync(0xffffffffu, f[(c >> 5) & 1], c & 31) : 0.f;
-      t[u] = fc[u] != 0.f ? base[(static_cast<size_t>(c) * kQ + qi) * kPartStride + 2 + d] : 0.f;
+      const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride + 2 + d0;
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) t[u][j] = fc[u] != 0.f ? pc[32 * j] : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < 16; ++u)
-      if (fc[u] != 0.f) o += fc[u] * t[u];
+    for (int u = 0; u < kB; ++u)
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if (fc[u] != 0.f) o[j] += fc[u] * t[u][j];
   }
   const int ld = a.n_q_heads * kHd;
-  const size_t idx = act_offset(r * 8 + i, h * kHd + d, ld, a.tiled_o);
-  const float v = o / den;
-  if (a.fmt == 0) {
-    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    p[idx] = hi;
-    if (a.act_o_lo) p[a.act_o_lo + idx] = __float2bfloat16_rn(v - __bfloat162float(hi));
-  } else {
-    __half* p = reinterpret_cast<__half*>(a.act_o);
-    const __half hi = __float2half_rn(v);
-    p[idx] = hi;
-    if (a.act_o_lo) p[a.act_o_lo + idx] = __float2half_rn(v - __half2float(hi));
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const size_t idx = act_offset(r * 8 + i, h * kHd + d0 + 32 * j, ld, a.tiled_o);
+    const float v = o[j] / den;
+    if (a.fmt == 0) {
+      __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      p[idx] = hi;
+      if (a.act_o_lo) p[a.act_o_lo + idx] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    } else {
+      __half* p = reinterpret_cast<__half*>(a.act_o);
+      const __half hi = __float2half_rn(v);
+      p[idx] = hi;
+      if (a.act_o_lo) p[a.act_o_lo + idx] = __float2half_rn(v - __half2float(hi));
+    }
   }
 }
 
@@ -389,7 +403,9 @@ cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_
   }
   cudaError_t e = launch_ex(attn_chunk_kernel, dim3(n_req * a.n_kv_heads, a.n_chunks), dim3(256), smem, st, pdl, a);
   if (e != cudaSuccess) return e;
-  return launch_ex(attn_combine_kernel, dim3(n_req, (a.n_q_heads * 8 * 4 + 7) / 8), dim3(256), 0, st, pdl, a);
+  if (n_req < 4)  // few requests: four warps per (head, position), 32 dimensions each
+    return launch_ex(attn_combine_kernel<4>, dim3(n_req, (a.n_q_heads * 8 * 4 + 7) / 8), dim3(256), 0, st, pdl, a);
+  return launch_ex(attn_combine_kernel<1>, dim3(n_req, (a.n_q_heads * 8 + 7) / 8), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace df2

@@ -57,6 +57,7 @@ using pipe::tma_load_2d;
 constexpr int kTM = 128;         // weight rows per block: the MMA's M
 constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of 16-bit values
 constexpr int kMaxN = 256;       // activation rows per product: the MMA's largest N
+constexpr int kMinStages = 4;    // shortest run of stages per CTA (small launches take fewer CTAs)
 
 // K per stage: one bf16 weight copy of 128-byte rows (64 K), or one int8 copy of
 // 128-byte rows (128 K: two atoms of fp16 operand).
@@ -505,7 +506,11 @@ int wide_plan(GemvArgs& a, int num_sms, int fmt) {
     T += static_cast<long long>(sg.M / kTM) * (sg.K / a.stage_k);
   }
   a.total_stages = T;
-  const long long C = static_cast<long long>(num_sms) * ctas_per_sm(fmt);
+  // one run of stages per CTA, at least kMinStages long: a small launch on fewer
+  // CTAs pays fewer prologues and leaves fewer partial planes to add
+  long long C = static_cast<long long>(num_sms) * ctas_per_sm(fmt);
+  const long long Cmin = (T + kMinStages - 1) / kMinStages;
+  if (Cmin < C) C = Cmin;
   return static_cast<int>(C < T ? C : (T > 0 ? T : 1));
 }
 
