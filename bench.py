@@ -16,6 +16,10 @@ its inputs from pinned host memory and reads its result back.  `roofline`
 covers the LM-head + top-16 kernel, timed with CUDA events captured inside the
 graph on the launching stream.  `cpu_baseline` times the oracle on the host.
 
+`r16` (default line only; `--no-r16` skips it) is the metric's second operating
+point, 16 requests (configuration 5: Q8 weights, ragged contexts 512..32768,
+mixed temperatures), timed the same way in the same process.
+
 `--impl reference` times the CPU oracle (the only reference this method has
 here) on the same workload and prints the same line with "impl": "reference".
 """
@@ -53,6 +57,8 @@ def parse():
     p.add_argument("--config", type=int, default=2)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=100)
+    p.add_argument("--no-r16", action="store_true",
+                   help="skip the 16-request measurement that rides along the default line")
     return p.parse_args()
 
 
@@ -195,6 +201,74 @@ def run_step(bd, h, R, S, ev=None):
                       S["n_acc"], S["emitted"], S["n_emit"], S["status"])
 
 
+def measure_r16(args, world, local_rank):
+    """The metric's second operating point, 16 requests (configuration 5: Q8, ragged
+    contexts, mixed temperatures; the tensor-core path), timed the same way as the
+    main line: one CUDA graph of K steps after W eager warm-up steps, max over ranks."""
+    import torch
+    import torch.distributed as dist
+    import block_drafter_pos_gb300 as bd
+    import workloads as wk
+
+    wl = wk.workload(5)
+    R = wl.n_req
+    drafter, S, _, _, _, _, setup_s = setup(wl, local_rank)
+    h = drafter.handle
+    K = max(10, min(args.steps, 50))
+    for _ in range(max(3, args.warmup)):
+        run_step(bd, h, R, S)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.current_stream()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(graph, stream=cap_stream):
+            for i in range(K):
+                bd.dflash2_set_lmhead_events(h, ev[i][0], ev[i][1])
+                run_step(bd, h, R, S)
+    bd.dflash2_set_lmhead_events(h, None, None)
+    stream.wait_stream(cap_stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = S["status"].cpu().numpy()
+    assert np.all(st == 0), st
+    lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    pk = peaks()
+    sb = step_bytes(wl, R)
+    step_s = ms / 1e3 / K
+    lm_bytes = bd.dflash2_lmhead_bytes(h, R)
+    out = {"workload": wl.name, "requests_per_gpu": R, "weights": wl.weight_format, "steps": K,
+           "value": world * K / (ms / 1e3), "unit": "steps/s", "ms_per_step": ms / K,
+           "drafted_tokens_per_s": world * K / (ms / 1e3) * 7 * R,
+           "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
+           "lmhead": {"kernel": "wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel", "launch_ms": lm_ms,
+                      "achieved_gbs": lm_bytes / (lm_ms / 1e3) / 1e9,
+                      "frac": lm_bytes / (lm_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
+           "setup_s": setup_s}
+    del graph, drafter, S
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -321,6 +395,8 @@ def main_ours(args, rank, world, local_rank):
         "clocks": clk,
         "setup_s": setup_s,
     }
+    if args.config == 2 and not args.no_r16:
+        line["r16"] = measure_r16(args, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
         cb, _ = cpu_baseline(wl, W, inp, kc_host, vc_host, S["target"].cpu().numpy())
         line["cpu_baseline"] = cb

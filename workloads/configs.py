@@ -137,5 +137,15 @@ WORKLOADS[6] = Workload("profile_one_full_layer", Geometry("full_width_1layer", 
                         description="profiling: one full-width layer, vocab 16384, 1 request, ctx 1024")
 
 
+# Profiling-only workload for the tensor-core path: the same layer with 16 Q8 requests
+# (about 1 GB on the device).
+WORKLOADS[7] = Workload("profile_q8_r16_one_full_layer",
+                        Geometry("full_width_1layer", hidden=5120, n_layers=1, n_q_heads=32, n_kv_heads=8,
+                                 head_dim=128, ffn=17408, vocab=16384),
+                        "q8", 16, [512] * 16, [0.0, 0.7, 1.0, 0.0] * 4, [1.0] * 16, seed=7, philox_seed=42,
+                        philox_offsets=[r << 32 for r in range(16)],
+                        description="profiling: one full-width layer, vocab 16384, Q8, 16 requests, ctx 512")
+
+
 def workload(i: int) -> Workload:
     return WORKLOADS[i]
