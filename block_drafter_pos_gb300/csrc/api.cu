@@ -49,6 +49,9 @@ struct dflash2_handle {
   CUtensorMap map_lm, xm_lm;  // LM head weights; final hidden (bf16 in both formats) for the LM head
   int* gemv_err;  // device word set by a GEMV whose pipeline wait gave up
   unsigned int* verify_cnt;  // [max_req] verify chunk counters (zero between launches)
+  float* sel_lat;            // [max_req][7][16][16] selector lattice scratch
+  int32_t* sel_bad;          // [max_req][7] nonfinite flags per position
+  unsigned int* sel_cnt;     // [max_req] selector position counters (zero between launches)
   // scratch
   char* arena;
   size_t arena_bytes;
@@ -335,6 +338,9 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
       {reinterpret_cast<void**>(&h->gemv_err), 4},
       {reinterpret_cast<void**>(&h->verify_cnt), static_cast<size_t>(max_requests) * 4},
+      {reinterpret_cast<void**>(&h->sel_lat), static_cast<size_t>(max_requests) * 7 * 16 * 16 * 4},
+      {reinterpret_cast<void**>(&h->sel_bad), static_cast<size_t>(max_requests) * 7 * 4},
+      {reinterpret_cast<void**>(&h->sel_cnt), static_cast<size_t>(max_requests) * 4},
   };
   h->lo_a = N * h->H;
   h->lo_qkv = 2 * N * h->H;
@@ -845,6 +851,9 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   a.q_rows = q_rows;
   a.scores_out = scores_out;
   a.status = status;
+  a.lat = h->sel_lat;
+  a.bad = h->sel_bad;
+  a.counters = h->sel_cnt;
   a.rank = h->cfg.rank;
   a.fmt = h->fmt;
   a.V = h->V;

@@ -198,6 +198,9 @@ struct SelectArgs {
   float* q_rows;
   float* scores_out;           // [R][7][16][16] or null
   int32_t* status;
+  float* lat;                  // scratch [R][7][16][16]: the lattice's scores, one position per CTA
+  int32_t* bad;                // scratch [R][7]: nonfinite logit or score seen at that position
+  unsigned int* counters;      // [R] finished positions of the launch; zero before and after it
   int rank, fmt, V;
 };
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st);

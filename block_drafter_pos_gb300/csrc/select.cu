@@ -5,11 +5,13 @@
 // verified anchor, takes the argmax at T = 0 and an inverse-CDF draw from
 // softmax(score / T) at T > 0, and returns q over the 16 candidates.
 //
-// One CTA per request.  The full 7 x 16 x 16 lattice is scored first (position 1
-// from the anchor), one thread per (position, predecessor, candidate) pair over
-// padded shared-memory rows, then one warp walks it (lane j = candidate j).  Any nonfinite candidate logit or
-// score marks the request DFLASH2_E_NONFINITE ("LSE docs/DFLASH2.md": the
-// selector rejects nonfinite scores).
+// One CTA per (request, position): it stages the 16 predecessor rows of A (the
+// anchor's row at position 1) and the 16 candidate rows of B in shared memory and
+// scores its 16 x 16 edges, one thread per (predecessor, candidate), into a scratch
+// lattice.  The CTA that completes a request's seven positions (fenced atomic
+// ticket, no waiting) walks the lattice with one warp (lane j = candidate j).  Any
+// nonfinite candidate logit or score marks the request DFLASH2_E_NONFINITE ("LSE
+// docs/DFLASH2.md": the selector rejects nonfinite scores).
 #include <math.h>
 
 #include "common.cuh"
@@ -23,34 +25,32 @@ namespace {
 
 constexpr int kP = 7, kK = 16, kRank = 256;
 
-constexpr int kRowsA = 1 + (kP - 1) * kK;  // anchor + candidates of positions 1..6
-constexpr int kRowsB = kP * kK;            // candidates of positions 1..7
-constexpr int kRows = kRowsA + kRowsB;
-
 // Codebook rows staged in shared memory in their stored format: bf16 (256 x 2 B) or
-// Q8 codes (256 B) plus 4 groups of (scale, bias).
+// Q8 codes (256 B) plus 4 groups of (scale, bias).  Rows 0..15: predecessors (A),
+// 16..31: candidates (B).
 constexpr int kPadBf = kRank + 8;   // bf16 row stride: consecutive rows start 16 B apart mod 128 B
 constexpr int kPadQ8 = kRank + 16;  // int8 row stride, same idea
 
 struct SelSmem {
-  uint16_t bf[kRows][kPadBf];  // BF16 rows (unused for Q8)
-  int8_t q8[kRows][kPadQ8];    // Q8 codes (unused for BF16)
-  uint16_t sb[kRows][8];       // Q8: scale[4], bias[4]
-  float gate[kP][kRank];
-  float lat[kP][kK][kK];       // scores [position][pred][cand]
+  uint16_t bf[2 * kK][kPadBf];  // BF16 rows (unused for Q8)
+  int8_t q8[2 * kK][kPadQ8];    // Q8 codes (unused for BF16)
+  uint16_t sb[2 * kK][8];       // Q8: scale[4], bias[4]
+  float gate[kRank];
+  float cl[kK];
   int cids[kP][kK];
-  float cl[kP][kK];
+  float lat[kP][kK][kK];        // the walker's copy of the lattice
   int bad;
+  int last;
 };
 
-constexpr int kThreads = 512;
+constexpr int kThreads = kK * kK;  // one thread per (predecessor, candidate)
 
 DF2_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 DF2_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Edge score of predecessor row ra and candidate row rb at position i (without the unary term).
-DF2_DEV float edge_dot(const SelSmem& sm, int fmt, int i, int ra, int rb) {
-  const float* g = sm.gate[i];
+// Edge score of predecessor row ra and candidate row rb (without the unary term).
+DF2_DEV float edge_dot(const SelSmem& sm, int fmt, int ra, int rb) {
+  const float* g = sm.gate;
   float s = 0.f;
   if (fmt == 0) {
     const uint4* A = reinterpret_cast<const uint4*>(sm.bf[ra]);
@@ -92,53 +92,51 @@ DF2_DEV float edge_dot(const SelSmem& sm, int fmt, int i, int ra, int rb) {
 }
 
 __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  __shared__ __align__(16) SelSmem sm;
   pdl_begin();
-  const int r = blockIdx.x;
+  const int r = blockIdx.x, i = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (tid == 0) sm.bad = 0;
-  for (int e = tid; e < kP * kK; e += kThreads) {
-    sm.cids[e / kK][e % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + e], 0), a.V - 1);
-    const float v = a.cand_logits[static_cast<size_t>(r) * kP * kK + e];
-    sm.cl[e / kK][e % kK] = v;
+  // candidates of this position (and of the previous one: the predecessors)
+  if (tid < 2 * kK) {
+    const int pos = tid < kK ? i : i - 1;
+    if (pos >= 0) {
+      const int e = pos * kK + (tid % kK);
+      sm.cids[pos][tid % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + e], 0), a.V - 1);
+    }
+  }
+  if (tid < kK) {
+    const float v = a.cand_logits[(static_cast<size_t>(r) * kP + i) * kK + tid];
+    sm.cl[tid] = v;
     if (!isfinite(v)) atomicOr(&sm.bad, 1);
   }
-  for (int e = tid; e < kP * kRank; e += kThreads) sm.gate[e / kRank][e % kRank] = a.gate[static_cast<size_t>(r) * kP * kRank + e];
+  sm.gate[tid] = a.gate[(static_cast<size_t>(r) * kP + i) * kRank + tid];
   __syncthreads();
   const int anchor = min(max(a.anchor_ids[r], 0), a.V - 1);
-  // stage every needed codebook row at once (one round trip): row k < kRowsA is the
-  // predecessor row A[id], k >= kRowsA the successor row B[id]
+  const int n_pred = i == 0 ? 1 : kK;
+  // stage the rows (every thread's pieces loaded before any is stored): row k < 16
+  // the predecessor A[id], k >= 16 the candidate B[id]
   const int chunks = a.fmt == 0 ? kRank * 2 / 16 : kRank / 16;  // 16-byte pieces per row
-  // every thread's pieces are loaded first (all in flight together), then stored
-  constexpr int kPer = (kRows * kRank * 2 / 16 + kThreads - 1) / kThreads;
+  constexpr int kPer = (2 * kK * kRank * 2 / 16 + kThreads - 1) / kThreads;
   uint4 piece[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int e = tid + kThreads * j;
+    const int k = e / chunks, c = e % chunks;
     piece[j] = make_uint4(0, 0, 0, 0);
-    if (e < kRows * chunks) {
-      const int k = e / chunks, c = e % chunks;
-      int id;
-      const void* cb;
-      if (k < kRowsA) {
-        id = k == 0 ? anchor : sm.cids[(k - 1) / kK][(k - 1) % kK];
-        cb = a.cb_a;
-      } else {
-        id = sm.cids[(k - kRowsA) / kK][(k - kRowsA) % kK];
-        cb = a.cb_b;
-      }
+    if (k < 2 * kK && (k >= kK || k < n_pred)) {
+      const int id = k < kK ? (i == 0 ? anchor : sm.cids[i - 1][k]) : sm.cids[i][k - kK];
+      const void* cb = k < kK ? a.cb_a : a.cb_b;
       piece[j] = a.fmt == 0 ? ld_cached(reinterpret_cast<const uint16_t*>(cb) + static_cast<size_t>(id) * kRank + c * 8)
                             : ld_cached(reinterpret_cast<const int8_t*>(cb) + static_cast<size_t>(id) * kRank + c * 16);
     }
   }
-  if (a.fmt != 0) {  // Q8: 4 groups of (scale, bias) per row
-    for (int e = tid; e < kRows * 4; e += kThreads) {
-      const int k = e >> 2, c = e & 3;
-      const int id = k < kRowsA ? (k == 0 ? anchor : sm.cids[(k - 1) / kK][(k - 1) % kK])
-                                : sm.cids[(k - kRowsA) / kK][(k - kRowsA) % kK];
-      const uint16_t* sc = k < kRowsA ? a.cb_a_scale : a.cb_b_scale;
-      const uint16_t* bi = k < kRowsA ? a.cb_a_bias : a.cb_b_bias;
+  if (a.fmt != 0 && tid < 2 * kK * 4) {  // Q8: 4 groups of (scale, bias) per row
+    const int k = tid >> 2, c = tid & 3;
+    if (k >= kK || k < n_pred) {
+      const int id = k < kK ? (i == 0 ? anchor : sm.cids[i - 1][k]) : sm.cids[i][k - kK];
+      const uint16_t* sc = k < kK ? a.cb_a_scale : a.cb_b_scale;
+      const uint16_t* bi = k < kK ? a.cb_a_bias : a.cb_b_bias;
       sm.sb[k][c] = sc[static_cast<size_t>(id) * 4 + c];
       sm.sb[k][4 + c] = bi[static_cast<size_t>(id) * 4 + c];
     }
@@ -146,8 +144,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int e = tid + kThreads * j;
-    if (e < kRows * chunks) {
-      const int k = e / chunks, c = e % chunks;
+    const int k = e / chunks, c = e % chunks;
+    if (k < 2 * kK && (k >= kK || k < n_pred)) {
       if (a.fmt == 0)
         *reinterpret_cast<uint4*>(&sm.bf[k][c * 8]) = piece[j];
       else
@@ -155,36 +153,38 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     }
   }
   __syncthreads();
-  // lattice: one thread per (position, pred, cand)
-  const int n_pairs = kK + (kP - 1) * kK * kK;
-  for (int pc = tid; pc < n_pairs; pc += kThreads) {
-    int i, p, c;
-    if (pc < kK) {
-      i = 0;
-      p = 0;
-      c = pc;
-    } else {
-      const int e = pc - kK;
-      i = 1 + e / (kK * kK);
-      p = (e / kK) % kK;
-      c = e % kK;
-    }
-    const int ra = i == 0 ? 0 : 1 + (i - 1) * kK + p;
-    const int rb = kRowsA + i * kK + c;
-    const float s = edge_dot(sm, a.fmt, i, ra, rb) + sm.cl[i][c];
+  // edge (p, c): position 1 has the anchor as its only predecessor (the same row for every p)
+  {
+    const int p = tid / kK, c = tid % kK;
+    const float s = edge_dot(sm, a.fmt, i == 0 ? 0 : p, kK + c) + sm.cl[c];
     if (!isfinite(s)) atomicOr(&sm.bad, 1);
-    if (i == 0) {
-      for (int pp = 0; pp < kK; ++pp) sm.lat[0][pp][c] = s;
-    } else {
-      sm.lat[i][p][c] = s;
+    a.lat[((static_cast<size_t>(r) * kP + i) * kK + p) * kK + c] = s;
+  }
+  __syncthreads();
+  // the CTA completing this request's seven positions walks the lattice
+  if (tid == 0) {
+    a.bad[r * kP + i] = sm.bad;
+    __threadfence();
+    const unsigned int done = atomicAdd(&a.counters[r], 1u);
+    sm.last = done == kP - 1;
+    if (sm.last) {
+      a.counters[r] = 0;  // zero for the next launch
+      __threadfence();
     }
   }
   __syncthreads();
-  if (a.scores_out) {
-    for (int e = tid; e < kP * kK * kK; e += kThreads)
-      a.scores_out[static_cast<size_t>(r) * kP * kK * kK + e] = (&sm.lat[0][0][0])[e];
+  if (!sm.last) return;
+  int bad_any = 0;
+  for (int e = tid; e < kP * kK * kK; e += kThreads) {
+    const float v = __ldcg(a.lat + static_cast<size_t>(r) * kP * kK * kK + e);
+    (&sm.lat[0][0][0])[e] = v;
+    if (a.scores_out) a.scores_out[static_cast<size_t>(r) * kP * kK * kK + e] = v;
   }
-  const int bad = sm.bad;
+  if (tid < kP * kK) sm.cids[tid / kK][tid % kK] =
+      min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + tid], 0), a.V - 1);
+  if (tid < kP) bad_any = __ldcg(a.bad + r * kP + tid);
+  bad_any = __syncthreads_or(bad_any);
+  const int bad = bad_any;
   auto& lat = sm.lat;
   auto& cids = sm.cids;
   if (wid != 0) return;
@@ -248,14 +248,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  static bool attr_set = false;  // set once, outside any later stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(SelSmem)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return launch_ex(select_kernel, dim3(n_req), dim3(kThreads), sizeof(SelSmem), st, pdl, a);
+  if (a.rank != kRank) return cudaErrorInvalidValue;
+  return launch_ex(select_kernel, dim3(n_req, kP), dim3(kThreads), 0, st, pdl, a);
 }
 
 }  // namespace df2
