@@ -18,7 +18,8 @@ graph on the launching stream.  `cpu_baseline` times the oracle on the host.
 
 `r16` (default line only; `--no-r16` skips it) is the metric's second operating
 point, 16 requests (configuration 5: Q8 weights, ragged contexts 512..32768,
-mixed temperatures), timed the same way in the same process.
+mixed temperatures): its 100 consecutive steps with the emitted tokens appended
+between steps, captured as one graph in the same process.
 
 `--impl reference` times the CPU oracle (the only reference this method has
 here) on the same workload and prints the same line with "impl": "reference".
@@ -203,8 +204,11 @@ def run_step(bd, h, R, S, ev=None):
 
 def measure_r16(args, world, local_rank):
     """The metric's second operating point, 16 requests (configuration 5: Q8, ragged
-    contexts, mixed temperatures; the tensor-core path), timed the same way as the
-    main line: one CUDA graph of K steps after W eager warm-up steps, max over ranks."""
+    contexts, mixed temperatures; the tensor-core path): its 100 consecutive steps,
+    each draft + select + verify followed by the device-side state update
+    (dflash2_advance: the emitted tokens become the next step's anchor and new
+    context rows), captured as one CUDA graph after W eager warm-up steps; the
+    initial state is restored before each replay.  Max over ranks."""
     import torch
     import torch.distributed as dist
     import block_drafter_pos_gb300 as bd
@@ -214,10 +218,22 @@ def measure_r16(args, world, local_rank):
     R = wl.n_req
     drafter, S, _, _, _, _, setup_s = setup(wl, local_rank)
     h = drafter.handle
-    K = max(10, min(args.steps, 50))
-    for _ in range(max(3, args.warmup)):
+    K = wl.steps  # 100
+
+    def loop_step():
         run_step(bd, h, R, S)
+        bd.dflash2_advance(h, R, S["emitted"], S["n_emit"], S["anchors"], S["ctx_len"], S["n_new"], S["offsets"])
+
+    state0 = {k: S[k].clone() for k in ("anchors", "ctx_len", "n_new", "offsets")}
+
+    def restore():
+        for k, v in state0.items():
+            S[k].copy_(v)
+
+    for _ in range(max(3, args.warmup)):
+        loop_step()
     torch.cuda.synchronize()
+    restore()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, b in ev:
         a.record()
@@ -231,10 +247,13 @@ def measure_r16(args, world, local_rank):
         with torch.cuda.graph(graph, stream=cap_stream):
             for i in range(K):
                 bd.dflash2_set_lmhead_events(h, ev[i][0], ev[i][1])
-                run_step(bd, h, R, S)
+                loop_step()
     bd.dflash2_set_lmhead_events(h, None, None)
     stream.wait_stream(cap_stream)
+    restore()
     graph.replay()
+    torch.cuda.synchronize()
+    restore()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -250,6 +269,7 @@ def measure_r16(args, world, local_rank):
         ms = float(t.item())
     st = S["status"].cpu().numpy()
     assert np.all(st == 0), st
+    grown = int((S["ctx_len"] - state0["ctx_len"]).sum().item())  # context rows appended over the K steps
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     pk = peaks()
     sb = step_bytes(wl, R)
@@ -262,6 +282,7 @@ def measure_r16(args, world, local_rank):
            "lmhead": {"kernel": "wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel", "launch_ms": lm_ms,
                       "achieved_gbs": lm_bytes / (lm_ms / 1e3) / 1e9,
                       "frac": lm_bytes / (lm_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
+           "loop": f"{K} consecutive steps with the emitted tokens appended ({grown} context rows over all requests)",
            "setup_s": setup_s}
     del graph, drafter, S
     torch.cuda.synchronize()
@@ -283,14 +304,32 @@ def main_ours(args, rank, world, local_rank):
     h = drafter.handle
     K, Wm = args.steps, args.warmup
     stream = torch.cuda.current_stream()
+    # a workload of consecutive steps (configuration 5) appends each step's emitted
+    # tokens before the next (dflash2_advance); its initial state is restored before
+    # every replay
+    loop = wl.steps > 1
+    if loop:
+        K = min(K, wl.steps)
+    state0 = {k: S[k].clone() for k in ("anchors", "ctx_len", "n_new", "offsets")}
+
+    def restore():
+        for k, v in state0.items():
+            S[k].copy_(v)
+
+    def one_step():
+        run_step(bd, h, R, S)
+        if loop:
+            bd.dflash2_advance(h, R, S["emitted"], S["n_emit"], S["anchors"], S["ctx_len"], S["n_new"], S["offsets"])
+
     # warm-up (eager), then count launches of one step
     for _ in range(Wm):
-        run_step(bd, h, R, S)
+        one_step()
     torch.cuda.synchronize()
     n0 = bd.dflash2_launch_count(h)
-    run_step(bd, h, R, S)
+    one_step()
     launches_per_step = bd.dflash2_launch_count(h) - n0
     torch.cuda.synchronize()
+    restore()
     # one CUDA graph of exactly K steps, with the LM-head kernel bracketed by events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, b in ev:  # torch creates the CUDA events on first record; the graph re-records them
@@ -304,10 +343,13 @@ def main_ours(args, rank, world, local_rank):
         with torch.cuda.graph(graph, stream=cap_stream):
             for i in range(K):
                 bd.dflash2_set_lmhead_events(h, ev[i][0], ev[i][1])
-                run_step(bd, h, R, S)
+                one_step()
     bd.dflash2_set_lmhead_events(h, None, None)
     stream.wait_stream(cap_stream)
+    restore()
     graph.replay()  # warm replay (graph upload)
+    torch.cuda.synchronize()
+    restore()
     torch.cuda.synchronize()
     clocks = Clocks(local_rank)
     clocks.start()
@@ -334,6 +376,7 @@ def main_ours(args, rank, world, local_rank):
     st = S["status"].cpu().numpy()
     ne = S["n_emit"].cpu().numpy()
     assert np.all(st == 0) and np.all(ne >= 1), (st, ne)
+    restore()
 
     # end to end through the C ABI with host buffers
     E = args.e2e_steps
@@ -381,7 +424,9 @@ def main_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded, drafter geometry; random weights, no checkpoint)",
         "config": {"workload": wl.name, "requests_per_gpu": R, "context": wl.ctx[:R], "weights": wl.weight_format,
                    "temperature": wl.temps[:R], "l2": "inputs larger than L2 (weights stream every step)",
-                   "parallelism": f"{world} independent replica(s)", "timing": "one CUDA graph of K steps"},
+                   "parallelism": f"{world} independent replica(s)",
+                   "timing": ("one CUDA graph of K consecutive steps, emitted tokens appended between steps" if loop
+                              else "one CUDA graph of K steps")},
         "drafted_tokens_per_s": steps_per_s * 7 * R,
         "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
         "roofline": {"kernel": ("lmhead_kernel (LM head GEMV + fused top-16)" if R < (5 if wl.weight_format == "bf16" else 4) else

@@ -753,6 +753,23 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   return DFLASH2_OK;
 }
 
+dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* emitted, const int32_t* n_emitted,
+                               int32_t* anchor_ids, int32_t* ctx_len, int32_t* n_new, uint64_t* philox_offset,
+                               void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
+  if (!emitted || !n_emitted || !anchor_ids || !ctx_len || !n_new || !philox_offset) return DFLASH2_E_INVAL;
+  AdvanceArgs a = {};
+  a.emitted = emitted;
+  a.n_emitted = n_emitted;
+  a.anchor_ids = anchor_ids;
+  a.ctx_len = ctx_len;
+  a.n_new = n_new;
+  a.offset = philox_offset;
+  DF2_CHECK(launch_advance(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
+  h->launches++;
+  return DFLASH2_OK;
+}
+
 dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
                                  float* cand_logits, float* logits_out, void* stream) {
   if (!h || n_rows < 8 || n_rows % 8 || n_rows > 8 * h->max_req) return DFLASH2_E_INVAL;

@@ -306,7 +306,25 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
   }
 }
 
+// ------------------------------------------------------------------ serving-loop state update
+// One thread per request: the rows appended this step become context, the last
+// emitted token the next anchor, the emitted tokens the next new rows.
+__global__ void __launch_bounds__(32) advance_kernel(const AdvanceArgs a, int n_req) {
+  pdl_begin();
+  const int r = blockIdx.x * 32 + threadIdx.x;
+  if (r >= n_req) return;
+  const int ne = min(max(a.n_emitted[r], 0), kB);
+  a.ctx_len[r] += min(max(a.n_new[r], 0), kB);
+  if (ne > 0) a.anchor_ids[r] = a.emitted[r * kB + ne - 1];
+  a.n_new[r] = ne;
+  a.offset[r] += 1;
+}
+
 }  // namespace
+
+cudaError_t launch_advance(const AdvanceArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  return launch_ex(advance_kernel, dim3((n_req + 31) / 32), dim3(32), 0, st, pdl, a, n_req);
+}
 
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st) {
   return launch_ex(start_kernel, dim3(n_req, (a.H + a.n_taps * a.H) / kCw), dim3(kThreads), 0, st, pdl, a);

@@ -231,4 +231,15 @@ struct VerifyArgs {
 };
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st);
 
+// ---------------------------------------------------------------- serving-loop state update
+struct AdvanceArgs {
+  const int32_t* emitted;   // [R][8]
+  const int32_t* n_emitted; // [R]
+  int32_t* anchor_ids;      // [R] in/out
+  int32_t* ctx_len;         // [R] in/out
+  int32_t* n_new;           // [R] in/out
+  uint64_t* offset;         // [R] in/out
+};
+cudaError_t launch_advance(const AdvanceArgs& a, int n_req, bool pdl, cudaStream_t st);
+
 }  // namespace df2

@@ -191,6 +191,21 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
                               const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
                               int32_t* emitted, int32_t* n_emitted, int32_t* status, void* stream);
 
+/* Serving-loop state update after dflash2_verify, on the device (so a multi-step
+ * loop can be captured in one graph).  For each request r:
+ *   ctx_len[r] += n_new[r]          the rows this step appended are now context
+ *   if n_emitted[r] > 0: anchor_ids[r] = emitted[r][n_emitted[r] - 1]
+ *   n_new[r] = n_emitted[r]          the emitted tokens are the next step's new rows
+ *   philox_offset[r] += 1            a fresh Philox counter range for the next step
+ * A request that verify skipped or rejected (n_emitted = 0) keeps its anchor and
+ * appends nothing next step.  The caller supplies the next step's taps for the new
+ * rows and keeps ctx_len + block <= kv_capacity.
+ *   anchor_ids, ctx_len, n_new [R] int32 in/out; philox_offset [R] uint64 in/out;
+ *   emitted [R][block], n_emitted [R] int32 (dflash2_verify's outputs). */
+dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* emitted, const int32_t* n_emitted,
+                               int32_t* anchor_ids, int32_t* ctx_len, int32_t* n_new, uint64_t* philox_offset,
+                               void* stream);
+
 /* LM head + top-16 alone (step a8 on given final hidden states): logits of block
  * positions 1..7 = W_lm . hidden (hidden already normalised, BF16), top-16 with the
  * ordering of dflash2_draft_block.  Row n of `hidden` is request n/8, block position

@@ -436,6 +436,19 @@ def _inverse_cdf(w: np.ndarray, u: float):
 
 # ----------------------------------------------------------------------------- one step
 
+def advance(ctx_len: int, n_new: int, anchor: int, emitted: Sequence[int], n_emitted: int, offset: int):
+    """Request state for the next draft + verify step ([LSE] block paragraph: every
+    draft is an anchor plus seven masks; [VLLM] PR description, candidate selector:
+    the walk starts at the verified anchor).  Reading: the rows appended this step
+    become context; the tokens verify emitted are the next step's new context rows,
+    the last of them the next anchor; each step draws from its own Philox counter
+    range, the offset advanced by one.  A request with nothing emitted keeps its
+    anchor and appends nothing.  Returns (ctx_len, n_new, anchor, offset)."""
+    ne = max(0, min(int(n_emitted), 8))
+    nxt_anchor = int(emitted[ne - 1]) if ne > 0 else int(anchor)
+    return int(ctx_len) + max(0, min(int(n_new), 8)), ne, nxt_anchor, int(offset) + 1
+
+
 def step(g, W: Dict, anchor: int, ctx_len: int, n_new: int, taps, k_cache, v_cache,
          temperature: float, seed: int, offset: int, target_logits_fn) -> Dict:
     """draft_block + top-16 + walk + verify for one request.  target_logits_fn maps the

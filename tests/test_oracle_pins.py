@@ -560,3 +560,19 @@ def test_philox_structure():
     assert len(outs) == 2000
     u = [philox.uniform(42, 0, s, p) for s in range(8) for p in range(3)]
     assert all(0.0 <= x < 1.0 for x in u) and len(set(u)) == 24
+
+
+def test_advance_worked_examples():
+    """The serving-loop state update on hand-worked cases: the appended rows become
+    context, the last emitted token the next anchor, the emitted tokens the next new
+    rows, the Philox offset advances by one; nothing emitted keeps the anchor."""
+    assert oracle.advance(100, 8, 5, [11, 12, 13, -1, -1, -1, -1, -1], 3, 7) == (108, 3, 13, 8)
+    assert oracle.advance(108, 3, 13, [-1] * 8, 0, 8) == (111, 0, 13, 9)          # verify emitted nothing
+    assert oracle.advance(0, 0, 2, [4, 5, 6, 7, 8, 9, 10, 11], 8, 1 << 32) == (0, 8, 11, (1 << 32) + 1)
+    # a whole loop: context grows by the previous step's emitted count
+    ctx, nn, anc, off = 50, 8, 1, 0
+    for ne in (2, 8, 1, 0, 5):
+        ctx_before, nn_before = ctx, nn
+        ctx, nn, anc, off = oracle.advance(ctx, nn, anc, list(range(100, 108)), ne, off)
+        assert ctx == ctx_before + nn_before and nn == ne
+    assert (ctx, nn, anc, off) == (50 + 8 + 2 + 8 + 1 + 0, 5, 104, 5)
