@@ -393,13 +393,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  static bool attr_set = false;  // set once, outside any later stream capture
+  static std::atomic<unsigned long long> attr_done{0};
   const size_t smem = sizeof(CtxSmem) > sizeof(BlkSmem) ? sizeof(CtxSmem) : sizeof(BlkSmem);
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  {
+    const cudaError_t e = set_smem_once(attn_chunk_kernel, static_cast<int>(smem), attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaError_t e = launch_ex(attn_chunk_kernel, dim3(n_req * a.n_kv_heads, a.n_chunks), dim3(256), smem, st, pdl, a);
   if (e != cudaSuccess) return e;

@@ -403,12 +403,9 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* p,
 template <int NT, int FMT>
 cudaError_t launch_nt(const GemvArgs& a, int ctas, bool pdl, cudaStream_t st) {
   constexpr int smem = StageGeo<FMT, NT>::kSmem;
-  static bool attr_set = false;  // set once, outside any later stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t e = set_smem_once(gemv_kernel<NT, FMT>, smem, attr_done);
+  if (e != cudaSuccess) return e;
   return launch_ex(gemv_kernel<NT, FMT>, dim3(ctas), dim3(kThreads), smem, st, pdl, a);
 }
 

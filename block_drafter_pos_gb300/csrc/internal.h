@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace df2 {
 
 constexpr int kMaxSeg = 4;
@@ -102,6 +104,21 @@ cudaError_t launch_wide(GemvArgs& a, int fmt, int num_sms, bool pdl, cudaStream_
 // fmt: 0 = BF16 weights, 1 = Q8G64 weights.  max_tiles: largest n_tiles over segments.
 // pdl: launch with programmatic stream serialisation.
 cudaError_t launch_gemv(GemvArgs& a, int fmt, int max_tiles, int num_sms, bool pdl, cudaStream_t st);
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once per
+// (call site, device): the attribute belongs to a device, so a process driving
+// several GPUs sets it on each.  `done` is the call site's set of devices (bit d).
+template <typename Kern>
+cudaError_t set_smem_once(Kern kern, int smem, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Launch helper: cudaLaunchKernelEx with the programmatic stream serialisation
 // attribute when pdl is set.

@@ -424,12 +424,9 @@ __global__ void __launch_bounds__(256) logits_topk_kernel(const LogitsTopkArgs a
 template <int NT, bool LO>
 cudaError_t launch_nt(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
   constexpr int smem = StageGeo<0, NT>::kSmem;
-  static bool attr_set = false;  // set once, outside any later stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<NT, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t e = set_smem_once(lmhead_kernel<NT, LO>, smem, attr_done);
+  if (e != cudaSuccess) return e;
   return launch_ex(lmhead_kernel<NT, LO>, dim3(a.n_cta), dim3(kThreads), smem, st, pdl, a);
 }
 

@@ -484,12 +484,9 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
 template <int FMT, int NMAX>
 cudaError_t launch_fmt(const GemvArgs& a, int ctas, bool pdl, cudaStream_t st) {
   constexpr int smem = WideGeo<FMT, NMAX>::kSmem;
-  static bool attr_set = false;  // set once, outside any later stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(wide_kernel<FMT, NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t e = set_smem_once(wide_kernel<FMT, NMAX>, smem, attr_done);
+  if (e != cudaSuccess) return e;
   return launch_ex(wide_kernel<FMT, NMAX>, dim3(ctas), dim3(WideGeo<FMT, NMAX>::kWarps * 32), smem, st, pdl, a);
 }
 
