@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
 // the entries >= the largest such T are candidates; one warp ranks those.  If the
 // candidates overflow the buffer (few distinct values, e.g. a chunk past the
 // vocabulary's end), every warp ranks its own entries and warp 0 merges.
-__global__ void __launch_bounds__(256) logits_topk_kernel(const LogitsTopkArgs a) {
+__global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArgs a) {
   constexpr int kCap = 1024;
   __shared__ unsigned long long cand[kCap];
   __shared__ unsigned long long wthr[8];
