@@ -49,7 +49,7 @@ METRIC = "DFlash2 draft+verify steps/s at 1 and 16 req; achieved HBM GB/s vs pea
 LMHEAD_TRAFFIC = {(248320, 5120, 1): 2.54e9 + 2.87e6}
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=400)
@@ -60,7 +60,33 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=100)
     p.add_argument("--no-r16", action="store_true",
                    help="skip the 16-request measurement that rides along the default line")
-    return p.parse_args()
+    return p.parse_args(argv)
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of each rank's value (a time: the job takes as long as its slowest
+    replica).  Works on a process group of either backend (nccl: a device tensor)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sync_ranks(world: int) -> None:
+    """Barrier across the replicas (no-op for one rank)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank units, the job took
+    the slowest rank's time (weak scaling: per-rank work fixed as ranks grow)."""
+    return world * units_per_rank / (ms_max / 1e3)
 
 
 def peaks():
@@ -255,18 +281,13 @@ def measure_r16(args, world, local_rank):
     torch.cuda.synchronize()
     restore()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    sync_ranks(world)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     graph.replay()
     t1.record()
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
     st = S["status"].cpu().numpy()
     assert np.all(st == 0), st
     grown = int((S["ctx_len"] - state0["ctx_len"]).sum().item())  # context rows appended over the K steps
@@ -276,8 +297,8 @@ def measure_r16(args, world, local_rank):
     step_s = ms / 1e3 / K
     lm_bytes = bd.dflash2_lmhead_bytes(h, R)
     out = {"workload": wl.name, "requests_per_gpu": R, "weights": wl.weight_format, "steps": K,
-           "value": world * K / (ms / 1e3), "unit": "steps/s", "ms_per_step": ms / K,
-           "drafted_tokens_per_s": world * K / (ms / 1e3) * 7 * R,
+           "value": job_rate(K, world, ms), "unit": "steps/s", "ms_per_step": ms / K,
+           "drafted_tokens_per_s": job_rate(K, world, ms) * 7 * R,
            "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
            "lmhead": {"kernel": "wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel", "launch_ms": lm_ms,
                       "achieved_gbs": lm_bytes / (lm_ms / 1e3) / 1e9,
@@ -354,24 +375,18 @@ def main_ours(args, rank, world, local_rank):
     clocks = Clocks(local_rank)
     clocks.start()
     time.sleep(0.15)
-    if world > 1:
-        dist.barrier()
+    sync_ranks(world)
     torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record()
     graph.replay()
     t_end.record()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    sync_ranks(world)
     clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     lm_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    steps_per_s = world * K / (ms / 1e3)
+    steps_per_s = job_rate(K, world, ms)
     # sanity of the timed outputs
     st = S["status"].cpu().numpy()
     ne = S["n_emit"].cpu().numpy()
@@ -396,20 +411,15 @@ def main_ours(args, rank, world, local_rank):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    sync_ranks(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(E):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * E / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_val = job_rate(E, world, e2e_ms)
 
     pk = peaks()
     lm_bytes = bd.dflash2_lmhead_bytes(h, R)
