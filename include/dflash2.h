@@ -192,7 +192,9 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
                               int32_t* emitted, int32_t* n_emitted, int32_t* status, void* stream);
 
 /* Serving-loop state update after dflash2_verify, on the device (so a multi-step
- * loop can be captured in one graph).  For each request r:
+ * loop can be captured in one graph; "LSE docs/DFLASH2.md", block paragraph: each
+ * draft is an anchor plus seven masks; vLLM PR #52816 description, candidate
+ * selector: the walk starts at the verified anchor).  For each request r:
  *   ctx_len[r] += n_new[r]          the rows this step appended are now context
  *   if n_emitted[r] > 0: anchor_ids[r] = emitted[r][n_emitted[r] - 1]
  *   n_new[r] = n_emitted[r]          the emitted tokens are the next step's new rows
@@ -201,7 +203,10 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
  * appends nothing next step.  The caller supplies the next step's taps for the new
  * rows and keeps ctx_len + block <= kv_capacity.
  *   anchor_ids, ctx_len, n_new [R] int32 in/out; philox_offset [R] uint64 in/out;
- *   emitted [R][block], n_emitted [R] int32 (dflash2_verify's outputs). */
+ *   emitted [R][block], n_emitted [R] int32 (dflash2_verify's outputs).
+ * All device pointers, caller-owned; asynchronous on `stream`.  Returns
+ * DFLASH2_E_INVAL for a null pointer or n_req outside 1..max_requests (nothing is
+ * launched), DFLASH2_E_CUDA if the launch fails. */
 dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* emitted, const int32_t* n_emitted,
                                int32_t* anchor_ids, int32_t* ctx_len, int32_t* n_new, uint64_t* philox_offset,
                                void* stream);
