@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
         L.dflash2_select.argtypes = [vp, i32] + [vp] * 12
         L.dflash2_verify.argtypes = [vp, i32] + [vp] * 12
         L.dflash2_advance.argtypes = [vp, i32] + [vp] * 7
+        L.dflash2_set_select_mode.argtypes = [vp, i32]
         L.dflash2_head_topk.argtypes = [vp, i32] + [vp] * 5
         L.dflash2_head_topk.restype = i32
         L.dflash2_head_topk_noalloc.argtypes = [vp, i32, i32, i32] + [vp] * 5
@@ -76,7 +77,7 @@ def lib() -> ctypes.CDLL:
         L.dflash2_status_string.argtypes = [i32]
         L.dflash2_status_string.restype = ctypes.c_char_p
         for f in ("dflash2_create", "dflash2_destroy", "dflash2_draft_block", "dflash2_select", "dflash2_verify",
-                  "dflash2_advance",
+                  "dflash2_advance", "dflash2_set_select_mode",
                   "dflash2_set_lmhead_events"):
             getattr(L, f).restype = i32
         _lib = L
@@ -142,6 +143,10 @@ def dflash2_verify(h, n_req, target_logits, path, cand_ids, q_rows, temperature,
     _check(lib().dflash2_verify(h, n_req, _p(target_logits), _p(path), _p(cand_ids), _p(q_rows), _p(temperature),
                                 _p(seed), _p(philox_offset), _p(n_accepted), _p(emitted), _p(n_emitted), _p(status),
                                 _stream(stream)), "dflash2_verify")
+
+
+def dflash2_set_select_mode(h, mode: int):
+    _check(lib().dflash2_set_select_mode(h, mode), "dflash2_set_select_mode")
 
 
 def dflash2_advance(h, n_req, emitted, n_emitted, anchor_ids, ctx_len, n_new, philox_offset, stream=None):

@@ -52,6 +52,7 @@ struct dflash2_handle {
   float* sel_lat;            // [max_req][7][16][16] selector lattice scratch
   int32_t* sel_bad;          // [max_req][7] nonfinite flags per position
   unsigned int* sel_cnt;     // [max_req] selector position counters (zero between launches)
+  int select_mode;           // 0: sequential walk, 1: Viterbi for greedy requests
   // scratch
   char* arena;
   size_t arena_bytes;
@@ -753,6 +754,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   return DFLASH2_OK;
 }
 
+dflash2_status dflash2_set_select_mode(dflash2_handle* h, int32_t mode) {
+  if (!h || mode < 0 || mode > 1) return DFLASH2_E_INVAL;
+  h->select_mode = mode;
+  return DFLASH2_OK;
+}
+
 dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* emitted, const int32_t* n_emitted,
                                int32_t* anchor_ids, int32_t* ctx_len, int32_t* n_new, uint64_t* philox_offset,
                                void* stream) {
@@ -871,6 +878,7 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   a.lat = h->sel_lat;
   a.bad = h->sel_bad;
   a.counters = h->sel_cnt;
+  a.mode = h->select_mode;
   a.rank = h->cfg.rank;
   a.fmt = h->fmt;
   a.V = h->V;

@@ -202,6 +202,7 @@ struct SelectArgs {
   int32_t* bad;                // scratch [R][7]: nonfinite logit or score seen at that position
   unsigned int* counters;      // [R] finished positions of the launch; zero before and after it
   int rank, fmt, V;
+  int mode;                    // 0: sequential walk; 1: globally best path (Viterbi) for greedy requests
 };
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st);
 

@@ -39,6 +39,7 @@ struct SelSmem {
   float cl[kK];
   int cids[kP][kK];
   float lat[kP][kK][kK];        // the walker's copy of the lattice
+  uint8_t back[kP][kK];         // Viterbi: best predecessor of each candidate
   int bad;
   int last;
 };
@@ -198,8 +199,53 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     if (lane == 0) a.status[r] = (T >= 0.f) ? 2 : 1;
     return;
   }
-  const uint64_t seed = a.seed[r], off = a.offset[r];
   const bool live = lane < kK;
+  if (T == 0.f && a.mode == 1) {
+    // globally best path: best_1(c) = s_1(c); best_i(c) = max_p best_{i-1}(p) + s_i(p, c)
+    // (float32 sums; equal -> the predecessor with the smaller id), then read back
+    float best = live ? lat[0][0][lane] : -INFINITY;
+    for (int i = 1; i < kP; ++i) {
+      float nb = -INFINITY;
+      int bp = 0, bid = 0x7FFFFFFF;
+      for (int p = 0; p < kK; ++p) {
+        const float bpv = __shfl_sync(0xffffffffu, best, p);
+        if (live) {
+          const float v = bpv + lat[i][p][lane];
+          const int pid = cids[i - 1][p];
+          if (v > nb || (v == nb && pid < bid)) {
+            nb = v;
+            bp = p;
+            bid = pid;
+          }
+        }
+      }
+      if (live) sm.back[i][lane] = static_cast<uint8_t>(bp);
+      best = live ? nb : -INFINITY;
+    }
+    // the end of the path: argmax over candidates, equal -> smaller id
+    float bv = best;
+    int bi = lane, bc = live ? cids[kP - 1][lane] : 0x7FFFFFFF;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o), oc = __shfl_xor_sync(0xffffffffu, bc, o);
+      if (ov > bv || (ov == bv && oc < bc)) {
+        bv = ov;
+        bi = oi;
+        bc = oc;
+      }
+    }
+    __syncwarp();
+    int c = bi;
+    for (int i = kP - 1; i >= 0; --i) {  // read back through the recorded predecessors
+      if (live) qrow[i * kK + lane] = lane == c ? 1.f : 0.f;
+      if (lane == 0) path[i] = cids[i][c];
+      c = i > 0 ? sm.back[i][c] : 0;
+    }
+    if (lane == 0) a.status[r] = 0;
+    return;
+  }
+  const uint64_t seed = a.seed[r], off = a.offset[r];
   int prev = 0;
   for (int i = 0; i < kP; ++i) {
     const float sj = live ? lat[i][prev][lane] : -INFINITY;

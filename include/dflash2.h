@@ -173,6 +173,17 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
                               const float* temperature, const uint64_t* seed, const uint64_t* philox_offset,
                               int32_t* path, float* q_rows, float* scores_out, int32_t* status, void* stream);
 
+/* Selector mode of the handle's later dflash2_select calls (an ablation of the
+ * walk; vLLM PR #52816 description: "walk the best path from the verified anchor").
+ *   0 (default): the sequential walk above.
+ *   1: for greedy requests (temperature 0) the globally best path instead, the
+ *      path of highest total edge score over the 16^7 candidate sequences, by
+ *      dynamic programming with float32 sums (equal sums -> the predecessor with
+ *      the smaller id; equal ends -> the smaller id); q rows one-hot.  Requests with
+ *      temperature > 0 still walk and sample.
+ * Returns DFLASH2_E_INVAL for another mode. */
+dflash2_status dflash2_set_select_mode(dflash2_handle* h, int32_t mode);
+
 /* Verification (step a11; "LSE docs/DFLASH2.md", first paragraph).
  *   target_logits [R][block][V] float32: row j is the target's distribution for
  *   block position j+1 (row block-1 = the bonus position).

@@ -352,6 +352,45 @@ def walk(g, cb_a, cb_b, anchor: int, cand_ids: np.ndarray, cand_logits: np.ndarr
     return {"path": path, "q_rows": q_rows, "scores": scores, "status": status, "margins": margins}
 
 
+def viterbi_path(scores: np.ndarray, cand_ids: np.ndarray) -> Dict:
+    """Globally best path through the selector lattice, the ablation of the
+    sequential walk ([VLLM] PR description: walk the best path from the verified
+    anchor, read here as the path of highest total edge score).  scores [P][K][K] =
+    s_i(p -> c), position 1's rows all from the anchor; cand_ids [P][K].
+
+    Dynamic programming over positions (Viterbi): best_1(c) = s_1(c);
+    best_i(c) = max_p best_{i-1}(p) + s_i(p, c), equal sums -> the predecessor with
+    the smaller vocabulary id; the path ends at argmax_c best_P(c) (equal -> smaller
+    id) and is read back through the recorded predecessors.  The decision is taken
+    on float32 scores with float32 sums in this order (the kernel's precision).
+    Returns dict(index int[P] into the candidates, path int32[P] vocabulary ids,
+    q_rows one-hot [P][K], total float32)."""
+    P, K = cand_ids.shape
+    s32 = np.asarray(scores, np.float32)
+    best = s32[0, 0].copy()
+    back = np.zeros((P, K), np.int64)
+    for i in range(1, P):
+        nb = np.empty(K, np.float32)
+        for c in range(K):
+            v = (best + s32[i, :, c]).astype(np.float32)   # float32 sums
+            top = v.max()
+            tied = [p for p in range(K) if v[p] == top]
+            p = min(tied, key=lambda pp: cand_ids[i - 1, pp])
+            nb[c] = v[p]
+            back[i, c] = p
+        best = nb
+    top = best.max()
+    c = min((cc for cc in range(K) if best[cc] == top), key=lambda cc: cand_ids[P - 1, cc])
+    index = np.zeros(P, np.int64)
+    for i in range(P - 1, -1, -1):
+        index[i] = c
+        c = back[i, c]
+    q_rows = np.zeros((P, K))
+    q_rows[np.arange(P), index] = 1.0
+    return {"index": index, "path": cand_ids[np.arange(P), index].astype(np.int32), "q_rows": q_rows,
+            "total": np.float32(top)}
+
+
 # ----------------------------------------------------------------------------- verify
 
 def verify(target_logits: np.ndarray, path: np.ndarray, cand_ids: np.ndarray, q_rows: np.ndarray,

@@ -274,3 +274,42 @@ def test_head_topk_exact_integer_logits_with_ties_nan_inf():
         lg = logits.cpu().numpy()[0, i - 1]
         fin = np.isfinite(ref)
         assert np.array_equal(lg[fin], ref[fin].astype(np.float32))
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_select_viterbi_mode_matches_oracle(integer):
+    """Selector mode 1: greedy requests take the globally best path.  The oracle's
+    dynamic program on the GPU's own lattice (float32 sums in the kernel's order)
+    gives the same path exactly; its total is never below the sequential walk's;
+    requests with T > 0 still walk and sample."""
+    R, V = 4, 8192
+    temps = [0.0, 0.0, 0.7, 0.0]
+    si, W, wl = _select_case(V, R, 21, integer, temps)
+    step = GpuStep(wl, W)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    seeds = np.array([42, 43, 44, 45], np.uint64)
+    offs = np.array([0, 1 << 32, 2 << 32, 3 << 32], np.uint64)
+    args = (t(si["anchors"]), t(np.array(temps, np.float32)), t(seeds.view(np.int64)), t(offs.view(np.int64)),
+            t(si["cand_ids"]), t(si["cand_logits"]), t(si["gate"]))
+    step.select(*args)
+    torch.cuda.synchronize()
+    walk_path = step.path.cpu().numpy().copy()
+    bd.dflash2_set_select_mode(step.drafter.handle, 1)
+    step.select(*args)
+    torch.cuda.synchronize()
+    bd.dflash2_set_select_mode(step.drafter.handle, 0)
+    path, q = step.path.cpu().numpy(), step.q_rows.cpu().numpy()
+    scores = step.scores.cpu().numpy()
+    st = step.status.cpu().numpy()
+    for r in range(R):
+        assert st[r] == 0
+        if temps[r] == 0.0:
+            ref = oracle.viterbi_path(scores[r], si["cand_ids"][r])
+            assert np.array_equal(path[r], ref["path"]), r
+            assert np.array_equal(q[r], ref["q_rows"].astype(np.float32))
+            idx_w = [int(np.nonzero(si["cand_ids"][r, i] == walk_path[r, i])[0][0]) for i in range(7)]
+            s32 = scores[r].astype(np.float32)
+            tot_w = s32[0, 0, idx_w[0]] + sum(s32[i, idx_w[i - 1], idx_w[i]] for i in range(1, 7))
+            assert ref["total"] >= tot_w - 1e-4 * max(1.0, abs(float(tot_w)))
+        else:
+            assert np.array_equal(path[r], walk_path[r])  # sampled requests are unaffected by the mode

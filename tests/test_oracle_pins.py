@@ -576,3 +576,34 @@ def test_advance_worked_examples():
         ctx, nn, anc, off = oracle.advance(ctx, nn, anc, list(range(100, 108)), ne, off)
         assert ctx == ctx_before + nn_before and nn == ne
     assert (ctx, nn, anc, off) == (50 + 8 + 2 + 8 + 1 + 0, 5, 104, 5)
+
+
+def test_viterbi_path_brute_force_and_examples():
+    """The Viterbi selector on small lattices: its path is the one of highest total
+    score over all K^P paths (brute force, tie-free random scores), greedy and Viterbi
+    differ on a hand-made lattice, and equal totals go to smaller candidate ids."""
+    import itertools
+    rng = np.random.default_rng(77)
+    for trial in range(20):
+        P, K = 4, 5
+        sc = rng.normal(0, 1, (P, K, K))
+        sc[0] = np.repeat(sc[0, :1], K, axis=0)          # position 1: every row from the anchor
+        ids = np.stack([rng.permutation(100)[:K] for _ in range(P)]).astype(np.int32)
+        res = oracle.viterbi_path(sc, ids)
+        s32 = sc.astype(np.float32)
+        best, arg = None, None
+        for path in itertools.product(range(K), repeat=P):
+            tot = s32[0, 0, path[0]] + sum(s32[i, path[i - 1], path[i]] for i in range(1, P))
+            if best is None or tot > best:
+                best, arg = tot, path
+        assert tuple(res["index"]) == arg
+        assert abs(float(res["total"]) - float(best)) <= 1e-5 * max(1.0, abs(float(best)))
+    # greedy takes 1.0 then 0 (total 1.0); the best path takes 0.9 then 5 (total 5.9)
+    sc = np.zeros((2, 2, 2))
+    sc[0] = [[1.0, 0.9], [1.0, 0.9]]
+    sc[1] = [[0.0, 0.0], [5.0, 0.0]]
+    ids = np.array([[10, 20], [30, 40]], np.int32)
+    assert list(oracle.viterbi_path(sc, ids)["path"]) == [20, 30]
+    # all-equal scores: the smallest ids at every position
+    ids = np.array([[7, 3, 9], [5, 2, 8], [6, 1, 4]], np.int32)
+    assert list(oracle.viterbi_path(np.zeros((3, 3, 3)), ids)["path"]) == [3, 2, 1]
