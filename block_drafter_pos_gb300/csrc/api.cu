@@ -465,6 +465,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.nch = h->nch_ss;
     a.fmt = fmt;
     a.V = h->V;
+    a.pipe_err = h->gemv_err;
     DF2_CHECK(launch_start(a, R, pdl, st));
     h->launches++;
   }
@@ -879,6 +880,7 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   a.bad = h->sel_bad;
   a.counters = h->sel_cnt;
   a.mode = h->select_mode;
+  a.pipe_err = h->gemv_err;
   a.rank = h->cfg.rank;
   a.fmt = h->fmt;
   a.V = h->V;

@@ -89,6 +89,9 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
             (i < nn) ? a.taps[idx] : 0.f);
   }
   pdl_wait();
+  // a new step: the previous step's select has read the error word by now (it ran
+  // before the previous verify, whose completion the wait above implies)
+  if (a.pipe_err != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.pipe_err = 0;
 }
 
 // ------------------------------------------------------------------ taps projection finish

@@ -27,6 +27,7 @@ struct StartArgs {
   size_t act_taps_lo;
   int H, n_taps, mask_id, nch, fmt, V;
   int tiled_a, tiled_taps;  // > 0: tensor-core operand layout with that many rows per slice (act_offset)
+  int* pipe_err;            // the step's weight-pipeline error word, cleared here (may be NULL)
 };
 
 struct FcFinishArgs {
@@ -203,6 +204,7 @@ struct SelectArgs {
   unsigned int* counters;      // [R] finished positions of the launch; zero before and after it
   int rank, fmt, V;
   int mode;                    // 0: sequential walk; 1: globally best path (Viterbi) for greedy requests
+  const int* pipe_err;         // nonzero: a pipeline wait of the step's draft gave up (may be NULL)
 };
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st);
 

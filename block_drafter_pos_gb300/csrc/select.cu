@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     if (!isfinite(s)) atomicOr(&sm.bad, 1);
     a.lat[((static_cast<size_t>(r) * kP + i) * kK + p) * kK + c] = s;
   }
+  __threadfence();  // every writer's lattice scores visible device-wide before the ticket
   __syncthreads();
   // the CTA completing this request's seven positions walks the lattice
   if (tid == 0) {
@@ -193,10 +194,12 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   const float T = a.temperature[r];
   int32_t* path = a.path + static_cast<size_t>(r) * kP;
   float* qrow = a.q_rows + static_cast<size_t>(r) * kP * kK;
-  if (!(T >= 0.f) || bad) {
+  // a weight-pipeline wait of this step's draft that gave up leaves its candidates undefined
+  const bool pipe_bad = a.pipe_err != nullptr && __ldcg(a.pipe_err) != 0;
+  if (!(T >= 0.f) || bad || pipe_bad) {
     if (lane < kP) path[lane] = -1;
     for (int e = lane; e < kP * kK; e += 32) qrow[e] = 0.f;
-    if (lane == 0) a.status[r] = (T >= 0.f) ? 2 : 1;
+    if (lane == 0) a.status[r] = pipe_bad ? 3 : (T >= 0.f) ? 2 : 1;
     return;
   }
   const bool live = lane < kK;

@@ -22,7 +22,8 @@
  *   - Errors the host can see (bad sizes, NULL pointers, misalignment) return
  *     DFLASH2_E_INVAL before anything is launched.  A launch failure returns
  *     DFLASH2_E_CUDA.  Errors found on the device (a NaN or +inf logit or
- *     selector score) go to the per-request `status` words; such a request gets
+ *     selector score; a bounded wait of a weight-streaming pipeline that gave up)
+ *     go to the per-request `status` words; such a request gets
  *     n_accepted = n_emitted = 0.
  *   - One handle serves one stream at a time (its scratch is shared by calls).
  *   - Integers are int32 unless stated; BF16 is stored as 16-bit patterns.
@@ -152,7 +153,9 @@ dflash2_status dflash2_destroy(dflash2_handle* h);
  *   gate [R][block-1][rank] float32  selector projection of the final hidden state
  *   logits_out [R][block-1][V] float32 or NULL: full drafter logits (debugging,
  *                        test harness)
- * Requires ctx_len + n_new + 0 <= kv_capacity. */
+ * Requires ctx_len + n_new <= kv_capacity.  Every wait in the weight-streaming
+ * pipelines is bounded; one that gives up sets the handle's error word (cleared at
+ * the start of each call), which the following dflash2_select reports per request. */
 dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
                                    const int32_t* ctx_len, const int32_t* n_new, const float* taps,
                                    void* k_cache, void* v_cache, int32_t* cand_ids, float* cand_logits,
@@ -166,7 +169,10 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
  * seed[r], counter = (philox_offset[r] lo32, hi32, slot = i-1, purpose 0).
  *   path [R][block-1] chosen ids; q_rows [R][block-1][top_k] float32
  *   scores_out [R][block-1][top_k][top_k] float32 or NULL: the score lattice
- *   status [R] written: DFLASH2_OK or DFLASH2_E_NONFINITE (nonfinite logit/score)
+ *   status [R] written: DFLASH2_OK, DFLASH2_E_NONFINITE (nonfinite logit/score),
+ *   DFLASH2_E_INVAL (negative temperature) or DFLASH2_E_CUDA (a pipeline wait of the
+ *   handle's last dflash2_draft_block gave up: its candidates and gate are undefined;
+ *   the handle's error word is cleared by the next dflash2_draft_block)
  *   temperature [R] float32 (negative -> status DFLASH2_E_INVAL); seed, philox_offset [R] uint64 */
 dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
                               const int32_t* cand_ids, const float* cand_logits, const float* gate,
