@@ -75,6 +75,13 @@ DF2_DEV void pdl_begin() {
   pdl_wait();
   pdl_trigger();
 }
+// For a kernel whose successor does nothing before its own wait but read weights and
+// set up its shared memory: the successor launches at once, so its CTAs take the
+// SMs the current weight stream frees and start their weight copies there.
+DF2_DEV void pdl_begin_early() {
+  pdl_trigger();
+  pdl_wait();
+}
 
 // 1/rms of one row from nch per-chunk sums of squares, computed by a whole warp
 // (fixed lane order and shuffle tree: bit-reproducible).  All lanes get the value.

@@ -63,11 +63,15 @@ DF2_DEV void emit_ss(float v, int row, float* ss, int nch) {
 // ------------------------------------------------------------------ start of the step
 // blockIdx.y < H/32: block embedding, first norm input and its sums of squares;
 // above: taps of the new context rows packed into the fc projection's input.
-// Everything it reads is a caller input and nothing the previous kernel reads is
-// written here, so the wait on the previous kernel comes last: it only keeps
-// that kernel ahead of every later one.
+// It reads caller inputs (ids, lengths, taps) that the previous kernel may have
+// written (the serving loop's state update, or the caller's own kernel), so it waits
+// for that kernel first; its successor, the taps projection, starts its weight copies
+// meanwhile.
 __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
-  pdl_trigger();
+  pdl_begin_early();
+  // a new step: the previous step's select has read the error word by now (it ran
+  // before the previous verify, whose completion the wait above implies)
+  if (a.pipe_err != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.pipe_err = 0;
   const int r = blockIdx.x;
   const int i = threadIdx.x >> 5;
   const int row = r * kB + i;
@@ -88,10 +92,6 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
     put_act(a.act_taps, a.act_taps_lo, a.fmt, act_offset(row, c, a.n_taps * a.H, a.tiled_taps),
             (i < nn) ? a.taps[idx] : 0.f);
   }
-  pdl_wait();
-  // a new step: the previous step's select has read the error word by now (it ran
-  // before the previous verify, whose completion the wait above implies)
-  if (a.pipe_err != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.pipe_err = 0;
 }
 
 // ------------------------------------------------------------------ taps projection finish
@@ -152,7 +152,7 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
 }
 
 __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
-  pdl_begin();
+  pdl_begin_early();  // followed by a weight launch
   conv_in_body(a);
 }
 
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
 // sublayer read different inputs and write different outputs, so they share one
 // launch (blockIdx.z selects the role).
 __global__ void __launch_bounds__(kThreads) fc_finish_conv_in_kernel(const FcFinishArgs f, const ConvInArgs c) {
-  pdl_begin();
+  pdl_begin_early();  // followed by a weight launch
   if (blockIdx.z == 0)
     fc_finish_body(f);
   else
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) fc_finish_conv_in_kernel(const FcFin
 // convolution wrapping the sublayer's output); act = x * w_next; ss of x.
 __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a) {
   __shared__ float ysh[kB][kCw];
-  pdl_begin();
+  pdl_begin_early();  // followed by a weight launch
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
   const int c = blockIdx.y * kCw + lane;
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
 // ------------------------------------------------------------------ SwiGLU
 // h = silu(gate) * up from the split planes of the two projections.
 __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
-  pdl_begin();
+  pdl_begin_early();  // followed by a weight launch
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
   const size_t idx = static_cast<size_t>(row) * a.F + c;

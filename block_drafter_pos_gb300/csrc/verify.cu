@@ -278,12 +278,12 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
   }
 }
 
-// The target logits and temperatures are caller inputs, so the chunk statistics are
-// computed before the wait on the previous kernel; only the store waits.
+// The target logits and temperatures are caller inputs that the previous kernel may
+// have written (the target model's), so the statistics wait for it.
 __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   __shared__ float sm_m[8], sm_s[8];
   __shared__ int sm_a[8], sm_f[8];
-  pdl_trigger();
+  pdl_begin_early();
   const int rj = blockIdx.x;  // r * 8 + j
   const int r = rj >> 3;
   const int chunk = blockIdx.y;
@@ -357,7 +357,6 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
     s = 0.f;
     for (int w = 0; w < 8; ++w) s += sm_s[w];
   }
-  pdl_wait();  // the statistics buffer is read by the previous step's chain
   if (threadIdx.x == 0) {
     VerifyStat st;
     st.m = M;
