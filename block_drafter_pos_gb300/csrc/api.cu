@@ -187,6 +187,9 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1 > 64)
     return DFLASH2_E_UNSUPPORTED;
   const int fmt = c.weight_format;
+  // the tensor-core GEMM (handles of wide_min_requests or more requests) takes weight
+  // blocks of 128 rows: the delta projections' hidden/4 and the vocabulary
+  if (max_requests >= wide_min_requests(fmt) && ((c.hidden / 4) % 128 || c.vocab % 128)) return DFLASH2_E_UNSUPPORTED;
   if (!w->embed || !w->lm_head || !w->hidden_norm || !w->final_norm || !aligned16(w->lm_head)) return DFLASH2_E_INVAL;
   if (!valid_matrix(w->fc, fmt) || !valid_matrix(w->sel_proj, fmt) || !valid_matrix(w->cb_a, fmt) ||
       !valid_matrix(w->cb_b, fmt))

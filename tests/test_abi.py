@@ -47,3 +47,61 @@ def test_host_validation_without_device_work():
     assert lib.dflash2_create(ctypes.byref(cfg), ctypes.byref(w), 1, 1024, ctypes.byref(h)) == bd.binding.E_UNSUPPORTED
     cfg.head_dim = 128
     assert lib.dflash2_create(ctypes.byref(cfg), ctypes.byref(w), 1, 1024, ctypes.byref(h)) == bd.binding.E_INVAL
+
+
+def _toy_config(**kw):
+    cfg = bd.binding.Config()
+    cfg.hidden, cfg.n_layers, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim = 512, 1, 4, 1, 128
+    cfg.ffn, cfg.vocab, cfg.n_taps, cfg.block, cfg.top_k, cfg.rank = 1536, 8192, 5, 8, 16, 256
+    cfg.window, cfg.conv_taps, cfg.conv_group, cfg.mask_token_id = 2048, 2, 16, 8191
+    cfg.rope_theta, cfg.rms_eps, cfg.weight_format = 1e7, 1e-6, 0
+    for k, v in kw.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+@pytest.mark.parametrize("kw,max_req,want", [
+    # geometry the kernels are not instantiated for (the header's dflash2_create limits)
+    (dict(hidden=384), 1, "E_UNSUPPORTED"),                    # hidden % 256
+    (dict(ffn=1600), 1, "E_UNSUPPORTED"),                      # bf16: ffn % 128
+    (dict(ffn=1664, weight_format=1), 1, "E_UNSUPPORTED"),     # Q8: ffn % 256
+    (dict(n_q_heads=8), 1, "E_UNSUPPORTED"),                   # 4 query heads per KV head
+    (dict(vocab=8200, mask_token_id=8199), 1, "E_UNSUPPORTED"),  # vocab % 16
+    (dict(), 17, "E_UNSUPPORTED"),                             # more than DFLASH2_MAX_REQUESTS
+    (dict(vocab=8208, mask_token_id=8207), 5, "E_UNSUPPORTED"),  # tensor-core path: vocab % 128
+    (dict(hidden=768, ffn=1536, n_q_heads=4), 5, "E_UNSUPPORTED"),  # tensor-core path: hidden/4 % 128
+    (dict(vocab=8208, mask_token_id=8207, weight_format=1), 4, "E_UNSUPPORTED"),  # Q8 from 4 requests
+    # within the limits, the next check is the (missing) weights: invalid argument
+    (dict(vocab=8208, mask_token_id=8207), 4, "E_INVAL"),      # bf16 GEMV path up to 4 requests
+    (dict(vocab=8208, mask_token_id=8207, weight_format=1), 3, "E_INVAL"),
+    (dict(mask_token_id=8192), 1, "E_INVAL"),                  # mask id outside the vocabulary
+    (dict(weight_format=2), 1, "E_INVAL"),
+    (dict(window=1), 1, "E_INVAL"),
+])
+def test_create_geometry_limits_on_the_host(kw, max_req, want):
+    """dflash2_create rejects unsupported geometry and bad arguments before any device call."""
+    lib = bd.lib()
+    h = ctypes.c_void_p()
+    rc = lib.dflash2_create(ctypes.byref(_toy_config(**kw)), ctypes.byref(bd.binding.Weights()), max_req, 1024,
+                            ctypes.byref(h))
+    assert rc == getattr(bd.binding, want)
+    assert not h.value
+
+
+def test_entry_points_reject_a_null_handle_or_bad_sizes():
+    lib = bd.lib()
+    E = bd.binding.E_INVAL
+    assert lib.dflash2_select(None, 1, *([None] * 12)) == E
+    assert lib.dflash2_verify(None, 1, *([None] * 12)) == E
+    assert lib.dflash2_advance(None, 1, *([None] * 7)) == E
+    assert lib.dflash2_set_select_mode(None, 0) == E
+    assert lib.dflash2_head_topk(None, 8, *([None] * 5)) == E
+    assert lib.dflash2_destroy(None) == E
+    # the entry that allocates nothing: its size checks come before any device call
+    buf = (ctypes.c_char * 64)()
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16, ctypes.c_void_p)
+    assert lib.dflash2_head_topk_noalloc(None, 8192, 512, 8, p, p, p, None, None) == E
+    assert lib.dflash2_head_topk_noalloc(p, 8192, 512, 12, p, p, p, None, None) == E     # rows % 8
+    assert lib.dflash2_head_topk_noalloc(p, 8, 512, 8, p, p, p, None, None) == E         # vocab < 16
+    assert lib.dflash2_head_topk_noalloc(p, 8200, 512, 8, p, p, p, None, None) == bd.binding.E_UNSUPPORTED
+    assert lib.dflash2_head_topk_noalloc(p, 8192, 576, 8, p, p, p, None, None) == bd.binding.E_UNSUPPORTED
