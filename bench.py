@@ -12,7 +12,8 @@ resident in HBM and far larger than L2 (6.1 GB of weights stream every step).
 
 `value` is steps/s summed over ranks (independent replicas, weak scaling).
 `e2e` is the same metric through the C ABI with host buffers: every step copies
-its inputs from pinned host memory and reads its result back.  `roofline`
+its inputs from pinned host memory and reads its result back (the target logits,
+needed only by verify, on a second stream while the draft runs).  `roofline`
 covers the LM-head + top-16 kernel, timed with CUDA events captured inside the
 graph on the launching stream.  `cpu_baseline` times the oracle on the host.
 
@@ -401,19 +402,39 @@ def main_ours(args, rank, world, local_rank):
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
+    # The target logits (nine tenths of the bytes in) are needed only by verify: they
+    # are copied on a side stream while the draft and select run, after the previous
+    # step's verify has read the same buffer; verify waits for the copy.
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    verified, landed = torch.cuda.Event(), torch.cuda.Event()
+
     def e2e_step():
+        side.wait_event(verified)
+        with torch.cuda.stream(side):
+            S["target"].copy_(host_in["target"], non_blocking=True)
+        landed.record(side)
         for k, v in host_in.items():
-            S[k].copy_(v, non_blocking=True)
-        run_step(bd, h, R, S)
+            if k != "target":
+                S[k].copy_(v, non_blocking=True)
+        bd.dflash2_draft_block(h, R, S["anchors"], S["ctx_len"], S["n_new"], S["taps"], S["kc"], S["vc"],
+                               S["cand_ids"], S["cand_logits"], S["gate"], None)
+        bd.dflash2_select(h, R, S["anchors"], S["cand_ids"], S["cand_logits"], S["gate"], S["temps"], S["seeds"],
+                          S["offsets"], S["path"], S["q_rows"], None, S["status"])
+        main.wait_event(landed)
+        bd.dflash2_verify(h, R, S["target"], S["path"], S["cand_ids"], S["q_rows"], S["temps"], S["seeds"],
+                          S["offsets"], S["n_acc"], S["emitted"], S["n_emit"], S["status"])
+        verified.record(main)
         for k, v in host_out.items():
             v.copy_(S[k], non_blocking=True)
 
+    verified.record(main)
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
     sync_ranks(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
+    verified.record(main)  # no copy of the timed steps starts before the timed region
     for _ in range(E):
         e2e_step()
     e1.record()
