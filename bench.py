@@ -33,6 +33,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -123,7 +124,7 @@ class Clocks:
     def __init__(self, dev_index):
         self.dev = dev_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"dflash2_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
