@@ -25,6 +25,11 @@
  *     selector score; a bounded wait of a weight-streaming pipeline that gave up)
  *     go to the per-request `status` words; such a request gets
  *     n_accepted = n_emitted = 0.
+ *   - Stream order holds for every input: a call's first kernel waits for the
+ *     stream's earlier work before it reads one, even when that work is a kernel
+ *     launched just before.  Weight copies may start earlier (overlapping the
+ *     previous kernel), so the weights given to dflash2_create must not change
+ *     while the handle is in use.
  *   - One handle serves one stream at a time (its scratch is shared by calls).
  *   - Integers are int32 unless stated; BF16 is stored as 16-bit patterns.
  */
