@@ -75,3 +75,19 @@ def test_step_bytes_weights_match_the_published_parameter_count():
     vec_params = sum(int(np.prod(s)) for k, s in shp.items()
                      if k not in ("embed", "lm_head") and not (len(s) == 2 and k.split(".")[-1] in wk.MATRIX_NAMES))
     assert expected - weights == 2 * vec_params
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """`bench.py --impl reference` on rank 0: one JSON line with the arm's keys, the
+    oracle timed on the host (toy workload, one step)."""
+    import json
+    import bench
+    args = bench.parse(["--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "0"])
+    bench.main_reference(args, 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "steps/s"
+    assert line["value"] > 0 and line["steps"] == 1 and line["n_gpus"] == 1 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "cfg1_toy"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
