@@ -1,6 +1,6 @@
 """Host logic of bench.py that needs no GPU: the clock sampler's parsing of
-nvidia-smi's CSV (a stand-in nvidia-smi on PATH prints fixed rows), and the
-step-byte count of the default workload."""
+nvidia-smi's CSV (a stand-in nvidia-smi on PATH prints fixed rows), the
+step-byte count of the default workload, and the reference arm's JSON line."""
 import os
 import stat
 import sys
