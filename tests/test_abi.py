@@ -105,3 +105,20 @@ def test_entry_points_reject_a_null_handle_or_bad_sizes():
     assert lib.dflash2_head_topk_noalloc(p, 8, 512, 8, p, p, p, None, None) == E         # vocab < 16
     assert lib.dflash2_head_topk_noalloc(p, 8200, 512, 8, p, p, p, None, None) == bd.binding.E_UNSUPPORTED
     assert lib.dflash2_head_topk_noalloc(p, 8192, 576, 8, p, p, p, None, None) == bd.binding.E_UNSUPPORTED
+
+
+def test_stream_k_plane_map_against_brute_force(tmp_path):
+    """The closed-form plane map (internal.h) that the partial-plane consumers use,
+    against the stream-K partition enumerated stage by stage (host code, g++)."""
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    cuda_inc = "/usr/local/cuda/include"
+    if gxx is None or not os.path.exists(os.path.join(cuda_inc, "cuda.h")):
+        pytest.skip("g++ or the CUDA headers are missing")
+    exe = str(tmp_path / "plane_map_check")
+    subprocess.run([gxx, "-std=c++17", "-O1", "-I", os.path.join(ROOT, "block_drafter_pos_gb300", "csrc"),
+                    "-I", cuda_inc, os.path.join(ROOT, "tests", "plane_map_check.cpp"), "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout
+    assert out.stdout.startswith("ok ") and int(out.stdout.split()[1]) > 10000
