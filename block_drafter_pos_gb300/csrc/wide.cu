@@ -95,6 +95,13 @@ struct WideGeo {
   static constexpr int kConvGroups = 2;  // int8: converter warp groups, taking alternate stages
   static constexpr int kWarps = FMT == 1 ? 8 + 8 * kConvGroups : 8;
   static_assert(kDW >= 2, "weight ring");
+  // int8: converter group g takes the stages i = g (mod kConvGroups) and waits on the
+  // code slot i mod kDW with the parity of i's use of that slot.  That wait is only
+  // sound if the slot's previous use (stage i - kDW) has landed, which holds when
+  // each group owns its slots (kDW == kConvGroups), or when the operand-slot wait the
+  // group passed at stage i - kConvGroups (the products of stage i - kConvGroups - kDA
+  // are done) already covers stage i - kDW.
+  static_assert(FMT == 0 || kDW == kConvGroups || kDW >= kDA + kConvGroups, "code ring depth vs converter groups");
   static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
