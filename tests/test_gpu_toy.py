@@ -313,3 +313,32 @@ def test_select_viterbi_mode_matches_oracle(integer):
             assert ref["total"] >= tot_w - 1e-4 * max(1.0, abs(float(tot_w)))
         else:
             assert np.array_equal(path[r], walk_path[r])  # sampled requests are unaffected by the mode
+
+
+@pytest.mark.parametrize("fmt,R", [("bf16", 3), ("q8", 5)])
+def test_draft_block_empty_context(fmt, R):
+    """Degenerate contexts: nothing in the cache and no new rows (the block attends to
+    its own 8 keys only), or only this call's new rows; every other cache row holds the
+    NaN sentinel.  GEMV path (3 bf16 requests) and tensor-core path (5 Q8 requests)."""
+    g = dataclasses.replace(wk.TOY, window=256)
+    wl = wk.Workload("toy_empty_ctx", g, fmt, R, [8] * R, [0.0] * R, [0.5] * R, seed=17)
+    W = wk.make_weights(g, fmt, wl.seed)
+    inp = wk.make_request_inputs(wl)
+    inp["n_new"] = np.array([0, 5, 8, 0, 1][:R], np.int32)  # ctx_len is 0 for every request
+    kc, vc = new_caches(wl, inp)
+    step = GpuStep(wl, W)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    kct, vct = i16(kc), i16(vc)
+    step.draft(t(inp["anchors"]), t(inp["ctx_len"]), t(inp["n_new"]), t(inp["taps"]), kct, vct)
+    torch.cuda.synchronize()
+    logits = step.logits.cpu().numpy()
+    kc_gpu = kct.cpu().numpy().view(np.uint16)
+    assert np.isfinite(logits).all()
+    for r in range(R):
+        tr = oracle_draft(wl, W, inp, kc, vc, r)
+        assert rel_l2(logits[r], tr["logits"]) < 2e-2, r
+        nn = int(inp["n_new"][r])
+        for l in range(g.n_layers):
+            if nn:
+                assert rel_l2(oracle.bf16_to_f64(kc_gpu[l, r, :nn]), oracle.bf16_to_f64(tr["k_cache"][l][:nn])) < 2e-2
+            assert np.array_equal(kc_gpu[l, r, nn:], kc[l, r, nn:])  # nothing written past the new rows
