@@ -342,3 +342,30 @@ def test_draft_block_empty_context(fmt, R):
             if nn:
                 assert rel_l2(oracle.bf16_to_f64(kc_gpu[l, r, :nn]), oracle.bf16_to_f64(tr["k_cache"][l][:nn])) < 2e-2
             assert np.array_equal(kc_gpu[l, r, nn:], kc[l, r, nn:])  # nothing written past the new rows
+
+
+def test_draft_block_fills_the_cache_to_capacity():
+    """The new rows end exactly at the cache's capacity (request 0: 256 keys after the
+    append in a 256-row cache, beyond the 256-key window) next to a shorter request."""
+    g = dataclasses.replace(wk.TOY, window=256)
+    wl = wk.Workload("toy_full_cache", g, "bf16", 2, [256, 100], [0.0, 0.0], [0.5] * 2, seed=19, steps=0)
+    assert wl.kv_capacity == 256
+    W = wk.make_weights(g, "bf16", wl.seed)
+    inp = wk.make_request_inputs(wl)
+    kc, vc = new_caches(wl, inp)
+    step = GpuStep(wl, W)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    kct, vct = i16(kc), i16(vc)
+    step.draft(t(inp["anchors"]), t(inp["ctx_len"]), t(inp["n_new"]), t(inp["taps"]), kct, vct)
+    torch.cuda.synchronize()
+    logits = step.logits.cpu().numpy()
+    kc_gpu, vc_gpu = kct.cpu().numpy().view(np.uint16), vct.cpu().numpy().view(np.uint16)
+    for r in range(2):
+        tr = oracle_draft(wl, W, inp, kc, vc, r)
+        assert rel_l2(logits[r], tr["logits"]) < 2e-2, r
+        ctx, nn = int(inp["ctx_len"][r]), int(inp["n_new"][r])
+        for l in range(g.n_layers):
+            assert rel_l2(oracle.bf16_to_f64(vc_gpu[l, r, ctx:ctx + nn]),
+                          oracle.bf16_to_f64(tr["v_cache"][l][ctx:ctx + nn])) < 2e-2, r
+            assert np.array_equal(kc_gpu[l, r, :ctx], kc[l, r, :ctx])
+            assert np.array_equal(kc_gpu[l, r, ctx + nn:], kc[l, r, ctx + nn:])
