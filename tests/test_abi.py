@@ -122,3 +122,38 @@ def test_stream_k_plane_map_against_brute_force(tmp_path):
     out = subprocess.run([exe], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout
     assert out.stdout.startswith("ok ") and int(out.stdout.split()[1]) > 10000
+
+
+def test_binding_structures_match_the_header(tmp_path):
+    """The ctypes structures of the binding have the C header's sizes and field
+    offsets (a small C program built with the host compiler prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "abi_layout")
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "abi_layout.c"),
+                    "-o", exe], check=True)
+    got = dict(line.split() for line in subprocess.run([exe], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    b = bd.binding
+    want = {
+        "dflash2_config": ctypes.sizeof(b.Config),
+        "dflash2_config.hidden": b.Config.hidden.offset,
+        "dflash2_config.mask_token_id": b.Config.mask_token_id.offset,
+        "dflash2_config.weight_format": b.Config.weight_format.offset,
+        "dflash2_config.rope_theta": b.Config.rope_theta.offset,
+        "dflash2_config.rms_eps": b.Config.rms_eps.offset,
+        "dflash2_matrix": ctypes.sizeof(b.Matrix),
+        "dflash2_layer_weights": ctypes.sizeof(b.LayerWeights),
+        "dflash2_layer_weights.mlp_base": b.LayerWeights.mlp_base.offset,
+        "dflash2_layer_weights.q": b.LayerWeights.q.offset,
+        "dflash2_layer_weights.mlp_delta": b.LayerWeights.mlp_delta.offset,
+        "dflash2_weights": ctypes.sizeof(b.Weights),
+        "dflash2_weights.final_norm": b.Weights.final_norm.offset,
+        "dflash2_weights.fc": b.Weights.fc.offset,
+        "dflash2_weights.cb_b": b.Weights.cb_b.offset,
+        "dflash2_weights.layers": b.Weights.layers.offset,
+    }
+    assert {k: int(v) for k, v in got.items()} == want
