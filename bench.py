@@ -227,7 +227,7 @@ def run_step(bd, h, R, S, ev=None):
     bd.dflash2_select(h, R, S["anchors"], S["cand_ids"], S["cand_logits"], S["gate"], S["temps"], S["seeds"],
                       S["offsets"], S["path"], S["q_rows"], None, S["status"])
     bd.dflash2_verify(h, R, S["target"], S["path"], S["cand_ids"], S["q_rows"], S["temps"], S["seeds"], S["offsets"],
-                      S["n_acc"], S["emitted"], S["n_emit"], S["status"])
+                      S["n_acc"], S["emitted"], S["n_emit"], None, S["status"])
 
 
 def measure_r16(args, world, local_rank):
@@ -423,7 +423,7 @@ def main_ours(args, rank, world, local_rank):
                           S["offsets"], S["path"], S["q_rows"], None, S["status"])
         main.wait_event(landed)
         bd.dflash2_verify(h, R, S["target"], S["path"], S["cand_ids"], S["q_rows"], S["temps"], S["seeds"],
-                          S["offsets"], S["n_acc"], S["emitted"], S["n_emit"], S["status"])
+                          S["offsets"], S["n_acc"], S["emitted"], S["n_emit"], None, S["status"])
         verified.record(main)
         for k, v in host_out.items():
             v.copy_(S[k], non_blocking=True)

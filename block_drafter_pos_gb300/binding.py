@@ -62,7 +62,7 @@ def lib() -> ctypes.CDLL:
         L.dflash2_destroy.argtypes = [vp]
         L.dflash2_draft_block.argtypes = [vp, i32] + [vp] * 11
         L.dflash2_select.argtypes = [vp, i32] + [vp] * 12
-        L.dflash2_verify.argtypes = [vp, i32] + [vp] * 12
+        L.dflash2_verify.argtypes = [vp, i32] + [vp] * 13
         L.dflash2_advance.argtypes = [vp, i32] + [vp] * 7
         L.dflash2_set_select_mode.argtypes = [vp, i32]
         L.dflash2_head_topk.argtypes = [vp, i32] + [vp] * 5
@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
         L.dflash2_set_lmhead_events.argtypes = [vp, vp, vp]
         L.dflash2_lmhead_bytes.argtypes = [vp, i32]
         L.dflash2_lmhead_bytes.restype = i64
+        L.dflash2_debug_set_pipeline_error.argtypes = [vp, vp]
+        L.dflash2_debug_set_pipeline_error.restype = i32
+        L.dflash2_debug_noalloc_inject_error.argtypes = [i32]
+        L.dflash2_debug_noalloc_inject_error.restype = i32
         L.dflash2_status_string.argtypes = [i32]
         L.dflash2_status_string.restype = ctypes.c_char_p
         for f in ("dflash2_create", "dflash2_destroy", "dflash2_draft_block", "dflash2_select", "dflash2_verify",
@@ -139,10 +143,10 @@ def dflash2_select(h, n_req, anchor_ids, cand_ids, cand_logits, gate, temperatur
 
 
 def dflash2_verify(h, n_req, target_logits, path, cand_ids, q_rows, temperature, seed, philox_offset, n_accepted,
-                   emitted, n_emitted, status, stream=None):
+                   emitted, n_emitted, probs_out, status, stream=None):
     _check(lib().dflash2_verify(h, n_req, _p(target_logits), _p(path), _p(cand_ids), _p(q_rows), _p(temperature),
-                                _p(seed), _p(philox_offset), _p(n_accepted), _p(emitted), _p(n_emitted), _p(status),
-                                _stream(stream)), "dflash2_verify")
+                                _p(seed), _p(philox_offset), _p(n_accepted), _p(emitted), _p(n_emitted),
+                                _p(probs_out), _p(status), _stream(stream)), "dflash2_verify")
 
 
 def dflash2_set_select_mode(h, mode: int):
@@ -166,6 +170,14 @@ def dflash2_head_topk_noalloc(lm_head, vocab, hidden_dim, n_rows, hidden, cand_i
     _check(lib().dflash2_head_topk_noalloc(_p(lm_head), vocab, hidden_dim, n_rows, _p(hidden), _p(cand_ids),
                                            _p(cand_logits), _p(logits_out), _stream(stream)),
            "dflash2_head_topk_noalloc")
+
+
+def dflash2_debug_set_pipeline_error(h, stream=None):
+    _check(lib().dflash2_debug_set_pipeline_error(h, _stream(stream)), "dflash2_debug_set_pipeline_error")
+
+
+def dflash2_debug_noalloc_inject_error(on: bool):
+    _check(lib().dflash2_debug_noalloc_inject_error(1 if on else 0), "dflash2_debug_noalloc_inject_error")
 
 
 def dflash2_launch_count(h) -> int:

@@ -406,6 +406,12 @@ dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* s
   return DFLASH2_OK;
 }
 
+dflash2_status dflash2_debug_set_pipeline_error(dflash2_handle* h, void* stream) {
+  if (!h) return DFLASH2_E_INVAL;
+  DF2_CHECK(cudaMemsetAsync(h->gemv_err, 1, sizeof(int), static_cast<cudaStream_t>(stream)));
+  return DFLASH2_OK;
+}
+
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
   if (!h || n_req < 1) return -1;
   const int64_t N = 8 * static_cast<int64_t>(n_req);
@@ -895,7 +901,8 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
 dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* target_logits, const int32_t* path,
                               const int32_t* cand_ids, const float* q_rows, const float* temperature,
                               const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
-                              int32_t* emitted, int32_t* n_emitted, int32_t* status, void* stream) {
+                              int32_t* emitted, int32_t* n_emitted, float* probs_out, int32_t* status,
+                              void* stream) {
   if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
   if (!target_logits || !path || !cand_ids || !q_rows || !temperature || !seed || !philox_offset || !n_accepted ||
       !emitted || !n_emitted || !status)
@@ -914,6 +921,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   a.emitted = emitted;
   a.n_emitted = n_emitted;
   a.status = status;
+  a.probs = probs_out;
   a.V = h->V;
   a.n_chunks = h->n_verify_chunks;
   DF2_CHECK(launch_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));

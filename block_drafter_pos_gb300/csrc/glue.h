@@ -177,6 +177,7 @@ struct TopkMergeArgs {
   int n_rows, n_cta, rank, nch, H;
   float eps;
   GemvPlanes psel;         // planes of sel
+  const int* err;          // or null: when nonzero, every row gets the sentinel (ids -1, logits NaN)
 };
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st);
 
@@ -212,7 +213,8 @@ cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t
 constexpr int kVerifyChunk = 4096;
 struct VerifyStat {
   float m;       // chunk max (of z)
-  float s;       // sum exp((z - m) / T) over the chunk (T > 0)
+  float s;       // sum exp((z - m) / T) over the chunk (T > 0), compensated: the sum is s + s_lo
+  float s_lo;
   int32_t arg;   // argmax (smallest index among equal maxima)
   int32_t flags; // bit 0: NaN seen, bit 1: +inf seen
 };
@@ -229,6 +231,7 @@ struct VerifyArgs {
   int32_t* emitted;            // [R][8]
   int32_t* n_emitted;
   int32_t* status;
+  float* probs;                // [R][8][2] or null: p_j at the proposal / bonus, residual mass (debug output)
   unsigned int* counters;      // [R] finished chunk statistics of the launch; zero before and after it
   int V, n_chunks;
 };

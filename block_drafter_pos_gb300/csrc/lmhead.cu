@@ -222,6 +222,14 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   const int pos = n & 7, rq = n >> 3;
   if (pos == 0) return;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (a.err != nullptr && __ldcg(a.err) != 0) {  // the per-CTA lists are incomplete: write the sentinel
+    if (threadIdx.x < kTopK) {
+      const size_t o = (static_cast<size_t>(rq) * 7 + pos - 1) * kTopK + threadIdx.x;
+      a.cand_ids[o] = -1;
+      a.cand_logits[o] = __int_as_float(0x7FC00000);
+    }
+    return;
+  }
   if (wid == 0) {
     const float v = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
     if (lane == 0) rs = v;

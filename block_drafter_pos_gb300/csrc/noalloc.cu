@@ -9,6 +9,7 @@
 // the LM-head kernel live in one fixed device array of this library.  The array
 // is loaded with the library and held on every GPU that uses it until the
 // process exits.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/dflash2.h"
@@ -21,21 +22,35 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kKeys = static_cast<size_t>(DFLASH2_NOALLOC_MAX_ROWS) * DFLASH2_NOALLOC_MAX_CTAS * 16;
 
-// [rows][CTAs][16] candidate keys (value bits + vocabulary id), 640 KiB.
+// [rows][CTAs][16] candidate keys (value bits + vocabulary id), 1.25 MiB.
 static __device__ __align__(256) unsigned long long g_noalloc_keys[kKeys];
+// Set by the LM-head kernel when one of its bounded pipeline waits gives up; the
+// merge then writes the sentinel instead of candidates.  Cleared by every call.
+static __device__ __align__(16) int g_noalloc_err;
 
 struct DeviceSlot {
   unsigned long long* keys;  // device address of g_noalloc_keys on this device
+  int* err;                  // device address of g_noalloc_err on this device
   int n_cta;
 };
 
 std::mutex g_mu;
 DeviceSlot g_slots[kMaxDevices];
 bool g_ready[kMaxDevices];
+std::atomic<int> g_inject_error{0};
 
-// Looks up the array's device address and the SM count once per device, with
-// that device current.  The name g_noalloc_keys is only a host-side stand-in in
-// host code; the kernels must get this address instead.
+// CTAs of one call: two per SM like the handle's LM head, so every SM streams the
+// same share of the vocabulary; where that exceeds the array's CTA bound, one per SM
+// (or the bound itself on a GPU with more SMs than it).
+int noalloc_ctas(int sms) {
+  const int two = lmhead_ctas(sms);
+  if (two <= DFLASH2_NOALLOC_MAX_CTAS) return two;
+  return sms <= DFLASH2_NOALLOC_MAX_CTAS ? sms : DFLASH2_NOALLOC_MAX_CTAS;
+}
+
+// Looks up the arrays' device addresses and the SM count once per device, with
+// that device current.  The names g_noalloc_keys and g_noalloc_err are only
+// host-side stand-ins in host code; the kernels must get these addresses instead.
 cudaError_t device_slot(DeviceSlot* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -46,12 +61,15 @@ cudaError_t device_slot(DeviceSlot* out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_keys);
     if (e != cudaSuccess) return e;
+    void* pe = nullptr;
+    e = cudaGetSymbolAddress(&pe, g_noalloc_err);
+    if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     g_slots[dev].keys = static_cast<unsigned long long*>(p);
-    const int ctas = lmhead_ctas(sms);
-    g_slots[dev].n_cta = ctas < DFLASH2_NOALLOC_MAX_CTAS ? ctas : DFLASH2_NOALLOC_MAX_CTAS;
+    g_slots[dev].err = static_cast<int*>(pe);
+    g_slots[dev].n_cta = noalloc_ctas(sms);
     g_ready[dev] = true;
   }
   *out = g_slots[dev];
@@ -59,6 +77,12 @@ cudaError_t device_slot(DeviceSlot* out) {
 }
 
 }  // namespace
+
+extern "C" dflash2_status dflash2_debug_noalloc_inject_error(int32_t on) {
+  if (on != 0 && on != 1) return DFLASH2_E_INVAL;
+  g_inject_error.store(on, std::memory_order_relaxed);
+  return DFLASH2_OK;
+}
 
 extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t vocab, int32_t hidden_dim,
                                                     int32_t n_rows, const void* hidden, int32_t* cand_ids,
@@ -72,6 +96,11 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   DeviceSlot slot;
   if (device_slot(&slot) != cudaSuccess) return DFLASH2_E_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The error word starts clear (set, under the test hook, as a pipeline wait that
+  // gave up would set it).  A memset of a device symbol allocates nothing.
+  if (cudaMemsetAsync(slot.err, g_inject_error.load(std::memory_order_relaxed) ? 1 : 0, sizeof(int), st) !=
+      cudaSuccess)
+    return DFLASH2_E_CUDA;
   // Every (row, CTA) list the merge reads is rewritten by the LM-head launch
   // first, so nothing left in the array by an earlier call is ever read.
   LmHeadArgs a;
@@ -88,7 +117,7 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   a.nch = hidden_dim / 32;
   a.n_cta = slot.n_cta;
   a.eps = 0.f;
-  a.err = nullptr;
+  a.err = slot.err;
   if (launch_lmhead(a, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
   TopkMergeArgs m = {};
   m.part_keys = slot.keys;
@@ -103,6 +132,7 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   m.nch = hidden_dim / 128;
   m.H = hidden_dim;
   m.eps = 0.f;
+  m.err = slot.err;
   if (launch_topk_merge(m, false, st) != cudaSuccess) return DFLASH2_E_CUDA;
   return DFLASH2_OK;
 }

@@ -27,75 +27,97 @@ DF2_DEV VerifyStat ldst(const VerifyStat* p) {
   VerifyStat v;
   v.m = __ldcg(&p->m);
   v.s = __ldcg(&p->s);
+  v.s_lo = __ldcg(&p->s_lo);
   v.arg = __ldcg(&p->arg);
   v.flags = __ldcg(&p->flags);
   return v;
 }
 
+// a + b = s + e exactly (Knuth's TwoSum; six float operations, no reassociation).
+DF2_DEV void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+
 // Inverse-CDF draw over the vocabulary of row j from weights w(x) = p(x) - min(p(x),
 // q(x)) (residual, use_q) or p(x) (bonus / zero residual).  Runs on the whole CTA.
+// A draw lands within eps of an entry boundary with probability about 2 eps V, so
+// at V = 248,320 the position of u * total among the cumulative masses must be far
+// finer than FP32 gives (an FP32 fold of 61 chunk masses alone errs by ~1e-7): the
+// chunk masses (compensated chunk sums, FP64 rescale), their fold, u * total and the
+// in-chunk prefix sums are FP64; the per-entry weights stay the FP32 values of p
+// that the accept test uses.
+// *mass_out (thread 0) receives the drawn-from weights' total before any fallback:
+// the residual mass sum_x max(0, p(x) - q(x)) when use_q, else the p-mass.
 __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* st, float M, float tot, float T,
-                        const int* cid, const float* qv, bool use_q, float u, float* csum, float* red) {
+                        const int* cid, const float* qv, bool use_q, float u, double* csum, double* red,
+                        float* mass_out) {
   // chunk masses (fixed order): p-mass of chunk c = s_c * exp((m_c - M)/T) / tot,
   // minus the candidates' min(p, q) in that chunk when drawing from the residual.
   const int nc = a.n_chunks;
   const float inv_t = 1.f / T;
+  const double dT = static_cast<double>(T), dtot = static_cast<double>(tot);
+  auto p_mass = [&](const VerifyStat& sc) {
+    return (sc.m > -INFINITY) ? (static_cast<double>(sc.s) + static_cast<double>(sc.s_lo)) *
+                                    exp((static_cast<double>(sc.m) - static_cast<double>(M)) / dT) / dtot
+                              : 0.0;
+  };
   for (int c = threadIdx.x; c < nc; c += blockDim.x) {
-    const VerifyStat sc = ldst(st + c);
-    float mass = (sc.m > -INFINITY) ? sc.s * expf((sc.m - M) * inv_t) / tot : 0.f;
+    double mass = p_mass(ldst(st + c));
     if (use_q) {
       for (int k = 0; k < kK; ++k) {
         if (cid[k] / kVerifyChunk == c) {
           const float p = expf((z[cid[k]] - M) * inv_t) / tot;
-          mass -= fminf(p, qv[k]);
+          mass -= static_cast<double>(fminf(p, qv[k]));
         }
       }
-      mass = fmaxf(mass, 0.f);
+      mass = fmax(mass, 0.0);
     }
     csum[c] = mass;
   }
   __syncthreads();
-  __shared__ int sh_chunk;
-  __shared__ float sh_before, sh_total;
+  __shared__ int sh_chunk, sh_fallback;
+  __shared__ double sh_need;
   if (threadIdx.x == 0) {
-    float total = 0.f;
+    double total = 0.0;
     for (int c = 0; c < nc; ++c) total += csum[c];
-    bool fallback = use_q && !(total > 1e-30f);
+    *mass_out = static_cast<float>(total);
+    const bool fallback = use_q && !(total > 1e-30);
     if (fallback) {
-      total = 0.f;
+      total = 0.0;
       for (int c = 0; c < nc; ++c) {
-        const VerifyStat sc = ldst(st + c);
-        csum[c] = (sc.m > -INFINITY) ? sc.s * expf((sc.m - M) * inv_t) / tot : 0.f;
+        csum[c] = p_mass(ldst(st + c));
         total += csum[c];
       }
     }
-    const float target = u * total;
-    float acc = 0.f;
+    const double target = static_cast<double>(u) * total;
+    double acc = 0.0;
     int pick = -1, lastpos = 0;
     for (int c = 0; c < nc; ++c) {
-      if (csum[c] > 0.f) lastpos = c;
+      if (csum[c] > 0.0) lastpos = c;
       if (pick < 0 && acc + csum[c] > target) pick = c;
       if (pick < 0) acc += csum[c];
     }
-    sh_before = target - acc;  // remaining mass to cover inside the chunk
+    sh_need = target - acc;  // remaining mass to cover inside the chunk
     if (pick < 0) {
-      pick = lastpos;               // rounding left u * total past the end:
-      sh_before = INFINITY;         // take the last positive entry of the last chunk
+      pick = lastpos;             // rounding left u * total past the end:
+      sh_need = INFINITY;         // take the last positive entry of the last chunk
     }
     sh_chunk = pick;
-    sh_total = fallback ? -1.f : 1.f;
+    sh_fallback = fallback;
   }
   __syncthreads();
   const int c = sh_chunk;
-  const bool q_on = use_q && sh_total > 0.f;
-  const float need = sh_before;
+  const bool q_on = use_q && !sh_fallback;
+  const double need = sh_need;
   const int v0 = c * kVerifyChunk;
   const int v1 = min(a.V, v0 + kVerifyChunk);
   // block-wide scan in id order: each thread owns a contiguous run of 16 ids
   const int per = kVerifyChunk / 256;
   const int b0 = v0 + threadIdx.x * per;
   float wv[kVerifyChunk / 256];
-  float run = 0.f;
+  double run = 0.0;
   for (int t = 0; t < per; ++t) {
     const int v = b0 + t;
     float w = 0.f;
@@ -108,21 +130,21 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
       }
     }
     wv[t] = w;
-    run += w;
+    run += static_cast<double>(w);
   }
   // exclusive prefix of the per-thread runs
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  float incl = run;
+  double incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) red[wid] = incl;
   __syncthreads();
-  float wbase = 0.f;
+  double wbase = 0.0;
   for (int w = 0; w < wid; ++w) wbase += red[w];
-  float acc = wbase + incl - run;
+  double acc = wbase + incl - run;
   __shared__ int sh_pick, sh_last;
   if (threadIdx.x == 0) {
     sh_pick = 0x7FFFFFFF;
@@ -132,7 +154,7 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
   int found = 0x7FFFFFFF, lastpos = -1;
   for (int t = 0; t < per; ++t) {
     if (wv[t] > 0.f) lastpos = b0 + t;
-    acc += wv[t];
+    acc += static_cast<double>(wv[t]);
     if (found == 0x7FFFFFFF && acc > need && wv[t] > 0.f) found = b0 + t;
   }
   if (found != 0x7FFFFFFF) atomicMin(&sh_pick, found);
@@ -147,14 +169,18 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
 // The accept / emit chain of request r (run by the statistics CTA that completes
 // the request's set).
 __device__ void chain_body(const VerifyArgs& a, int r) {
-  extern __shared__ float csum[];  // [n_chunks]
-  __shared__ float red[8];
+  extern __shared__ double csum[];  // [n_chunks]
+  __shared__ double red[8];
   __shared__ float rowM[kB], rowS[kB];
   __shared__ int rowA[kB], rowF[kB], rowBad;
   __shared__ int cid[kK];
   __shared__ float qv[kK];
   __shared__ int sh_decision;
   int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
+  // debug output: NaN wherever this request gets no probability
+  float* probs = a.probs != nullptr ? a.probs + static_cast<size_t>(r) * kB * 2 : nullptr;
+  if (probs != nullptr && threadIdx.x < 2 * kB) probs[threadIdx.x] = __int_as_float(0x7FC00000);
+  __shared__ float sh_mass;
   if (a.status[r] != 0) {
     if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
     if (threadIdx.x == 0) {
@@ -192,7 +218,7 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
     float S = 0.f;
     if (T > 0.f && M > -INFINITY && M < INFINITY)
       for (int c = lane; c < a.n_chunks; c += 32)
-        if (const VerifyStat sc = ldst(sj + c); sc.m > -INFINITY) S += sc.s * expf((sc.m - M) / T);
+        if (const VerifyStat sc = ldst(sj + c); sc.m > -INFINITY) S += (sc.s + sc.s_lo) * expf((sc.m - M) / T);
     S = warp_sum(S);
     if (lane == 0) {
       rowM[j] = M;
@@ -234,6 +260,12 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
   }
   const uint64_t seed = a.seed[r], off = a.offset[r];
   const float* zr = a.logits + static_cast<size_t>(r) * kB * a.V;
+  __syncthreads();  // the NaN fill above is done before these entries are written
+  if (probs != nullptr && threadIdx.x < kP) {  // p_j at every row's proposal (same arithmetic as the accept test)
+    const int j = threadIdx.x;
+    const int d = min(max(path[j], 0), a.V - 1);
+    probs[2 * j] = expf((zr[static_cast<size_t>(j) * a.V + d] - rowM[j]) / T) / rowS[j];
+  }
   for (int j = 0; j < kP; ++j) {
     const float* z = zr + static_cast<size_t>(j) * a.V;
     if (threadIdx.x < kK) {
@@ -258,8 +290,9 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
     }
     const float u = philox_uniform(seed, off, static_cast<uint32_t>(j), kPurposeResample);
     const int x = draw_row(a, z, st + static_cast<size_t>(j) * a.n_chunks, rowM[j], rowS[j], T, cid, qv, true, u,
-                           csum, red);
+                           csum, red, &sh_mass);
     if (threadIdx.x == 0) {
+      if (probs != nullptr) probs[2 * j + 1] = sh_mass;
       emitted[j] = x;
       for (int t = j + 1; t < kB; ++t) emitted[t] = -1;
       a.n_accepted[r] = j;
@@ -270,8 +303,9 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
   const float u = philox_uniform(seed, off, static_cast<uint32_t>(kP), kPurposeResample);
   const float* z = zr + static_cast<size_t>(kP) * a.V;
   const int x = draw_row(a, z, st + static_cast<size_t>(kP) * a.n_chunks, rowM[kP], rowS[kP], T, cid, qv, false, u,
-                         csum, red);
+                         csum, red, &sh_mass);
   if (threadIdx.x == 0) {
+    if (probs != nullptr) probs[2 * kP] = expf((z[x] - rowM[kP]) / T) / rowS[kP];
     emitted[kP] = x;
     a.n_accepted[r] = kP;
     a.n_emitted[r] = kP + 1;
@@ -281,7 +315,7 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
 // The target logits and temperatures are caller inputs that the previous kernel may
 // have written (the target model's), so the statistics wait for it.
 __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
-  __shared__ float sm_m[8], sm_s[8];
+  __shared__ float sm_m[8], sm_s[8], sm_sl[8];
   __shared__ int sm_a[8], sm_f[8];
   pdl_begin_early();
   const int rj = blockIdx.x;  // r * 8 + j
@@ -342,25 +376,49 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
     }
     F |= sm_f[w];
   }
-  float s = 0.f;
+  // sum of exp((z - M) / T) over the chunk, compensated (sum + error term, both kept):
+  // the draws of the chain need the chunk masses far finer than one FP32 rounding
+  float s = 0.f, s_lo = 0.f;
   if (T > 0.f && M > -INFINITY && M < INFINITY) {
     const float inv_t = 1.f / T;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int v = v0 + threadIdx.x + 256 * j;
-      if (v < v1 && !isnan(xs[j])) s += expf((xs[j] - M) * inv_t);
+      if (v < v1 && !isnan(xs[j])) {
+        float t, e;
+        two_sum(s, expf((xs[j] - M) * inv_t), t, e);
+        s = t;
+        s_lo += e;
+      }
     }
-    s = warp_sum(s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, s, o), ol = __shfl_xor_sync(0xffffffffu, s_lo, o);
+      float t, e;
+      two_sum(s, os, t, e);
+      s = t;
+      s_lo += ol + e;
+    }
     __syncthreads();
-    if (lane == 0) sm_s[wid] = s;
+    if (lane == 0) {
+      sm_s[wid] = s;
+      sm_sl[wid] = s_lo;
+    }
     __syncthreads();
-    s = 0.f;
-    for (int w = 0; w < 8; ++w) s += sm_s[w];
+    s = sm_s[0];
+    s_lo = sm_sl[0];
+    for (int w = 1; w < 8; ++w) {
+      float t, e;
+      two_sum(s, sm_s[w], t, e);
+      s = t;
+      s_lo += sm_sl[w] + e;
+    }
   }
   if (threadIdx.x == 0) {
     VerifyStat st;
     st.m = M;
     st.s = s;
+    st.s_lo = s_lo;
     st.arg = A;
     st.flags = F;
     a.stats[static_cast<size_t>(rj) * a.n_chunks + chunk] = st;
@@ -383,7 +441,8 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
 }  // namespace
 
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), a.n_chunks * sizeof(float), st, pdl, a);
+  return launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), a.n_chunks * sizeof(double), st, pdl,
+                   a);
 }
 
 }  // namespace df2

@@ -205,13 +205,19 @@ dflash2_status dflash2_set_select_mode(dflash2_handle* h, int32_t mode);
  *   order (purpose 2, slot j; from p_j if that mass <= 1e-30); if all accepted draw
  *   the bonus from the last row (purpose 2, slot block-1).
  *   n_accepted [R]; emitted [R][block] (-1 padded); n_emitted [R] = n_accepted+1.
+ *   probs_out [R][block][2] float32 or NULL (debugging, test harness): for a request
+ *   with T > 0, [j][0] = p_j(path[j]) for j < block-1 and [block-1][0] = p of the
+ *   bonus token when all proposals were accepted; [j][1] = the residual mass
+ *   sum_x max(0, p_j(x) - q_j(x)) of the rejected row j.  Every other entry (and
+ *   every entry of a greedy, skipped or nonfinite request) is NaN.
  *   status [R] in/out: a request whose status is nonzero on entry is skipped
  *   (n_accepted = n_emitted = 0); a NaN or +inf in a row, or a row whose maximum
  *   is -inf, sets DFLASH2_E_NONFINITE. */
 dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* target_logits, const int32_t* path,
                               const int32_t* cand_ids, const float* q_rows, const float* temperature,
                               const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
-                              int32_t* emitted, int32_t* n_emitted, int32_t* status, void* stream);
+                              int32_t* emitted, int32_t* n_emitted, float* probs_out, int32_t* status,
+                              void* stream);
 
 /* Serving-loop state update after dflash2_verify, on the device (so a multi-step
  * loop can be captured in one graph; "LSE docs/DFLASH2.md", block paragraph: each
@@ -270,8 +276,8 @@ int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req);
  * what dflash2_head_topk computes (logits of block positions 1..7 of each
  * request and their top-16, with hidden already normalised), but needs no
  * handle.  Its scratch (the per-CTA candidate lists, 640 KiB) is one fixed
- * device array inside this library, held on every GPU that uses it until the
- * process exits.
+ * device array inside this library (1.25 MiB), plus one error word, held on every
+ * GPU that uses it until the process exits.
  *   lm_head  [vocab][hidden_dim] bf16, 16-byte aligned, caller-owned.
  *   hidden   [n_rows][hidden_dim] bf16, 16-byte aligned; row n is block position
  *            n%8 of request n/8 (position 0 is not projected).
@@ -279,20 +285,39 @@ int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req);
  * Returns DFLASH2_E_INVAL for null or misaligned pointers, n_rows not a positive
  * multiple of 8, vocab < 16 or hidden_dim < 128, and DFLASH2_E_UNSUPPORTED for
  * n_rows > DFLASH2_NOALLOC_MAX_ROWS, vocab not a multiple of 16 or hidden_dim not
- * a multiple of 128; nothing is launched then.  Uses
- * min(SM count, DFLASH2_NOALLOC_MAX_CTAS) CTAs.
- * The first call on each device looks up the array's device address (with that
+ * a multiple of 128; nothing is launched then.  CTAs: two per SM (as the handle's
+ * LM head) when that is <= DFLASH2_NOALLOC_MAX_CTAS, else one per SM (at most
+ * DFLASH2_NOALLOC_MAX_CTAS), so every SM streams an equal share of the vocabulary.
+ * Failure on the device: every wait of the LM head's weight pipeline is bounded;
+ * one that gives up sets the call's error word (cleared at the start of each call)
+ * and the call then writes the sentinel cand_ids = -1, cand_logits = NaN for every
+ * row (its logits_out are undefined).  The return value cannot report it: the
+ * call does not synchronise.
+ * The first call on each device looks up the arrays' device addresses (with that
  * device current); make that first call before any stream capture.  It calls no
  * cudaMalloc or cudaFree and no allocating library routine.  All calls share the
  * one array: calls whose kernels overlap on the GPU (other streams, other
  * threads) race on it and must be serialised by the caller.  Every entry a call
- * reads is written earlier in the same call, so nothing needs clearing between
- * calls. */
+ * reads is written earlier in the same call (the error word is cleared by an
+ * asynchronous memset on `stream`), so nothing needs clearing between calls. */
 #define DFLASH2_NOALLOC_MAX_ROWS 32
-#define DFLASH2_NOALLOC_MAX_CTAS 160
+#define DFLASH2_NOALLOC_MAX_CTAS 320
 dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t vocab, int32_t hidden_dim, int32_t n_rows,
                                          const void* hidden, int32_t* cand_ids, float* cand_logits,
                                          float* logits_out, void* stream);
+
+/* ---- Test hooks (failure paths driven from the host; no kernel waits out a
+ * limit or faults) ----
+ * dflash2_debug_set_pipeline_error: marks the handle's pipeline error word on
+ * `stream`, as a bounded weight-pipeline wait of the last dflash2_draft_block
+ * that gave up would.  The next dflash2_select then reports DFLASH2_E_CUDA for
+ * every request (path -1, q rows 0) and dflash2_verify emits nothing for them;
+ * the next dflash2_draft_block clears the word.
+ * dflash2_debug_noalloc_inject_error(1): until called with 0, every
+ * dflash2_head_topk_noalloc call starts with its error word set instead of
+ * clear, as if its LM head's pipeline wait had given up (process-wide). */
+dflash2_status dflash2_debug_set_pipeline_error(dflash2_handle* h, void* stream);
+dflash2_status dflash2_debug_noalloc_inject_error(int32_t on);
 
 /* Human-readable text of a status code (static string). */
 const char* dflash2_status_string(dflash2_status s);

@@ -411,7 +411,14 @@ def verify(target_logits: np.ndarray, path: np.ndarray, cand_ids: np.ndarray, q_
     A row that holds a NaN or +inf, or whose maximum is -inf, makes the request
     nonfinite (then n_accepted = n_emitted = 0).
 
-    Returns dict(n_accepted, emitted int32[8] (-1 padded), n_emitted, status, margins).
+    Returns dict(n_accepted, emitted int32[8] (-1 padded), n_emitted, status,
+    margins, decisions).  `decisions` lists each sampled decision in chain order
+    as (kind, row, margin, scale): kind "accept" (margin relative to the ratio
+    p/q), "residual" or "bonus" (margin relative to the drawn-from mass, whose
+    total in p units is `scale`).  For T > 0 it also returns `p_path` [7] (p_j at
+    the proposal of every row), `p_bonus` (p_7 at the bonus token, NaN unless all
+    7 were accepted) and `residual_mass` [7] (sum_x max(0, p_j(x) - q_j(x)) of the
+    rejected row, NaN elsewhere): the verify probabilities themselves.
     """
     Bk, V = target_logits.shape
     P = Bk - 1
@@ -419,11 +426,14 @@ def verify(target_logits: np.ndarray, path: np.ndarray, cand_ids: np.ndarray, q_
     emitted = np.full(Bk, -1, np.int32)
     z = np.asarray(target_logits, np.float64)
     if status_in != STATUS_OK:
-        return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": status_in, "margins": []}
+        return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": status_in, "margins": [],
+                "decisions": []}
     rowmax = z.max(axis=1)
     if np.any(np.isnan(z)) or np.any(np.isposinf(z)) or np.any(~np.isfinite(rowmax)):
-        return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": STATUS_NONFINITE, "margins": []}
+        return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": STATUS_NONFINITE, "margins": [],
+                "decisions": []}
     margins = []
+    decisions = []
     if temperature == 0.0:
         t = [int(np.argmax(z[j])) for j in range(Bk)]      # argmax returns the first (smallest) index
         n = 0
@@ -431,9 +441,12 @@ def verify(target_logits: np.ndarray, path: np.ndarray, cand_ids: np.ndarray, q_
             emitted[n] = path[n]
             n += 1
         emitted[n] = t[n]
-        return {"n_accepted": n, "emitted": emitted, "n_emitted": n + 1, "status": STATUS_OK, "margins": margins}
+        return {"n_accepted": n, "emitted": emitted, "n_emitted": n + 1, "status": STATUS_OK, "margins": margins,
+                "decisions": decisions}
     p = np.exp((z - rowmax[:, None]) / temperature)
     p /= p.sum(axis=1, keepdims=True)
+    probs = {"p_path": np.array([p[j, int(path[j])] for j in range(P)]), "p_bonus": math.nan,
+             "residual_mass": np.full(P, math.nan)}
     for j in range(P):
         d = int(path[j])
         jj = int(np.nonzero(cand_ids[j] == d)[0][0])
@@ -441,22 +454,29 @@ def verify(target_logits: np.ndarray, path: np.ndarray, cand_ids: np.ndarray, q_
         u = uni(j, philox.PURPOSE_ACCEPT)
         ratio = p[j, d] / qd if qd > 0 else math.inf
         margins.append(abs(u - ratio) / max(ratio, 1e-300) if math.isfinite(ratio) else math.inf)
+        decisions.append(("accept", j, margins[-1], ratio))
         if u < ratio:
             emitted[j] = d
             continue
         q_full = np.zeros(V)
         q_full[cand_ids[j]] = q_rows[j]
         r = np.maximum(0.0, p[j] - q_full)
+        probs["residual_mass"][j] = r.sum()
         if r.sum() <= 1e-30:
             r = p[j]
         x, mg = _inverse_cdf(r, uni(j, philox.PURPOSE_RESAMPLE))
         margins.append(mg)
+        decisions.append(("residual", j, mg, float(r.sum())))
         emitted[j] = x
-        return {"n_accepted": j, "emitted": emitted, "n_emitted": j + 1, "status": STATUS_OK, "margins": margins}
+        return {"n_accepted": j, "emitted": emitted, "n_emitted": j + 1, "status": STATUS_OK, "margins": margins,
+                "decisions": decisions, **probs}
     x, mg = _inverse_cdf(p[P], uni(P, philox.PURPOSE_RESAMPLE))
     margins.append(mg)
+    decisions.append(("bonus", P, mg, 1.0))
     emitted[P] = x
-    return {"n_accepted": P, "emitted": emitted, "n_emitted": P + 1, "status": STATUS_OK, "margins": margins}
+    probs["p_bonus"] = p[P, x]
+    return {"n_accepted": P, "emitted": emitted, "n_emitted": P + 1, "status": STATUS_OK, "margins": margins,
+            "decisions": decisions, **probs}
 
 
 def _inverse_cdf(w: np.ndarray, u: float):

@@ -60,6 +60,7 @@ class GpuStep:
         self.n_acc = torch.zeros((R,), dtype=torch.int32, device=dev)
         self.emitted = torch.zeros((R, 8), dtype=torch.int32, device=dev)
         self.n_emit = torch.zeros((R,), dtype=torch.int32, device=dev)
+        self.probs = torch.zeros((R, 8, 2), dtype=torch.float32, device=dev)
 
     def draft(self, anchors, ctx_len, n_new, taps, kc, vc, with_logits=True):
         h = self.drafter.handle
@@ -78,7 +79,7 @@ class GpuStep:
         h = self.drafter.handle
         bd.dflash2_verify(h, self.wl.n_req, target, self.path if path is None else path,
                           self.cand_ids if cand_ids is None else cand_ids, self.q_rows if q_rows is None else q_rows,
-                          temps, seeds, offsets, self.n_acc, self.emitted, self.n_emit, self.status)
+                          temps, seeds, offsets, self.n_acc, self.emitted, self.n_emit, self.probs, self.status)
 
 
 def oracle_draft(wl, W, inp, kc_host, vc_host, r):
@@ -130,3 +131,96 @@ def certified_topk(gpu_ids: np.ndarray, ref_logits: np.ndarray, err: float, k: i
             near += hi - j + 1
         j = e + 1
     return near
+
+
+# ----------------------------------------------------------------------------- sampled-decision parity
+# The oracle decides in FP64; the kernels in FP32.  A decision of the oracle is
+# "decided" when it sits farther from its boundary than the kernels' rounding can
+# move it; only those must match bit for bit.  Undecided ones are counted.
+
+U24 = 2.0 ** -24
+
+
+def lattice_error_bounds(W, anchor, cand_ids, gate, scores, q8: bool):
+    """Rounding bound of each FP32 lattice score s_i(p -> c) of the selector kernel:
+    |fl(s) - s| <= gamma_n * sum_r |a_r g_r b_r| + 2u/(1-u) |s|, the mixed bound of the
+    LSE page's selector test paragraph (n = 256 products + 2 roundings per term; Q8
+    codebooks add the two dequantisations per term).  scores: the oracle's FP64
+    lattice [7][16][16] (row p of position 1 repeats the anchor row).  -> [7][16][16]"""
+    n = 262 if q8 else 258
+    gam = n * U24 / (1 - n * U24)
+    out = np.zeros((7, 16, 16))
+    B_all = [np.abs(oracle.codebook_rows(W["cb_b"], cand_ids[i])) for i in range(7)]
+    for i in range(7):
+        preds = [anchor] * 16 if i == 0 else cand_ids[i - 1]
+        A = np.abs(oracle.codebook_rows(W["cb_a"], preds))                 # [16][r]
+        absprod = (A * np.abs(gate[i])[None, :]) @ B_all[i].T              # [p][c]
+        out[i] = gam * absprod + 2 * U24 / (1 - U24) * np.abs(scores[i])
+    return out
+
+
+def compare_walk(res, gpu_path, gpu_q, bounds, T, cand_ids, exact=False):
+    """Follows the oracle's walk (fed the GPU's candidates, logits and gate) and checks
+    the GPU's path position by position while each decision is decided:
+      greedy: the top-2 gap exceeds 3x the row's largest score bound (the FP64 order
+      and the kernel's FP32 order agree), or exact (integer inputs: exact scores);
+      sampled: |u * sum - nearest cumsum| / sum exceeds 4 E / T + 64 u (a score error E
+      moves each q by at most a factor exp(2E/T); FP32 exp, 16-term sums and the
+      product u * sum add well under 64 ulp).
+    Returns (positions compared, undecided: bool, list of (gpu q row, oracle q row))."""
+    prev = 0
+    qs = []
+    for i in range(7):
+        E = 0.0 if exact else float(np.max(bounds[i, prev]))  # integer inputs: every score is exact
+        if T == 0.0:
+            decided = exact or res["margins"][i] > 3 * E
+        else:
+            decided = res["margins"][i] > 4 * E / T + 64 * U24
+        if not decided:
+            return i, True, qs
+        assert gpu_path[i] == res["path"][i], (i, gpu_path, res["path"])
+        qs.append((gpu_q[i], res["q_rows"][i]))
+        prev = int(np.nonzero(cand_ids[i] == res["path"][i])[0][0])
+    return 7, False, qs
+
+
+# Decision thresholds of the verify comparison.  The kernel's p at one entry carries
+# a few FP32 roundings (exp, the scaled argument, one division): relative ~2e-7 for the
+# tokens a ratio test meets, so an accept test is decided beyond 4e-6 of the ratio.
+# Its inverse-CDF draws accumulate in FP64 over compensated chunk sums, leaving the
+# independent per-entry FP32 roundings (~1e-9 of probability mass at V = 248,320);
+# a draw is decided beyond 2e-8 of mass.  A draw lands that close to a boundary with
+# probability about 2 * 2e-8 * V: 1% of draws at the full vocabulary.
+ACCEPT_REL = 4e-6
+DRAW_ABS = 2e-8
+
+
+def verify_decided(res) -> bool:
+    """Every sampled decision of the oracle's chain lies beyond the thresholds above."""
+    for kind, _row, margin, scale in res["decisions"]:
+        if kind == "accept":
+            if margin <= ACCEPT_REL:
+                return False
+        elif margin * scale <= DRAW_ABS:
+            return False
+    return True
+
+
+def compare_verify(res, na, em, ne, probs, T):
+    """Bit-exact outputs; the verify probabilities (T > 0) as pairs for a rel-L2 check:
+    p at every proposal, and the residual mass / bonus p where both sides took that
+    branch (the same branch whenever the outputs agree)."""
+    assert na == res["n_accepted"] and ne == res["n_emitted"], (na, ne, res["n_accepted"], res["n_emitted"])
+    assert np.array_equal(em, res["emitted"]), (em, res["emitted"])
+    pairs = []
+    if T > 0:
+        pairs += list(zip(probs[:7, 0], res["p_path"]))
+        if res["n_accepted"] < 7:
+            j = res["n_accepted"]
+            pairs.append((probs[j, 1], res["residual_mass"][j]))
+            assert np.all(np.isnan(np.delete(probs[:7, 1], j)))
+        else:
+            pairs.append((probs[7, 0], res["p_bonus"]))
+    else:
+        assert np.all(np.isnan(probs))
+    return pairs

@@ -92,7 +92,7 @@ def test_entry_points_reject_a_null_handle_or_bad_sizes():
     lib = bd.lib()
     E = bd.binding.E_INVAL
     assert lib.dflash2_select(None, 1, *([None] * 12)) == E
-    assert lib.dflash2_verify(None, 1, *([None] * 12)) == E
+    assert lib.dflash2_verify(None, 1, *([None] * 13)) == E
     assert lib.dflash2_advance(None, 1, *([None] * 7)) == E
     assert lib.dflash2_set_select_mode(None, 0) == E
     assert lib.dflash2_head_topk(None, 8, *([None] * 5)) == E

@@ -1,8 +1,12 @@
 """GPU parity at the full DFlash2 geometry (5 layers, width 5120, vocab 248320) on
 the benchmark workloads: the drafter outputs of every request (a spread of four
 of the 16 requests of configuration 5, which runs on the tensor-core path) against
-the FP64 oracle, and the select/verify outputs against properties that hold at any
-size."""
+the FP64 oracle; the selector walk and the verification of EVERY request against
+the oracle fed the GPU's own candidates, candidate logits, gate, path, q rows and
+target rows (discrete outputs bit-exact wherever the decision lies outside the
+kernels' FP32 rounding, such near-boundary decisions counted: at most one per
+configuration; verify probabilities and q rows at rel-L2 <= 1e-4); and properties
+that hold at any size."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +15,8 @@ import block_drafter_pos_gb300 as bd
 import oracle
 import workloads as wk
 
-from gpu_common import GpuStep, certified_topk, i16, new_caches, oracle_draft, rel_l2, topk_of
+from gpu_common import (GpuStep, certified_topk, compare_verify, compare_walk, i16, lattice_error_bounds, new_caches,
+                        oracle_draft, rel_l2, topk_of, verify_decided)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +77,36 @@ def test_full_geometry_step(cfg):
     q = step.q_rows.cpu().numpy()
     st = step.status.cpu().numpy()
     na, em, ne = step.n_acc.cpu().numpy(), step.emitted.cpu().numpy(), step.n_emit.cpu().numpy()
+    probs = step.probs.cpu().numpy()
+    cl = step.cand_logits.cpu().numpy()
+    # the oracle's walk and verify on the GPU's own inputs, every request
+    offs_h = wl.philox_offsets or [0] * R
+    undecided_walk = undecided_verify = 0
+    q_pairs, p_pairs = [], []
+    for r in range(R):
+        T = float(np.float32(wl.temps[r]))  # the kernel's FP32 temperature
+        res = oracle.walk(g, W["cb_a"], W["cb_b"], int(inp["anchors"][r]), ids[r], cl[r].astype(np.float64),
+                          gate[r].astype(np.float64), T, wl.philox_seed, int(offs_h[r]))
+        assert res["status"] == 0
+        bounds = lattice_error_bounds(W, int(inp["anchors"][r]), ids[r], gate[r].astype(np.float64), res["scores"],
+                                      wl.weight_format == "q8")
+        n_cmp, und, qs = compare_walk(res, path[r], q[r], bounds, T, ids[r])
+        undecided_walk += und
+        q_pairs += qs
+        ver = oracle.verify(target[r].astype(np.float64), path[r], ids[r], q[r].astype(np.float64), T,
+                            wl.philox_seed, int(offs_h[r]))
+        if verify_decided(ver):
+            p_pairs += compare_verify(ver, na[r], em[r], ne[r], probs[r], T)
+        else:
+            undecided_verify += 1
+    print(f"cfg {cfg}: walk undecided {undecided_walk}/{R}, verify undecided {undecided_verify}/{R}")
+    assert undecided_walk <= 1 and undecided_verify <= 1
+    if q_pairs:
+        qg, qo = np.array([a for a, _ in q_pairs]), np.array([b for _, b in q_pairs])
+        assert rel_l2(qg, qo) <= 1e-4, rel_l2(qg, qo)
+    if p_pairs:
+        pg, po = np.array([a for a, _ in p_pairs], np.float64), np.array([b for _, b in p_pairs])
+        assert rel_l2(pg, po) <= 1e-4, rel_l2(pg, po)
     for r in range(R):
         assert st[r] == 0
         for i in range(7):

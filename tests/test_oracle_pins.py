@@ -441,6 +441,61 @@ def test_verify_two_positions_conditional_lossless():
     assert np.allclose(marg, P[1], atol=1e-12)
 
 
+def test_verify_reported_probabilities():
+    """The verify probabilities the oracle reports are the ones its decisions use, pinned
+    by two identities of speculative sampling, both uniforms integrated exactly:
+      * the acceptance probability of a row, with the draft token drawn from q, is
+        sum_x min(p(x), q(x)) = 1 - sum_x max(0, p(x) - q(x)): one minus the reported
+        residual mass; and P(accept | d) = min(1, p_path / q(d));
+      * the bonus token x is drawn from p_7, so E[1 / p_bonus] = the number of tokens
+        with p_7 > 0 (all V of them)."""
+    V, K = 5, 2
+    rng = np.random.default_rng(15)
+    for trial in range(4):
+        z = rng.normal(0, 1.5, (8, V))
+        T = [1.0, 0.7, 2.0, 1.3][trial]
+        cand = np.stack([rng.choice(V, K, replace=False) for _ in range(7)]).astype(np.int32)
+        qv = rng.dirichlet(np.ones(K))
+        q_rows = np.tile(qv, (7, 1))
+        acc = 0.0
+        resid = []
+        for jd in range(K):
+            d = cand[0, jd]
+            path = cand[:, 0].copy()
+            path[0] = d
+            acc_d = 0.0
+            cuts = list(np.linspace(0, 1, 2001)[1:-1])
+            probe = oracle.verify(z, path, cand, q_rows, T, 0, 0, uniform_fn=lambda s, p: 0.0)
+            cuts.append(probe["p_path"][0] / qv[jd])
+            for wa, ua in _breakpoint_integral(lambda u: u, cuts):
+                def uni(slot, purpose, ua=ua):
+                    if slot == 0 and purpose == philox.PURPOSE_ACCEPT:
+                        return ua
+                    return 0.999999 if purpose == philox.PURPOSE_ACCEPT else 0.5
+                res = oracle.verify(z, path, cand, q_rows, T, 0, 0, uniform_fn=uni)
+                if res["n_accepted"] >= 1:
+                    acc_d += wa
+                else:
+                    resid.append(res["residual_mass"][0])
+            assert abs(acc_d - min(1.0, probe["p_path"][0] / qv[jd])) < 1e-12
+            acc += qv[jd] * acc_d
+        if resid:
+            assert np.allclose(resid, resid[0], rtol=0, atol=1e-15)
+            assert abs((1.0 - acc) - resid[0]) < 1e-12, (acc, resid[0])
+        # bonus: every proposal accepted (u = 0), the bonus uniform integrated exactly
+        path = cand[:, 0].copy()
+        probe = oracle.verify(z, path, cand, q_rows, T, 0, 0, uniform_fn=lambda s, p: 0.0)
+        assert probe["n_accepted"] == 7
+        p7 = np.exp((z[7] - z[7].max()) / T)
+        cuts = list(np.cumsum(p7 / p7.sum()))
+        inv = 0.0
+        for wr, ur in _breakpoint_integral(lambda u: u, cuts):
+            res = oracle.verify(z, path, cand, q_rows, T, 0, 0,
+                                uniform_fn=lambda s, p, ur=ur: ur if p == philox.PURPOSE_RESAMPLE else 0.0)
+            inv += wr / res["p_bonus"]
+        assert abs(inv - V) < 1e-9, inv
+
+
 def test_verify_greedy_is_argmax_chain():
     rng = np.random.default_rng(14)
     V = 50

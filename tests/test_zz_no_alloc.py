@@ -81,3 +81,65 @@ def test_noalloc_matches_handle_head_topk_on_two_calls_in_a_row():
             assert np.linalg.norm(gv - rv) <= 1e-6 * np.linalg.norm(rv), call
     finally:
         drafter.close()
+
+
+def _f64_topk(ref):
+    """Top-16 of float64 logits built here (value descending, equal values -> smaller id)."""
+    order = np.lexsort((np.arange(ref.size), -ref))
+    return order[:16]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_rows,vocab,hidden", [(32, 8192, 512), (24, 8208, 384), (8, 8208, 384)])
+def test_noalloc_shapes_against_float64_matmul(n_rows, vocab, hidden):
+    """Shapes the handle path never runs through this call: 32 rows (the array's row
+    bound, four 8-row tiles), 24 rows (three tiles in the four-tile kernel), a
+    vocabulary that ends inside a 64-row block (8208), and an odd number of 128-wide
+    K stages (384).  Integer weights and hidden states make every logit exact, so the
+    ids and logits equal a float64 matmul's top-16 computed here, bit for bit."""
+    rng = np.random.default_rng(n_rows + vocab + hidden)
+    lm = rng.integers(-3, 4, (vocab, hidden)).astype(np.float32)
+    x = rng.integers(-1, 2, (n_rows, hidden)).astype(np.float32)
+    R = n_rows // 8
+    ids = torch.full((R, 7, 16), -1, dtype=torch.int32, device="cuda")
+    vals = torch.full((R, 7, 16), float("nan"), dtype=torch.float32, device="cuda")
+    logits = torch.full((R, 7, vocab), float("nan"), dtype=torch.float32, device="cuda")
+    for _ in range(2):  # two calls in a row on the shared array
+        bd.dflash2_head_topk_noalloc(_i16(wk.bf16_bits_from_f32(lm)), vocab, hidden, n_rows,
+                                     _i16(wk.bf16_bits_from_f32(x)), ids, vals, logits)
+        torch.cuda.synchronize()
+    gi, gv, gl = ids.cpu().numpy(), vals.cpu().numpy(), logits.cpu().numpy()
+    ref = x.astype(np.float64) @ lm.astype(np.float64).T          # [n_rows][vocab]
+    for n in range(n_rows):
+        if n % 8 == 0:
+            continue                                             # the anchor position is not projected
+        rq, pos = n // 8, n % 8
+        want = _f64_topk(ref[n])
+        assert np.array_equal(gi[rq, pos - 1], want), (n, gi[rq, pos - 1], want)
+        assert np.array_equal(gv[rq, pos - 1], ref[n][want].astype(np.float32))
+        assert np.array_equal(gl[rq, pos - 1], ref[n].astype(np.float32))
+
+
+@pytest.mark.gpu
+def test_noalloc_device_error_writes_the_sentinel():
+    """A failed pipeline wait cannot be reported by the return value (the call does not
+    synchronise), so the call writes cand_ids = -1 and cand_logits = NaN.  Driven from
+    the host by the test hook that starts the call's error word set; the next call with
+    the hook off is correct again."""
+    V, H = 8192, 512
+    rng = np.random.default_rng(5)
+    lm = _i16(wk.bf16_bits_from_f32(rng.integers(-3, 4, (V, H)).astype(np.float32)))
+    x = _i16(wk.bf16_bits_from_f32(rng.integers(-1, 2, (16, H)).astype(np.float32)))
+    ids = torch.zeros((2, 7, 16), dtype=torch.int32, device="cuda")
+    vals = torch.zeros((2, 7, 16), dtype=torch.float32, device="cuda")
+    try:
+        bd.dflash2_debug_noalloc_inject_error(True)
+        bd.dflash2_head_topk_noalloc(lm, V, H, 16, x, ids, vals, None)
+        torch.cuda.synchronize()
+        assert np.all(ids.cpu().numpy() == -1)
+        assert np.all(np.isnan(vals.cpu().numpy()))
+    finally:
+        bd.dflash2_debug_noalloc_inject_error(False)
+    bd.dflash2_head_topk_noalloc(lm, V, H, 16, x, ids, vals, None)
+    torch.cuda.synchronize()
+    assert np.all(ids.cpu().numpy() >= 0) and np.all(np.isfinite(vals.cpu().numpy()))
