@@ -15,12 +15,17 @@ resident in HBM and far larger than L2 (6.1 GB of weights stream every step).
 its inputs from pinned host memory and reads its result back (the target logits,
 needed only by verify, on a second stream while the draft runs).  `roofline`
 covers the LM-head + top-16 kernel, timed with CUDA events captured inside the
-graph on the launching stream.  `cpu_baseline` times the oracle on the host.
+graph on the launching stream; `roofline.projections` covers the drafter's weight
+projections (every other weight stream), each launch bracketed by events in a
+separate graph.  Fractions are given against the measured copy bandwidth and
+against the nominal 8 TB/s.  `cpu_baseline` times the oracle on the host.
 
-`r16` (default line only; `--no-r16` skips it) is the metric's second operating
-point, 16 requests (configuration 5: Q8 weights, ragged contexts 512..32768,
-mixed temperatures): its 100 consecutive steps with the emitted tokens appended
-between steps, captured as one graph in the same process.
+The default line also carries the metric's other operating points, each measured
+in the same process (`--no-r16` skips them): `r16`, 16 requests (configuration 5:
+Q8 weights, ragged contexts 512..32768, mixed temperatures), its 100 consecutive
+steps with the emitted tokens appended between steps, captured as one graph;
+`q8_r1` (configuration 3: Q8, one request, context 2048, T = 1.0) and `r4`
+(configuration 4: Q8, four requests, context 8192, T = 0.7), 100 steps each.
 
 `--impl reference` times the CPU oracle (the only reference this method has
 here) on the same workload and prints the same line with "impl": "reference".
@@ -45,10 +50,14 @@ import numpy as np  # noqa: E402
 METRIC = "DFlash2 draft+verify steps/s at 1 and 16 req; achieved HBM GB/s vs peak"
 
 
-# DRAM bytes (read + write) of one LM-head launch, from the ncu capture summarised in
-# profiles/lmhead_topk_traffic.md, keyed by (vocabulary, width, requests).  Taken on
-# the current lmhead_kernel; re-capture when the kernel changes.
+# DRAM bytes (read + write) of one LM-head launch, keyed by (vocabulary, width,
+# requests): dram__bytes_read.sum + dram__bytes_write.sum of lmhead_kernel in a
+# one-pass ncu capture of the full-size one-request workload (the launch-list capture
+# of this benchmark's own command).  Valid for the current lmhead_kernel; re-capture
+# when the kernel changes.
 LMHEAD_TRAFFIC = {(248320, 5120, 1): 2.54e9 + 2.87e6}
+TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum of lmhead_kernel, full-size 1-request capture"
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s quoted for GB300 HBM3e, beside the measured copy rate
 
 
 def parse(argv=None):
@@ -61,7 +70,7 @@ def parse(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=100)
     p.add_argument("--no-r16", action="store_true",
-                   help="skip the 16-request measurement that rides along the default line")
+                   help="skip the other operating points (configurations 5, 3 and 4) that ride along the default line")
     return p.parse_args(argv)
 
 
@@ -230,27 +239,29 @@ def run_step(bd, h, R, S, ev=None):
                       S["n_acc"], S["emitted"], S["n_emit"], None, S["status"])
 
 
-def measure_r16(args, world, local_rank):
-    """The metric's second operating point, 16 requests (configuration 5: Q8, ragged
-    contexts, mixed temperatures; the tensor-core path): its 100 consecutive steps,
-    each draft + select + verify followed by the device-side state update
-    (dflash2_advance: the emitted tokens become the next step's anchor and new
-    context rows), captured as one CUDA graph after W eager warm-up steps; the
-    initial state is restored before each replay.  Max over ranks."""
+def measure_point(args, world, local_rank, cfg):
+    """One more operating point of the metric, measured in the same process: a
+    workload's step captured as one CUDA graph after W eager warm-up steps.  A
+    workload of consecutive steps (configuration 5: 16 Q8 requests, ragged contexts,
+    mixed temperatures) runs its 100 steps, each draft + select + verify followed by
+    the device-side state update (dflash2_advance: the emitted tokens become the next
+    step's anchor and new context rows), the initial state restored before each
+    replay; the others run 100 repetitions of their step.  Max over ranks."""
     import torch
-    import torch.distributed as dist
     import block_drafter_pos_gb300 as bd
     import workloads as wk
 
-    wl = wk.workload(5)
+    wl = wk.workload(cfg)
     R = wl.n_req
     drafter, S, _, _, _, _, setup_s = setup(wl, local_rank)
     h = drafter.handle
-    K = wl.steps  # 100
+    loop = wl.steps > 1
+    K = wl.steps if loop else 100
 
-    def loop_step():
+    def one_step():
         run_step(bd, h, R, S)
-        bd.dflash2_advance(h, R, S["emitted"], S["n_emit"], S["anchors"], S["ctx_len"], S["n_new"], S["offsets"])
+        if loop:
+            bd.dflash2_advance(h, R, S["emitted"], S["n_emit"], S["anchors"], S["ctx_len"], S["n_new"], S["offsets"])
 
     state0 = {k: S[k].clone() for k in ("anchors", "ctx_len", "n_new", "offsets")}
 
@@ -259,7 +270,7 @@ def measure_r16(args, world, local_rank):
             S[k].copy_(v)
 
     for _ in range(max(3, args.warmup)):
-        loop_step()
+        one_step()
     torch.cuda.synchronize()
     restore()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -275,7 +286,7 @@ def measure_r16(args, world, local_rank):
         with torch.cuda.graph(graph, stream=cap_stream):
             for i in range(K):
                 bd.dflash2_set_lmhead_events(h, ev[i][0], ev[i][1])
-                loop_step()
+                one_step()
     bd.dflash2_set_lmhead_events(h, None, None)
     stream.wait_stream(cap_stream)
     restore()
@@ -292,25 +303,72 @@ def measure_r16(args, world, local_rank):
     ms = max_over_ranks(t0.elapsed_time(t1), world)
     st = S["status"].cpu().numpy()
     assert np.all(st == 0), st
-    grown = int((S["ctx_len"] - state0["ctx_len"]).sum().item())  # context rows appended over the K steps
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     pk = peaks()
     sb = step_bytes(wl, R)
     step_s = ms / 1e3 / K
     lm_bytes = bd.dflash2_lmhead_bytes(h, R)
-    out = {"workload": wl.name, "requests_per_gpu": R, "weights": wl.weight_format, "steps": K,
-           "value": job_rate(K, world, ms), "unit": "steps/s", "ms_per_step": ms / K,
+    wide = R >= (5 if wl.weight_format == "bf16" else 4)
+    out = {"workload": wl.name, "requests_per_gpu": R, "context": wl.ctx[:R] if R <= 4 else "U[512, 32768]",
+           "weights": wl.weight_format, "temperature": wl.temps[:R] if R <= 4 else "round-robin 0, 0.7, 1.0",
+           "steps": K, "value": job_rate(K, world, ms), "unit": "steps/s", "ms_per_step": ms / K,
            "drafted_tokens_per_s": job_rate(K, world, ms) * 7 * R,
            "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
-           "lmhead": {"kernel": "wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel", "launch_ms": lm_ms,
+           "step_frac_vs_8tbs": sb / step_s / 1e9 / NOMINAL_HBM_GBS,
+           "lmhead": {"kernel": ("wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel" if wide
+                                 else "lmhead_kernel (LM head GEMV + fused top-16)"), "launch_ms": lm_ms,
                       "achieved_gbs": lm_bytes / (lm_ms / 1e3) / 1e9,
                       "frac": lm_bytes / (lm_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
-           "loop": f"{K} consecutive steps with the emitted tokens appended ({grown} context rows over all requests)",
            "setup_s": setup_s}
+    if loop:
+        grown = int((S["ctx_len"] - state0["ctx_len"]).sum().item())  # context rows appended over the K steps
+        out["loop"] = f"{K} consecutive steps with the emitted tokens appended ({grown} context rows over all requests)"
     del graph, drafter, S
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
+
+
+def measure_projections(bd, h, one_step, restore, n_launch, proj_bytes, steps=10):
+    """Roofline of the drafter's weight projections (the GEMV / tensor-core GEMM family,
+    every projection launch of the step but the LM head): a separate graph of `steps`
+    steps whose projection launches are each bracketed by CUDA events on the launching
+    stream.  An event record between launches removes their dependent-launch overlap,
+    so this is the family's rate launch by launch, not inside the timed step (whose
+    graph carries no such events)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * n_launch)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.current_stream()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(graph, stream=cap_stream):
+            for i in range(steps):
+                bd.dflash2_set_projection_events(h, evs[i])
+                one_step()
+    bd.dflash2_set_projection_events(h, None)
+    stream.wait_stream(cap_stream)
+    restore()
+    graph.replay()
+    torch.cuda.synchronize()
+    restore()
+    graph.replay()
+    torch.cuda.synchronize()
+    per_step = [sum(row[2 * j].elapsed_time(row[2 * j + 1]) for j in range(n_launch)) for row in evs]
+    ms = statistics.median(per_step)
+    pk = peaks()
+    gbs = proj_bytes / (ms / 1e3) / 1e9
+    del graph
+    return {"kernels": "gemv_kernel (bulk-copy pipeline + mma.sync) / wide_kernel (tcgen05)", "launches": n_launch,
+            "bytes": proj_bytes, "ms": ms, "achieved": gbs, "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+            "frac_vs_8tbs": gbs / NOMINAL_HBM_GBS,
+            "timing": f"each launch bracketed by events in a separate graph of {steps} steps (median step); "
+                      "launch by launch, without the dependent-launch overlap of the timed step"}
 
 
 def main_ours(args, rank, world, local_rank):
@@ -443,6 +501,9 @@ def main_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_val = job_rate(E, world, e2e_ms)
 
+    proj = measure_projections(bd, h, one_step, restore, bd.dflash2_projection_launches(h),
+                               bd.dflash2_projection_bytes(h))
+    restore()
     pk = peaks()
     lm_bytes = bd.dflash2_lmhead_bytes(h, R)
     lm_avg_s = statistics.mean(lm_ms) / 1e3
@@ -461,19 +522,29 @@ def main_ours(args, rank, world, local_rank):
                               else "one CUDA graph of K steps")},
         "drafted_tokens_per_s": steps_per_s * 7 * R,
         "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
+        "step_frac_vs_8tbs": sb / step_s / 1e9 / NOMINAL_HBM_GBS,
         "roofline": {"kernel": ("lmhead_kernel (LM head GEMV + fused top-16)" if R < (5 if wl.weight_format == "bf16" else 4) else
                                 "wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel"), "bound": "hbm",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "frac_vs_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": LMHEAD_TRAFFIC.get((wl.geom.vocab, wl.geom.hidden, R)),
+                     "traffic_source": TRAFFIC_SOURCE if (wl.geom.vocab, wl.geom.hidden, R) in LMHEAD_TRAFFIC else None,
                      "launch_ms": statistics.mean(lm_ms), "share_of_step": statistics.mean(lm_ms) / (ms / K),
-                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"},
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
+                     "projections": proj},
         "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches_per_step * K),
         "clocks": clk,
         "setup_s": setup_s,
     }
     if args.config == 2 and not args.no_r16:
-        line["r16"] = measure_r16(args, world, local_rank)
+        # the metric's other operating points: 16 requests (configuration 5), and the
+        # Q8 one-request and four-request workloads (configurations 3 and 4)
+        del graph
+        torch.cuda.synchronize()
+        line["r16"] = measure_point(args, world, local_rank, 5)
+        line["q8_r1"] = measure_point(args, world, local_rank, 3)
+        line["r4"] = measure_point(args, world, local_rank, 4)
     if rank == 0 and not args.no_cpu_baseline:
         cb, _ = cpu_baseline(wl, W, inp, kc_host, vc_host, S["target"].cpu().numpy())
         line["cpu_baseline"] = cb

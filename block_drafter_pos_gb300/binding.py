@@ -74,6 +74,12 @@ def lib() -> ctypes.CDLL:
         L.dflash2_set_lmhead_events.argtypes = [vp, vp, vp]
         L.dflash2_lmhead_bytes.argtypes = [vp, i32]
         L.dflash2_lmhead_bytes.restype = i64
+        L.dflash2_set_projection_events.argtypes = [vp, vp, i32]
+        L.dflash2_set_projection_events.restype = i32
+        L.dflash2_projection_launches.argtypes = [vp]
+        L.dflash2_projection_launches.restype = i32
+        L.dflash2_projection_bytes.argtypes = [vp]
+        L.dflash2_projection_bytes.restype = i64
         L.dflash2_debug_set_pipeline_error.argtypes = [vp, vp]
         L.dflash2_debug_set_pipeline_error.restype = i32
         L.dflash2_debug_noalloc_inject_error.argtypes = [i32]
@@ -188,6 +194,32 @@ def dflash2_set_lmhead_events(h, start, stop):
     _check(lib().dflash2_set_lmhead_events(h, start.cuda_event if start is not None else None,
                                            stop.cuda_event if stop is not None else None),
            "dflash2_set_lmhead_events")
+
+
+def dflash2_set_projection_events(h, events):
+    """events: a flat list of torch.cuda.Event (start, stop, start, stop, ...), already
+    created on the device (recorded once), or None.  The ctypes array is kept on the
+    binding while set."""
+    global _proj_events_keep
+    if events is None:
+        _proj_events_keep = None
+        _check(lib().dflash2_set_projection_events(h, None, 0), "dflash2_set_projection_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _proj_events_keep = arr
+    _check(lib().dflash2_set_projection_events(h, ctypes.cast(arr, ctypes.c_void_p), len(events) // 2),
+           "dflash2_set_projection_events")
+
+
+_proj_events_keep = None
+
+
+def dflash2_projection_launches(h) -> int:
+    return int(lib().dflash2_projection_launches(h))
+
+
+def dflash2_projection_bytes(h) -> int:
+    return int(lib().dflash2_projection_bytes(h))
 
 
 def dflash2_lmhead_bytes(h, n_req) -> int:

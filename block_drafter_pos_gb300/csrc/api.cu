@@ -67,6 +67,10 @@ struct dflash2_handle {
   double* inv_freq;
   int64_t launches;
   cudaEvent_t ev_lm0, ev_lm1;
+  // profiling: event pairs around the weight-projection launches of draft_block calls
+  cudaEvent_t* proj_ev;
+  int proj_pairs, proj_next;
+  bool in_draft;
 };
 
 namespace {
@@ -115,9 +119,13 @@ SegSpec seg(const CUtensorMap& wmap, const CUtensorMap& wide_map, const dflash2_
 }
 
 // Launches the segments on the GEMV (wide == false) or on the tensor-core GEMM.
+// proj: a drafter weight projection (not the LM head), bracketed by the profiling
+// events when they are set.
 dflash2_status run_gemv(dflash2_handle* h, bool wide, std::initializer_list<SegSpec> segs, cudaStream_t st,
-                        int fmt = -1) {
+                        int fmt = -1, bool proj = true) {
   if (fmt < 0) fmt = h->fmt;
+  const bool timed = proj && h->in_draft && h->proj_ev != nullptr && h->proj_next < h->proj_pairs;
+  if (timed) DF2_CHECK(cudaEventRecordWithFlags(h->proj_ev[2 * h->proj_next], st, cudaEventRecordExternal));
   GemvArgs a;
   memset(&a, 0, sizeof(a));
   int max_tiles = 0;
@@ -141,8 +149,22 @@ dflash2_status run_gemv(dflash2_handle* h, bool wide, std::initializer_list<SegS
   else
     DF2_CHECK(launch_gemv(a, fmt, max_tiles, h->num_sms, h->pdl, st));
   h->launches += 1;
+  if (timed) {
+    DF2_CHECK(cudaEventRecordWithFlags(h->proj_ev[2 * h->proj_next + 1], st, cudaEventRecordExternal));
+    ++h->proj_next;
+  }
   return DFLASH2_OK;
 }
+
+// Marks the span of one draft_block call (the projection events count from its start).
+struct DraftScope {
+  dflash2_handle* h;
+  explicit DraftScope(dflash2_handle* hh) : h(hh) {
+    h->in_draft = true;
+    h->proj_next = 0;
+  }
+  ~DraftScope() { h->in_draft = false; }
+};
 
 // Calls with at least this many requests run every projection on the tensor-core
 // GEMM (measured: with int8 weights it overtakes the GEMV at four requests, whose
@@ -406,6 +428,30 @@ dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* s
   return DFLASH2_OK;
 }
 
+dflash2_status dflash2_set_projection_events(dflash2_handle* h, void* const* events, int32_t n_pairs) {
+  if (!h || (events == nullptr) != (n_pairs == 0) || n_pairs < 0) return DFLASH2_E_INVAL;
+  h->proj_ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
+  h->proj_pairs = n_pairs;
+  return DFLASH2_OK;
+}
+
+int32_t dflash2_projection_launches(const dflash2_handle* h) {
+  if (!h) return -1;
+  // fc + first delta; per layer: q/k/v, o, mlp delta, gate/up, down, and the attention
+  // delta from the second layer on; the selector projection
+  return 1 + h->cfg.n_layers * 5 + (h->cfg.n_layers - 1) + 1;
+}
+
+int64_t dflash2_projection_bytes(const dflash2_handle* h) {
+  if (!h) return -1;
+  const int64_t H = h->H, G4 = 4 * h->G;
+  const int64_t per_layer = static_cast<int64_t>(h->qd) * H + 2 * static_cast<int64_t>(h->kvd) * H +
+                            H * h->qd + 3 * static_cast<int64_t>(h->F) * H + 2 * G4 * H;
+  const int64_t elems = per_layer * h->cfg.n_layers + H * h->KT + static_cast<int64_t>(h->cfg.rank) * H;
+  // bf16: 2 bytes per weight; Q8/g64: one code byte plus a bf16 scale and bias per 64
+  return h->fmt == DFLASH2_WEIGHTS_BF16 ? 2 * elems : elems + elems / 64 * 4;
+}
+
 dflash2_status dflash2_debug_set_pipeline_error(dflash2_handle* h, void* stream) {
   if (!h) return DFLASH2_E_INVAL;
   DF2_CHECK(cudaMemsetAsync(h->gemv_err, 1, sizeof(int), static_cast<cudaStream_t>(stream)));
@@ -434,6 +480,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     return DFLASH2_E_INVAL;
   if (!aligned16(taps) || !aligned16(k_cache) || !aligned16(v_cache)) return DFLASH2_E_INVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DraftScope scope(h);
   const dflash2_config& c = h->cfg;
   const int fmt = h->fmt;
   const bool pdl = h->pdl;
@@ -720,7 +767,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     dflash2_status s = run_gemv(
         h, true, {seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm, h->act_fin,
                       N8, R, h->V, H, h->lm_part)},
-        st, 0);
+        st, 0, false);
     if (s) return s;
     LogitsTopkArgs a = {};
     a.part = h->lm_part;
@@ -797,7 +844,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
     SegSpec sp = seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm, hidden, n_rows,
                      n_rows / 8, h->V, h->H, h->lm_part);
     sp.x_tiled = false;  // the caller's row-major hidden state: bulk tensor copies
-    dflash2_status s = run_gemv(h, true, {sp}, st, 0);
+    dflash2_status s = run_gemv(h, true, {sp}, st, 0, false);
     if (s) return s;
     LogitsTopkArgs a = {};
     a.part = h->lm_part;

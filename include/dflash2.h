@@ -261,6 +261,23 @@ int64_t dflash2_launch_count(const dflash2_handle* h);
  * path) on the call's stream.  NULL, NULL turns it off. */
 dflash2_status dflash2_set_lmhead_events(dflash2_handle* h, void* start, void* stop);
 
+/* Profiling hook: when `events` is non-NULL (an array of 2 * n_pairs cudaEvent_t
+ * passed as void*, kept alive by the caller while set), each dflash2_draft_block
+ * call records events[2i] right before and events[2i+1] right after its i-th
+ * drafter weight-projection launch (the taps projection with the first delta, then
+ * per layer q/k/v, o, delta, gate/up, down and, from the second layer on, the
+ * attention delta, and finally the selector projection; not the LM head), for
+ * i < n_pairs, on the call's stream.  An event record between two launches keeps the
+ * later one from overlapping the earlier one's tail, so the pairs time each launch
+ * alone.  NULL, 0 turns it off. */
+dflash2_status dflash2_set_projection_events(dflash2_handle* h, void* const* events, int32_t n_pairs);
+
+/* Number of drafter weight-projection launches of one dflash2_draft_block call, and
+ * the weight bytes they stream together (every drafter matrix once, Q8 scale and
+ * bias included), for roofline reports. */
+int32_t dflash2_projection_launches(const dflash2_handle* h);
+int64_t dflash2_projection_bytes(const dflash2_handle* h);
+
 /* Algorithmic bytes the LM-head + top-16 kernel of one draft_block call streams
  * (LM-head weights + activations + candidate outputs; on the tensor-core path
  * also the logits the GEMM writes and the top-16 kernel reads), for
