@@ -57,8 +57,13 @@ struct GemvPlanes {
   int bshift;         // log2 of the rows of one weight block (64 for the GEMV, 128 for the GEMM)
 };
 
+// (the element-wise kernels evaluate this per thread: in 32-bit arithmetic whenever
+// the product fits, since a 64-bit division costs several times as many instructions)
 DF2_HD inline int gemv_cta_of_stage(long long t, int C, long long T) {
-  return static_cast<int>(((t + 1) * static_cast<long long>(C) - 1) / T);
+  const unsigned long long num = static_cast<unsigned long long>(t + 1) * static_cast<unsigned long long>(C) - 1ull;
+  if (num <= 0xFFFFFFFFull && T <= 0xFFFFFFFFll)
+    return static_cast<int>(static_cast<unsigned int>(num) / static_cast<unsigned int>(T));
+  return static_cast<int>(num / static_cast<unsigned long long>(T));
 }
 
 DF2_HD inline int gemv_plane_count(const GemvPlanes& p, int m) {
@@ -91,7 +96,8 @@ bool tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void
 // for calls with many activation rows (8 * n_tiles <= 256): weight blocks of 128
 // rows, stages of 64 K (bf16) or 128 K (int8), activations one 16-bit plane, read
 // from the operand layout the element-wise kernels write (xt) or through xmap.
-// Fills stage_begin, total_stages and stage_k; returns the CTA count (one per SM).
+// Fills stage_begin, total_stages and stage_k; returns the CTA count (two per SM for
+// bf16, one for int8).
 int wide_plan(GemvArgs& a, int num_sms, int fmt);
 GemvPlanes wide_planes(const GemvArgs& a, int i, int C);
 int wide_max_planes(const GemvArgs& a, int i, int C);

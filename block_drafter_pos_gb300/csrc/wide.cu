@@ -4,30 +4,29 @@
 // new context rows for the key and value projections).
 //
 // Design (sm_103a):
-//  * Work is cut like the GEMV's: the stages (128-row weight block x 64 K) of the
-//    launch's segments are split into contiguous runs, one per CTA (one CTA per SM,
-//    stream-K), and a block shared by several CTAs gets one partial plane per CTA
-//    (plane = CTA - first CTA of the block), which the next kernel adds in order.
-//  * One CTA per SM with warp roles: warp 0 issues the bulk tensor copies of the
-//    weight tiles into a deep ring (they come from HBM and never depend on the
-//    previous kernel), warp 2 those of the activation tiles into a shallow one (they
-//    stay in L2), each completing on its stage's "full" mbarrier (128-byte swizzle);
-//    one thread of warp 1 issues tcgen05.mma (M = 128
-//    weight rows, N = the activation rows rounded up to 16, K = 16 per instruction,
-//    both operands from shared memory through matrix descriptors) into an fp32
-//    accumulator in tensor memory, and tcgen05.commit releases the stage; warps 4..7
-//    read a finished accumulator out of tensor memory (tcgen05.ld, one weight row
-//    per thread) and store the partial plane.  The accumulator is double-buffered
-//    (2 x 256 of the 512 tensor-memory columns), so the epilogue of one block
-//    overlaps the products of the next.
+//  * Work is cut like the GEMV's: the stages (weight block x stage K) of the
+//    launch's segments are split into contiguous runs, one per CTA (stream-K), and a
+//    block shared by several CTAs gets one partial plane per CTA (plane = CTA - first
+//    CTA of the block), which the next kernel adds in order.
+//  * Warp roles: warp 0 issues the bulk tensor copies of the weight tiles into a
+//    deep ring (they come from HBM and never depend on the previous kernel), warp 2
+//    those of the activation tiles into a shallow one (they stay in L2), each
+//    completing on its stage's "full" mbarrier (128-byte swizzle); one thread of
+//    warp 1 issues tcgen05.mma (M = 128 weight rows, N = the activation rows rounded
+//    up to 16, K = 16 per instruction) into fp32 accumulators in tensor memory, and
+//    tcgen05.commit releases the stage; warps 4..7 read a finished accumulator out
+//    of tensor memory (tcgen05.ld, one weight row per thread) and store the partial
+//    plane.  Accumulators are double-buffered where the columns allow, so the
+//    epilogue of one block overlaps the products of the next.
+//  * bf16 weights: two CTAs per SM, A and B both from shared memory through matrix
+//    descriptors; stages of one 128-row block x 64 K.
 //  * Q8/group64 weights ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias
-//    per group of 64 along K): the copy brings the int8 codes (64-byte swizzle), and
-//    warps 8..15 turn them into fp16 values in a ring of operand tiles (one weight
-//    row and half the stage's K per thread: byte permute against the 1024 exponent,
-//    w = q * s + b in fp16), release the code slot once the codes have been used,
-//    and hand the operand tile to the MMA thread through its mbarrier after a
-//    proxy fence.
-//    One stage is exactly one quantisation group along K.
+//    per group of 64 along K): the copy brings the int8 codes, and sixteen converter
+//    warps (two groups taking alternate stages) turn them into fp16 values
+//    (byte permute against the 1024 exponent, w = q * s + b in fp16) written
+//    straight into tensor memory (tcgen05.st), where the MMA reads its A operand.
+//    No fp16 tile passes through shared memory: no store bank conflicts, and the
+//    freed shared memory deepens the code ring.
 //  * The activations are read as one 16-bit plane (bf16 for bf16 weights, fp16 for
 //    Q8), the high plane of the buffers the element-wise kernels write.
 //  * Every mbarrier wait is bounded; a wait that gives up sets the error word and
@@ -54,7 +53,7 @@ using pipe::mbar_wait;
 using pipe::smem_u32;
 using pipe::tma_load_2d;
 
-constexpr int kTM = 128;         // weight rows per block: the MMA's M
+constexpr int kTM = 128;         // weight rows per MMA: the MMA's M
 constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of 16-bit values
 constexpr int kMaxN = 256;       // activation rows per product: the MMA's largest N
 constexpr int kMinStages = 4;    // shortest run of stages per CTA (small launches take fewer CTAs)
@@ -65,42 +64,44 @@ template <int FMT>
 constexpr int stage_k() { return FMT == 0 ? 64 : 128; }
 // CTAs per SM: bf16 runs two independent pipelines per SM (each with half the
 // tensor memory); int8 one, whose sixteen converter warps fill the register file.
+// (Measured with the operand in tensor memory: two int8 CTAs per SM with one
+// converter group each, or pairs of weight blocks sharing an activation tile, are
+// both slower.)
 constexpr int ctas_per_sm(int fmt) { return fmt == 0 ? 2 : 1; }
 
-// Three rings of shared-memory stages, each region on a 1 KB boundary (the swizzle
-// atoms): the weight copies W [128 rows][128 bytes] (bf16: the A operand itself;
-// int8: codes), which come from HBM; for int8 the fp16 operand tiles A (two atoms
-// [128 rows][64 K]) the converter warps write; and the activation tiles B
-// (stage_k / 64 atoms [NMAX rows][64 K]), which come from L2.  The accumulators:
-// kBufs of NMAX fp32 columns in tensor memory (two, so the epilogue of one block
-// overlaps the products of the next, where the columns allow).
+// Shared memory: two rings, each region on a 1 KB boundary (the swizzle atoms):
+// the weight copies W [128 rows][128 bytes] (bf16: the A operand itself; int8: the
+// codes), which come from HBM, and the activation tiles B (stage_k / 64 atoms
+// [NMAX rows][64 K]), which come from L2.  Tensor memory (columns of 128 lanes x
+// 32 bits): for int8 kDA slots of the fp16 A operand (64 columns: 128 K per weight
+// row, two values per column), then kBufs accumulators of NMAX fp32 columns.
 template <int FMT, int NMAX>
 struct WideGeo {
   static constexpr int kKS = stage_k<FMT>();
   static constexpr int kAtoms = kKS / kAtomK;
   static constexpr int kW = kTM * 128;
-  static constexpr int kA = FMT == 1 ? kTM * kKS * 2 : 0;
   static constexpr int kBAtom = NMAX * kAtomK * 2;
   static constexpr int kB = kAtoms * kBAtom;
   static constexpr int kCtas = ctas_per_sm(FMT);
   static constexpr int kTmemCols = 512 / kCtas;
-  static constexpr int kBufs = kTmemCols / NMAX >= 2 ? 2 : 1;
-  static constexpr int kDA = FMT == 1 ? 2 : 0;
+  static constexpr int kDA = FMT == 1 ? 2 : 0;            // A-operand slots in tensor memory (int8)
+  static constexpr int kACols = FMT == 1 ? kKS / 2 : 0;  // columns of one slot
+  static constexpr int kDCol0 = kDA * kACols;             // first accumulator column
+  static constexpr int kBufs = (kTmemCols - kDCol0) / NMAX >= 2 ? 2 : 1;
   static constexpr int kDB = FMT == 1 ? 2 : (NMAX == 128 ? 2 : 1);
-  static constexpr int kRing = (FMT == 0 ? 100 : NMAX == 256 ? 224 : 208) * 1024;
-  static constexpr int kDW = (kRing - kDB * kB - kDA * kA) / kW;
-  static constexpr int kOffA = kDW * kW;
-  static constexpr int kOffB = kOffA + kDA * kA;
+  static constexpr int kRing = (FMT == 0 ? 100 : 224) * 1024;
+  static constexpr int kDW = (kRing - kDB * kB) / kW;
+  static constexpr int kOffB = kDW * kW;
   static constexpr int kSmem = kOffB + kDB * kB + 1024;
-  static constexpr int kConvGroups = 2;  // int8: converter warp groups, taking alternate stages
-  static constexpr int kWarps = FMT == 1 ? 8 + 8 * kConvGroups : 8;
+  static constexpr int kConvGroups = FMT == 1 ? 2 : 0;  // int8: converter warp groups, taking alternate stages
+  static constexpr int kWarps = 8 + 8 * kConvGroups;
+  static_assert(kDCol0 + NMAX <= kTmemCols, "tensor memory columns");
   static_assert(kDW >= 2, "weight ring");
-  // int8: converter group g takes the stages i = g (mod kConvGroups) and waits on the
-  // code slot i mod kDW with the parity of i's use of that slot.  That wait is only
-  // sound if the slot's previous use (stage i - kDW) has landed, which holds when
-  // each group owns its slots (kDW == kConvGroups), or when the operand-slot wait the
-  // group passed at stage i - kConvGroups (the products of stage i - kConvGroups - kDA
-  // are done) already covers stage i - kDW.
+  // int8: converter group g takes the stages i = g (mod 2) and waits on the code slot
+  // i mod kDW with the parity of i's use of that slot.  That wait is only sound if the
+  // slot's previous use (stage i - kDW) has landed, which holds when the A-slot wait
+  // the group passed at stage i - 2 (the products of stage i - 2 - kDA are done, so
+  // their codes were converted) covers stage i - kDW.
   static_assert(FMT == 0 || kDW == kConvGroups || kDW >= kDA + kConvGroups, "code ring depth vs converter groups");
   static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
 };
@@ -150,8 +151,28 @@ DF2_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-DF2_DEV void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane (lane group of the
+// warp: warp w reaches lanes 32 (w mod 4) .. 32 (w mod 4) + 31).
+DF2_DEV void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+DF2_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D (tensor memory) += A (tensor memory, [128 rows][16 K], row i in lane i, two 16-bit
+// values per column in K order) x B (shared memory descriptor).
+DF2_DEV void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Position in the launch's stage sequence: CTA c takes [c T / C, (c + 1) T / C).
@@ -217,11 +238,13 @@ DF2_DEV uint32_t dequant_pair(uint32_t codes_biased, uint32_t sel, __half2 s, __
 }
 
 template <int FMT, int NMAX>
-__global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, NMAX>::kCtas) wide_kernel(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, NMAX>::kCtas)
+    wide_kernel(const __grid_constant__ GemvArgs a) {
   using Geo = WideGeo<FMT, NMAX>;
   using Cur = WCursor<Geo::kKS>;
   constexpr int DW = Geo::kDW, DB = Geo::kDB, DA = Geo::kDA > 0 ? Geo::kDA : 1;
   constexpr int kConv = 8;  // converter warps per group (int8)
+  constexpr int NG = Geo::kConvGroups > 0 ? Geo::kConvGroups : 1;
   constexpr int NB = Geo::kBufs;
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t wfull_b[DW], wempty_b[DW], bfull_b[DB], bempty_b[DB], afull_b[DA], aempty_b[DA];
@@ -253,7 +276,7 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
     mbar_init_count(done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (wid == 1) {  // the whole warp allocates the accumulator columns (and frees them at the end)
+  if (wid == 1) {  // the whole warp allocates the tensor-memory columns (and frees them at the end)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
                  "r"(Geo::kTmemCols)
                  : "memory");
@@ -339,7 +362,7 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
             break;
           }
           tc_fence_after();
-          d_tmem = tmem + static_cast<uint32_t>(buf * NMAX);
+          d_tmem = tmem + static_cast<uint32_t>(Geo::kDCol0 + buf * NMAX);
           idesc = instr_desc(FMT, n_mma_of(a.seg[c.seg]));
         }
         const int sb = i % DB, sw = i % DW, sa = i % DA;
@@ -351,14 +374,23 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
           break;
         }
         tc_fence_after();
-        const uint32_t aaddr = FMT == 0 ? ring + sw * Geo::kW : ring + Geo::kOffA + sa * Geo::kA;
         const uint32_t baddr = ring + Geo::kOffB + sb * Geo::kB;
 #pragma unroll
         for (int j = 0; j < Geo::kAtoms; ++j) {
-          const uint64_t ad = sw128_desc(aaddr + j * kTM * 128), bd = sw128_desc(baddr + j * Geo::kBAtom);
+          const uint64_t bd = sw128_desc(baddr + j * Geo::kBAtom);
+          if (FMT == 0) {
+            const uint64_t ad = sw128_desc(ring + sw * Geo::kW + j * kTM * 128);
 #pragma unroll
-          for (int k = 0; k < kAtomK / 16; ++k)  // 16 K = 32 bytes further along the swizzled rows
-            umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (first && j == 0 && k == 0) ? 0u : 1u);
+            for (int k = 0; k < kAtomK / 16; ++k)  // 16 K = 32 bytes further along the swizzled rows
+              umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (first && j == 0 && k == 0) ? 0u : 1u);
+          } else {
+            // A from tensor memory: slot sa, 8 columns per 16 K
+            const uint32_t a_col = tmem + static_cast<uint32_t>(sa * Geo::kACols + j * (kAtomK / 2));
+#pragma unroll
+            for (int k = 0; k < kAtomK / 16; ++k)
+              umma_f16_ts(d_tmem, a_col + static_cast<uint32_t>(8 * k), bd + 2 * k, idesc,
+                          (first && j == 0 && k == 0) ? 0u : 1u);
+          }
         }
         // the stages are free once these products are done
         umma_commit(bempty + 8 * sb);
@@ -393,7 +425,8 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
         const int n_rows = sg.n_tiles * 8, nm = n_mma_of(sg);
         const int m = c.row0 + quarter * 32 + lane;
         float* out = sg.out + static_cast<size_t>(c.plane(a)) * n_rows * sg.M + m;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * NMAX);
+        const uint32_t taddr =
+            tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(Geo::kDCol0 + buf * NMAX);
         for (int n0 = 0; n0 < nm; n0 += 16) {
           uint32_t r[16];
           tmem_ld16(taddr + n0, r);
@@ -409,14 +442,15 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
       c.next(a);
     }
   } else if (FMT == 1 && wid >= 8) {
-    // ------------------------------------------------------------ int8 codes -> fp16 operand tiles
+    // ------------------------------------------------------------ int8 codes -> fp16 A operand in tensor memory
     const int cw = wid - 8;
-    const int grp = cw >> 3;                    // this group converts the stages i with i mod 2 == grp
-    const int r = (cw & 3) * 32 + lane;         // weight row within the block
+    const int grp = cw >> 3;                    // this group converts the stages i with i mod NG == grp
+    const int quarter = cw & 3;                 // = wid mod 4: the lane group this warp reaches
+    const int r = quarter * 32 + lane;          // weight row within the block
     const int hk = (cw >> 2) & 1;               // 64-K half of the stage: one quantisation group, one atom
     Cur c;
     c.start(a);
-    if (grp == 1) c.next(a);
+    for (int g = 0; g < grp; ++g) c.next(a);
     auto affine = [&](const Cur& cc, uint16_t& s, uint16_t& b) {
       const GemvSeg& sg = a.seg[cc.seg];
       const size_t idx = static_cast<size_t>(cc.row0 + r) * (sg.K >> 6) + (cc.kabs >> 6) + hk;
@@ -429,10 +463,9 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
     while (c.valid) {
       const int sw = i % DW, sa = i % DA;
       Cur cn = c;
-      cn.next(a);
-      if (cn.valid) cn.next(a);
+      for (int g = 0; g < NG && cn.valid; ++g) cn.next(a);
       uint16_t s_nx = s_cur, b_nx = b_cur;
-      if (cn.valid) affine(cn, s_nx, b_nx);  // the next group's scale and bias, loaded during this stage
+      if (cn.valid) affine(cn, s_nx, b_nx);  // the next stage's scale and bias, loaded during this one
       if (!mbar_wait(wfull + 8 * sw, static_cast<uint32_t>((i / DW) & 1))) {
         ok = false;
         break;
@@ -442,40 +475,42 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
       uint4 w[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) w[j] = lds128(crow + (((4 * hk + j) ^ (r & 7)) << 4));
+      // the products that read this A slot last (stage i - DA) are done
       if (i >= DA && !mbar_wait(aempty + 8 * sa, static_cast<uint32_t>(((i / DA) + 1) & 1))) {
         ok = false;
         break;
       }
-      // atom hk of the operand tile: 128-byte rows, 128-byte swizzle
-      const uint32_t arow = ring + Geo::kOffA + sa * Geo::kA + hk * (kTM * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+      tc_fence_after();
       const __half2 sh = __float2half2_rn(bf16_to_f32(s_cur)), bh = __float2half2_rn(bf16_to_f32(b_cur));
+      uint32_t hv[32];  // 64 fp16 values of K 64 hk .. 64 hk + 63 in K order, two per column
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {  // codes 16 j .. 16 j + 15 of the group -> fp16 pieces 2 j, 2 j + 1
+      for (int j = 0; j < 4; ++j) {
         const uint32_t u[4] = {w[j].x ^ 0x80808080u, w[j].y ^ 0x80808080u, w[j].z ^ 0x80808080u,
                                w[j].w ^ 0x80808080u};
-        uint32_t hv[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          hv[2 * m] = dequant_pair(u[m], 0x4140, sh, bh);
-          hv[2 * m + 1] = dequant_pair(u[m], 0x4342, sh, bh);
+          hv[8 * j + 2 * m] = dequant_pair(u[m], 0x4140, sh, bh);
+          hv[8 * j + 2 * m + 1] = dequant_pair(u[m], 0x4342, sh, bh);
         }
-        sts128(arow + (((2 * j) ^ (r & 7)) << 4), hv[0], hv[1], hv[2], hv[3]);
-        sts128(arow + (((2 * j + 1) ^ (r & 7)) << 4), hv[4], hv[5], hv[6], hv[7]);
       }
+      tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                    static_cast<uint32_t>(sa * Geo::kACols + hk * (kAtomK / 2)),
+                hv);
       // Every lane has used its codes (the stores above depend on them), so none of
       // its loads of the code slot is still in flight: the slot is free for the next
       // copy.  Releasing it before the values are used would let the copy overwrite
       // a slot a load is still reading.
       __syncwarp();
       if (lane == 0) mbar_arrive(wempty + 8 * sw);
-      // generic-proxy stores become visible to the tensor cores' reads before the hand-over
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // the tensor-memory stores complete before the hand-over to the MMA thread
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(afull + 8 * sa);
       s_cur = s_nx;
       b_cur = b_nx;
       c = cn;
-      i += 2;
+      i += NG;
     }
   }
   if (!ok && a.err != nullptr) atomicExch(a.err, 1);
