@@ -25,7 +25,9 @@ in the same process (`--no-r16` skips them): `r16`, 16 requests (configuration 5
 Q8 weights, ragged contexts 512..32768, mixed temperatures), its 100 consecutive
 steps with the emitted tokens appended between steps, captured as one graph;
 `q8_r1` (configuration 3: Q8, one request, context 2048, T = 1.0) and `r4`
-(configuration 4: Q8, four requests, context 8192, T = 0.7), 100 steps each.
+(configuration 4: Q8, four requests, context 8192, T = 0.7), 100 steps each; and
+`tree`: the draft-tree variant of the default workload (draft block + tree of 12
+nodes + greedy tree verification), 100 steps.
 
 `--impl reference` times the CPU oracle (the only reference this method has
 here) on the same workload and prints the same line with "impl": "reference".
@@ -329,6 +331,70 @@ def measure_point(args, world, local_rank, cfg):
     return out
 
 
+def measure_tree(bd, h, R, S, wl, budget=12, steps=100):
+    """The draft-tree variant of the step on the same workload (the pages' DDTree,
+    budget 12): draft block + tree build + greedy tree verification against
+    budget + 1 target rows per request (the root's and each node's), captured as one
+    graph of `steps` steps.  The rows are the drafter's logits of the node's next
+    block position plus N(0, sigma) noise, built once from an untimed tree."""
+    import torch
+    g = wl.geom
+    dev = S["anchors"].device
+    z = lambda shape, dt=torch.int32: torch.zeros(shape, dtype=dt, device=dev)
+    T = {"token": z((R, budget)), "parent": z((R, budget)), "depth": z((R, budget)),
+         "score": z((R, budget), torch.float32), "n": z((R,)), "status": z((R,)), "n_acc": z((R,)),
+         "emitted": z((R, 8)), "n_emit": z((R,))}
+
+    def build():
+        bd.dflash2_draft_block(h, R, S["anchors"], S["ctx_len"], S["n_new"], S["taps"], S["kc"], S["vc"],
+                               S["cand_ids"], S["cand_logits"], S["gate"], None)
+        bd.dflash2_tree_build(h, R, budget, S["anchors"], S["cand_ids"], S["cand_logits"], S["gate"], T["token"],
+                              T["parent"], T["depth"], T["score"], T["n"], None, T["status"])
+
+    build()
+    torch.cuda.synchronize()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed + 7)
+    rows = torch.empty((R, budget + 1, g.vocab), dtype=torch.float32, device=dev)
+    dep = T["depth"].clamp(1, 7) - 1
+    for r in range(R):
+        rows[r, 0] = S["logits"][r, 0]
+        rows[r, 1:] = S["logits"][r, torch.clamp(dep[r] + 1, max=6).long()]
+        rows[r] += torch.randn((budget + 1, g.vocab), generator=gen, device=dev) * wl.sigma[r]
+
+    def one():
+        build()
+        bd.dflash2_tree_verify(h, R, budget, rows, T["token"], T["parent"], T["n"], T["n_acc"], T["emitted"],
+                               T["n_emit"], T["status"])
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.current_stream()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(stream)
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(graph, stream=cs):
+            for _ in range(steps):
+                one()
+    stream.wait_stream(cs)
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    assert int(T["status"].abs().sum().item()) == 0
+    del graph
+    return {"workload": wl.name, "budget": budget, "steps": steps, "value": 1e3 / ms, "unit": "steps/s",
+            "ms_per_step": ms, "nodes_per_step": int(T["n"].sum().item()),
+            "emitted_per_step": float(T["n_emit"].float().mean().item()),
+            "timing": "draft block + tree build + greedy tree verify, one CUDA graph; target rows resident"}
+
+
 def measure_projections(bd, h, one_step, restore, n_launch, proj_bytes, steps=10):
     """Roofline of the drafter's weight projections (the GEMV / tensor-core GEMM family,
     every projection launch of the step but the LM head): a separate graph of `steps`
@@ -504,6 +570,10 @@ def main_ours(args, rank, world, local_rank):
     proj = measure_projections(bd, h, one_step, restore, bd.dflash2_projection_launches(h),
                                bd.dflash2_projection_bytes(h))
     restore()
+    tree = None
+    if not loop:
+        tree = measure_tree(bd, h, R, S, wl)
+        restore()
     pk = peaks()
     lm_bytes = bd.dflash2_lmhead_bytes(h, R)
     lm_avg_s = statistics.mean(lm_ms) / 1e3
@@ -533,6 +603,7 @@ def main_ours(args, rank, world, local_rank):
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
                      "projections": proj},
         "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "tree": tree,
         "gpu_launches": int(launches_per_step * K),
         "clocks": clk,
         "setup_s": setup_s,

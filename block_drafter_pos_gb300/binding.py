@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
         L.dflash2_set_lmhead_events.argtypes = [vp, vp, vp]
         L.dflash2_lmhead_bytes.argtypes = [vp, i32]
         L.dflash2_lmhead_bytes.restype = i64
+        L.dflash2_tree_build.argtypes = [vp, i32, i32] + [vp] * 12
+        L.dflash2_tree_build.restype = i32
+        L.dflash2_tree_verify.argtypes = [vp, i32, i32] + [vp] * 9
+        L.dflash2_tree_verify.restype = i32
         L.dflash2_set_projection_events.argtypes = [vp, vp, i32]
         L.dflash2_set_projection_events.restype = i32
         L.dflash2_projection_launches.argtypes = [vp]
@@ -153,6 +157,20 @@ def dflash2_verify(h, n_req, target_logits, path, cand_ids, q_rows, temperature,
     _check(lib().dflash2_verify(h, n_req, _p(target_logits), _p(path), _p(cand_ids), _p(q_rows), _p(temperature),
                                 _p(seed), _p(philox_offset), _p(n_accepted), _p(emitted), _p(n_emitted),
                                 _p(probs_out), _p(status), _stream(stream)), "dflash2_verify")
+
+
+def dflash2_tree_build(h, n_req, budget, anchor_ids, cand_ids, cand_logits, gate, node_token, node_parent, node_depth,
+                       node_score, n_nodes, scores_out, status, stream=None):
+    _check(lib().dflash2_tree_build(h, n_req, budget, _p(anchor_ids), _p(cand_ids), _p(cand_logits), _p(gate),
+                                    _p(node_token), _p(node_parent), _p(node_depth), _p(node_score), _p(n_nodes),
+                                    _p(scores_out), _p(status), _stream(stream)), "dflash2_tree_build")
+
+
+def dflash2_tree_verify(h, n_req, budget, target_logits, node_token, node_parent, n_nodes, n_accepted, emitted,
+                        n_emitted, status, stream=None):
+    _check(lib().dflash2_tree_verify(h, n_req, budget, _p(target_logits), _p(node_token), _p(node_parent),
+                                     _p(n_nodes), _p(n_accepted), _p(emitted), _p(n_emitted), _p(status),
+                                     _stream(stream)), "dflash2_tree_verify")
 
 
 def dflash2_set_select_mode(h, mode: int):

@@ -22,6 +22,8 @@
 
 using namespace df2;
 
+static_assert(DFLASH2_TREE_MAX_NODES == kTreeMaxNodes, "draft-tree bound of the header and the kernels");
+
 struct dflash2_handle {
   dflash2_config cfg;
   dflash2_weights w;
@@ -52,6 +54,8 @@ struct dflash2_handle {
   float* sel_lat;            // [max_req][7][16][16] selector lattice scratch
   int32_t* sel_bad;          // [max_req][7] nonfinite flags per position
   unsigned int* sel_cnt;     // [max_req] selector position counters (zero between launches)
+  VerifyStat* tstats;        // [max_req][kTreeMaxNodes + 1][n_verify_chunks] draft-tree row statistics
+  unsigned int* tree_cnt;    // [max_req] draft-tree verify counters (zero between launches)
   int select_mode;           // 0: sequential walk, 1: Viterbi for greedy requests
   // scratch
   char* arena;
@@ -367,6 +371,9 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->sel_lat), static_cast<size_t>(max_requests) * 7 * 16 * 16 * 4},
       {reinterpret_cast<void**>(&h->sel_bad), static_cast<size_t>(max_requests) * 7 * 4},
       {reinterpret_cast<void**>(&h->sel_cnt), static_cast<size_t>(max_requests) * 4},
+      {reinterpret_cast<void**>(&h->tstats),
+       static_cast<size_t>(max_requests) * (kTreeMaxNodes + 1) * h->n_verify_chunks * sizeof(VerifyStat)},
+      {reinterpret_cast<void**>(&h->tree_cnt), static_cast<size_t>(max_requests) * 4},
   };
   h->lo_a = N * h->H;
   h->lo_qkv = 2 * N * h->H;
@@ -941,6 +948,73 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   a.fmt = h->fmt;
   a.V = h->V;
   DF2_CHECK(launch_select(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
+  h->launches++;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_tree_build(dflash2_handle* h, int32_t n_req, int32_t budget, const int32_t* anchor_ids,
+                                  const int32_t* cand_ids, const float* cand_logits, const float* gate,
+                                  int32_t* node_token, int32_t* node_parent, int32_t* node_depth, float* node_score,
+                                  int32_t* n_nodes, float* scores_out, int32_t* status, void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
+  if (budget < 1 || budget > DFLASH2_TREE_MAX_NODES) return DFLASH2_E_INVAL;
+  if (!anchor_ids || !cand_ids || !cand_logits || !gate || !node_token || !node_parent || !node_depth ||
+      !node_score || !n_nodes || !status)
+    return DFLASH2_E_INVAL;
+  SelectArgs a = {};
+  a.anchor_ids = anchor_ids;
+  a.cand_ids = cand_ids;
+  a.cand_logits = cand_logits;
+  a.gate = gate;
+  a.cb_a = h->w.cb_a.w;
+  a.cb_a_scale = static_cast<const uint16_t*>(h->w.cb_a.scale);
+  a.cb_a_bias = static_cast<const uint16_t*>(h->w.cb_a.bias);
+  a.cb_b = h->w.cb_b.w;
+  a.cb_b_scale = static_cast<const uint16_t*>(h->w.cb_b.scale);
+  a.cb_b_bias = static_cast<const uint16_t*>(h->w.cb_b.bias);
+  a.scores_out = scores_out;
+  a.status = status;
+  a.lat = h->sel_lat;
+  a.bad = h->sel_bad;
+  a.counters = h->sel_cnt;
+  a.pipe_err = h->gemv_err;
+  a.rank = h->cfg.rank;
+  a.fmt = h->fmt;
+  a.V = h->V;
+  a.tree_budget = budget;
+  a.t_token = node_token;
+  a.t_parent = node_parent;
+  a.t_depth = node_depth;
+  a.t_score = node_score;
+  a.t_n = n_nodes;
+  DF2_CHECK(launch_select(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
+  h->launches++;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_tree_verify(dflash2_handle* h, int32_t n_req, int32_t budget, const float* target_logits,
+                                   const int32_t* node_token, const int32_t* node_parent, const int32_t* n_nodes,
+                                   int32_t* n_accepted, int32_t* emitted, int32_t* n_emitted, int32_t* status,
+                                   void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
+  if (budget < 1 || budget > DFLASH2_TREE_MAX_NODES) return DFLASH2_E_INVAL;
+  if (!target_logits || !node_token || !node_parent || !n_nodes || !n_accepted || !emitted || !n_emitted || !status)
+    return DFLASH2_E_INVAL;
+  TreeVerifyArgs a = {};
+  a.logits = target_logits;
+  a.token = node_token;
+  a.parent = node_parent;
+  a.n_nodes = n_nodes;
+  a.stats = h->tstats;
+  a.counters = h->tree_cnt;
+  a.n_accepted = n_accepted;
+  a.emitted = emitted;
+  a.n_emitted = n_emitted;
+  a.status = status;
+  a.V = h->V;
+  a.n_chunks = h->n_verify_chunks;
+  a.budget = budget;
+  DF2_CHECK(launch_tree_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches++;
   return DFLASH2_OK;
 }

@@ -206,8 +206,18 @@ struct SelectArgs {
   int rank, fmt, V;
   int mode;                    // 0: sequential walk; 1: globally best path (Viterbi) for greedy requests
   const int* pipe_err;         // nonzero: a pipeline wait of the step's draft gave up (may be NULL)
+  // draft tree instead of a path (tree_budget > 0): best-first growth over the lattice
+  int tree_budget;
+  int32_t* t_token;            // [R][tree_budget]
+  int32_t* t_parent;           // [R][tree_budget]: -1 = the root (anchor), else an earlier node
+  int32_t* t_depth;            // [R][tree_budget]: block position 1..7
+  float* t_score;              // [R][tree_budget]: cumulative log-probability
+  int32_t* t_n;                // [R]: nodes built
 };
+constexpr int kTreeMaxNodes = 32;
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st);
+
+
 
 // ---------------------------------------------------------------- verify
 constexpr int kVerifyChunk = 4096;
@@ -236,6 +246,22 @@ struct VerifyArgs {
   int V, n_chunks;
 };
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st);
+
+// ---------------------------------------------------------------- draft-tree verification (greedy)
+struct TreeVerifyArgs {
+  const float* logits;         // [R][budget + 1][V]: row 0 the root, row 1 + k node k
+  const int32_t* token;        // [R][budget]
+  const int32_t* parent;       // [R][budget]
+  const int32_t* n_nodes;      // [R]
+  VerifyStat* stats;           // [R][budget + 1][n_chunks]
+  unsigned int* counters;      // [R] (zero between launches)
+  int32_t* n_accepted;
+  int32_t* emitted;            // [R][8]
+  int32_t* n_emitted;
+  int32_t* status;
+  int V, n_chunks, budget;
+};
+cudaError_t launch_tree_verify(const TreeVerifyArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- serving-loop state update
 struct AdvanceArgs {

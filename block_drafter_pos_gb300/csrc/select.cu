@@ -40,6 +40,10 @@ struct SelSmem {
   int cids[kP][kK];
   float lat[kP][kK][kK];        // the walker's copy of the lattice
   uint8_t back[kP][kK];         // Viterbi: best predecessor of each candidate
+  // draft tree: node 0 is the root (the anchor), nodes 1..n the tree's
+  float t_score[kTreeMaxNodes + 1];
+  int t_cand[kTreeMaxNodes + 1], t_depth[kTreeMaxNodes + 1];
+  uint32_t t_taken[kTreeMaxNodes + 1];  // children already in the tree (bit c)
   int bad;
   int last;
 };
@@ -90,6 +94,92 @@ DF2_DEV float edge_dot(const SelSmem& sm, int fmt, int ra, int rb) {
     }
   }
   return s;
+}
+
+// Draft tree of one request ("qwen35: DSpark speculative decoding ... #625", DDTree
+// commit: each expansion scores the candidates as the draft log-prob plus the
+// selector compatibility with the branch's actual parent, log-softmax-normalised per
+// position, so best-first comparisons across depths are on a log-prob scale).  The
+// lattice holds unary logit + compatibility; the vocabulary normaliser of the draft
+// log-prob is a per-position constant and cancels in the per-parent log-softmax.
+// One warp: each lattice row (position, parent candidate) is turned into log q in
+// place, then the tree grows best-first: every step adds the highest-scoring child,
+// over the root and every node already in, that is not in yet (equal scores: the
+// earlier parent, then the smaller candidate index), until the budget is reached.
+// FP32 throughout; node k of the output is tree node k + 1 (parent -1 = the root).
+__device__ void tree_grow(const SelectArgs& a, SelSmem& sm, int r) {
+  const int lane = threadIdx.x & 31;
+  for (int row = lane; row < kP * kK; row += 32) {
+    float* v = sm.lat[row / kK][row % kK];
+    float m = v[0];
+#pragma unroll
+    for (int c = 1; c < kK; ++c) m = fmaxf(m, v[c]);
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kK; ++c) s += expf(v[c] - m);
+    const float lse = m + logf(s);
+#pragma unroll
+    for (int c = 0; c < kK; ++c) v[c] -= lse;
+  }
+  if (lane == 0) {
+    sm.t_score[0] = 0.f;
+    sm.t_cand[0] = 0;  // position 1's rows all come from the anchor: row 0
+    sm.t_depth[0] = 0;
+    sm.t_taken[0] = 0u;
+  }
+  __syncwarp();
+  const size_t o = static_cast<size_t>(r) * a.tree_budget;
+  int n = 0;
+  while (n < a.tree_budget) {
+    // this lane's best option over parents lane, lane + 32 (node indices 0..n)
+    float bv = -INFINITY;
+    int bq = 0x7FFFFFFF, bc = 0x7FFFFFFF;
+    for (int q = lane; q <= n; q += 32) {
+      const int d = sm.t_depth[q];
+      if (d >= kP) continue;
+      const float base = sm.t_score[q];
+      const float* row = sm.lat[d][sm.t_cand[q]];
+      const uint32_t taken = sm.t_taken[q];
+      for (int c = 0; c < kK; ++c) {
+        if (taken & (1u << c)) continue;
+        const float v = base + row[c];
+        if (v > bv || (v == bv && (q < bq || (q == bq && c < bc)))) {
+          bv = v;
+          bq = q;
+          bc = c;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oq = __shfl_xor_sync(0xffffffffu, bq, off), oc = __shfl_xor_sync(0xffffffffu, bc, off);
+      if (ov > bv || (ov == bv && (oq < bq || (oq == bq && oc < bc)))) {
+        bv = ov;
+        bq = oq;
+        bc = oc;
+      }
+    }
+    if (bq == 0x7FFFFFFF) break;  // every node is at the last position and every child is in
+    ++n;
+    if (lane == 0) {
+      const int d = sm.t_depth[bq] + 1;
+      sm.t_score[n] = bv;
+      sm.t_cand[n] = bc;
+      sm.t_depth[n] = d;
+      sm.t_taken[n] = 0u;
+      sm.t_taken[bq] |= 1u << bc;
+      a.t_token[o + n - 1] = sm.cids[d - 1][bc];
+      a.t_parent[o + n - 1] = bq - 1;
+      a.t_depth[o + n - 1] = d;
+      a.t_score[o + n - 1] = bv;
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    a.t_n[r] = n;
+    a.status[r] = 0;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
@@ -191,18 +281,26 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   auto& cids = sm.cids;
   if (wid != 0) return;
   // ---- the walk: one warp, lane j < 16 holds candidate j
-  const float T = a.temperature[r];
-  int32_t* path = a.path + static_cast<size_t>(r) * kP;
-  float* qrow = a.q_rows + static_cast<size_t>(r) * kP * kK;
+  const float T = a.tree_budget > 0 ? 0.f : a.temperature[r];  // the tree is built for greedy verification
+  int32_t* path = a.tree_budget > 0 ? nullptr : a.path + static_cast<size_t>(r) * kP;
+  float* qrow = a.tree_budget > 0 ? nullptr : a.q_rows + static_cast<size_t>(r) * kP * kK;
   // a weight-pipeline wait of this step's draft that gave up leaves its candidates undefined
   const bool pipe_bad = a.pipe_err != nullptr && __ldcg(a.pipe_err) != 0;
   if (!(T >= 0.f) || bad || pipe_bad) {
-    if (lane < kP) path[lane] = -1;
-    for (int e = lane; e < kP * kK; e += 32) qrow[e] = 0.f;
+    if (a.tree_budget > 0) {
+      if (lane == 0) a.t_n[r] = 0;
+    } else {
+      if (lane < kP) path[lane] = -1;
+      for (int e = lane; e < kP * kK; e += 32) qrow[e] = 0.f;
+    }
     if (lane == 0) a.status[r] = pipe_bad ? 3 : (T >= 0.f) ? 2 : 1;
     return;
   }
   const bool live = lane < kK;
+  if (a.tree_budget > 0) {
+    tree_grow(a, sm, r);
+    return;
+  }
   if (T == 0.f && a.mode == 1) {
     // globally best path: best_1(c) = s_1(c); best_i(c) = max_p best_{i-1}(p) + s_i(p, c)
     // (float32 sums; equal -> the predecessor with the smaller id), then read back

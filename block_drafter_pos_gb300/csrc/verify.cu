@@ -438,7 +438,179 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   chain_body(a, r);
 }
 
+// ------------------------------------------------------------------ draft tree, greedy
+// Greedy verification of a draft tree ("qwen35: DSpark speculative decoding ...
+// #625", DDTree commits: tree verification emits the text plain decoding emits).
+// Pass 1: one CTA per (request, target row, 4096-id chunk): chunk max, argmax
+// (smallest id on ties), NaN / +inf flags; rows past the request's tree are skipped
+// but still counted.  The CTA completing a request's set folds each row's argmax and
+// walks the tree from the root: move to the child carrying the current row's argmax
+// while one exists; emit the path, then the last row's argmax.
+__device__ void tree_chain(const TreeVerifyArgs& a, int r) {
+  __shared__ int am[kTreeMaxNodes + 1], bad_row[kTreeMaxNodes + 1];
+  const int n = min(max(a.n_nodes[r], 0), a.budget);
+  int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
+  if (a.status[r] != 0) {
+    if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
+    if (threadIdx.x == 0) {
+      a.n_accepted[r] = 0;
+      a.n_emitted[r] = 0;
+    }
+    return;
+  }
+  // warp w folds rows w, w + 8, ... (lane-strided over chunks, fixed shuffle tree)
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int row = w; row <= n; row += 8) {
+    const VerifyStat* sj = a.stats + (static_cast<size_t>(r) * (a.budget + 1) + row) * a.n_chunks;
+    float M = -INFINITY;
+    int A = 0x7FFFFFFF, F = 0;
+    for (int c = lane; c < a.n_chunks; c += 32) {
+      const VerifyStat sc = ldst(sj + c);
+      F |= sc.flags;
+      if (sc.m > M || (sc.m == M && sc.arg < A)) {
+        M = sc.m;
+        A = sc.arg;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, M, o);
+      const int oa = __shfl_xor_sync(0xffffffffu, A, o);
+      if (om > M || (om == M && oa < A)) {
+        M = om;
+        A = oa;
+      }
+      F |= __shfl_xor_sync(0xffffffffu, F, o);
+    }
+    if (lane == 0) {
+      am[row] = A;
+      bad_row[row] = F != 0 || !(M > -INFINITY) || !(M < INFINITY);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  int bad = 0;
+  for (int row = 0; row <= n; ++row) bad |= bad_row[row];
+  if (bad) {
+    for (int j = 0; j < kB; ++j) emitted[j] = -1;
+    a.n_accepted[r] = 0;
+    a.n_emitted[r] = 0;
+    a.status[r] = 2;
+    return;
+  }
+  const int32_t* tok = a.token + static_cast<size_t>(r) * a.budget;
+  const int32_t* par = a.parent + static_cast<size_t>(r) * a.budget;
+  int cur = -1, acc = 0;
+  while (acc < kB - 1) {
+    const int t = am[cur + 1];
+    int nxt = -1;
+    for (int k = 0; k < n; ++k)
+      if (par[k] == cur && tok[k] == t) {
+        nxt = k;
+        break;
+      }
+    if (nxt < 0) break;
+    emitted[acc++] = t;
+    cur = nxt;
+  }
+  emitted[acc] = am[cur + 1];
+  for (int j = acc + 1; j < kB; ++j) emitted[j] = -1;
+  a.n_accepted[r] = acc;
+  a.n_emitted[r] = acc + 1;
+}
+
+__global__ void __launch_bounds__(256) tree_stats_kernel(const TreeVerifyArgs a) {
+  __shared__ float sm_m[8];
+  __shared__ int sm_a[8], sm_f[8];
+  pdl_begin_early();
+  const int r = blockIdx.x / (a.budget + 1), row = blockIdx.x % (a.budget + 1);
+  const int chunk = blockIdx.y;
+  const int n = min(max(a.n_nodes[r], 0), a.budget);
+  if (row <= n) {
+    const float* z = a.logits + (static_cast<size_t>(r) * (a.budget + 1) + row) * a.V;
+    const int v0 = chunk * kVerifyChunk;
+    const int v1 = min(a.V, v0 + kVerifyChunk);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    constexpr int kPer = kVerifyChunk / 256;
+    float xs[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = v0 + threadIdx.x + 256 * j;
+      xs[j] = v < v1 ? z[v] : -INFINITY;
+    }
+    float m = -INFINITY;
+    int arg = 0x7FFFFFFF, flags = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = v0 + threadIdx.x + 256 * j;
+      const float x = xs[j];
+      if (v >= v1) continue;
+      if (isnan(x)) {
+        flags |= 1;
+        continue;
+      }
+      if (x == INFINITY) flags |= 2;
+      if (x > m || (x == m && v < arg)) {
+        m = x;
+        arg = v;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m, o);
+      const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
+      if (om > m || (om == m && oa < arg)) {
+        m = om;
+        arg = oa;
+      }
+      flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+    }
+    if (lane == 0) {
+      sm_m[wid] = m;
+      sm_a[wid] = arg;
+      sm_f[wid] = flags;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float M = sm_m[0];
+      int A = sm_a[0], F = 0;
+      for (int w = 0; w < 8; ++w) {
+        if (sm_m[w] > M || (sm_m[w] == M && sm_a[w] < A)) {
+          M = sm_m[w];
+          A = sm_a[w];
+        }
+        F |= sm_f[w];
+      }
+      VerifyStat st;
+      st.m = M;
+      st.s = 0.f;
+      st.s_lo = 0.f;
+      st.arg = A;
+      st.flags = F;
+      a.stats[(static_cast<size_t>(r) * (a.budget + 1) + row) * a.n_chunks + chunk] = st;
+    }
+  }
+  // count this CTA; the one completing request r's rows x chunks walks its tree
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int prev = atomicAdd(a.counters + r, 1u);
+    last = prev == static_cast<unsigned int>((a.budget + 1) * a.n_chunks - 1);
+    if (last) a.counters[r] = 0u;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  tree_chain(a, r);
+}
+
 }  // namespace
+
+cudaError_t launch_tree_verify(const TreeVerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  if (a.budget < 1 || a.budget > kTreeMaxNodes || a.n_chunks < 1) return cudaErrorInvalidValue;
+  return launch_ex(tree_stats_kernel, dim3(n_req * (a.budget + 1), a.n_chunks), dim3(256), 0, st, pdl, a);
+}
 
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
   return launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), a.n_chunks * sizeof(double), st, pdl,

@@ -219,6 +219,47 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
                               int32_t* emitted, int32_t* n_emitted, float* probs_out, int32_t* status,
                               void* stream);
 
+/* ---- Draft tree (DDTree) ----
+ * "qwen35: DSpark speculative decoding (Qwen3.8-27B drafters) - #625", DDTree
+ * commit: a draft tree whose branches are chosen by the draft log-prob plus the
+ * selector compatibility with the branch's actual parent, log-softmax-normalised per
+ * position, grown best-first under a node budget.
+ * dflash2_tree_build: from one draft block's candidates (the outputs of
+ * dflash2_draft_block), for each request a tree rooted at the anchor.  A node at
+ * depth d (1..block-1) carries one of the top_k candidates of block position d; the
+ * children of a node are the candidates of the next position.  Child c of a parent
+ * whose own candidate is p scores log q(c | p) = s(p -> c) - logsumexp_c' s(p -> c'),
+ * s the selector score of dflash2_select; a node's score is the sum along its path.
+ * The tree grows by adding, one at a time, the highest-scoring child (over the root
+ * and every node already in) not yet in it, until `budget` nodes (1..
+ * DFLASH2_TREE_MAX_NODES; the root not counted) are in; equal scores go to the
+ * child of the earlier-added parent (the root first), then to the smaller candidate
+ * index.  FP32.
+ *   node_token, node_parent, node_depth [R][budget] int32, node_score [R][budget]
+ *   float32, in the order the nodes were added: node k's parent is -1 (the root) or
+ *   a node j < k; n_nodes [R]; scores_out: the selector lattice as in dflash2_select,
+ *   or NULL.  status [R] written as by dflash2_select (no temperature: the tree is
+ *   verified greedily).
+ * dflash2_tree_verify: greedy verification of the trees.  target_logits
+ *   [R][budget + 1][V] float32: row 0 is the target's distribution after the anchor,
+ *   row 1 + k after tree node k (rows past n_nodes are not read).  From the root,
+ *   move to the child whose token is the argmax of the current row (ties -> smaller
+ *   id) while one exists; emitted [R][block] holds the path's tokens, then the argmax
+ *   of the last row (-1 padded); n_accepted = the path's length, n_emitted =
+ *   n_accepted + 1.  status in/out as in dflash2_verify (nonzero on entry: skipped;
+ *   a NaN or +inf in a read row, or a row whose maximum is -inf: E_NONFINITE).
+ * Both return DFLASH2_E_INVAL for a NULL pointer, n_req outside 1..max_requests or a
+ * budget outside 1..DFLASH2_TREE_MAX_NODES (nothing is launched). */
+#define DFLASH2_TREE_MAX_NODES 32
+dflash2_status dflash2_tree_build(dflash2_handle* h, int32_t n_req, int32_t budget, const int32_t* anchor_ids,
+                                  const int32_t* cand_ids, const float* cand_logits, const float* gate,
+                                  int32_t* node_token, int32_t* node_parent, int32_t* node_depth, float* node_score,
+                                  int32_t* n_nodes, float* scores_out, int32_t* status, void* stream);
+dflash2_status dflash2_tree_verify(dflash2_handle* h, int32_t n_req, int32_t budget, const float* target_logits,
+                                   const int32_t* node_token, const int32_t* node_parent, const int32_t* n_nodes,
+                                   int32_t* n_accepted, int32_t* emitted, int32_t* n_emitted, int32_t* status,
+                                   void* stream);
+
 /* Serving-loop state update after dflash2_verify, on the device (so a multi-step
  * loop can be captured in one graph; "LSE docs/DFLASH2.md", block paragraph: each
  * draft is an anchor plus seven masks; vLLM PR #52816 description, candidate

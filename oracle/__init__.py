@@ -14,6 +14,7 @@ from . import philox  # noqa: F401
 from .dflash2 import (  # noqa: F401
     STATUS_OK, STATUS_INVAL, STATUS_NONFINITE, bf16_to_f64, round_to_bf16, matrix_f64,
     rmsnorm, rope_neox, rope_inv_freq, dyn_conv, block_attention, visible_context_range,
-    draft_block, topk, codebook_rows, selector_scores, walk, verify, step,
+    draft_block, topk, codebook_rows, selector_scores, selector_lattice, walk, verify, step,
+    ddtree_build, ddtree_verify,
     advance, viterbi_path,
 )

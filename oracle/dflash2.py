@@ -295,6 +295,22 @@ def selector_scores(A_pred: np.ndarray, gate: np.ndarray, B_cand: np.ndarray, un
     return s
 
 
+def selector_lattice(cb_a, cb_b, anchor: int, cand_ids: np.ndarray, cand_logits: np.ndarray,
+                     gate: np.ndarray) -> np.ndarray:
+    """Every edge score of the block ([VLLM] PR description, candidate selector):
+    position 1 from the anchor, positions 2..7 from every candidate of the previous
+    position.  Returns [P][K][K]: scores[i][p][c] = s_{i+1}(pred p -> cand c), where
+    the predecessor of position 1 is the anchor for every p (its row repeats)."""
+    P, K = cand_ids.shape
+    scores = np.zeros((P, K, K))
+    Bc = [codebook_rows(cb_b, cand_ids[i]) for i in range(P)]
+    a_anchor = codebook_rows(cb_a, [anchor])
+    scores[0] = np.repeat(selector_scores(a_anchor, gate[0], Bc[0], cand_logits[0]), K, axis=0)
+    for i in range(1, P):
+        scores[i] = selector_scores(codebook_rows(cb_a, cand_ids[i - 1]), gate[i], Bc[i], cand_logits[i])
+    return scores
+
+
 def walk(g, cb_a, cb_b, anchor: int, cand_ids: np.ndarray, cand_logits: np.ndarray, gate: np.ndarray,
          temperature: float, seed: int, offset: int, uniform_fn=None):
     """Selector path from the verified anchor over the top-16 candidates of block
@@ -314,13 +330,7 @@ def walk(g, cb_a, cb_b, anchor: int, cand_ids: np.ndarray, cand_logits: np.ndarr
     P, K = cand_ids.shape
     status = STATUS_OK
     uni = uniform_fn or (lambda slot, purpose: philox.uniform(seed, offset, slot, purpose))
-    # full lattice: position 1 from the anchor, positions 2..7 from every candidate of the previous one
-    scores = np.zeros((P, K, K))
-    Bc = [codebook_rows(cb_b, cand_ids[i]) for i in range(P)]
-    a_anchor = codebook_rows(cb_a, [anchor])
-    scores[0] = np.repeat(selector_scores(a_anchor, gate[0], Bc[0], cand_logits[0]), K, axis=0)
-    for i in range(1, P):
-        scores[i] = selector_scores(codebook_rows(cb_a, cand_ids[i - 1]), gate[i], Bc[i], cand_logits[i])
+    scores = selector_lattice(cb_a, cb_b, anchor, cand_ids, cand_logits, gate)
     if not np.all(np.isfinite(scores)) or not np.all(np.isfinite(cand_logits)):
         return {"path": np.full(P, -1, np.int32), "q_rows": np.zeros((P, K)), "scores": scores,
                 "status": STATUS_NONFINITE, "margins": np.zeros(P)}
@@ -389,6 +399,107 @@ def viterbi_path(scores: np.ndarray, cand_ids: np.ndarray) -> Dict:
     q_rows[np.arange(P), index] = 1.0
     return {"index": index, "path": cand_ids[np.arange(P), index].astype(np.int32), "q_rows": q_rows,
             "total": np.float32(top)}
+
+
+# ----------------------------------------------------------------------------- draft tree (DDTree)
+
+def ddtree_build(scores: np.ndarray, cand_ids: np.ndarray, budget: int) -> Dict:
+    """Draft tree with selector-scored branches ([LUCE] DDTree commit: each expansion
+    scores candidates as the draft log-prob plus the selector compatibility with the
+    branch's actual parent, log-softmax-normalised per position, so that cumulative
+    best-first comparisons across depths stay on a log-prob scale).
+
+    scores [P][K][K]: the selector lattice (selector_lattice: unary drafter logit +
+    compatibility), whose vocabulary log-normaliser is a per-position constant and
+    cancels in the per-parent normalisation.  Readings:
+      * the root is the verified anchor (depth 0, not counted in the budget); a node
+        at depth d < P has the K candidates of block position d + 1 as children;
+      * child c of a node whose own candidate index is p (p = 0 for the root, whose
+        row repeats) scores log q(c | p) = s[d][p][c] - logsumexp_c' s[d][p][c'];
+        a node's score is the sum of log q along its path from the root;
+      * best-first: repeatedly add the highest-scoring child, over every node already
+        in the tree, that is not in it yet, until `budget` nodes are in; equal scores
+        -> the child of the earlier-added parent (the root first), then the smaller
+        candidate index (top-k order).
+    Returns dict(token int32[n], parent int32[n] (-1 = the root, else the index of an
+    earlier node), depth int32[n] (1..P), cand int32[n] (candidate index), score
+    float64[n], margins float64[n]: each step's gap between the added node's score and
+    the best remaining one (inf when none remains)).  n = min(budget, the K + K^2 + ...
+    nodes that exist)."""
+    P, K = cand_ids.shape
+    logq = np.zeros((P, K, K))
+    for d in range(P):
+        for p in range(K):
+            row = np.asarray(scores[d][p], np.float64)
+            m = row.max()
+            logq[d][p] = row - (m + math.log(np.exp(row - m).sum()))
+    token, parent, depth, cand, score, margins = [], [], [], [], [], []
+    # a node is (depth, own candidate index, cumulative score); the root is index -1
+    node_depth = {-1: 0}
+    node_cand = {-1: 0}
+    node_score = {-1: 0.0}
+    taken = {-1: set()}
+    while len(token) < budget:
+        options = []
+        for q in [-1] + list(range(len(token))):
+            d = node_depth[q]
+            if d >= P:
+                continue
+            for c in range(K):
+                if c in taken[q]:
+                    continue
+                options.append((node_score[q] + logq[d][node_cand[q]][c], q, c))
+        if not options:
+            break
+        # highest score; equal -> earlier parent (root -1 first), then smaller candidate index
+        options.sort(key=lambda o: (-o[0], o[1], o[2]))
+        best = options[0]
+        margins.append(best[0] - options[1][0] if len(options) > 1 else math.inf)
+        sc, q, c = best
+        d = node_depth[q] + 1
+        idx = len(token)
+        token.append(int(cand_ids[d - 1][c]))
+        parent.append(q)
+        depth.append(d)
+        cand.append(c)
+        score.append(sc)
+        taken[q].add(c)
+        node_depth[idx], node_cand[idx], node_score[idx], taken[idx] = d, c, sc, set()
+    return {"token": np.array(token, np.int32), "parent": np.array(parent, np.int32),
+            "depth": np.array(depth, np.int32), "cand": np.array(cand, np.int32),
+            "score": np.array(score), "margins": np.array(margins)}
+
+
+def ddtree_verify(target_rows: np.ndarray, token: np.ndarray, parent: np.ndarray, status_in: int = STATUS_OK):
+    """Greedy verification of a draft tree ([LUCE] DDTree commits: tree verification
+    emits the same text as plain decoding; [LSE] first paragraph: greedy requests are
+    deterministic).  target_rows [n + 1][V]: row 0 is the target's distribution after
+    the anchor (the root), row 1 + k after tree node k.  From the root, move to the
+    child whose token is the argmax of the current node's row (ties -> smaller id)
+    while one exists; the accepted tokens are the path's, then the argmax of the last
+    node's row is emitted.  A used row with NaN or +inf, or a maximum of -inf, makes
+    the request nonfinite.  Returns dict(n_accepted, emitted int32[8] (-1 padded),
+    n_emitted, status, path (node indices))."""
+    emitted = np.full(8, -1, np.int32)
+    if status_in != STATUS_OK:
+        return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": status_in, "path": []}
+    z = np.asarray(target_rows, np.float64)
+    n = len(token)
+    used = z[: n + 1]
+    if np.any(np.isnan(used)) or np.any(np.isposinf(used)) or np.any(~np.isfinite(used.max(axis=1))):
+        return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": STATUS_NONFINITE, "path": []}
+    cur, path = -1, []
+    while True:
+        t = int(np.argmax(z[cur + 1]))
+        nxt = [k for k in range(n) if parent[k] == cur and int(token[k]) == t]
+        if not nxt:
+            break
+        cur = nxt[0]
+        emitted[len(path)] = t
+        path.append(cur)
+    emitted[len(path)] = int(np.argmax(z[cur + 1]))
+    return {"n_accepted": len(path), "emitted": emitted, "n_emitted": len(path) + 1, "status": STATUS_OK,
+            "path": path}
 
 
 # ----------------------------------------------------------------------------- verify

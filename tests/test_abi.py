@@ -93,6 +93,10 @@ def test_entry_points_reject_a_null_handle_or_bad_sizes():
     E = bd.binding.E_INVAL
     assert lib.dflash2_select(None, 1, *([None] * 12)) == E
     assert lib.dflash2_verify(None, 1, *([None] * 13)) == E
+    lib.dflash2_tree_build.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32] + [ctypes.c_void_p] * 12
+    lib.dflash2_tree_verify.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32] + [ctypes.c_void_p] * 9
+    assert lib.dflash2_tree_build(None, 1, 12, *([None] * 12)) == E
+    assert lib.dflash2_tree_verify(None, 1, 12, *([None] * 9)) == E
     assert lib.dflash2_advance(None, 1, *([None] * 7)) == E
     assert lib.dflash2_set_select_mode(None, 0) == E
     assert lib.dflash2_head_topk(None, 8, *([None] * 5)) == E

@@ -662,3 +662,125 @@ def test_viterbi_path_brute_force_and_examples():
     # all-equal scores: the smallest ids at every position
     ids = np.array([[7, 3, 9], [5, 2, 8], [6, 1, 4]], np.int32)
     assert list(oracle.viterbi_path(np.zeros((3, 3, 3)), ids)["path"]) == [3, 2, 1]
+
+
+# ----------------------------------------------------------------------------- draft tree (DDTree)
+
+def _all_paths(scores, K, P):
+    """Every root path of the tree (tuples of candidate indices) with its probability,
+    enumerated by brute force: the product of the per-parent softmax of the lattice
+    rows along the path (position 1 uses the anchor row 0)."""
+    out = {}
+    def rec(path, prob):
+        d = len(path)
+        if d == P:
+            return
+        prev = path[-1] if path else 0
+        row = np.asarray(scores[d][prev], np.float64)
+        pr = np.exp(row - row.max())
+        pr /= pr.sum()
+        for c in range(K):
+            np_ = path + (c,)
+            out[np_] = prob * pr[c]
+            rec(np_, prob * pr[c])
+    rec((), 1.0)
+    return out
+
+
+def test_ddtree_is_the_budget_most_probable_nodes():
+    """Best-first growth on log-softmax-normalised scores yields exactly the `budget`
+    most probable nodes of the whole tree (a child is never more probable than its
+    parent), each after its parent (LUCE DDTree commit: cumulative best-first
+    comparisons on a log-prob scale).  Brute force over every path, K = 3, depth 4."""
+    rng = np.random.default_rng(31)
+    K, P = 3, 4
+    cand = np.arange(100, 100 + P * K, dtype=np.int32).reshape(P, K)
+    for trial in range(20):
+        scores = rng.normal(0, 1.5, (P, K, K))
+        scores[0] = scores[0][0][None, :]               # position 1: the anchor row repeats
+        paths = _all_paths(scores, K, P)
+        ranked = sorted(paths.items(), key=lambda kv: -kv[1])
+        for budget in (1, 4, 12, len(paths)):
+            tr = oracle.ddtree_build(scores, cand, budget)
+            assert len(tr["token"]) == min(budget, len(paths))
+            got = {}
+            for k in range(len(tr["token"])):
+                pre = () if tr["parent"][k] < 0 else got[int(tr["parent"][k])]
+                assert tr["parent"][k] < k                  # parents come first
+                got[k] = pre + (int(tr["cand"][k]),)
+                assert tr["depth"][k] == len(got[k])
+                assert tr["token"][k] == cand[tr["depth"][k] - 1][tr["cand"][k]]
+                assert abs(tr["score"][k] - math.log(paths[got[k]])) < 1e-12
+            want = {p for p, _ in ranked[:len(tr["token"])]}
+            assert set(got.values()) == want, (trial, budget)
+
+
+def test_ddtree_children_of_a_node_normalise():
+    """The normalised scores of a node's K children are log-probabilities: their
+    exponentials, relative to the parent, sum to one."""
+    rng = np.random.default_rng(32)
+    K, P = 4, 3
+    cand = np.arange(K * P, dtype=np.int32).reshape(P, K)
+    scores = rng.normal(0, 2.0, (P, K, K))
+    scores[0] = scores[0][0][None, :]
+    full = K + K * K + K ** 3
+    tr = oracle.ddtree_build(scores, cand, full)
+    assert len(tr["token"]) == full
+    for q in [-1] + list(range(full)):
+        kids = [k for k in range(full) if tr["parent"][k] == q]
+        if not kids:
+            continue
+        base = 0.0 if q < 0 else tr["score"][q]
+        assert len(kids) == K
+        assert abs(sum(math.exp(tr["score"][k] - base) for k in kids) - 1.0) < 1e-12
+
+
+def test_ddtree_verify_on_a_chain_is_the_greedy_verify():
+    """A tree that is a single chain verifies exactly as the chain (the greedy verify,
+    pinned above as the argmax chain)."""
+    rng = np.random.default_rng(33)
+    V = 40
+    for trial in range(20):
+        z = rng.normal(0, 1, (8, V))
+        t = np.argmax(z, axis=1)
+        n_match = trial % 8
+        path = np.array([t[j] if j < n_match else (t[j] + 1) % V for j in range(7)], np.int32)
+        res = oracle.ddtree_verify(z, path, np.arange(-1, 6, dtype=np.int32))
+        ref = oracle.verify(z, path, np.zeros((7, 16), np.int32), np.zeros((7, 16)), 0.0, 0, 0)
+        assert res["n_accepted"] == ref["n_accepted"] and res["n_emitted"] == ref["n_emitted"]
+        assert np.array_equal(res["emitted"], ref["emitted"])
+
+
+def test_ddtree_verify_accepts_the_deepest_fully_matching_node():
+    """Brute force on random trees: a node is accepted iff every node on its root path
+    carries the argmax token of its parent's row; the verify ends at the deepest such
+    node (unique: siblings carry distinct tokens) and emits that node's row argmax."""
+    rng = np.random.default_rng(34)
+    V = 6
+    for trial in range(200):
+        n = int(rng.integers(1, 14))
+        parent = np.array([int(rng.integers(-1, k)) for k in range(n)], np.int32)
+        token = np.zeros(n, np.int32)
+        for k in range(n):  # siblings distinct
+            used = {int(token[j]) for j in range(k) if parent[j] == parent[k]}
+            token[k] = int(rng.choice([x for x in range(V) if x not in used])) if len(used) < V else 0
+        depth = np.zeros(n, int)
+        for k in range(n):
+            depth[k] = 1 if parent[k] < 0 else depth[parent[k]] + 1
+        if depth.max() > 7 or any(len({int(token[j]) for j in range(n) if parent[j] == q}) !=
+                                  sum(1 for j in range(n) if parent[j] == q) for q in range(-1, n)):
+            continue
+        z = rng.integers(0, 3, (n + 1, V)).astype(np.float64)   # integer rows: ties to the smaller id
+        am = [int(np.argmax(z[k])) for k in range(n + 1)]
+        def matched(k):
+            while k >= 0:
+                if int(token[k]) != am[parent[k] + 1]:
+                    return False
+                k = parent[k]
+            return True
+        ok = [k for k in range(n) if matched(k)]
+        deepest = max(ok, key=lambda k: depth[k]) if ok else -1
+        res = oracle.ddtree_verify(z, token, parent)
+        assert res["n_accepted"] == (depth[deepest] if deepest >= 0 else 0)
+        assert res["emitted"][res["n_accepted"]] == am[deepest + 1]
+        assert res["n_emitted"] == res["n_accepted"] + 1
