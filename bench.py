@@ -571,7 +571,7 @@ def main_ours(args, rank, world, local_rank):
                                bd.dflash2_projection_bytes(h))
     restore()
     tree = None
-    if not loop:
+    if args.config == 2 and not args.no_r16:
         tree = measure_tree(bd, h, R, S, wl)
         restore()
     pk = peaks()
@@ -603,7 +603,7 @@ def main_ours(args, rank, world, local_rank):
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
                      "projections": proj},
         "e2e": {"value": e2e_val, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "tree": tree,
+        **({"tree": tree} if tree is not None else {}),
         "gpu_launches": int(launches_per_step * K),
         "clocks": clk,
         "setup_s": setup_s,

@@ -9,10 +9,13 @@
 // 64 context keys), plus one CTA for the 8 block keys; all 32 queries of a KV
 // head group (4 heads x 8 positions) are handled together so every key is read
 // once.  Keys outside the window are never read.  Context chunks run on the
-// tensor cores (mma.sync m16n8k16, bf16 K/V as stored, queries and probabilities
-// split into bf16 hi + lo for fp32-level accuracy); the block chunk uses FFMA on
-// the fp32 block keys.  A combine kernel merges the chunk partials (max, sum,
-// unnormalised output) in a fixed order.
+// tensor cores (mma.sync m16n8k16 in fp16, fp32 accumulators): the bf16 K/V rows
+// convert to fp16 exactly inside fp16's normal range (saturated at +-65504 beyond
+// it), queries and probabilities round to fp16 (2^-11 relative).  One product per
+// MMA: a bf16 hi + lo split of queries and probabilities doubled the shared-memory
+// fragment loads, which bound the kernel, and bf16 alone (2^-8) is too coarse.
+// The block chunk uses FFMA on the fp32 block keys.  A combine kernel merges the
+// chunk partials (max, sum, unnormalised output) in a fixed order.
 #include <math.h>
 
 #include "common.cuh"
@@ -31,12 +34,12 @@ constexpr int kLd = kHd + 8;    // bf16 row pitch (272 B): conflict-free fragmen
 constexpr int kPLd = kKeys + 8;
 
 struct CtxSmem {
-  __nv_bfloat16 qh[kQ][kLd], ql[kQ][kLd];  // scaled queries, hi and lo parts
-  __nv_bfloat16 k[kKeys][kLd];
-  __nv_bfloat16 v[kKeys][kLd];
-  float s[kQ][kKeys + 4];                  // scores (log2 units), then probabilities
-  __nv_bfloat16 ph[kQ][kPLd], pl[kQ][kPLd];
-  float alpha[kQ];                         // rescale of the running output, per query
+  __half q[kQ][kLd];              // scaled queries
+  __half k[kKeys][kLd];
+  __half v[kKeys][kLd];
+  float s[kQ][kKeys + 4];         // scores (log2 units), then probabilities
+  __half p[kQ][kPLd];
+  float alpha[kQ];                // rescale of the running output, per query
 };
 
 struct BlkSmem {
@@ -45,7 +48,19 @@ struct BlkSmem {
   float p[kQ][8];
 };
 
-DF2_DEV uint32_t ld32(const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); }
+DF2_DEV uint32_t ld32(const __half* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// Eight bf16 values -> eight fp16 values (exact inside fp16's normal range; saturated
+// at +-65504 beyond it, so no infinity enters the softmax).
+DF2_DEV uint4 bf16x8_to_f16x8(uint4 v) {
+  auto cv = [](uint32_t w) {
+    const float a = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
+    const float b = fminf(fmaxf(__uint_as_float(w & 0xFFFF0000u), -65504.f), 65504.f);
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  };
+  return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
+}
 
 DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* smem_row) {
   const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(smem_row));
@@ -97,7 +112,7 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   pdl_wait();
   pdl_trigger();
   if (!early) kv = load_kv(a, r, kvh, kbeg(c0), nkeys(c0));
-  // queries -> bf16 hi/lo (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i); loads first
+  // queries -> fp16 (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i); loads first
   float qv[kQ * kHd / 256];
 #pragma unroll
   for (int j = 0; j < kQ * kHd / 256; ++j) {
@@ -110,10 +125,7 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   for (int j = 0; j < kQ * kHd / 256; ++j) {
     const int e = tid + 256 * j;
     const int qi = e / kHd, d = e % kHd;
-    const float v = qv[j] * qscale;
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    sm.qh[qi][d] = h;
-    sm.ql[qi][d] = __float2bfloat16_rn(v - __bfloat162float(h));
+    sm.q[qi][d] = __float2half_rn(qv[j] * qscale);
   }
   float m_run[4], l_run[4];  // queries 4 wid .. 4 wid + 3 (the same in every lane of the warp)
 #pragma unroll
@@ -128,8 +140,8 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
     for (int j = 0; j < 4; ++j) {
       const int e = tid + 256 * j;
       const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-      *reinterpret_cast<uint4*>(&sm.k[k][d8]) = kv.k[j];
-      *reinterpret_cast<uint4*>(&sm.v[k][d8]) = kv.v[j];
+      *reinterpret_cast<uint4*>(&sm.k[k][d8]) = bf16x8_to_f16x8(kv.k[j]);
+      *reinterpret_cast<uint4*>(&sm.v[k][d8]) = bf16x8_to_f16x8(kv.v[j]);
     }
     if (c + 1 < c1) kv = load_kv(a, r, kvh, kbeg(c + 1), nkeys(c + 1));  // in flight during this chunk
     __syncthreads();
@@ -144,10 +156,8 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const int r0 = mt * 16 + g;
-          mma_bf16(cs[mt], ld32(&sm.qh[r0][ks * 16 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 2 * q]),
-                   ld32(&sm.qh[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.qh[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
-          mma_bf16(cs[mt], ld32(&sm.ql[r0][ks * 16 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 2 * q]),
-                   ld32(&sm.ql[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ql[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+          mma_f16(cs[mt], ld32(&sm.q[r0][ks * 16 + 2 * q]), ld32(&sm.q[r0 + 8][ks * 16 + 2 * q]),
+                  ld32(&sm.q[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.q[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
         }
       }
       const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
@@ -179,11 +189,8 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
       const float p1 = none ? 0.f : exp2f(v1 - m_new);
       l_run[i] = l_run[i] * alpha + warp_sum(p0 + p1);
       m_run[i] = m_new;
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-      sm.ph[qi][lane] = h0;
-      sm.ph[qi][lane + 32] = h1;
-      sm.pl[qi][lane] = __float2bfloat16_rn(p0 - __bfloat162float(h0));
-      sm.pl[qi][lane + 32] = __float2bfloat16_rn(p1 - __bfloat162float(h1));
+      sm.p[qi][lane] = __float2half_rn(p0);
+      sm.p[qi][lane + 32] = __float2half_rn(p1);
       if (lane == 0) sm.alpha[qi] = alpha;
     }
     __syncthreads();
@@ -209,10 +216,8 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const int r0 = mt * 16 + g;
-          mma_bf16(o[dn][mt], ld32(&sm.ph[r0][ks * 16 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 2 * q]),
-                   ld32(&sm.ph[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.ph[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
-          mma_bf16(o[dn][mt], ld32(&sm.pl[r0][ks * 16 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 2 * q]),
-                   ld32(&sm.pl[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.pl[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+          mma_f16(o[dn][mt], ld32(&sm.p[r0][ks * 16 + 2 * q]), ld32(&sm.p[r0 + 8][ks * 16 + 2 * q]),
+                  ld32(&sm.p[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.p[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
         }
       }
     }

@@ -115,11 +115,15 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
   const int row = blockIdx.x * kB + i;
   const int c = blockIdx.y * kCw + lane;
   const int G = a.H / 16;
-  const float rr = warp_inv_rms(a.ss, row, a.nch, a.H, a.eps);
+  // loads independent of the planes and of 1/rms first: one round of latency
+  const size_t idx = static_cast<size_t>(row) * a.H + c;
+  const float x0 = a.x[idx], w = bf16_to_f32(a.norm_w[c]);
+  const float b0 = bf16_to_f32(a.base[c]), b1 = bf16_to_f32(a.base[a.H + c]);
   // the (io, tap, local group) delta values of this row and the CTA's 2 groups: value
   // e = lane & 7, its split planes pg, pg + 4, ... summed by lane e + 8 pg, then the
   // four partial sums combined in a fixed tree (lanes 0..7 end with the total)
   float dv;
+  float rr;
   {
     const int e = lane & 7, pg = lane >> 3;
     const int io = e >> 2, t = (e >> 1) & 1, gl = e & 1;
@@ -137,17 +141,16 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
     }
     part += __shfl_xor_sync(0xffffffffu, part, 8);
     part += __shfl_xor_sync(0xffffffffu, part, 16);
+    rr = warp_inv_rms(a.ss, row, a.nch, a.H, a.eps);
     dv = part * rr;
     if (lane < 8) a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
   }
   const int gl = lane >> 4;
   const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 2 + gl);
-  const size_t idx = static_cast<size_t>(row) * a.H + c;
-  const float ai = a.x[idx] * rr * bf16_to_f32(a.norm_w[c]);
+  const float ai = x0 * rr * w;
   ash[i][lane] = ai;
   __syncthreads();
   const float prev = i > 0 ? ash[i - 1][lane] : 0.f;
-  const float b0 = bf16_to_f32(a.base[c]), b1 = bf16_to_f32(a.base[a.H + c]);
   put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), (b0 + d0) * ai + (b1 + d1) * prev);
 }
 
@@ -179,15 +182,18 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
   const int G = a.H / 16;
   const int g = c >> 4;
   const size_t idx = static_cast<size_t>(row) * a.H + c;
+  // every load independent of the planes is issued first: one round of latency
+  const float* d = a.delta + static_cast<size_t>(row) * (4 * G);
+  const float d2 = d[2 * G + g], d3 = d[3 * G + g];
+  const float b2 = bf16_to_f32(a.base[2 * a.H + c]), b3 = bf16_to_f32(a.base[3 * a.H + c]);
+  const float x0 = a.x[idx];
+  const float w = bf16_to_f32(a.norm_w[c]);
   const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, gemv_plane_count(a.pl, c));
   ysh[i][lane] = y;
   __syncthreads();
   const float yprev = i > 0 ? ysh[i - 1][lane] : 0.f;
-  const float* d = a.delta + static_cast<size_t>(row) * (4 * G);
-  const float b2 = bf16_to_f32(a.base[2 * a.H + c]), b3 = bf16_to_f32(a.base[3 * a.H + c]);
-  const float xv = a.x[idx] + (b2 + d[2 * G + g]) * y + (b3 + d[3 * G + g]) * yprev;
+  const float xv = x0 + (b2 + d2) * y + (b3 + d3) * yprev;
   a.x[idx] = xv;
-  const float w = bf16_to_f32(a.norm_w[c]);
   put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), xv * w);
   if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, act_offset(row, c, a.H, a.tiled2), xv * w);
   emit_ss(xv, row, a.ss, a.nch);
@@ -201,8 +207,22 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
   const size_t idx = static_cast<size_t>(row) * a.F + c;
   const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
-  const float gs = plane_sum(a.part_g + idx, plane, gemv_plane_count(a.pg, c));
-  const float us = plane_sum(a.part_u + idx, plane, gemv_plane_count(a.pu, c));
+  // the gate and up planes' loads all in flight together, each added in split order
+  const int ng = gemv_plane_count(a.pg, c), nu = gemv_plane_count(a.pu, c);
+  float gs = 0.f, us = 0.f;
+  for (int s0 = 0; s0 < (ng > nu ? ng : nu); s0 += 8) {
+    float tg[8], tu[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      tg[j] = (s0 + j < ng) ? a.part_g[idx + static_cast<size_t>(s0 + j) * plane] : 0.f;
+      tu[j] = (s0 + j < nu) ? a.part_u[idx + static_cast<size_t>(s0 + j) * plane] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      gs += tg[j];
+      us += tu[j];
+    }
+  }
   put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.F, a.tiled), gs / (1.f + __expf(-gs)) * us);
 }
 

@@ -175,7 +175,6 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
   __shared__ int rowA[kB], rowF[kB], rowBad;
   __shared__ int cid[kK];
   __shared__ float qv[kK];
-  __shared__ int sh_decision;
   int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
   // debug output: NaN wherever this request gets no probability
   float* probs = a.probs != nullptr ? a.probs + static_cast<size_t>(r) * kB * 2 : nullptr;
@@ -260,39 +259,46 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
   }
   const uint64_t seed = a.seed[r], off = a.offset[r];
   const float* zr = a.logits + static_cast<size_t>(r) * kB * a.V;
+  // The accept tests of the seven rows depend only on the path, q and the target
+  // row, not on each other: thread j < 7 takes row j (all loads of the rows in
+  // flight together), then the chain stops at the first rejection.
+  __shared__ int acc_row[kP];
   __syncthreads();  // the NaN fill above is done before these entries are written
-  if (probs != nullptr && threadIdx.x < kP) {  // p_j at every row's proposal (same arithmetic as the accept test)
+  if (threadIdx.x < kP) {
     const int j = threadIdx.x;
     const int d = min(max(path[j], 0), a.V - 1);
-    probs[2 * j] = expf((zr[static_cast<size_t>(j) * a.V + d] - rowM[j]) / T) / rowS[j];
+    const int32_t* ci = a.cand_ids + (static_cast<size_t>(r) * kP + j) * kK;
+    const float* qj = a.q_rows + (static_cast<size_t>(r) * kP + j) * kK;
+    const float zd = zr[static_cast<size_t>(j) * a.V + d];
+    float qd = 0.f;
+    for (int k = 0; k < kK; ++k)
+      if (min(max(ci[k], 0), a.V - 1) == d) qd = qj[k];
+    const float pd = expf((zd - rowM[j]) / T) / rowS[j];
+    const float u = philox_uniform(seed, off, static_cast<uint32_t>(j), kPurposeAccept);
+    acc_row[j] = (qd > 0.f) ? (u * qd < pd) : 1;
+    if (probs != nullptr) probs[2 * j] = pd;  // p_j at every row's proposal (the accept test's value)
   }
-  for (int j = 0; j < kP; ++j) {
-    const float* z = zr + static_cast<size_t>(j) * a.V;
+  __syncthreads();
+  int n_acc = kP;
+  for (int j = 0; j < kP; ++j)
+    if (!acc_row[j]) {
+      n_acc = j;
+      break;
+    }
+  if (n_acc < kP) {
+    const int j = n_acc;
     if (threadIdx.x < kK) {
       cid[threadIdx.x] = min(max(a.cand_ids[(static_cast<size_t>(r) * kP + j) * kK + threadIdx.x], 0), a.V - 1);
       qv[threadIdx.x] = a.q_rows[(static_cast<size_t>(r) * kP + j) * kK + threadIdx.x];
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      const int d = min(max(path[j], 0), a.V - 1);
-      float qd = 0.f;
-      for (int k = 0; k < kK; ++k)
-        if (cid[k] == d) qd = qv[k];
-      const float pd = expf((z[d] - rowM[j]) / T) / rowS[j];
-      const float u = philox_uniform(seed, off, static_cast<uint32_t>(j), kPurposeAccept);
-      sh_decision = (qd > 0.f) ? (u * qd < pd) : 1;
-    }
-    __syncthreads();
-    if (sh_decision) {
-      if (threadIdx.x == 0) emitted[j] = path[j];
-      __syncthreads();
-      continue;
-    }
+    const float* z = zr + static_cast<size_t>(j) * a.V;
     const float u = philox_uniform(seed, off, static_cast<uint32_t>(j), kPurposeResample);
     const int x = draw_row(a, z, st + static_cast<size_t>(j) * a.n_chunks, rowM[j], rowS[j], T, cid, qv, true, u,
                            csum, red, &sh_mass);
     if (threadIdx.x == 0) {
       if (probs != nullptr) probs[2 * j + 1] = sh_mass;
+      for (int t = 0; t < j; ++t) emitted[t] = path[t];
       emitted[j] = x;
       for (int t = j + 1; t < kB; ++t) emitted[t] = -1;
       a.n_accepted[r] = j;
@@ -306,6 +312,7 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
                          csum, red, &sh_mass);
   if (threadIdx.x == 0) {
     if (probs != nullptr) probs[2 * kP] = expf((z[x] - rowM[kP]) / T) / rowS[kP];
+    for (int t = 0; t < kP; ++t) emitted[t] = path[t];
     emitted[kP] = x;
     a.n_accepted[r] = kP;
     a.n_emitted[r] = kP + 1;

@@ -138,13 +138,22 @@ WORKLOADS[6] = Workload("profile_one_full_layer", Geometry("full_width_1layer", 
 
 
 # Profiling-only workload for the tensor-core path: the same layer with 16 Q8 requests
-# (about 1 GB on the device).
+# whose 2048-key windows are full, as in configuration 5 (about 1 GB on the device).
 WORKLOADS[7] = Workload("profile_q8_r16_one_full_layer",
                         Geometry("full_width_1layer", hidden=5120, n_layers=1, n_q_heads=32, n_kv_heads=8,
                                  head_dim=128, ffn=17408, vocab=16384),
-                        "q8", 16, [512] * 16, [0.0, 0.7, 1.0, 0.0] * 4, [1.0] * 16, seed=7, philox_seed=42,
+                        "q8", 16, [2048] * 16, [0.0, 0.7, 1.0, 0.0] * 4, [1.0] * 16, seed=7, philox_seed=42,
                         philox_offsets=[r << 32 for r in range(16)],
-                        description="profiling: one full-width layer, vocab 16384, Q8, 16 requests, ctx 512")
+                        description="profiling: one full-width layer, vocab 16384, Q8, 16 requests, ctx 2048")
+
+
+# Profiling-only workload for the one-request int8 GEMV: the same layer with one Q8
+# request (about 0.6 GB on the device).
+WORKLOADS[8] = Workload("profile_q8_r1_one_full_layer",
+                        Geometry("full_width_1layer", hidden=5120, n_layers=1, n_q_heads=32, n_kv_heads=8,
+                                 head_dim=128, ffn=17408, vocab=16384),
+                        "q8", 1, [2048], [1.0], [1.5], seed=8, philox_seed=42, philox_offsets=[0],
+                        description="profiling: one full-width layer, vocab 16384, Q8, 1 request, ctx 2048, T=1.0")
 
 
 def workload(i: int) -> Workload:
