@@ -54,6 +54,16 @@ DF2_DEV float plane_sum(const float* p, size_t plane, int S) {
   return S <= 8 ? plane_sum_b<8>(p, plane, S) : plane_sum_b<32>(p, plane, S);
 }
 
+// The plane count of the weight block holding this CTA's 32 channels (c0 = the
+// first): every channel of a 32-channel chunk lies in one block (64 or 128 rows),
+// so it is evaluated once per CTA, by thread 0, not per thread (its divisions
+// dominated the element-wise kernels at many requests).  Ends with a barrier.
+DF2_DEV int cta_plane_count(const GemvPlanes& pl, int c0, int* sh) {
+  if (threadIdx.x == 0) *sh = gemv_plane_count(pl, c0);
+  __syncthreads();
+  return *sh;
+}
+
 // Per-row sum of squares of this CTA's 32 channels -> ss[row][blockIdx.y] (one warp = one row).
 DF2_DEV void emit_ss(float v, int row, float* ss, int nch) {
   const float s = warp_sum(v * v);
@@ -98,10 +108,11 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
 // c = y * w_hidden_norm into the context rows of the QKV input (1/rms of y is
 // applied after the K/V projection); ss of y.
 DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
+  __shared__ int np_sh;
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
-  const float y =
-      plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, gemv_plane_count(a.pl, c));
+  const int np = cta_plane_count(a.pl, blockIdx.y * kCw, &np_sh);
+  const float y = plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, np);
   put_act(a.act, a.act_lo, a.fmt, act_offset(a.act_row0 + row, c, a.H, a.tiled), y * bf16_to_f32(a.norm_w[c]));
   emit_ss(y, row, a.ss, a.nch);
 }
@@ -111,10 +122,17 @@ DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
 // a_i = r_i x_i w;  a'_i = (b0 + d0_i) a_i + (b1 + d1_i) a_{i-1}.
 DF2_DEV void conv_in_body(const ConvInArgs& a) {
   __shared__ float ash[kB][kCw];
+  __shared__ int np_sh[8];
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
   const int c = blockIdx.y * kCw + lane;
   const int G = a.H / 16;
+  // plane counts of the CTA's 8 delta values (io, tap, local group), once per CTA
+  if (threadIdx.x < 8) {
+    const int e = threadIdx.x;
+    np_sh[e] = gemv_plane_count(a.pl, ((e >> 2) * 2 + ((e >> 1) & 1)) * G + blockIdx.y * 2 + (e & 1));
+  }
+  __syncthreads();
   // loads independent of the planes and of 1/rms first: one round of latency
   const size_t idx = static_cast<size_t>(row) * a.H + c;
   const float x0 = a.x[idx], w = bf16_to_f32(a.norm_w[c]);
@@ -130,7 +148,7 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
     const int gidx = (io * 2 + t) * G + blockIdx.y * 2 + gl;
     const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
     const float* p = a.dproj + static_cast<size_t>(row) * (4 * G) + gidx;
-    const int np = gemv_plane_count(a.pl, gidx);
+    const int np = np_sh[e];
     float part = 0.f;
     for (int s0 = pg; s0 < np; s0 += 32) {
       float tt[8];
@@ -175,6 +193,8 @@ __global__ void __launch_bounds__(kThreads) fc_finish_conv_in_kernel(const FcFin
 // convolution wrapping the sublayer's output); act = x * w_next; ss of x.
 __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a) {
   __shared__ float ysh[kB][kCw];
+  __shared__ int np_sh;
+  const int np = cta_plane_count(a.pl, blockIdx.y * kCw, &np_sh);  // before the wait: shapes only
   pdl_begin_early();  // followed by a weight launch
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
@@ -188,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
   const float b2 = bf16_to_f32(a.base[2 * a.H + c]), b3 = bf16_to_f32(a.base[3 * a.H + c]);
   const float x0 = a.x[idx];
   const float w = bf16_to_f32(a.norm_w[c]);
-  const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, gemv_plane_count(a.pl, c));
+  const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, np);
   ysh[i][lane] = y;
   __syncthreads();
   const float yprev = i > 0 ? ysh[i - 1][lane] : 0.f;
@@ -202,13 +222,19 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
 // ------------------------------------------------------------------ SwiGLU
 // h = silu(gate) * up from the split planes of the two projections.
 __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
+  __shared__ int np_sh[2];
+  if (threadIdx.x == 0) {  // before the wait: shapes only
+    np_sh[0] = gemv_plane_count(a.pg, blockIdx.y * kCw);
+    np_sh[1] = gemv_plane_count(a.pu, blockIdx.y * kCw);
+  }
+  __syncthreads();
   pdl_begin_early();  // followed by a weight launch
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
   const int c = blockIdx.y * kCw + (threadIdx.x & 31);
   const size_t idx = static_cast<size_t>(row) * a.F + c;
   const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
   // the gate and up planes' loads all in flight together, each added in split order
-  const int ng = gemv_plane_count(a.pg, c), nu = gemv_plane_count(a.pu, c);
+  const int ng = np_sh[0], nu = np_sh[1];
   float gs = 0.f, us = 0.f;
   for (int s0 = 0; s0 < (ng > nu ? ng : nu); s0 += 8) {
     float tg[8], tu[8];

@@ -309,6 +309,10 @@ __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArg
   __shared__ unsigned long long wtop[8][kTopK];
   __shared__ int n_cand;
   __shared__ float rs_sh;
+  __shared__ int np_sh[kLogitChunk / 16 / 8];  // plane counts of the chunk's 128-id blocks (at least 64 ids)
+  // before the wait: shapes only (once per CTA, not per thread)
+  if (threadIdx.x < kLogitChunk / 128)
+    np_sh[threadIdx.x] = gemv_plane_count(a.pl, blockIdx.x * kLogitChunk + threadIdx.x * 128);
   pdl_begin();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int rq = blockIdx.y / 7, pos = blockIdx.y % 7 + 1, n = rq * 8 + pos;
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArg
   if (v0 < a.V) {  // V is a multiple of 16: the thread's 16 entries are all in range, in one weight block
     const size_t plane = static_cast<size_t>(a.n_rows) * a.V;
     const float* src = a.part + static_cast<size_t>(n) * a.V + v0;
-    const int np = gemv_plane_count(a.pl, v0);
+    const int np = np_sh[(threadIdx.x * 16) >> 7];  // v0's block within the chunk (blocks of 128 ids)
     float acc[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;

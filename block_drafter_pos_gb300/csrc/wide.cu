@@ -89,8 +89,11 @@ struct WideGeo {
   static constexpr int kDCol0 = kDA * kACols;             // first accumulator column
   static constexpr int kBufs = (kTmemCols - kDCol0) / NMAX >= 2 ? 2 : 1;
   static constexpr int kDB = FMT == 1 ? 2 : (NMAX == 128 ? 2 : 1);
-  static constexpr int kRing = (FMT == 0 ? 100 : 224) * 1024;
-  static constexpr int kDW = (kRing - kDB * kB) / kW;
+  static constexpr int kRing = (FMT == 0 ? 100 : 224) * 1024;  // bf16: two CTAs per SM
+  // int8: a 4-stage code ring (64 KB of codes in flight).  Measured at 16 requests:
+  // gate/up 78 us at 2 or 4 stages, 80 at 6, 82 at 10 (the codes queued ahead delay
+  // the activation copies behind them).
+  static constexpr int kDW = FMT == 1 ? 4 : (kRing - kDB * kB) / kW;
   static constexpr int kOffB = kDW * kW;
   static constexpr int kSmem = kOffB + kDB * kB + 1024;
   static constexpr int kConvGroups = FMT == 1 ? 2 : 0;  // int8: converter warp groups, taking alternate stages
