@@ -16,5 +16,5 @@ from .dflash2 import (  # noqa: F401
     rmsnorm, rope_neox, rope_inv_freq, dyn_conv, block_attention, visible_context_range,
     draft_block, topk, codebook_rows, selector_scores, selector_lattice, walk, verify, step,
     ddtree_build, ddtree_verify,
-    advance, viterbi_path,
+    advance, block_width, viterbi_path,
 )

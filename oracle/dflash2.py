@@ -470,7 +470,8 @@ def ddtree_build(scores: np.ndarray, cand_ids: np.ndarray, budget: int) -> Dict:
             "score": np.array(score), "margins": np.array(margins)}
 
 
-def ddtree_verify(target_rows: np.ndarray, token: np.ndarray, parent: np.ndarray, status_in: int = STATUS_OK):
+def ddtree_verify(target_rows: np.ndarray, token: np.ndarray, parent: np.ndarray, status_in: int = STATUS_OK,
+                  block: int = 8):
     """Greedy verification of a draft tree ([LUCE] DDTree commits: tree verification
     emits the same text as plain decoding; [LSE] first paragraph: greedy requests are
     deterministic).  target_rows [n + 1][V]: row 0 is the target's distribution after
@@ -478,9 +479,9 @@ def ddtree_verify(target_rows: np.ndarray, token: np.ndarray, parent: np.ndarray
     child whose token is the argmax of the current node's row (ties -> smaller id)
     while one exists; the accepted tokens are the path's, then the argmax of the last
     node's row is emitted.  A used row with NaN or +inf, or a maximum of -inf, makes
-    the request nonfinite.  Returns dict(n_accepted, emitted int32[8] (-1 padded),
-    n_emitted, status, path (node indices))."""
-    emitted = np.full(8, -1, np.int32)
+    the request nonfinite.  Returns dict(n_accepted, emitted int32[block] (-1 padded),
+    n_emitted, status, path (node indices)); a tree is at most block - 1 deep."""
+    emitted = np.full(block, -1, np.int32)
     if status_in != STATUS_OK:
         return {"n_accepted": 0, "emitted": emitted, "n_emitted": 0, "status": status_in, "path": []}
     z = np.asarray(target_rows, np.float64)
@@ -606,7 +607,8 @@ def _inverse_cdf(w: np.ndarray, u: float):
 
 # ----------------------------------------------------------------------------- one step
 
-def advance(ctx_len: int, n_new: int, anchor: int, emitted: Sequence[int], n_emitted: int, offset: int):
+def advance(ctx_len: int, n_new: int, anchor: int, emitted: Sequence[int], n_emitted: int, offset: int,
+            block: int = 8):
     """Request state for the next draft + verify step ([LSE] block paragraph: every
     draft is an anchor plus seven masks; [VLLM] PR description, candidate selector:
     the walk starts at the verified anchor).  Reading: the rows appended this step
@@ -614,9 +616,21 @@ def advance(ctx_len: int, n_new: int, anchor: int, emitted: Sequence[int], n_emi
     the last of them the next anchor; each step draws from its own Philox counter
     range, the offset advanced by one.  A request with nothing emitted keeps its
     anchor and appends nothing.  Returns (ctx_len, n_new, anchor, offset)."""
-    ne = max(0, min(int(n_emitted), 8))
+    ne = max(0, min(int(n_emitted), block))
     nxt_anchor = int(emitted[ne - 1]) if ne > 0 else int(anchor)
-    return int(ctx_len) + max(0, min(int(n_new), 8)), ne, nxt_anchor, int(offset) + 1
+    return int(ctx_len) + max(0, min(int(n_new), block)), ne, nxt_anchor, int(offset) + 1
+
+
+def block_width(ctx_len: int, n_new: int, block: int, ctx_threshold: int = 8192, narrow_width: int = 8) -> int:
+    """Draft-block width of one request for a step ([LUCE] long-context commits: the
+    verify's cost scales with the block's rows and the KV length, so past a context
+    threshold the block narrows; the rule reads the context length only, never the
+    acceptance rate; threshold 0 disables it; the first cut's 32768 default moved to
+    8192, with narrowing to 8 inside a block-16 drafter).  Reading: the context is
+    the keys the step's block attends to, ctx_len + n_new, and "past" is strictly
+    greater.  A narrowed request's step is the step of a block of that width."""
+    L = max(0, int(ctx_len)) + max(0, int(n_new))
+    return narrow_width if (ctx_threshold > 0 and L > ctx_threshold) else block
 
 
 def step(g, W: Dict, anchor: int, ctx_len: int, n_new: int, taps, k_cache, v_cache,

@@ -158,10 +158,11 @@ def test_conv_identity_init():
     assert np.array_equal(oracle.dyn_conv(x, base, np.zeros((8, 2, 4)), 16), x)
 
 
-def test_conv_pure_shift_and_block_boundary():
-    x, _, _ = _conv_inputs()
+@pytest.mark.parametrize("B", [8, 16])
+def test_conv_pure_shift_and_block_boundary(B):
+    x, _, _ = _conv_inputs(B=B)
     base = np.stack([np.zeros(64), np.ones(64)])
-    y = oracle.dyn_conv(x, base, np.zeros((8, 2, 4)), 16)
+    y = oracle.dyn_conv(x, base, np.zeros((B, 2, 4)), 16)
     assert np.array_equal(y[0], np.zeros(64))          # the anchor sees nothing before the block
     assert np.array_equal(y[1:], x[:-1])
 
@@ -187,11 +188,12 @@ def _sdpa(q, k, v, mask=None):
     return torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=mask).numpy()
 
 
-def test_attention_dense_case_matches_library():
+@pytest.mark.parametrize("B", [8, 16])
+def test_attention_dense_case_matches_library(B):
     """With every context key inside the window the block attention is plain
-    noncausal GQA softmax attention (torch SDPA in float64)."""
+    noncausal GQA softmax attention (torch SDPA in float64), for blocks of 8 and 16."""
     rng = np.random.default_rng(6)
-    B, nq, nkv, hd, L = 8, 8, 2, 128, 300
+    nq, nkv, hd, L = 8, 2, 128, 300
     q = rng.normal(0, 1, (B, nq, hd))
     kb, vb = rng.normal(0, 1, (B, nkv, hd)), rng.normal(0, 1, (B, nkv, hd))
     kc, vc = rng.normal(0, 1, (L, nkv, hd)), rng.normal(0, 1, (L, nkv, hd))
@@ -205,9 +207,10 @@ def test_attention_dense_case_matches_library():
     assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
 
 
-def test_attention_window_matches_masked_library_and_ignores_masked_keys():
+@pytest.mark.parametrize("B", [8, 16])
+def test_attention_window_matches_masked_library_and_ignores_masked_keys(B):
     rng = np.random.default_rng(7)
-    B, nq, nkv, hd, W = 8, 4, 1, 128, 64
+    nq, nkv, hd, W = 4, 1, 128, 64
     L = 200
     q = rng.normal(0, 1, (B, nq, hd))
     kb, vb = rng.normal(0, 1, (B, nkv, hd)), rng.normal(0, 1, (B, nkv, hd))
@@ -534,9 +537,10 @@ def _torch_layer_reference(g, W, x, c, kctx, vctx, L, pos_blk):
     H, hd, nq, nkv = g.hidden, g.head_dim, g.n_q_heads, g.n_kv_heads
     x = T(x)
     a = F.rms_norm(x, (H,), v("l0.input_norm"), eps=g.rms_eps)
-    q = F.rms_norm(F.linear(a, w("l0.q")).view(8, nq, hd), (hd,), v("l0.q_norm"), eps=g.rms_eps)
-    k = F.rms_norm(F.linear(a, w("l0.k")).view(8, nkv, hd), (hd,), v("l0.k_norm"), eps=g.rms_eps)
-    vv = F.linear(a, w("l0.v")).view(8, nkv, hd)
+    B = x.shape[0]
+    q = F.rms_norm(F.linear(a, w("l0.q")).view(B, nq, hd), (hd,), v("l0.q_norm"), eps=g.rms_eps)
+    k = F.rms_norm(F.linear(a, w("l0.k")).view(B, nkv, hd), (hd,), v("l0.k_norm"), eps=g.rms_eps)
+    vv = F.linear(a, w("l0.v")).view(B, nkv, hd)
     inv = T(oracle.rope_inv_freq(hd, g.rope_theta))
     ang = T(pos_blk)[:, None] * inv[None]
     rot = lambda t: torch.view_as_real(torch.view_as_complex(
@@ -551,35 +555,39 @@ def _torch_layer_reference(g, W, x, c, kctx, vctx, L, pos_blk):
     rep = nq // nkv
     o = F.scaled_dot_product_attention(q.transpose(0, 1), K.transpose(0, 1).repeat_interleave(rep, 0),
                                        V.transpose(0, 1).repeat_interleave(rep, 0))
-    x = x + F.linear(o.transpose(0, 1).reshape(8, nq * hd), w("l0.o"))
+    x = x + F.linear(o.transpose(0, 1).reshape(B, nq * hd), w("l0.o"))
     m = F.rms_norm(x, (H,), v("l0.post_norm"), eps=g.rms_eps)
     x = x + F.linear(F.silu(F.linear(m, w("l0.gate"))) * F.linear(m, w("l0.up")), w("l0.down"))
     return x.numpy()
 
 
-def test_draft_layer_reduces_to_qwen3_layer_with_identity_conv():
+@pytest.mark.parametrize("block", [8, 16])
+def test_draft_layer_reduces_to_qwen3_layer_with_identity_conv(block):
+    """With identity convolutions a draft layer is a Qwen3 decoder layer over the
+    block rows (anchor + block-1 masks, noncausal) and the context keys, for blocks
+    of 8 and of 16 positions ([LUCE] greedy-width commit: block 16)."""
     import dataclasses
-    g = dataclasses.replace(wk.TOY, hidden=256, ffn=512, vocab=1024, n_q_heads=4, n_kv_heads=2)
+    g = dataclasses.replace(wk.TOY, hidden=256, ffn=512, vocab=1024, n_q_heads=4, n_kv_heads=2, block=block)
     W = wk.make_weights(g, "bf16", 21)
     for n in ("l0.attn_base", "l0.mlp_base"):
         W[n] = wk.bf16_bits_from_f32(np.stack([np.ones(g.hidden), np.zeros(g.hidden)] * 2).astype(np.float32))
     for n in ("l0.attn_delta", "l0.mlp_delta"):
         W[n] = {"kind": "bf16", "w": np.zeros_like(W[n]["w"])}
     rng = np.random.default_rng(22)
-    ctx_len, n_new = 40, 8
+    ctx_len, n_new = 40, block
     cap = 64
     kc = [wk.bf16_bits_from_f32(rng.normal(0, 1, (cap, 2, 128)).astype(np.float32))]
     vc = [wk.bf16_bits_from_f32(rng.normal(0, 1, (cap, 2, 128)).astype(np.float32))]
     taps = rng.normal(0, 1, (n_new, 5 * g.hidden)).astype(np.float32)
     tr = oracle.draft_block(g, W, 17, ctx_len, n_new, taps, kc, vc)
     L = ctx_len + n_new
-    x0 = oracle.bf16_to_f64(W["embed"][[17] + [g.mask_id] * 7])
+    x0 = oracle.bf16_to_f64(W["embed"][[17] + [g.mask_id] * (block - 1)])
     ref = _torch_layer_reference(g, W, x0, tr["c"], oracle.bf16_to_f64(kc[0][:L]), oracle.bf16_to_f64(vc[0][:L]),
-                                 L, np.arange(L, L + 8))
+                                 L, np.arange(L, L + block))
     assert np.allclose(tr["x0"], ref, rtol=1e-10, atol=1e-10)
     # the appended context rows are the taps projection through W_k / W_v of that layer
     c = tr["c"]
-    kref = oracle.rope_neox(oracle.rmsnorm((c @ oracle.matrix_f64(W["l0.k"]).T).reshape(8, 2, 128),
+    kref = oracle.rope_neox(oracle.rmsnorm((c @ oracle.matrix_f64(W["l0.k"]).T).reshape(block, 2, 128),
                                            W["l0.k_norm"], g.rms_eps), np.arange(ctx_len, L), g.rope_theta)
     assert np.allclose(oracle.bf16_to_f64(kc[0][ctx_len:L]), kref, rtol=2 ** -8, atol=1e-30)
 
@@ -784,3 +792,92 @@ def test_ddtree_verify_accepts_the_deepest_fully_matching_node():
         assert res["n_accepted"] == (depth[deepest] if deepest >= 0 else 0)
         assert res["emitted"][res["n_accepted"]] == am[deepest + 1]
         assert res["n_emitted"] == res["n_accepted"] + 1
+
+
+# ----------------------------------------------------------------------------- wider blocks, narrowing
+
+def _plain_next(seq, V):
+    """A deterministic stand-in for the target's greedy next token: a fixed hash of the
+    last three tokens (any function of the prefix would do)."""
+    a, b, c = (list(seq[-3:]) + [0, 0, 0])[:3]
+    return (a * 1_000_003 + b * 7_919 + c * 104_729 + len(seq) * 31) % V
+
+
+@pytest.mark.parametrize("block", [8, 10, 12, 16, 20, 24])
+def test_greedy_chain_equals_plain_decode_at_any_width(block):
+    """[LUCE] greedy-width commit: greedy chain verification emits exactly what plain
+    decoding emits at any draft width (byte-identical completions at widths 8 to 24).
+    Drafts that are right with probability 0.7 per position (else a random token) go
+    through the oracle's greedy verify and serving-loop update, with target rows whose
+    argmax is the stand-in target's next token after the proposals; the emitted text
+    must equal plain decoding's, and every step must emit between 1 and block tokens."""
+    V = 97
+    rng = np.random.default_rng(block)
+    prompt = [5, 9, 13]
+    plain = list(prompt)
+    for _ in range(200):
+        plain.append(_plain_next(plain, V))
+    seq = list(prompt)
+    ctx, nn, anchor, off = len(prompt) - 1, 1, prompt[-1], 0
+    steps = 0
+    while len(seq) < len(plain):
+        path = []
+        for j in range(block - 1):
+            right = _plain_next(seq + path, V)
+            path.append(right if rng.random() < 0.7 else int(rng.integers(V)))
+        z = rng.normal(0, 1, (block, V))
+        for j in range(block):
+            z[j, _plain_next(seq + path[:j], V)] = 10.0
+        res = oracle.verify(z, np.array(path), np.zeros((block - 1, 16), np.int32), np.zeros((block - 1, 16)),
+                            0.0, 0, off)
+        ne = res["n_emitted"]
+        assert 1 <= ne <= block and res["n_accepted"] == ne - 1
+        em = [int(t) for t in res["emitted"][:ne]]
+        assert list(res["emitted"][ne:]) == [-1] * (block - ne)
+        seq += em
+        ctx, nn, anchor, off = oracle.advance(ctx, nn, anchor, res["emitted"], ne, off, block)
+        assert anchor == seq[-1] and nn == ne
+        steps += 1
+    n = min(len(seq), len(plain))
+    assert seq[:n] == plain[:n]
+    assert steps < len(plain) - len(prompt)      # wider than one token per step on average
+
+
+def test_block_width_rule_page_points():
+    """[LUCE] long-context commits: past the threshold (default 8192 after the first
+    cut's 32768) a block-16 drafter narrows to 8; below it nothing changes; the rule
+    reads the context length only; 0 disables it.  The page's measured prompts:
+    6,208 keeps the wide block, 13,148 / 26,728 / 39,861 / 81,365 narrow."""
+    bw = oracle.block_width
+    assert bw(6_208, 16, 16) == 16
+    for ctx in (13_148, 26_728, 39_861, 81_365):
+        assert bw(ctx, 16, 16) == 8
+    assert bw(39_861, 16, 16, ctx_threshold=32_768) == 8 and bw(26_728, 16, 16, ctx_threshold=32_768) == 16
+    assert bw(81_365, 16, 16, ctx_threshold=0) == 16
+    # the boundary (reading: strictly past the threshold; the context is ctx_len + n_new)
+    assert bw(8_192 - 16, 16, 16) == 16 and bw(8_192 - 15, 16, 16) == 8
+    assert bw(8_000, 0, 8) == 8                  # a block-8 drafter has nothing to narrow
+
+
+def test_advance_block16():
+    """The serving-loop update with blocks of 16: up to 16 emitted tokens become the next
+    step's new rows."""
+    em = list(range(200, 216))
+    assert oracle.advance(1000, 16, 3, em, 16, 0, 16) == (1016, 16, 215, 1)
+    assert oracle.advance(1016, 16, 215, em[:11] + [-1] * 5, 11, 1, 16) == (1032, 11, 210, 2)
+    assert oracle.advance(1032, 11, 210, [-1] * 16, 0, 2, 16) == (1043, 0, 210, 3)
+
+
+def test_ddtree_verify_block16_depth():
+    """A chain tree as deep as a block of 16 allows (15 nodes) accepted end to end emits
+    16 tokens."""
+    V = 50
+    tok = np.arange(1, 16, dtype=np.int32)
+    par = np.arange(-1, 14, dtype=np.int32)
+    z = np.zeros((16, V))
+    for j in range(15):
+        z[j, tok[j]] = 1.0
+    z[15, 42] = 1.0
+    res = oracle.ddtree_verify(z, tok, par, block=16)
+    assert res["n_accepted"] == 15 and res["n_emitted"] == 16
+    assert list(res["emitted"]) == list(range(1, 16)) + [42]

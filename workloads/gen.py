@@ -263,22 +263,23 @@ def make_selector_inputs(V: int, R: int, seed: int, integer: bool = False, K: in
     return {"anchors": anchors, "cand_ids": cand, "cand_logits": cl, "gate": gate}
 
 
-def make_verify_inputs(V: int, R: int, seed: int, temps, integer: bool = False, accept_depth=None, K: int = 16):
-    """Synthetic verify inputs: target rows [R][8][V], a path through distinct candidate
-    ids [R][7][16] with q rows [R][7][16].  Target rows are N(0, 1.5) (integers in
-    [-4, 4] when integer=True) with the path token raised by `boost` on the first
-    accept_depth[r] rows, so acceptance depths vary."""
+def make_verify_inputs(V: int, R: int, seed: int, temps, integer: bool = False, accept_depth=None, K: int = 16,
+                       block: int = 8):
+    """Synthetic verify inputs: target rows [R][block][V], a path through distinct
+    candidate ids [R][block-1][16] with q rows [R][block-1][16].  Target rows are
+    N(0, 1.5) (integers in [-4, 4] when integer=True) with the path token raised by
+    `boost` on the first accept_depth[r] rows, so acceptance depths vary."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x7E2])))
-    P = 7
+    P = block - 1
     if integer:
-        z = rng.integers(-4, 5, size=(R, 8, V)).astype(np.float32)
+        z = rng.integers(-4, 5, size=(R, block, V)).astype(np.float32)
     else:
-        z = rng.normal(0, 1.5, size=(R, 8, V)).astype(np.float32)
+        z = rng.normal(0, 1.5, size=(R, block, V)).astype(np.float32)
     cand = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(P)]) for _ in range(R)]).astype(np.int32)
     q = rng.dirichlet(np.ones(K) * 0.5, size=(R, P)).astype(np.float32)
     pick = rng.integers(0, K, size=(R, P))
     path = np.take_along_axis(cand, pick[..., None], axis=2)[..., 0].astype(np.int32)
-    depth = accept_depth if accept_depth is not None else rng.integers(0, 8, size=R)
+    depth = accept_depth if accept_depth is not None else rng.integers(0, block, size=R)
     for r in range(R):
         for j in range(min(int(depth[r]), P)):
             z[r, j, path[r, j]] += 6.0 if not integer else 8.0
