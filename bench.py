@@ -118,11 +118,12 @@ def step_bytes(wl, n_req):
     per_weight = 2.0 if wl.weight_format == "bf16" else 68.0 / 64.0
     w = (mats * g.n_layers + H * g.n_taps * H + g.rank * H) * per_weight
     w += V * H * 2                                           # LM head (BF16 in both formats)
-    w += (1 + 6 * 16 + 7 * 16) * g.rank * per_weight * n_req  # codebook rows gathered
+    P = g.block - 1                                          # proposals per request
+    w += (1 + (P - 1) * 16 + P * 16) * g.rank * per_weight * n_req  # codebook rows gathered
     kv_key = 2 * g.kv_dim * 2 * g.n_layers                   # K and V, BF16, all layers
-    kv = sum(min(c, g.window - 1) for c in wl.ctx[:n_req]) * kv_key + 8 * n_req * kv_key
-    taps = n_req * 8 * g.n_taps * H * 4
-    target = n_req * 8 * V * 4
+    kv = sum(min(c, g.window - 1) for c in wl.ctx[:n_req]) * kv_key + g.block * n_req * kv_key
+    taps = n_req * g.block * g.n_taps * H * 4
+    target = n_req * g.block * V * 4
     return w + kv + taps + target
 
 
@@ -199,22 +200,23 @@ def setup(wl, device_index):
             vc[l, r, lo:lo + len(V)] = V
     drafter = bd.Drafter(g, wl.weight_format, W, R, cap)
     dev = torch.device("cuda", device_index)
+    B, P = g.block, g.block - 1
     T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     S = {
         "anchors": T(inp["anchors"]), "ctx_len": T(inp["ctx_len"]), "n_new": T(inp["n_new"]),
         "taps": T(inp["taps"]), "kc": T(kc.view(np.int16)), "vc": T(vc.view(np.int16)),
-        "cand_ids": torch.zeros((R, 7, 16), dtype=torch.int32, device=dev),
-        "cand_logits": torch.zeros((R, 7, 16), dtype=torch.float32, device=dev),
-        "gate": torch.zeros((R, 7, g.rank), dtype=torch.float32, device=dev),
-        "logits": torch.zeros((R, 7, g.vocab), dtype=torch.float32, device=dev),
+        "cand_ids": torch.zeros((R, P, 16), dtype=torch.int32, device=dev),
+        "cand_logits": torch.zeros((R, P, 16), dtype=torch.float32, device=dev),
+        "gate": torch.zeros((R, P, g.rank), dtype=torch.float32, device=dev),
+        "logits": torch.zeros((R, P, g.vocab), dtype=torch.float32, device=dev),
         "temps": T(np.array(wl.temps, np.float32)),
         "seeds": T(np.full(R, wl.philox_seed, np.uint64).view(np.int64)),
         "offsets": T(np.array(wl.philox_offsets or [0] * R, np.uint64).view(np.int64)),
-        "path": torch.zeros((R, 7), dtype=torch.int32, device=dev),
-        "q_rows": torch.zeros((R, 7, 16), dtype=torch.float32, device=dev),
+        "path": torch.zeros((R, P), dtype=torch.int32, device=dev),
+        "q_rows": torch.zeros((R, P, 16), dtype=torch.float32, device=dev),
         "status": torch.zeros((R,), dtype=torch.int32, device=dev),
         "n_acc": torch.zeros((R,), dtype=torch.int32, device=dev),
-        "emitted": torch.zeros((R, 8), dtype=torch.int32, device=dev),
+        "emitted": torch.zeros((R, B), dtype=torch.int32, device=dev),
         "n_emit": torch.zeros((R,), dtype=torch.int32, device=dev),
     }
     # untimed pass: drafter logits -> synthetic target rows = drafter logits + N(0, sigma)
@@ -222,11 +224,11 @@ def setup(wl, device_index):
                            S["cand_ids"], S["cand_logits"], S["gate"], S["logits"])
     torch.cuda.synchronize()
     lg = S["logits"]
-    target = torch.empty((R, 8, g.vocab), dtype=torch.float32, device=dev)
+    target = torch.empty((R, B, g.vocab), dtype=torch.float32, device=dev)
     for r in range(R):
         noise = torch.from_numpy(wk.make_target_noise(wl, 0, r)).to(dev)
-        target[r, :7] = lg[r] + noise[:7]
-        target[r, 7] = lg[r, 6] + noise[7]
+        target[r, :P] = lg[r] + noise[:P]
+        target[r, P] = lg[r, P - 1] + noise[P]
     S["target"] = target
     setup_s = time.time() - t0
     return drafter, S, W, inp, kc, vc, setup_s
@@ -310,11 +312,11 @@ def measure_point(args, world, local_rank, cfg):
     sb = step_bytes(wl, R)
     step_s = ms / 1e3 / K
     lm_bytes = bd.dflash2_lmhead_bytes(h, R)
-    wide = R >= (5 if wl.weight_format == "bf16" else 4)
-    out = {"workload": wl.name, "requests_per_gpu": R, "context": wl.ctx[:R] if R <= 4 else "U[512, 32768]",
+    wide = R * wl.geom.block >= (40 if wl.weight_format == "bf16" else 32)
+    out = {"workload": wl.name, "block": wl.geom.block, "requests_per_gpu": R, "context": wl.ctx[:R] if R <= 4 else "U[512, 32768]",
            "weights": wl.weight_format, "temperature": wl.temps[:R] if R <= 4 else "round-robin 0, 0.7, 1.0",
            "steps": K, "value": job_rate(K, world, ms), "unit": "steps/s", "ms_per_step": ms / K,
-           "drafted_tokens_per_s": job_rate(K, world, ms) * 7 * R,
+           "drafted_tokens_per_s": job_rate(K, world, ms) * (wl.geom.block - 1) * R,
            "step_bytes": sb, "step_gbs": sb / step_s / 1e9, "step_hbm_frac": sb / step_s / 1e9 / pk["hbm_gbs"],
            "step_frac_vs_8tbs": sb / step_s / 1e9 / NOMINAL_HBM_GBS,
            "lmhead": {"kernel": ("wide_kernel<0> (LM head, tcgen05 GEMM) + logits_topk_kernel" if wide
@@ -609,13 +611,15 @@ def main_ours(args, rank, world, local_rank):
         "setup_s": setup_s,
     }
     if args.config == 2 and not args.no_r16:
-        # the metric's other operating points: 16 requests (configuration 5), and the
-        # Q8 one-request and four-request workloads (configurations 3 and 4)
+        # the metric's other operating points: 16 requests (configuration 5), the Q8
+        # one-request and four-request workloads (configurations 3 and 4), and the
+        # one-request workload with blocks of 16
         del graph
         torch.cuda.synchronize()
         line["r16"] = measure_point(args, world, local_rank, 5)
         line["q8_r1"] = measure_point(args, world, local_rank, 3)
         line["r4"] = measure_point(args, world, local_rank, 4)
+        line["block16"] = measure_point(args, world, local_rank, 9)
     if rank == 0 and not args.no_cpu_baseline:
         cb, _ = cpu_baseline(wl, W, inp, kc_host, vc_host, S["target"].cpu().numpy())
         line["cpu_baseline"] = cb

@@ -60,10 +60,11 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         L.dflash2_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, i32, ctypes.POINTER(vp)]
         L.dflash2_destroy.argtypes = [vp]
-        L.dflash2_draft_block.argtypes = [vp, i32] + [vp] * 11
-        L.dflash2_select.argtypes = [vp, i32] + [vp] * 12
-        L.dflash2_verify.argtypes = [vp, i32] + [vp] * 13
+        L.dflash2_draft_block.argtypes = [vp, i32] + [vp] * 12
+        L.dflash2_select.argtypes = [vp, i32] + [vp] * 13
+        L.dflash2_verify.argtypes = [vp, i32] + [vp] * 14
         L.dflash2_advance.argtypes = [vp, i32] + [vp] * 7
+        L.dflash2_block_width.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp]
         L.dflash2_set_select_mode.argtypes = [vp, i32]
         L.dflash2_head_topk.argtypes = [vp, i32] + [vp] * 5
         L.dflash2_head_topk.restype = i32
@@ -139,24 +140,24 @@ def dflash2_destroy(h: int):
 
 
 def dflash2_draft_block(h, n_req, anchor_ids, ctx_len, n_new, taps, k_cache, v_cache, cand_ids, cand_logits, gate,
-                        logits_out=None, stream=None):
+                        logits_out=None, width=None, stream=None):
     _check(lib().dflash2_draft_block(h, n_req, _p(anchor_ids), _p(ctx_len), _p(n_new), _p(taps), _p(k_cache),
                                      _p(v_cache), _p(cand_ids), _p(cand_logits), _p(gate), _p(logits_out),
-                                     _stream(stream)), "dflash2_draft_block")
+                                     _p(width), _stream(stream)), "dflash2_draft_block")
 
 
 def dflash2_select(h, n_req, anchor_ids, cand_ids, cand_logits, gate, temperature, seed, philox_offset, path, q_rows,
-                   scores_out, status, stream=None):
+                   scores_out, status, width=None, stream=None):
     _check(lib().dflash2_select(h, n_req, _p(anchor_ids), _p(cand_ids), _p(cand_logits), _p(gate), _p(temperature),
                                 _p(seed), _p(philox_offset), _p(path), _p(q_rows), _p(scores_out), _p(status),
-                                _stream(stream)), "dflash2_select")
+                                _p(width), _stream(stream)), "dflash2_select")
 
 
 def dflash2_verify(h, n_req, target_logits, path, cand_ids, q_rows, temperature, seed, philox_offset, n_accepted,
-                   emitted, n_emitted, probs_out, status, stream=None):
+                   emitted, n_emitted, probs_out, status, width=None, stream=None):
     _check(lib().dflash2_verify(h, n_req, _p(target_logits), _p(path), _p(cand_ids), _p(q_rows), _p(temperature),
                                 _p(seed), _p(philox_offset), _p(n_accepted), _p(emitted), _p(n_emitted),
-                                _p(probs_out), _p(status), _stream(stream)), "dflash2_verify")
+                                _p(probs_out), _p(status), _p(width), _stream(stream)), "dflash2_verify")
 
 
 def dflash2_tree_build(h, n_req, budget, anchor_ids, cand_ids, cand_logits, gate, node_token, node_parent, node_depth,
@@ -180,6 +181,11 @@ def dflash2_set_select_mode(h, mode: int):
 def dflash2_advance(h, n_req, emitted, n_emitted, anchor_ids, ctx_len, n_new, philox_offset, stream=None):
     _check(lib().dflash2_advance(h, n_req, _p(emitted), _p(n_emitted), _p(anchor_ids), _p(ctx_len), _p(n_new),
                                  _p(philox_offset), _stream(stream)), "dflash2_advance")
+
+
+def dflash2_block_width(h, n_req, ctx_len, n_new, ctx_threshold: int, narrow_width: int, width, stream=None):
+    _check(lib().dflash2_block_width(h, n_req, _p(ctx_len), _p(n_new), ctx_threshold, narrow_width, _p(width),
+                                     _stream(stream)), "dflash2_block_width")
 
 
 def dflash2_head_topk(h, n_rows, hidden, cand_ids, cand_logits, logits_out=None, stream=None):

@@ -28,13 +28,14 @@ struct dflash2_handle {
   dflash2_config cfg;
   dflash2_weights w;
   int max_req, kv_cap, num_sms, fmt;
+  int B;  // block positions per request (8 or 16); rows are request-major, B per request
   bool pdl;
   int H, G, F, V, nq, nkv, qd, kvd, KT;
   int nch_ss;  // 32-channel chunks of the sums-of-squares partials
   int n_attn_chunks, n_verify_chunks, lm_ctas;
   // where each projection's partial planes are (the launches' shapes are fixed at create)
   // plane maps of every projection launch: the GEMV (up to 4 requests) and the
-  // tensor-core GEMM (calls with at least wide_min_requests requests; set up when
+  // tensor-core GEMM (calls with at least wide_min_rows block rows; set up when
   // max_requests reaches that)
   struct PlaneSet {
     GemvPlanes fc, d0, d, q, k, v, o, g, u, down, sel, lm;
@@ -51,8 +52,8 @@ struct dflash2_handle {
   CUtensorMap map_lm, xm_lm;  // LM head weights; final hidden (bf16 in both formats) for the LM head
   int* gemv_err;  // device word set by a GEMV whose pipeline wait gave up
   unsigned int* verify_cnt;  // [max_req] verify chunk counters (zero between launches)
-  float* sel_lat;            // [max_req][7][16][16] selector lattice scratch
-  int32_t* sel_bad;          // [max_req][7] nonfinite flags per position
+  float* sel_lat;            // [max_req][B-1][16][16] selector lattice scratch
+  int32_t* sel_bad;          // [max_req][B-1] nonfinite flags per position
   unsigned int* sel_cnt;     // [max_req] selector position counters (zero between launches)
   VerifyStat* tstats;        // [max_req][kTreeMaxNodes + 1][n_verify_chunks] draft-tree row statistics
   unsigned int* tree_cnt;    // [max_req] draft-tree verify counters (zero between launches)
@@ -88,7 +89,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
   } while (0)
 
 // One projection segment: out[s] = W[:, split s] X[:, split s]^T for the
-// 8 * n_tiles activation rows starting at x.
+// 8 * n_tiles activation rows starting at x (tiles of 8 rows; B / 8 tiles per request).
 enum { kQ, kK, kV, kO, kGate, kUp, kDown, kAttnDelta, kMlpDelta };
 
 // One projection segment of either path.  x_rows: rows of one plane of the
@@ -170,10 +171,11 @@ struct DraftScope {
   ~DraftScope() { h->in_draft = false; }
 };
 
-// Calls with at least this many requests run every projection on the tensor-core
-// GEMM (measured: with int8 weights it overtakes the GEMV at four requests, whose
-// key/value launch needs the GEMV's 8-tile variant; with bf16 at five).
-int wide_min_requests(int fmt) { return fmt == DFLASH2_WEIGHTS_BF16 ? 5 : 4; }
+// Calls with at least this many block rows run every projection on the tensor-core
+// GEMM (measured with blocks of 8: with int8 weights it overtakes the GEMV at 32 rows,
+// whose key/value launch needs the GEMV's 8-tile variant; with bf16 at 40).
+int wide_min_rows(int fmt) { return fmt == DFLASH2_WEIGHTS_BF16 ? 40 : 32; }
+bool wide_call(const dflash2_handle* h, int n_req) { return n_req * h->B >= wide_min_rows(h->fmt); }
 
 bool valid_matrix(const dflash2_matrix& m, int fmt) {
   if (!m.w || !aligned16(m.w)) return false;
@@ -207,15 +209,17 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
     return DFLASH2_E_INVAL;
   if (c.mask_token_id < 0 || c.mask_token_id >= c.vocab) return DFLASH2_E_INVAL;
   if (c.weight_format != DFLASH2_WEIGHTS_BF16 && c.weight_format != DFLASH2_WEIGHTS_Q8G64) return DFLASH2_E_INVAL;
-  if (c.head_dim != 128 || c.block != 8 || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
+  if (c.head_dim != 128 || (c.block != 8 && c.block != 16) || c.top_k != 16 || c.rank != 256 || c.conv_taps != 2 ||
       c.conv_group != 16 || c.n_layers > DFLASH2_MAX_LAYERS || c.n_q_heads != 4 * c.n_kv_heads ||
-      c.hidden % 256 || c.ffn % (c.weight_format == DFLASH2_WEIGHTS_BF16 ? 128 : 256) || c.vocab % 16 || max_requests > DFLASH2_MAX_REQUESTS ||
+      c.hidden % 256 || c.ffn % (c.weight_format == DFLASH2_WEIGHTS_BF16 ? 128 : 256) || c.vocab % 16 ||
+      max_requests * c.block > 8 * DFLASH2_MAX_REQUESTS ||
       (c.window - 1 + kAttnChunk - 1) / kAttnChunk + 1 > 64)
     return DFLASH2_E_UNSUPPORTED;
   const int fmt = c.weight_format;
-  // the tensor-core GEMM (handles of wide_min_requests or more requests) takes weight
+  // the tensor-core GEMM (handles of wide_min_rows or more block rows) takes weight
   // blocks of 128 rows: the delta projections' hidden/4 and the vocabulary
-  if (max_requests >= wide_min_requests(fmt) && ((c.hidden / 4) % 128 || c.vocab % 128)) return DFLASH2_E_UNSUPPORTED;
+  if (max_requests * c.block >= wide_min_rows(fmt) && ((c.hidden / 4) % 128 || c.vocab % 128))
+    return DFLASH2_E_UNSUPPORTED;
   if (!w->embed || !w->lm_head || !w->hidden_norm || !w->final_norm || !aligned16(w->lm_head)) return DFLASH2_E_INVAL;
   if (!valid_matrix(w->fc, fmt) || !valid_matrix(w->sel_proj, fmt) || !valid_matrix(w->cb_a, fmt) ||
       !valid_matrix(w->cb_b, fmt))
@@ -235,6 +239,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->max_req = max_requests;
   h->kv_cap = kv_capacity;
   h->fmt = fmt;
+  h->B = c.block;
   h->pdl = true;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -257,7 +262,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   h->lm_ctas = lmhead_ctas(h->num_sms);
   // plane maps of every projection launch (shapes only; the same plans as launch_gemv's
   // and launch_wide's), and the largest plane count of each output buffer over both
-  h->wide = max_requests >= wide_min_requests(fmt);
+  h->wide = max_requests * h->B >= wide_min_rows(fmt);
   h->lm_chunks = (c.vocab + kLogitChunk - 1) / kLogitChunk;
   int maxp_fc = 0, maxp_d = 0, maxp_q = 0, maxp_k = 0, maxp_v = 0, maxp_y = 0, maxp_g = 0, maxp_u = 0, maxp_sel = 0,
       maxp_lm = 0;
@@ -329,7 +334,7 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
     delete h;
     return DFLASH2_E_UNSUPPORTED;
   }
-  const size_t N = 8 * static_cast<size_t>(max_requests);
+  const size_t N = static_cast<size_t>(h->B) * max_requests;  // block rows
   const size_t esz = 2;  // bf16 / fp16 activations
   struct Buf {
     void** p;
@@ -350,8 +355,8 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->q), N * h->qd * 4},
       {reinterpret_cast<void**>(&h->kb), N * h->kvd * 4},
       {reinterpret_cast<void**>(&h->vb), N * h->kvd * 4},
-      {reinterpret_cast<void**>(&h->attn_part),
-       static_cast<size_t>(max_requests) * h->nkv * h->n_attn_chunks * 32 * 130 * 4},
+      // per (request, KV head, part): 4 B queries x (max, sum, 128 outputs)
+      {reinterpret_cast<void**>(&h->attn_part), 4 * N * h->nkv * h->n_attn_chunks * 130 * 4},
       {reinterpret_cast<void**>(&h->ypart), maxp_y * N * h->H * 4},
       {reinterpret_cast<void**>(&h->gpart), maxp_g * N * h->F * 4},
       {reinterpret_cast<void**>(&h->upart), maxp_u * N * h->F * 4},
@@ -364,12 +369,12 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       {reinterpret_cast<void**>(&h->topk_keys), N * std::max(h->lm_ctas, h->wide ? h->lm_chunks : 0) * 16 * 8},
       {reinterpret_cast<void**>(&h->lm_part), static_cast<size_t>(maxp_lm) * N * h->V * 4},
       {reinterpret_cast<void**>(&h->vstats),
-       static_cast<size_t>(max_requests) * 8 * h->n_verify_chunks * sizeof(VerifyStat)},
+       N * h->n_verify_chunks * sizeof(VerifyStat)},
       {reinterpret_cast<void**>(&h->inv_freq), 64 * 8},
       {reinterpret_cast<void**>(&h->gemv_err), 4},
       {reinterpret_cast<void**>(&h->verify_cnt), static_cast<size_t>(max_requests) * 4},
-      {reinterpret_cast<void**>(&h->sel_lat), static_cast<size_t>(max_requests) * 7 * 16 * 16 * 4},
-      {reinterpret_cast<void**>(&h->sel_bad), static_cast<size_t>(max_requests) * 7 * 4},
+      {reinterpret_cast<void**>(&h->sel_lat), static_cast<size_t>(max_requests) * (h->B - 1) * 16 * 16 * 4},
+      {reinterpret_cast<void**>(&h->sel_bad), static_cast<size_t>(max_requests) * (h->B - 1) * 4},
       {reinterpret_cast<void**>(&h->sel_cnt), static_cast<size_t>(max_requests) * 4},
       {reinterpret_cast<void**>(&h->tstats),
        static_cast<size_t>(max_requests) * (kTreeMaxNodes + 1) * h->n_verify_chunks * sizeof(VerifyStat)},
@@ -467,8 +472,8 @@ dflash2_status dflash2_debug_set_pipeline_error(dflash2_handle* h, void* stream)
 
 int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
   if (!h || n_req < 1) return -1;
-  const int64_t N = 8 * static_cast<int64_t>(n_req);
-  if (n_req >= wide_min_requests(h->fmt))          // tensor-core GEMM + chunked top-16
+  const int64_t N = static_cast<int64_t>(h->B) * n_req;
+  if (wide_call(h, n_req))                         // tensor-core GEMM + chunked top-16
     return static_cast<int64_t>(h->V) * h->H * 2   // LM-head weights, read once
            + N * h->H * 2                          // bf16 hidden state, one plane
            + 2 * N * h->V * 4                      // logits written, then read by the top-16
@@ -481,7 +486,7 @@ int64_t dflash2_lmhead_bytes(const dflash2_handle* h, int32_t n_req) {
 dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
                                    const int32_t* ctx_len, const int32_t* n_new, const float* taps, void* k_cache,
                                    void* v_cache, int32_t* cand_ids, float* cand_logits, float* gate,
-                                   float* logits_out, void* stream) {
+                                   float* logits_out, const int32_t* width, void* stream) {
   if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
   if (!anchor_ids || !ctx_len || !n_new || !taps || !k_cache || !v_cache || !cand_ids || !cand_logits || !gate)
     return DFLASH2_E_INVAL;
@@ -491,16 +496,17 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   const dflash2_config& c = h->cfg;
   const int fmt = h->fmt;
   const bool pdl = h->pdl;
-  const int R = n_req;
-  const int N = 8 * R;
+  const int R = n_req, B = h->B;
+  const int N = B * R;    // block rows
+  const int NT = N / 8;   // 8-row tiles of the projections
   const int H = h->H, G = h->G;
   const size_t layer_stride = static_cast<size_t>(h->max_req) * h->kv_cap * h->kvd;  // elements
-  const int N8 = 8 * h->max_req;  // rows of one plane of each activation buffer
-  // many requests: every projection on the tensor-core GEMM
-  const bool wide = R >= wide_min_requests(fmt);
+  const int N8 = B * h->max_req;  // rows of one plane of each activation buffer
+  // many block rows: every projection on the tensor-core GEMM
+  const bool wide = wide_call(h, R);
   const dflash2_handle::PlaneSet& P = wide ? h->pw : h->pn;
   // the tensor-core path reads its activations as one plane in the GEMM's operand
-  // layout, slices of 8 max_requests rows rounded up to 16 (16 max_requests for the
+  // layout, slices of B max_requests rows rounded up to 16 (2 B max_requests for the
   // QKV input): a slice holds every row the MMA reads (rows rounded up to 16)
   const int tA = wide ? (N8 + 15) & ~15 : 0, tQ = wide ? 2 * N8 : 0;
   // the projections' inputs carry a low-order plane only on the GEMV path with bf16
@@ -529,6 +535,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.fmt = fmt;
     a.V = h->V;
     a.pipe_err = h->gemv_err;
+    a.B = h->B;
     DF2_CHECK(launch_start(a, R, pdl, st));
     h->launches++;
   }
@@ -550,6 +557,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.fmt = fmt;
     a.pl = l == 0 ? P.d0 : P.d;
     a.n_rows = N;
+    a.B = B;
     a.eps = c.rms_eps;
     return a;
   };
@@ -559,8 +567,8 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   {
     dflash2_status s =
         run_gemv(h, wide,
-                 {seg(h->map_fc, h->wmap_fc, h->w.fc, h->xm_taps, h->act_taps, N8, R, H, h->KT, h->fc_out),
-                  seg(h->map_layer[0][kAttnDelta], h->wmap_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, h->act_a, N8, R, 4 * G, H,
+                 {seg(h->map_fc, h->wmap_fc, h->w.fc, h->xm_taps, h->act_taps, N8, NT, H, h->KT, h->fc_out),
+                  seg(h->map_layer[0][kAttnDelta], h->wmap_layer[0][kAttnDelta], h->w.layers[0].attn_delta, h->xm_a, h->act_a, N8, NT, 4 * G, H,
                       h->dproj)},
                  st);
     if (s) return s;
@@ -587,7 +595,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     dflash2_status s = DFLASH2_OK;
     if (l > 0) {
       // ---- a3: delta projection of the normed input, conv-in
-      s = run_gemv(h, wide, {seg(h->map_layer[l][kAttnDelta], h->wmap_layer[l][kAttnDelta], L.attn_delta, h->xm_a, h->act_a, N8, R, 4 * G, H, h->dproj)},
+      s = run_gemv(h, wide, {seg(h->map_layer[l][kAttnDelta], h->wmap_layer[l][kAttnDelta], L.attn_delta, h->xm_a, h->act_a, N8, NT, 4 * G, H, h->dproj)},
                    st);
       if (s) return s;
       DF2_CHECK(launch_conv_in(conv_in_attn(l), R, pdl, st));
@@ -595,9 +603,9 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     }
     // ---- a4: q (block rows), k and v (block + new context rows)
     s = run_gemv(h, wide,
-                 {seg(h->map_layer[l][kQ], h->wmap_layer[l][kQ], L.q, h->xm_qkv, h->act_qkv, 2 * N8, R, h->qd, H, h->q_out),
-                  seg(h->map_layer[l][kK], h->wmap_layer[l][kK], L.k, h->xm_qkv, h->act_qkv, 2 * N8, 2 * R, h->kvd, H, h->k_out),
-                  seg(h->map_layer[l][kV], h->wmap_layer[l][kV], L.v, h->xm_qkv, h->act_qkv, 2 * N8, 2 * R, h->kvd, H, h->v_out)},
+                 {seg(h->map_layer[l][kQ], h->wmap_layer[l][kQ], L.q, h->xm_qkv, h->act_qkv, 2 * N8, NT, h->qd, H, h->q_out),
+                  seg(h->map_layer[l][kK], h->wmap_layer[l][kK], L.k, h->xm_qkv, h->act_qkv, 2 * N8, 2 * NT, h->kvd, H, h->k_out),
+                  seg(h->map_layer[l][kV], h->wmap_layer[l][kV], L.v, h->xm_qkv, h->act_qkv, 2 * N8, 2 * NT, h->kvd, H, h->v_out)},
                  st);
     if (s) return s;
     {
@@ -626,6 +634,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.pk = P.k;
       a.pv = P.v;
       a.eps = c.rms_eps;
+      a.B = h->B;
       DF2_CHECK(launch_qkv_finish(a, R, pdl, st));
       h->launches++;
     }
@@ -651,11 +660,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.cpc = R >= 4 ? 4 : 1;
       a.n_chunks = (h->n_attn_chunks - 1 + a.cpc - 1) / a.cpc + 1;
       a.fmt = fmt;
+      a.B = h->B;
+      a.width = width;
       DF2_CHECK(launch_attention(a, R, pdl, st));
       h->launches += 2;
     }
     // ---- a6: output projection, conv-out + residual, post-attention norm input
-    s = run_gemv(h, wide, {seg(h->map_layer[l][kO], h->wmap_layer[l][kO], L.o, h->xm_o, h->act_o, N8, R, H, h->qd, h->ypart)}, st);
+    s = run_gemv(h, wide, {seg(h->map_layer[l][kO], h->wmap_layer[l][kO], L.o, h->xm_o, h->act_o, N8, NT, H, h->qd, h->ypart)}, st);
     if (s) return s;
     {
       ConvOutArgs a = {};
@@ -675,11 +686,12 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.fmt = fmt;
       a.pl = P.o;
       a.n_rows = N;
+      a.B = h->B;
       DF2_CHECK(launch_conv_out(a, R, pdl, st));
       h->launches++;
     }
     // ---- a7: MLP sublayer
-    s = run_gemv(h, wide, {seg(h->map_layer[l][kMlpDelta], h->wmap_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, h->act_a, N8, R, 4 * G, H, h->dproj)}, st);
+    s = run_gemv(h, wide, {seg(h->map_layer[l][kMlpDelta], h->wmap_layer[l][kMlpDelta], L.mlp_delta, h->xm_a, h->act_a, N8, NT, 4 * G, H, h->dproj)}, st);
     if (s) return s;
     {
       ConvInArgs a = {};
@@ -698,12 +710,13 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.pl = P.d;
       a.n_rows = N;
       a.eps = c.rms_eps;
+      a.B = h->B;
       DF2_CHECK(launch_conv_in(a, R, pdl, st));
       h->launches++;
     }
     s = run_gemv(h, wide,
-                 {seg(h->map_layer[l][kGate], h->wmap_layer[l][kGate], L.gate, h->xm_qkv, h->act_qkv, 2 * N8, R, h->F, H, h->gpart),
-                  seg(h->map_layer[l][kUp], h->wmap_layer[l][kUp], L.up, h->xm_qkv, h->act_qkv, 2 * N8, R, h->F, H, h->upart)},
+                 {seg(h->map_layer[l][kGate], h->wmap_layer[l][kGate], L.gate, h->xm_qkv, h->act_qkv, 2 * N8, NT, h->F, H, h->gpart),
+                  seg(h->map_layer[l][kUp], h->wmap_layer[l][kUp], L.up, h->xm_qkv, h->act_qkv, 2 * N8, NT, h->F, H, h->upart)},
                  st);
     if (s) return s;
     {
@@ -721,7 +734,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       DF2_CHECK(launch_swiglu(a, R, pdl, st));
       h->launches++;
     }
-    s = run_gemv(h, wide, {seg(h->map_layer[l][kDown], h->wmap_layer[l][kDown], L.down, h->xm_h, h->act_h, N8, R, H, h->F, h->ypart)}, st);
+    s = run_gemv(h, wide, {seg(h->map_layer[l][kDown], h->wmap_layer[l][kDown], L.down, h->xm_h, h->act_h, N8, NT, H, h->F, h->ypart)}, st);
     if (s) return s;
     {
       const bool last = l == c.n_layers - 1;
@@ -744,6 +757,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.fmt = fmt;
       a.pl = P.down;
       a.n_rows = N;
+      a.B = h->B;
       DF2_CHECK(launch_conv_out(a, R, pdl, st));
       h->launches++;
     }
@@ -766,6 +780,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.n_cta = h->lm_ctas;
     a.eps = c.rms_eps;
     a.err = h->gemv_err;
+    a.B = h->B;
     DF2_CHECK(launch_lmhead(a, pdl, st));
     h->launches++;
   } else {
@@ -773,7 +788,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     // then the top-16 of each vocabulary chunk of each sampled row
     dflash2_status s = run_gemv(
         h, true, {seg(h->map_lm, h->wmap_lm, dflash2_matrix{h->w.lm_head, nullptr, nullptr}, h->xm_lm, h->act_fin,
-                      N8, R, h->V, H, h->lm_part)},
+                      N8, NT, h->V, H, h->lm_part)},
         st, 0, false);
     if (s) return s;
     LogitsTopkArgs a = {};
@@ -788,6 +803,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.n_chunks = h->lm_chunks;
     a.eps = c.rms_eps;
     a.pl = P.lm;
+    a.B = h->B;
     DF2_CHECK(launch_logits_topk(a, R, pdl, st));
     h->launches++;
   }
@@ -796,7 +812,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
   {
     const CUtensorMap& xin = fmt == 0 ? h->xm_fin : h->xm_a;  // same final hidden, in the matrix's format
     const void* xin_p = fmt == 0 ? static_cast<const void*>(h->act_fin) : h->act_a;
-    dflash2_status s = run_gemv(h, wide, {seg(h->map_sel, h->wmap_sel, h->w.sel_proj, xin, xin_p, N8, R, c.rank, H, h->sel_out)}, st);
+    dflash2_status s = run_gemv(h, wide, {seg(h->map_sel, h->wmap_sel, h->w.sel_proj, xin, xin_p, N8, NT, c.rank, H, h->sel_out)}, st);
     if (s) return s;
     TopkMergeArgs a = {};
     a.part_keys = h->topk_keys;
@@ -812,6 +828,7 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
     a.psel = P.sel;
     a.H = H;
     a.eps = c.rms_eps;
+    a.B = h->B;
     DF2_CHECK(launch_topk_merge(a, pdl, st));
     h->launches++;
   }
@@ -836,14 +853,31 @@ dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* 
   a.ctx_len = ctx_len;
   a.n_new = n_new;
   a.offset = philox_offset;
+  a.B = h->B;
   DF2_CHECK(launch_advance(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
+  h->launches++;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_block_width(dflash2_handle* h, int32_t n_req, const int32_t* ctx_len, const int32_t* n_new,
+                                  int32_t ctx_threshold, int32_t narrow_width, int32_t* width, void* stream) {
+  if (!h || n_req < 1 || n_req > h->max_req || !ctx_len || !n_new || !width) return DFLASH2_E_INVAL;
+  if (ctx_threshold < 0 || narrow_width < 2 || narrow_width > h->B) return DFLASH2_E_INVAL;
+  BlockWidthArgs a = {};
+  a.ctx_len = ctx_len;
+  a.n_new = n_new;
+  a.width = width;
+  a.B = h->B;
+  a.threshold = ctx_threshold;
+  a.narrow = narrow_width;
+  DF2_CHECK(launch_block_width(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches++;
   return DFLASH2_OK;
 }
 
 dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
                                  float* cand_logits, float* logits_out, void* stream) {
-  if (!h || n_rows < 8 || n_rows % 8 || n_rows > 8 * h->max_req) return DFLASH2_E_INVAL;
+  if (!h || n_rows < h->B || n_rows % h->B || n_rows > h->B * h->max_req) return DFLASH2_E_INVAL;
   if (!hidden || !cand_ids || !cand_logits || !aligned16(hidden)) return DFLASH2_E_INVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (n_rows > 32) {  // more rows than the LM-head kernel holds: tensor-core GEMM, chunked top-16
@@ -865,7 +899,8 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
     a.n_chunks = h->lm_chunks;
     a.eps = h->cfg.rms_eps;
     a.pl = h->pw.lm;
-    DF2_CHECK(launch_logits_topk(a, n_rows / 8, h->pdl, st));
+    a.B = h->B;
+    DF2_CHECK(launch_logits_topk(a, n_rows / h->B, h->pdl, st));
     TopkMergeArgs m = {};
     m.part_keys = h->topk_keys;
     m.cand_ids = cand_ids;
@@ -876,6 +911,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
     m.nch = h->nch_ss;
     m.H = h->H;
     m.eps = h->cfg.rms_eps;
+    m.B = h->B;
     DF2_CHECK(launch_topk_merge(m, h->pdl, st));
     h->launches += 2;
     return DFLASH2_OK;
@@ -894,6 +930,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   a.n_cta = h->lm_ctas;
   a.eps = h->cfg.rms_eps;
   a.err = h->gemv_err;
+  a.B = h->B;
   DF2_CHECK(launch_lmhead(a, h->pdl, st));
   TopkMergeArgs m = {};
   m.part_keys = h->topk_keys;
@@ -908,6 +945,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
   m.nch = h->nch_ss;
   m.H = h->H;
   m.eps = h->cfg.rms_eps;
+  m.B = h->B;
   DF2_CHECK(launch_topk_merge(m, h->pdl, st));
   h->launches += 2;
   return DFLASH2_OK;
@@ -916,7 +954,7 @@ dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* 
 dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids, const int32_t* cand_ids,
                               const float* cand_logits, const float* gate, const float* temperature,
                               const uint64_t* seed, const uint64_t* philox_offset, int32_t* path, float* q_rows,
-                              float* scores_out, int32_t* status, void* stream) {
+                              float* scores_out, int32_t* status, const int32_t* width, void* stream) {
   if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
   if (!anchor_ids || !cand_ids || !cand_logits || !gate || !temperature || !seed || !philox_offset || !path ||
       !q_rows || !status)
@@ -943,10 +981,12 @@ dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* a
   a.bad = h->sel_bad;
   a.counters = h->sel_cnt;
   a.mode = h->select_mode;
+  a.width = width;
   a.pipe_err = h->gemv_err;
   a.rank = h->cfg.rank;
   a.fmt = h->fmt;
   a.V = h->V;
+  a.B = h->B;
   DF2_CHECK(launch_select(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches++;
   return DFLASH2_OK;
@@ -987,6 +1027,7 @@ dflash2_status dflash2_tree_build(dflash2_handle* h, int32_t n_req, int32_t budg
   a.t_depth = node_depth;
   a.t_score = node_score;
   a.t_n = n_nodes;
+  a.B = h->B;
   DF2_CHECK(launch_select(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches++;
   return DFLASH2_OK;
@@ -1014,6 +1055,7 @@ dflash2_status dflash2_tree_verify(dflash2_handle* h, int32_t n_req, int32_t bud
   a.V = h->V;
   a.n_chunks = h->n_verify_chunks;
   a.budget = budget;
+  a.B = h->B;
   DF2_CHECK(launch_tree_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches++;
   return DFLASH2_OK;
@@ -1023,7 +1065,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
                               const int32_t* cand_ids, const float* q_rows, const float* temperature,
                               const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
                               int32_t* emitted, int32_t* n_emitted, float* probs_out, int32_t* status,
-                              void* stream) {
+                              const int32_t* width, void* stream) {
   if (!h || n_req < 1 || n_req > h->max_req) return DFLASH2_E_INVAL;
   if (!target_logits || !path || !cand_ids || !q_rows || !temperature || !seed || !philox_offset || !n_accepted ||
       !emitted || !n_emitted || !status)
@@ -1043,8 +1085,10 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   a.n_emitted = n_emitted;
   a.status = status;
   a.probs = probs_out;
+  a.width = width;
   a.V = h->V;
   a.n_chunks = h->n_verify_chunks;
+  a.B = h->B;
   DF2_CHECK(launch_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches += 1;
   return DFLASH2_OK;

@@ -1,14 +1,15 @@
-// Block attention of the drafter (step a5): 8 block queries per request attend,
-// noncausally, to all 8 block keys and to the context keys inside the sliding
+// Block attention of the drafter (step a5): B block queries per request (B = 8 or
+// 16) attend, noncausally, to all B block keys and to the context keys inside the sliding
 // window ("LSE docs/DFLASH2.md", block paragraph: noncausal within the block,
 // context keys obey the 2048-position sliding window).  Query i sits at absolute
 // position L + i (L = keys in the cache); it sees context key k iff
 // L + i - k < window.  GQA: the 4 query heads of one KV head share its keys.
 //
 // Split over keys (flash-decoding style): one CTA per (request, KV head, chunk of
-// 64 context keys), plus one CTA for the 8 block keys; all 32 queries of a KV
-// head group (4 heads x 8 positions) are handled together so every key is read
-// once.  Keys outside the window are never read.  Context chunks run on the
+// 64 context keys), plus one CTA for the B block keys; all 4 B queries of a KV
+// head group (4 heads x B positions) are handled together so every key is read
+// once.  A request narrowed to a block width w < B masks its block keys at
+// positions >= w, so its first w rows are exactly a block-w forward.  Keys outside the window are never read.  Context chunks run on the
 // tensor cores (mma.sync m16n8k16 in fp16, fp32 accumulators): the bf16 K/V rows
 // convert to fp16 exactly inside fp16's normal range (saturated at +-65504 beyond
 // it), queries and probabilities round to fp16 (2^-11 relative).  One product per
@@ -27,13 +28,16 @@ namespace df2 {
 namespace {
 
 constexpr int kHd = 128;
-constexpr int kQ = 32;          // queries per KV head group (4 heads x 8 positions)
 constexpr int kKeys = kAttnChunk;
 constexpr int kPartStride = kHd + 2;
 constexpr int kLd = kHd + 8;    // bf16 row pitch (272 B): conflict-free fragment loads
 constexpr int kPLd = kKeys + 8;
 
+// B block positions: kQ = 4 B queries per KV head group (4 heads x B positions),
+// query qi = hr * B + i is head kvh * 4 + hr at block position i.
+template <int B>
 struct CtxSmem {
+  static constexpr int kQ = 4 * B;
   __half q[kQ][kLd];              // scaled queries
   __half k[kKeys][kLd];
   __half v[kKeys][kLd];
@@ -42,10 +46,12 @@ struct CtxSmem {
   float alpha[kQ];                // rescale of the running output, per query
 };
 
+template <int B>
 struct BlkSmem {
+  static constexpr int kQ = 4 * B;
   float q[kQ][kHd];
-  float kv[8][kHd + 1];
-  float p[kQ][8];
+  float kv[B][kHd + 1];
+  float p[kQ][B];
 };
 
 DF2_DEV uint32_t ld32(const __half* p) { return *reinterpret_cast<const uint32_t*>(p); }
@@ -97,9 +103,11 @@ DF2_DEV KvRegs load_kv(const AttnArgs& a, int r, int kvh, int k_begin, int nk) {
 // grows.  The next chunk's K/V loads are issued before the current chunk is
 // computed.  The first chunk's K/V are loaded before the wait on the previous
 // kernel when none of its rows is appended by it.  Writes the part's (m, l, O).
+template <int B>
 DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, int lo0, int c0, int c1, int L,
                       int nn, float* out) {
-  CtxSmem& sm = *reinterpret_cast<CtxSmem*>(smem_raw);
+  constexpr int kQ = 4 * B, kMT = kQ / 16, kQW = kQ / 8;  // queries, query tiles, queries per warp
+  CtxSmem<B>& sm = *reinterpret_cast<CtxSmem<B>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int rep = a.n_q_heads / a.n_kv_heads;
@@ -112,14 +120,14 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   pdl_wait();
   pdl_trigger();
   if (!early) kv = load_kv(a, r, kvh, kbeg(c0), nkeys(c0));
-  // queries -> fp16 (qi = hr * 8 + i: head kvh*rep + hr, block row r*8 + i); loads first
+  // queries -> fp16 (qi = hr * B + i: head kvh*rep + hr, block row r*B + i); loads first
   float qv[kQ * kHd / 256];
 #pragma unroll
   for (int j = 0; j < kQ * kHd / 256; ++j) {
     const int e = tid + 256 * j;
     const int qi = e / kHd, d = e % kHd;
-    const int hr = qi >> 3, i = qi & 7;
-    qv[j] = a.q[((static_cast<size_t>(r) * 8 + i) * a.n_q_heads + kvh * rep + hr) * kHd + d];
+    const int hr = qi / B, i = qi % B;
+    qv[j] = a.q[((static_cast<size_t>(r) * B + i) * a.n_q_heads + kvh * rep + hr) * kHd + d];
   }
 #pragma unroll
   for (int j = 0; j < kQ * kHd / 256; ++j) {
@@ -127,13 +135,13 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
     const int qi = e / kHd, d = e % kHd;
     sm.q[qi][d] = __float2half_rn(qv[j] * qscale);
   }
-  float m_run[4], l_run[4];  // queries 4 wid .. 4 wid + 3 (the same in every lane of the warp)
+  float m_run[kQW], l_run[kQW];  // queries kQW wid .. kQW wid + kQW - 1 (the same in every lane)
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < kQW; ++i) {
     m_run[i] = -INFINITY;
     l_run[i] = 0.f;
   }
-  float o[2][2][4] = {};  // dim tiles 2 wid + dn, query tiles mt
+  float o[2][kMT][4] = {};  // dim tiles 2 wid + dn, query tiles mt
   for (int c = c0; c < c1; ++c) {
     const int k_begin = kbeg(c), nk = nkeys(c);
 #pragma unroll
@@ -145,16 +153,16 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
     }
     if (c + 1 < c1) kv = load_kv(a, r, kvh, kbeg(c + 1), nkeys(c + 1));  // in flight during this chunk
     __syncthreads();
-    // S = Q K^T: 2 query tiles x 8 key tiles; warp w takes key tile w for both query tiles
+    // S = Q K^T: kMT query tiles x 8 key tiles; warp w takes key tile w for every query tile
     {
       const int nt = wid;
-      float cs[2][4] = {};
+      float cs[kMT][4] = {};
 #pragma unroll
       for (int ks = 0; ks < kHd / 16; ++ks) {
         const uint32_t b0 = ld32(&sm.k[nt * 8 + g][ks * 16 + 2 * q]);
         const uint32_t b1 = ld32(&sm.k[nt * 8 + g][ks * 16 + 8 + 2 * q]);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
           const int r0 = mt * 16 + g;
           mma_f16(cs[mt], ld32(&sm.q[r0][ks * 16 + 2 * q]), ld32(&sm.q[r0 + 8][ks * 16 + 2 * q]),
                   ld32(&sm.q[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.q[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
@@ -162,11 +170,11 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
       }
       const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int qi = mt * 16 + g + 8 * h2;
-          const int pos_i = qi & 7;
+          const int pos_i = qi % B;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int k = nt * 8 + 2 * q + e;
@@ -177,10 +185,11 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
       }
     }
     __syncthreads();
-    // running softmax statistics: warp w handles queries 4w..4w+3, lane keys lane, lane+32
+    // running softmax statistics: warp w handles queries kQW w .. kQW w + kQW - 1, lane keys
+    // lane, lane + 32
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int qi = wid * 4 + i;
+    for (int i = 0; i < kQW; ++i) {
+      const int qi = wid * kQW + i;
       const float v0 = sm.s[qi][lane], v1 = sm.s[qi][lane + 32];
       const float m_new = fmaxf(m_run[i], warp_max(fmaxf(v0, v1)));
       const bool none = m_new == -INFINITY;  // no visible key yet
@@ -194,9 +203,9 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
       if (lane == 0) sm.alpha[qi] = alpha;
     }
     __syncthreads();
-    // O = alpha O + P V: 2 query tiles x 16 dim tiles; warp w takes dim tiles 2w, 2w+1
+    // O = alpha O + P V: kMT query tiles x 16 dim tiles; warp w takes dim tiles 2w, 2w+1
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < kMT; ++mt) {
       const float a0 = sm.alpha[mt * 16 + g], a1 = sm.alpha[mt * 16 + g + 8];
 #pragma unroll
       for (int dn = 0; dn < 2; ++dn) {
@@ -214,7 +223,7 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
         uint32_t b0, b1;
         ldmatrix_x2_trans(b0, b1, &sm.v[ks * 16 + (lane & 15)][nt * 8]);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
           const int r0 = mt * 16 + g;
           mma_f16(o[dn][mt], ld32(&sm.p[r0][ks * 16 + 2 * q]), ld32(&sm.p[r0 + 8][ks * 16 + 2 * q]),
                   ld32(&sm.p[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.p[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
@@ -225,16 +234,16 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   }
   if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      out[(wid * 4 + i) * kPartStride + 0] = m_run[i];
-      out[(wid * 4 + i) * kPartStride + 1] = l_run[i];
+    for (int i = 0; i < kQW; ++i) {
+      out[(wid * kQW + i) * kPartStride + 0] = m_run[i];
+      out[(wid * kQW + i) * kPartStride + 1] = l_run[i];
     }
   }
 #pragma unroll
   for (int dn = 0; dn < 2; ++dn) {
     const int nt = wid * 2 + dn;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < kMT; ++mt) {
       const int q0 = mt * 16 + g, d0 = nt * 8 + 2 * q;
       out[q0 * kPartStride + 2 + d0] = o[dn][mt][0];
       out[q0 * kPartStride + 2 + d0 + 1] = o[dn][mt][1];
@@ -244,23 +253,28 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   }
 }
 
-// ------------------------------------------------------------------ block chunk (8 fp32 keys, FFMA)
+// ------------------------------------------------------------------ block chunk (B fp32 keys, FFMA)
+// Keys at block positions >= the request's width are masked (p = 0).
+template <int B>
 DF2_DEV void blk_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, float* out) {
-  BlkSmem& sm = *reinterpret_cast<BlkSmem*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  constexpr int kQ = 4 * B;
+  BlkSmem<B>& sm = *reinterpret_cast<BlkSmem<B>*>(smem_raw);
+  const int tid = threadIdx.x;
   const int nkv = a.n_kv_heads, rep = a.n_q_heads / nkv;
+  const int w = a.width != nullptr ? min(max(a.width[r], 2), B) : B;
   const float qscale = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;
   for (int e = tid; e < kQ * kHd; e += 256) {
     const int qi = e / kHd, d = e % kHd;
-    sm.q[qi][d] = a.q[((static_cast<size_t>(r) * 8 + (qi & 7)) * a.n_q_heads + kvh * rep + (qi >> 3)) * kHd + d] * qscale;
+    sm.q[qi][d] = a.q[((static_cast<size_t>(r) * B + (qi % B)) * a.n_q_heads + kvh * rep + (qi / B)) * kHd + d] * qscale;
   }
-  for (int e = tid; e < 8 * kHd; e += 256) {
+  for (int e = tid; e < B * kHd; e += 256) {
     const int k = e / kHd, d = e % kHd;
-    sm.kv[k][d] = a.kb[((static_cast<size_t>(r) * 8 + k) * nkv + kvh) * kHd + d];
+    sm.kv[k][d] = a.kb[((static_cast<size_t>(r) * B + k) * nkv + kvh) * kHd + d];
   }
   __syncthreads();
-  {  // 32 queries x 8 keys = 256 dot products, one per thread
-    const int qi = tid >> 3, k = tid & 7;
+  // kQ queries x B keys: B * B / 64 dot products per thread (1 at B = 8)
+  for (int e = tid; e < kQ * B; e += 256) {
+    const int qi = e / B, k = e % B;
     float s = 0.f;
     for (int d = 0; d < kHd; ++d) s = fmaf(sm.q[qi][d], sm.kv[k][d], s);
     sm.p[qi][k] = s;
@@ -268,40 +282,41 @@ DF2_DEV void blk_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kv
   __syncthreads();
   if (tid < kQ) {
     float m = -INFINITY;
-    for (int k = 0; k < 8; ++k) m = fmaxf(m, sm.p[tid][k]);
+    for (int k = 0; k < w; ++k) m = fmaxf(m, sm.p[tid][k]);
     float l = 0.f;
-    for (int k = 0; k < 8; ++k) {
-      const float p = exp2f(sm.p[tid][k] - m);
+    for (int k = 0; k < B; ++k) {
+      const float p = k < w ? exp2f(sm.p[tid][k] - m) : 0.f;
       sm.p[tid][k] = p;
       l += p;
     }
     out[tid * kPartStride + 0] = m;
     out[tid * kPartStride + 1] = l;
   }
-  for (int e = tid; e < 8 * kHd; e += 256) {
+  for (int e = tid; e < B * kHd; e += 256) {
     const int k = e / kHd, d = e % kHd;
-    sm.kv[k][d] = a.vb[((static_cast<size_t>(r) * 8 + k) * nkv + kvh) * kHd + d];
+    sm.kv[k][d] = a.vb[((static_cast<size_t>(r) * B + k) * nkv + kvh) * kHd + d];
   }
   __syncthreads();
   for (int e = tid; e < kQ * kHd; e += 256) {
     const int qi = e / kHd, d = e % kHd;
     float o = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o = fmaf(sm.p[qi][k], sm.kv[k][d], o);
+    for (int k = 0; k < B; ++k) o = fmaf(sm.p[qi][k], sm.kv[k][d], o);
     out[qi * kPartStride + 2 + d] = o;
   }
-  (void)lane;
-  (void)wid;
 }
 
 // grid (R * nkv, n_chunks): part p < n_chunks - 1 takes context chunks
-// p cpc .. p cpc + cpc - 1 (those that exist); the last part the 8 block keys.
-__global__ void __launch_bounds__(256, 3) attn_chunk_kernel(const AttnArgs a) {
+// p cpc .. p cpc + cpc - 1 (those that exist); the last part the B block keys.
+// Three CTAs per SM at B = 8, two at B = 16 (the context chunk's shared memory).
+template <int B>
+__global__ void __launch_bounds__(256, B == 8 ? 3 : 2) attn_chunk_kernel(const AttnArgs a) {
+  constexpr int kQ = 4 * B;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int nkv = a.n_kv_heads;
   const int r = blockIdx.x / nkv, kvh = blockIdx.x % nkv;
   const int part = blockIdx.y;
-  const int nn = min(max(a.n_new[r], 0), 8);
+  const int nn = min(max(a.n_new[r], 0), B);
   const int L = min(max(a.ctx_len[r], 0), a.kv_capacity - nn) + nn;  // same clamping as the cache append
   const int lo0 = max(0, L - (a.window - 1));
   const int n_ctx_chunks = (L - lo0 + kKeys - 1) / kKeys;
@@ -309,9 +324,9 @@ __global__ void __launch_bounds__(256, 3) attn_chunk_kernel(const AttnArgs a) {
   float* out = a.part + ((static_cast<size_t>(r) * nkv + kvh) * a.n_chunks + part) * kQ * kPartStride;
   if (part == a.n_chunks - 1) {
     pdl_begin();
-    blk_chunk(a, smem_raw, r, kvh, out);
+    blk_chunk<B>(a, smem_raw, r, kvh, out);
   } else if (c0 < c1) {
-    ctx_part(a, smem_raw, r, kvh, lo0, c0, c1, L, nn, out);
+    ctx_part<B>(a, smem_raw, r, kvh, lo0, c0, c1, L, nn, out);
   } else {
     pdl_begin();
     if (threadIdx.x < kQ) {  // no keys in this part
@@ -325,19 +340,20 @@ __global__ void __launch_bounds__(256, 3) attn_chunk_kernel(const AttnArgs a) {
 // merges the parts' partials in part order; lane holds dimensions
 // (128 / DW) quarter + lane + 32 j.  DW = 4 spreads a request over more warps when
 // there are few requests.
-template <int DW>
+template <int B, int DW>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  constexpr int kQ = 4 * B;
   constexpr int kJ = 4 / DW;  // dimensions per lane
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x;
-  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // (head * 8 + position) * DW + quarter
-  if (item >= a.n_q_heads * 8 * DW) return;
-  const int quarter = item % DW, h = item / (8 * DW), i = (item / DW) & 7;
+  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);  // (head * B + position) * DW + quarter
+  if (item >= a.n_q_heads * B * DW) return;
+  const int quarter = item % DW, h = item / (B * DW), i = (item / DW) % B;
   const int nkv = a.n_kv_heads;
   const int rep = a.n_q_heads / nkv;
   const int kvh = h / rep, hr = h % rep;
-  const int qi = hr * 8 + i;
+  const int qi = hr * B + i;
   const int d0 = quarter * (kHd / DW) + lane;
   const float* base = a.part + (static_cast<size_t>(r) * nkv + kvh) * a.n_chunks * kQ * kPartStride;
   // part statistics: lane c holds parts c and c + 32 (n_chunks <= 64)
@@ -359,11 +375,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   float o[kJ];
 #pragma unroll
   for (int j = 0; j < kJ; ++j) o[j] = 0.f;
-  constexpr int kB = 32 / kJ;  // parts whose loads are in flight together
-  for (int c0 = 0; c0 < a.n_chunks; c0 += kB) {  // added in part order
-    float fc[kB], t[kB][kJ];
+  constexpr int kP = 32 / kJ;  // parts whose loads are in flight together
+  for (int c0 = 0; c0 < a.n_chunks; c0 += kP) {  // added in part order
+    float fc[kP], t[kP][kJ];
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
+    for (int u = 0; u < kP; ++u) {
       const int c = c0 + u;
       fc[u] = c < a.n_chunks ? __shfl_sync(0xffffffffu, f[(c >> 5) & 1], c & 31) : 0.f;
       const float* pc = base + (static_cast<size_t>(c) * kQ + qi) * kPartStride + 2 + d0;
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
       for (int j = 0; j < kJ; ++j) t[u][j] = fc[u] != 0.f ? pc[32 * j] : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < kB; ++u)
+    for (int u = 0; u < kP; ++u)
 #pragma unroll
       for (int j = 0; j < kJ; ++j)
         if (fc[u] != 0.f) o[j] += fc[u] * t[u][j];
@@ -379,7 +395,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   const int ld = a.n_q_heads * kHd;
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
-    const size_t idx = act_offset(r * 8 + i, h * kHd + d0 + 32 * j, ld, a.tiled_o);
+    const size_t idx = act_offset(r * B + i, h * kHd + d0 + 32 * j, ld, a.tiled_o);
     const float v = o[j] / den;
     if (a.fmt == 0) {
       __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(a.act_o);
@@ -395,20 +411,27 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
   }
 }
 
+template <int B>
+cudaError_t launch_attention_b(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  static std::atomic<unsigned long long> attr_done{0};
+  const size_t smem = sizeof(CtxSmem<B>) > sizeof(BlkSmem<B>) ? sizeof(CtxSmem<B>) : sizeof(BlkSmem<B>);
+  {
+    const cudaError_t e = set_smem_once(attn_chunk_kernel<B>, static_cast<int>(smem), attr_done);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch_ex(attn_chunk_kernel<B>, dim3(n_req * a.n_kv_heads, a.n_chunks), dim3(256), smem, st, pdl, a);
+  if (e != cudaSuccess) return e;
+  if (n_req * B < 32)  // few block rows: four warps per (head, position), 32 dimensions each
+    return launch_ex(attn_combine_kernel<B, 4>, dim3(n_req, (a.n_q_heads * B * 4 + 7) / 8), dim3(256), 0, st, pdl, a);
+  return launch_ex(attn_combine_kernel<B, 1>, dim3(n_req, (a.n_q_heads * B + 7) / 8), dim3(256), 0, st, pdl, a);
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  static std::atomic<unsigned long long> attr_done{0};
-  const size_t smem = sizeof(CtxSmem) > sizeof(BlkSmem) ? sizeof(CtxSmem) : sizeof(BlkSmem);
-  {
-    const cudaError_t e = set_smem_once(attn_chunk_kernel, static_cast<int>(smem), attr_done);
-    if (e != cudaSuccess) return e;
-  }
-  cudaError_t e = launch_ex(attn_chunk_kernel, dim3(n_req * a.n_kv_heads, a.n_chunks), dim3(256), smem, st, pdl, a);
-  if (e != cudaSuccess) return e;
-  if (n_req < 4)  // few requests: four warps per (head, position), 32 dimensions each
-    return launch_ex(attn_combine_kernel<4>, dim3(n_req, (a.n_q_heads * 8 * 4 + 7) / 8), dim3(256), 0, st, pdl, a);
-  return launch_ex(attn_combine_kernel<1>, dim3(n_req, (a.n_q_heads * 8 + 7) / 8), dim3(256), 0, st, pdl, a);
+  if (a.B == 8) return launch_attention_b<8>(a, n_req, pdl, st);
+  if (a.B == 16) return launch_attention_b<16>(a, n_req, pdl, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace df2

@@ -6,7 +6,12 @@
 // split order.
 //
 // RMSNorm is deferred: producers write x * w and per-chunk sums of squares, and
-// the consumer applies 1/rms (the scale commutes with the projections).  Row
+// the consumer applies 1/rms (the scale commutes with the projections).
+//
+// A CTA takes one tile of 8 rows (warp i = row i of the tile).  Rows are request-
+// major, B block positions per request (8 or 16): row n is position n % B of
+// request n / B, so a block of 16 spans two tiles and the convolutions read the
+// row before a tile's first from global memory when it belongs to the same block.  Row
 // statistics cross CTAs only through those partial sums, read in a fixed order
 // (bit-reproducible).
 #include "common.cuh"
@@ -17,8 +22,8 @@ namespace df2 {
 
 namespace {
 
-constexpr int kB = 8;       // block positions
-constexpr int kCw = 32;     // channels per CTA of the channel kernels: warp i = block row i, lane = channel
+constexpr int kB = 8;       // rows per tile (one CTA of the channel kernels)
+constexpr int kCw = 32;     // channels per CTA of the channel kernels: warp i = tile row i, lane = channel
 constexpr int kThreads = kB * kCw;
 
 DF2_DEV void put_act(void* act, size_t lo, int fmt, size_t idx, float v) {
@@ -82,14 +87,14 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
   // a new step: the previous step's select has read the error word by now (it ran
   // before the previous verify, whose completion the wait above implies)
   if (a.pipe_err != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.pipe_err = 0;
-  const int r = blockIdx.x;
   const int i = threadIdx.x >> 5;
-  const int row = r * kB + i;
+  const int row = blockIdx.x * kB + i;
+  const int r = row / a.B, pos = row % a.B;
   const int ny = a.H / kCw;
   if (static_cast<int>(blockIdx.y) < ny) {
     const int c = blockIdx.y * kCw + (threadIdx.x & 31);
     const int anchor = min(max(a.anchor_ids[r], 0), a.V - 1);  // ids are clamped into the table
-    const int id = (i == 0) ? anchor : a.mask_id;
+    const int id = (pos == 0) ? anchor : a.mask_id;
     const float xv = bf16_to_f32(a.embed[static_cast<size_t>(id) * a.H + c]);
     const size_t idx = static_cast<size_t>(row) * a.H + c;
     a.x[idx] = xv;
@@ -97,10 +102,10 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
     emit_ss(xv, row, a.ss_x, a.nch);
   } else {
     const int c = (blockIdx.y - ny) * kCw + (threadIdx.x & 31);
-    const int nn = min(max(a.n_new[r], 0), kB);  // rows >= n_new are zero
+    const int nn = min(max(a.n_new[r], 0), a.B);  // rows >= n_new are zero
     const size_t idx = static_cast<size_t>(row) * (a.n_taps * a.H) + c;
     put_act(a.act_taps, a.act_taps_lo, a.fmt, act_offset(row, c, a.n_taps * a.H, a.tiled_taps),
-            (i < nn) ? a.taps[idx] : 0.f);
+            (pos < nn) ? a.taps[idx] : 0.f);
   }
 }
 
@@ -167,8 +172,14 @@ DF2_DEV void conv_in_body(const ConvInArgs& a) {
   const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 2 + gl);
   const float ai = x0 * rr * w;
   ash[i][lane] = ai;
+  // a tile that starts inside a block (B = 16): its first row's predecessor, from global
+  float prev0 = 0.f;
+  if (i == 0 && row % a.B != 0) {
+    const float rp = warp_inv_rms(a.ss, row - 1, a.nch, a.H, a.eps);
+    prev0 = a.x[idx - a.H] * rp * w;
+  }
   __syncthreads();
-  const float prev = i > 0 ? ash[i - 1][lane] : 0.f;
+  const float prev = i > 0 ? ash[i - 1][lane] : prev0;
   put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), (b0 + d0) * ai + (b1 + d1) * prev);
 }
 
@@ -210,8 +221,11 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
   const float w = bf16_to_f32(a.norm_w[c]);
   const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, np);
   ysh[i][lane] = y;
+  // a tile that starts inside a block (B = 16): its first row's predecessor, from global
+  float yp0 = 0.f;
+  if (i == 0 && row % a.B != 0) yp0 = plane_sum(a.part + idx - a.H, static_cast<size_t>(a.n_rows) * a.H, np);
   __syncthreads();
-  const float yprev = i > 0 ? ysh[i - 1][lane] : 0.f;
+  const float yprev = i > 0 ? ysh[i - 1][lane] : yp0;
   const float xv = x0 + (b2 + d2) * y + (b3 + d3) * yprev;
   a.x[idx] = xv;
   put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), xv * w);
@@ -254,36 +268,36 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
 
 // ------------------------------------------------------------------ q/k norm, RoPE, cache append
 // One warp per (row, head); lane holds dims lane + 32 c (c = 0..3), so the NEOX
-// pair (d, d + 64) is (c, c + 2) of the same lane.  Items: 8 query rows x nq heads,
-// then 16 key rows (8 block + 8 context) x nkv, then 16 value rows x nkv.
+// pair (d, d + 64) is (c, c + 2) of the same lane.  Items per request: B query rows
+// x nq heads, then 2 B key rows (B block + B context) x nkv, then 2 B value rows x nkv.
 __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) {
   pdl_begin();
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.y * 8 + (threadIdx.x >> 5);
-  const int nq = a.n_q_heads, nkv = a.n_kv_heads;
-  const int n_items = kB * nq + 2 * 2 * kB * nkv;
+  const int nq = a.n_q_heads, nkv = a.n_kv_heads, B = a.B;
+  const int n_items = B * nq + 2 * 2 * B * nkv;
   if (item >= n_items) return;
   // lengths are clamped so a bad length can never address outside the cache
-  const int nn = min(max(a.n_new[r], 0), kB);
+  const int nn = min(max(a.n_new[r], 0), B);
   const int ctx = min(max(a.ctx_len[r], 0), a.kv_capacity - nn);
   const int L = ctx + nn;
   int kind, j, hh;
-  if (item < kB * nq) {
+  if (item < B * nq) {
     kind = 0;
     j = item / nq;
     hh = item % nq;
   } else {
-    const int e = item - kB * nq;
-    kind = 1 + e / (2 * kB * nkv);
-    const int e2 = e % (2 * kB * nkv);
+    const int e = item - B * nq;
+    kind = 1 + e / (2 * B * nkv);
+    const int e2 = e % (2 * B * nkv);
     j = e2 / nkv;
     hh = e2 % nkv;
   }
-  const bool ctx_row = j >= kB;
-  const int jj = ctx_row ? j - kB : j;
+  const bool ctx_row = j >= B;
+  const int jj = ctx_row ? j - B : j;
   if (ctx_row && jj >= nn) return;
-  const int row0 = r * kB;
+  const int row0 = r * B;
   const float* src;
   size_t plane;
   const GemvPlanes& pm = kind == 0 ? a.pq : (kind == 1 ? a.pk : a.pv);
@@ -362,37 +376,64 @@ __global__ void __launch_bounds__(32) advance_kernel(const AdvanceArgs a, int n_
   pdl_begin();
   const int r = blockIdx.x * 32 + threadIdx.x;
   if (r >= n_req) return;
-  const int ne = min(max(a.n_emitted[r], 0), kB);
-  a.ctx_len[r] += min(max(a.n_new[r], 0), kB);
-  if (ne > 0) a.anchor_ids[r] = a.emitted[r * kB + ne - 1];
+  const int ne = min(max(a.n_emitted[r], 0), a.B);
+  a.ctx_len[r] += min(max(a.n_new[r], 0), a.B);
+  if (ne > 0) a.anchor_ids[r] = a.emitted[r * a.B + ne - 1];
   a.n_new[r] = ne;
   a.offset[r] += 1;
 }
 
+// ------------------------------------------------------------------ block width by context length
+// The long-context narrowing of "qwen35: DSpark speculative decoding ... #625" (its
+// long-context commits): verify cost grows with the block's rows times the context, so
+// a request whose context passes a threshold drafts and verifies a narrower block.
+// The rule reads the context length only.  One thread per request; the lengths may
+// come from the previous kernel (the loop's state update), so it waits for it.
+__global__ void __launch_bounds__(32) block_width_kernel(const BlockWidthArgs a, int n_req) {
+  pdl_begin();
+  const int r = blockIdx.x * 32 + threadIdx.x;
+  if (r >= n_req) return;
+  const long long L = static_cast<long long>(max(a.ctx_len[r], 0)) + max(a.n_new[r], 0);
+  a.width[r] = (a.threshold > 0 && L > a.threshold) ? a.narrow : a.B;
+}
+
 }  // namespace
 
+cudaError_t launch_block_width(const BlockWidthArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  if ((a.B != 8 && a.B != 16) || a.narrow < 2 || a.narrow > a.B) return cudaErrorInvalidValue;
+  return launch_ex(block_width_kernel, dim3((n_req + 31) / 32), dim3(32), 0, st, pdl, a, n_req);
+}
+
 cudaError_t launch_advance(const AdvanceArgs& a, int n_req, bool pdl, cudaStream_t st) {
+  if (a.B != 8 && a.B != 16) return cudaErrorInvalidValue;
   return launch_ex(advance_kernel, dim3((n_req + 31) / 32), dim3(32), 0, st, pdl, a, n_req);
 }
 
+// The channel kernels' grids: one CTA per (8-row tile, 32-channel chunk); n_rows =
+// B n_req is a multiple of 8.
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(start_kernel, dim3(n_req, (a.H + a.n_taps * a.H) / kCw), dim3(kThreads), 0, st, pdl, a);
+  if ((a.B != 8 && a.B != 16)) return cudaErrorInvalidValue;
+  return launch_ex(start_kernel, dim3(n_req * a.B / kB, (a.H + a.n_taps * a.H) / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_fc_finish_conv_in(const FcFinishArgs& f, const ConvInArgs& c, int n_req, bool pdl, cudaStream_t st) {
-  if (f.H != c.H) return cudaErrorInvalidValue;
-  return launch_ex(fc_finish_conv_in_kernel, dim3(n_req, f.H / kCw, 2), dim3(kThreads), 0, st, pdl, f, c);
+  if (f.H != c.H || f.n_rows != c.n_rows || f.n_rows % kB) return cudaErrorInvalidValue;
+  return launch_ex(fc_finish_conv_in_kernel, dim3(f.n_rows / kB, f.H / kCw, 2), dim3(kThreads), 0, st, pdl, f, c);
 }
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(conv_in_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
+  if (a.n_rows % kB) return cudaErrorInvalidValue;
+  return launch_ex(conv_in_kernel, dim3(a.n_rows / kB, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(conv_out_kernel, dim3(n_req, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
+  if (a.n_rows % kB) return cudaErrorInvalidValue;
+  return launch_ex(conv_out_kernel, dim3(a.n_rows / kB, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(swiglu_kernel, dim3(n_req, a.F / kCw), dim3(kThreads), 0, st, pdl, a);
+  if (a.n_rows % kB) return cudaErrorInvalidValue;
+  return launch_ex(swiglu_kernel, dim3(a.n_rows / kB, a.F / kCw), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  const int n_items = kB * a.n_q_heads + 4 * kB * a.n_kv_heads;
+  if ((a.B != 8 && a.B != 16) || a.n_rows != a.B * n_req) return cudaErrorInvalidValue;
+  const int n_items = a.B * a.n_q_heads + 4 * a.B * a.n_kv_heads;
   return launch_ex(qkv_finish_kernel, dim3(n_req, (n_items + 7) / 8), dim3(256), 0, st, pdl, a);
 }
 

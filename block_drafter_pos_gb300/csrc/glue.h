@@ -26,6 +26,7 @@ struct StartArgs {
   void* act_taps;          // [N][n_taps*H]
   size_t act_taps_lo;
   int H, n_taps, mask_id, nch, fmt, V;
+  int B;                    // block positions per request (8 or 16); rows are request-major
   int tiled_a, tiled_taps;  // > 0: tensor-core operand layout with that many rows per slice (act_offset)
   int* pipe_err;            // the step's weight-pipeline error word, cleared here (may be NULL)
 };
@@ -54,6 +55,7 @@ struct ConvInArgs {
   float eps;
   GemvPlanes pl;           // planes of dproj
   int tiled;               // > 0: act in the tensor-core operand layout (act_offset)
+  int B;                   // block positions per request (the convolution stops at a block's start)
 };
 
 // Dynamic convolution after a sublayer, residual add, next norm's input.
@@ -71,6 +73,7 @@ struct ConvOutArgs {
   int H, nch, fmt, n_rows;
   GemvPlanes pl;           // planes of part
   int tiled, tiled2;       // > 0: act / act2 in the tensor-core operand layout (act_offset)
+  int B;                   // block positions per request (the convolution stops at a block's start)
 };
 
 // SwiGLU of the gate and up projections: act = silu(gate) * up.
@@ -102,6 +105,7 @@ struct QkvFinishArgs {
   int n_q_heads, n_kv_heads, n_rows, kv_capacity, H, nch;
   float eps;
   GemvPlanes pq, pk, pv;   // planes of the three projections
+  int B;                   // block positions per request; new context rows per request <= B
 };
 
 cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t st);
@@ -127,6 +131,9 @@ struct AttnArgs {
   int n_chunks;            // parts: ceil(context chunks / cpc) + 1 (the block keys)
   int cpc;                 // context chunks of 64 keys per part
   int tiled_o;             // > 0: act_o in the tensor-core operand layout (act_offset)
+  int B;                   // block positions per request (8 or 16): 4 B queries per KV head group
+  const int32_t* width;    // [R] block width of each request (2..B; keys at positions >= width are
+                           // masked, so its first width rows are a block-width forward), or null: B
 };
 constexpr int kAttnChunk = 64;
 cudaError_t launch_attention(const AttnArgs& a, int n_req, bool pdl, cudaStream_t st);
@@ -142,6 +149,7 @@ struct LmHeadArgs {
   int V, H, n_rows, nch, n_cta;
   float eps;
   int* err;                // set nonzero if a pipeline wait gave up, or null
+  int B;                   // block positions per request: row n is position n % B of request n / B
 };
 // Bulk-copy map of a bf16 matrix [rows][inner] in boxes of box_rows x 64 elements
 // (128-byte rows, 128-byte swizzle); rows past the end read as zero.
@@ -164,6 +172,7 @@ struct LogitsTopkArgs {
   int V, H, n_rows, nch, n_chunks;
   float eps;
   GemvPlanes pl;           // planes of part
+  int B;                   // block positions per request
 };
 cudaError_t launch_logits_topk(const LogitsTopkArgs& a, int n_req, bool pdl, cudaStream_t st);
 
@@ -178,6 +187,7 @@ struct TopkMergeArgs {
   float eps;
   GemvPlanes psel;         // planes of sel
   const int* err;          // or null: when nonzero, every row gets the sentinel (ids -1, logits NaN)
+  int B;                   // block positions per request
 };
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st);
 
@@ -213,8 +223,11 @@ struct SelectArgs {
   int32_t* t_depth;            // [R][tree_budget]: block position 1..7
   float* t_score;              // [R][tree_budget]: cumulative log-probability
   int32_t* t_n;                // [R]: nodes built
+  int B;                       // block positions per request: B - 1 proposal positions
+  const int32_t* width;        // [R] block width (2..B): positions 1..width-1 are walked; null: B
 };
 constexpr int kTreeMaxNodes = 32;
+constexpr int kMaxBlock = 16;  // block positions per request: 8 or 16
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 
@@ -244,6 +257,8 @@ struct VerifyArgs {
   float* probs;                // [R][8][2] or null: p_j at the proposal / bonus, residual mass (debug output)
   unsigned int* counters;      // [R] finished chunk statistics of the launch; zero before and after it
   int V, n_chunks;
+  int B;                       // block positions per request: B target rows, B - 1 proposals
+  const int32_t* width;        // [R] block width (2..B): rows 0..width-1 are verified; null: B
 };
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st);
 
@@ -260,6 +275,7 @@ struct TreeVerifyArgs {
   int32_t* n_emitted;
   int32_t* status;
   int V, n_chunks, budget;
+  int B;                       // block positions per request (emitted rows)
 };
 cudaError_t launch_tree_verify(const TreeVerifyArgs& a, int n_req, bool pdl, cudaStream_t st);
 
@@ -271,7 +287,18 @@ struct AdvanceArgs {
   int32_t* ctx_len;         // [R] in/out
   int32_t* n_new;           // [R] in/out
   uint64_t* offset;         // [R] in/out
+  int B;                    // block positions per request
 };
 cudaError_t launch_advance(const AdvanceArgs& a, int n_req, bool pdl, cudaStream_t st);
+
+// Block width of each request by context length: width[r] = narrow if threshold > 0
+// and ctx_len[r] + n_new[r] > threshold, else B.
+struct BlockWidthArgs {
+  const int32_t* ctx_len;
+  const int32_t* n_new;
+  int32_t* width;
+  int B, threshold, narrow;
+};
+cudaError_t launch_block_width(const BlockWidthArgs& a, int n_req, bool pdl, cudaStream_t st);
 
 }  // namespace df2

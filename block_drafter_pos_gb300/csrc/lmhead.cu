@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __gr
     consumer_sync();
     const int v0 = blk * kBlockRows;
     for (int n = wid; n < n_rows; n += kConsumers) {
-      const int pos = n & 7;
+      const int pos = n % a.B;
       if (pos == 0) continue;  // the anchor position is not sampled
       const float rs = rscale[n];
       unsigned long long* rn = run[n];
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) lmhead_kernel(const __gr
         const int v = v0 + idx;
         const float val = logit[n][idx] * rs;
         if (a.logits_out != nullptr && v < a.V)
-          a.logits_out[(static_cast<size_t>(n >> 3) * 7 + pos - 1) * a.V + v] = val;
+          a.logits_out[(static_cast<size_t>(n / a.B) * (a.B - 1) + pos - 1) * a.V + v] = val;
         const unsigned long long key = v < a.V ? topk_key(val, static_cast<uint32_t>(v)) : 0ull;
         mine[j] = key > thr ? key : 0ull;
         any |= mine[j] != 0ull;
@@ -219,12 +219,12 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   __shared__ float rs;
   pdl_begin();
   const int n = blockIdx.x;
-  const int pos = n & 7, rq = n >> 3;
+  const int pos = n % a.B, rq = n / a.B;
   if (pos == 0) return;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (a.err != nullptr && __ldcg(a.err) != 0) {  // the per-CTA lists are incomplete: write the sentinel
     if (threadIdx.x < kTopK) {
-      const size_t o = (static_cast<size_t>(rq) * 7 + pos - 1) * kTopK + threadIdx.x;
+      const size_t o = (static_cast<size_t>(rq) * (a.B - 1) + pos - 1) * kTopK + threadIdx.x;
       a.cand_ids[o] = -1;
       a.cand_logits[o] = __int_as_float(0x7FC00000);
     }
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
       const unsigned long long win = warp_max_u64(best);
       last = win;
       if (lane == 0) {
-        const size_t o = (static_cast<size_t>(rq) * 7 + pos - 1) * kTopK + round;
+        const size_t o = (static_cast<size_t>(rq) * (a.B - 1) + pos - 1) * kTopK + round;
         a.cand_ids[o] = static_cast<int32_t>(key_index(win));
         a.cand_logits[o] = key_value(win);
       }
@@ -291,11 +291,11 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
 #pragma unroll
       for (int k = 0; k < 16; ++k) v += t[k];
     }
-    a.gate[(static_cast<size_t>(rq) * 7 + pos - 1) * a.rank + j] = v * rs;
+    a.gate[(static_cast<size_t>(rq) * (a.B - 1) + pos - 1) * a.rank + j] = v * rs;
   }
 }
 
-// grid (n_chunks, 7 R), 256 threads, 16 consecutive vocabulary entries per thread.
+// grid (n_chunks, (B - 1) R), 256 threads, 16 consecutive vocabulary entries per thread.
 // The chunk's 16 largest keys are found without ranking all 4096: the 16th largest
 // of a warp's 32 per-thread maxima (a bitonic sort across the warp) is a lower
 // bound T of the chunk's 16th largest key (16 distinct entries reach it), so only
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArg
     np_sh[threadIdx.x] = gemv_plane_count(a.pl, blockIdx.x * kLogitChunk + threadIdx.x * 128);
   pdl_begin();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int rq = blockIdx.y / 7, pos = blockIdx.y % 7 + 1, n = rq * 8 + pos;
+  const int rq = blockIdx.y / (a.B - 1), pos = blockIdx.y % (a.B - 1) + 1, n = rq * a.B + pos;
   if (wid == 0) {
     const float v = a.ss != nullptr ? warp_inv_rms(a.ss, n, a.nch, a.H, a.eps) : 1.f;
     if (lane == 0) {
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArg
       keys[j] = topk_key(acc[j], static_cast<uint32_t>(v0 + j));
     }
     if (a.logits_out != nullptr) {
-      float4* o = reinterpret_cast<float4*>(a.logits_out + (static_cast<size_t>(rq) * 7 + pos - 1) * a.V + v0);
+      float4* o = reinterpret_cast<float4*>(a.logits_out + (static_cast<size_t>(rq) * (a.B - 1) + pos - 1) * a.V + v0);
 #pragma unroll
       for (int j = 0; j < 4; ++j) o[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
     }
@@ -449,6 +449,7 @@ int lmhead_ctas(int num_sms) { return num_sms * kCtasPerSm; }
 cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
   const int nt = a.n_rows / 8;
   if (a.n_rows < 8 || a.n_rows % 8 || a.H % kStageK || a.n_cta < 1) return cudaErrorInvalidValue;
+  if ((a.B != 8 && a.B != 16) || a.n_rows % a.B) return cudaErrorInvalidValue;
   const bool lo = a.x_lo_row >= 0;
   if (nt <= 1) return lo ? launch_nt<1, true>(a, pdl, st) : launch_nt<1, false>(a, pdl, st);
   if (nt <= 2) return lo ? launch_nt<2, true>(a, pdl, st) : launch_nt<2, false>(a, pdl, st);
@@ -458,12 +459,14 @@ cudaError_t launch_lmhead(const LmHeadArgs& a, bool pdl, cudaStream_t st) {
 
 cudaError_t launch_topk_merge(const TopkMergeArgs& a, bool pdl, cudaStream_t st) {
   if (a.n_cta < 1 || a.n_cta * kTopK > 256 * 32) return cudaErrorInvalidValue;
+  if ((a.B != 8 && a.B != 16) || a.n_rows % a.B) return cudaErrorInvalidValue;
   return launch_ex(topk_merge_kernel, dim3(a.n_rows), dim3(256), 0, st, pdl, a);
 }
 
 cudaError_t launch_logits_topk(const LogitsTopkArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if (a.V % 16 || a.n_chunks < 1 || a.n_chunks * kTopK > 8192) return cudaErrorInvalidValue;
-  return launch_ex(logits_topk_kernel, dim3(a.n_chunks, 7 * n_req), dim3(256), 0, st, pdl, a);
+  if (a.B != 8 && a.B != 16) return cudaErrorInvalidValue;
+  return launch_ex(logits_topk_kernel, dim3(a.n_chunks, (a.B - 1) * n_req), dim3(256), 0, st, pdl, a);
 }
 
 }  // namespace df2

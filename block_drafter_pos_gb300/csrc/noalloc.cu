@@ -114,6 +114,7 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   a.V = vocab;
   a.H = hidden_dim;
   a.n_rows = n_rows;
+  a.B = 8;  // rows are (request, block position) of blocks of 8
   a.nch = hidden_dim / 32;
   a.n_cta = slot.n_cta;
   a.eps = 0.f;
@@ -127,6 +128,7 @@ extern "C" dflash2_status dflash2_head_topk_noalloc(const void* lm_head, int32_t
   m.cand_logits = cand_logits;
   m.gate = nullptr;
   m.n_rows = n_rows;
+  m.B = 8;
   m.n_cta = slot.n_cta;
   m.rank = 0;
   m.nch = hidden_dim / 128;

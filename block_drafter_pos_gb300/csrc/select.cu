@@ -8,8 +8,10 @@
 // One CTA per (request, position): it stages the 16 predecessor rows of A (the
 // anchor's row at position 1) and the 16 candidate rows of B in shared memory and
 // scores its 16 x 16 edges, one thread per (predecessor, candidate), into a scratch
-// lattice.  The CTA that completes a request's seven positions (fenced atomic
-// ticket, no waiting) walks the lattice with one warp (lane j = candidate j).  Any
+// lattice.  The CTA that completes a request's B - 1 positions (fenced atomic
+// ticket, no waiting) walks the lattice with one warp (lane j = candidate j): all
+// B - 1 positions, or the first width - 1 for a request narrowed to a block width
+// below B (the positions past it get no proposal).  Any
 // nonfinite candidate logit or score marks the request DFLASH2_E_NONFINITE ("LSE
 // docs/DFLASH2.md": the selector rejects nonfinite scores).
 #include <math.h>
@@ -23,7 +25,7 @@ namespace df2 {
 
 namespace {
 
-constexpr int kP = 7, kK = 16, kRank = 256;
+constexpr int kMaxP = kMaxBlock - 1, kK = 16, kRank = 256;
 
 // Codebook rows staged in shared memory in their stored format: bf16 (256 x 2 B) or
 // Q8 codes (256 B) plus 4 groups of (scale, bias).  Rows 0..15: predecessors (A),
@@ -37,9 +39,9 @@ struct SelSmem {
   uint16_t sb[2 * kK][8];       // Q8: scale[4], bias[4]
   float gate[kRank];
   float cl[kK];
-  int cids[kP][kK];
-  float lat[kP][kK][kK];        // the walker's copy of the lattice
-  uint8_t back[kP][kK];         // Viterbi: best predecessor of each candidate
+  int cids[kMaxP][kK];
+  float lat[kMaxP][kK][kK];     // the walker's copy of the lattice
+  uint8_t back[kMaxP][kK];      // Viterbi: best predecessor of each candidate
   // draft tree: node 0 is the root (the anchor), nodes 1..n the tree's
   float t_score[kTreeMaxNodes + 1];
   int t_cand[kTreeMaxNodes + 1], t_depth[kTreeMaxNodes + 1];
@@ -107,9 +109,9 @@ DF2_DEV float edge_dot(const SelSmem& sm, int fmt, int ra, int rb) {
 // over the root and every node already in, that is not in yet (equal scores: the
 // earlier parent, then the smaller candidate index), until the budget is reached.
 // FP32 throughout; node k of the output is tree node k + 1 (parent -1 = the root).
-__device__ void tree_grow(const SelectArgs& a, SelSmem& sm, int r) {
+__device__ void tree_grow(const SelectArgs& a, SelSmem& sm, int r, int np) {
   const int lane = threadIdx.x & 31;
-  for (int row = lane; row < kP * kK; row += 32) {
+  for (int row = lane; row < np * kK; row += 32) {
     float* v = sm.lat[row / kK][row % kK];
     float m = v[0];
 #pragma unroll
@@ -136,7 +138,7 @@ __device__ void tree_grow(const SelectArgs& a, SelSmem& sm, int r) {
     int bq = 0x7FFFFFFF, bc = 0x7FFFFFFF;
     for (int q = lane; q <= n; q += 32) {
       const int d = sm.t_depth[q];
-      if (d >= kP) continue;
+      if (d >= np) continue;
       const float base = sm.t_score[q];
       const float* row = sm.lat[d][sm.t_cand[q]];
       const uint32_t taken = sm.t_taken[q];
@@ -186,6 +188,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   __shared__ __align__(16) SelSmem sm;
   pdl_begin();
   const int r = blockIdx.x, i = blockIdx.y;
+  const int P = a.B - 1;  // positions of a request's rows of candidates, gate, lattice and path
+  // positions walked: 1..width-1 (the request's block width; every position is scored)
+  const int np = a.width != nullptr ? min(max(a.width[r], 2), a.B) - 1 : P;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (tid == 0) sm.bad = 0;
   // candidates of this position (and of the previous one: the predecessors)
@@ -193,15 +198,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     const int pos = tid < kK ? i : i - 1;
     if (pos >= 0) {
       const int e = pos * kK + (tid % kK);
-      sm.cids[pos][tid % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + e], 0), a.V - 1);
+      sm.cids[pos][tid % kK] = min(max(a.cand_ids[static_cast<size_t>(r) * P * kK + e], 0), a.V - 1);
     }
   }
   if (tid < kK) {
-    const float v = a.cand_logits[(static_cast<size_t>(r) * kP + i) * kK + tid];
+    const float v = a.cand_logits[(static_cast<size_t>(r) * P + i) * kK + tid];
     sm.cl[tid] = v;
     if (!isfinite(v)) atomicOr(&sm.bad, 1);
   }
-  sm.gate[tid] = a.gate[(static_cast<size_t>(r) * kP + i) * kRank + tid];
+  sm.gate[tid] = a.gate[(static_cast<size_t>(r) * P + i) * kRank + tid];
   __syncthreads();
   const int anchor = min(max(a.anchor_ids[r], 0), a.V - 1);
   const int n_pred = i == 0 ? 1 : kK;
@@ -249,16 +254,16 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     const int p = tid / kK, c = tid % kK;
     const float s = edge_dot(sm, a.fmt, i == 0 ? 0 : p, kK + c) + sm.cl[c];
     if (!isfinite(s)) atomicOr(&sm.bad, 1);
-    a.lat[((static_cast<size_t>(r) * kP + i) * kK + p) * kK + c] = s;
+    a.lat[((static_cast<size_t>(r) * P + i) * kK + p) * kK + c] = s;
   }
   __threadfence();  // every writer's lattice scores visible device-wide before the ticket
   __syncthreads();
   // the CTA completing this request's seven positions walks the lattice
   if (tid == 0) {
-    a.bad[r * kP + i] = sm.bad;
+    a.bad[r * P + i] = sm.bad;
     __threadfence();
     const unsigned int done = atomicAdd(&a.counters[r], 1u);
-    sm.last = done == kP - 1;
+    sm.last = done == P - 1;
     if (sm.last) {
       a.counters[r] = 0;  // zero for the next launch
       __threadfence();
@@ -267,14 +272,14 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   __syncthreads();
   if (!sm.last) return;
   int bad_any = 0;
-  for (int e = tid; e < kP * kK * kK; e += kThreads) {
-    const float v = __ldcg(a.lat + static_cast<size_t>(r) * kP * kK * kK + e);
+  for (int e = tid; e < P * kK * kK; e += kThreads) {
+    const float v = __ldcg(a.lat + static_cast<size_t>(r) * P * kK * kK + e);
     (&sm.lat[0][0][0])[e] = v;
-    if (a.scores_out) a.scores_out[static_cast<size_t>(r) * kP * kK * kK + e] = v;
+    if (a.scores_out) a.scores_out[static_cast<size_t>(r) * P * kK * kK + e] = v;
   }
-  if (tid < kP * kK) sm.cids[tid / kK][tid % kK] =
-      min(max(a.cand_ids[static_cast<size_t>(r) * kP * kK + tid], 0), a.V - 1);
-  if (tid < kP) bad_any = __ldcg(a.bad + r * kP + tid);
+  if (tid < P * kK) sm.cids[tid / kK][tid % kK] =
+      min(max(a.cand_ids[static_cast<size_t>(r) * P * kK + tid], 0), a.V - 1);
+  if (tid < np) bad_any = __ldcg(a.bad + r * P + tid);
   bad_any = __syncthreads_or(bad_any);
   const int bad = bad_any;
   auto& lat = sm.lat;
@@ -282,30 +287,33 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   if (wid != 0) return;
   // ---- the walk: one warp, lane j < 16 holds candidate j
   const float T = a.tree_budget > 0 ? 0.f : a.temperature[r];  // the tree is built for greedy verification
-  int32_t* path = a.tree_budget > 0 ? nullptr : a.path + static_cast<size_t>(r) * kP;
-  float* qrow = a.tree_budget > 0 ? nullptr : a.q_rows + static_cast<size_t>(r) * kP * kK;
+  int32_t* path = a.tree_budget > 0 ? nullptr : a.path + static_cast<size_t>(r) * P;
+  float* qrow = a.tree_budget > 0 ? nullptr : a.q_rows + static_cast<size_t>(r) * P * kK;
   // a weight-pipeline wait of this step's draft that gave up leaves its candidates undefined
   const bool pipe_bad = a.pipe_err != nullptr && __ldcg(a.pipe_err) != 0;
   if (!(T >= 0.f) || bad || pipe_bad) {
     if (a.tree_budget > 0) {
       if (lane == 0) a.t_n[r] = 0;
     } else {
-      if (lane < kP) path[lane] = -1;
-      for (int e = lane; e < kP * kK; e += 32) qrow[e] = 0.f;
+      if (lane < P) path[lane] = -1;
+      for (int e = lane; e < P * kK; e += 32) qrow[e] = 0.f;
     }
     if (lane == 0) a.status[r] = pipe_bad ? 3 : (T >= 0.f) ? 2 : 1;
     return;
   }
   const bool live = lane < kK;
   if (a.tree_budget > 0) {
-    tree_grow(a, sm, r);
+    tree_grow(a, sm, r, np);
     return;
   }
+  // positions past the width: no proposal
+  if (lane >= np && lane < P) path[lane] = -1;
+  for (int e = np * kK + lane; e < P * kK; e += 32) qrow[e] = 0.f;
   if (T == 0.f && a.mode == 1) {
     // globally best path: best_1(c) = s_1(c); best_i(c) = max_p best_{i-1}(p) + s_i(p, c)
     // (float32 sums; equal -> the predecessor with the smaller id), then read back
     float best = live ? lat[0][0][lane] : -INFINITY;
-    for (int i = 1; i < kP; ++i) {
+    for (int i = 1; i < np; ++i) {
       float nb = -INFINITY;
       int bp = 0, bid = 0x7FFFFFFF;
       for (int p = 0; p < kK; ++p) {
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     }
     // the end of the path: argmax over candidates, equal -> smaller id
     float bv = best;
-    int bi = lane, bc = live ? cids[kP - 1][lane] : 0x7FFFFFFF;
+    int bi = lane, bc = live ? cids[np - 1][lane] : 0x7FFFFFFF;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     }
     __syncwarp();
     int c = bi;
-    for (int i = kP - 1; i >= 0; --i) {  // read back through the recorded predecessors
+    for (int i = np - 1; i >= 0; --i) {  // read back through the recorded predecessors
       if (live) qrow[i * kK + lane] = lane == c ? 1.f : 0.f;
       if (lane == 0) path[i] = cids[i][c];
       c = i > 0 ? sm.back[i][c] : 0;
@@ -348,7 +356,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   }
   const uint64_t seed = a.seed[r], off = a.offset[r];
   int prev = 0;
-  for (int i = 0; i < kP; ++i) {
+  for (int i = 0; i < np; ++i) {
     const float sj = live ? lat[i][prev][lane] : -INFINITY;
     const int cid = live ? cids[i][lane] : 0x7FFFFFFF;
     int pick;
@@ -395,8 +403,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  if (a.rank != kRank) return cudaErrorInvalidValue;
-  return launch_ex(select_kernel, dim3(n_req, kP), dim3(kThreads), 0, st, pdl, a);
+  if (a.rank != kRank || (a.B != 8 && a.B != 16)) return cudaErrorInvalidValue;
+  return launch_ex(select_kernel, dim3(n_req, a.B - 1), dim3(kThreads), 0, st, pdl, a);
 }
 
 }  // namespace df2

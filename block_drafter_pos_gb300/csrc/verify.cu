@@ -1,11 +1,14 @@
-// Verification of the 7 proposals (step a11): exact match against the target
-// argmax for greedy requests; probability-ratio rejection with residual sampling
-// for T > 0 ("LSE docs/DFLASH2.md", first paragraph: the target verifies all
-// seven proposals with probability-ratio rejection and residual sampling, greedy
-// requests stay deterministic).
+// Verification of the B - 1 proposals of a block of B positions (step a11): exact
+// match against the target argmax for greedy requests; probability-ratio rejection
+// with residual sampling for T > 0 ("LSE docs/DFLASH2.md", first paragraph: the
+// target verifies all seven proposals of a block of 8 with probability-ratio
+// rejection and residual sampling, greedy requests stay deterministic).  A request
+// narrowed to width w < B verifies its first w - 1 proposals with rows 0..w-1
+// (the long-context narrowing of "qwen35: DSpark speculative decoding ... #625").
 //
-// Pass 1 (grid R x 8 rows x vocab chunks): per chunk max, argmax (smallest index on
-// ties), sum of exp((z - m) / T), NaN / +inf flags.  Pass 2 (one CTA per request):
+// Pass 1 (grid R x B rows x vocab chunks): per chunk max, argmax (smallest index on
+// ties), sum of exp((z - m) / T), NaN / +inf flags; rows at or past a request's width
+// are skipped but counted.  Pass 2 (one CTA per request):
 // folds the chunk statistics in a fixed order and runs the sequential accept chain;
 // a residual or bonus draw locates its vocabulary chunk from per-chunk masses and
 // scans that one chunk with a block-wide prefix sum.
@@ -20,7 +23,10 @@ namespace df2 {
 
 namespace {
 
-constexpr int kB = 8, kP = 7, kK = 16;
+constexpr int kK = 16;
+
+// Block width of request r: 2..B, B when no widths are given.
+DF2_DEV int width_of(const int32_t* width, int r, int B) { return width != nullptr ? min(max(width[r], 2), B) : B; }
 
 // Chunk statistics written by other CTAs of the launch, read from L2.
 DF2_DEV VerifyStat ldst(const VerifyStat* p) {
@@ -171,17 +177,19 @@ __device__ int draw_row(const VerifyArgs& a, const float* z, const VerifyStat* s
 __device__ void chain_body(const VerifyArgs& a, int r) {
   extern __shared__ double csum[];  // [n_chunks]
   __shared__ double red[8];
-  __shared__ float rowM[kB], rowS[kB];
-  __shared__ int rowA[kB], rowF[kB], rowBad;
+  __shared__ float rowM[kMaxBlock], rowS[kMaxBlock];
+  __shared__ int rowA[kMaxBlock], rowF[kMaxBlock], rowBad;
   __shared__ int cid[kK];
   __shared__ float qv[kK];
-  int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
+  const int B = a.B, P = B - 1;  // block positions, proposal slots of a row of path / q
+  const int w = width_of(a.width, r, B), np = w - 1;  // rows verified, proposals tested (bonus row np)
+  int32_t* emitted = a.emitted + static_cast<size_t>(r) * B;
   // debug output: NaN wherever this request gets no probability
-  float* probs = a.probs != nullptr ? a.probs + static_cast<size_t>(r) * kB * 2 : nullptr;
-  if (probs != nullptr && threadIdx.x < 2 * kB) probs[threadIdx.x] = __int_as_float(0x7FC00000);
+  float* probs = a.probs != nullptr ? a.probs + static_cast<size_t>(r) * B * 2 : nullptr;
+  if (probs != nullptr && threadIdx.x < 2 * B) probs[threadIdx.x] = __int_as_float(0x7FC00000);
   __shared__ float sh_mass;
   if (a.status[r] != 0) {
-    if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
+    if (threadIdx.x < B) emitted[threadIdx.x] = -1;
     if (threadIdx.x == 0) {
       a.n_accepted[r] = 0;
       a.n_emitted[r] = 0;
@@ -189,10 +197,10 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
     return;
   }
   const float T = a.temperature[r];
-  const VerifyStat* st = a.stats + static_cast<size_t>(r) * kB * a.n_chunks;
-  {
-    // warp j folds the chunk statistics of row j (lane-strided, fixed shuffle tree)
-    const int j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const VerifyStat* st = a.stats + static_cast<size_t>(r) * B * a.n_chunks;
+  // warp j folds the chunk statistics of rows j, j + 8 (lane-strided, fixed shuffle tree)
+  for (int j = threadIdx.x >> 5; j < w; j += 8) {
+    const int lane = threadIdx.x & 31;
     const VerifyStat* sj = st + static_cast<size_t>(j) * a.n_chunks;
     float M = -INFINITY;
     int A = 0x7FFFFFFF, F = 0;
@@ -229,12 +237,12 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int bad = 0;
-    for (int j = 0; j < kB; ++j) bad |= rowF[j];
+    for (int j = 0; j < w; ++j) bad |= rowF[j];
     rowBad = bad;
   }
   __syncthreads();
   if (rowBad) {
-    if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
+    if (threadIdx.x < B) emitted[threadIdx.x] = -1;
     if (threadIdx.x == 0) {
       a.n_accepted[r] = 0;
       a.n_emitted[r] = 0;
@@ -242,33 +250,33 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
     }
     return;
   }
-  const int32_t* path = a.path + static_cast<size_t>(r) * kP;
+  const int32_t* path = a.path + static_cast<size_t>(r) * P;
   if (!(T > 0.f)) {
     if (threadIdx.x == 0) {
       int n = 0;
-      while (n < kP && path[n] == rowA[n]) {
+      while (n < np && path[n] == rowA[n]) {
         emitted[n] = path[n];
         ++n;
       }
       emitted[n] = rowA[n];
-      for (int j = n + 1; j < kB; ++j) emitted[j] = -1;
+      for (int j = n + 1; j < B; ++j) emitted[j] = -1;
       a.n_accepted[r] = n;
       a.n_emitted[r] = n + 1;
     }
     return;
   }
   const uint64_t seed = a.seed[r], off = a.offset[r];
-  const float* zr = a.logits + static_cast<size_t>(r) * kB * a.V;
-  // The accept tests of the seven rows depend only on the path, q and the target
-  // row, not on each other: thread j < 7 takes row j (all loads of the rows in
+  const float* zr = a.logits + static_cast<size_t>(r) * B * a.V;
+  // The accept tests of the w - 1 rows depend only on the path, q and the target
+  // row, not on each other: thread j < w - 1 takes row j (all loads of the rows in
   // flight together), then the chain stops at the first rejection.
-  __shared__ int acc_row[kP];
+  __shared__ int acc_row[kMaxBlock];
   __syncthreads();  // the NaN fill above is done before these entries are written
-  if (threadIdx.x < kP) {
+  if (threadIdx.x < np) {
     const int j = threadIdx.x;
     const int d = min(max(path[j], 0), a.V - 1);
-    const int32_t* ci = a.cand_ids + (static_cast<size_t>(r) * kP + j) * kK;
-    const float* qj = a.q_rows + (static_cast<size_t>(r) * kP + j) * kK;
+    const int32_t* ci = a.cand_ids + (static_cast<size_t>(r) * P + j) * kK;
+    const float* qj = a.q_rows + (static_cast<size_t>(r) * P + j) * kK;
     const float zd = zr[static_cast<size_t>(j) * a.V + d];
     float qd = 0.f;
     for (int k = 0; k < kK; ++k)
@@ -279,17 +287,17 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
     if (probs != nullptr) probs[2 * j] = pd;  // p_j at every row's proposal (the accept test's value)
   }
   __syncthreads();
-  int n_acc = kP;
-  for (int j = 0; j < kP; ++j)
+  int n_acc = np;
+  for (int j = 0; j < np; ++j)
     if (!acc_row[j]) {
       n_acc = j;
       break;
     }
-  if (n_acc < kP) {
+  if (n_acc < np) {
     const int j = n_acc;
     if (threadIdx.x < kK) {
-      cid[threadIdx.x] = min(max(a.cand_ids[(static_cast<size_t>(r) * kP + j) * kK + threadIdx.x], 0), a.V - 1);
-      qv[threadIdx.x] = a.q_rows[(static_cast<size_t>(r) * kP + j) * kK + threadIdx.x];
+      cid[threadIdx.x] = min(max(a.cand_ids[(static_cast<size_t>(r) * P + j) * kK + threadIdx.x], 0), a.V - 1);
+      qv[threadIdx.x] = a.q_rows[(static_cast<size_t>(r) * P + j) * kK + threadIdx.x];
     }
     __syncthreads();
     const float* z = zr + static_cast<size_t>(j) * a.V;
@@ -300,34 +308,31 @@ __device__ void chain_body(const VerifyArgs& a, int r) {
       if (probs != nullptr) probs[2 * j + 1] = sh_mass;
       for (int t = 0; t < j; ++t) emitted[t] = path[t];
       emitted[j] = x;
-      for (int t = j + 1; t < kB; ++t) emitted[t] = -1;
+      for (int t = j + 1; t < B; ++t) emitted[t] = -1;
       a.n_accepted[r] = j;
       a.n_emitted[r] = j + 1;
     }
     return;
   }
-  const float u = philox_uniform(seed, off, static_cast<uint32_t>(kP), kPurposeResample);
-  const float* z = zr + static_cast<size_t>(kP) * a.V;
-  const int x = draw_row(a, z, st + static_cast<size_t>(kP) * a.n_chunks, rowM[kP], rowS[kP], T, cid, qv, false, u,
+  const float u = philox_uniform(seed, off, static_cast<uint32_t>(np), kPurposeResample);
+  const float* z = zr + static_cast<size_t>(np) * a.V;
+  const int x = draw_row(a, z, st + static_cast<size_t>(np) * a.n_chunks, rowM[np], rowS[np], T, cid, qv, false, u,
                          csum, red, &sh_mass);
   if (threadIdx.x == 0) {
-    if (probs != nullptr) probs[2 * kP] = expf((z[x] - rowM[kP]) / T) / rowS[kP];
-    for (int t = 0; t < kP; ++t) emitted[t] = path[t];
-    emitted[kP] = x;
-    a.n_accepted[r] = kP;
-    a.n_emitted[r] = kP + 1;
+    if (probs != nullptr) probs[2 * np] = expf((z[x] - rowM[np]) / T) / rowS[np];
+    for (int t = 0; t < np; ++t) emitted[t] = path[t];
+    emitted[np] = x;
+    for (int t = np + 1; t < B; ++t) emitted[t] = -1;
+    a.n_accepted[r] = np;
+    a.n_emitted[r] = np + 1;
   }
 }
 
-// The target logits and temperatures are caller inputs that the previous kernel may
-// have written (the target model's), so the statistics wait for it.
-__global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
+// Statistics of one (target row, vocabulary chunk): max, argmax, compensated sum of
+// exp((z - max) / T), flags.
+DF2_DEV void row_chunk_stats(const VerifyArgs& a, int rj, int r, int chunk) {
   __shared__ float sm_m[8], sm_s[8], sm_sl[8];
   __shared__ int sm_a[8], sm_f[8];
-  pdl_begin_early();
-  const int rj = blockIdx.x;  // r * 8 + j
-  const int r = rj >> 3;
-  const int chunk = blockIdx.y;
   const float T = a.temperature[r];
   const float* z = a.logits + static_cast<size_t>(rj) * a.V;
   const int v0 = chunk * kVerifyChunk;
@@ -430,13 +435,24 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
     st.flags = F;
     a.stats[static_cast<size_t>(rj) * a.n_chunks + chunk] = st;
   }
-  // count this chunk; the CTA that completes request r's 8 x n_chunks runs its chain
+}
+
+// The target logits and temperatures are caller inputs that the previous kernel may
+// have written (the target model's), so the statistics wait for it.
+__global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
+  pdl_begin_early();
+  const int rj = blockIdx.x;  // r * B + j
+  const int r = rj / a.B, j_row = rj % a.B;
+  const int chunk = blockIdx.y;
+  // rows at or past the request's width are not read, only counted
+  if (j_row < width_of(a.width, r, a.B)) row_chunk_stats(a, rj, r, chunk);
+  // count this chunk; the CTA that completes request r's B x n_chunks runs its chain
   __shared__ bool last;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned int prev = atomicAdd(a.counters + r, 1u);
-    last = prev == static_cast<unsigned int>(kB * a.n_chunks - 1);
+    last = prev == static_cast<unsigned int>(a.B * a.n_chunks - 1);
     if (last) a.counters[r] = 0u;  // every CTA of the set has counted
   }
   __syncthreads();
@@ -456,6 +472,7 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
 __device__ void tree_chain(const TreeVerifyArgs& a, int r) {
   __shared__ int am[kTreeMaxNodes + 1], bad_row[kTreeMaxNodes + 1];
   const int n = min(max(a.n_nodes[r], 0), a.budget);
+  const int kB = a.B;
   int32_t* emitted = a.emitted + static_cast<size_t>(r) * kB;
   if (a.status[r] != 0) {
     if (threadIdx.x < kB) emitted[threadIdx.x] = -1;
@@ -616,11 +633,13 @@ __global__ void __launch_bounds__(256) tree_stats_kernel(const TreeVerifyArgs a)
 
 cudaError_t launch_tree_verify(const TreeVerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if (a.budget < 1 || a.budget > kTreeMaxNodes || a.n_chunks < 1) return cudaErrorInvalidValue;
+  if (a.B != 8 && a.B != 16) return cudaErrorInvalidValue;
   return launch_ex(tree_stats_kernel, dim3(n_req * (a.budget + 1), a.n_chunks), dim3(256), 0, st, pdl, a);
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  return launch_ex(verify_stats_kernel, dim3(n_req * kB, a.n_chunks), dim3(256), a.n_chunks * sizeof(double), st, pdl,
+  if (a.B != 8 && a.B != 16) return cudaErrorInvalidValue;
+  return launch_ex(verify_stats_kernel, dim3(n_req * a.B, a.n_chunks), dim3(256), a.n_chunks * sizeof(double), st, pdl,
                    a);
 }
 

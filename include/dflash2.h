@@ -11,7 +11,18 @@
  *     weight format;
  *   - "[Spec Decode] DFlash2: local convolution + candidate selector - #52816"
  *     (vLLM PR description): the convolution formula, the selector edge score,
- *     the walk from the verified anchor and the q returned for the verify.
+ *     the walk from the verified anchor and the q returned for the verify;
+ *   - "qwen35: DSpark speculative decoding (Qwen3.8-27B drafters) - #625": the
+ *     wider draft block (16 positions; greedy chains stay those of plain decoding
+ *     at any width), the long-context narrowing of the block, and the draft tree.
+ *
+ * Blocks: a handle drafts blocks of B = cfg.block positions (8 or 16): position 0
+ * is the anchor, 1..B-1 are mask tokens, so a request has B - 1 proposals and B
+ * target rows.  Rows of per-position tensors are request-major.  A request may be
+ * narrowed to a block width w (2..B) for a step (`width` arguments; see
+ * dflash2_block_width): it is then drafted, walked and verified exactly as a block
+ * of w positions of the same drafter, and entries for its positions w..B-1 are
+ * unspecified (drafter outputs) or padding (path -1, q 0, emitted -1).
  *
  * Conventions (all entry points):
  *   - Every tensor argument is a DEVICE pointer owned by the caller, unless the
@@ -54,7 +65,8 @@ enum {
 enum { DFLASH2_WEIGHTS_BF16 = 0, DFLASH2_WEIGHTS_Q8G64 = 1 };
 
 #define DFLASH2_MAX_LAYERS 8
-/* Largest max_requests of dflash2_create (128 block rows per step). */
+/* Largest max_requests of dflash2_create with blocks of 8; max_requests * block
+ * <= 8 * DFLASH2_MAX_REQUESTS (128 block rows per step). */
 #define DFLASH2_MAX_REQUESTS 16
 
 /* Drafter geometry ("LSE docs/DFLASH2.md", compatible-drafter paragraph). */
@@ -67,7 +79,7 @@ typedef struct dflash2_config {
   int32_t ffn;            /* F: 17408                                             */
   int32_t vocab;          /* V: 248320                                            */
   int32_t n_taps;         /* target feature taps: 5                               */
-  int32_t block;          /* positions per draft block: 8 (anchor + 7 masks)      */
+  int32_t block;          /* positions per draft block: 8 (anchor + 7 masks) or 16 */
   int32_t top_k;          /* candidates per position: 16                          */
   int32_t rank;           /* selector codebook rank: 256                          */
   int32_t window;         /* sliding window over context keys: 2048               */
@@ -125,14 +137,14 @@ typedef struct dflash2_handle dflash2_handle;
  * scratch for up to `max_requests` requests.  `kv_capacity` is the number of
  * positions per request in the caller's K/V caches.  Must be called with the
  * target device current.  Returns DFLASH2_E_UNSUPPORTED for a geometry the
- * kernels do not cover: head_dim != 128, block != 8, top_k != 16, rank != 256,
- * conv taps != 2 or group != 16, n_q_heads != 4 * n_kv_heads, hidden not a
+ * kernels do not cover: head_dim != 128, block not 8 or 16, top_k != 16, rank !=
+ * 256, conv taps != 2 or group != 16, n_q_heads != 4 * n_kv_heads, hidden not a
  * multiple of 256, ffn not a multiple of 128 (BF16) or 256 (Q8G64), vocab not a
- * multiple of 16, more than DFLASH2_MAX_LAYERS layers or DFLASH2_MAX_REQUESTS
- * requests, or a window over 64 attention chunks of 64 keys; and, when
- * max_requests reaches 5 (BF16) or 4 (Q8G64), hidden / 4 or vocab not a multiple
- * of 128: calls with that many requests run every projection on the tensor-core
- * GEMM, in 128-row weight blocks.  Every weight
+ * multiple of 16, more than DFLASH2_MAX_LAYERS layers, max_requests * block over
+ * 8 * DFLASH2_MAX_REQUESTS, or a window over 64 attention chunks of 64 keys; and,
+ * when max_requests * block reaches 40 (BF16) or 32 (Q8G64) rows, hidden / 4 or
+ * vocab not a multiple of 128: calls with that many block rows run every
+ * projection on the tensor-core GEMM, in 128-row weight blocks.  Every weight
  * matrix, Q8 scale and Q8 bias must start on a 16-byte boundary
  * (DFLASH2_E_INVAL otherwise).  Encodes one bulk-copy descriptor per projection
  * matrix, so the weights must not move while the handle lives. */
@@ -144,27 +156,32 @@ dflash2_status dflash2_destroy(dflash2_handle* h);
 /* Draft block: steps a1-a9 of the method for n_req requests.
  *   anchor_ids [R]       verified anchor token of each request
  *   ctx_len [R]          keys already in the cache before this call
- *   n_new [R]            new context rows to append (0..block)
+ *   n_new [R]            new context rows to append (0..block; at most the previous
+ *                        step's width)
  *   taps [R][block][n_taps*H] float32: target feature taps of the new rows
  *                        (rows >= n_new[r] are ignored)
  *   k_cache, v_cache     bf16 [n_layers][max_requests][kv_capacity][nkv][hd]; rows
  *                        ctx_len..ctx_len+n_new-1 of each request are written (the
  *                        new context rows' K after k_norm and RoPE, and V), then
  *                        rows max(0, L-window+1)..L-1 are read, L = ctx_len+n_new
- *   cand_ids [R][block-1][top_k]     top-16 vocabulary ids of positions 1..7, in
+ *   cand_ids [R][block-1][top_k]     top-16 vocabulary ids of positions 1..block-1, in
  *                        order: NaN first (by id), then value descending, ties to
  *                        the smaller id ("LSE docs/DFLASH2.md", top-k paragraph)
  *   cand_logits [R][block-1][top_k] float32 drafter logits of those ids
  *   gate [R][block-1][rank] float32  selector projection of the final hidden state
  *   logits_out [R][block-1][V] float32 or NULL: full drafter logits (debugging,
  *                        test harness)
+ *   width [R] or NULL    block width of each request (clamped into 2..block; NULL:
+ *                        block): the block keys at positions >= width are masked
+ *                        in the attention, so positions 0..width-1 are a block of
+ *                        width positions
  * Requires ctx_len + n_new <= kv_capacity.  Every wait in the weight-streaming
  * pipelines is bounded; one that gives up sets the handle's error word (cleared at
  * the start of each call), which the following dflash2_select reports per request. */
 dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
                                    const int32_t* ctx_len, const int32_t* n_new, const float* taps,
                                    void* k_cache, void* v_cache, int32_t* cand_ids, float* cand_logits,
-                                   float* gate, float* logits_out, void* stream);
+                                   float* gate, float* logits_out, const int32_t* width, void* stream);
 
 /* Selector walk (step a10; vLLM PR #52816 description, candidate selector):
  * score(p -> c) = <A[p] * gate_i, B[c]> + cand_logit_i[c]; the walk starts at the
@@ -178,17 +195,21 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
  *   DFLASH2_E_INVAL (negative temperature) or DFLASH2_E_CUDA (a pipeline wait of the
  *   handle's last dflash2_draft_block gave up: its candidates and gate are undefined;
  *   the handle's error word is cleared by the next dflash2_draft_block)
- *   temperature [R] float32 (negative -> status DFLASH2_E_INVAL); seed, philox_offset [R] uint64 */
+ *   temperature [R] float32 (negative -> status DFLASH2_E_INVAL); seed, philox_offset [R] uint64
+ *   width [R] or NULL: the walk takes positions 1..width-1 (clamped into 2..block;
+ *   NULL: block); path entries past them are -1 and their q rows 0.  Every
+ *   position's lattice is still scored (scores_out). */
 dflash2_status dflash2_select(dflash2_handle* h, int32_t n_req, const int32_t* anchor_ids,
                               const int32_t* cand_ids, const float* cand_logits, const float* gate,
                               const float* temperature, const uint64_t* seed, const uint64_t* philox_offset,
-                              int32_t* path, float* q_rows, float* scores_out, int32_t* status, void* stream);
+                              int32_t* path, float* q_rows, float* scores_out, int32_t* status,
+                              const int32_t* width, void* stream);
 
 /* Selector mode of the handle's later dflash2_select calls (an ablation of the
  * walk; vLLM PR #52816 description: "walk the best path from the verified anchor").
  *   0 (default): the sequential walk above.
  *   1: for greedy requests (temperature 0) the globally best path instead, the
- *      path of highest total edge score over the 16^7 candidate sequences, by
+ *      path of highest total edge score over the 16^(width-1) candidate sequences, by
  *      dynamic programming with float32 sums (equal sums -> the predecessor with
  *      the smaller id; equal ends -> the smaller id); q rows one-hot.  Requests with
  *      temperature > 0 still walk and sample.
@@ -204,6 +225,9 @@ dflash2_status dflash2_set_select_mode(dflash2_handle* h, int32_t mode);
  *   j); on rejection draw from max(0, p_j - q_j) normalised by inverse CDF in id
  *   order (purpose 2, slot j; from p_j if that mass <= 1e-30); if all accepted draw
  *   the bonus from the last row (purpose 2, slot block-1).
+ *   width [R] or NULL: a request of width w (clamped into 2..block; NULL: block)
+ *   tests proposals 0..w-2 against rows 0..w-2, takes its bonus from row w-1
+ *   (slot w-1), and its rows w..block-1 are not read.
  *   n_accepted [R]; emitted [R][block] (-1 padded); n_emitted [R] = n_accepted+1.
  *   probs_out [R][block][2] float32 or NULL (debugging, test harness): for a request
  *   with T > 0, [j][0] = p_j(path[j]) for j < block-1 and [block-1][0] = p of the
@@ -217,7 +241,7 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
                               const int32_t* cand_ids, const float* q_rows, const float* temperature,
                               const uint64_t* seed, const uint64_t* philox_offset, int32_t* n_accepted,
                               int32_t* emitted, int32_t* n_emitted, float* probs_out, int32_t* status,
-                              void* stream);
+                              const int32_t* width, void* stream);
 
 /* ---- Draft tree (DDTree) ----
  * "qwen35: DSpark speculative decoding (Qwen3.8-27B drafters) - #625", DDTree
@@ -262,7 +286,7 @@ dflash2_status dflash2_tree_verify(dflash2_handle* h, int32_t n_req, int32_t bud
 
 /* Serving-loop state update after dflash2_verify, on the device (so a multi-step
  * loop can be captured in one graph; "LSE docs/DFLASH2.md", block paragraph: each
- * draft is an anchor plus seven masks; vLLM PR #52816 description, candidate
+ * draft is an anchor plus block-1 masks; vLLM PR #52816 description, candidate
  * selector: the walk starts at the verified anchor).  For each request r:
  *   ctx_len[r] += n_new[r]          the rows this step appended are now context
  *   if n_emitted[r] > 0: anchor_ids[r] = emitted[r][n_emitted[r] - 1]
@@ -280,15 +304,31 @@ dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* 
                                int32_t* anchor_ids, int32_t* ctx_len, int32_t* n_new, uint64_t* philox_offset,
                                void* stream);
 
+/* Block width of each request by context length ("qwen35: DSpark speculative
+ * decoding ... #625", long-context commits: the verify's cost grows with the
+ * block's rows times the context, so past a context threshold the block narrows;
+ * the rule reads the context length only, so a prompt's width is reproducible):
+ *   width[r] = narrow_width  if ctx_threshold > 0 and ctx_len[r] + n_new[r] > ctx_threshold
+ *              block         otherwise
+ * ctx_len + n_new is the context the step's block attends to (the keys after this
+ * step's append).  The pages' default is ctx_threshold 8192, narrow_width 8 for a
+ * drafter of block 16; ctx_threshold 0 disables narrowing.
+ *   ctx_len, n_new [R] int32 (dflash2_draft_block's inputs); width [R] int32 out.
+ * Returns DFLASH2_E_INVAL for a null pointer, n_req outside 1..max_requests, a
+ * negative threshold or narrow_width outside 2..block (nothing is launched). */
+dflash2_status dflash2_block_width(dflash2_handle* h, int32_t n_req, const int32_t* ctx_len, const int32_t* n_new,
+                                  int32_t ctx_threshold, int32_t narrow_width, int32_t* width, void* stream);
+
 /* LM head + top-16 alone (step a8 on given final hidden states): logits of block
- * positions 1..7 = W_lm . hidden (hidden already normalised, BF16), top-16 with the
- * ordering of dflash2_draft_block.  Row n of `hidden` is request n/8, block position
- * n%8 (position 0 is not projected).  n_rows: multiple of 8, <= 8*max_requests.
- * Up to 32 rows run on the LM-head kernel; more rows (a handle whose calls reach
- * the tensor-core GEMM, see dflash2_create, else DFLASH2_E_UNSUPPORTED) on the
- * tensor-core GEMM, with the logits in handle scratch, then a chunked top-16.
- *   hidden [n_rows][H] bf16; cand_ids, cand_logits [n_rows/8][block-1][top_k];
- *   logits_out [n_rows/8][block-1][V] float32 or NULL. */
+ * positions 1..B-1 = W_lm . hidden (hidden already normalised, BF16), top-16 with
+ * the ordering of dflash2_draft_block.  Row n of `hidden` is request n/B, block
+ * position n%B (position 0 is not projected), B = the handle's block.  n_rows: a
+ * multiple of B, <= B*max_requests.  Up to 32 rows run on the LM-head kernel; more
+ * rows (a handle whose calls reach the tensor-core GEMM, see dflash2_create, else
+ * DFLASH2_E_UNSUPPORTED) on the tensor-core GEMM, with the logits in handle
+ * scratch, then a chunked top-16.
+ *   hidden [n_rows][H] bf16; cand_ids, cand_logits [n_rows/B][B-1][top_k];
+ *   logits_out [n_rows/B][B-1][V] float32 or NULL. */
 dflash2_status dflash2_head_topk(dflash2_handle* h, int32_t n_rows, const void* hidden, int32_t* cand_ids,
                                  float* cand_logits, float* logits_out, void* stream);
 

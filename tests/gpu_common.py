@@ -48,38 +48,41 @@ class GpuStep:
         self.g = g
         self.drafter = drafter or bd.Drafter(g, wl.weight_format, W, wl.n_req, wl.kv_capacity)
         R = wl.n_req
+        B, P = g.block, g.block - 1
         dev = "cuda"
-        self.cand_ids = torch.zeros((R, 7, 16), dtype=torch.int32, device=dev)
-        self.cand_logits = torch.zeros((R, 7, 16), dtype=torch.float32, device=dev)
-        self.gate = torch.zeros((R, 7, g.rank), dtype=torch.float32, device=dev)
-        self.logits = torch.zeros((R, 7, g.vocab), dtype=torch.float32, device=dev)
-        self.path = torch.zeros((R, 7), dtype=torch.int32, device=dev)
-        self.q_rows = torch.zeros((R, 7, 16), dtype=torch.float32, device=dev)
-        self.scores = torch.zeros((R, 7, 16, 16), dtype=torch.float32, device=dev)
+        self.cand_ids = torch.zeros((R, P, 16), dtype=torch.int32, device=dev)
+        self.cand_logits = torch.zeros((R, P, 16), dtype=torch.float32, device=dev)
+        self.gate = torch.zeros((R, P, g.rank), dtype=torch.float32, device=dev)
+        self.logits = torch.zeros((R, P, g.vocab), dtype=torch.float32, device=dev)
+        self.path = torch.zeros((R, P), dtype=torch.int32, device=dev)
+        self.q_rows = torch.zeros((R, P, 16), dtype=torch.float32, device=dev)
+        self.scores = torch.zeros((R, P, 16, 16), dtype=torch.float32, device=dev)
         self.status = torch.zeros((R,), dtype=torch.int32, device=dev)
         self.n_acc = torch.zeros((R,), dtype=torch.int32, device=dev)
-        self.emitted = torch.zeros((R, 8), dtype=torch.int32, device=dev)
+        self.emitted = torch.zeros((R, B), dtype=torch.int32, device=dev)
         self.n_emit = torch.zeros((R,), dtype=torch.int32, device=dev)
-        self.probs = torch.zeros((R, 8, 2), dtype=torch.float32, device=dev)
+        self.probs = torch.zeros((R, B, 2), dtype=torch.float32, device=dev)
+        self.width = None  # [R] int32 device tensor of block widths, or None (full blocks)
 
     def draft(self, anchors, ctx_len, n_new, taps, kc, vc, with_logits=True):
         h = self.drafter.handle
         R = self.wl.n_req
         bd.dflash2_draft_block(h, R, anchors, ctx_len, n_new, taps, kc, vc, self.cand_ids, self.cand_logits,
-                               self.gate, self.logits if with_logits else None)
+                               self.gate, self.logits if with_logits else None, width=self.width)
 
     def select(self, anchors, temps, seeds, offsets, cand_ids=None, cand_logits=None, gate=None):
         h = self.drafter.handle
         bd.dflash2_select(h, self.wl.n_req, anchors, self.cand_ids if cand_ids is None else cand_ids,
                           self.cand_logits if cand_logits is None else cand_logits,
                           self.gate if gate is None else gate, temps, seeds, offsets, self.path, self.q_rows,
-                          self.scores, self.status)
+                          self.scores, self.status, width=self.width)
 
     def verify(self, target, temps, seeds, offsets, path=None, cand_ids=None, q_rows=None):
         h = self.drafter.handle
         bd.dflash2_verify(h, self.wl.n_req, target, self.path if path is None else path,
                           self.cand_ids if cand_ids is None else cand_ids, self.q_rows if q_rows is None else q_rows,
-                          temps, seeds, offsets, self.n_acc, self.emitted, self.n_emit, self.probs, self.status)
+                          temps, seeds, offsets, self.n_acc, self.emitted, self.n_emit, self.probs, self.status,
+                          width=self.width)
 
 
 def oracle_draft(wl, W, inp, kc_host, vc_host, r):
@@ -146,12 +149,13 @@ def lattice_error_bounds(W, anchor, cand_ids, gate, scores, q8: bool):
     |fl(s) - s| <= gamma_n * sum_r |a_r g_r b_r| + 2u/(1-u) |s|, the mixed bound of the
     LSE page's selector test paragraph (n = 256 products + 2 roundings per term; Q8
     codebooks add the two dequantisations per term).  scores: the oracle's FP64
-    lattice [7][16][16] (row p of position 1 repeats the anchor row).  -> [7][16][16]"""
+    lattice [P][16][16] (row p of position 1 repeats the anchor row).  -> [P][16][16]"""
     n = 262 if q8 else 258
     gam = n * U24 / (1 - n * U24)
-    out = np.zeros((7, 16, 16))
-    B_all = [np.abs(oracle.codebook_rows(W["cb_b"], cand_ids[i])) for i in range(7)]
-    for i in range(7):
+    P = len(cand_ids)
+    out = np.zeros((P, 16, 16))
+    B_all = [np.abs(oracle.codebook_rows(W["cb_b"], cand_ids[i])) for i in range(P)]
+    for i in range(P):
         preds = [anchor] * 16 if i == 0 else cand_ids[i - 1]
         A = np.abs(oracle.codebook_rows(W["cb_a"], preds))                 # [16][r]
         absprod = (A * np.abs(gate[i])[None, :]) @ B_all[i].T              # [p][c]
@@ -170,7 +174,8 @@ def compare_walk(res, gpu_path, gpu_q, bounds, T, cand_ids, exact=False):
     Returns (positions compared, undecided: bool, list of (gpu q row, oracle q row))."""
     prev = 0
     qs = []
-    for i in range(7):
+    P = len(res["path"])
+    for i in range(P):
         E = 0.0 if exact else float(np.max(bounds[i, prev]))  # integer inputs: every score is exact
         if T == 0.0:
             decided = exact or res["margins"][i] > 3 * E
@@ -181,7 +186,7 @@ def compare_walk(res, gpu_path, gpu_q, bounds, T, cand_ids, exact=False):
         assert gpu_path[i] == res["path"][i], (i, gpu_path, res["path"])
         qs.append((gpu_q[i], res["q_rows"][i]))
         prev = int(np.nonzero(cand_ids[i] == res["path"][i])[0][0])
-    return 7, False, qs
+    return P, False, qs
 
 
 # Decision thresholds of the verify comparison.  The kernel's p at one entry carries
@@ -209,18 +214,24 @@ def verify_decided(res) -> bool:
 def compare_verify(res, na, em, ne, probs, T):
     """Bit-exact outputs; the verify probabilities (T > 0) as pairs for a rel-L2 check:
     p at every proposal, and the residual mass / bonus p where both sides took that
-    branch (the same branch whenever the outputs agree)."""
+    branch (the same branch whenever the outputs agree).  The oracle's verify may run
+    on fewer rows w than the GPU's block (a narrowed request): the GPU's entries past
+    them are padding (emitted -1, probabilities NaN)."""
     assert na == res["n_accepted"] and ne == res["n_emitted"], (na, ne, res["n_accepted"], res["n_emitted"])
-    assert np.array_equal(em, res["emitted"]), (em, res["emitted"])
+    w = len(res["emitted"])
+    assert np.array_equal(em[:w], res["emitted"]), (em, res["emitted"])
+    assert np.all(em[w:] == -1)
+    P = w - 1
     pairs = []
     if T > 0:
-        pairs += list(zip(probs[:7, 0], res["p_path"]))
-        if res["n_accepted"] < 7:
+        pairs += list(zip(probs[:P, 0], res["p_path"]))
+        if res["n_accepted"] < P:
             j = res["n_accepted"]
             pairs.append((probs[j, 1], res["residual_mass"][j]))
-            assert np.all(np.isnan(np.delete(probs[:7, 1], j)))
+            assert np.all(np.isnan(np.delete(probs[:P, 1], j)))
         else:
-            pairs.append((probs[7, 0], res["p_bonus"]))
+            pairs.append((probs[P, 0], res["p_bonus"]))
+        assert np.all(np.isnan(probs[w:]))
     else:
         assert np.all(np.isnan(probs))
     return pairs

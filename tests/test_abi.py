@@ -33,8 +33,8 @@ def test_library_exports_every_declared_symbol():
 def test_host_validation_without_device_work():
     """Bad arguments are rejected on the host before any launch."""
     lib = bd.lib()
-    lib.dflash2_draft_block.argtypes = [ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 11
-    assert lib.dflash2_draft_block(None, 1, *([None] * 11)) == bd.binding.E_INVAL
+    lib.dflash2_draft_block.argtypes = [ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 12
+    assert lib.dflash2_draft_block(None, 1, *([None] * 12)) == bd.binding.E_INVAL
     assert lib.dflash2_status_string(2) == b"nonfinite logit or selector score"
     h = ctypes.c_void_p()
     cfg = bd.binding.Config()
@@ -68,6 +68,12 @@ def _toy_config(**kw):
     (dict(n_q_heads=8), 1, "E_UNSUPPORTED"),                   # 4 query heads per KV head
     (dict(vocab=8200, mask_token_id=8199), 1, "E_UNSUPPORTED"),  # vocab % 16
     (dict(), 17, "E_UNSUPPORTED"),                             # more than DFLASH2_MAX_REQUESTS
+    (dict(block=12), 1, "E_UNSUPPORTED"),                      # blocks of 8 or 16 only
+    (dict(block=16), 9, "E_UNSUPPORTED"),                      # more than 128 block rows
+    (dict(block=16, vocab=8208, mask_token_id=8207), 3, "E_UNSUPPORTED"),  # bf16 tensor-core path: 48 rows
+    (dict(block=16, vocab=8208, mask_token_id=8207), 2, "E_INVAL"),       # 32 rows: GEMV path
+    (dict(block=16, vocab=8208, mask_token_id=8207, weight_format=1), 2, "E_UNSUPPORTED"),  # Q8 from 32 rows
+    (dict(block=16, vocab=8208, mask_token_id=8207, weight_format=1), 1, "E_INVAL"),
     (dict(vocab=8208, mask_token_id=8207), 5, "E_UNSUPPORTED"),  # tensor-core path: vocab % 128
     (dict(hidden=768, ffn=1536, n_q_heads=4), 5, "E_UNSUPPORTED"),  # tensor-core path: hidden/4 % 128
     (dict(vocab=8208, mask_token_id=8207, weight_format=1), 4, "E_UNSUPPORTED"),  # Q8 from 4 requests
@@ -91,8 +97,11 @@ def test_create_geometry_limits_on_the_host(kw, max_req, want):
 def test_entry_points_reject_a_null_handle_or_bad_sizes():
     lib = bd.lib()
     E = bd.binding.E_INVAL
-    assert lib.dflash2_select(None, 1, *([None] * 12)) == E
-    assert lib.dflash2_verify(None, 1, *([None] * 13)) == E
+    assert lib.dflash2_select(None, 1, *([None] * 13)) == E
+    assert lib.dflash2_verify(None, 1, *([None] * 14)) == E
+    lib.dflash2_block_width.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.dflash2_block_width(None, 1, None, None, 8192, 8, None, None) == E
     lib.dflash2_tree_build.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32] + [ctypes.c_void_p] * 12
     lib.dflash2_tree_verify.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32] + [ctypes.c_void_p] * 9
     assert lib.dflash2_tree_build(None, 1, 12, *([None] * 12)) == E

@@ -156,5 +156,13 @@ WORKLOADS[8] = Workload("profile_q8_r1_one_full_layer",
                         description="profiling: one full-width layer, vocab 16384, Q8, 1 request, ctx 2048, T=1.0")
 
 
+# The one-request BF16 workload with blocks of 16 positions (anchor + 15 masks): the
+# wider draft block of the DSpark pull request's greedy-width commit, on the drafter
+# geometry otherwise unchanged.
+WORKLOADS[9] = Workload("cfg2_bf16_r1_ctx1024_block16", dataclasses.replace(FULL, block=16), "bf16", 1, [1024],
+                        [0.0], [1.0], seed=2,
+                        description="full geometry with blocks of 16, BF16 weights, 1 request, ctx 1024, greedy")
+
+
 def workload(i: int) -> Workload:
     return WORKLOADS[i]
