@@ -39,6 +39,7 @@ struct dflash2_handle {
   // max_requests reaches that)
   struct PlaneSet {
     GemvPlanes fc, d0, d, q, k, v, o, g, u, down, sel, lm;
+    GemvPlanes q2, k2, v2;  // the GEMM's q/k/v launch with more than 128 key/value rows
   } pn, pw;
   bool wide;  // the tensor-core path is set up
   CUtensorMap wmap_fc, wmap_sel, wmap_lm, wmap_layer[DFLASH2_MAX_LAYERS][9];  // its weight maps
@@ -278,11 +279,11 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
     for (int path = 0; path < (h->wide ? 2 : 1); ++path) {
       dflash2_handle::PlaneSet& P = path == 0 ? h->pn : h->pw;
       auto plan = [&](std::initializer_list<GemvSeg> segs, std::initializer_list<GemvPlanes*> pls,
-                      std::initializer_list<int*> maxes, int f) {
+                      std::initializer_list<int*> maxes, int f, int nmax = 128) {
         GemvArgs a;
         memset(&a, 0, sizeof(a));
         for (const GemvSeg& g : segs) a.seg[a.nseg++] = g;
-        const int C = path == 0 ? gemv_plan(a, h->num_sms, fmt) : wide_plan(a, h->num_sms, f);
+        const int C = path == 0 ? gemv_plan(a, h->num_sms, fmt) : wide_plan(a, h->num_sms, f, nmax);
         int i = 0;
         for (GemvPlanes* p : pls) *p = path == 0 ? gemv_planes(a, i++, C) : wide_planes(a, i++, C);
         i = 0;
@@ -296,6 +297,10 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
       plan({shape(4 * h->G, h->H)}, {&P.d}, {&maxp_d}, fmt);
       plan({shape(h->qd, h->H), shape(h->kvd, h->H), shape(h->kvd, h->H)}, {&P.q, &P.k, &P.v},
            {&maxp_q, &maxp_k, &maxp_v}, fmt);
+      // the GEMM's launch with more than 128 key/value rows runs shorter int8 stages
+      if (path == 1)
+        plan({shape(h->qd, h->H), shape(h->kvd, h->H), shape(h->kvd, h->H)}, {&P.q2, &P.k2, &P.v2},
+             {&maxp_q, &maxp_k, &maxp_v}, fmt, 256);
       plan({shape(h->H, h->qd)}, {&P.o}, {&maxp_y}, fmt);
       plan({shape(h->F, h->H), shape(h->F, h->H)}, {&P.g, &P.u}, {&maxp_g, &maxp_u}, fmt);
       plan({shape(h->H, h->F)}, {&P.down}, {&maxp_y}, fmt);
@@ -630,9 +635,10 @@ dflash2_status dflash2_draft_block(dflash2_handle* h, int32_t n_req, const int32
       a.kv_capacity = h->kv_cap;
       a.H = H;
       a.nch = h->nch_ss;
-      a.pq = P.q;
-      a.pk = P.k;
-      a.pv = P.v;
+      const bool kv256 = wide && 2 * N > 128;  // the launch's plan (wide_nmax of its segments)
+      a.pq = kv256 ? P.q2 : P.q;
+      a.pk = kv256 ? P.k2 : P.k;
+      a.pv = kv256 ? P.v2 : P.v;
       a.eps = c.rms_eps;
       a.B = h->B;
       DF2_CHECK(launch_qkv_finish(a, R, pdl, st));

@@ -98,7 +98,10 @@ bool tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void
 // from the operand layout the element-wise kernels write (xt) or through xmap.
 // Fills stage_begin, total_stages and stage_k; returns the CTA count (two per SM for
 // bf16, one for int8).
-int wide_plan(GemvArgs& a, int num_sms, int fmt);
+// nmax: the launch's largest activation-row count rounded up to 16, 128 or 256 (the
+// int8 stage length depends on it; wide_nmax gives the launch's).
+int wide_plan(GemvArgs& a, int num_sms, int fmt, int nmax);
+int wide_nmax(const GemvArgs& a);
 GemvPlanes wide_planes(const GemvArgs& a, int i, int C);
 int wide_max_planes(const GemvArgs& a, int i, int C);
 // Weight map: bf16 boxes 64 K x 128 rows or int8 boxes 128 K x 128 rows (128-byte rows, 128-byte swizzle).

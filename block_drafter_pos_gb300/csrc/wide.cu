@@ -56,12 +56,16 @@ using pipe::tma_load_2d;
 constexpr int kTM = 128;         // weight rows per MMA: the MMA's M
 constexpr int kAtomK = 64;       // K of one 128-byte swizzle atom of 16-bit values
 constexpr int kMaxN = 256;       // activation rows per product: the MMA's largest N
-constexpr int kMinStages = 4;    // shortest run of stages per CTA (small launches take fewer CTAs)
+constexpr int kMinStages = 4;    // shortest run of 128-K stages per CTA (small launches take fewer CTAs)
 
-// K per stage: one bf16 weight copy of 128-byte rows (64 K), or one int8 copy of
-// 128-byte rows (128 K: two atoms of fp16 operand).
-template <int FMT>
-constexpr int stage_k() { return FMT == 0 ? 64 : 128; }
+// K per stage: one bf16 weight copy of 128-byte rows (64 K); int8 codes in copies of
+// 128-byte rows (128 K each): two per stage (256 K: four atoms of fp16 operand) for
+// up to 128 activation rows, one (128 K) for more, whose activation tiles are twice
+// the size.  Every stage costs the pipeline a fixed round of hand-offs (copies,
+// converters, products, commits; about 0.45 us measured with the data movement
+// taken out), so stages as long as the buffers allow keep it off the stream.
+template <int FMT, int NMAX>
+constexpr int stage_k() { return FMT == 0 ? 64 : (NMAX <= 128 ? 256 : 128); }
 // CTAs per SM: bf16 runs two independent pipelines per SM (each with half the
 // tensor memory); int8 one, whose sixteen converter warps fill the register file.
 // (Measured with the operand in tensor memory: two int8 CTAs per SM with one
@@ -77,9 +81,10 @@ constexpr int ctas_per_sm(int fmt) { return fmt == 0 ? 2 : 1; }
 // row, two values per column), then kBufs accumulators of NMAX fp32 columns.
 template <int FMT, int NMAX>
 struct WideGeo {
-  static constexpr int kKS = stage_k<FMT>();
+  static constexpr int kKS = stage_k<FMT, NMAX>();
   static constexpr int kAtoms = kKS / kAtomK;
-  static constexpr int kW = kTM * 128;
+  static constexpr int kW = kTM * (FMT == 0 ? 128 : kKS);  // bytes of one weight (code) stage
+  static constexpr int kWBoxes = FMT == 0 ? 1 : kKS / 128;   // copies of 128-byte rows per stage
   static constexpr int kBAtom = NMAX * kAtomK * 2;
   static constexpr int kB = kAtoms * kBAtom;
   static constexpr int kCtas = ctas_per_sm(FMT);
@@ -90,14 +95,16 @@ struct WideGeo {
   static constexpr int kBufs = (kTmemCols - kDCol0) / NMAX >= 2 ? 2 : 1;
   static constexpr int kDB = FMT == 1 ? 2 : (NMAX == 128 ? 2 : 1);
   static constexpr int kRing = (FMT == 0 ? 100 : 224) * 1024;  // bf16: two CTAs per SM
-  // int8: a 4-stage code ring (64 KB of codes in flight).  Measured at 16 requests:
-  // gate/up 78 us at 2 or 4 stages, 80 at 6, 82 at 10 (the codes queued ahead delay
-  // the activation copies behind them).
-  static constexpr int kDW = FMT == 1 ? 4 : (kRing - kDB * kB) / kW;
+  // int8: a code ring of 64 KB (2 stages of 256 K, or 4 of 128 K).  Measured at 16
+  // requests with 128-K stages: gate/up 78 us at 2 or 4 stages, 80 at 6, 82 at 10.
+  static constexpr int kDW = FMT == 1 ? 64 * 1024 / kW : (kRing - kDB * kB) / kW;
   static constexpr int kOffB = kDW * kW;
   static constexpr int kSmem = kOffB + kDB * kB + 1024;
-  static constexpr int kConvGroups = FMT == 1 ? 2 : 0;  // int8: converter warp groups, taking alternate stages
-  static constexpr int kWarps = 8 + 8 * kConvGroups;
+  // int8: sixteen converter warps, each converting 64 K of 32 weight rows per stage: one
+  // group for 256-K stages, two taking alternate stages for 128-K stages
+  static constexpr int kConvGroups = FMT == 1 ? (kKS == 256 ? 1 : 2) : 0;
+  static constexpr int kConv = FMT == 1 ? 16 / kConvGroups : 4;  // converter warps per group
+  static constexpr int kWarps = FMT == 1 ? 24 : 8;
   static_assert(kDCol0 + NMAX <= kTmemCols, "tensor memory columns");
   static_assert(kDW >= 2, "weight ring");
   // int8: converter group g takes the stages i = g (mod 2) and waits on the code slot
@@ -105,7 +112,9 @@ struct WideGeo {
   // slot's previous use (stage i - kDW) has landed, which holds when the A-slot wait
   // the group passed at stage i - 2 (the products of stage i - 2 - kDA are done, so
   // their codes were converted) covers stage i - kDW.
-  static_assert(FMT == 0 || kDW == kConvGroups || kDW >= kDA + kConvGroups, "code ring depth vs converter groups");
+  static_assert(FMT == 0 || kConvGroups == 1 || kDW == kConvGroups || kDW >= kDA + kConvGroups,
+                "code ring depth vs converter groups");
+  static_assert(FMT == 0 || kConv == 4 * (kKS / 64), "converter warps: four lane groups per 64 K");
   static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
@@ -246,7 +255,7 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
   using Geo = WideGeo<FMT, NMAX>;
   using Cur = WCursor<Geo::kKS>;
   constexpr int DW = Geo::kDW, DB = Geo::kDB, DA = Geo::kDA > 0 ? Geo::kDA : 1;
-  constexpr int kConv = 8;  // converter warps per group (int8)
+  constexpr int kConv = Geo::kConv;  // converter warps per group (int8)
   constexpr int NG = Geo::kConvGroups > 0 ? Geo::kConvGroups : 1;
   constexpr int NB = Geo::kBufs;
   extern __shared__ unsigned char smem_raw[];
@@ -307,7 +316,10 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
           break;
         }
         mbar_expect_tx(wfull + 8 * s, Geo::kW);
-        tma_load_2d(ring + s * Geo::kW, &a.seg[c.seg].wmap, c.kabs, c.row0, wfull + 8 * s, pol);
+#pragma unroll
+        for (int b = 0; b < Geo::kWBoxes; ++b)  // int8: 128 K per copy
+          tma_load_2d(ring + s * Geo::kW + b * (kTM * 128), &a.seg[c.seg].wmap, c.kabs + 128 * b, c.row0,
+                      wfull + 8 * s, pol);
         c.next(a);
         ++i;
       }
@@ -447,10 +459,10 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
   } else if (FMT == 1 && wid >= 8) {
     // ------------------------------------------------------------ int8 codes -> fp16 A operand in tensor memory
     const int cw = wid - 8;
-    const int grp = cw >> 3;                    // this group converts the stages i with i mod NG == grp
+    const int grp = cw / kConv;                 // this group converts the stages i with i mod NG == grp
     const int quarter = cw & 3;                 // = wid mod 4: the lane group this warp reaches
     const int r = quarter * 32 + lane;          // weight row within the block
-    const int hk = (cw >> 2) & 1;               // 64-K half of the stage: one quantisation group, one atom
+    const int hk = (cw >> 2) % (kConv / 4);     // 64 K of the stage: one quantisation group, one atom
     Cur c;
     c.start(a);
     for (int g = 0; g < grp; ++g) c.next(a);
@@ -473,11 +485,12 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
         ok = false;
         break;
       }
-      // 128-byte code rows under the 128-byte swizzle: piece p (16 codes) of row r at p ^ (r mod 8)
-      const uint32_t crow = ring + sw * Geo::kW + r * 128;
+      // 128-byte code rows (128 K per copy) under the 128-byte swizzle: piece p (16 codes)
+      // of row r at p ^ (r mod 8); this warp's 64 K are pieces 4 (hk mod 2) .. + 3 of copy hk / 2
+      const uint32_t crow = ring + sw * Geo::kW + (hk >> 1) * (kTM * 128) + r * 128;
       uint4 w[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = lds128(crow + (((4 * hk + j) ^ (r & 7)) << 4));
+      for (int j = 0; j < 4; ++j) w[j] = lds128(crow + (((4 * (hk & 1) + j) ^ (r & 7)) << 4));
       // the products that read this A slot last (stage i - DA) are done
       if (i >= DA && !mbar_wait(aempty + 8 * sa, static_cast<uint32_t>(((i / DA) + 1) & 1))) {
         ok = false;
@@ -535,12 +548,14 @@ cudaError_t launch_fmt(const GemvArgs& a, int ctas, bool pdl, cudaStream_t st) {
   return launch_ex(wide_kernel<FMT, NMAX>, dim3(ctas), dim3(WideGeo<FMT, NMAX>::kWarps * 32), smem, st, pdl, a);
 }
 
-int ks_of(int fmt) { return fmt == 0 ? stage_k<0>() : stage_k<1>(); }
+int ks_of(int fmt, int nmax) {
+  return fmt == 0 ? stage_k<0, 128>() : (nmax <= 128 ? stage_k<1, 128>() : stage_k<1, 256>());
+}
 
 }  // namespace
 
-int wide_plan(GemvArgs& a, int num_sms, int fmt) {
-  a.stage_k = ks_of(fmt);
+int wide_plan(GemvArgs& a, int num_sms, int fmt, int nmax) {
+  a.stage_k = ks_of(fmt, nmax);
   long long T = 0;
   for (int i = 0; i < a.nseg; ++i) {
     GemvSeg& sg = a.seg[i];
@@ -551,7 +566,8 @@ int wide_plan(GemvArgs& a, int num_sms, int fmt) {
   // one run of stages per CTA, at least kMinStages long: a small launch on fewer
   // CTAs pays fewer prologues and leaves fewer partial planes to add
   long long C = static_cast<long long>(num_sms) * ctas_per_sm(fmt);
-  const long long Cmin = (T + kMinStages - 1) / kMinStages;
+  const long long min_run = fmt == 1 ? kMinStages * 128 / a.stage_k : kMinStages;  // the same bytes per CTA
+  const long long Cmin = (T + min_run - 1) / min_run;
   if (Cmin < C) C = Cmin;
   return static_cast<int>(C < T ? C : (T > 0 ? T : 1));
 }
@@ -577,7 +593,7 @@ int wide_max_planes(const GemvArgs& a, int i, int C) {
 }
 
 bool wide_encode_wmap(CUtensorMap* map, const void* w, int M, int K, int fmt) {
-  if (M % kTM || K % ks_of(fmt)) return false;
+  if (M % kTM || K % 128) return false;
   if (fmt == 0)
     return tma_encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, K, M, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B);
   return tma_encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, K, M, 128, kTM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -590,8 +606,17 @@ bool wide_encode_xmap(CUtensorMap* map, const void* x, int rows, int K, int fmt)
                        rows, kAtomK, nm, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+int wide_nmax(const GemvArgs& a) {
+  int nmax = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    const int nm = (a.seg[i].n_tiles * 8 + 15) & ~15;
+    nmax = nm > nmax ? nm : nmax;
+  }
+  return nmax <= 128 ? 128 : 256;
+}
+
 cudaError_t launch_wide(GemvArgs& a, int fmt, int num_sms, bool pdl, cudaStream_t st) {
-  const int ks = ks_of(fmt);
+  const int ks = ks_of(fmt, wide_nmax(a));
   int nmax = 0;
   for (int i = 0; i < a.nseg; ++i) {
     const GemvSeg& sg = a.seg[i];
@@ -601,7 +626,7 @@ cudaError_t launch_wide(GemvArgs& a, int fmt, int num_sms, bool pdl, cudaStream_
     if (sg.xt != nullptr && (sg.xt_rows < nm || (reinterpret_cast<uintptr_t>(sg.xt) & 15u))) return cudaErrorInvalidValue;
     nmax = nm > nmax ? nm : nmax;
   }
-  const int C = wide_plan(a, num_sms, fmt);
+  const int C = wide_plan(a, num_sms, fmt, nmax <= 128 ? 128 : 256);
   if (a.total_stages < 1) return cudaErrorInvalidValue;
   if (fmt == 0) return nmax <= 128 ? launch_fmt<0, 128>(a, C, pdl, st) : launch_fmt<0, 256>(a, C, pdl, st);
   return nmax <= 128 ? launch_fmt<1, 128>(a, C, pdl, st) : launch_fmt<1, 256>(a, C, pdl, st);
