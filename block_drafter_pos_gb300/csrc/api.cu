@@ -221,13 +221,18 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
   // blocks of 128 rows: the delta projections' hidden/4 and the vocabulary
   if (max_requests * c.block >= wide_min_rows(fmt) && ((c.hidden / 4) % 128 || c.vocab % 128))
     return DFLASH2_E_UNSUPPORTED;
-  if (!w->embed || !w->lm_head || !w->hidden_norm || !w->final_norm || !aligned16(w->lm_head)) return DFLASH2_E_INVAL;
+  // norm weights and convolution bases are read 4 channels (8 bytes) at a time
+  if (!w->embed || !w->lm_head || !w->hidden_norm || !w->final_norm || !aligned16(w->lm_head) ||
+      !aligned16(w->hidden_norm) || !aligned16(w->final_norm))
+    return DFLASH2_E_INVAL;
   if (!valid_matrix(w->fc, fmt) || !valid_matrix(w->sel_proj, fmt) || !valid_matrix(w->cb_a, fmt) ||
       !valid_matrix(w->cb_b, fmt))
     return DFLASH2_E_INVAL;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& L = w->layers[l];
     if (!L.input_norm || !L.post_norm || !L.q_norm || !L.k_norm || !L.attn_base || !L.mlp_base) return DFLASH2_E_INVAL;
+    if (!aligned16(L.input_norm) || !aligned16(L.post_norm) || !aligned16(L.attn_base) || !aligned16(L.mlp_base))
+      return DFLASH2_E_INVAL;
     const dflash2_matrix* ms[] = {&L.q, &L.k, &L.v, &L.o, &L.gate, &L.up, &L.down, &L.attn_delta, &L.mlp_delta};
     for (const dflash2_matrix* m : ms)
       if (!valid_matrix(*m, fmt)) return DFLASH2_E_INVAL;

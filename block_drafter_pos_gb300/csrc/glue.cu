@@ -59,20 +59,77 @@ DF2_DEV float plane_sum(const float* p, size_t plane, int S) {
   return S <= 8 ? plane_sum_b<8>(p, plane, S) : plane_sum_b<32>(p, plane, S);
 }
 
-// The plane count of the weight block holding this CTA's 32 channels (c0 = the
-// first): every channel of a 32-channel chunk lies in one block (64 or 128 rows),
-// so it is evaluated once per CTA, by thread 0, not per thread (its divisions
-// dominated the element-wise kernels at many requests).  Ends with a barrier.
-DF2_DEV int cta_plane_count(const GemvPlanes& pl, int c0, int* sh) {
-  if (threadIdx.x == 0) *sh = gemv_plane_count(pl, c0);
-  __syncthreads();
-  return *sh;
-}
-
 // Per-row sum of squares of this CTA's 32 channels -> ss[row][blockIdx.y] (one warp = one row).
 DF2_DEV void emit_ss(float v, int row, float* ss, int nch) {
   const float s = warp_sum(v * v);
   if ((threadIdx.x & 31) == 0) ss[static_cast<size_t>(row) * nch + blockIdx.y] = s;
+}
+
+// The channel kernels after the projections take 4 channels per thread, 128 per CTA
+// (one row per warp), with 16-byte loads and 8-byte stores: at many requests these
+// kernels are bound by instruction issue, not by their bytes.
+constexpr int kV = 4;
+constexpr int kCv = kCw * kV;
+
+DF2_DEV float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+DF2_DEV float4 ld_bf16x4(const uint16_t* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+DF2_DEV float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+DF2_DEV float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+DF2_DEV float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
+
+// Sum of the split planes p[s * plane] of 4 channels, s = 0..S-1, added in split order
+// (the same order, per channel, as plane_sum); up to 8 planes' loads in flight.
+DF2_DEV float4 plane_sum4(const float* p, size_t plane, int S) {
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float4 t[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = (s0 + j < S) ? ld4(p + static_cast<size_t>(s0 + j) * plane) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y = add4(y, t[j]);
+  }
+  return y;
+}
+
+// Four consecutive activations (col a multiple of 4: contiguous in both layouts of
+// act_offset) as 16-bit values, one 8-byte store per plane.
+DF2_DEV void put_act4(void* act, size_t lo, int fmt, size_t idx, float4 v) {
+  uint2 hi, low;
+  if (fmt == 0) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+    hi = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    if (lo) {
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y),
+                           l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+      low = make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+    }
+  } else {
+    const __half2 h0 = __floats2half2_rn(v.x, v.y), h1 = __floats2half2_rn(v.z, v.w);
+    hi = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+    if (lo) {
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      const __half2 l0 = __floats2half2_rn(v.x - f0.x, v.y - f0.y), l1 = __floats2half2_rn(v.z - f1.x, v.w - f1.y);
+      low = make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
+    }
+  }
+  uint16_t* p = reinterpret_cast<uint16_t*>(act);
+  *reinterpret_cast<uint2*>(p + idx) = hi;
+  if (lo) *reinterpret_cast<uint2*>(p + lo + idx) = low;
+}
+
+// Per-row sums of squares of 32-channel chunks (8 lanes x 4 channels each) ->
+// ss[row][c / 32]: each lane's 4 squares in order, then a fixed shuffle tree.
+DF2_DEV void emit_ss4(float4 v, int row, float* ss, int nch, int c) {
+  float s = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  if ((threadIdx.x & 7) == 0) ss[static_cast<size_t>(row) * nch + (c >> 5)] = s;
 }
 
 // ------------------------------------------------------------------ start of the step
@@ -113,74 +170,66 @@ __global__ void __launch_bounds__(kThreads) start_kernel(const StartArgs a) {
 // c = y * w_hidden_norm into the context rows of the QKV input (1/rms of y is
 // applied after the K/V projection); ss of y.
 DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
-  __shared__ int np_sh;
+  __shared__ int np_sh[2];
+  const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
-  const int c = blockIdx.y * kCw + (threadIdx.x & 31);
-  const int np = cta_plane_count(a.pl, blockIdx.y * kCw, &np_sh);
-  const float y = plane_sum(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, np);
-  put_act(a.act, a.act_lo, a.fmt, act_offset(a.act_row0 + row, c, a.H, a.tiled), y * bf16_to_f32(a.norm_w[c]));
-  emit_ss(y, row, a.ss, a.nch);
+  const int c = blockIdx.y * kCv + kV * lane;
+  if (threadIdx.x < 2) np_sh[threadIdx.x] = gemv_plane_count(a.pl, blockIdx.y * kCv + 64 * threadIdx.x);
+  __syncthreads();
+  const float4 w = ld_bf16x4(a.norm_w + c);
+  const float4 y =
+      plane_sum4(a.y + static_cast<size_t>(row) * a.H + c, static_cast<size_t>(a.n_rows) * a.H, np_sh[lane >> 4]);
+  put_act4(a.act, a.act_lo, a.fmt, act_offset(a.act_row0 + row, c, a.H, a.tiled), mul4(y, w));
+  emit_ss4(y, row, a.ss, a.nch, c);
 }
 
 // ------------------------------------------------------------------ conv before a sublayer
 // r_i = 1/rms(x_i); delta = r_i * (W_delta (x_i * w)) for all four (io, tap) rows;
 // a_i = r_i x_i w;  a'_i = (b0 + d0_i) a_i + (b1 + d1_i) a_{i-1}.
 DF2_DEV void conv_in_body(const ConvInArgs& a) {
-  __shared__ float ash[kB][kCw];
-  __shared__ int np_sh[8];
+  __shared__ float4 ash[kB][kCw];
+  __shared__ int np_sh[4];
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
-  const int c = blockIdx.y * kCw + lane;
+  const int c = blockIdx.y * kCv + kV * lane;
   const int G = a.H / 16;
-  // plane counts of the CTA's 8 delta values (io, tap, local group), once per CTA
-  if (threadIdx.x < 8) {
-    const int e = threadIdx.x;
-    np_sh[e] = gemv_plane_count(a.pl, ((e >> 2) * 2 + ((e >> 1) & 1)) * G + blockIdx.y * 2 + (e & 1));
-  }
+  // the CTA's 128 channels are 8 groups: plane counts of the (io, tap) rows of those
+  // groups (8 consecutive rows each, inside one weight block), once per CTA
+  if (threadIdx.x < 4) np_sh[threadIdx.x] = gemv_plane_count(a.pl, threadIdx.x * G + blockIdx.y * 8);
   __syncthreads();
   // loads independent of the planes and of 1/rms first: one round of latency
   const size_t idx = static_cast<size_t>(row) * a.H + c;
-  const float x0 = a.x[idx], w = bf16_to_f32(a.norm_w[c]);
-  const float b0 = bf16_to_f32(a.base[c]), b1 = bf16_to_f32(a.base[a.H + c]);
-  // the (io, tap, local group) delta values of this row and the CTA's 2 groups: value
-  // e = lane & 7, its split planes pg, pg + 4, ... summed by lane e + 8 pg, then the
-  // four partial sums combined in a fixed tree (lanes 0..7 end with the total)
-  float dv;
-  float rr;
+  const float4 x0 = ld4(a.x + idx), w = ld_bf16x4(a.norm_w + c);
+  const float4 b0 = ld_bf16x4(a.base + c), b1 = ld_bf16x4(a.base + a.H + c);
+  // lane e holds delta value e of the row: (io, tap) = e / 8, local group e % 8
+  float dv, rr;
   {
-    const int e = lane & 7, pg = lane >> 3;
-    const int io = e >> 2, t = (e >> 1) & 1, gl = e & 1;
-    const int gidx = (io * 2 + t) * G + blockIdx.y * 2 + gl;
-    const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
-    const float* p = a.dproj + static_cast<size_t>(row) * (4 * G) + gidx;
-    const int np = np_sh[e];
-    float part = 0.f;
-    for (int s0 = pg; s0 < np; s0 += 32) {
-      float tt[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) tt[j] = (s0 + 4 * j < np) ? p[static_cast<size_t>(s0 + 4 * j) * plane] : 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) part += tt[j];
-    }
-    part += __shfl_xor_sync(0xffffffffu, part, 8);
-    part += __shfl_xor_sync(0xffffffffu, part, 16);
+    const int it = lane >> 3, gl = lane & 7;
+    const int gidx = it * G + blockIdx.y * 8 + gl;
+    const float part = plane_sum(a.dproj + static_cast<size_t>(row) * (4 * G) + gidx,
+                                 static_cast<size_t>(a.n_rows) * (4 * G), np_sh[it]);
     rr = warp_inv_rms(a.ss, row, a.nch, a.H, a.eps);
     dv = part * rr;
-    if (lane < 8) a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
+    a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
   }
-  const int gl = lane >> 4;
-  const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 2 + gl);
-  const float ai = x0 * rr * w;
+  const int gl = lane >> 2;  // this lane's 4 channels: local group lane / 4
+  const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 8 + gl);
+  const float4 ai = mul4(scale4(x0, rr), w);
   ash[i][lane] = ai;
   // a tile that starts inside a block (B = 16): its first row's predecessor, from global
-  float prev0 = 0.f;
+  float4 prev0 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (i == 0 && row % a.B != 0) {
     const float rp = warp_inv_rms(a.ss, row - 1, a.nch, a.H, a.eps);
-    prev0 = a.x[idx - a.H] * rp * w;
+    prev0 = mul4(scale4(ld4(a.x + idx - a.H), rp), w);
   }
   __syncthreads();
-  const float prev = i > 0 ? ash[i - 1][lane] : prev0;
-  put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), (b0 + d0) * ai + (b1 + d1) * prev);
+  const float4 prev = i > 0 ? ash[i - 1][lane] : prev0;
+  float4 o;
+  o.x = (b0.x + d0) * ai.x + (b1.x + d1) * prev.x;
+  o.y = (b0.y + d0) * ai.y + (b1.y + d1) * prev.y;
+  o.z = (b0.z + d0) * ai.z + (b1.z + d1) * prev.z;
+  o.w = (b0.w + d0) * ai.w + (b1.w + d1) * prev.w;
+  put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), o);
 }
 
 __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
@@ -203,67 +252,79 @@ __global__ void __launch_bounds__(kThreads) fc_finish_conv_in_kernel(const FcFin
 // y = sum of split planes; x_i += (b2 + d2_i) y_i + (b3 + d3_i) y_{i-1} (the
 // convolution wrapping the sublayer's output); act = x * w_next; ss of x.
 __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a) {
-  __shared__ float ysh[kB][kCw];
-  __shared__ int np_sh;
-  const int np = cta_plane_count(a.pl, blockIdx.y * kCw, &np_sh);  // before the wait: shapes only
+  __shared__ float4 ysh[kB][kCw];
+  __shared__ int np_sh[2];
+  if (threadIdx.x < 2) np_sh[threadIdx.x] = gemv_plane_count(a.pl, blockIdx.y * kCv + 64 * threadIdx.x);  // shapes only
+  __syncthreads();
   pdl_begin_early();  // followed by a weight launch
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
-  const int c = blockIdx.y * kCw + lane;
+  const int c = blockIdx.y * kCv + kV * lane;
   const int G = a.H / 16;
   const int g = c >> 4;
   const size_t idx = static_cast<size_t>(row) * a.H + c;
   // every load independent of the planes is issued first: one round of latency
   const float* d = a.delta + static_cast<size_t>(row) * (4 * G);
   const float d2 = d[2 * G + g], d3 = d[3 * G + g];
-  const float b2 = bf16_to_f32(a.base[2 * a.H + c]), b3 = bf16_to_f32(a.base[3 * a.H + c]);
-  const float x0 = a.x[idx];
-  const float w = bf16_to_f32(a.norm_w[c]);
-  const float y = plane_sum(a.part + idx, static_cast<size_t>(a.n_rows) * a.H, np);
+  const float4 b2 = ld_bf16x4(a.base + 2 * a.H + c), b3 = ld_bf16x4(a.base + 3 * a.H + c);
+  const float4 x0 = ld4(a.x + idx);
+  const float4 w = ld_bf16x4(a.norm_w + c);
+  const size_t plane = static_cast<size_t>(a.n_rows) * a.H;
+  const int np = np_sh[lane >> 4];
+  const float4 y = plane_sum4(a.part + idx, plane, np);
   ysh[i][lane] = y;
   // a tile that starts inside a block (B = 16): its first row's predecessor, from global
-  float yp0 = 0.f;
-  if (i == 0 && row % a.B != 0) yp0 = plane_sum(a.part + idx - a.H, static_cast<size_t>(a.n_rows) * a.H, np);
+  float4 yp0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (i == 0 && row % a.B != 0) yp0 = plane_sum4(a.part + idx - a.H, plane, np);
   __syncthreads();
-  const float yprev = i > 0 ? ysh[i - 1][lane] : yp0;
-  const float xv = x0 + (b2 + d2) * y + (b3 + d3) * yprev;
-  a.x[idx] = xv;
-  put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), xv * w);
-  if (a.act2 != nullptr) put_act(a.act2, a.act2_lo, 0, act_offset(row, c, a.H, a.tiled2), xv * w);
-  emit_ss(xv, row, a.ss, a.nch);
+  const float4 yp = i > 0 ? ysh[i - 1][lane] : yp0;
+  float4 xv;
+  xv.x = x0.x + (b2.x + d2) * y.x + (b3.x + d3) * yp.x;
+  xv.y = x0.y + (b2.y + d2) * y.y + (b3.y + d3) * yp.y;
+  xv.z = x0.z + (b2.z + d2) * y.z + (b3.z + d3) * yp.z;
+  xv.w = x0.w + (b2.w + d2) * y.w + (b3.w + d3) * yp.w;
+  *reinterpret_cast<float4*>(a.x + idx) = xv;
+  const float4 act = mul4(xv, w);
+  put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), act);
+  if (a.act2 != nullptr) put_act4(a.act2, a.act2_lo, 0, act_offset(row, c, a.H, a.tiled2), act);
+  emit_ss4(xv, row, a.ss, a.nch, c);
 }
 
 // ------------------------------------------------------------------ SwiGLU
 // h = silu(gate) * up from the split planes of the two projections.
 __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
-  __shared__ int np_sh[2];
-  if (threadIdx.x == 0) {  // before the wait: shapes only
-    np_sh[0] = gemv_plane_count(a.pg, blockIdx.y * kCw);
-    np_sh[1] = gemv_plane_count(a.pu, blockIdx.y * kCw);
-  }
+  __shared__ int np_sh[4];
+  if (threadIdx.x < 4)  // before the wait: shapes only (gate, up) x (channel halves: 64-row GEMV blocks)
+    np_sh[threadIdx.x] = gemv_plane_count(threadIdx.x < 2 ? a.pg : a.pu, blockIdx.y * kCv + 64 * (threadIdx.x & 1));
   __syncthreads();
   pdl_begin_early();  // followed by a weight launch
+  const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + (threadIdx.x >> 5);
-  const int c = blockIdx.y * kCw + (threadIdx.x & 31);
+  const int c = blockIdx.y * kCv + kV * lane;
   const size_t idx = static_cast<size_t>(row) * a.F + c;
   const size_t plane = static_cast<size_t>(a.n_rows) * a.F;
   // the gate and up planes' loads all in flight together, each added in split order
-  const int ng = np_sh[0], nu = np_sh[1];
-  float gs = 0.f, us = 0.f;
-  for (int s0 = 0; s0 < (ng > nu ? ng : nu); s0 += 8) {
-    float tg[8], tu[8];
+  const int ng = np_sh[lane >> 4], nu = np_sh[2 + (lane >> 4)];
+  float4 gs = make_float4(0.f, 0.f, 0.f, 0.f), us = gs;
+  for (int s0 = 0; s0 < (ng > nu ? ng : nu); s0 += 4) {
+    float4 tg[4], tu[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      tg[j] = (s0 + j < ng) ? a.part_g[idx + static_cast<size_t>(s0 + j) * plane] : 0.f;
-      tu[j] = (s0 + j < nu) ? a.part_u[idx + static_cast<size_t>(s0 + j) * plane] : 0.f;
+    for (int j = 0; j < 4; ++j) {
+      tg[j] = (s0 + j < ng) ? ld4(a.part_g + idx + static_cast<size_t>(s0 + j) * plane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      tu[j] = (s0 + j < nu) ? ld4(a.part_u + idx + static_cast<size_t>(s0 + j) * plane) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      gs += tg[j];
-      us += tu[j];
+    for (int j = 0; j < 4; ++j) {
+      gs = add4(gs, tg[j]);
+      us = add4(us, tu[j]);
     }
   }
-  put_act(a.act, a.act_lo, a.fmt, act_offset(row, c, a.F, a.tiled), gs / (1.f + __expf(-gs)) * us);
+  float4 h;
+  h.x = gs.x / (1.f + __expf(-gs.x)) * us.x;
+  h.y = gs.y / (1.f + __expf(-gs.y)) * us.y;
+  h.z = gs.z / (1.f + __expf(-gs.z)) * us.z;
+  h.w = gs.w / (1.f + __expf(-gs.w)) * us.w;
+  put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.F, a.tiled), h);
 }
 
 // ------------------------------------------------------------------ q/k norm, RoPE, cache append
@@ -417,19 +478,20 @@ cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t s
 }
 cudaError_t launch_fc_finish_conv_in(const FcFinishArgs& f, const ConvInArgs& c, int n_req, bool pdl, cudaStream_t st) {
   if (f.H != c.H || f.n_rows != c.n_rows || f.n_rows % kB) return cudaErrorInvalidValue;
-  return launch_ex(fc_finish_conv_in_kernel, dim3(f.n_rows / kB, f.H / kCw, 2), dim3(kThreads), 0, st, pdl, f, c);
+  if (f.H % kCv) return cudaErrorInvalidValue;
+  return launch_ex(fc_finish_conv_in_kernel, dim3(f.n_rows / kB, f.H / kCv, 2), dim3(kThreads), 0, st, pdl, f, c);
 }
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  if (a.n_rows % kB) return cudaErrorInvalidValue;
-  return launch_ex(conv_in_kernel, dim3(a.n_rows / kB, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
+  if (a.n_rows % kB || a.H % kCv) return cudaErrorInvalidValue;
+  return launch_ex(conv_in_kernel, dim3(a.n_rows / kB, a.H / kCv), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  if (a.n_rows % kB) return cudaErrorInvalidValue;
-  return launch_ex(conv_out_kernel, dim3(a.n_rows / kB, a.H / kCw), dim3(kThreads), 0, st, pdl, a);
+  if (a.n_rows % kB || a.H % kCv) return cudaErrorInvalidValue;
+  return launch_ex(conv_out_kernel, dim3(a.n_rows / kB, a.H / kCv), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_swiglu(const SwigluArgs& a, int n_req, bool pdl, cudaStream_t st) {
-  if (a.n_rows % kB) return cudaErrorInvalidValue;
-  return launch_ex(swiglu_kernel, dim3(a.n_rows / kB, a.F / kCw), dim3(kThreads), 0, st, pdl, a);
+  if (a.n_rows % kB || a.F % kCv) return cudaErrorInvalidValue;
+  return launch_ex(swiglu_kernel, dim3(a.n_rows / kB, a.F / kCv), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_qkv_finish(const QkvFinishArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if ((a.B != 8 && a.B != 16) || a.n_rows != a.B * n_req) return cudaErrorInvalidValue;

@@ -145,9 +145,10 @@ typedef struct dflash2_handle dflash2_handle;
  * when max_requests * block reaches 40 (BF16) or 32 (Q8G64) rows, hidden / 4 or
  * vocab not a multiple of 128: calls with that many block rows run every
  * projection on the tensor-core GEMM, in 128-row weight blocks.  Every weight
- * matrix, Q8 scale and Q8 bias must start on a 16-byte boundary
- * (DFLASH2_E_INVAL otherwise).  Encodes one bulk-copy descriptor per projection
- * matrix, so the weights must not move while the handle lives. */
+ * matrix, Q8 scale and Q8 bias, and every norm weight and convolution base except
+ * q_norm and k_norm, must start on a 16-byte boundary (DFLASH2_E_INVAL
+ * otherwise).  Encodes one bulk-copy descriptor per projection matrix, so the
+ * weights must not move while the handle lives. */
 dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* w, int32_t max_requests,
                               int32_t kv_capacity, dflash2_handle** out);
 
