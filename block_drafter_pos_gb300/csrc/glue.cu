@@ -122,6 +122,44 @@ DF2_DEV void put_act4(void* act, size_t lo, int fmt, size_t idx, float4 v) {
   if (lo) *reinterpret_cast<uint2*>(p + lo + idx) = low;
 }
 
+// V = 2 or 4 consecutive values (16- or 8-byte aligned).
+template <int V>
+DF2_DEV void ld_f32v(const float* p, float (&v)[V]) {
+  if constexpr (V == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x, v[1] = t.y;
+  }
+}
+template <int V>
+DF2_DEV void st_f32v(float* p, const float (&v)[V]) {
+  if constexpr (V == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+}
+template <int V>
+DF2_DEV void ld_bf16v(const uint16_t* p, float (&v)[V]) {
+  if constexpr (V == 4) {
+    const float4 t = ld_bf16x4(p);
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    v[0] = __uint_as_float(u << 16), v[1] = __uint_as_float(u & 0xFFFF0000u);
+  }
+}
+template <int V>
+DF2_DEV void put_actv(void* act, size_t lo, int fmt, size_t idx, const float (&v)[V]) {
+  if constexpr (V == 4) {
+    put_act4(act, lo, fmt, idx, make_float4(v[0], v[1], v[2], v[3]));
+  } else {
+    put_act(act, lo, fmt, idx, v[0]);
+    put_act(act, lo, fmt, idx + 1, v[1]);
+  }
+}
+
 // Per-row sums of squares of 32-channel chunks (8 lanes x 4 channels each) ->
 // ss[row][c / 32]: each lane's 4 squares in order, then a fixed shuffle tree.
 DF2_DEV void emit_ss4(float4 v, int row, float* ss, int nch, int c) {
@@ -186,66 +224,102 @@ DF2_DEV void fc_finish_body(const FcFinishArgs& a) {
 // ------------------------------------------------------------------ conv before a sublayer
 // r_i = 1/rms(x_i); delta = r_i * (W_delta (x_i * w)) for all four (io, tap) rows;
 // a_i = r_i x_i w;  a'_i = (b0 + d0_i) a_i + (b1 + d1_i) a_{i-1}.
+// 32 V channels per CTA (V per thread): a row's 8 V dynamic coefficients of the CTA's
+// 2 V groups are summed over their split planes by 4 / V lanes each (planes split by
+// residue), so with few block rows (V = 2, about 15 planes a coefficient at one
+// request) one round of plane loads suffices, and with many (V = 4) the kernel issues
+// a quarter of the one-channel kernel's instructions.
+template <int V>
 DF2_DEV void conv_in_body(const ConvInArgs& a) {
-  __shared__ float4 ash[kB][kCw];
+  constexpr int kCta = kCw * V;     // channels per CTA
+  constexpr int kVals = 8 * V;      // coefficients per row: (io, tap) x local group
+  constexpr int kSplit = 32 / kVals;  // lanes per coefficient
+  __shared__ __align__(16) float ash[kB][kCta];
   __shared__ int np_sh[4];
   const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kB + i;
-  const int c = blockIdx.y * kCv + kV * lane;
+  const int c = blockIdx.y * kCta + V * lane;
   const int G = a.H / 16;
-  // the CTA's 128 channels are 8 groups: plane counts of the (io, tap) rows of those
-  // groups (8 consecutive rows each, inside one weight block), once per CTA
-  if (threadIdx.x < 4) np_sh[threadIdx.x] = gemv_plane_count(a.pl, threadIdx.x * G + blockIdx.y * 8);
+  // plane counts of the (io, tap) rows of the CTA's groups (2 V consecutive rows each,
+  // inside one weight block), once per CTA
+  if (threadIdx.x < 4) np_sh[threadIdx.x] = gemv_plane_count(a.pl, threadIdx.x * G + blockIdx.y * 2 * V);
   __syncthreads();
   // loads independent of the planes and of 1/rms first: one round of latency
   const size_t idx = static_cast<size_t>(row) * a.H + c;
-  const float4 x0 = ld4(a.x + idx), w = ld_bf16x4(a.norm_w + c);
-  const float4 b0 = ld_bf16x4(a.base + c), b1 = ld_bf16x4(a.base + a.H + c);
-  // lane e holds delta value e of the row: (io, tap) = e / 8, local group e % 8
+  float x0[V], w[V], b0[V], b1[V];
+  ld_f32v<V>(a.x + idx, x0);
+  ld_bf16v<V>(a.norm_w + c, w);
+  ld_bf16v<V>(a.base + c, b0);
+  ld_bf16v<V>(a.base + a.H + c, b1);
   float dv, rr;
   {
-    const int it = lane >> 3, gl = lane & 7;
-    const int gidx = it * G + blockIdx.y * 8 + gl;
-    const float part = plane_sum(a.dproj + static_cast<size_t>(row) * (4 * G) + gidx,
-                                 static_cast<size_t>(a.n_rows) * (4 * G), np_sh[it]);
+    const int e = lane % kVals, part_id = lane / kVals;
+    const int it = e / (2 * V), gl = e % (2 * V);
+    const int gidx = it * G + blockIdx.y * 2 * V + gl;
+    const size_t plane = static_cast<size_t>(a.n_rows) * (4 * G);
+    const float* p = a.dproj + static_cast<size_t>(row) * (4 * G) + gidx;
+    const int np = np_sh[it];
+    float part = 0.f;
+    for (int s0 = part_id; s0 < np; s0 += 16 * kSplit) {  // 16 planes' loads in flight, added in order
+      float t[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        t[j] = (s0 + kSplit * j < np) ? p[static_cast<size_t>(s0 + kSplit * j) * plane] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) part += t[j];
+    }
+#pragma unroll
+    for (int o = kVals; o < 32; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     rr = warp_inv_rms(a.ss, row, a.nch, a.H, a.eps);
     dv = part * rr;
-    a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
+    if (part_id == 0) a.delta[static_cast<size_t>(row) * (4 * G) + gidx] = dv;
   }
-  const int gl = lane >> 2;  // this lane's 4 channels: local group lane / 4
-  const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 8 + gl);
-  const float4 ai = mul4(scale4(x0, rr), w);
-  ash[i][lane] = ai;
+  const int gl = (V * lane) >> 4;  // local group of this lane's channels
+  const float d0 = __shfl_sync(0xffffffffu, dv, gl), d1 = __shfl_sync(0xffffffffu, dv, 2 * V + gl);
+  float ai[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) ai[k] = x0[k] * rr * w[k];
+  st_f32v<V>(&ash[i][V * lane], ai);
   // a tile that starts inside a block (B = 16): its first row's predecessor, from global
-  float4 prev0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float prev0[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) prev0[k] = 0.f;
   if (i == 0 && row % a.B != 0) {
     const float rp = warp_inv_rms(a.ss, row - 1, a.nch, a.H, a.eps);
-    prev0 = mul4(scale4(ld4(a.x + idx - a.H), rp), w);
+    float xp[V];
+    ld_f32v<V>(a.x + idx - a.H, xp);
+#pragma unroll
+    for (int k = 0; k < V; ++k) prev0[k] = xp[k] * rp * w[k];
   }
   __syncthreads();
-  const float4 prev = i > 0 ? ash[i - 1][lane] : prev0;
-  float4 o;
-  o.x = (b0.x + d0) * ai.x + (b1.x + d1) * prev.x;
-  o.y = (b0.y + d0) * ai.y + (b1.y + d1) * prev.y;
-  o.z = (b0.z + d0) * ai.z + (b1.z + d1) * prev.z;
-  o.w = (b0.w + d0) * ai.w + (b1.w + d1) * prev.w;
-  put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), o);
+  float prev[V], o[V];
+  if (i > 0) ld_f32v<V>(&ash[i - 1][V * lane], prev);
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    if (i == 0) prev[k] = prev0[k];
+    o[k] = (b0[k] + d0) * ai[k] + (b1[k] + d1) * prev[k];
+  }
+  put_actv<V>(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), o);
 }
 
+template <int V>
 __global__ void __launch_bounds__(kThreads) conv_in_kernel(const ConvInArgs a) {
   pdl_begin_early();  // followed by a weight launch
-  conv_in_body(a);
+  conv_in_body<V>(a);
 }
 
 // First layer: the taps-projection finish and the conv before the attention
 // sublayer read different inputs and write different outputs, so they share one
-// launch (blockIdx.z selects the role).
+// launch (blockIdx.z selects the role; the grid is the conv's, 32 V channels per
+// CTA, of which the finish's 128-channel CTAs take the first H / 128).
+template <int V>
 __global__ void __launch_bounds__(kThreads) fc_finish_conv_in_kernel(const FcFinishArgs f, const ConvInArgs c) {
   pdl_begin_early();  // followed by a weight launch
-  if (blockIdx.z == 0)
-    fc_finish_body(f);
-  else
-    conv_in_body(c);
+  if (blockIdx.z == 0) {
+    if (static_cast<int>(blockIdx.y) < f.H / kCv) fc_finish_body(f);
+  } else {
+    conv_in_body<V>(c);
+  }
 }
 
 // ------------------------------------------------------------------ conv after a sublayer + residual
@@ -460,6 +534,11 @@ __global__ void __launch_bounds__(32) block_width_kernel(const BlockWidthArgs a,
 
 }  // namespace
 
+// Channels per thread of the conv-in: 2 with few block rows (one round of coefficient
+// plane loads; measured 18 us a step faster at one request), 4 with many (fewer
+// instructions; 34 us faster at 16 requests).
+int conv_in_v(int n_rows) { return n_rows >= 32 ? 4 : 2; }
+
 cudaError_t launch_block_width(const BlockWidthArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if ((a.B != 8 && a.B != 16) || a.narrow < 2 || a.narrow > a.B) return cudaErrorInvalidValue;
   return launch_ex(block_width_kernel, dim3((n_req + 31) / 32), dim3(32), 0, st, pdl, a, n_req);
@@ -479,11 +558,15 @@ cudaError_t launch_start(const StartArgs& a, int n_req, bool pdl, cudaStream_t s
 cudaError_t launch_fc_finish_conv_in(const FcFinishArgs& f, const ConvInArgs& c, int n_req, bool pdl, cudaStream_t st) {
   if (f.H != c.H || f.n_rows != c.n_rows || f.n_rows % kB) return cudaErrorInvalidValue;
   if (f.H % kCv) return cudaErrorInvalidValue;
-  return launch_ex(fc_finish_conv_in_kernel, dim3(f.n_rows / kB, f.H / kCv, 2), dim3(kThreads), 0, st, pdl, f, c);
+  if (conv_in_v(c.n_rows) == 4)
+    return launch_ex(fc_finish_conv_in_kernel<4>, dim3(f.n_rows / kB, f.H / kCv, 2), dim3(kThreads), 0, st, pdl, f, c);
+  return launch_ex(fc_finish_conv_in_kernel<2>, dim3(f.n_rows / kB, f.H / 64, 2), dim3(kThreads), 0, st, pdl, f, c);
 }
 cudaError_t launch_conv_in(const ConvInArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if (a.n_rows % kB || a.H % kCv) return cudaErrorInvalidValue;
-  return launch_ex(conv_in_kernel, dim3(a.n_rows / kB, a.H / kCv), dim3(kThreads), 0, st, pdl, a);
+  if (conv_in_v(a.n_rows) == 4)
+    return launch_ex(conv_in_kernel<4>, dim3(a.n_rows / kB, a.H / kCv), dim3(kThreads), 0, st, pdl, a);
+  return launch_ex(conv_in_kernel<2>, dim3(a.n_rows / kB, a.H / 64), dim3(kThreads), 0, st, pdl, a);
 }
 cudaError_t launch_conv_out(const ConvOutArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if (a.n_rows % kB || a.H % kCv) return cudaErrorInvalidValue;
