@@ -15,6 +15,7 @@
 // statistics cross CTAs only through those partial sums, read in a fixed order
 // (bit-reproducible).
 #include "common.cuh"
+#include "elementwise.cuh"
 #include "glue.h"
 #include "internal.h"
 
@@ -22,23 +23,11 @@ namespace df2 {
 
 namespace {
 
+using namespace ew;
+
 constexpr int kB = 8;       // rows per tile (one CTA of the channel kernels)
 constexpr int kCw = 32;     // channels per CTA of the channel kernels: warp i = tile row i, lane = channel
 constexpr int kThreads = kB * kCw;
-
-DF2_DEV void put_act(void* act, size_t lo, int fmt, size_t idx, float v) {
-  if (fmt == 0) {
-    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(act);
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    p[idx] = h;
-    if (lo) p[lo + idx] = __float2bfloat16_rn(v - __bfloat162float(h));
-  } else {
-    __half* p = reinterpret_cast<__half*>(act);
-    const __half h = __float2half_rn(v);
-    p[idx] = h;
-    if (lo) p[lo + idx] = __float2half_rn(v - __half2float(h));
-  }
-}
 
 // Sum of the split planes p[s * plane], s = 0..S-1, added in split order.  The
 // loads of up to B planes are issued together so their latency is paid once.
@@ -70,57 +59,6 @@ DF2_DEV void emit_ss(float v, int row, float* ss, int nch) {
 // kernels are bound by instruction issue, not by their bytes.
 constexpr int kV = 4;
 constexpr int kCv = kCw * kV;
-
-DF2_DEV float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-DF2_DEV float4 ld_bf16x4(const uint16_t* p) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                     __uint_as_float(u.y & 0xFFFF0000u));
-}
-DF2_DEV float4 add4(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
-DF2_DEV float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
-DF2_DEV float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
-
-// Sum of the split planes p[s * plane] of 4 channels, s = 0..S-1, added in split order
-// (the same order, per channel, as plane_sum); up to 8 planes' loads in flight.
-DF2_DEV float4 plane_sum4(const float* p, size_t plane, int S) {
-  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < S; s0 += 8) {
-    float4 t[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) t[j] = (s0 + j < S) ? ld4(p + static_cast<size_t>(s0 + j) * plane) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) y = add4(y, t[j]);
-  }
-  return y;
-}
-
-// Four consecutive activations (col a multiple of 4: contiguous in both layouts of
-// act_offset) as 16-bit values, one 8-byte store per plane.
-DF2_DEV void put_act4(void* act, size_t lo, int fmt, size_t idx, float4 v) {
-  uint2 hi, low;
-  if (fmt == 0) {
-    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
-    hi = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-    if (lo) {
-      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-      const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y),
-                           l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
-      low = make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
-    }
-  } else {
-    const __half2 h0 = __floats2half2_rn(v.x, v.y), h1 = __floats2half2_rn(v.z, v.w);
-    hi = make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-    if (lo) {
-      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-      const __half2 l0 = __floats2half2_rn(v.x - f0.x, v.y - f0.y), l1 = __floats2half2_rn(v.z - f1.x, v.w - f1.y);
-      low = make_uint2(*reinterpret_cast<const uint32_t*>(&l0), *reinterpret_cast<const uint32_t*>(&l1));
-    }
-  }
-  uint16_t* p = reinterpret_cast<uint16_t*>(act);
-  *reinterpret_cast<uint2*>(p + idx) = hi;
-  if (lo) *reinterpret_cast<uint2*>(p + lo + idx) = low;
-}
 
 // V = 2 or 4 consecutive values (16- or 8-byte aligned).
 template <int V>
@@ -158,16 +96,6 @@ DF2_DEV void put_actv(void* act, size_t lo, int fmt, size_t idx, const float (&v
     put_act(act, lo, fmt, idx, v[0]);
     put_act(act, lo, fmt, idx + 1, v[1]);
   }
-}
-
-// Per-row sums of squares of 32-channel chunks (8 lanes x 4 channels each) ->
-// ss[row][c / 32]: each lane's 4 squares in order, then a fixed shuffle tree.
-DF2_DEV void emit_ss4(float4 v, int row, float* ss, int nch, int c) {
-  float s = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-  s += __shfl_xor_sync(0xffffffffu, s, 1);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
-  s += __shfl_xor_sync(0xffffffffu, s, 4);
-  if ((threadIdx.x & 7) == 0) ss[static_cast<size_t>(row) * nch + (c >> 5)] = s;
 }
 
 // ------------------------------------------------------------------ start of the step
@@ -352,11 +280,7 @@ __global__ void __launch_bounds__(kThreads) conv_out_kernel(const ConvOutArgs a)
   if (i == 0 && row % a.B != 0) yp0 = plane_sum4(a.part + idx - a.H, plane, np);
   __syncthreads();
   const float4 yp = i > 0 ? ysh[i - 1][lane] : yp0;
-  float4 xv;
-  xv.x = x0.x + (b2.x + d2) * y.x + (b3.x + d3) * yp.x;
-  xv.y = x0.y + (b2.y + d2) * y.y + (b3.y + d3) * yp.y;
-  xv.z = x0.z + (b2.z + d2) * y.z + (b3.z + d3) * yp.z;
-  xv.w = x0.w + (b2.w + d2) * y.w + (b3.w + d3) * yp.w;
+  const float4 xv = conv_out4(x0, y, yp, b2, b3, d2, d3);
   *reinterpret_cast<float4*>(a.x + idx) = xv;
   const float4 act = mul4(xv, w);
   put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.H, a.tiled), act);
@@ -393,12 +317,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
       us = add4(us, tu[j]);
     }
   }
-  float4 h;
-  h.x = gs.x / (1.f + __expf(-gs.x)) * us.x;
-  h.y = gs.y / (1.f + __expf(-gs.y)) * us.y;
-  h.z = gs.z / (1.f + __expf(-gs.z)) * us.z;
-  h.w = gs.w / (1.f + __expf(-gs.w)) * us.w;
-  put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.F, a.tiled), h);
+  put_act4(a.act, a.act_lo, a.fmt, act_offset(row, c, a.F, a.tiled), swiglu4(gs, us));
 }
 
 // ------------------------------------------------------------------ q/k norm, RoPE, cache append
