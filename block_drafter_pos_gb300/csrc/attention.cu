@@ -9,8 +9,9 @@
 // 64 context keys), plus one CTA for the B block keys; all 4 B queries of a KV
 // head group (4 heads x B positions) are handled together so every key is read
 // once.  A request narrowed to a block width w < B masks its block keys at
-// positions >= w, so its first w rows are exactly a block-w forward.  Keys outside the window are never read.  Context chunks run on the
-// tensor cores (mma.sync m16n8k16 in fp16, fp32 accumulators): the bf16 K/V rows
+// positions >= w, so its first w rows are exactly a block-w forward.  Keys outside
+// the window are never read.  Context chunks run on the tensor cores (mma.sync
+// m16n8k16 in fp16, fp32 accumulators; fragments by ldmatrix): the bf16 K/V rows
 // convert to fp16 exactly inside fp16's normal range (saturated at +-65504 beyond
 // it), queries and probabilities round to fp16 (2^-11 relative).  One product per
 // MMA: a bf16 hi + lo split of queries and probabilities doubled the shared-memory
@@ -54,8 +55,6 @@ struct BlkSmem {
   float p[kQ][B];
 };
 
-DF2_DEV uint32_t ld32(const __half* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
 // Eight bf16 values -> eight fp16 values (exact inside fp16's normal range; saturated
 // at +-65504 beyond it, so no infinity enters the softmax).
 DF2_DEV uint4 bf16x8_to_f16x8(uint4 v) {
@@ -66,6 +65,25 @@ DF2_DEV uint4 bf16x8_to_f16x8(uint4 v) {
     return *reinterpret_cast<uint32_t*>(&h);
   };
   return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
+}
+
+// A fragment of mma m16n8k16 (rows 0..15 x K 0..15 of an fp16 tile whose rows are 16-byte
+// aligned): lane L supplies row (L mod 8) + 8 ((L / 8) mod 2), K offset 8 (L / 16), so
+// the registers are {rows 0-7 K 0-7, rows 8-15 K 0-7, rows 0-7 K 8-15, rows 8-15 K 8-15}.
+DF2_DEV void ldmatrix_a(uint32_t (&r)[4], const __half* row0, int pitch, int lane) {
+  const __half* p = row0 + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 8;
+  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// B fragment (K 0..15 x n 0..7) from an fp16 tile stored n-major ([n][K], rows 16-byte
+// aligned): lane L < 16 supplies row L mod 8, K offset 8 (L / 8).
+DF2_DEV void ldmatrix_b(uint32_t& b0, uint32_t& b1, const __half* row0, int pitch, int lane) {
+  const __half* p = row0 + (lane & 7) * pitch + ((lane >> 3) & 1) * 8;
+  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(addr));
 }
 
 DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* smem_row) {
@@ -159,13 +177,13 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
       float cs[kMT][4] = {};
 #pragma unroll
       for (int ks = 0; ks < kHd / 16; ++ks) {
-        const uint32_t b0 = ld32(&sm.k[nt * 8 + g][ks * 16 + 2 * q]);
-        const uint32_t b1 = ld32(&sm.k[nt * 8 + g][ks * 16 + 8 + 2 * q]);
+        uint32_t b0, b1;
+        ldmatrix_b(b0, b1, &sm.k[nt * 8][ks * 16], kLd, lane);
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt) {
-          const int r0 = mt * 16 + g;
-          mma_f16(cs[mt], ld32(&sm.q[r0][ks * 16 + 2 * q]), ld32(&sm.q[r0 + 8][ks * 16 + 2 * q]),
-                  ld32(&sm.q[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.q[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
+          uint32_t af[4];
+          ldmatrix_a(af, &sm.q[mt * 16][ks * 16], kLd, lane);
+          mma_f16(cs[mt], af[0], af[1], af[2], af[3], b0, b1);
         }
       }
       const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
@@ -216,18 +234,16 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
       }
     }
 #pragma unroll
-    for (int dn = 0; dn < 2; ++dn) {
-      const int nt = wid * 2 + dn;
+    for (int ks = 0; ks < kKeys / 16; ++ks) {
+      uint32_t bv[2][2];
 #pragma unroll
-      for (int ks = 0; ks < kKeys / 16; ++ks) {
-        uint32_t b0, b1;
-        ldmatrix_x2_trans(b0, b1, &sm.v[ks * 16 + (lane & 15)][nt * 8]);
+      for (int dn = 0; dn < 2; ++dn) ldmatrix_x2_trans(bv[dn][0], bv[dn][1], &sm.v[ks * 16 + (lane & 15)][(wid * 2 + dn) * 8]);
 #pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          const int r0 = mt * 16 + g;
-          mma_f16(o[dn][mt], ld32(&sm.p[r0][ks * 16 + 2 * q]), ld32(&sm.p[r0 + 8][ks * 16 + 2 * q]),
-                  ld32(&sm.p[r0][ks * 16 + 8 + 2 * q]), ld32(&sm.p[r0 + 8][ks * 16 + 8 + 2 * q]), b0, b1);
-        }
+      for (int mt = 0; mt < kMT; ++mt) {  // one probability fragment serves both dimension tiles
+        uint32_t af[4];
+        ldmatrix_a(af, &sm.p[mt * 16][ks * 16], kPLd, lane);
+#pragma unroll
+        for (int dn = 0; dn < 2; ++dn) mma_f16(o[dn][mt], af[0], af[1], af[2], af[3], bv[dn][0], bv[dn][1]);
       }
     }
     __syncthreads();  // k, v, p and alpha are rewritten by the next chunk
