@@ -5,19 +5,19 @@
 // position L + i (L = keys in the cache); it sees context key k iff
 // L + i - k < window.  GQA: the 4 query heads of one KV head share its keys.
 //
-// Split over keys (flash-decoding style): one CTA per (request, KV head, chunk of
-// 64 context keys), plus one CTA for the B block keys; all 4 B queries of a KV
-// head group (4 heads x B positions) are handled together so every key is read
-// once.  A request narrowed to a block width w < B masks its block keys at
+// Split over keys (flash-decoding style): one CTA per (request, KV head, part of
+// cpc chunks of 64 context keys), plus one CTA for the B block keys; all 4 B queries
+// of a KV head group (4 heads x B positions) are handled together so every key is
+// read once.  A request narrowed to a block width w < B masks its block keys at
 // positions >= w, so its first w rows are exactly a block-w forward.  Keys outside
 // the window are never read.  Context chunks run on the tensor cores (mma.sync
-// m16n8k16 in fp16, fp32 accumulators; fragments by ldmatrix): the bf16 K/V rows
-// convert to fp16 exactly inside fp16's normal range (saturated at +-65504 beyond
-// it), queries and probabilities round to fp16 (2^-11 relative).  One product per
-// MMA: a bf16 hi + lo split of queries and probabilities doubled the shared-memory
-// fragment loads, which bound the kernel, and bf16 alone (2^-8) is too coarse.
-// The block chunk uses FFMA on the fp32 block keys.  A combine kernel merges the
-// chunk partials (max, sum, unnormalised output) in a fixed order.
+// m16n8k16 in bf16, fp32 accumulators; fragments by ldmatrix): K and V are used as
+// stored (bf16, exact), queries and probabilities as bf16 hi + lo pairs (two products
+// each, ~2^-16 relative), and each warp keeps its scores, probabilities and running
+// softmax in registers.  An earlier version converted every K/V chunk to fp16 so
+// queries and probabilities could be single fp16 products; the conversion was most of
+// its instructions.  The block part uses FFMA on the fp32 block keys.  A combine
+// kernel merges the parts' (max, sum, unnormalised output) in a fixed order.
 #include <math.h>
 
 #include "common.cuh"
@@ -32,19 +32,21 @@ constexpr int kHd = 128;
 constexpr int kKeys = kAttnChunk;
 constexpr int kPartStride = kHd + 2;
 constexpr int kLd = kHd + 8;    // bf16 row pitch (272 B): conflict-free fragment loads
-constexpr int kPLd = kKeys + 8;
 
 // B block positions: kQ = 4 B queries per KV head group (4 heads x B positions),
 // query qi = hr * B + i is head kvh * 4 + hr at block position i.
 template <int B>
 struct CtxSmem {
   static constexpr int kQ = 4 * B;
-  __half q[kQ][kLd];              // scaled queries
-  __half k[kKeys][kLd];
-  __half v[kKeys][kLd];
-  float s[kQ][kKeys + 4];         // scores (log2 units), then probabilities
-  __half p[kQ][kPLd];
-  float alpha[kQ];                // rescale of the running output, per query
+  __nv_bfloat16 qh[kQ][kLd], ql[kQ][kLd];  // scaled queries, bf16 hi and lo parts
+  union {
+    struct {
+      uint16_t k[2][kKeys][kLd];  // bf16 K and V of a chunk, double-buffered
+      uint16_t v[2][kKeys][kLd];
+    };
+    float so[kQ][kHd + 4];        // the merged output of the part (after the last chunk)
+  };
+  float mw[8][16], lw[8][16];     // per warp: running maximum and sum of its 16 query rows
 };
 
 template <int B>
@@ -55,33 +57,21 @@ struct BlkSmem {
   float p[kQ][B];
 };
 
-// Eight bf16 values -> eight fp16 values (exact inside fp16's normal range; saturated
-// at +-65504 beyond it, so no infinity enters the softmax).
-DF2_DEV uint4 bf16x8_to_f16x8(uint4 v) {
-  auto cv = [](uint32_t w) {
-    const float a = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
-    const float b = fminf(fmaxf(__uint_as_float(w & 0xFFFF0000u), -65504.f), 65504.f);
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-  };
-  return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
-}
-
-// A fragment of mma m16n8k16 (rows 0..15 x K 0..15 of an fp16 tile whose rows are 16-byte
+// A fragment of mma m16n8k16 (rows 0..15 x K 0..15 of a 16-bit tile whose rows are 16-byte
 // aligned): lane L supplies row (L mod 8) + 8 ((L / 8) mod 2), K offset 8 (L / 16), so
 // the registers are {rows 0-7 K 0-7, rows 8-15 K 0-7, rows 0-7 K 8-15, rows 8-15 K 8-15}.
-DF2_DEV void ldmatrix_a(uint32_t (&r)[4], const __half* row0, int pitch, int lane) {
-  const __half* p = row0 + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 8;
+DF2_DEV void ldmatrix_a(uint32_t (&r)[4], const void* row0, int pitch, int lane) {
+  const uint16_t* p = static_cast<const uint16_t*>(row0) + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 8;
   const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(p));
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
 
-// B fragment (K 0..15 x n 0..7) from an fp16 tile stored n-major ([n][K], rows 16-byte
+// B fragment (K 0..15 x n 0..7) from a 16-bit tile stored n-major ([n][K], rows 16-byte
 // aligned): lane L < 16 supplies row L mod 8, K offset 8 (L / 8).
-DF2_DEV void ldmatrix_b(uint32_t& b0, uint32_t& b1, const __half* row0, int pitch, int lane) {
-  const __half* p = row0 + (lane & 7) * pitch + ((lane >> 3) & 1) * 8;
+DF2_DEV void ldmatrix_b(uint32_t& b0, uint32_t& b1, const void* row0, int pitch, int lane) {
+  const uint16_t* p = static_cast<const uint16_t*>(row0) + (lane & 7) * pitch + ((lane >> 3) & 1) * 8;
   const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(p));
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(addr));
 }
@@ -91,54 +81,72 @@ DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* smem_row)
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
-// ------------------------------------------------------------------ context chunk (tensor cores)
-// Every thread's K/V loads of the chunk, issued together: 4 rows x 16 bytes of K and of V.
-struct KvRegs {
-  uint4 k[4], v[4];
-};
+// 16-byte asynchronous copy global -> shared; bytes = 0 fills the 16 bytes with zeros.
+DF2_DEV void cp_async16(void* smem_dst, const void* src, uint32_t bytes) {
+  const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
 
-DF2_DEV KvRegs load_kv(const AttnArgs& a, int r, int kvh, int k_begin, int nk) {
+// Two floats -> bf16x2 hi and lo parts (x = hi + lo to ~2^-16 relative).
+DF2_DEV void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 f = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - f.x, y - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// ------------------------------------------------------------------ context chunk (tensor cores)
+// The bf16 K/V rows of one chunk straight into buffer `buf` of the K/V tiles by
+// asynchronous copies (cp.async, 16 bytes each; rows at or past nk are zero-filled).
+template <int B>
+DF2_DEV void stage_kv(const AttnArgs& a, CtxSmem<B>& sm, int buf, int r, int kvh, int k_begin, int nk) {
   const int tid = threadIdx.x, nkv = a.n_kv_heads;
   const uint16_t* kc = a.k_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
   const uint16_t* vc = a.v_cache + (static_cast<size_t>(r) * a.kv_capacity + k_begin) * nkv * kHd + kvh * kHd;
-  KvRegs x;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = tid + 256 * j;
     const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-    x.k[j] = x.v[j] = make_uint4(0, 0, 0, 0);
-    if (k < nk) {
-      x.k[j] = ld_stream(kc + static_cast<size_t>(k) * nkv * kHd + d8);
-      x.v[j] = ld_stream(vc + static_cast<size_t>(k) * nkv * kHd + d8);
-    }
+    const int kk = k < nk ? k : 0;  // a valid address; the copy reads nothing then
+    const uint32_t bytes = k < nk ? 16u : 0u;
+    cp_async16(&sm.k[buf][k][d8], kc + static_cast<size_t>(kk) * nkv * kHd + d8, bytes);
+    cp_async16(&sm.v[buf][k][d8], vc + static_cast<size_t>(kk) * nkv * kHd + d8, bytes);
   }
-  return x;
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Context chunks c0 .. c1 - 1 of one (request, KV head), 64 keys each, with a
-// running (online) softmax: per query the running maximum m and sum l, and the
-// unnormalised output O, rescaled by 2^(m_old - m_new) whenever the maximum
-// grows.  The next chunk's K/V loads are issued before the current chunk is
-// computed.  The first chunk's K/V are loaded before the wait on the previous
-// kernel when none of its rows is appended by it.  Writes the part's (m, l, O).
+// Context chunks c0 .. c1 - 1 of one (request, KV head), 64 keys each.  Warp w takes
+// query tile w / WPM (16 queries) and keys (w mod WPM) KW .. + KW - 1 of every chunk
+// (WPM = 8 / query tiles warps share a tile, KW = 64 / WPM keys each), and keeps its
+// scores, probabilities and running softmax in registers: per query row the running
+// maximum m and sum l (over the lanes of a quad) and the unnormalised output O
+// (16 x 128, rescaled by 2^(m_old - m_new) when the maximum grows); the score
+// accumulators become the probability operand of the next product.  K and V stay
+// bf16 (exact); queries and probabilities enter the products as bf16 hi + lo pairs
+// (two products each, ~2^-16 relative).  The chunks' K/V tiles are double-buffered:
+// the next chunk's copies run while a chunk is computed, one barrier per chunk.  At
+// the end the WPM warps of a query tile merge their (m, l, O) in warp order through
+// shared memory and the part's (m, l, O) is written.
 template <int B>
 DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh, int lo0, int c0, int c1, int L,
                       int nn, float* out) {
-  constexpr int kQ = 4 * B, kMT = kQ / 16, kQW = kQ / 8;  // queries, query tiles, queries per warp
+  constexpr int kQ = 4 * B, kMT = kQ / 16;
+  constexpr int WPM = 8 / kMT, KW = kKeys / WPM, NTW = KW / 8, KSP = KW / 16;
   CtxSmem<B>& sm = *reinterpret_cast<CtxSmem<B>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
+  const int mt = wid / WPM, wp = wid % WPM;
   const int rep = a.n_q_heads / a.n_kv_heads;
   const float qscale = rsqrtf(static_cast<float>(kHd)) * 1.4426950408889634f;  // log2(e)/sqrt(hd)
   auto kbeg = [&](int c) { return lo0 + c * kKeys; };
   auto nkeys = [&](int c) { return min(kKeys, L - kbeg(c)); };
-  KvRegs kv;
   const bool early = kbeg(c0) + nkeys(c0) <= L - nn;  // rows L - nn .. L - 1 are appended by the previous kernel
-  if (early) kv = load_kv(a, r, kvh, kbeg(c0), nkeys(c0));
+  if (early) stage_kv<B>(a, sm, 0, r, kvh, kbeg(c0), nkeys(c0));
   pdl_wait();
   pdl_trigger();
-  if (!early) kv = load_kv(a, r, kvh, kbeg(c0), nkeys(c0));
-  // queries -> fp16 (qi = hr * B + i: head kvh*rep + hr, block row r*B + i); loads first
+  if (!early) stage_kv<B>(a, sm, 0, r, kvh, kbeg(c0), nkeys(c0));
+  // queries -> bf16 hi + lo (qi = hr * B + i: head kvh*rep + hr, block row r*B + i)
   float qv[kQ * kHd / 256];
 #pragma unroll
   for (int j = 0; j < kQ * kHd / 256; ++j) {
@@ -150,122 +158,160 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
 #pragma unroll
   for (int j = 0; j < kQ * kHd / 256; ++j) {
     const int e = tid + 256 * j;
-    const int qi = e / kHd, d = e % kHd;
-    sm.q[qi][d] = __float2half_rn(qv[j] * qscale);
+    const float x = qv[j] * qscale;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    sm.qh[e / kHd][e % kHd] = hi;
+    sm.ql[e / kHd][e % kHd] = __float2bfloat16_rn(x - __bfloat162float(hi));
   }
-  float m_run[kQW], l_run[kQW];  // queries kQW wid .. kQW wid + kQW - 1 (the same in every lane)
+  const int qi0 = mt * 16 + g, qi1 = qi0 + 8;  // this lane's two query rows
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[kHd / 8][4];
 #pragma unroll
-  for (int i = 0; i < kQW; ++i) {
-    m_run[i] = -INFINITY;
-    l_run[i] = 0.f;
-  }
-  float o[2][kMT][4] = {};  // dim tiles 2 wid + dn, query tiles mt
+  for (int dt = 0; dt < kHd / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
   for (int c = c0; c < c1; ++c) {
+    const int buf = (c - c0) & 1;
     const int k_begin = kbeg(c), nk = nkeys(c);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = tid + 256 * j;
-      const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
-      *reinterpret_cast<uint4*>(&sm.k[k][d8]) = bf16x8_to_f16x8(kv.k[j]);
-      *reinterpret_cast<uint4*>(&sm.v[k][d8]) = bf16x8_to_f16x8(kv.v[j]);
-    }
-    if (c + 1 < c1) kv = load_kv(a, r, kvh, kbeg(c + 1), nkeys(c + 1));  // in flight during this chunk
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // every thread's copies of this chunk have landed, every warp is done with the other
+    // buffer (the previous chunk), and the queries are in place
     __syncthreads();
-    // S = Q K^T: kMT query tiles x 8 key tiles; warp w takes key tile w for every query tile
-    {
-      const int nt = wid;
-      float cs[kMT][4] = {};
+    if (c + 1 < c1) stage_kv<B>(a, sm, buf ^ 1, r, kvh, kbeg(c + 1), nkeys(c + 1));  // in flight during this chunk
+    // S = Q K^T for the warp's 16 queries x KW keys
+    float s[NTW][4];
 #pragma unroll
-      for (int ks = 0; ks < kHd / 16; ++ks) {
+    for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kHd / 16; ++ks) {
+      uint32_t ah[4], al[4];
+      ldmatrix_a(ah, &sm.qh[mt * 16][ks * 16], kLd, lane);
+      ldmatrix_a(al, &sm.ql[mt * 16][ks * 16], kLd, lane);
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) {
         uint32_t b0, b1;
-        ldmatrix_b(b0, b1, &sm.k[nt * 8][ks * 16], kLd, lane);
+        ldmatrix_b(b0, b1, &sm.k[buf][wp * KW + nt * 8][ks * 16], kLd, lane);
+        mma_bf16(s[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
+        mma_bf16(s[nt], al[0], al[1], al[2], al[3], b0, b1);
+      }
+    }
+    // window and chunk-end masks; row maxima over the quad's lanes
+    const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
+    const int p0 = qi0 % B, p1 = qi1 % B;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          uint32_t af[4];
-          ldmatrix_a(af, &sm.q[mt * 16][ks * 16], kLd, lane);
-          mma_f16(cs[mt], af[0], af[1], af[2], af[3], b0, b1);
+    for (int nt = 0; nt < NTW; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int k = wp * KW + nt * 8 + 2 * q + e;
+        if (!(k < nk && k >= lim + p0)) s[nt][e] = -INFINITY;
+        if (!(k < nk && k >= lim + p1)) s[nt][2 + e] = -INFINITY;
+        mx0 = fmaxf(mx0, s[nt][e]);
+        mx1 = fmaxf(mx1, s[nt][2 + e]);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const bool none0 = mn0 == -INFINITY, none1 = mn1 == -INFINITY;  // no visible key yet
+    const float al0 = none0 ? 1.f : exp2f(m0 - mn0), al1 = none1 ? 1.f : exp2f(m1 - mn1);
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        s[nt][e] = none0 ? 0.f : exp2f(s[nt][e] - mn0);
+        s[nt][2 + e] = none1 ? 0.f : exp2f(s[nt][2 + e] - mn1);
+        ps0 += s[nt][e];
+        ps1 += s[nt][2 + e];
+      }
+    }
+    ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+    ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+    ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+    ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int dt = 0; dt < kHd / 8; ++dt) {
+      o[dt][0] *= al0;
+      o[dt][1] *= al0;
+      o[dt][2] *= al1;
+      o[dt][3] *= al1;
+    }
+    // O += P V: the probabilities of key tiles 2j, 2j + 1 (bf16 hi + lo) are the A
+    // fragments of the j-th 16 keys
+#pragma unroll
+    for (int j = 0; j < KSP; ++j) {
+      uint32_t ph[4], pl[4];
+      split_bf16(s[2 * j][0], s[2 * j][1], ph[0], pl[0]);
+      split_bf16(s[2 * j][2], s[2 * j][3], ph[1], pl[1]);
+      split_bf16(s[2 * j + 1][0], s[2 * j + 1][1], ph[2], pl[2]);
+      split_bf16(s[2 * j + 1][2], s[2 * j + 1][3], ph[3], pl[3]);
+#pragma unroll
+      for (int dt = 0; dt < kHd / 8; ++dt) {
+        uint32_t b0, b1;
+        ldmatrix_x2_trans(b0, b1, &sm.v[buf][wp * KW + j * 16 + (lane & 15)][dt * 8]);
+        mma_bf16(o[dt], ph[0], ph[1], ph[2], ph[3], b0, b1);
+        mma_bf16(o[dt], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      }
+    }
+  }
+  __syncthreads();  // every warp is done with the K/V tiles: the merge area overlays them
+  // merge the WPM warps of each query tile, in warp order
+  if (q == 0) {
+    sm.mw[wid][g] = m0;
+    sm.mw[wid][g + 8] = m1;
+    sm.lw[wid][g] = l0;
+    sm.lw[wid][g + 8] = l1;
+  }
+  __syncthreads();
+  float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < WPM; ++u) {
+    M0 = fmaxf(M0, sm.mw[mt * WPM + u][g]);
+    M1 = fmaxf(M1, sm.mw[mt * WPM + u][g + 8]);
+  }
+  const float f0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - M0), f1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - M1);
+  float(*so)[kHd + 4] = sm.so;  // overlays the K/V tiles, free now
+#pragma unroll
+  for (int u = 0; u < WPM; ++u) {
+    if (wp == u) {
+#pragma unroll
+      for (int dt = 0; dt < kHd / 8; ++dt) {
+        const int d = dt * 8 + 2 * q;
+        if (u == 0) {
+          so[qi0][d] = o[dt][0] * f0;
+          so[qi0][d + 1] = o[dt][1] * f0;
+          so[qi1][d] = o[dt][2] * f1;
+          so[qi1][d + 1] = o[dt][3] * f1;
+        } else {
+          so[qi0][d] += o[dt][0] * f0;
+          so[qi0][d + 1] += o[dt][1] * f0;
+          so[qi1][d] += o[dt][2] * f1;
+          so[qi1][d + 1] += o[dt][3] * f1;
         }
       }
-      const int lim = L - (a.window - 1) - k_begin;  // query i sees chunk key k iff k >= lim + i
-#pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int qi = mt * 16 + g + 8 * h2;
-          const int pos_i = qi % B;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int k = nt * 8 + 2 * q + e;
-            const bool ok = k < nk && k >= lim + pos_i;
-            sm.s[qi][k] = ok ? cs[mt][2 * h2 + e] : -INFINITY;
-          }
+      if (u == 0 && q == 0) {
+        float L0 = 0.f, L1 = 0.f;
+        for (int v = 0; v < WPM; ++v) {
+          const float mv0 = sm.mw[mt * WPM + v][g], mv1 = sm.mw[mt * WPM + v][g + 8];
+          if (mv0 > -INFINITY) L0 += sm.lw[mt * WPM + v][g] * exp2f(mv0 - M0);
+          if (mv1 > -INFINITY) L1 += sm.lw[mt * WPM + v][g + 8] * exp2f(mv1 - M1);
         }
+        out[qi0 * kPartStride + 0] = M0;
+        out[qi0 * kPartStride + 1] = L0;
+        out[qi1 * kPartStride + 0] = M1;
+        out[qi1 * kPartStride + 1] = L1;
       }
     }
     __syncthreads();
-    // running softmax statistics: warp w handles queries kQW w .. kQW w + kQW - 1, lane keys
-    // lane, lane + 32
-#pragma unroll
-    for (int i = 0; i < kQW; ++i) {
-      const int qi = wid * kQW + i;
-      const float v0 = sm.s[qi][lane], v1 = sm.s[qi][lane + 32];
-      const float m_new = fmaxf(m_run[i], warp_max(fmaxf(v0, v1)));
-      const bool none = m_new == -INFINITY;  // no visible key yet
-      const float alpha = none ? 1.f : exp2f(m_run[i] - m_new);
-      const float p0 = none ? 0.f : exp2f(v0 - m_new);
-      const float p1 = none ? 0.f : exp2f(v1 - m_new);
-      l_run[i] = l_run[i] * alpha + warp_sum(p0 + p1);
-      m_run[i] = m_new;
-      sm.p[qi][lane] = __float2half_rn(p0);
-      sm.p[qi][lane + 32] = __float2half_rn(p1);
-      if (lane == 0) sm.alpha[qi] = alpha;
-    }
-    __syncthreads();
-    // O = alpha O + P V: kMT query tiles x 16 dim tiles; warp w takes dim tiles 2w, 2w+1
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt) {
-      const float a0 = sm.alpha[mt * 16 + g], a1 = sm.alpha[mt * 16 + g + 8];
-#pragma unroll
-      for (int dn = 0; dn < 2; ++dn) {
-        o[dn][mt][0] *= a0;
-        o[dn][mt][1] *= a0;
-        o[dn][mt][2] *= a1;
-        o[dn][mt][3] *= a1;
-      }
-    }
-#pragma unroll
-    for (int ks = 0; ks < kKeys / 16; ++ks) {
-      uint32_t bv[2][2];
-#pragma unroll
-      for (int dn = 0; dn < 2; ++dn) ldmatrix_x2_trans(bv[dn][0], bv[dn][1], &sm.v[ks * 16 + (lane & 15)][(wid * 2 + dn) * 8]);
-#pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {  // one probability fragment serves both dimension tiles
-        uint32_t af[4];
-        ldmatrix_a(af, &sm.p[mt * 16][ks * 16], kPLd, lane);
-#pragma unroll
-        for (int dn = 0; dn < 2; ++dn) mma_f16(o[dn][mt], af[0], af[1], af[2], af[3], bv[dn][0], bv[dn][1]);
-      }
-    }
-    __syncthreads();  // k, v, p and alpha are rewritten by the next chunk
   }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kQW; ++i) {
-      out[(wid * kQW + i) * kPartStride + 0] = m_run[i];
-      out[(wid * kQW + i) * kPartStride + 1] = l_run[i];
-    }
-  }
-#pragma unroll
-  for (int dn = 0; dn < 2; ++dn) {
-    const int nt = wid * 2 + dn;
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt) {
-      const int q0 = mt * 16 + g, d0 = nt * 8 + 2 * q;
-      out[q0 * kPartStride + 2 + d0] = o[dn][mt][0];
-      out[q0 * kPartStride + 2 + d0 + 1] = o[dn][mt][1];
-      out[(q0 + 8) * kPartStride + 2 + d0] = o[dn][mt][2];
-      out[(q0 + 8) * kPartStride + 2 + d0 + 1] = o[dn][mt][3];
-    }
+  for (int e = tid; e < kQ * kHd; e += 256) {
+    const int qi = e / kHd, d = e % kHd;
+    out[qi * kPartStride + 2 + d] = so[qi][d];
   }
 }
 
@@ -324,9 +370,9 @@ DF2_DEV void blk_chunk(const AttnArgs& a, unsigned char* smem_raw, int r, int kv
 
 // grid (R * nkv, n_chunks): part p < n_chunks - 1 takes context chunks
 // p cpc .. p cpc + cpc - 1 (those that exist); the last part the B block keys.
-// Three CTAs per SM at B = 8, two at B = 16 (the context chunk's shared memory).
+// Two CTAs per SM (the context part's registers: a 16 x 128 output tile per warp).
 template <int B>
-__global__ void __launch_bounds__(256, B == 8 ? 3 : 2) attn_chunk_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(256, 2) attn_chunk_kernel(const AttnArgs a) {
   constexpr int kQ = 4 * B;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int nkv = a.n_kv_heads;
