@@ -17,7 +17,9 @@
 //    tcgen05.commit releases the stage; warps 4..7 read a finished accumulator out
 //    of tensor memory (tcgen05.ld, one weight row per thread) and store the partial
 //    plane.  Accumulators are double-buffered where the columns allow, so the
-//    epilogue of one block overlaps the products of the next.
+//    epilogue of one block overlaps the products of the next.  The CTA's last piece
+//    sits on the launch's tail: it is staged in the (by then idle) rings and leaves by
+//    bulk copies (cp.async.bulk), which takes about half the time of plain stores.
 //  * bf16 weights: two CTAs per SM, A and B both from shared memory through matrix
 //    descriptors; stages of one 128-row block x 64 K.
 //  * Q8/group64 weights ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias
@@ -100,6 +102,8 @@ struct WideGeo {
   static constexpr int kDW = FMT == 1 ? 64 * 1024 / kW : (kRing - kDB * kB) / kW;
   static constexpr int kOffB = kDW * kW;
   static constexpr int kSmem = kOffB + kDB * kB + 1024;
+  // Final epilogue: activation rows staged per pass, [n][128 weight rows] fp32 in the rings
+  static constexpr int kFinCols = ((kOffB + kDB * kB) / (kTM * 4) < NMAX ? (kOffB + kDB * kB) / (kTM * 4) : NMAX) & ~15;
   // int8: sixteen converter warps, each converting 64 K of 32 weight rows per stage: one
   // group for 256-K stages, two taking alternate stages for 128-K stages
   static constexpr int kConvGroups = FMT == 1 ? (kKS == 256 ? 1 : 2) : 0;
@@ -242,6 +246,21 @@ DF2_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+
+// Bulk copy of `bytes` contiguous bytes from shared to global memory (16-byte aligned
+// addresses, size a multiple of 16), tracked by this thread's bulk async-group.
+DF2_DEV void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+// Closes this thread's bulk async-group and waits until its copies have completed.
+DF2_DEV void bulk_commit_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+DF2_DEV void sts32(uint32_t addr, uint32_t v) { asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory"); }
+// Orders this thread's shared-memory stores before later bulk copies that read them.
+DF2_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 DF2_DEV uint32_t dequant_pair(uint32_t codes_biased, uint32_t sel, __half2 s, __half2 b) {
   const uint32_t qh = codes_to_half2(codes_biased, sel);
@@ -438,16 +457,38 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
         tc_fence_after();
         const GemvSeg& sg = a.seg[c.seg];
         const int n_rows = sg.n_tiles * 8, nm = n_mma_of(sg);
-        const int m = c.row0 + quarter * 32 + lane;
-        float* out = sg.out + static_cast<size_t>(c.plane(a)) * n_rows * sg.M + m;
+        float* out = sg.out + static_cast<size_t>(c.plane(a)) * n_rows * sg.M + c.row0 + quarter * 32;
         const uint32_t taddr =
             tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(Geo::kDCol0 + buf * NMAX);
-        for (int n0 = 0; n0 < nm; n0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(taddr + n0, r);
+        if (c.t == c.t1 - 1) {
+          // The CTA's last piece, on the launch's tail: every stage has been consumed, so the
+          // rings are free.  The warp's 32 weight rows go through shared memory ([n][32] fp32)
+          // and leave by bulk copies of 128 bytes, one per activation row: about half the time
+          // of plain stores from four warps.
+          const uint32_t stg = ring + static_cast<uint32_t>(quarter * Geo::kFinCols * 128);
+          for (int c0 = 0; c0 < n_rows; c0 += Geo::kFinCols) {
+            const int cols = min(Geo::kFinCols, n_rows - c0);
+            for (int n0 = 0; n0 < cols; n0 += 16) {
+              uint32_t r[16];
+              tmem_ld16(taddr + c0 + n0, r);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (n0 + j < n_rows) out[static_cast<size_t>(n0 + j) * sg.M] = __uint_as_float(r[j]);
+              for (int j = 0; j < 16; ++j) sts32(stg + static_cast<uint32_t>(((n0 + j) * 32 + lane) * 4), r[j]);
+            }
+            fence_proxy_async_smem();  // the bulk copies read what these stores wrote
+            __syncwarp();
+            for (int n = lane; n < cols; n += 32)
+              bulk_store(out + static_cast<size_t>(c0 + n) * sg.M, stg + static_cast<uint32_t>(n * 128), 128);
+            bulk_commit_wait_all();  // written before the staging is reused or the CTA exits
+            __syncwarp();
+          }
+        } else {
+          for (int n0 = 0; n0 < nm; n0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(taddr + n0, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (n0 + j < n_rows) out[static_cast<size_t>(n0 + j) * sg.M + lane] = __uint_as_float(r[j]);
+          }
         }
         tc_fence_before();
         __syncwarp();
