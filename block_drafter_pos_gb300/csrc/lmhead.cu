@@ -295,13 +295,29 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const TopkMergeArgs a) 
   }
 }
 
+// The warp's 32 keys in decreasing order across the lanes (bitonic sorting network).
+DF2_DEV unsigned long long warp_sort_desc(unsigned long long v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  }
+  return v;
+}
+
 // grid (n_chunks, (B - 1) R), 256 threads, 16 consecutive vocabulary entries per thread.
 // The chunk's 16 largest keys are found without ranking all 4096: the 16th largest
 // of a warp's 32 per-thread maxima (a bitonic sort across the warp) is a lower
 // bound T of the chunk's 16th largest key (16 distinct entries reach it), so only
 // the entries >= the largest such T are candidates; one warp ranks those.  If the
 // candidates overflow the buffer (few distinct values, e.g. a chunk past the
-// vocabulary's end), every warp ranks its own entries and warp 0 merges.
+// vocabulary's end), every warp ranks its own entries and warp 0 merges.  Up to 64
+// candidates (the usual case) are ranked by sorting networks rather than by 16
+// rounds of warp maxima.
 __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArgs a) {
   constexpr int kCap = 1024;
   __shared__ unsigned long long cand[kCap];
@@ -361,19 +377,11 @@ __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArg
 #pragma unroll
     for (int j = 0; j < 16; ++j) keys[j] = 0ull;
   }
-  // the warp's per-thread maxima sorted in decreasing order (bitonic network); lane 15 holds the 16th
+  // the warp's per-thread maxima sorted in decreasing order; lane 15 holds the 16th
   unsigned long long v = 0ull;
 #pragma unroll
   for (int j = 0; j < 16; ++j) v = keys[j] > v ? keys[j] : v;
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
-      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
-    }
-  }
+  v = warp_sort_desc(v, lane);
   if (lane == 15) wthr[wid] = v;
   __syncthreads();
   unsigned long long T = wthr[0];
@@ -391,14 +399,28 @@ __global__ void __launch_bounds__(256, 4) logits_topk_kernel(const LogitsTopkArg
   if (nc <= kCap) {
     if (wid != 0) return;
     unsigned long long out = 0ull;
-    for (int round = 0; round < kTopK; ++round) {
-      unsigned long long best = 0ull;
-      for (int i = lane; i < nc; i += 32) {
-        const unsigned long long c = cand[i];
-        if (c < last && c > best) best = c;
+    if (nc <= 64) {
+      // two sorted halves; the 32 largest of both, x[i] vs y[31 - i], form a bitonic
+      // sequence that five merge stages put in decreasing order
+      const unsigned long long x = warp_sort_desc(lane < nc ? cand[lane] : 0ull, lane);
+      const unsigned long long y = warp_sort_desc(lane + 32 < nc ? cand[lane + 32] : 0ull, lane);
+      const unsigned long long yr = __shfl_sync(0xffffffffu, y, 31 - lane);
+      out = x > yr ? x : yr;
+#pragma unroll
+      for (int j = 16; j > 0; j >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, out, j);
+        out = (lane & j) == 0 ? (o > out ? o : out) : (o < out ? o : out);
       }
-      last = warp_max_u64(best);
-      if (lane == round) out = last;
+    } else {
+      for (int round = 0; round < kTopK; ++round) {
+        unsigned long long best = 0ull;
+        for (int i = lane; i < nc; i += 32) {
+          const unsigned long long c = cand[i];
+          if (c < last && c > best) best = c;
+        }
+        last = warp_max_u64(best);
+        if (lane == round) out = last;
+      }
     }
     if (lane < kTopK) a.part_keys[(static_cast<size_t>(n) * a.n_chunks + blockIdx.x) * kTopK + lane] = out;
     return;

@@ -6,7 +6,7 @@
 // narrowed to width w < B verifies its first w - 1 proposals with rows 0..w-1
 // (the long-context narrowing of "qwen35: DSpark speculative decoding ... #625").
 //
-// Pass 1 (grid R x B rows x vocab chunks): per chunk max, argmax (smallest index on
+// Pass 1 (grid vocab chunks x R x B rows, chunks fastest): per chunk max, argmax (smallest index on
 // ties), sum of exp((z - m) / T), NaN / +inf flags; rows at or past a request's width
 // are skipped but counted.  Pass 2 (one CTA per request):
 // folds the chunk statistics in a fixed order and runs the sequential accept chain;
@@ -441,9 +441,11 @@ DF2_DEV void row_chunk_stats(const VerifyArgs& a, int rj, int r, int chunk) {
 // have written (the target model's), so the statistics wait for it.
 __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   pdl_begin_early();
-  const int rj = blockIdx.x;  // r * B + j
+  // chunks vary fastest in launch order, so a request's set completes early and its
+  // chain overlaps the statistics of the requests after it
+  const int rj = blockIdx.y;  // r * B + j
   const int r = rj / a.B, j_row = rj % a.B;
-  const int chunk = blockIdx.y;
+  const int chunk = blockIdx.x;
   // rows at or past the request's width are not read, only counted
   if (j_row < width_of(a.width, r, a.B)) row_chunk_stats(a, rj, r, chunk);
   // count this chunk; the CTA that completes request r's B x n_chunks runs its chain
@@ -547,8 +549,8 @@ __global__ void __launch_bounds__(256) tree_stats_kernel(const TreeVerifyArgs a)
   __shared__ float sm_m[8];
   __shared__ int sm_a[8], sm_f[8];
   pdl_begin_early();
-  const int r = blockIdx.x / (a.budget + 1), row = blockIdx.x % (a.budget + 1);
-  const int chunk = blockIdx.y;
+  const int r = blockIdx.y / (a.budget + 1), row = blockIdx.y % (a.budget + 1);
+  const int chunk = blockIdx.x;
   const int n = min(max(a.n_nodes[r], 0), a.budget);
   if (row <= n) {
     const float* z = a.logits + (static_cast<size_t>(r) * (a.budget + 1) + row) * a.V;
@@ -633,13 +635,15 @@ __global__ void __launch_bounds__(256) tree_stats_kernel(const TreeVerifyArgs a)
 
 cudaError_t launch_tree_verify(const TreeVerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if (a.budget < 1 || a.budget > kTreeMaxNodes || a.n_chunks < 1) return cudaErrorInvalidValue;
+  if (static_cast<long long>(n_req) * (a.budget + 1) > 65535) return cudaErrorInvalidValue;  // grid rows
   if (a.B != 8 && a.B != 16) return cudaErrorInvalidValue;
-  return launch_ex(tree_stats_kernel, dim3(n_req * (a.budget + 1), a.n_chunks), dim3(256), 0, st, pdl, a);
+  return launch_ex(tree_stats_kernel, dim3(a.n_chunks, n_req * (a.budget + 1)), dim3(256), 0, st, pdl, a);
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, int n_req, bool pdl, cudaStream_t st) {
   if (a.B != 8 && a.B != 16) return cudaErrorInvalidValue;
-  return launch_ex(verify_stats_kernel, dim3(n_req * a.B, a.n_chunks), dim3(256), a.n_chunks * sizeof(double), st, pdl,
+  if (static_cast<long long>(n_req) * a.B > 65535) return cudaErrorInvalidValue;  // grid rows
+  return launch_ex(verify_stats_kernel, dim3(a.n_chunks, n_req * a.B), dim3(256), a.n_chunks * sizeof(double), st, pdl,
                    a);
 }
 
