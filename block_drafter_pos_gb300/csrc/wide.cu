@@ -20,6 +20,8 @@
 //    epilogue of one block overlaps the products of the next.  The CTA's last piece
 //    sits on the launch's tail: it is staged in the (by then idle) rings and leaves by
 //    bulk copies (cp.async.bulk), which takes about half the time of plain stores.
+//    With int8 weights the other pieces pass through 32 KB of staging the rings leave
+//    free, 64 activation rows at a time, also by bulk copies.
 //  * bf16 weights: two CTAs per SM, A and B both from shared memory through matrix
 //    descriptors; stages of one 128-row block x 64 K.
 //  * Q8/group64 weights ("LSE docs/DFLASH2.md", Q8 paragraph: w = scale * q + bias
@@ -101,7 +103,9 @@ struct WideGeo {
   // requests with 128-K stages: gate/up 78 us at 2 or 4 stages, 80 at 6, 82 at 10.
   static constexpr int kDW = FMT == 1 ? 64 * 1024 / kW : (kRing - kDB * kB) / kW;
   static constexpr int kOffB = kDW * kW;
-  static constexpr int kSmem = kOffB + kDB * kB + 1024;
+  // int8: the 32 KB the rings leave free stage the epilogue of the pieces before the last
+  static constexpr int kEpiStage = FMT == 1 ? 32 * 1024 : 0;
+  static constexpr int kSmem = kOffB + kDB * kB + kEpiStage + 1024;
   // Final epilogue: activation rows staged per pass, [n][128 weight rows] fp32 in the rings
   static constexpr int kFinCols = ((kOffB + kDB * kB) / (kTM * 4) < NMAX ? (kOffB + kDB * kB) / (kTM * 4) : NMAX) & ~15;
   // int8: sixteen converter warps, each converting 64 K of 32 weight rows per stage: one
@@ -120,6 +124,7 @@ struct WideGeo {
                 "code ring depth vs converter groups");
   static_assert(FMT == 0 || kConv == 4 * (kKS / 64), "converter warps: four lane groups per 64 K");
   static_assert(kCtas * (kSmem + 1024) <= 228 * 1024, "shared memory per SM");
+  static_assert(kSmem <= 227 * 1024, "dynamic shared memory per CTA");
 };
 
 // Shared-memory matrix descriptor of a K-major tile of 128-byte rows under the
@@ -253,11 +258,14 @@ DF2_DEV void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
                : "memory");
 }
-// Closes this thread's bulk async-group and waits until its copies have completed.
+DF2_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Closes this thread's bulk async-group and waits until all its copies have completed.
 DF2_DEV void bulk_commit_wait_all() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  bulk_commit();
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until all this thread's committed bulk copies have read their sources.
+DF2_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 DF2_DEV void sts32(uint32_t addr, uint32_t v) { asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory"); }
 // Orders this thread's shared-memory stores before later bulk copies that read them.
 DF2_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -481,6 +489,28 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
             bulk_commit_wait_all();  // written before the staging is reused or the CTA exits
             __syncwarp();
           }
+        } else if (Geo::kEpiStage > 0) {
+          // Other pieces (the rings busy): through this warp's part of the epilogue staging,
+          // kEpiRows activation rows a pass, by bulk copies as above.  The tensor memory is
+          // read out before the accumulator is released; the copies may still be running.
+          constexpr int kRows = Geo::kEpiStage / (4 * 128);
+          const uint32_t stg = ring + static_cast<uint32_t>(Geo::kOffB + DB * Geo::kB + quarter * kRows * 128);
+          for (int c0 = 0; c0 < n_rows; c0 += kRows) {
+            const int cols = min(kRows, n_rows - c0);
+            bulk_wait_read_all();  // the staging's previous copies have read it
+            __syncwarp();
+            for (int n0 = 0; n0 < cols; n0 += 16) {
+              uint32_t r[16];
+              tmem_ld16(taddr + c0 + n0, r);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sts32(stg + static_cast<uint32_t>(((n0 + j) * 32 + lane) * 4), r[j]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            for (int n = lane; n < cols; n += 32)
+              bulk_store(out + static_cast<size_t>(c0 + n) * sg.M, stg + static_cast<uint32_t>(n * 128), 128);
+            bulk_commit();
+          }
         } else {
           for (int n0 = 0; n0 < nm; n0 += 16) {
             uint32_t r[16];
@@ -497,6 +527,7 @@ __global__ void __launch_bounds__(WideGeo<FMT, NMAX>::kWarps * 32, WideGeo<FMT, 
       }
       c.next(a);
     }
+    bulk_commit_wait_all();  // no copy still reads the staging when the CTA exits (also after an error)
   } else if (FMT == 1 && wid >= 8) {
     // ------------------------------------------------------------ int8 codes -> fp16 A operand in tensor memory
     const int cw = wid - 8;
