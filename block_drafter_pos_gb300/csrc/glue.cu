@@ -324,24 +324,40 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const SwigluArgs a) {
 // One warp per (row, head); lane holds dims lane + 32 c (c = 0..3), so the NEOX
 // pair (d, d + 64) is (c, c + 2) of the same lane.  Items per request: B query rows
 // x nq heads, then 2 B key rows (B block + B context) x nkv, then 2 B value rows x nkv.
+// The eight items of a CTA are consecutive heads of one row whenever the head counts
+// allow (the usual case), so the rotation angles (FP64 reduction, the costly part on
+// a part with few FP64 units) are computed once per CTA into shared memory; a CTA
+// whose items sit at different positions computes them per lane, the same way.
+
+// cos and sin of position pos x inverse frequency f: the angle in FP64, reduced by 2 pi
+// in FP64 (Cody-Waite, with 2 pi split into a double and its remainder); only the
+// reduced angle in [-pi, pi] goes through single-precision sincos.
+DF2_DEV void rope_angle(int pos, double f, float& sn, float& cs) {
+  const double ang = static_cast<double>(pos) * f;
+  const double turns = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
+  const double red = fma(-turns, 6.283185307179586, ang) - turns * 2.4492935982947064e-16;
+  sincosf(static_cast<float>(red), &sn, &cs);
+}
+
 __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) {
+  __shared__ int pos_sh[8];
+  __shared__ float sn_sh[64], cs_sh[64];
   pdl_begin();
   const int r = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  const int item = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int item = blockIdx.y * 8 + wid;
   const int nq = a.n_q_heads, nkv = a.n_kv_heads, B = a.B;
   const int n_items = B * nq + 2 * 2 * B * nkv;
-  if (item >= n_items) return;
   // lengths are clamped so a bad length can never address outside the cache
   const int nn = min(max(a.n_new[r], 0), B);
   const int ctx = min(max(a.ctx_len[r], 0), a.kv_capacity - nn);
   const int L = ctx + nn;
-  int kind, j, hh;
+  int kind = 2, j = 0, hh = 0;
   if (item < B * nq) {
     kind = 0;
     j = item / nq;
     hh = item % nq;
-  } else {
+  } else if (item < n_items) {
     const int e = item - B * nq;
     kind = 1 + e / (2 * B * nkv);
     const int e2 = e % (2 * B * nkv);
@@ -350,7 +366,25 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
   }
   const bool ctx_row = j >= B;
   const int jj = ctx_row ? j - B : j;
-  if (ctx_row && jj >= nn) return;
+  const bool valid = item < n_items && !(ctx_row && jj >= nn);
+  const int pos = ctx_row ? ctx + jj : L + jj;
+  // the CTA's rotated positions: one shared angle table when they agree
+  if (lane == 0) pos_sh[wid] = (valid && kind != 2) ? pos : -1;
+  __syncthreads();
+  int upos = -1;
+  bool uniform = true;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int p = pos_sh[w];
+    if (p >= 0) {
+      if (upos < 0) upos = p;
+      else if (p != upos) uniform = false;
+    }
+  }
+  uniform = uniform && upos >= 0;
+  if (uniform && threadIdx.x < 64) rope_angle(upos, a.inv_freq[threadIdx.x], sn_sh[threadIdx.x], cs_sh[threadIdx.x]);
+  __syncthreads();
+  if (!valid) return;
   const int row0 = r * B;
   const float* src;
   size_t plane;
@@ -384,7 +418,6 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
 #pragma unroll
     for (int c = 0; c < 4; ++c) v[c] *= rc;
   }
-  const int pos = ctx_row ? ctx + jj : L + jj;
   if (kind != 2) {
     const uint16_t* nw = kind == 0 ? a.q_norm : a.k_norm;
     const float ms = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]) / 128.f;
@@ -394,14 +427,13 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const QkvFinishArgs a) 
     // NEOX: out[j] = x[j] cos - x[j+64] sin; out[j+64] = x[j+64] cos + x[j] sin
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      // angle in FP64 (position x FP64 inverse frequency), reduced by 2 pi in FP64
-      // (Cody-Waite, with 2 pi split into a double and its remainder); only the
-      // reduced angle in [-pi, pi] goes through single-precision sin/cos
-      const double ang = static_cast<double>(pos) * a.inv_freq[lane + 32 * c];
-      const double turns = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
-      const double red = fma(-turns, 6.283185307179586, ang) - turns * 2.4492935982947064e-16;
       float sn, cs;
-      sincosf(static_cast<float>(red), &sn, &cs);
+      if (uniform) {
+        sn = sn_sh[lane + 32 * c];
+        cs = cs_sh[lane + 32 * c];
+      } else {
+        rope_angle(pos, a.inv_freq[lane + 32 * c], sn, cs);
+      }
       const float x1 = v[c], x2 = v[c + 2];
       v[c] = x1 * cs - x2 * sn;
       v[c + 2] = x2 * cs + x1 * sn;
