@@ -98,19 +98,17 @@ enum { kQ, kK, kV, kO, kGate, kUp, kDown, kAttnDelta, kMlpDelta };
 // which the GEMM path encodes its own activation map; wide_map: the weight map of
 // the GEMM path.
 // Context chunks per attention part.  A part's CTA streams its chunks one after the
-// other, and each CTA pays a fixed latency (queries, first copy, merge, partial
-// stores), so parts are made as long as the grid stays at least 7/4 of the SM count:
-// measured at 4 requests (context 8192) 4 chunks best (1.311 ms per step; 2: 1.341,
-// 8: 1.342), at 16 requests 16 (1.948; 4: 2.010, 8: 1.977, 32: 2.104).  Below four
-// requests one chunk per part (parts fill the GPU alone).
+// other; each part costs a fixed latency (queries, first copy, merge, partial
+// stores) and a partial for the combine.  Parts are at most 8 per (request, KV head),
+// and longer while the grid exceeds 1.3 waves of two CTAs per SM.  Measured (ms per
+// step): 1 request, context 1024: 1 chunk 1.181, 2: 1.168, 4: 1.172; context 2048:
+// 1: 1.032, 2: 1.022, 4: 1.016; 4 requests, context 8192: 2: 1.341, 4: 1.311,
+// 8: 1.342; 16 requests: 4: 2.010, 8: 1.977, 16: 1.948, 32: 2.104.
 int attn_chunks_per_part(int n_req, int nkv, int n_ctx_chunks, int num_sms) {
-  if (n_req < 4) return 1;
-  int best = 1;
-  for (int c = 2; c <= 16; c *= 2) {
-    const long long ctas = static_cast<long long>(n_req) * nkv * ((n_ctx_chunks + c - 1) / c + 1);
-    if (4 * ctas >= 7LL * num_sms) best = c;
-  }
-  return best;
+  int c = 1;
+  while (c < 16 && (n_ctx_chunks + c - 1) / c > 8) c *= 2;
+  while (c < 16 && 10LL * n_req * nkv * ((n_ctx_chunks + c - 1) / c + 1) > 26LL * num_sms) c *= 2;
+  return c;
 }
 
 struct SegSpec {
