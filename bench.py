@@ -12,8 +12,9 @@ resident in HBM and far larger than L2 (6.1 GB of weights stream every step).
 
 `value` is steps/s summed over ranks (independent replicas, weak scaling).
 `e2e` is the same metric through the C ABI with host buffers: every step copies
-its inputs from pinned host memory and reads its result back (the target logits,
-needed only by verify, on a second stream while the draft runs).  `roofline`
+its inputs from pinned host memory, runs as one dflash2_step call (the handle's
+CUDA graph of the step) and reads its result back; the inputs go on a second
+stream into one of two buffer sets, overlapping the previous step.  `roofline`
 covers the LM-head + top-16 kernel, timed with CUDA events captured inside the
 graph on the launching stream; `roofline.projections` covers the drafter's weight
 projections (every other weight stream), each launch bracketed by events in a
@@ -529,39 +530,44 @@ def main_ours(args, rank, world, local_rank):
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
-    # The target logits (nine tenths of the bytes in) are needed only by verify: they
-    # are copied on a side stream while the draft and select run, after the previous
-    # step's verify has read the same buffer; verify waits for the copy.
+    # One call per step: dflash2_step replays the handle's CUDA graph of the step's
+    # argument set (captured on its first call).  A step's inputs go into one of two
+    # sets of device buffers on a side stream, once the step two steps back (the last
+    # to read that set) has verified, so the copies of step i overlap step i - 1; the
+    # step waits for its copies.  Two buffer sets, two argument sets, two graphs.
     main, side = torch.cuda.current_stream(), torch.cuda.Stream()
-    verified, landed = torch.cuda.Event(), torch.cuda.Event()
+    dev_in = [{k: S[k] for k in host_in}, {k: torch.empty_like(S[k]) for k in host_in}]
+    verified = [torch.cuda.Event(), torch.cuda.Event()]
+    landed = [torch.cuda.Event(), torch.cuda.Event()]
+    n_e2e = [0]
 
     def e2e_step():
-        side.wait_event(verified)
+        j = n_e2e[0] % 2
+        n_e2e[0] += 1
+        D = dev_in[j]
+        side.wait_event(verified[j])
         with torch.cuda.stream(side):
-            S["target"].copy_(host_in["target"], non_blocking=True)
-        landed.record(side)
-        for k, v in host_in.items():
-            if k != "target":
-                S[k].copy_(v, non_blocking=True)
-        bd.dflash2_draft_block(h, R, S["anchors"], S["ctx_len"], S["n_new"], S["taps"], S["kc"], S["vc"],
-                               S["cand_ids"], S["cand_logits"], S["gate"], None)
-        bd.dflash2_select(h, R, S["anchors"], S["cand_ids"], S["cand_logits"], S["gate"], S["temps"], S["seeds"],
-                          S["offsets"], S["path"], S["q_rows"], None, S["status"])
-        main.wait_event(landed)
-        bd.dflash2_verify(h, R, S["target"], S["path"], S["cand_ids"], S["q_rows"], S["temps"], S["seeds"],
-                          S["offsets"], S["n_acc"], S["emitted"], S["n_emit"], None, S["status"])
-        verified.record(main)
+            for k, v in host_in.items():
+                D[k].copy_(v, non_blocking=True)
+        landed[j].record(side)
+        main.wait_event(landed[j])
+        bd.dflash2_step(h, R, D["anchors"], D["ctx_len"], D["n_new"], D["taps"], S["kc"], S["vc"], S["cand_ids"],
+                        S["cand_logits"], S["gate"], D["temps"], D["seeds"], D["offsets"], S["path"], S["q_rows"],
+                        S["status"], D["target"], S["n_acc"], S["emitted"], S["n_emit"])
+        verified[j].record(main)
         for k, v in host_out.items():
             v.copy_(S[k], non_blocking=True)
 
-    verified.record(main)
-    for _ in range(2):
+    for ev in verified:
+        ev.record(main)
+    for _ in range(4):  # both argument sets: first calls (capture), then replays
         e2e_step()
     torch.cuda.synchronize()
     sync_ranks(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    verified.record(main)  # no copy of the timed steps starts before the timed region
+    for ev in verified:
+        ev.record(main)  # no copy of the timed steps starts before the timed region
     for _ in range(E):
         e2e_step()
     e1.record()

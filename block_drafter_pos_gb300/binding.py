@@ -42,6 +42,14 @@ class LayerWeights(ctypes.Structure):
                                                  "mlp_base")] + [(n, Matrix) for n in _LAYER_MATS]
 
 
+class StepArgs(ctypes.Structure):
+    """dflash2_step_args: the device buffers of one draft + select + verify step."""
+    _fields_ = [("n_req", ctypes.c_int32)] + [(n, ctypes.c_void_p) for n in (
+        "anchor_ids", "ctx_len", "n_new", "taps", "k_cache", "v_cache", "cand_ids", "cand_logits", "gate",
+        "temperature", "seed", "philox_offset", "path", "q_rows", "status", "target_logits", "n_accepted",
+        "emitted", "n_emitted", "width")]
+
+
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("embed", "lm_head", "hidden_norm", "final_norm")] + [
         (n, Matrix) for n in ("fc", "sel_proj", "cb_a", "cb_b")] + [("layers", LayerWeights * MAX_LAYERS)]
@@ -89,6 +97,10 @@ def lib() -> ctypes.CDLL:
         L.dflash2_debug_set_pipeline_error.restype = i32
         L.dflash2_debug_noalloc_inject_error.argtypes = [i32]
         L.dflash2_debug_noalloc_inject_error.restype = i32
+        L.dflash2_step.argtypes = [vp, ctypes.POINTER(StepArgs), vp]
+        L.dflash2_step.restype = i32
+        L.dflash2_step_graphs_clear.argtypes = [vp]
+        L.dflash2_step_graphs_clear.restype = i32
         L.dflash2_status_string.argtypes = [i32]
         L.dflash2_status_string.restype = ctypes.c_char_p
         for f in ("dflash2_create", "dflash2_destroy", "dflash2_draft_block", "dflash2_select", "dflash2_verify",
@@ -172,6 +184,21 @@ def dflash2_tree_verify(h, n_req, budget, target_logits, node_token, node_parent
     _check(lib().dflash2_tree_verify(h, n_req, budget, _p(target_logits), _p(node_token), _p(node_parent),
                                      _p(n_nodes), _p(n_accepted), _p(emitted), _p(n_emitted), _p(status),
                                      _stream(stream)), "dflash2_tree_verify")
+
+
+def dflash2_step(h, n_req, anchor_ids, ctx_len, n_new, taps, k_cache, v_cache, cand_ids, cand_logits, gate,
+                 temperature, seed, philox_offset, path, q_rows, status, target_logits, n_accepted, emitted,
+                 n_emitted, width=None, stream=None):
+    """One draft + select + verify step, replayed from the handle's CUDA graph of this
+    argument set after its first call (dflash2.h, dflash2_step)."""
+    a = StepArgs(n_req, _p(anchor_ids), _p(ctx_len), _p(n_new), _p(taps), _p(k_cache), _p(v_cache), _p(cand_ids),
+                 _p(cand_logits), _p(gate), _p(temperature), _p(seed), _p(philox_offset), _p(path), _p(q_rows),
+                 _p(status), _p(target_logits), _p(n_accepted), _p(emitted), _p(n_emitted), _p(width))
+    _check(lib().dflash2_step(h, ctypes.byref(a), _stream(stream)), "dflash2_step")
+
+
+def dflash2_step_graphs_clear(h):
+    _check(lib().dflash2_step_graphs_clear(h), "dflash2_step_graphs_clear")
 
 
 def dflash2_set_select_mode(h, mode: int):

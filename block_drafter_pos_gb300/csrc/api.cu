@@ -77,6 +77,17 @@ struct dflash2_handle {
   cudaEvent_t* proj_ev;
   int proj_pairs, proj_next;
   bool in_draft;
+  // dflash2_step: graphs of the argument sets seen, least recently used replaced
+  struct StepGraph {
+    dflash2_step_args key;
+    cudaGraphExec_t exec;
+    int64_t launches;  // kernels in the graph
+    uint64_t used;
+  };
+  StepGraph step_graph[DFLASH2_STEP_GRAPHS] = {};
+  int n_step_graphs = 0;
+  uint64_t step_clock = 0;
+  cudaStream_t cap_stream = nullptr;  // the handle's own stream for the captures
 };
 
 namespace {
@@ -450,6 +461,8 @@ dflash2_status dflash2_create(const dflash2_config* cfg, const dflash2_weights* 
 
 dflash2_status dflash2_destroy(dflash2_handle* h) {
   if (!h) return DFLASH2_E_INVAL;
+  dflash2_step_graphs_clear(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   cudaFree(h->arena);
   delete h;
   return DFLASH2_OK;
@@ -1115,6 +1128,102 @@ dflash2_status dflash2_verify(dflash2_handle* h, int32_t n_req, const float* tar
   a.B = h->B;
   DF2_CHECK(launch_verify(a, n_req, h->pdl, static_cast<cudaStream_t>(stream)));
   h->launches += 1;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_step_graphs_clear(dflash2_handle* h) {
+  if (!h) return DFLASH2_E_INVAL;
+  for (int i = 0; i < h->n_step_graphs; ++i)
+    if (h->step_graph[i].exec) cudaGraphExecDestroy(h->step_graph[i].exec);
+  h->n_step_graphs = 0;
+  return DFLASH2_OK;
+}
+
+dflash2_status dflash2_step(dflash2_handle* h, const dflash2_step_args* args, void* stream) {
+  if (!h || !args) return DFLASH2_E_INVAL;
+  // the key: the fields only (a zeroed copy, so padding never differs)
+  dflash2_step_args k;
+  memset(&k, 0, sizeof(k));
+  k.n_req = args->n_req;
+  k.anchor_ids = args->anchor_ids;
+  k.ctx_len = args->ctx_len;
+  k.n_new = args->n_new;
+  k.taps = args->taps;
+  k.k_cache = args->k_cache;
+  k.v_cache = args->v_cache;
+  k.cand_ids = args->cand_ids;
+  k.cand_logits = args->cand_logits;
+  k.gate = args->gate;
+  k.temperature = args->temperature;
+  k.seed = args->seed;
+  k.philox_offset = args->philox_offset;
+  k.path = args->path;
+  k.q_rows = args->q_rows;
+  k.status = args->status;
+  k.target_logits = args->target_logits;
+  k.n_accepted = args->n_accepted;
+  k.emitted = args->emitted;
+  k.n_emitted = args->n_emitted;
+  k.width = args->width;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < h->n_step_graphs; ++i) {
+    dflash2_handle::StepGraph& g = h->step_graph[i];
+    if (memcmp(&g.key, &k, sizeof(k)) == 0) {
+      DF2_CHECK(cudaGraphLaunch(g.exec, st));
+      h->launches += g.launches;
+      g.used = ++h->step_clock;
+      return DFLASH2_OK;
+    }
+  }
+  // a new set: the three calls as they are, on the caller's stream
+  auto run = [&](cudaStream_t s) {
+    dflash2_status r = dflash2_draft_block(h, k.n_req, k.anchor_ids, k.ctx_len, k.n_new, k.taps, k.k_cache, k.v_cache,
+                                           k.cand_ids, k.cand_logits, k.gate, nullptr, k.width, s);
+    if (r == DFLASH2_OK)
+      r = dflash2_select(h, k.n_req, k.anchor_ids, k.cand_ids, k.cand_logits, k.gate, k.temperature, k.seed,
+                         k.philox_offset, k.path, k.q_rows, nullptr, k.status, k.width, s);
+    if (r == DFLASH2_OK)
+      r = dflash2_verify(h, k.n_req, k.target_logits, k.path, k.cand_ids, k.q_rows, k.temperature, k.seed,
+                         k.philox_offset, k.n_accepted, k.emitted, k.n_emitted, nullptr, k.status, k.width, s);
+    return r;
+  };
+  const dflash2_status r = run(st);
+  if (r != DFLASH2_OK) return r;
+  // then its graph, captured on the handle's own stream (nothing runs)
+  if (!h->cap_stream && cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    h->cap_stream = nullptr;
+    cudaGetLastError();
+    return DFLASH2_OK;
+  }
+  const int64_t n0 = h->launches;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  bool ok = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+  if (ok) {
+    const dflash2_status rc = run(h->cap_stream);
+    ok = cudaStreamEndCapture(h->cap_stream, &graph) == cudaSuccess && rc == DFLASH2_OK && graph != nullptr;
+  }
+  const int64_t n_graph = h->launches - n0;
+  h->launches = n0;  // the capture launched nothing
+  if (ok) ok = cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+  if (graph) cudaGraphDestroy(graph);
+  if (!ok) {
+    cudaGetLastError();  // the set stays uncached; the step itself has run
+    return DFLASH2_OK;
+  }
+  int slot = h->n_step_graphs;
+  if (slot == DFLASH2_STEP_GRAPHS) {  // replace the least recently used
+    slot = 0;
+    for (int i = 1; i < DFLASH2_STEP_GRAPHS; ++i)
+      if (h->step_graph[i].used < h->step_graph[slot].used) slot = i;
+    cudaGraphExecDestroy(h->step_graph[slot].exec);
+  } else {
+    ++h->n_step_graphs;
+  }
+  h->step_graph[slot].key = k;
+  h->step_graph[slot].exec = exec;
+  h->step_graph[slot].launches = n_graph;
+  h->step_graph[slot].used = ++h->step_clock;
   return DFLASH2_OK;
 }
 

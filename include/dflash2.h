@@ -305,6 +305,59 @@ dflash2_status dflash2_advance(dflash2_handle* h, int32_t n_req, const int32_t* 
                                int32_t* anchor_ids, int32_t* ctx_len, int32_t* n_new, uint64_t* philox_offset,
                                void* stream);
 
+/* ---- One step from a captured CUDA graph ----
+ * The arguments of one draft + select + verify step: the fields of
+ * dflash2_draft_block, dflash2_select and dflash2_verify of the same names and
+ * meanings (logits_out, scores_out and probs_out are NULL in a step).  width is
+ * shared by the three calls (NULL: block). */
+typedef struct dflash2_step_args {
+  int32_t n_req;
+  const int32_t* anchor_ids;    /* [R] */
+  const int32_t* ctx_len;       /* [R] */
+  const int32_t* n_new;         /* [R] */
+  const float* taps;            /* [R][block][n_taps*H] */
+  void* k_cache;                /* bf16 [n_layers][max_requests][kv_capacity][nkv][hd] */
+  void* v_cache;
+  int32_t* cand_ids;            /* [R][block-1][top_k] */
+  float* cand_logits;           /* [R][block-1][top_k] */
+  float* gate;                  /* [R][block-1][rank] */
+  const float* temperature;     /* [R] */
+  const uint64_t* seed;         /* [R] */
+  const uint64_t* philox_offset; /* [R] */
+  int32_t* path;                /* [R][block-1] */
+  float* q_rows;                /* [R][block-1][top_k] */
+  int32_t* status;              /* [R] written by the select, read and written by the verify */
+  const float* target_logits;   /* [R][block][V] */
+  int32_t* n_accepted;          /* [R] */
+  int32_t* emitted;             /* [R][block] */
+  int32_t* n_emitted;           /* [R] */
+  const int32_t* width;         /* [R] or NULL */
+} dflash2_step_args;
+
+/* Number of argument sets whose step graphs a handle keeps (least recently used
+ * replaced). */
+#define DFLASH2_STEP_GRAPHS 4
+
+/* One step: dflash2_draft_block, dflash2_select and dflash2_verify on `args`, in
+ * that order on `stream`, with the same results.  The first call with a given
+ * argument set (the same values in every field) runs the three calls as they are
+ * and then captures them into a CUDA graph on a stream of the handle's own (the
+ * capture launches nothing); later calls with that set launch the graph on `stream`,
+ * one launch instead of about seventy.  The graph reads the buffers each time it
+ * runs, so a serving loop changes their contents between steps, not their
+ * addresses (dflash2_advance keeps them).  A handle keeps DFLASH2_STEP_GRAPHS sets;
+ * their graphs are freed by dflash2_step_graphs_clear or dflash2_destroy, and must
+ * be cleared before a buffer they name is freed.  Not for concurrent use of one
+ * handle from several threads.  Returns what the three calls return (their checks
+ * run on the first call with a set; nothing is cached when one fails) or
+ * DFLASH2_E_CUDA if a launch fails; a failed capture leaves the set uncached, and
+ * the next call with it runs the three calls again. */
+dflash2_status dflash2_step(dflash2_handle* h, const dflash2_step_args* args, void* stream);
+
+/* Frees the handle's step graphs (waits for none of their launches: the caller
+ * orders this after them, e.g. by synchronising the streams they ran on). */
+dflash2_status dflash2_step_graphs_clear(dflash2_handle* h);
+
 /* Block width of each request by context length ("qwen35: DSpark speculative
  * decoding ... #625", long-context commits: the verify's cost grows with the
  * block's rows times the context, so past a context threshold the block narrows;

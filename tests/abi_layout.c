@@ -24,5 +24,9 @@ int main(void) {
   OFF(dflash2_weights, fc);
   OFF(dflash2_weights, cb_b);
   OFF(dflash2_weights, layers);
+  printf("dflash2_step_args %zu\n", sizeof(dflash2_step_args));
+  OFF(dflash2_step_args, anchor_ids);
+  OFF(dflash2_step_args, status);
+  OFF(dflash2_step_args, width);
   return 0;
 }

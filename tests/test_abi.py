@@ -110,6 +110,8 @@ def test_entry_points_reject_a_null_handle_or_bad_sizes():
     assert lib.dflash2_set_select_mode(None, 0) == E
     assert lib.dflash2_head_topk(None, 8, *([None] * 5)) == E
     assert lib.dflash2_destroy(None) == E
+    assert lib.dflash2_step(None, None, None) == E
+    assert lib.dflash2_step_graphs_clear(None) == E
     # the entry that allocates nothing: its size checks come before any device call
     buf = (ctypes.c_char * 64)()
     p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16, ctypes.c_void_p)
@@ -168,5 +170,9 @@ def test_binding_structures_match_the_header(tmp_path):
         "dflash2_weights.fc": b.Weights.fc.offset,
         "dflash2_weights.cb_b": b.Weights.cb_b.offset,
         "dflash2_weights.layers": b.Weights.layers.offset,
+        "dflash2_step_args": ctypes.sizeof(b.StepArgs),
+        "dflash2_step_args.anchor_ids": b.StepArgs.anchor_ids.offset,
+        "dflash2_step_args.status": b.StepArgs.status.offset,
+        "dflash2_step_args.width": b.StepArgs.width.offset,
     }
     assert {k: int(v) for k, v in got.items()} == want
