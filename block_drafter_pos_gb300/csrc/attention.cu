@@ -31,22 +31,29 @@ namespace {
 constexpr int kHd = 128;
 constexpr int kKeys = kAttnChunk;
 constexpr int kPartStride = kHd + 2;
-constexpr int kLd = kHd + 8;    // bf16 row pitch (272 B): conflict-free fragment loads
+// Query and K/V tiles: rows of 128 bf16 (256 bytes, 16 pieces of 16 bytes), piece p of
+// row r stored at p ^ (r mod 8): the eight rows of every 8 x 8 fragment load fall on
+// distinct banks without padding.
+DF2_DEV int swz_off(int r, int piece) { return r * 256 + ((piece ^ (r & 7)) << 4); }
 
 // B block positions: kQ = 4 B queries per KV head group (4 heads x B positions),
 // query qi = hr * B + i is head kvh * 4 + hr at block position i.
 template <int B>
 struct CtxSmem {
   static constexpr int kQ = 4 * B;
-  __nv_bfloat16 qh[kQ][kLd], ql[kQ][kLd];  // scaled queries, bf16 hi and lo parts
+  // K/V buffers: three at B = 8 (112 KB: two CTAs per SM), two at B = 16
+  static constexpr int kNB = B == 8 ? 3 : 2;
+  uint16_t qh[kQ][kHd], ql[kQ][kHd];  // scaled queries, bf16 hi and lo parts (swizzled rows)
   union {
     struct {
-      uint16_t k[2][kKeys][kLd];  // bf16 K and V of a chunk, double-buffered
-      uint16_t v[2][kKeys][kLd];
+      uint16_t k[kNB][kKeys][kHd];  // bf16 K and V of a chunk (swizzled rows)
+      uint16_t v[kNB][kKeys][kHd];
     };
-    float so[kQ][kHd + 4];        // the merged output of the part (after the last chunk)
+    struct {  // after the last chunk
+      float so[kQ][kHd + 4];        // the merged output of the part
+      float mw[8][16], lw[8][16];   // per warp: running maximum and sum of its 16 query rows
+    };
   };
-  float mw[8][16], lw[8][16];     // per warp: running maximum and sum of its 16 query rows
 };
 
 template <int B>
@@ -60,9 +67,9 @@ struct BlkSmem {
 // A fragment of mma m16n8k16 (rows 0..15 x K 0..15 of a 16-bit tile whose rows are 16-byte
 // aligned): lane L supplies row (L mod 8) + 8 ((L / 8) mod 2), K offset 8 (L / 16), so
 // the registers are {rows 0-7 K 0-7, rows 8-15 K 0-7, rows 0-7 K 8-15, rows 8-15 K 8-15}.
-DF2_DEV void ldmatrix_a(uint32_t (&r)[4], const void* row0, int pitch, int lane) {
-  const uint16_t* p = static_cast<const uint16_t*>(row0) + ((lane & 7) + ((lane >> 3) & 1) * 8) * pitch + (lane >> 4) * 8;
-  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(p));
+DF2_DEV void ldmatrix_a(uint32_t (&r)[4], const void* tile, int row0, int piece0, int lane) {
+  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(tile)) +
+                        swz_off(row0 + (lane & 7) + ((lane >> 3) & 1) * 8, piece0 + (lane >> 4));
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
@@ -70,14 +77,14 @@ DF2_DEV void ldmatrix_a(uint32_t (&r)[4], const void* row0, int pitch, int lane)
 
 // B fragment (K 0..15 x n 0..7) from a 16-bit tile stored n-major ([n][K], rows 16-byte
 // aligned): lane L < 16 supplies row L mod 8, K offset 8 (L / 8).
-DF2_DEV void ldmatrix_b(uint32_t& b0, uint32_t& b1, const void* row0, int pitch, int lane) {
-  const uint16_t* p = static_cast<const uint16_t*>(row0) + (lane & 7) * pitch + ((lane >> 3) & 1) * 8;
-  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(p));
+DF2_DEV void ldmatrix_b(uint32_t& b0, uint32_t& b1, const void* tile, int row0, int piece0, int lane) {
+  const unsigned addr =
+      static_cast<unsigned>(__cvta_generic_to_shared(tile)) + swz_off(row0 + (lane & 7), piece0 + ((lane >> 3) & 1));
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(addr));
 }
 
-DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* smem_row) {
-  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(smem_row));
+DF2_DEV void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* tile, int row, int piece) {
+  const unsigned addr = static_cast<unsigned>(__cvta_generic_to_shared(tile)) + swz_off(row, piece);
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
@@ -110,8 +117,11 @@ DF2_DEV void stage_kv(const AttnArgs& a, CtxSmem<B>& sm, int buf, int r, int kvh
     const int k = e / (kHd / 8), d8 = (e % (kHd / 8)) * 8;
     const int kk = k < nk ? k : 0;  // a valid address; the copy reads nothing then
     const uint32_t bytes = k < nk ? 16u : 0u;
-    cp_async16(&sm.k[buf][k][d8], kc + static_cast<size_t>(kk) * nkv * kHd + d8, bytes);
-    cp_async16(&sm.v[buf][k][d8], vc + static_cast<size_t>(kk) * nkv * kHd + d8, bytes);
+    const int off = swz_off(k, d8 / 8);
+    cp_async16(reinterpret_cast<unsigned char*>(&sm.k[buf][0][0]) + off, kc + static_cast<size_t>(kk) * nkv * kHd + d8,
+               bytes);
+    cp_async16(reinterpret_cast<unsigned char*>(&sm.v[buf][0][0]) + off, vc + static_cast<size_t>(kk) * nkv * kHd + d8,
+               bytes);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -124,8 +134,10 @@ DF2_DEV void stage_kv(const AttnArgs& a, CtxSmem<B>& sm, int buf, int r, int kvh
 // (16 x 128, rescaled by 2^(m_old - m_new) when the maximum grows); the score
 // accumulators become the probability operand of the next product.  K and V stay
 // bf16 (exact); queries and probabilities enter the products as bf16 hi + lo pairs
-// (two products each, ~2^-16 relative).  The chunks' K/V tiles are double-buffered:
-// the next chunk's copies run while a chunk is computed, one barrier per chunk.  At
+// (two products each, ~2^-16 relative).  The chunks' K/V tiles are triple-buffered
+// at B = 8 (the copies of the next two chunks run while a chunk is computed; 112 KB,
+// two CTAs per SM with unpadded, swizzled rows) and double-buffered at B = 16; one
+// barrier per chunk.  At
 // the end the WPM warps of a query tile merge their (m, l, O) in warp order through
 // shared memory and the part's (m, l, O) is written.
 template <int B>
@@ -146,6 +158,13 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   pdl_wait();
   pdl_trigger();
   if (!early) stage_kv<B>(a, sm, 0, r, kvh, kbeg(c0), nkeys(c0));
+  constexpr int NB = CtxSmem<B>::kNB;
+  for (int j = 1; j < NB - 1; ++j) {  // the first NB - 1 chunks in flight (one group each, empty past the part)
+    if (c0 + j < c1)
+      stage_kv<B>(a, sm, j, r, kvh, kbeg(c0 + j), nkeys(c0 + j));
+    else
+      asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   // queries -> bf16 hi + lo (qi = hr * B + i: head kvh*rep + hr, block row r*B + i)
   float qv[kQ * kHd / 256];
 #pragma unroll
@@ -159,9 +178,11 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
   for (int j = 0; j < kQ * kHd / 256; ++j) {
     const int e = tid + 256 * j;
     const float x = qv[j] * qscale;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-    sm.qh[e / kHd][e % kHd] = hi;
-    sm.ql[e / kHd][e % kHd] = __float2bfloat16_rn(x - __bfloat162float(hi));
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x), lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    const int qi = e / kHd, d = e % kHd;
+    const int off = swz_off(qi, d >> 3) / 2 + (d & 7);  // in bf16 elements
+    (&sm.qh[0][0])[off] = *reinterpret_cast<const uint16_t*>(&hi);
+    (&sm.ql[0][0])[off] = *reinterpret_cast<const uint16_t*>(&lo);
   }
   const int qi0 = mt * 16 + g, qi1 = qi0 + 8;  // this lane's two query rows
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -169,13 +190,20 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
 #pragma unroll
   for (int dt = 0; dt < kHd / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
   for (int c = c0; c < c1; ++c) {
-    const int buf = (c - c0) & 1;
+    const int buf = (c - c0) % NB;
     const int k_begin = kbeg(c), nk = nkeys(c);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    // every thread's copies of this chunk have landed, every warp is done with the other
-    // buffer (the previous chunk), and the queries are in place
+    // this chunk's group has completed (NB - 2 later groups may still be in flight)
+    if (NB == 3)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // every thread's copies of this chunk have landed, every warp is done with the
+    // buffer of the previous chunk, and the queries are in place
     __syncthreads();
-    if (c + 1 < c1) stage_kv<B>(a, sm, buf ^ 1, r, kvh, kbeg(c + 1), nkeys(c + 1));  // in flight during this chunk
+    if (c + NB - 1 < c1)  // in flight during the next NB - 1 chunks
+      stage_kv<B>(a, sm, (buf + NB - 1) % NB, r, kvh, kbeg(c + NB - 1), nkeys(c + NB - 1));
+    else
+      asm volatile("cp.async.commit_group;" ::: "memory");
     // S = Q K^T for the warp's 16 queries x KW keys
     float s[NTW][4];
 #pragma unroll
@@ -183,12 +211,12 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
 #pragma unroll
     for (int ks = 0; ks < kHd / 16; ++ks) {
       uint32_t ah[4], al[4];
-      ldmatrix_a(ah, &sm.qh[mt * 16][ks * 16], kLd, lane);
-      ldmatrix_a(al, &sm.ql[mt * 16][ks * 16], kLd, lane);
+      ldmatrix_a(ah, &sm.qh[0][0], mt * 16, ks * 2, lane);
+      ldmatrix_a(al, &sm.ql[0][0], mt * 16, ks * 2, lane);
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt) {
         uint32_t b0, b1;
-        ldmatrix_b(b0, b1, &sm.k[buf][wp * KW + nt * 8][ks * 16], kLd, lane);
+        ldmatrix_b(b0, b1, &sm.k[buf][0][0], wp * KW + nt * 8, ks * 2, lane);
         mma_bf16(s[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
         mma_bf16(s[nt], al[0], al[1], al[2], al[3], b0, b1);
       }
@@ -253,7 +281,7 @@ DF2_DEV void ctx_part(const AttnArgs& a, unsigned char* smem_raw, int r, int kvh
 #pragma unroll
       for (int dt = 0; dt < kHd / 8; ++dt) {
         uint32_t b0, b1;
-        ldmatrix_x2_trans(b0, b1, &sm.v[buf][wp * KW + j * 16 + (lane & 15)][dt * 8]);
+        ldmatrix_x2_trans(b0, b1, &sm.v[buf][0][0], wp * KW + j * 16 + (lane & 15), dt);
         mma_bf16(o[dt], ph[0], ph[1], ph[2], ph[3], b0, b1);
         mma_bf16(o[dt], pl[0], pl[1], pl[2], pl[3], b0, b1);
       }
