@@ -28,6 +28,14 @@ constexpr int kK = 16;
 // Block width of request r: 2..B, B when no widths are given.
 DF2_DEV int width_of(const int32_t* width, int r, int B) { return width != nullptr ? min(max(width[r], 2), B) : B; }
 
+// One count on a request's device-wide counter, ordered after this thread's earlier
+// writes (release) and before its later reads (acquire); returns the previous value.
+DF2_DEV unsigned int count_acq_rel(unsigned int* counter) {
+  unsigned int prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
+  return prev;
+}
+
 // Chunk statistics written by other CTAs of the launch, read from L2.
 DF2_DEV VerifyStat ldst(const VerifyStat* p) {
   VerifyStat v;
@@ -448,12 +456,13 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const VerifyArgs a) {
   const int chunk = blockIdx.x;
   // rows at or past the request's width are not read, only counted
   if (j_row < width_of(a.width, r, a.B)) row_chunk_stats(a, rj, r, chunk);
-  // count this chunk; the CTA that completes request r's B x n_chunks runs its chain
+  // count this chunk; the CTA that completes request r's B x n_chunks runs its chain.
+  // Thread 0 wrote this chunk's statistics itself, so its count releases them (no fence
+  // by every thread); the count also acquires the other chunks' statistics for the chain.
   __shared__ bool last;
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned int prev = atomicAdd(a.counters + r, 1u);
+    const unsigned int prev = count_acq_rel(a.counters + r);
     last = prev == static_cast<unsigned int>(a.B * a.n_chunks - 1);
     if (last) a.counters[r] = 0u;  // every CTA of the set has counted
   }
@@ -616,12 +625,12 @@ __global__ void __launch_bounds__(256) tree_stats_kernel(const TreeVerifyArgs a)
       a.stats[(static_cast<size_t>(r) * (a.budget + 1) + row) * a.n_chunks + chunk] = st;
     }
   }
-  // count this CTA; the one completing request r's rows x chunks walks its tree
+  // count this CTA; the one completing request r's rows x chunks walks its tree (thread
+  // 0 wrote the statistics: its count releases them and acquires the others')
   __shared__ bool last;
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned int prev = atomicAdd(a.counters + r, 1u);
+    const unsigned int prev = count_acq_rel(a.counters + r);
     last = prev == static_cast<unsigned int>((a.budget + 1) * a.n_chunks - 1);
     if (last) a.counters[r] = 0u;
   }
