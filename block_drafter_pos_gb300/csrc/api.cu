@@ -108,20 +108,6 @@ enum { kQ, kK, kV, kO, kGate, kUp, kDown, kAttnDelta, kMlpDelta };
 // activation buffer behind xmap (its lo plane starts there); x: that buffer, from
 // which the GEMM path encodes its own activation map; wide_map: the weight map of
 // the GEMM path.
-// Context chunks per attention part.  A part's CTA streams its chunks one after the
-// other; each part costs a fixed latency (queries, first copy, merge, partial
-// stores) and a partial for the combine.  Parts are at most 8 per (request, KV head),
-// and longer while the grid exceeds 1.3 waves of two CTAs per SM.  Measured (ms per
-// step): 1 request, context 1024: 1 chunk 1.181, 2: 1.168, 4: 1.172; context 2048:
-// 1: 1.032, 2: 1.022, 4: 1.016; 4 requests, context 8192: 2: 1.341, 4: 1.311,
-// 8: 1.342; 16 requests: 4: 2.010, 8: 1.977, 16: 1.948, 32: 2.104.
-int attn_chunks_per_part(int n_req, int nkv, int n_ctx_chunks, int num_sms) {
-  int c = 1;
-  while (c < 16 && (n_ctx_chunks + c - 1) / c > 8) c *= 2;
-  while (c < 16 && 10LL * n_req * nkv * ((n_ctx_chunks + c - 1) / c + 1) > 26LL * num_sms) c *= 2;
-  return c;
-}
-
 struct SegSpec {
   GemvSeg g;
   const CUtensorMap* wide_map;

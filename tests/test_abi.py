@@ -139,6 +139,24 @@ def test_stream_k_plane_map_against_brute_force(tmp_path):
     assert out.stdout.startswith("ok ") and int(out.stdout.split()[1]) > 10000
 
 
+def test_attention_part_length_rule(tmp_path):
+    """The attention's context chunks per part (internal.h): the lengths measured best
+    at 1, 4 and 16 requests on the drafter's geometry, and the rule's limits for every
+    shape in range (host code, g++)."""
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    cuda_inc = "/usr/local/cuda/include"
+    if gxx is None or not os.path.exists(os.path.join(cuda_inc, "cuda.h")):
+        pytest.skip("g++ or the CUDA headers are missing")
+    exe = str(tmp_path / "attn_parts_check")
+    subprocess.run([gxx, "-std=c++17", "-O1", "-I", os.path.join(ROOT, "block_drafter_pos_gb300", "csrc"),
+                    "-I", cuda_inc, os.path.join(ROOT, "tests", "attn_parts_check.cpp"), "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout
+    assert out.stdout.startswith("ok ") and int(out.stdout.split()[1]) > 100000
+
+
 def test_binding_structures_match_the_header(tmp_path):
     """The ctypes structures of the binding have the C header's sizes and field
     offsets (a small C program built with the host compiler prints them)."""
