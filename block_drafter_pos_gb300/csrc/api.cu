@@ -80,6 +80,7 @@ struct dflash2_handle {
   // dflash2_step: graphs of the argument sets seen, least recently used replaced
   struct StepGraph {
     dflash2_step_args key;
+    int select_mode;  // the handle's selector mode when captured (a graph keeps its kernels' arguments)
     cudaGraphExec_t exec;
     int64_t launches;  // kernels in the graph
     uint64_t used;
@@ -1152,9 +1153,12 @@ dflash2_status dflash2_step(dflash2_handle* h, const dflash2_step_args* args, vo
   k.n_emitted = args->n_emitted;
   k.width = args->width;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  for (int i = 0; i < h->n_step_graphs; ++i) {
+  // with profiling events set, the calls run as they are (a graph would keep recording
+  // the events after the caller has cleared them)
+  const bool profiling = h->ev_lm0 != nullptr || h->proj_ev != nullptr;
+  for (int i = 0; i < h->n_step_graphs && !profiling; ++i) {
     dflash2_handle::StepGraph& g = h->step_graph[i];
-    if (memcmp(&g.key, &k, sizeof(k)) == 0) {
+    if (g.select_mode == h->select_mode && memcmp(&g.key, &k, sizeof(k)) == 0) {
       DF2_CHECK(cudaGraphLaunch(g.exec, st));
       h->launches += g.launches;
       g.used = ++h->step_clock;
@@ -1174,7 +1178,7 @@ dflash2_status dflash2_step(dflash2_handle* h, const dflash2_step_args* args, vo
     return r;
   };
   const dflash2_status r = run(st);
-  if (r != DFLASH2_OK) return r;
+  if (r != DFLASH2_OK || profiling) return r;
   // then its graph, captured on the handle's own stream (nothing runs)
   if (!h->cap_stream && cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
     h->cap_stream = nullptr;
@@ -1207,6 +1211,7 @@ dflash2_status dflash2_step(dflash2_handle* h, const dflash2_step_args* args, vo
     ++h->n_step_graphs;
   }
   h->step_graph[slot].key = k;
+  h->step_graph[slot].select_mode = h->select_mode;
   h->step_graph[slot].exec = exec;
   h->step_graph[slot].launches = n_graph;
   h->step_graph[slot].used = ++h->step_clock;

@@ -340,14 +340,16 @@ typedef struct dflash2_step_args {
 
 /* One step: dflash2_draft_block, dflash2_select and dflash2_verify on `args`, in
  * that order on `stream`, with the same results.  The first call with a given
- * argument set (the same values in every field) runs the three calls as they are
- * and then captures them into a CUDA graph on a stream of the handle's own (the
- * capture launches nothing); later calls with that set launch the graph on `stream`,
- * one launch instead of about seventy.  The graph reads the buffers each time it
- * runs, so a serving loop changes their contents between steps, not their
- * addresses (dflash2_advance keeps them).  A handle keeps DFLASH2_STEP_GRAPHS sets;
+ * argument set (the same values in every field, under the same selector mode) runs
+ * the three calls as they are and then captures them into a CUDA graph on a stream
+ * of the handle's own (the capture launches nothing); later calls with that set
+ * launch the graph on `stream`, one launch instead of about seventy.  The graph
+ * reads the buffers each time it runs, so a serving loop changes their contents
+ * between steps, not their addresses (dflash2_advance keeps them).  A handle keeps DFLASH2_STEP_GRAPHS sets;
  * their graphs are freed by dflash2_step_graphs_clear or dflash2_destroy, and must
- * be cleared before a buffer they name is freed.  Not for concurrent use of one
+ * be cleared before a buffer they name is freed.  While the handle has profiling
+ * events set (dflash2_set_lmhead_events, dflash2_set_projection_events) the calls
+ * run as they are, nothing captured or replayed.  Not for concurrent use of one
  * handle from several threads.  Returns what the three calls return (their checks
  * run on the first call with a set; nothing is cached when one fails) or
  * DFLASH2_E_CUDA if a launch fails; a failed capture leaves the set uncached, and

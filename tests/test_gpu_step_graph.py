@@ -5,7 +5,8 @@ rows copied into the same buffers), its outputs equal those of the three separat
 calls bit for bit, on both paths (3 bf16 requests: GEMV; 5 Q8 requests: tensor
 cores), and a replay counts the same kernels as a step of separate calls.  More
 argument sets than the handle keeps replace the least recently used graph and still
-give the same results."""
+give the same results, and a change of the selector mode is not replayed from a
+graph captured under the other mode."""
 import numpy as np
 import pytest
 import torch
@@ -130,4 +131,48 @@ def test_step_graph_more_argument_sets_than_kept():
         b["status"] = statuses[it % n_sets].cpu().numpy()
         for k in a:
             assert np.array_equal(a[k], b[k]), (it, k)
+    bd.dflash2_step_graphs_clear(h)
+
+
+def test_step_graph_follows_the_selector_mode():
+    """A set captured under the sequential walk, then the Viterbi mode (mode 1, for the
+    greedy requests): the step must use the mode in force, like the separate calls."""
+    fmt, R = "bf16", 3
+    g, wl, W, inp, temps, offs0, taps, noise = _loop_setup(fmt, R)
+    # selector tables 16x larger (a power of two: exact in bf16), so that the pairwise
+    # scores outweigh the candidates' logits and the best path is often not the walk's
+    W = dict(W)
+    for name in ("cb_a", "cb_b"):
+        f = (W[name]["w"].astype(np.uint32) << 16).view(np.float32) * np.float32(16.0)
+        W[name] = {"kind": "bf16", "w": (f.view(np.uint32) >> 16).astype(np.uint16)}
+    kc, vc = new_caches(wl, inp)
+    step = GpuStep(wl, W)
+    h = step.drafter.handle
+    greedy = [0.0] * R  # mode 1 changes the greedy requests' paths only
+    A = Side(g, inp, kc, vc, greedy, offs0, R)
+    Bs = Side(g, inp, kc, vc, greedy, offs0, R)
+    rng = np.random.default_rng(5)
+    differs = 0  # requests whose mode-1 path differs from the walk's (else the test proves nothing)
+    for it, mode in enumerate((0, 0, 1, 1, 1, 1, 0)):
+        bd.dflash2_set_select_mode(h, mode)
+        tg = (rng.standard_normal((R, 8, g.vocab)) * 3.0).astype(np.float32)
+        for S in (A, Bs):
+            S.taps.copy_(t(taps[it % STEPS]))
+            S.target.copy_(t(tg))
+        _separate(h, R, A)
+        _step(h, R, Bs)
+        torch.cuda.synchronize()
+        a, b = A.outputs(), Bs.outputs()
+        for k in a:
+            assert np.array_equal(a[k], b[k]), (it, mode, k)
+        if mode == 1:
+            bd.dflash2_set_select_mode(h, 0)
+            walk_path = torch.empty_like(A.path)
+            bd.dflash2_select(h, R, A.anchors, A.cand_ids, A.cand_logits, A.gate, A.temps, A.seeds, A.offs, walk_path,
+                              torch.empty_like(A.q_rows), None, torch.empty_like(A.status))
+            torch.cuda.synchronize()
+            wp = walk_path.cpu().numpy()
+            differs += sum(int(not np.array_equal(wp[r], a["path"][r])) for r in range(R))
+    bd.dflash2_set_select_mode(h, 0)
+    assert differs >= 1
     bd.dflash2_step_graphs_clear(h)
